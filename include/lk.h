@@ -1,0 +1,208 @@
+/*
+ * lk.h -- C ABI of the GB300 (sm_103a) Q8_0 decode-projection library.
+ *
+ * The operations are the ones of the lane kernel library "kernels.rs"
+ * (logicaffeine_compile codegen_cuda lane), the QWEN38_EXTRA_KERNELS constant
+ * and model-as-a-kernel "megakernel.cu"; each entry point below names the
+ * passage that defines it.
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller (for
+ *     example a torch tensor's data_ptr()), except where a parameter says
+ *     "host".  The library never allocates, frees or retains device memory; it
+ *     keeps only a small per-device cache of device attributes.
+ *   - Every call is asynchronous on the given stream (0 = the legacy default
+ *     stream) and never synchronizes, except lk_device_error.
+ *   - Arguments are validated before anything is launched; a failed check
+ *     returns a negative status and launches nothing.  A launch failure
+ *     reported by the CUDA runtime returns LK_ERR_CUDA.
+ *   - Layouts are row-major and dense:
+ *       wq  int8   [N][K]       weight levels of a Q8_0 matrix
+ *       ws  uint16 [N][K/32]    f16 bit patterns, one scale per 32 weights
+ *       x   f32    [M][K]       activation rows (M <= LK_MAX_M)
+ *       xq  int8   [M][K]       high words of the quantized activation
+ *       xl  int8   [M][K]       low words (TwoPassInt8 only)
+ *       xs  f32    [M][K/32]    one activation scale per 32 values
+ *       y   f32    [M][N]       y[t*N + o] = row o dotted with activation t
+ *   - K must be a multiple of 32.  wq, x, xq, xl must be 16-byte aligned;
+ *     ws 2-byte, xs and y 4-byte, 64-bit buffers 8-byte aligned.
+ *   - M == 0 or N == 0 is an empty problem: nothing is launched, LK_OK.
+ */
+#ifndef LK_H
+#define LK_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Numerics modes ("kernels.rs" module doc, Q8MatKind -> mode()):
+ *   LK_DEQUANT  f32 activations, the dot summed in f64;
+ *   LK_INT8ACT  activations quantized to int8 per 32-group (one word);
+ *   LK_TWOPASS  a high and a low int8 word per activation value. */
+typedef enum { LK_DEQUANT = 0, LK_INT8ACT = 1, LK_TWOPASS = 2 } lk_mode;
+
+typedef int lk_status;
+#define LK_OK                   0
+#define LK_ERR_ARG             -1  /* null pointer, unknown mode or option   */
+#define LK_ERR_ALIGN           -2  /* pointer misaligned for its element/vec */
+#define LK_ERR_SHAPE           -3  /* K % 32 != 0, M or S out of range, ...  */
+#define LK_ERR_WORKSPACE       -4  /* caller's workspace too small           */
+#define LK_ERR_CUDA            -5  /* the CUDA runtime reported an error     */
+#define LK_ERR_DEVICE_TIMEOUT  -6  /* a device-side bounded wait gave up     */
+
+#define LK_MAX_M      8   /* activation rows that share one weight read */
+#define LK_MAX_SPLITK 64  /* split-K chunks */
+
+/* A static, human-readable name of a status. */
+const char* lk_status_string(lk_status s);
+
+/* Library ABI version (major*100 + minor). */
+int lk_version(void);
+
+/*
+ * RMSNorm of M rows, then the activation quantizer of `mode`.
+ * ("kernels.rs" RMSNORM lk_rmsnorm / lk_rmsnorm_row with lk_quant_lane;
+ *  module doc: "an RMSNorm divides by sqrt(mean + 1e-6) then scales".)
+ *   y[t][i] = x[t][i] / sqrt(sum_k x[t][k]^2 / K + eps) * gain[i]
+ * The sum of squares is accumulated in f64 under LK_DEQUANT and in f32
+ * otherwise, in the fixed order of a block of min(roundup32(K), 1024)
+ * threads (strided per-thread fused multiply-adds, then a shuffle-down tree
+ * per warp and over the warps), so results are bit-reproducible.
+ *   x     f32 [M][K]   input rows           gain f32 [K]
+ *   xn    f32 [M][K]   normed rows; required under LK_DEQUANT (the GEMV's
+ *                      activation), optional (may be NULL) otherwise
+ *   xq,xs              quantized output (LK_INT8ACT, LK_TWOPASS); ignored
+ *                      under LK_DEQUANT
+ *   xl                 low words, LK_TWOPASS only
+ */
+lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, float eps,
+                           lk_mode mode, float* xn, int8_t* xq, int8_t* xl, float* xs,
+                           cudaStream_t stream);
+
+/*
+ * The activation quantizer alone ("kernels.rs" QUANT lk_quant, PRELUDE
+ * lk_quant_lane / lk_two_scale / lk_two_words).  Per 32-value group with
+ * a = max|v|:
+ *   LK_INT8ACT: s = a > 0 ? a/127 : 1; hi = rn(v/s)
+ *   LK_TWOPASS: s = max(a, 1e-30)/127; hi = clamp(rn(v/s));
+ *               lo = clamp(rn(fma(-hi, s, v) / (s/128)))
+ * rn rounds to nearest even; divisions are IEEE.  mode LK_DEQUANT is an
+ * argument error (nothing to quantize).
+ */
+lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq, int8_t* xl,
+                          float* xs, cudaStream_t stream);
+
+/*
+ * y = W x for M <= 8 activation rows that share each weight read
+ * ("kernels.rs" GEMV_Q8 lk_gemv_q8 and lk_q8_rows_dot; PRELUDE lk_q8_term,
+ *  lk_q8_sum4).  Quantized modes: each 32-block's int8 dot d (and e of the
+ *  low words) is exact; block b's step goes into partial b mod 4 in ascending
+ *  b:  Int8Act p = fma(w*s, d, p);  TwoPass p = fma(w, fma(s, d, (s/128)*e), p);
+ *  y = (p0 + p2) + (p1 + p3).  Dequant: each block's 32 products are summed
+ *  in f32 and the blocks, scaled by the f16 weight scale, in f64; the f64 row
+ *  sum is rounded to f32 once.
+ *   Dequant reads x; Int8Act reads xq, xs; TwoPass reads xq, xl, xs.
+ *   argmax_parts  optional u64 [M][*n_parts_out]: the lm-head epilogue
+ *                 (model-as-a-kernel "megakernel.cu" amax_key with
+ *                 EP_F32_AMAX): each launched block writes the largest key
+ *                 of its rows, key = order-preserving bits of the f32 logit
+ *                 (with -0 read as +0) in the high half and 0xFFFFFFFF - row
+ *                 in the low half.  Reduce with lk_argmax.  Size it with
+ *                 lk_argmax_parts_max(N) entries per activation row.
+ *   n_parts_out   HOST int*, required when argmax_parts is given: the number
+ *                 of partial keys written per activation row.
+ */
+lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
+                     const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
+                     float* y, uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream);
+
+/*
+ * Bytes of the split-K partial buffer for (mode, S, M, N): S*M*N values,
+ * f64 under LK_DEQUANT, f32 otherwise.
+ */
+size_t lk_splitk_workspace_bytes(lk_mode mode, int S, int M, int N);
+
+/*
+ * The split-K partial GEMV (QWEN38_EXTRA_KERNELS "SPLIT-K FOR THE NARROW
+ * PROJECTIONS", gk_gemv_hl_sk).  Chunk c in [0, S) owns the 32-blocks
+ * [4*floor(c*G/S), 4*floor((c+1)*G/S)) with G = floor(K/128), the last chunk
+ * ending at K/32 (the balanced split of "kernels.rs" GEMM_BLK over four-block
+ * groups).  A chunk's value is lk_gemv_q8's rule restricted to its blocks
+ * (partial index = global block index mod 4); Dequant chunks are f64 sums.
+ * Writes part[c][t][o] (layout [S][M][N], f32 or f64 by mode).  1 <= S <= 64.
+ * part_bytes must be >= lk_splitk_workspace_bytes(mode, S, M, N).
+ */
+lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
+                            const float* x, const int8_t* xq, const int8_t* xl, const float* xs,
+                            int M, int S, void* part, size_t part_bytes, cudaStream_t stream);
+
+/*
+ * The split-K combine (QWEN38_EXTRA_KERNELS gk_sk_combine): a separate
+ * kernel, never atomics: y[t][o] = (((0 + part[0][t][o]) + part[1][t][o]) +
+ * ...) in ascending chunk order, in f32 (f64 then one rounding to f32 under
+ * LK_DEQUANT).  Same inputs give the same bits on every run.
+ */
+lk_status lk_splitk_combine(lk_mode mode, const void* part, int S, int M, int N, float* y,
+                            cudaStream_t stream);
+
+/* Upper bound on the argmax partial keys per activation row that lk_gemv_q8
+ * writes for an N-row matrix. */
+int lk_argmax_parts_max(int N);
+
+/* Entries of the u64 scratch lk_argmax needs per activation row when it
+ * reduces logits directly ("kernels.rs" argmax_blocks: clamp(ceil(N/2048),
+ * 1, 64) blocks). */
+int lk_argmax_scratch_entries(int N);
+
+/*
+ * First index of the maximum of each of M rows ("kernels.rs" module doc: the
+ * arg-max keeps the first of equal maxima; "megakernel.cu" ph_argmax_part /
+ * ph_argmax_fin).  Two forms:
+ *   parts != NULL: reduce the n_parts keys per row that lk_gemv_q8 wrote
+ *                  (logits and scratch are ignored);
+ *   parts == NULL: reduce logits f32 [M][N] in two kernels through scratch
+ *                  (u64, M * lk_argmax_scratch_entries(N) entries).
+ * idx int32 [M].  Logits compare as f32 values with -0 == +0; the result for
+ * NaN logits is unspecified.  N >= 1.
+ */
+lk_status lk_argmax(const float* logits, const uint64_t* parts, int n_parts, int M, int N,
+                    int32_t* idx, uint64_t* scratch, cudaStream_t stream);
+
+/*
+ * Test hook: the exact int32 block dots of one activation row, computed by the
+ * same lane arrangement the GEMV uses ("kernels.rs" lk_q8_block_dot).
+ *   d[o][b] = sum_k wq[o][32b+k] * xq[32b+k];  e likewise with xl (if both xl
+ *   and e are non-NULL).  d, e int32 [N][K/32].
+ */
+lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, const int8_t* xl,
+                           int32_t* d, int32_t* e, cudaStream_t stream);
+
+/*
+ * Tuning and test options (process-wide; not thread-safe against concurrent
+ * launches).  Names:
+ *   "gemv_path"   0 auto, 1 direct-load kernel, 2 bulk-copy ring kernel
+ *   "ring_stages" ring depth of the bulk-copy kernel (0 = default)
+ *   "grid_ctas"   blocks of the ring kernel (0 = one per SM)
+ *   "wait_cap"    iteration cap of every device-side wait (0 = default)
+ * Unknown names or out-of-range values return LK_ERR_ARG.
+ */
+lk_status lk_set_option(const char* name, long value);
+long lk_get_option(const char* name);
+
+/*
+ * Synchronizes the current device and reads the device-side error word that
+ * bounded waits set when they give up (0 = none).  *code receives the raw
+ * word; returns LK_ERR_DEVICE_TIMEOUT if it is non-zero, LK_OK otherwise.
+ * reset != 0 clears the word.
+ */
+lk_status lk_device_error(int reset, int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LK_H */

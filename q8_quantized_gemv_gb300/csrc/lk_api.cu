@@ -1,0 +1,340 @@
+// The small entry points of the C ABI: status names, options, device
+// attributes, RMSNorm + quantize, the standalone quantizer, the argmax
+// reductions and the block-dot test hook.
+#include <string.h>
+
+#include "lk_device.cuh"
+#include "lk_host.h"
+
+using namespace lk;
+
+namespace lkh {
+
+long opt_gemv_path = 0;
+long opt_ring_stages = 0;
+long opt_grid_ctas = 0;
+long opt_wait_cap = 0;
+
+static const int kMaxDevices = 64;
+static DeviceInfo g_info[kMaxDevices];
+static int g_info_ok[kMaxDevices];
+
+const DeviceInfo* device_info(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (dev_out) *dev_out = dev;
+  if (!g_info_ok[dev]) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      return nullptr;
+    g_info[dev] = d;
+    g_info_ok[dev] = 1;
+  }
+  return &g_info[dev];
+}
+
+}  // namespace lkh
+
+using namespace lkh;
+
+// ---------------------------------------------------------------------------
+// RMSNorm (+ quantize).  One block per activation row, blockDim.x =
+// min(roundup32(K), 1024) ("kernels.rs" norm_threads): that block size fixes
+// the order of the f32 sum of squares.  Q 0 (Dequant) accumulates in f64 and
+// writes only the normed row.
+template <int Q>
+struct acc_of { typedef float t; };
+template <>
+struct acc_of<0> { typedef double t; };
+
+__device__ __forceinline__ float fma_acc(float v, float acc) { return __fmaf_rn(v, v, acc); }
+__device__ __forceinline__ double fma_acc(double v, double acc) { return __fma_rn(v, v, acc); }
+__device__ __forceinline__ float norm_div_add(float sum, int K, float eps) {
+  return __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, (float)K), eps));
+}
+__device__ __forceinline__ double norm_div_add(double sum, int K, float eps) {
+  return __dsqrt_rn(__dadd_rn(__ddiv_rn(sum, (double)K), (double)eps));
+}
+__device__ __forceinline__ float norm_scale(float v, float den, float g) {
+  return __fmul_rn(__fdiv_rn(v, den), g);
+}
+__device__ __forceinline__ float norm_scale(float v, double den, float g) {
+  return __double2float_rn(__dmul_rn(__ddiv_rn((double)v, den), (double)g));
+}
+
+template <int Q>
+__global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __restrict__ x,
+                                                             const float* __restrict__ g, int K,
+                                                             float eps, float* __restrict__ xn,
+                                                             int8_t* __restrict__ xq,
+                                                             int8_t* __restrict__ xl,
+                                                             float* __restrict__ xs) {
+  typedef typename acc_of<Q>::t A;
+  __shared__ A red[32];
+  __shared__ A total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int vt = blockDim.x, nw = vt >> 5;
+  const long row = blockIdx.x;
+  const float* xr = x + row * K;
+
+  A acc = 0;
+  for (int i = threadIdx.x; i < K; i += vt) acc = fma_acc((A)__ldg(xr + i), acc);
+  acc = warp_tree_sum(acc);
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    A v = lane < nw ? red[lane] : (A)0;
+    v = warp_tree_sum(v);
+    if (lane == 0) total = v;
+  }
+  __syncthreads();
+  const A den = norm_div_add(total, K, eps);
+
+  // warp w holds the 32-groups starting at 32w, 32w + vt, ... (vt % 32 == 0)
+  for (int base = warp * 32; base < K; base += vt) {
+    const int i = base + lane;
+    const float yv = norm_scale(__ldg(xr + i), den, __ldg(g + i));
+    if (xn) xn[row * K + i] = yv;
+    if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, row * K + i, (row * K + i) >> 5, lane);
+  }
+}
+
+template <int Q>
+__global__ void quantize_kernel(const float* __restrict__ x, long groups, int8_t* __restrict__ xq,
+                                int8_t* __restrict__ xl, float* __restrict__ xs) {
+  const long g = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (g >= groups) return;  // whole warps exit together
+  const int lane = threadIdx.x & 31;
+  const long i = g * 32 + lane;
+  quant_lane<Q>(__ldg(x + i), xq, xl, xs, i, g, lane);
+}
+
+static lk_status check_act_out(lk_mode mode, const int8_t* xq, const int8_t* xl, const float* xs) {
+  if (!xq || !xs || (mode == LK_TWOPASS && !xl)) return LK_ERR_ARG;
+  if (!aligned(xs, 4)) return LK_ERR_ALIGN;
+  return LK_OK;
+}
+
+extern "C" {
+
+const char* lk_status_string(lk_status s) {
+  switch (s) {
+    case LK_OK: return "ok";
+    case LK_ERR_ARG: return "invalid argument";
+    case LK_ERR_ALIGN: return "misaligned pointer";
+    case LK_ERR_SHAPE: return "unsupported shape";
+    case LK_ERR_WORKSPACE: return "workspace too small";
+    case LK_ERR_CUDA: return "CUDA runtime error";
+    case LK_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int lk_version(void) { return 100; }
+
+lk_status lk_set_option(const char* name, long value) {
+  if (!name) return LK_ERR_ARG;
+  if (!strcmp(name, "gemv_path")) {
+    if (value < 0 || value > 2) return LK_ERR_ARG;
+    opt_gemv_path = value;
+  } else if (!strcmp(name, "ring_stages")) {
+    if (value < 0 || value > 32) return LK_ERR_ARG;
+    opt_ring_stages = value;
+  } else if (!strcmp(name, "grid_ctas")) {
+    if (value < 0 || value > (1L << 20)) return LK_ERR_ARG;
+    opt_grid_ctas = value;
+  } else if (!strcmp(name, "wait_cap")) {
+    if (value < 0) return LK_ERR_ARG;
+    opt_wait_cap = value;
+  } else {
+    return LK_ERR_ARG;
+  }
+  return LK_OK;
+}
+
+long lk_get_option(const char* name) {
+  if (!name) return -1;
+  if (!strcmp(name, "gemv_path")) return opt_gemv_path;
+  if (!strcmp(name, "ring_stages")) return opt_ring_stages;
+  if (!strcmp(name, "grid_ctas")) return opt_grid_ctas;
+  if (!strcmp(name, "wait_cap")) return opt_wait_cap;
+  return -1;
+}
+
+lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, float eps, lk_mode mode,
+                           float* xn, int8_t* xq, int8_t* xl, float* xs, cudaStream_t stream) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+  if (M < 0 || M > LK_MAX_M || K < 0 || K % 32) return LK_ERR_SHAPE;
+  if (M == 0 || K == 0) return LK_OK;
+  if (!x || !gain) return LK_ERR_ARG;
+  if (!aligned(x, 4) || !aligned(gain, 4) || (xn && !aligned(xn, 4))) return LK_ERR_ALIGN;
+  const int vt = K < 1024 ? K : 1024;  // K % 32 == 0: roundup32(K) == K
+  if (mode == LK_DEQUANT) {
+    if (!xn) return LK_ERR_ARG;
+    rmsnorm_quant_kernel<0><<<M, vt, 0, stream>>>(x, gain, K, eps, xn, nullptr, nullptr, nullptr);
+  } else {
+    lk_status st = check_act_out(mode, xq, xl, xs);
+    if (st) return st;
+    if (mode == LK_INT8ACT)
+      rmsnorm_quant_kernel<1><<<M, vt, 0, stream>>>(x, gain, K, eps, xn, xq, nullptr, xs);
+    else
+      rmsnorm_quant_kernel<2><<<M, vt, 0, stream>>>(x, gain, K, eps, xn, xq, xl, xs);
+  }
+  return launch_status();
+}
+
+lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq, int8_t* xl,
+                          float* xs, cudaStream_t stream) {
+  if (mode != LK_INT8ACT && mode != LK_TWOPASS) return LK_ERR_ARG;
+  if (M < 0 || M > LK_MAX_M || K < 0 || K % 32) return LK_ERR_SHAPE;
+  if (M == 0 || K == 0) return LK_OK;
+  if (!x) return LK_ERR_ARG;
+  if (!aligned(x, 4)) return LK_ERR_ALIGN;
+  lk_status st = check_act_out(mode, xq, xl, xs);
+  if (st) return st;
+  const long groups = (long)M * (K / 32);
+  const int per_block = 8;
+  const long blocks = (groups + per_block - 1) / per_block;
+  if (mode == LK_INT8ACT)
+    quantize_kernel<1><<<(unsigned)blocks, 32 * per_block, 0, stream>>>(x, groups, xq, nullptr, xs);
+  else
+    quantize_kernel<2><<<(unsigned)blocks, 32 * per_block, 0, stream>>>(x, groups, xq, xl, xs);
+  return launch_status();
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Argmax.  Keys are exact, so the max over any partition is the same: the
+// block-partial + final-reduce split changes nothing in the result.
+__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v,
+                                                            unsigned long long* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max_u64(v);
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  v = lane < nw ? sh[lane] : 0ull;
+  return warp_max_u64(v);
+}
+
+// Final reduce: row t's n keys -> first index of the maximum.
+__global__ void __launch_bounds__(256) argmax_reduce_kernel(const unsigned long long* __restrict__ parts,
+                                                            int n, int* __restrict__ idx) {
+  __shared__ unsigned long long sh[32];
+  const long t = blockIdx.x;
+  unsigned long long best = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const unsigned long long k = parts[t * n + i];
+    best = k > best ? k : best;
+  }
+  best = block_max_u64(best, sh);
+  if (threadIdx.x == 0) idx[t] = (int)(0xFFFFFFFFu - (unsigned)(best & 0xFFFFFFFFull));
+}
+
+// Partial keys of logits: block b of row t scans its slice ("kernels.rs"
+// argmax_blocks spreads the row over at most 64 blocks).
+__global__ void __launch_bounds__(256) argmax_logits_kernel(const float* __restrict__ logits, long N,
+                                                            unsigned long long* __restrict__ out) {
+  __shared__ unsigned long long sh[32];
+  const long t = blockIdx.y;
+  const long per = (N + gridDim.x - 1) / gridDim.x;
+  const long i0 = (long)blockIdx.x * per, i1 = i0 + per < N ? i0 + per : N;
+  unsigned long long best = 0;
+  for (long i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    const unsigned long long k = amax_key(__ldg(logits + t * N + i), (unsigned)i);
+    best = k > best ? k : best;
+  }
+  best = block_max_u64(best, sh);
+  if (threadIdx.x == 0) out[t * gridDim.x + blockIdx.x] = best;
+}
+
+// Exact block dots, lanes arranged as in the GEMV: 8 lanes per row, lane j
+// holding bytes 16j..16j+15 of a 128-byte segment (4 blocks); lanes 2q, 2q+1
+// hold block q and meet with one xor-shuffle.
+__global__ void __launch_bounds__(256) block_dots_kernel(const int8_t* __restrict__ wq, long N, int K,
+                                                         const int8_t* __restrict__ xq,
+                                                         const int8_t* __restrict__ xl,
+                                                         int* __restrict__ d, int* __restrict__ e) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rr = lane >> 3, j = lane & 7, q = j >> 1, hf = j & 1;
+  const long o = ((long)blockIdx.x * 8 + warp) * 4 + rr;
+  const bool row_ok = o < N;
+  const int nb = K >> 5, nsg = (nb + 3) >> 2;
+  const int4 zero = make_int4(0, 0, 0, 0);
+  for (int sg = 0; sg < nsg; ++sg) {
+    const int b = 4 * sg + q;
+    const bool ok = row_ok && b < nb;
+    const long off = 32L * b + 16 * hf;
+    const int4 w = ok ? *(const int4*)(wq + o * K + off) : zero;
+    const int4 h = ok ? *(const int4*)(xq + off) : zero;
+    int dd = dot16(w, h);
+    dd += __shfl_xor_sync(FULL, dd, 1);
+    int ee = 0;
+    if (xl) {
+      const int4 l = ok ? *(const int4*)(xl + off) : zero;
+      ee = dot16(w, l);
+      ee += __shfl_xor_sync(FULL, ee, 1);
+    }
+    if (ok && hf == 0) {
+      d[o * nb + b] = dd;
+      if (xl && e) e[o * nb + b] = ee;
+    }
+  }
+}
+
+extern "C" {
+
+int lk_argmax_parts_max(int N) {
+  if (N <= 0) return 0;
+  const long a = lkh::ring_max_ctas(N);
+  const long b = ((long)N + 31) / 32;
+  return (int)(a > b ? a : b);
+}
+
+int lk_argmax_scratch_entries(int N) {
+  if (N <= 0) return 0;
+  long n = ((long)N + 2047) / 2048;
+  return (int)(n < 1 ? 1 : (n > 64 ? 64 : n));
+}
+
+lk_status lk_argmax(const float* logits, const uint64_t* parts, int n_parts, int M, int N,
+                    int32_t* idx, uint64_t* scratch, cudaStream_t stream) {
+  if (M < 0 || M > LK_MAX_M) return LK_ERR_SHAPE;
+  if (M == 0) return LK_OK;
+  if (N < 1) return LK_ERR_SHAPE;
+  if (!idx) return LK_ERR_ARG;
+  if (!aligned(idx, 4)) return LK_ERR_ALIGN;
+  if (parts) {
+    if (n_parts < 1) return LK_ERR_SHAPE;
+    if (!aligned(parts, 8)) return LK_ERR_ALIGN;
+    argmax_reduce_kernel<<<M, 256, 0, stream>>>((const unsigned long long*)parts, n_parts, idx);
+    return launch_status();
+  }
+  if (!logits || !scratch) return LK_ERR_ARG;
+  if (!aligned(logits, 4) || !aligned(scratch, 8)) return LK_ERR_ALIGN;
+  const int nblk = lk_argmax_scratch_entries(N);
+  argmax_logits_kernel<<<dim3(nblk, M), 256, 0, stream>>>(logits, N, (unsigned long long*)scratch);
+  lk_status st = launch_status();
+  if (st) return st;
+  argmax_reduce_kernel<<<M, 256, 0, stream>>>((const unsigned long long*)scratch, nblk, idx);
+  return launch_status();
+}
+
+lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, const int8_t* xl,
+                           int32_t* d, int32_t* e, cudaStream_t stream) {
+  if (N < 0 || K < 0 || K % 32) return LK_ERR_SHAPE;
+  if (N == 0 || K == 0) return LK_OK;
+  if (!wq || !xq || !d) return LK_ERR_ARG;
+  if (!aligned(wq, 16) || !aligned(xq, 16) || (xl && !aligned(xl, 16)) || !aligned(d, 4) ||
+      (e && !aligned(e, 4)))
+    return LK_ERR_ALIGN;
+  const long blocks = ((long)N + 31) / 32;
+  block_dots_kernel<<<(unsigned)blocks, 256, 0, stream>>>(wq, N, K, xq, (xl && e) ? xl : nullptr, d, e);
+  return launch_status();
+}
+
+}  // extern "C"

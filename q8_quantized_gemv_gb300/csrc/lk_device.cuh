@@ -1,0 +1,110 @@
+// Device helpers shared by the library's kernels (sm_103a).
+//
+// Every float operation whose rounding is part of the result is written with
+// an explicit IEEE intrinsic (__fdiv_rn, __fmul_rn, __fmaf_rn, ...) so that no
+// compiler contraction or fast-math flag can change it.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace lk {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// ---- order-free warp reductions (exact: max) ---------------------------------
+__device__ __forceinline__ float warp_max_xor(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    unsigned long long w = __shfl_xor_sync(FULL, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+// ---- the canonical sum tree ("kernels.rs" lk_warp_sum) -------------------------
+// Lane l adds lane l+d for d = 16, 8, 4, 2, 1; lane 0 ends with the total.
+template <typename A>
+__device__ __forceinline__ A warp_tree_sum(A v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = v + __shfl_down_sync(FULL, v, o);
+  return v;
+}
+
+// ---- the activation quantizer ("kernels.rs" lk_quant_lane / lk_two_words) ------
+// The calling warp holds one 32-value group, value v in this lane.  Writes
+// the lane's word(s) at index i and (lane 0) the group's scale at g.
+template <int Q>
+__device__ __forceinline__ void quant_lane(float v, int8_t* __restrict__ hi, int8_t* __restrict__ lo,
+                                           float* __restrict__ xs, long i, long g, int lane) {
+  const float a = warp_max_xor(fabsf(v));
+  float s;
+  if (Q == 1) {
+    s = a > 0.f ? __fdiv_rn(a, 127.0f) : 1.0f;
+  } else {
+    s = __fdiv_rn(a > 1e-30f ? a : 1e-30f, 127.0f);
+  }
+  if (lane == 0) xs[g] = s;
+  int h = __float2int_rn(__fdiv_rn(v, s));
+  if (Q == 1) {
+    hi[i] = (int8_t)h;
+  } else {
+    h = h > 127 ? 127 : (h < -128 ? -128 : h);
+    const float r = __fmaf_rn(-(float)h, s, v);
+    int l = __float2int_rn(__fdiv_rn(r, __fmul_rn(s, 0.0078125f)));
+    l = l > 127 ? 127 : (l < -128 ? -128 : l);
+    hi[i] = (int8_t)h;
+    lo[i] = (int8_t)l;
+  }
+}
+
+// ---- argmax key ("megakernel.cu" amax_key) --------------------------------------
+// Order-preserving image of the f32 value (after -0 -> +0) in the high word,
+// 0xFFFFFFFF - index in the low word: the largest key is the largest value,
+// then the lowest index.
+__device__ __forceinline__ unsigned long long amax_key(float v, unsigned idx) {
+  if (v == 0.0f) v = 0.0f;
+  unsigned u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+
+// ---- the quantized block step ("kernels.rs" lk_q8_term / lk_q8_acc) --------------
+template <int Q>
+__device__ __forceinline__ float q8_step(float p, float w, float s, int d, int e) {
+  if (Q == 1) return __fmaf_rn(__fmul_rn(w, s), (float)d, p);
+  const float u = __fmaf_rn(s, (float)d, __fmul_rn(__fmul_rn(s, 0.0078125f), (float)e));
+  return __fmaf_rn(w, u, p);
+}
+
+__device__ __forceinline__ int dot16(int4 w, int4 x) {
+  int d = __dp4a(w.x, x.x, 0);
+  d = __dp4a(w.y, x.y, d);
+  d = __dp4a(w.z, x.z, d);
+  d = __dp4a(w.w, x.w, d);
+  return d;
+}
+
+// Streaming 16-byte load of weights: read-only path, no L1 allocation.
+__device__ __forceinline__ int4 ld_stream16(const void* p) {
+  int4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// Split-K chunk bound: the balanced split over four-block groups
+// ("kernels.rs" GEMM_BLK), the last chunk ending at nb.
+__host__ __device__ __forceinline__ int splitk_bound(int nb, int S, int c) {
+  if (c >= S) return nb;
+  const int G = nb >> 2;
+  return 4 * (int)(((long long)c * G) / S);
+}
+
+}  // namespace lk

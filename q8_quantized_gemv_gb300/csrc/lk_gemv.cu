@@ -1,0 +1,306 @@
+// The Q8_0 GEMV entry points: plain GEMV (with the optional argmax
+// epilogue), the split-K partial GEMV and the split-K combine.
+//
+// Direct-load kernel (any K % 32 == 0).  A warp owns 4 consecutive rows;
+// lane = 8*r + j serves row r, and within each 128-byte segment of the row
+// (four 32-blocks) lane j reads bytes 16j..16j+15, so the 8 lanes of a row
+// read one contiguous 128-byte line and lanes 2q, 2q+1 hold block q of the
+// segment.  The pair's two 16-value dots meet by one xor-shuffle, which
+// makes the block's int32 dot exact on both lanes.  Block b = 4*seg + q is
+// always in partial q = b mod 4 ("kernels.rs" lk_q8_rows_dot), so lane 2q
+// carries that partial's fused chain over the row's segments in ascending
+// order with no per-block shuffles; at the end (p0 + p2) + (p1 + p3)
+// (lk_q8_sum4) takes two shuffle-downs inside the 8 lanes.  U segments'
+// weights are loaded before any is used, so each lane keeps U 16-byte loads
+// in flight.
+#include "lk_device.cuh"
+#include "lk_host.h"
+
+using namespace lk;
+using namespace lkh;
+
+namespace {
+
+constexpr int kWarps = 8;          // warps per block
+constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerBlock = kWarps * kRowsPerWarp;
+constexpr int kU = 8;              // segments in flight per lane
+
+template <int Q>
+struct part_t { typedef float t; };
+template <>
+struct part_t<0> { typedef double t; };
+
+template <int Q, int M, bool SPLIT>
+__global__ void __launch_bounds__(256) gemv_direct_kernel(GemvProblem a) {
+  typedef typename part_t<Q>::t P;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rr = lane >> 3, j = lane & 7, q = j >> 1, hf = j & 1;
+  const long o = ((long)blockIdx.x * kWarps + warp) * kRowsPerWarp + rr;
+  const bool row_ok = o < a.N;
+  const int K = a.K, nb = K >> 5;
+  int b_lo = 0, b_hi = nb;
+  if (SPLIT) {
+    b_lo = splitk_bound(nb, a.S, blockIdx.y);
+    b_hi = splitk_bound(nb, a.S, blockIdx.y + 1);
+  }
+  const int sg_lo = b_lo >> 2, sg_hi = (b_hi + 3) >> 2;
+  const long orow = row_ok ? o : 0;
+  const int8_t* __restrict__ wrow = a.wq + orow * K + 16 * hf;
+  const __half* __restrict__ srow = a.ws + orow * nb;
+  const int4 zero = make_int4(0, 0, 0, 0);
+
+  P p[M];
+#pragma unroll
+  for (int t = 0; t < M; ++t) p[t] = (P)0;
+
+  for (int sg0 = sg_lo; sg0 < sg_hi; sg0 += kU) {
+    int4 wv[kU];
+    float wsv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int b = 4 * (sg0 + u) + q;
+      const bool ok = row_ok && b < b_hi;
+      wv[u] = ok ? ld_stream16(wrow + 32L * b) : zero;
+      wsv[u] = ok ? __half2float(srow[b]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (sg0 + u >= sg_hi) break;  // warp-uniform
+      const int b = 4 * (sg0 + u) + q;
+      const bool bok = b < b_hi;
+      const long off = 32L * b + 16 * hf;
+#pragma unroll
+      for (int t = 0; t < M; ++t) {
+        if constexpr (Q == 0) {
+          const float4* xv = (const float4*)(a.x + (long)t * K + off);
+          float4 xx[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) xx[c] = bok ? __ldg(xv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const int wi[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+          float h = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float xe[4] = {xx[c].x, xx[c].y, xx[c].z, xx[c].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) h = __fmaf_rn((float)(int8_t)(wi[c] >> (8 * k)), xe[k], h);
+          }
+          const float blk = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
+          if (bok) p[t] = __fma_rn((double)wsv[u], (double)blk, (double)p[t]);
+        } else {
+          const int4 hv = bok ? __ldg((const int4*)(a.xq + (long)t * K + off)) : zero;
+          int d = dot16(wv[u], hv);
+          d += __shfl_xor_sync(FULL, d, 1);
+          int e = 0;
+          if constexpr (Q == 2) {
+            const int4 lv = bok ? __ldg((const int4*)(a.xl + (long)t * K + off)) : zero;
+            e = dot16(wv[u], lv);
+            e += __shfl_xor_sync(FULL, e, 1);
+          }
+          const float s = bok ? __ldg(a.xs + (long)t * nb + b) : 0.f;
+          if (bok) p[t] = q8_step<Q>((float)p[t], wsv[u], s, d, e);
+        }
+      }
+    }
+  }
+
+  // (p0 + p2) + (p1 + p3) within the row's 8 lanes; lane 8r holds the row.
+  unsigned long long best[M];
+#pragma unroll
+  for (int t = 0; t < M; ++t) {
+    P v = p[t];
+    v = v + __shfl_down_sync(FULL, v, 4);
+    v = v + __shfl_down_sync(FULL, v, 2);
+    best[t] = 0;
+    if (j == 0 && row_ok) {
+      if (SPLIT) {
+        const long idx = ((long)blockIdx.y * M + t) * a.N + o;
+        if constexpr (Q == 0) a.part64[idx] = (double)v;
+        else a.y[idx] = (float)v;
+      } else {
+        const float yv = Q == 0 ? __double2float_rn((double)v) : (float)v;
+        a.y[(long)t * a.N + o] = yv;
+        best[t] = amax_key(yv, (unsigned)o);
+      }
+    }
+  }
+  if (!SPLIT && a.amax) {
+    __shared__ unsigned long long sh[M][kWarps];
+#pragma unroll
+    for (int t = 0; t < M; ++t) {
+      const unsigned long long w = warp_max_u64(best[t]);
+      if (lane == 0) sh[t][warp] = w;
+    }
+    __syncthreads();
+    if (threadIdx.x < M) {
+      unsigned long long m = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) m = sh[threadIdx.x][w] > m ? sh[threadIdx.x][w] : m;
+      a.amax[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
+    }
+  }
+}
+
+typedef void (*kernel_fn)(GemvProblem);
+
+template <int Q, bool SPLIT>
+kernel_fn pick_m(int M) {
+  switch (M) {
+    case 1: return gemv_direct_kernel<Q, 1, SPLIT>;
+    case 2: return gemv_direct_kernel<Q, 2, SPLIT>;
+    case 3: return gemv_direct_kernel<Q, 3, SPLIT>;
+    case 4: return gemv_direct_kernel<Q, 4, SPLIT>;
+    case 5: return gemv_direct_kernel<Q, 5, SPLIT>;
+    case 6: return gemv_direct_kernel<Q, 6, SPLIT>;
+    case 7: return gemv_direct_kernel<Q, 7, SPLIT>;
+    default: return gemv_direct_kernel<Q, 8, SPLIT>;
+  }
+}
+
+kernel_fn pick(int mode, int M, bool split) {
+  if (split) {
+    if (mode == 0) return pick_m<0, true>(M);
+    if (mode == 1) return pick_m<1, true>(M);
+    return pick_m<2, true>(M);
+  }
+  if (mode == 0) return pick_m<0, false>(M);
+  if (mode == 1) return pick_m<1, false>(M);
+  return pick_m<2, false>(M);
+}
+
+lk_status direct_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
+  const long blocks = (p.N + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (blocks > 0x7fffffffL) return LK_ERR_SHAPE;
+  kernel_fn f = pick(p.mode, p.M, false);
+  f<<<(unsigned)blocks, kWarps * 32, 0, stream>>>(p);
+  if (n_parts) *n_parts = (int)blocks;
+  return launch_status();
+}
+
+lk_status check_common(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
+                       const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+  if (N < 0 || K < 0 || K % 32 || M < 0 || M > LK_MAX_M) return LK_ERR_SHAPE;
+  if (K == 0) return LK_OK;  // nothing is read: every output is 0
+  if (!wq || !ws) return LK_ERR_ARG;
+  if (mode == LK_DEQUANT ? !x : (!xq || !xs || (mode == LK_TWOPASS && !xl))) return LK_ERR_ARG;
+  if (!aligned(wq, 16) || !aligned(ws, 2)) return LK_ERR_ALIGN;
+  if (mode == LK_DEQUANT ? !aligned(x, 16)
+                         : (!aligned(xq, 16) || !aligned(xs, 4) || (mode == LK_TWOPASS && !aligned(xl, 16))))
+    return LK_ERR_ALIGN;
+  return LK_OK;
+}
+
+GemvProblem make_problem(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
+                         const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M) {
+  GemvProblem p;
+  p.wq = wq;
+  p.ws = (const __half*)ws;
+  p.N = N;
+  p.K = K;
+  p.mode = mode;
+  p.x = x;
+  p.xq = xq;
+  p.xl = xl;
+  p.xs = xs;
+  p.M = M;
+  p.S = 1;
+  p.y = nullptr;
+  p.part64 = nullptr;
+  p.amax = nullptr;
+  return p;
+}
+
+// Combine: y = (((0 + c0) + c1) + ...) in ascending chunk order.
+template <bool F64>
+__global__ void __launch_bounds__(256) splitk_combine_kernel(const void* __restrict__ part, int S, long MN,
+                                                             float* __restrict__ y) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= MN) return;
+  if (F64) {
+    const double* pp = (const double*)part;
+    double acc = 0.0;
+    for (int c = 0; c < S; ++c) acc = __dadd_rn(acc, pp[(long)c * MN + i]);
+    y[i] = __double2float_rn(acc);
+  } else {
+    const float* pp = (const float*)part;
+    float acc = 0.f;
+    for (int c = 0; c < S; ++c) acc = __fadd_rn(acc, pp[(long)c * MN + i]);
+    y[i] = acc;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode, const float* x,
+                     const int8_t* xq, const int8_t* xl, const float* xs, int M, float* y,
+                     uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream) {
+  lk_status st = check_common(wq, ws, N, K, mode, x, xq, xl, xs, M);
+  if (st) return st;
+  if (argmax_parts && !n_parts_out) return LK_ERR_ARG;
+  if (N == 0 || M == 0) {
+    if (n_parts_out) *n_parts_out = 0;
+    return LK_OK;
+  }
+  if (!y) return LK_ERR_ARG;
+  if (!aligned(y, 4) || (argmax_parts && !aligned(argmax_parts, 8))) return LK_ERR_ALIGN;
+  GemvProblem p = make_problem(wq, ws, N, K, mode, x, xq, xl, xs, M);
+  p.y = y;
+  p.amax = (unsigned long long*)argmax_parts;
+  int n_parts = 0;
+  if (opt_gemv_path != 1 && ring_supports(p)) {
+    st = ring_gemv(p, stream, &n_parts);
+  } else {
+    if (opt_gemv_path == 2 && !ring_supports(p)) return LK_ERR_SHAPE;
+    st = direct_gemv(p, stream, &n_parts);
+  }
+  if (n_parts_out) *n_parts_out = n_parts;
+  return st;
+}
+
+size_t lk_splitk_workspace_bytes(lk_mode mode, int S, int M, int N) {
+  if (S < 1 || M < 0 || N < 0) return 0;
+  return (size_t)S * (size_t)M * (size_t)N * (mode == LK_DEQUANT ? 8 : 4);
+}
+
+lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
+                            const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
+                            int S, void* part, size_t part_bytes, cudaStream_t stream) {
+  lk_status st = check_common(wq, ws, N, K, mode, x, xq, xl, xs, M);
+  if (st) return st;
+  if (S < 1 || S > LK_MAX_SPLITK) return LK_ERR_SHAPE;
+  if (N == 0 || M == 0) return LK_OK;
+  if (!part) return LK_ERR_ARG;
+  if (!aligned(part, mode == LK_DEQUANT ? 8 : 4)) return LK_ERR_ALIGN;
+  if (part_bytes < lk_splitk_workspace_bytes(mode, S, M, N)) return LK_ERR_WORKSPACE;
+  GemvProblem p = make_problem(wq, ws, N, K, mode, x, xq, xl, xs, M);
+  p.S = S;
+  if (mode == LK_DEQUANT) p.part64 = (double*)part;
+  else p.y = (float*)part;
+  if (opt_gemv_path != 1 && ring_supports(p)) return ring_gemv(p, stream, nullptr);
+  if (opt_gemv_path == 2) return LK_ERR_SHAPE;
+  const long blocks = (p.N + kRowsPerBlock - 1) / kRowsPerBlock;
+  kernel_fn f = pick(p.mode, p.M, true);
+  f<<<dim3((unsigned)blocks, S), kWarps * 32, 0, stream>>>(p);
+  return launch_status();
+}
+
+lk_status lk_splitk_combine(lk_mode mode, const void* part, int S, int M, int N, float* y,
+                            cudaStream_t stream) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+  if (S < 1 || S > LK_MAX_SPLITK || M < 0 || M > LK_MAX_M || N < 0) return LK_ERR_SHAPE;
+  if (N == 0 || M == 0) return LK_OK;
+  if (!part || !y) return LK_ERR_ARG;
+  if (!aligned(part, mode == LK_DEQUANT ? 8 : 4) || !aligned(y, 4)) return LK_ERR_ALIGN;
+  const long MN = (long)M * N;
+  const long blocks = (MN + 255) / 256;
+  if (mode == LK_DEQUANT)
+    splitk_combine_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(part, S, MN, y);
+  else
+    splitk_combine_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(part, S, MN, y);
+  return launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Host-side helpers shared by the library's translation units (not part of
+// the public ABI).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lk.h"
+
+namespace lkh {
+
+// Per-device attributes, queried once per device and cached.
+struct DeviceInfo {
+  int sm_count;
+  int smem_optin;     // max dynamic shared memory per block (opt-in)
+  int smem_per_sm;
+  int l2_bytes;
+};
+const DeviceInfo* device_info(int* dev_out);
+
+// Process-wide options (lk_set_option).
+extern long opt_gemv_path;    // 0 auto, 1 direct, 2 ring
+extern long opt_ring_stages;  // 0 default
+extern long opt_grid_ctas;    // 0 default
+extern long opt_wait_cap;     // 0 default
+
+inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+inline lk_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? LK_OK : LK_ERR_CUDA;
+}
+
+// Everything one GEMV launch needs (plain, split-K partial, argmax epilogue).
+struct GemvProblem {
+  const int8_t* wq;
+  const __half* ws;
+  long N;
+  int K;
+  int mode;
+  const float* x;
+  const int8_t* xq;
+  const int8_t* xl;
+  const float* xs;
+  int M;
+  int S;                         // 1 = plain GEMV
+  float* y;                      // plain: y [M][N]; split quantized: part f32 [S][M][N]
+  double* part64;                // split Dequant: part f64 [S][M][N]
+  unsigned long long* amax;      // plain only: [M][n_parts]
+};
+
+// Bulk-copy ring kernel (lk_ring.cu).  Returns LK_ERR_SHAPE when the problem
+// is outside what the ring kernel takes (the caller then uses the direct
+// kernel), otherwise the launch status; *n_parts receives the blocks launched.
+lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts);
+bool ring_supports(const GemvProblem& p);
+int ring_max_ctas(long N);
+
+}  // namespace lkh

@@ -1,0 +1,207 @@
+"""Thin ctypes binding of liblk.so (the C ABI declared in include/lk.h).
+
+Each ``lk_*`` function here has the name and argument order of the C entry
+point; it only checks and marshals torch tensors (dtype, device, contiguity,
+sizes) into pointers and the current CUDA stream.  All arithmetic runs in the
+library's sm_103a kernels.  If liblk.so is missing the first call raises: there
+is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblk.so")
+
+LK_DEQUANT, LK_INT8ACT, LK_TWOPASS = 0, 1, 2
+MODES = {"dequant": LK_DEQUANT, "int8act": LK_INT8ACT, "twopass": LK_TWOPASS}
+LK_MAX_M = 8
+LK_MAX_SPLITK = 64
+
+STATUS = {0: "LK_OK", -1: "LK_ERR_ARG", -2: "LK_ERR_ALIGN", -3: "LK_ERR_SHAPE",
+          -4: "LK_ERR_WORKSPACE", -5: "LK_ERR_CUDA", -6: "LK_ERR_DEVICE_TIMEOUT"}
+
+
+class LkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({_load().lk_status_string(status).decode()})")
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built: run q8_quantized_gemv_gb300.build.build() "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, L, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "lk_status_string": ([I], ctypes.c_char_p),
+        "lk_version": ([], I),
+        "lk_rmsnorm_quant": ([P, P, I, I, F, I, P, P, P, P, P], I),
+        "lk_quantize_act": ([P, I, I, I, P, P, P, P], I),
+        "lk_gemv_q8": ([P, P, I, I, I, P, P, P, P, I, P, P, P, P], I),
+        "lk_splitk_workspace_bytes": ([I, I, I, I], S),
+        "lk_gemv_q8_splitk": ([P, P, I, I, I, P, P, P, P, I, I, P, S, P], I),
+        "lk_splitk_combine": ([I, P, I, I, I, P, P], I),
+        "lk_argmax_parts_max": ([I], I),
+        "lk_argmax_scratch_entries": ([I], I),
+        "lk_argmax": ([P, P, I, I, I, P, P, P], I),
+        "lk_q8_block_dots": ([P, I, I, P, P, P, P, P], I),
+        "lk_set_option": ([ctypes.c_char_p, L], I),
+        "lk_get_option": ([ctypes.c_char_p], L),
+        "lk_device_error": ([I, ctypes.POINTER(I)], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def exported_symbols():
+    return ["lk_status_string", "lk_version", "lk_rmsnorm_quant", "lk_quantize_act", "lk_gemv_q8",
+            "lk_splitk_workspace_bytes", "lk_gemv_q8_splitk", "lk_splitk_combine",
+            "lk_argmax_parts_max", "lk_argmax_scratch_entries", "lk_argmax", "lk_q8_block_dots",
+            "lk_set_option", "lk_get_option", "lk_device_error"]
+
+
+def _ok(st, where):
+    if st != 0:
+        raise LkError(st, where)
+
+
+def _mode(mode):
+    return MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+_I8 = torch.int8
+_F32 = torch.float32
+_WS = (torch.int16, torch.float16)
+
+
+def lk_status_string(status: int) -> str:
+    return _load().lk_status_string(status).decode()
+
+
+def lk_version() -> int:
+    return _load().lk_version()
+
+
+def lk_rmsnorm_quant(x, gain, mode, eps=1e-6, xn=None, xq=None, xl=None, xs=None, stream=None):
+    M, K = x.shape
+    _ok(_load().lk_rmsnorm_quant(_ptr(x, _F32, "x"), _ptr(gain, _F32, "gain"), M, K, eps, _mode(mode),
+                                 _ptr(xn, _F32, "xn"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"),
+                                 _ptr(xs, _F32, "xs"), _stream(stream)), "lk_rmsnorm_quant")
+
+
+def lk_quantize_act(x, mode, xq, xl, xs, stream=None):
+    M, K = x.shape
+    _ok(_load().lk_quantize_act(_ptr(x, _F32, "x"), M, K, _mode(mode), _ptr(xq, _I8, "xq"),
+                                _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), _stream(stream)),
+        "lk_quantize_act")
+
+
+def lk_gemv_q8(wq, ws, mode, y, x=None, xq=None, xl=None, xs=None, argmax_parts=None, M=None,
+               stream=None) -> int:
+    """y[M, N] = W x.  Returns the number of argmax partial keys written per
+    activation row (0 when argmax_parts is None)."""
+    N, K = wq.shape
+    if M is None:
+        M = (x if x is not None else xq).shape[0]
+    n = ctypes.c_int(0)
+    _ok(_load().lk_gemv_q8(_ptr(wq, _I8, "wq"), _ptr(ws, _WS, "ws"), N, K, _mode(mode),
+                           _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"),
+                           _ptr(xs, _F32, "xs"), M, _ptr(y, _F32, "y"),
+                           _ptr(argmax_parts, torch.int64, "argmax_parts"),
+                           ctypes.byref(n) if argmax_parts is not None else None, _stream(stream)),
+        "lk_gemv_q8")
+    return n.value
+
+
+def lk_splitk_workspace_bytes(mode, S, M, N) -> int:
+    return _load().lk_splitk_workspace_bytes(_mode(mode), S, M, N)
+
+
+def lk_gemv_q8_splitk(wq, ws, mode, S, part, x=None, xq=None, xl=None, xs=None, M=None, stream=None):
+    N, K = wq.shape
+    if M is None:
+        M = (x if x is not None else xq).shape[0]
+    _ok(_load().lk_gemv_q8_splitk(_ptr(wq, _I8, "wq"), _ptr(ws, _WS, "ws"), N, K, _mode(mode),
+                                  _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"),
+                                  _ptr(xs, _F32, "xs"), M, S, _ptr(part, None, "part"),
+                                  part.numel() * part.element_size(), _stream(stream)),
+        "lk_gemv_q8_splitk")
+
+
+def lk_splitk_combine(mode, part, S, M, N, y, stream=None):
+    _ok(_load().lk_splitk_combine(_mode(mode), _ptr(part, None, "part"), S, M, N, _ptr(y, _F32, "y"),
+                                  _stream(stream)), "lk_splitk_combine")
+
+
+def lk_argmax_parts_max(N) -> int:
+    return _load().lk_argmax_parts_max(N)
+
+
+def lk_argmax_scratch_entries(N) -> int:
+    return _load().lk_argmax_scratch_entries(N)
+
+
+def lk_argmax(idx, M, N, logits=None, parts=None, n_parts=0, scratch=None, stream=None):
+    _ok(_load().lk_argmax(_ptr(logits, _F32, "logits"), _ptr(parts, torch.int64, "parts"), n_parts, M,
+                          N, _ptr(idx, torch.int32, "idx"), _ptr(scratch, torch.int64, "scratch"),
+                          _stream(stream)), "lk_argmax")
+
+
+def lk_q8_block_dots(wq, xq, d, xl=None, e=None, stream=None):
+    N, K = wq.shape
+    _ok(_load().lk_q8_block_dots(_ptr(wq, _I8, "wq"), N, K, _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"),
+                                 _ptr(d, torch.int32, "d"), _ptr(e, torch.int32, "e"), _stream(stream)),
+        "lk_q8_block_dots")
+
+
+def lk_set_option(name: str, value: int):
+    _ok(_load().lk_set_option(name.encode(), int(value)), f"lk_set_option({name})")
+
+
+def lk_get_option(name: str) -> int:
+    return _load().lk_get_option(name.encode())
+
+
+def lk_device_error(reset: bool = True) -> int:
+    code = ctypes.c_int(0)
+    st = _load().lk_device_error(1 if reset else 0, ctypes.byref(code))
+    if st not in (0, -6):
+        raise LkError(st, "lk_device_error")
+    return code.value

@@ -1,0 +1,118 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point that
+include/lk.h declares, and rejects bad arguments on the host before any
+launch.  No GPU: only host-side validation paths are called (the pointers
+below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+torch = pytest.importorskip("torch")
+
+from q8_quantized_gemv_gb300 import build, lk  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return lk._load()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "lk.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lk_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(lk.exported_symbols()) == names
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lk.lk_status_string(code) != "unknown status"
+    assert lk.lk_version() >= 100
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+def P(v):
+    return ctypes.c_void_p(v)
+
+
+def test_gemv_argument_checks(lib):
+    g = lib.lk_gemv_q8
+    ok_ptrs = dict(wq=P(FAKE), ws=P(FAKE), x=P(FAKE), xq=P(FAKE), xl=P(FAKE), xs=P(FAKE), y=P(FAKE))
+
+    def call(N=64, K=64, mode=1, M=1, **kw):
+        a = dict(ok_ptrs, **kw)
+        return g(a["wq"], a["ws"], N, K, mode, a["x"], a["xq"], a["xl"], a["xs"], M, a["y"], None, None,
+                 None)
+
+    assert call(K=48) == -3             # K % 32
+    assert call(M=9) == -3              # M > LK_MAX_M
+    assert call(N=-1) == -3
+    assert call(mode=3) == -1
+    assert call(wq=None) == -1
+    assert call(mode=2, xl=None) == -1  # TwoPass needs the low words
+    assert call(mode=0, x=None) == -1   # Dequant needs f32 x
+    assert call(wq=P(FAKE + 8)) == -2   # 16-byte rows
+    assert call(xq=P(FAKE + 4)) == -2
+    assert call(xs=P(FAKE + 2)) == -2
+    assert call(mode=0, x=P(FAKE + 4)) == -2
+    assert call(N=0) == 0 and call(M=0) == 0  # empty problems launch nothing
+    # argmax parts need the host count pointer
+    a = ok_ptrs
+    assert g(a["wq"], a["ws"], 64, 64, 1, None, a["xq"], None, a["xs"], 1, a["y"], P(FAKE), None,
+             None) == -1
+
+
+def test_splitk_and_combine_checks(lib):
+    f = lib.lk_gemv_q8_splitk
+    args = [P(FAKE), P(FAKE), 64, 256, 1, None, P(FAKE), None, P(FAKE), 1]
+    need = lk.lk_splitk_workspace_bytes(1, 4, 1, 64)
+    assert need == 4 * 64 * 4
+    assert lk.lk_splitk_workspace_bytes(0, 4, 2, 64) == 4 * 2 * 64 * 8
+    assert f(*args, 0, P(FAKE), need, None) == -3
+    assert f(*args, 65, P(FAKE), need, None) == -3
+    assert f(*args, 4, P(FAKE), need - 1, None) == -4
+    assert f(*args, 4, None, need, None) == -1
+    c = lib.lk_splitk_combine
+    assert c(1, P(FAKE), 0, 1, 64, P(FAKE), None) == -3
+    assert c(0, P(FAKE + 4), 2, 1, 64, P(FAKE), None) == -2  # f64 partials
+    assert c(1, P(FAKE), 2, 0, 64, P(FAKE), None) == 0
+
+
+def test_norm_quant_argmax_checks(lib):
+    r = lib.lk_rmsnorm_quant
+    assert r(P(FAKE), P(FAKE), 1, 33, 1e-6, 1, None, P(FAKE), None, P(FAKE), None) == -3
+    assert r(P(FAKE), P(FAKE), 1, 64, 1e-6, 0, None, None, None, None, None) == -1  # Dequant needs xn
+    assert r(P(FAKE), P(FAKE), 1, 64, 1e-6, 2, None, P(FAKE), None, P(FAKE), None) == -1
+    q = lib.lk_quantize_act
+    assert q(P(FAKE), 1, 64, 0, P(FAKE), None, P(FAKE), None) == -1  # nothing to quantize
+    assert q(P(FAKE), 9, 64, 1, P(FAKE), None, P(FAKE), None) == -3
+    a = lib.lk_argmax
+    assert a(P(FAKE), None, 0, 1, 0, P(FAKE), P(FAKE), None) == -3  # N >= 1
+    assert a(P(FAKE), None, 0, 1, 10, P(FAKE), None, None) == -1    # logits form needs scratch
+    assert a(None, P(FAKE), 0, 1, 10, P(FAKE), None, None) == -3    # parts form needs n_parts
+    assert [lk.lk_argmax_scratch_entries(n) for n in (1, 2048, 2049, 151936, 10 ** 8)] == [1, 1, 2, 64, 64]
+    assert lk.lk_argmax_parts_max(151936) >= (151936 + 31) // 32
+
+
+def test_options(lib):
+    assert lk.lk_get_option("gemv_path") == 0
+    lk.lk_set_option("gemv_path", 1)
+    assert lk.lk_get_option("gemv_path") == 1
+    lk.lk_set_option("gemv_path", 0)
+    with pytest.raises(lk.LkError):
+        lk.lk_set_option("gemv_path", 7)
+    with pytest.raises(lk.LkError):
+        lk.lk_set_option("no_such_option", 1)
