@@ -1,0 +1,546 @@
+"""Benchmark: weight-streaming Q8_0 decode projections on GB300.
+
+One step = one decode token through the whole projection path of a synthetic
+36-layer decoder (hidden 4096; q 4096x4096, k and v 1024x4096, o 4096x4096,
+fused gate/up 24576x4096, down 4096x12288, lm-head 151936x4096; RMSNorm ->
+quantize before q/k/v and gate/up; lm-head with the argmax epilogue and the
+argmax reduce), about 8.04 GB of Q8_0 weights per token, batch 1 (or
+--batch 8: 8 activations share each weight read), Int8Act by default.
+
+  value           effective weight GB/s = weight bytes per token / device
+                  time per token, inputs resident in HBM, one CUDA graph per
+                  token (8 GB of weights per step: every step streams from
+                  HBM, nothing fits the 129 MB L2)
+  e2e             the same metric with the token input copied from pinned
+                  host memory and the argmax read back to the host every step
+  roofline        the fused gate/up GEMV launches (the largest share of the
+                  token's bytes), timed with CUDA events around each launch
+  cpu_baseline    the CPU oracle on a bounded sample of the same sequence
+
+``--impl reference`` times the CPU oracle (the reference arm of this
+method, which has no other implementation) on the host cores.
+Multi-GPU: replicas only (each rank runs its own copy of the sequence).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q8_0 GEMV effective weight GB/s (36-layer decode projection sequence, per token)"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mode", default="int8act", choices=["dequant", "int8act", "twopass"])
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=36)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="sequence", choices=["sequence", "gemv"],
+                    help="sequence: the per-token decode projections (default); gemv: one "
+                         "GEMV shape, launched back to back over rotated weight copies")
+    ap.add_argument("--N", type=int, default=24576)
+    ap.add_argument("--K", type=int, default=4096)
+    ap.add_argument("--S", type=int, default=1, help="split-K chunks (gemv workload)")
+    ap.add_argument("--argmax", action="store_true", help="argmax epilogue + reduce (gemv workload)")
+    ap.add_argument("--path", default="auto", choices=["auto", "direct", "ring"])
+    return ap.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+def workload_name(a):
+    return (f"decode projections: {a.layers} layers, hidden 4096, q 4096x4096, k/v 1024x4096, "
+            f"o 4096x4096, gate/up 24576x4096, down 4096x12288, lm-head 151936x4096 + argmax, "
+            f"batch {a.batch}, {a.mode}")
+
+
+# ---- clocks ------------------------------------------------------------------------
+
+class Clocks:
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.rows if t0 <= t <= t1] or [r for (_, r) in self.rows]
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[2]))
+                smax = max(smax, float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- CPU oracle sample ---------------------------------------------------------------
+
+def oracle_layer(oracle, w, mode, x, eps=1e-6):
+    """One layer of the sequence on the CPU oracle; returns (y_down, bytes)."""
+    def acts(v):
+        if mode == oracle.DEQUANT:
+            return dict(x=v)
+        hi, lo, s = oracle.quantize(v, mode)
+        return dict(hi=hi, lo=lo, s=s)
+
+    nbytes = 0
+    a = acts(oracle.rmsnorm(x, w["g_attn"], mode, eps))
+    for n in ("q", "k", "v"):
+        oracle.gemv(w[n][0], w[n][1], mode, **a)
+        nbytes += w[n][0].size * 17 // 16
+    o = oracle.gemv(w["o"][0], w["o"][1], mode, **acts(w["o_in"]))
+    nbytes += w["o"][0].size * 17 // 16
+    a = acts(oracle.rmsnorm(o, w["g_mlp"], mode, eps))
+    oracle.gemv(w["gu"][0], w["gu"][1], mode, **a)
+    nbytes += w["gu"][0].size * 17 // 16
+    h = oracle.gemv(w["down"][0], w["down"][1], mode, **acts(w["d_in"]))
+    nbytes += w["down"][0].size * 17 // 16
+    return h, nbytes
+
+
+def host_layer(stack_or_none, l, B, mode_seed=0):
+    """Host (numpy) copy of layer l's inputs, from the device stack when given,
+    else freshly drawn with the same recipe."""
+    import numpy as np
+
+    from q8_quantized_gemv_gb300 import synth
+    if stack_or_none is not None:
+        w = stack_or_none.layers[l]
+        out = {}
+        for n in ("q", "k", "v", "o", "gu", "down"):
+            out[n] = (w[n][0].cpu().numpy(), w[n][1].cpu().numpy().view(np.uint16))
+        for n in ("g_attn", "g_mlp", "o_in", "d_in"):
+            out[n] = w[n].cpu().numpy()
+        return out
+    shapes = {"q": (4096, 4096), "k": (1024, 4096), "v": (1024, 4096), "o": (4096, 4096),
+              "gu": (24576, 4096), "down": (4096, 12288)}
+    s = synth.SEED_BASE + 4 + 1000 * l + mode_seed
+    out = {n: synth.q8_matrix(N, K, s + i) for i, (n, (N, K)) in enumerate(shapes.items())}
+    out["g_attn"] = synth.norm_gain(4096, s + 10)
+    out["g_mlp"] = synth.norm_gain(4096, s + 11)
+    out["o_in"] = synth.activation(B, 4096, s + 12, outliers=True)
+    out["d_in"] = synth.activation(B, 12288, s + 13, outliers=True)
+    return out
+
+
+def cpu_baseline(stack, a, budget_s):
+    import oracle
+
+    mode = {"dequant": 0, "int8act": 1, "twopass": 2}[a.mode]
+    import numpy as np
+    x = stack.x0.cpu().numpy() if stack is not None else np.ones((a.batch, 4096), np.float32)
+    tot_b, tot_t, layers = 0, 0.0, 0
+    for l in range(a.layers):
+        w = host_layer(stack, l, a.batch)
+        t0 = time.perf_counter()
+        x, nb = oracle_layer(oracle, w, mode, x)
+        tot_t += time.perf_counter() - t0
+        tot_b += nb
+        layers += 1
+        if tot_t >= budget_s:
+            break
+    return {"value": tot_b / tot_t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"layers 0..{layers - 1} of the sequence (full matrices, norm + quantize + "
+                      f"6 GEMVs each, batch {a.batch}, {a.mode}), single-threaded C oracle",
+            "seconds": tot_t}
+
+
+# ---- reference arm: the CPU oracle -----------------------------------------------------
+
+def run_reference(a, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    mode = {"dequant": 0, "int8act": 1, "twopass": 2}[a.mode]
+    import numpy as np
+    layers = [host_layer(None, l, a.batch) for l in range(2)]
+    x0 = np.ones((a.batch, 4096), np.float32)
+
+    def step():
+        x, nb = x0, 0
+        for w in layers:
+            x, b = oracle_layer(oracle, w, mode, x)
+            nb += b
+        return nb
+
+    for _ in range(a.warmup):
+        step()
+    t0 = time.perf_counter()
+    nb = 0
+    for _ in range(a.steps):
+        nb += step()
+    dt = time.perf_counter() - t0
+    value = nb / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt / a.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": _dtype(a.mode),
+        "data": "synthetic", "config": {"workload": workload_name(a),
+                                        "sample": "2 of the layers per step, on the host"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "each step: layers 0-1 of the sequence (full matrices) in the "
+                                   "single-threaded C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def _dtype(mode):
+    return {"dequant": "f32 x int8 -> f64", "int8act": "int8 x int8 -> int32, f32 combine",
+            "twopass": "2x int8 x int8 -> int32, f32 combine"}[mode]
+
+
+# ---- our arm ---------------------------------------------------------------------------------
+
+def run_ours(a, rank, world):
+    import torch
+
+    from q8_quantized_gemv_gb300 import build, lk
+    from q8_quantized_gemv_gb300.decode import DecodeStack
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev)
+    tok_bytes = stack.weight_bytes()
+    stream = torch.cuda.Stream(device=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # eager warm-up (also sets any per-kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            stack.run_token()
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) == 0
+
+    # one CUDA graph per token
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        stack.run_token()
+    x_in = torch.empty_like(stack.x0)
+    graph_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_e2e, stream=stream):
+        stack.run_token(x_in=x_in)
+
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.5)
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K tokens, inputs resident -------------------------------------
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    tw0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(a.steps):
+            graph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    barrier()
+    ms = ev0.elapsed_time(ev1) / a.steps
+    clk = clocks.summary(tw0, tw1)
+    clocks.stop()
+    ms_max = _max_over_ranks(ms, dist, dev)
+    value = tok_bytes * world / (ms_max * 1e-3) / 1e9
+
+    # ---- e2e: pinned host input -> device, graph, argmax -> pinned host, every step ------
+    x_host = stack.x0.cpu().pin_memory()
+    idx_host = torch.empty_like(stack.idx, device="cpu").pin_memory()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            x_in.copy_(x_host, non_blocking=True)
+            graph_e2e.replay()
+            idx_host.copy_(stack.idx, non_blocking=True)
+            stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(1, min(a.steps, 200))
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_e2e):
+            x_in.copy_(x_host, non_blocking=True)
+            graph_e2e.replay()
+            idx_host.copy_(stack.idx, non_blocking=True)
+            stream.synchronize()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = _max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, dev)
+    e2e = {"value": tok_bytes * world / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
+           "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": idx_host.numel() * 4,
+           "ms_per_step": ms_e2e, "steps": n_e2e}
+
+    # ---- roofline: CUDA events around every GEMV launch, one graph per token -------------
+    roof, per_name = roofline(stack, stream, a, torch)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": _dtype(a.mode), "data": "synthetic (seeded, see DESIGN.md)",
+        "config": {"workload": workload_name(a), "weight_bytes_per_step": tok_bytes,
+                   "l2": "inputs larger than L2 (8.04 GB of weights per step)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "gemv_path": "auto"},
+        "us_per_token": ms_max * 1e3,
+        "pct_of_nominal_8TBs": value / world / NOMINAL_HBM_GBS,
+        "roofline": roof,
+        "gemv_by_projection": per_name,
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": stack.launches_per_token() * a.steps,
+    }
+    if rank == 0 and not a.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(stack, a, a.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _timing_event(torch, external):
+    if external:
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+    return torch.cuda.Event(enable_timing=True)
+
+
+def run_gemv(a, rank, world):
+    """One GEMV shape: per-launch CUDA-event durations over weight copies
+    rotated so that every launch streams from HBM (copies x bytes >= 4 x L2)."""
+    import torch
+
+    from q8_quantized_gemv_gb300 import build, lk, synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    lk.lk_set_option("gemv_path", {"auto": 0, "direct": 1, "ring": 2}[a.path])
+    mode = lk.MODES[a.mode]
+    N, K, B, S = a.N, a.K, a.batch, a.S
+    wbytes = N * K + N * K // 16
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, -(-4 * l2 // wbytes))
+    mats = [synth.q8_matrix_torch(N, K, synth.SEED_BASE + 50 + r, dev) for r in range(R)]
+    x = synth.activation_torch(B, K, synth.SEED_BASE + 49, dev, outliers=True)
+    acts = {"x": x}
+    if mode != lk.LK_DEQUANT:
+        xq = torch.empty((B, K), dtype=torch.int8, device=dev)
+        xl = torch.empty((B, K), dtype=torch.int8, device=dev) if mode == lk.LK_TWOPASS else None
+        xs = torch.empty((B, K // 32), dtype=torch.float32, device=dev)
+        lk.lk_quantize_act(x, mode, xq, xl, xs)
+        acts = {"xq": xq, "xl": xl, "xs": xs}
+    y = torch.empty((B, N), dtype=torch.float32, device=dev)
+    parts = torch.zeros((B * lk.lk_argmax_parts_max(N),), dtype=torch.int64, device=dev) if a.argmax else None
+    idx = torch.empty((B,), dtype=torch.int32, device=dev)
+    part = None
+    if S > 1:
+        part = torch.empty((lk.lk_splitk_workspace_bytes(mode, S, B, N),), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch(r):
+        wq, ws = mats[r % R]
+        if S > 1:
+            lk.lk_gemv_q8_splitk(wq, ws, mode, S, part, M=B, **acts)
+            lk.lk_splitk_combine(mode, part, S, B, N, y)
+        else:
+            n = lk.lk_gemv_q8(wq, ws, mode, y, M=B, argmax_parts=parts, **acts)
+            if a.argmax:
+                lk.lk_argmax(idx, B, N, parts=parts, n_parts=n)
+
+    with torch.cuda.stream(stream):
+        for r in range(max(a.warmup, 3)):
+            launch(r)
+    torch.cuda.synchronize()
+    evs = [(_timing_event(torch, False), _timing_event(torch, False)) for _ in range(a.steps)]
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    tw0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(a.steps):
+            evs[i][0].record(stream)
+            launch(i)
+            evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    clk = clocks.summary(tw0, tw1)
+    clocks.stop()
+    us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+    act_b = B * K * 4 if mode == lk.LK_DEQUANT else B * K * (2 if mode == lk.LK_TWOPASS else 1) + B * (K // 32) * 4
+    alg = wbytes + act_b + B * N * 4 + (2 * S * B * N * (8 if mode == lk.LK_DEQUANT else 4) if S > 1 else 0)
+    peaks, src = measured_peaks()
+    gbs = wbytes / (us * 1e-6) / 1e9
+    out = {"metric": "Q8_0 GEMV effective weight GB/s", "value": gbs, "unit": UNIT, "n_gpus": world,
+           "steps": a.steps, "warmup": a.warmup, "ms_per_step": us * 1e-3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": _dtype(a.mode), "data": "synthetic",
+           "config": {"workload": f"Q8_0 GEMV N={N} K={K} batch {B} {a.mode} S={S}"
+                                  + (" + argmax" if a.argmax else ""),
+                      "rotation": f"{R} weight copies ({R * wbytes} bytes >= 4x L2)", "path": a.path},
+           "us_per_gemv": us, "pct_of_nominal_8TBs": gbs / NOMINAL_HBM_GBS,
+           "roofline": {"bound": "hbm", "achieved": alg / (us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": alg / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                        "peak_source": src, "algorithmic_bytes_per_launch": alg},
+           "clocks": clk, "gpu_launches": a.steps * (2 if (S > 1 or a.argmax) else 1)}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def _max_over_ranks(v, dist, dev):
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def roofline(stack, stream, a, torch):
+    peaks, src = measured_peaks()
+    steps = max(1, min(a.steps, 50))
+    graphs, marks = [], []
+    for _ in range(steps):
+        evs = []
+
+        def hook(name, launch, evs=evs):
+            e0 = _timing_event(torch, True)
+            e1 = _timing_event(torch, True)
+            if e0 is None:
+                raise RuntimeError("this torch has no external CUDA events")
+            e0.record(stream)
+            r = launch()
+            e1.record(stream)
+            evs.append((name, e0, e1))
+            return r
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            stack.run_token(hook=hook)
+        graphs.append(g)
+        marks.append(evs)
+    with torch.cuda.stream(stream):
+        graphs[0].replay()
+        torch.cuda.synchronize()
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    # the evs of each graph hold that replay's times
+    times = {}
+    for evs in marks:
+        for name, e0, e1 in evs:
+            times.setdefault(name, []).append(e0.elapsed_time(e1))
+    B = stack.B
+    act_b = B * (1 if stack.mode != 2 else 2)
+
+    def alg_bytes(name):
+        if name == "lm":
+            N, K = stack.V, stack.H
+        else:
+            N, K = stack.shapes[name]
+        return N * K + N * K // 16 + (act_b * K + B * (K // 32) * 4 if stack.mode else B * K * 4) + B * N * 4
+
+    per = {}
+    for name, ts in times.items():
+        avg = sum(ts) / len(ts)
+        per[name] = {"us": avg * 1e3, "GB/s": alg_bytes(name) / (avg * 1e-3) / 1e9, "launches": len(ts)}
+    gu = per["gu"]
+    peak = peaks["hbm_gbs"]
+    traffic = None
+    roof = {"bound": "hbm", "achieved": gu["GB/s"], "peak": peak, "unit": "GB/s",
+            "frac": gu["GB/s"] / peak, "traffic": traffic, "peak_source": src,
+            "kernel": "fused gate/up GEMV 24576x4096", "algorithmic_bytes_per_launch": alg_bytes("gu"),
+            "avg_launch_us": gu["us"], "launches_timed": gu["launches"]}
+    tot_b = sum(alg_bytes(n) * len(ts) for n, ts in times.items())
+    tot_t = sum(sum(ts) for ts in times.values())
+    roof["all_gemv_achieved"] = tot_b / (tot_t * 1e-3) / 1e9
+    return roof, per
+
+
+def main():
+    a = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if a.impl == "reference":
+        run_reference(a, rank)
+        return
+    if a.workload == "gemv":
+        run_gemv(a, rank, world)
+        return
+    run_ours(a, rank, world)
+
+
+if __name__ == "__main__":
+    main()

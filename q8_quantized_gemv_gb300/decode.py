@@ -1,0 +1,128 @@
+"""The per-token projection sequence of a synthetic decoder, run through the
+C ABI: per layer RMSNorm -> quantize -> q, k, v; quantize -> o; RMSNorm ->
+quantize -> fused gate/up; quantize -> down; then RMSNorm -> quantize ->
+lm-head with the argmax epilogue -> argmax.
+
+Attention and the gated activation are not part of the projection path, so
+the inputs they would produce are fixed seeded vectors: the o-projection's and
+the down-projection's inputs are N(0,1) with 1% x20 outliers, one per layer,
+quantized every token.  The residual stream is the chain of projection
+outputs: the o output feeds the MLP norm and the down output feeds the next
+layer's attention norm.
+
+Weights live on the device for the life of the object (about 8 GB for the
+36-layer, hidden-4096 configuration); every buffer is allocated once here and
+``run_token`` only launches kernels, so it can be captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import lk, synth
+
+
+class DecodeStack:
+    def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
+                 batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6):
+        self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
+        self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
+        dev = self.dev
+        s = seed
+        self.shapes = {"q": (q_dim, hidden), "k": (kv_dim, hidden), "v": (kv_dim, hidden),
+                       "o": (hidden, q_dim), "gu": (2 * ffn, hidden), "down": (hidden, ffn)}
+        self.layers = []
+        for l in range(layers):
+            w = {}
+            for i, (name, (N, K)) in enumerate(self.shapes.items()):
+                w[name] = synth.q8_matrix_torch(N, K, s + 1000 * l + i, dev)
+            w["g_attn"] = synth.norm_gain_torch(hidden, s + 1000 * l + 10, dev)
+            w["g_mlp"] = synth.norm_gain_torch(hidden, s + 1000 * l + 11, dev)
+            w["o_in"] = synth.activation_torch(batch, q_dim, s + 1000 * l + 12, dev, outliers=True)
+            w["d_in"] = synth.activation_torch(batch, ffn, s + 1000 * l + 13, dev, outliers=True)
+            self.layers.append(w)
+        self.lm = synth.q8_matrix_torch(vocab, hidden, s + 999_000, dev)
+        self.g_final = synth.norm_gain_torch(hidden, s + 999_001, dev)
+        self.x0 = synth.activation_torch(batch, hidden, s + 999_002, dev, outliers=True)
+
+        f32, i8 = torch.float32, torch.int8
+        B = batch
+        self.h = torch.empty((B, hidden), dtype=f32, device=dev)        # residual stream
+        self.xn = torch.empty((B, hidden), dtype=f32, device=dev)       # normed (Dequant GEMV input)
+        self.acts = {K: self._act_bufs(K) for K in {hidden, q_dim, ffn}}
+        self.out = {name: torch.empty((B, N), dtype=f32, device=dev) for name, (N, _) in self.shapes.items()}
+        self.logits = torch.empty((B, vocab), dtype=f32, device=dev)
+        self.parts = torch.zeros((B * lk.lk_argmax_parts_max(vocab),), dtype=torch.int64, device=dev)
+        self.idx = torch.empty((B,), dtype=torch.int32, device=dev)
+        self.n_parts = 0
+
+    def _act_bufs(self, K):
+        B = self.B
+        d = {"xq": torch.empty((B, K), dtype=torch.int8, device=self.dev),
+             "xs": torch.empty((B, K // 32), dtype=torch.float32, device=self.dev)}
+        if self.mode == lk.LK_TWOPASS:
+            d["xl"] = torch.empty((B, K), dtype=torch.int8, device=self.dev)
+        return d
+
+    # -- the launches of one token ---------------------------------------------------
+    def _norm(self, x, g):
+        """RMSNorm -> quantize; returns the GEMV activation arguments."""
+        if self.mode == lk.LK_DEQUANT:
+            lk.lk_rmsnorm_quant(x, g, self.mode, self.eps, self.xn)
+            return {"x": self.xn}
+        a = self.acts[x.shape[1]]
+        lk.lk_rmsnorm_quant(x, g, self.mode, self.eps, None, a["xq"], a.get("xl"), a["xs"])
+        return a
+
+    def _quant(self, x):
+        if self.mode == lk.LK_DEQUANT:
+            return {"x": x}
+        a = self.acts[x.shape[1]]
+        lk.lk_quantize_act(x, self.mode, a["xq"], a.get("xl"), a["xs"])
+        return a
+
+    def _gemv(self, w, y, acts, parts=None):
+        return lk.lk_gemv_q8(w[0], w[1], self.mode, y, M=self.B, argmax_parts=parts, **acts)
+
+    def run_token(self, x_in=None, hook=None):
+        """Launch one token's sequence on the current stream and return the
+        device int32 [B] argmax.  ``hook``, if given, is called as
+        hook(name, launch) around each GEMV launch (for per-kernel timing)."""
+        def g(name, w, y, a, parts=None):
+            if hook is None:
+                return self._gemv(w, y, a, parts)
+            return hook(name, lambda: self._gemv(w, y, a, parts))
+
+        x = self.x0 if x_in is None else x_in
+        for w in self.layers:
+            a = self._norm(x, w["g_attn"])
+            g("q", w["q"], self.out["q"], a)
+            g("k", w["k"], self.out["k"], a)
+            g("v", w["v"], self.out["v"], a)
+            a = self._quant(w["o_in"])
+            g("o", w["o"], self.out["o"], a)
+            a = self._norm(self.out["o"], w["g_mlp"])
+            g("gu", w["gu"], self.out["gu"], a)
+            a = self._quant(w["d_in"])
+            g("down", w["down"], self.h, a)
+            x = self.h
+        a = self._norm(x, self.g_final)
+        self.n_parts = g("lm", self.lm, self.logits, a, self.parts)
+        lk.lk_argmax(self.idx, self.B, self.V, parts=self.parts, n_parts=self.n_parts)
+        return self.idx
+
+    # -- accounting ------------------------------------------------------------------------
+    def weight_bytes(self, name=None):
+        """Algorithmic weight bytes (N*K levels + N*K/16 scale bytes)."""
+        def mb(N, K):
+            return N * K + N * K // 16
+        if name == "lm":
+            return mb(self.V, self.H)
+        if name is not None:
+            return mb(*self.shapes[name])
+        return self.L * sum(mb(N, K) for N, K in self.shapes.values()) + mb(self.V, self.H)
+
+    def launches_per_token(self):
+        norm_quant = 2 * self.L + 1
+        quant = 0 if self.mode == lk.LK_DEQUANT else 2 * self.L
+        gemv = 6 * self.L + 1
+        return norm_quant + quant + gemv + 1  # + argmax reduce
