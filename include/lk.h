@@ -187,7 +187,8 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *   "gemv_path"   0 auto, 1 direct-load kernel, 2 bulk-copy ring kernel
  *   "ring_stages" ring depth of the bulk-copy kernel (0 = default)
  *   "grid_ctas"   blocks of the ring kernel (0 = one per SM)
- *   "wait_cap"    iteration cap of every device-side wait (0 = default)
+ *   "wait_us"     time limit of every device-side wait, microseconds
+ *                 (0 = default, 2 s)
  * Unknown names or out-of-range values return LK_ERR_ARG.
  */
 lk_status lk_set_option(const char* name, long value);
@@ -200,6 +201,15 @@ long lk_get_option(const char* name);
  * reset != 0 clears the word.
  */
 lk_status lk_device_error(int reset, int* code);
+
+/*
+ * Test hook of the failure path: launches one block that waits, with the
+ * library's bounded wait, on an mbarrier that nothing completes.  The wait
+ * gives up after limit_us microseconds (1 .. 10^7), sets the device error
+ * word and returns; lk_device_error then reports LK_ERR_DEVICE_TIMEOUT and the
+ * context stays usable.
+ */
+lk_status lk_selftest_wait_timeout(unsigned limit_us, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -13,7 +13,7 @@ namespace lkh {
 long opt_gemv_path = 0;
 long opt_ring_stages = 0;
 long opt_grid_ctas = 0;
-long opt_wait_cap = 0;
+long opt_wait_us = 0;
 
 static const int kMaxDevices = 64;
 static DeviceInfo g_info[kMaxDevices];
@@ -146,9 +146,9 @@ lk_status lk_set_option(const char* name, long value) {
   } else if (!strcmp(name, "grid_ctas")) {
     if (value < 0 || value > (1L << 20)) return LK_ERR_ARG;
     opt_grid_ctas = value;
-  } else if (!strcmp(name, "wait_cap")) {
-    if (value < 0) return LK_ERR_ARG;
-    opt_wait_cap = value;
+  } else if (!strcmp(name, "wait_us")) {
+    if (value < 0 || value > 60000000L) return LK_ERR_ARG;
+    opt_wait_us = value;
   } else {
     return LK_ERR_ARG;
   }
@@ -160,7 +160,7 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "gemv_path")) return opt_gemv_path;
   if (!strcmp(name, "ring_stages")) return opt_ring_stages;
   if (!strcmp(name, "grid_ctas")) return opt_grid_ctas;
-  if (!strcmp(name, "wait_cap")) return opt_wait_cap;
+  if (!strcmp(name, "wait_us")) return opt_wait_us;
   return -1;
 }
 

@@ -205,6 +205,7 @@ GemvProblem make_problem(const int8_t* wq, const uint16_t* ws, int N, int K, lk_
   p.xs = xs;
   p.M = M;
   p.S = 1;
+  p.split = false;
   p.y = nullptr;
   p.part64 = nullptr;
   p.amax = nullptr;
@@ -277,6 +278,7 @@ lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, 
   if (part_bytes < lk_splitk_workspace_bytes(mode, S, M, N)) return LK_ERR_WORKSPACE;
   GemvProblem p = make_problem(wq, ws, N, K, mode, x, xq, xl, xs, M);
   p.S = S;
+  p.split = true;
   if (mode == LK_DEQUANT) p.part64 = (double*)part;
   else p.y = (float*)part;
   if (opt_gemv_path != 1 && ring_supports(p)) return ring_gemv(p, stream, nullptr);

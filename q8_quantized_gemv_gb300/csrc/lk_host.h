@@ -23,7 +23,7 @@ const DeviceInfo* device_info(int* dev_out);
 extern long opt_gemv_path;    // 0 auto, 1 direct, 2 ring
 extern long opt_ring_stages;  // 0 default
 extern long opt_grid_ctas;    // 0 default
-extern long opt_wait_cap;     // 0 default
+extern long opt_wait_us;      // bound of every device-side wait, microseconds (0 = 2 s)
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
@@ -44,7 +44,8 @@ struct GemvProblem {
   const int8_t* xl;
   const float* xs;
   int M;
-  int S;                         // 1 = plain GEMV
+  int S;                         // split-K chunks (1 for the plain GEMV)
+  bool split;                    // write split-K partials instead of y
   float* y;                      // plain: y [M][N]; split quantized: part f32 [S][M][N]
   double* part64;                // split Dequant: part f64 [S][M][N]
   unsigned long long* amax;      // plain only: [M][n_parts]

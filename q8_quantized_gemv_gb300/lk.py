@@ -59,6 +59,7 @@ def _load():
         "lk_set_option": ([ctypes.c_char_p, L], I),
         "lk_get_option": ([ctypes.c_char_p], L),
         "lk_device_error": ([I, ctypes.POINTER(I)], I),
+        "lk_selftest_wait_timeout": ([ctypes.c_uint, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -72,7 +73,7 @@ def exported_symbols():
     return ["lk_status_string", "lk_version", "lk_rmsnorm_quant", "lk_quantize_act", "lk_gemv_q8",
             "lk_splitk_workspace_bytes", "lk_gemv_q8_splitk", "lk_splitk_combine",
             "lk_argmax_parts_max", "lk_argmax_scratch_entries", "lk_argmax", "lk_q8_block_dots",
-            "lk_set_option", "lk_get_option", "lk_device_error"]
+            "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout"]
 
 
 def _ok(st, where):
@@ -205,3 +206,7 @@ def lk_device_error(reset: bool = True) -> int:
     if st not in (0, -6):
         raise LkError(st, "lk_device_error")
     return code.value
+
+
+def lk_selftest_wait_timeout(limit_us: int, stream=None):
+    _ok(_load().lk_selftest_wait_timeout(int(limit_us), _stream(stream)), "lk_selftest_wait_timeout")

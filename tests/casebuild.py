@@ -17,11 +17,13 @@ def parse_scale(tok):
     return float(tok)
 
 
-def block_case(K, blocks):
+def block_case(K, blocks, pad_to=None):
     """Inputs of an order example: every block's activation group is
     [127,127,127,127,4,1,0,...] (s = 1 and hi = the values); a block listed
     as b:scale:d gets weight levels giving dot d and that f16 scale; other
-    blocks have zero weights and scale 1."""
+    blocks have zero weights and scale 1.  pad_to appends zero-weight blocks
+    up to that K (each adds an exact zero step, so the results do not change)."""
+    K = max(K, pad_to or 0)
     nb = K // 32
     x = np.zeros((1, K), np.float32)
     wq = np.zeros((1, K), np.int8)
@@ -43,8 +45,8 @@ def block_case(K, blocks):
     return wq, f16_bits(sc).reshape(1, nb), x
 
 
-def lo_case(rec):
-    K = int(rec["K"])
+def lo_case(rec, pad_to=None):
+    K = max(int(rec["K"]), pad_to or 0)
     x = np.zeros((1, K), np.float32)
     act = [float(v) for v in rec["act"].split()]
     x[0, : len(act)] = act

@@ -18,7 +18,7 @@ from q8_quantized_gemv_gb300 import build, lk, synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 DQ, I8, TP = 0, 1, 2
-PATHS = {"direct": 1}
+PATHS = {"direct": 1, "ring": 2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -36,6 +36,12 @@ def path(request):
     lk.lk_set_option("gemv_path", PATHS[request.param])
     yield request.param
     lk.lk_set_option("gemv_path", 0)
+
+
+def need(path, K):
+    """The bulk-copy ring kernel takes K % 256 == 0 (16-byte aligned scale rows)."""
+    if path == "ring" and (K < 256 or K % 256):
+        pytest.skip("ring kernel needs K % 256 == 0")
 
 
 def sync_check():
@@ -129,13 +135,15 @@ def test_block_dots_exact(N, K):
 
 # ---- GEMV --------------------------------------------------------------------------
 
-SHAPES = [(33, 32), (37, 544), (100, 4096), (1024, 1024), (257, 1056)]
+SHAPES = [(33, 32), (37, 544), (100, 4096), (1024, 1024), (257, 1056), (33, 256), (300, 1280),
+          (1000, 512)]
 
 
 @pytest.mark.parametrize("mode", [DQ, I8, TP])
 @pytest.mark.parametrize("M", [1, 2, 5, 8])
 @pytest.mark.parametrize("N,K", SHAPES)
 def test_gemv_parity(path, mode, M, N, K):
+    need(path, K)
     wq, ws = synth.q8_matrix(N, K, 4000 + N + K)
     x = synth.activation(M, K, 4001 + M, outliers=True)
     y_or = oracle.gemv(wq, ws, mode, **oracle_acts(x, mode))
@@ -166,7 +174,9 @@ def test_gemv_batch_invariance(path, mode):
 @pytest.mark.parametrize("mode", ["dequant", "int8act", "twopass"])
 def test_gemv_order_fixture_on_gpu(path, name, mode):
     rec = order_records()[name]
-    wq, ws, x = block_case(int(rec["K"]), rec["blocks"])
+    K = int(rec["K"])
+    pad = -(-K // 256) * 256 if path == "ring" else None  # zero-weight blocks up to K % 256 == 0
+    wq, ws, x = block_case(K, rec["blocks"], pad_to=pad)
     m = MODES[mode]
     y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), 1)
     sync_check()
@@ -176,7 +186,7 @@ def test_gemv_order_fixture_on_gpu(path, name, mode):
 @pytest.mark.parametrize("mode", ["dequant", "int8act", "twopass"])
 def test_gemv_low_word_fixture_on_gpu(path, mode):
     rec = order_records()["gemv_lo"]
-    wq, ws, x = lo_case(rec)
+    wq, ws, x = lo_case(rec, pad_to=256 if path == "ring" else None)
     m = MODES[mode]
     y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), 1)
     sync_check()
@@ -198,8 +208,9 @@ def test_gemv_k_zero_and_empty():
 
 @pytest.mark.parametrize("mode", [DQ, I8, TP])
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 8])
-@pytest.mark.parametrize("N,K,M", [(37, 544, 1), (64, 5120, 2), (40, 1024, 8)])
+@pytest.mark.parametrize("N,K,M", [(37, 544, 1), (64, 5120, 2), (40, 1024, 8), (300, 2304, 3)])
 def test_splitk_parity(path, mode, S, N, K, M):
+    need(path, K)
     wq, ws = synth.q8_matrix(N, K, 5000 + K)
     x = synth.activation(M, K, 5001, outliers=True)
     y_or, ch_or = oracle.gemv_splitk(wq, ws, mode, S, **oracle_acts(x, mode))
@@ -235,6 +246,7 @@ def test_splitk_parity(path, mode, S, N, K, M):
 def test_splitk_combine_fixture_on_gpu(path, mode):
     rec = order_records()["splitk_combine"]
     K, S = int(rec["K"]), int(rec["S"])
+    need(path, K)
     wq, ws, x = block_case(K, rec["blocks"])
     m = MODES[mode]
     part = torch.zeros((S, 1, 1), dtype=torch.float64 if m == DQ else torch.float32, device=DEV)
@@ -288,3 +300,24 @@ def test_gemv_argmax_epilogue_planted_ties(path, mode):
     assert want[0] == 31
     assert host(idx).tolist() == want
     assert_gemv_close(host(y), y_or, wq, ws, x, mode)
+
+
+# ---- failure path: a bounded device wait gives up without hanging the GPU ------------
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    lk.lk_device_error(reset=True)
+    lk.lk_selftest_wait_timeout(2000)  # 2 ms on an mbarrier nothing completes
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) != 0
+    assert lk.lk_device_error(reset=True) == 0
+    # the context is still usable: a GEMV on each path matches the oracle
+    N, K = 64, 512
+    wq, ws = synth.q8_matrix(N, K, 7000)
+    x = synth.activation(1, K, 7001)
+    y_or = oracle.gemv(wq, ws, I8, **oracle_acts(x, I8))
+    for p in (1, 2):
+        lk.lk_set_option("gemv_path", p)
+        y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), I8, dev_acts(x, I8), 1)
+        sync_check()
+        assert np.array_equal(bits(host(y)), bits(y_or))
+    lk.lk_set_option("gemv_path", 0)
