@@ -59,6 +59,11 @@ def parse():
     ap.add_argument("--S", type=int, default=1, help="split-K chunks (gemv workload)")
     ap.add_argument("--argmax", action="store_true", help="argmax epilogue + reduce (gemv workload)")
     ap.add_argument("--path", default="auto", choices=["auto", "direct", "ring"])
+    ap.add_argument("--unfused", action="store_true",
+                    help="sequence: separate norm/quantize launches instead of the fused prologue")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="no programmatic dependent launches between the fused GEMVs")
+    ap.add_argument("--fused", action="store_true", help="gemv workload: RMSNorm->quantize->GEMV in one launch")
     return ap.parse_args()
 
 
@@ -263,7 +268,8 @@ def run_ours(a, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev)
+    lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
+    stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=not a.unfused)
     tok_bytes = stack.weight_bytes()
     stream = torch.cuda.Stream(device=dev)
 
@@ -351,7 +357,8 @@ def run_ours(a, rank, world):
         "config": {"workload": workload_name(a), "weight_bytes_per_step": tok_bytes,
                    "l2": "inputs larger than L2 (8.04 GB of weights per step)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "gemv_path": "auto"},
+                   "gemv_path": "auto", "fused_prologue": {k: v for k, v in stack.fused.items()},
+                   "pdl": not a.no_pdl},
         "us_per_token": ms_max * 1e3,
         "pct_of_nominal_8TBs": value / world / NOMINAL_HBM_GBS,
         "roofline": roof,
@@ -389,6 +396,7 @@ def run_gemv(a, rank, world):
     dev = torch.device("cuda", local)
     build.build()
     lk.lk_set_option("gemv_path", {"auto": 0, "direct": 1, "ring": 2}[a.path])
+    lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
     mode = lk.MODES[a.mode]
     N, K, B, S = a.N, a.K, a.batch, a.S
     wbytes = N * K + N * K // 16
@@ -411,9 +419,15 @@ def run_gemv(a, rank, world):
         part = torch.empty((lk.lk_splitk_workspace_bytes(mode, S, B, N),), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
+    gain = synth.norm_gain_torch(K, synth.SEED_BASE + 48, dev)
+
     def launch(r):
         wq, ws = mats[r % R]
-        if S > 1:
+        if a.fused:
+            n = lk.lk_rmsnorm_quant_gemv_q8(wq, ws, mode, x, y, gain=gain, argmax_parts=parts)
+            if a.argmax:
+                lk.lk_argmax(idx, B, N, parts=parts, n_parts=n)
+        elif S > 1:
             lk.lk_gemv_q8_splitk(wq, ws, mode, S, part, M=B, **acts)
             lk.lk_splitk_combine(mode, part, S, B, N, y)
         else:
@@ -425,21 +439,32 @@ def run_gemv(a, rank, world):
         for r in range(max(a.warmup, 3)):
             launch(r)
     torch.cuda.synchronize()
-    evs = [(_timing_event(torch, False), _timing_event(torch, False)) for _ in range(a.steps)]
+    # R back-to-back launches over the rotated copies, captured once, replayed
+    # `steps` times: the per-launch time carries no host launch gaps
+    Rg = max(R, 8)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for r in range(Rg):
+            launch(r)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     tw0 = time.time()
     with torch.cuda.stream(stream):
-        for i in range(a.steps):
-            evs[i][0].record(stream)
-            launch(i)
-            evs[i][1].record(stream)
+        e0.record(stream)
+        for _ in range(a.steps):
+            graph.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     tw1 = time.time()
     clk = clocks.summary(tw0, tw1)
     clocks.stop()
-    us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+    us = e0.elapsed_time(e1) * 1e3 / (a.steps * Rg)
     act_b = B * K * 4 if mode == lk.LK_DEQUANT else B * K * (2 if mode == lk.LK_TWOPASS else 1) + B * (K // 32) * 4
     alg = wbytes + act_b + B * N * 4 + (2 * S * B * N * (8 if mode == lk.LK_DEQUANT else 4) if S > 1 else 0)
     peaks, src = measured_peaks()
@@ -448,13 +473,15 @@ def run_gemv(a, rank, world):
            "steps": a.steps, "warmup": a.warmup, "ms_per_step": us * 1e-3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": _dtype(a.mode), "data": "synthetic",
            "config": {"workload": f"Q8_0 GEMV N={N} K={K} batch {B} {a.mode} S={S}"
-                                  + (" + argmax" if a.argmax else ""),
-                      "rotation": f"{R} weight copies ({R * wbytes} bytes >= 4x L2)", "path": a.path},
+                                  + (" + argmax" if a.argmax else "") + (" fused norm+quant" if a.fused else ""),
+                      "rotation": f"{R} weight copies ({R * wbytes} bytes >= 4x L2), {max(R, 8)} launches per graph",
+                      "path": a.path},
            "us_per_gemv": us, "pct_of_nominal_8TBs": gbs / NOMINAL_HBM_GBS,
            "roofline": {"bound": "hbm", "achieved": alg / (us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": alg / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], "traffic": None,
                         "peak_source": src, "algorithmic_bytes_per_launch": alg},
-           "clocks": clk, "gpu_launches": a.steps * (2 if (S > 1 or a.argmax) else 1)}
+           "clocks": clk, "gpu_launches": a.steps * Rg * (2 if (S > 1 or a.argmax) else 1),
+           "kernel": {1: "direct", 2: "ring", 0: "none"}[lk.lk_gemv_kernel_for(N, K, mode, B, S if S > 1 else 0)]}
     if rank == 0:
         print(json.dumps(out), flush=True)
 

@@ -121,6 +121,38 @@ lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode
                      float* y, uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream);
 
 /*
+ * RMSNorm -> quantize -> GEMV in one launch: every block of the bulk-copy
+ * ring kernel computes the activation in shared memory from the raw rows x
+ * itself (the in-block norm prologue of model-as-a-kernel "megakernel.cu"
+ * ph_gemv, with the arithmetic of lk_rmsnorm_quant / lk_quantize_act), then
+ * runs lk_gemv_q8's GEMV on it.  The results are bit for bit those of
+ * lk_rmsnorm_quant (gain != NULL) or lk_quantize_act (gain == NULL; Dequant
+ * then uses x as is) followed by lk_gemv_q8, without the intermediate
+ * buffers or launches.
+ *   x     f32 [M][K] raw activation rows (4-byte aligned)
+ *   gain  f32 [K] RMSNorm gain, or NULL for the quantizer alone
+ *   y, argmax_parts, n_parts_out   as lk_gemv_q8
+ * Needs the ring kernel: K % 256 == 0 and the activation area fitting in
+ * shared memory (lk_gemv_kernel_for(...) == 2); otherwise LK_ERR_SHAPE.  With
+ * the option "pdl" set, the launch is a programmatic dependent launch: its
+ * weight stream starts while the previous kernel on the stream finishes, and
+ * it reads x only after that kernel has completed.
+ */
+lk_status lk_rmsnorm_quant_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
+                                   const float* x, const float* gain, float eps, int M, float* y,
+                                   uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream);
+
+/*
+ * Which GEMV kernel a call of this shape would launch under the current
+ * options, for 16-byte aligned operands: 1 the direct-load kernel (any
+ * K % 32 == 0), 2 the bulk-copy ring kernel (K % 256 == 0 and the activation
+ * fits in shared memory), 0 none (invalid shape, or the ring kernel forced
+ * by "gemv_path" 2 but not applicable).  S = 0 asks about lk_gemv_q8,
+ * S >= 1 about lk_gemv_q8_splitk.
+ */
+int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S);
+
+/*
  * Bytes of the split-K partial buffer for (mode, S, M, N): S*M*N values,
  * f64 under LK_DEQUANT, f32 otherwise.
  */
@@ -185,8 +217,14 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  * Tuning and test options (process-wide; not thread-safe against concurrent
  * launches).  Names:
  *   "gemv_path"   0 auto, 1 direct-load kernel, 2 bulk-copy ring kernel
- *   "ring_stages" ring depth of the bulk-copy kernel (0 = default)
+ *   "ring_stages" ring depth of the bulk-copy kernel (0 = as deep as shared
+ *                 memory allows, at most 16)
  *   "grid_ctas"   blocks of the ring kernel (0 = one per SM)
+ *   "ring_hint"   1 (default): L2 evict-first hint on the ring's weight
+ *                 copies; 0: no hint
+ *   "ring_warps"  consumer warps of the ring kernel: 0 auto, 4, 6 or 8
+ *   "pdl"         1: lk_rmsnorm_quant_gemv_q8 launches as a programmatic
+ *                 dependent launch (default 0)
  *   "wait_us"     time limit of every device-side wait, microseconds
  *                 (0 = default, 2 s)
  * Unknown names or out-of-range values return LK_ERR_ARG.

@@ -14,6 +14,9 @@ long opt_gemv_path = 0;
 long opt_ring_stages = 0;
 long opt_grid_ctas = 0;
 long opt_wait_us = 0;
+long opt_ring_hint = 1;
+long opt_ring_warps = 0;
+long opt_pdl = 0;
 
 static const int kMaxDevices = 64;
 static DeviceInfo g_info[kMaxDevices];
@@ -45,26 +48,6 @@ using namespace lkh;
 // min(roundup32(K), 1024) ("kernels.rs" norm_threads): that block size fixes
 // the order of the f32 sum of squares.  Q 0 (Dequant) accumulates in f64 and
 // writes only the normed row.
-template <int Q>
-struct acc_of { typedef float t; };
-template <>
-struct acc_of<0> { typedef double t; };
-
-__device__ __forceinline__ float fma_acc(float v, float acc) { return __fmaf_rn(v, v, acc); }
-__device__ __forceinline__ double fma_acc(double v, double acc) { return __fma_rn(v, v, acc); }
-__device__ __forceinline__ float norm_div_add(float sum, int K, float eps) {
-  return __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, (float)K), eps));
-}
-__device__ __forceinline__ double norm_div_add(double sum, int K, float eps) {
-  return __dsqrt_rn(__dadd_rn(__ddiv_rn(sum, (double)K), (double)eps));
-}
-__device__ __forceinline__ float norm_scale(float v, float den, float g) {
-  return __fmul_rn(__fdiv_rn(v, den), g);
-}
-__device__ __forceinline__ float norm_scale(float v, double den, float g) {
-  return __double2float_rn(__dmul_rn(__ddiv_rn((double)v, den), (double)g));
-}
-
 template <int Q>
 __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __restrict__ x,
                                                              const float* __restrict__ g, int K,
@@ -141,11 +124,20 @@ lk_status lk_set_option(const char* name, long value) {
     if (value < 0 || value > 2) return LK_ERR_ARG;
     opt_gemv_path = value;
   } else if (!strcmp(name, "ring_stages")) {
-    if (value < 0 || value > 32) return LK_ERR_ARG;
+    if (value < 0 || value > 16) return LK_ERR_ARG;
     opt_ring_stages = value;
   } else if (!strcmp(name, "grid_ctas")) {
     if (value < 0 || value > (1L << 20)) return LK_ERR_ARG;
     opt_grid_ctas = value;
+  } else if (!strcmp(name, "ring_warps")) {
+    if (value != 0 && value != 4 && value != 6 && value != 8) return LK_ERR_ARG;
+    opt_ring_warps = value;
+  } else if (!strcmp(name, "pdl")) {
+    if (value < 0 || value > 1) return LK_ERR_ARG;
+    opt_pdl = value;
+  } else if (!strcmp(name, "ring_hint")) {
+    if (value < 0 || value > 1) return LK_ERR_ARG;
+    opt_ring_hint = value;
   } else if (!strcmp(name, "wait_us")) {
     if (value < 0 || value > 60000000L) return LK_ERR_ARG;
     opt_wait_us = value;
@@ -161,6 +153,9 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "ring_stages")) return opt_ring_stages;
   if (!strcmp(name, "grid_ctas")) return opt_grid_ctas;
   if (!strcmp(name, "wait_us")) return opt_wait_us;
+  if (!strcmp(name, "ring_hint")) return opt_ring_hint;
+  if (!strcmp(name, "ring_warps")) return opt_ring_warps;
+  if (!strcmp(name, "pdl")) return opt_pdl;
   return -1;
 }
 

@@ -63,6 +63,28 @@ __device__ __forceinline__ void quant_lane(float v, int8_t* __restrict__ hi, int
   }
 }
 
+// ---- RMSNorm arithmetic ("kernels.rs" lk_rmsnorm_row: accumulator f64 under
+// Dequant (Q 0), f32 otherwise; y = v / sqrt(sum/K + eps) * g)
+template <int Q>
+struct acc_of { typedef float t; };
+template <>
+struct acc_of<0> { typedef double t; };
+
+__device__ __forceinline__ float fma_acc(float v, float acc) { return __fmaf_rn(v, v, acc); }
+__device__ __forceinline__ double fma_acc(double v, double acc) { return __fma_rn(v, v, acc); }
+__device__ __forceinline__ float norm_div_add(float sum, int K, float eps) {
+  return __fsqrt_rn(__fadd_rn(__fdiv_rn(sum, (float)K), eps));
+}
+__device__ __forceinline__ double norm_div_add(double sum, int K, float eps) {
+  return __dsqrt_rn(__dadd_rn(__ddiv_rn(sum, (double)K), (double)eps));
+}
+__device__ __forceinline__ float norm_scale(float v, float den, float g) {
+  return __fmul_rn(__fdiv_rn(v, den), g);
+}
+__device__ __forceinline__ float norm_scale(float v, double den, float g) {
+  return __double2float_rn(__dmul_rn(__ddiv_rn((double)v, den), (double)g));
+}
+
 // ---- argmax key ("megakernel.cu" amax_key) --------------------------------------
 // Order-preserving image of the f32 value (after -0 -> +0) in the high word,
 // 0xFFFFFFFF - index in the low word: the largest key is the largest value,

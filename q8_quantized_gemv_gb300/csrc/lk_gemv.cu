@@ -209,6 +209,10 @@ GemvProblem make_problem(const int8_t* wq, const uint16_t* ws, int N, int K, lk_
   p.y = nullptr;
   p.part64 = nullptr;
   p.amax = nullptr;
+  p.fuse = false;
+  p.xraw = nullptr;
+  p.gain = nullptr;
+  p.eps = 0.f;
   return p;
 }
 
@@ -257,6 +261,48 @@ lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode
     if (opt_gemv_path == 2 && !ring_supports(p)) return LK_ERR_SHAPE;
     st = direct_gemv(p, stream, &n_parts);
   }
+  if (n_parts_out) *n_parts_out = n_parts;
+  return st;
+}
+
+int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS || N < 1 || K < 32 || K % 32 || M < 1 || M > LK_MAX_M || S < 0 ||
+      S > LK_MAX_SPLITK)
+    return 0;
+  // 16-byte aligned stand-in pointers: only the shape decides
+  const void* a16 = (const void*)(uintptr_t)256;
+  GemvProblem p = make_problem((const int8_t*)a16, (const uint16_t*)a16, N, K, mode, (const float*)a16,
+                               (const int8_t*)a16, (const int8_t*)a16, (const float*)a16, M);
+  p.split = S > 0;
+  p.S = S > 0 ? S : 1;
+  if (opt_gemv_path == 1) return 1;
+  return ring_supports(p) ? 2 : (opt_gemv_path == 2 ? 0 : 1);
+}
+
+lk_status lk_rmsnorm_quant_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
+                                   const float* x, const float* gain, float eps, int M, float* y,
+                                   uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+  if (N < 0 || K < 0 || K % 32 || M < 0 || M > LK_MAX_M) return LK_ERR_SHAPE;
+  if (argmax_parts && !n_parts_out) return LK_ERR_ARG;
+  if (N == 0 || M == 0) {
+    if (n_parts_out) *n_parts_out = 0;
+    return LK_OK;
+  }
+  if (!wq || !ws || !x || !y) return LK_ERR_ARG;
+  if (!aligned(wq, 16) || !aligned(ws, 2) || !aligned(x, 4) || (gain && !aligned(gain, 4)) || !aligned(y, 4) ||
+      (argmax_parts && !aligned(argmax_parts, 8)))
+    return LK_ERR_ALIGN;
+  GemvProblem p = make_problem(wq, ws, N, K, mode, nullptr, nullptr, nullptr, nullptr, M);
+  p.fuse = true;
+  p.xraw = x;
+  p.gain = gain;
+  p.eps = eps;
+  p.y = y;
+  p.amax = (unsigned long long*)argmax_parts;
+  if (!ring_supports(p)) return LK_ERR_SHAPE;
+  int n_parts = 0;
+  lk_status st = ring_gemv(p, stream, &n_parts);
   if (n_parts_out) *n_parts_out = n_parts;
   return st;
 }

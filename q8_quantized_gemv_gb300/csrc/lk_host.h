@@ -23,6 +23,9 @@ const DeviceInfo* device_info(int* dev_out);
 extern long opt_gemv_path;    // 0 auto, 1 direct, 2 ring
 extern long opt_ring_stages;  // 0 default
 extern long opt_grid_ctas;    // 0 default
+extern long opt_ring_warps;   // 0 auto, else 4, 6 or 8 consumer warps
+extern long opt_pdl;          // 1: fused ring launches are programmatic dependents
+extern long opt_ring_hint;    // 1: L2 evict-first hint on the weight copies (default)
 extern long opt_wait_us;      // bound of every device-side wait, microseconds (0 = 2 s)
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
@@ -49,6 +52,10 @@ struct GemvProblem {
   float* y;                      // plain: y [M][N]; split quantized: part f32 [S][M][N]
   double* part64;                // split Dequant: part f64 [S][M][N]
   unsigned long long* amax;      // plain only: [M][n_parts]
+  bool fuse;                     // activation computed in the kernel from xraw
+  const float* xraw;             // fused: raw f32 rows [M][K]
+  const float* gain;             // fused: RMSNorm gain [K], or NULL for quantize only
+  float eps;
 };
 
 // Bulk-copy ring kernel (lk_ring.cu).  Returns LK_ERR_SHAPE when the problem

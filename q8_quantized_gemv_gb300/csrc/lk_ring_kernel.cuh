@@ -1,0 +1,513 @@
+// Device side of the bulk-copy ring GEMV: layout constants, the launch
+// arguments, PTX wrappers, the fused activation prologue and the kernel
+// template.  Included by the per-mode translation units lk_ring_q*.cu, which
+// instantiate the kernels, and by lk_ring.cu (host side).
+#pragma once
+#include "lk_device.cuh"
+#include "lk_host.h"
+
+namespace lkring {
+
+
+using namespace lk;
+
+constexpr int MAXW = 8;                // consumer warps at most
+constexpr int THREADS_MAX = (MAXW + 1) * 32;
+constexpr int QR = 4;                  // rows per stage (one warp's quad)
+constexpr int TKMAX = 4096;            // bytes of K per stage
+constexpr int MAX_STAGES = 16;
+// barriers (2 per stage + the activation's), abort flag, argmax keys [M][MAXW],
+// norm partial sums [M][32] and norm denominators [M] (8 bytes each)
+constexpr unsigned TAIL =
+    8 * (2 * MAX_STAGES + 1) + 16 + 8 * LK_MAX_M * MAXW + 8 * LK_MAX_M * 32 + 8 * LK_MAX_M;
+
+enum : int { ERR_WAIT_FULL = 1, ERR_WAIT_EMPTY = 2, ERR_DRAIN = 4, ERR_SELFTEST = 8, ERR_WAIT_ACT = 16 };
+
+struct RingArgs {
+  lkh::GemvProblem p;
+  int nwc;                 // consumer warps; the block is (nwc + 1) warps, the last the producer
+  int depth;               // ring stages owned by each consumer warp
+  int gx;                  // blocks along the rows
+  unsigned tk;             // bytes of K per stage (<= TKMAX)
+  unsigned srow;           // bytes per row of a stage's scale area
+  unsigned stage_bytes;
+  unsigned s_off;          // scale area inside a stage
+  unsigned act_len;        // bytes of K in the activation area (the widest chunk)
+  unsigned ring_off;       // ring start (after the activation area)
+  unsigned long long wait_ns;
+  unsigned long long pol_w;  // nonzero: L2 evict-first hint on the weight copies
+  int pdl;                 // launched as a programmatic dependent of the previous kernel
+  int* err;                // the device error word
+};
+
+typedef void (*ring_fn)(const RingArgs);
+template <int Q>
+ring_fn ring_pick(int M, bool split, bool fuse);
+
+// ---- PTX wrappers -------------------------------------------------------------------------
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned bar, unsigned bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(unsigned bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase of parity `parity` to complete.  Returns false if
+// the limit ran out or another thread raised the abort flag.
+__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity, unsigned long long limit_ns,
+                                          volatile int* abort_flag) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = gtimer();
+  for (unsigned n = 1;; ++n) {
+    if (mbar_try(bar, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (gtimer() - t0 > limit_ns) return false;
+    }
+  }
+}
+__device__ __forceinline__ unsigned long long evict_first_policy() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ unsigned long long evict_last_policy() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// 1-D bulk copy global -> this block's shared memory, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned bar,
+                                         unsigned long long policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_nohint(void* dst, const void* src, unsigned bytes, unsigned bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void raise_error(int* err, int code, volatile int* abort_flag) {
+  atomicOr(err, code);
+  *abort_flag = 1;
+}
+
+template <int Q>
+struct part_t { typedef float t; };
+template <>
+struct part_t<0> { typedef double t; };
+
+// Bytes of the activation area for `len` bytes of K (M rows).
+template <int Q, int M>
+__host__ __device__ constexpr unsigned act_area(unsigned len) {
+  return Q == 0 ? M * len * 4u : M * len * (Q == 2 ? 2u : 1u) + M * len / 8u;
+}
+
+__device__ __forceinline__ void bulk(void* dst, const void* src, unsigned bytes, unsigned bar,
+                                     unsigned long long policy) {
+  if (policy) bulk_g2s(dst, src, bytes, bar, policy);
+  else bulk_g2s_nohint(dst, src, bytes, bar);
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+__device__ __forceinline__ void consumers_sync(int nwc) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nwc * 32) : "memory");
+}
+
+// The activation area computed in the block from the raw f32 rows: RMSNorm
+// (when a gain is given) and the quantizer of mode Q, bit for bit what
+// lk_rmsnorm_quant / lk_quantize_act compute.  The norm's sum of squares
+// follows the block of vt = min(K, 1024) threads of "kernels.rs"
+// lk_rmsnorm_row: the nwc consumer warps play its vt/32 warps in turn.
+template <int Q, int M>
+__device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, unsigned L, unsigned char* act,
+                               void* red_raw, void* den_raw) {
+  typedef typename acc_of<Q>::t A;
+  A* red = (A*)red_raw;
+  A* den = (A*)den_raw;
+  const int lane = threadIdx.x & 31, cw = threadIdx.x >> 5;
+  const int K = a.K;
+  const bool norm = a.gain != nullptr;
+  if (norm) {
+    const int vt = K < 1024 ? K : 1024, vw = vt >> 5;
+    for (int t = 0; t < M; ++t) {
+      const float* xr = a.xraw + (long)t * K;
+      for (int w = cw; w < vw; w += nwc) {
+        A acc = 0;
+        for (int i = 32 * w + lane; i < K; i += vt) acc = fma_acc((A)__ldg(xr + i), acc);
+        acc = warp_tree_sum(acc);
+        if (lane == 0) red[t * 32 + w] = acc;
+      }
+    }
+    consumers_sync(nwc);
+    if (cw == 0) {
+      for (int t = 0; t < M; ++t) {
+        A v = lane < vw ? red[t * 32 + lane] : (A)0;
+        v = warp_tree_sum(v);
+        if (lane == 0) den[t] = norm_div_add(v, K, a.eps);
+      }
+    }
+    consumers_sync(nwc);
+  }
+  const int ng = (int)(L >> 5);
+  for (int t = 0; t < M; ++t) {
+    const float* xr = a.xraw + (long)t * K + k_lo;
+    const A dn = norm ? den[t] : (A)1;
+    for (int g = cw; g < ng; g += nwc) {
+      const int i = 32 * g + lane;
+      // past the row's end (a chunk narrower than the area) the area keeps zeros
+      const bool in = k_lo + i < K;
+      float v = in ? __ldg(xr + i) : 0.f;
+      if (norm && in) v = norm_scale(v, dn, __ldg(a.gain + k_lo + i));
+      if constexpr (Q == 0) {
+        ((float*)act)[(size_t)t * L + i] = v;
+      } else {
+        int8_t* XQ = (int8_t*)act + (size_t)t * L;
+        int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
+        float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
+        quant_lane<Q>(v, XQ, XL, XS, i, g, lane);
+      }
+    }
+  }
+  consumers_sync(nwc);
+}
+
+template <int Q, int M, bool SPLIT, bool FUSE>
+__global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArgs ra) {
+  typedef typename part_t<Q>::t P;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const lkh::GemvProblem& a = ra.p;
+  const int nwc = ra.nwc, D = ra.depth, NS = nwc * D;
+  unsigned char* act = smem;
+  unsigned char* ring = smem + ra.ring_off;
+  unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
+  volatile int* abort_flag = (volatile int*)(bars + 2 * MAX_STAGES + 1);
+  unsigned long long* keys = (unsigned long long*)(bars + 2 * MAX_STAGES + 3);  // [M][MAXW]
+  double* nred = (double*)(keys + LK_MAX_M * MAXW);                              // [M][32]
+  double* nden = nred + LK_MAX_M * 32;                                           // [M]
+  const unsigned full0 = smem_u32(bars), empty0 = smem_u32(bars + MAX_STAGES);
+  const unsigned act_bar = smem_u32(bars + 2 * MAX_STAGES);
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int K = a.K, nb = K >> 5;
+  const long N = a.N;
+  const long r0 = (long)blockIdx.x * N / ra.gx, r1 = (long)(blockIdx.x + 1) * N / ra.gx;
+  int b_lo = 0, b_hi = nb;
+  if (SPLIT) {
+    b_lo = splitk_bound(nb, a.S, blockIdx.y);
+    b_hi = splitk_bound(nb, a.S, blockIdx.y + 1);
+  }
+  const int k_lo = 32 * b_lo, k_hi = 32 * b_hi;
+  const unsigned L = ra.act_len;
+  const int tk = (int)ra.tk;
+  const int nsl = (k_hi - k_lo + tk - 1) / tk;  // K slices per quad
+  const bool whole = (k_lo == 0 && k_hi == K && tk >= K);  // a quad's bytes are contiguous
+  const int per_group = QR * nwc;
+  const long ngroups = (r1 - r0 + per_group - 1) / per_group;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(act_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (ra.pdl && threadIdx.x == 0) griddep_launch();
+
+  if (warp == nwc) {
+    // ------------------------------------------------------------------ producer
+    const unsigned long long pol_a = evict_last_policy();
+    const unsigned long long pol_w = ra.pol_w ? evict_first_policy() : 0ull;
+    if (!FUSE && L > 0) {
+      if (ra.pdl) griddep_wait();  // the activation is the previous kernel's output
+      if (lane == 0) mbar_arrive_expect_tx(act_bar, act_area<Q, M>(L));
+      __syncwarp();
+      if (Q == 0) {
+        if (lane < M) bulk(act + (size_t)lane * L * 4, a.x + (long)lane * K + k_lo, L * 4, act_bar, pol_a);
+      } else {
+        if (lane < M) bulk(act + (size_t)lane * L, a.xq + (long)lane * K + k_lo, L, act_bar, pol_a);
+        if (Q == 2 && lane >= 8 && lane < 8 + M)
+          bulk(act + (size_t)M * L + (lane - 8) * L, a.xl + (long)(lane - 8) * K + k_lo, L, act_bar, pol_a);
+        if (lane >= 16 && lane < 16 + M) {
+          const int t = lane - 16;
+          bulk(act + (size_t)M * L * (Q == 2 ? 2 : 1) + t * (L / 8), a.xs + (long)t * nb + b_lo, L / 8, act_bar,
+               pol_a);
+        }
+      }
+    }
+    bool ok = true;
+    for (long gi = 0; ok && gi < ngroups; ++gi) {
+      const long g0 = r0 + gi * per_group;
+      const int rows_g = (int)(r1 - g0 < per_group ? r1 - g0 : per_group);
+      const int nq = (rows_g + QR - 1) / QR;
+      for (int c = 0; ok && c < nsl; ++c) {
+        const int k0 = k_lo + c * tk;
+        const int len = (k_hi - k0 < tk) ? k_hi - k0 : tk;
+        const int b0 = k0 >> 5, b1 = b0 + (len >> 5);
+        const unsigned sh = (unsigned)(b0 & 7) * 2u;               // scales' offset in the first 16 B
+        const unsigned slen = ((b1 - b0) * 2u + sh + 15u) & ~15u;  // 16-byte superset of a row's scales
+        const int n = (int)gi * nsl + c;  // every warp's stage count before this one
+        const unsigned ph = (unsigned)(n / D) & 1u;
+        for (int qd = 0; qd < nq; ++qd) {
+          const int rows = rows_g - QR * qd < QR ? rows_g - QR * qd : QR;
+          const long row0 = g0 + QR * qd;
+          const int slot = qd * D + n % D;  // each warp owns its D slots
+          if (!__all_sync(FULL, mbar_wait(empty0 + 8 * slot, ph ^ 1u, ra.wait_ns, abort_flag))) {
+            if (lane == 0) raise_error(ra.err, ERR_WAIT_EMPTY, abort_flag);
+            ok = false;
+            break;
+          }
+          const unsigned full = full0 + 8 * slot;
+          unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
+          if (whole) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)K * 17u / 16u);
+              bulk(st, a.wq + row0 * K, rows * K, full, pol_w);
+              bulk(st + ra.s_off, (const unsigned char*)a.ws + row0 * nb * 2, rows * nb * 2, full, pol_w);
+            }
+          } else {
+            if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * (len + slen));
+            __syncwarp();
+            if (lane < rows) {
+              const long row = row0 + lane;
+              bulk(st + lane * tk, a.wq + row * K + k0, len, full, pol_w);
+              bulk(st + ra.s_off + lane * ra.srow, (const unsigned char*)a.ws + ((row * nb + b0) * 2 - sh), slen,
+                   full, pol_w);
+            }
+          }
+          __syncwarp();
+        }
+      }
+    }
+    // Drain: every copy issued must have landed before this warp lets the
+    // block end.  Warp w's stages are counted as above; its last D stages are
+    // the latest phases of its D slots.
+    if (lane == 0) {
+      const long rows_last = (r1 - r0) - (ngroups - 1) * per_group;
+      const int nq_last = ngroups > 0 ? (int)((rows_last + QR - 1) / QR) : 0;
+      for (int w = 0; w < nwc; ++w) {
+        const long T = ngroups > 0 ? (ngroups - 1) * nsl + (w < nq_last ? nsl : 0) : 0;
+        for (long n = T - D > 0 ? T - D : 0; n < T; ++n) {
+          const unsigned bar = full0 + 8 * (unsigned)(w * D + n % D);
+          const unsigned long long t0 = gtimer();
+          while (!mbar_try(bar, (unsigned)(n / D) & 1u)) {
+            if (gtimer() - t0 > ra.wait_ns) {
+              atomicOr(ra.err, ERR_DRAIN);
+              break;
+            }
+          }
+        }
+      }
+      if (!FUSE && L > 0) {
+        const unsigned long long t0 = gtimer();
+        while (!mbar_try(act_bar, 0)) {
+          if (gtimer() - t0 > ra.wait_ns) {
+            atomicOr(ra.err, ERR_DRAIN);
+            break;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < nwc) {
+    // ------------------------------------------------------------------ consumers
+    const int rr = lane >> 3, j = lane & 7, q = j >> 1;
+    unsigned long long best[M];
+#pragma unroll
+    for (int t = 0; t < M; ++t) best[t] = 0;
+    bool ok = true;
+    if (FUSE) {
+      if (ra.pdl) griddep_wait();  // the raw activation is the previous kernel's output
+      fused_prologue<Q, M>(a, nwc, k_lo, L, act, nred, nden);
+    } else if (L > 0) {
+      ok = __all_sync(FULL, mbar_wait(act_bar, 0, ra.wait_ns, abort_flag));
+      if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
+    }
+    if (ra.pdl && !FUSE) griddep_wait();  // before the first write of an output
+    const unsigned char* XQ = act;
+    const unsigned char* XL = act + (size_t)M * L;
+    const float* XS = (const float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1));
+    const float* XF = (const float*)act;
+    for (long gi = 0; ok && gi < ngroups; ++gi) {
+      const long g0 = r0 + gi * per_group;
+      const int rows_g = (int)(r1 - g0 < per_group ? r1 - g0 : per_group);
+      const int nq = (rows_g + QR - 1) / QR;
+      if (warp >= nq) continue;
+      const int rows = rows_g - QR * warp < QR ? rows_g - QR * warp : QR;
+      const bool row_ok = rr < rows;
+      P p[M];
+#pragma unroll
+      for (int t = 0; t < M; ++t) p[t] = (P)0;
+      for (int c = 0; c < nsl; ++c) {
+        const int k0 = k_lo + c * tk;
+        const int len = (k_hi - k0 < tk) ? k_hi - k0 : tk;
+        const int n = (int)gi * nsl + c;
+        const int slot = warp * D + n % D;
+        const unsigned ph = (unsigned)(n / D) & 1u;
+        if (!__all_sync(FULL, mbar_wait(full0 + 8 * slot, ph, ra.wait_ns, abort_flag))) {
+          if (lane == 0) raise_error(ra.err, ERR_WAIT_FULL, abort_flag);
+          ok = false;
+          break;
+        }
+        const unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
+        const int b0 = k0 >> 5;
+        const unsigned sh = whole ? 0u : (unsigned)(b0 & 7) * 2u;
+        const unsigned srow = whole ? (unsigned)nb * 2u : ra.srow;
+        const unsigned wrow = whole ? (unsigned)K : (unsigned)tk;
+        const unsigned char* Wr = st + rr * wrow + 16 * j;
+        const unsigned char* Sr = st + ra.s_off + rr * srow + sh + 2 * q;
+        const int ka = k0 - k_lo;  // offset of this slice in the activation area
+        const int nseg = len >> 7;
+#pragma unroll 4
+        for (int seg = 0; seg < nseg; ++seg) {
+          const int4 w = *(const int4*)(Wr + 128 * seg);
+          const float wsc = __half2float(*(const __half*)(Sr + 8 * seg));
+          const int xo = ka + 128 * seg + 16 * j;
+          const int bi = (ka >> 5) + 4 * seg + q;
+#pragma unroll
+          for (int t = 0; t < M; ++t) {
+            if constexpr (Q == 0) {
+              const float4* xv = (const float4*)(XF + (size_t)t * L + xo);
+              const int wi[4] = {w.x, w.y, w.z, w.w};
+              float h = 0.f;
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                const float4 xx = xv[cc];
+                const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) h = __fmaf_rn((float)(int8_t)(wi[cc] >> (8 * k)), xe[k], h);
+              }
+              const float blk = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
+              p[t] = __fma_rn((double)wsc, (double)blk, (double)p[t]);
+            } else {
+              const int4 hv = *(const int4*)(XQ + (size_t)t * L + xo);
+              int d = dot16(w, hv);
+              d += __shfl_xor_sync(FULL, d, 1);
+              int e = 0;
+              if constexpr (Q == 2) {
+                const int4 lv = *(const int4*)(XL + (size_t)t * L + xo);
+                e = dot16(w, lv);
+                e += __shfl_xor_sync(FULL, e, 1);
+              }
+              const float s = XS[(size_t)t * (L / 32) + bi];
+              p[t] = q8_step<Q>((float)p[t], wsc, s, d, e);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+      }
+      if (!ok) break;
+      // quad done: (p0 + p2) + (p1 + p3) within each row's 8 lanes
+#pragma unroll
+      for (int t = 0; t < M; ++t) {
+        P v = p[t];
+        v = v + __shfl_down_sync(FULL, v, 4);
+        v = v + __shfl_down_sync(FULL, v, 2);
+        if (j == 0 && row_ok) {
+          const long o = g0 + QR * warp + rr;
+          if (SPLIT) {
+            const long idx = ((long)blockIdx.y * M + t) * N + o;
+            if constexpr (Q == 0) a.part64[idx] = (double)v;
+            else a.y[idx] = (float)v;
+          } else {
+            const float yv = Q == 0 ? __double2float_rn((double)v) : (float)v;
+            a.y[(long)t * N + o] = yv;
+            const unsigned long long kk = amax_key(yv, (unsigned)o);
+            best[t] = kk > best[t] ? kk : best[t];
+          }
+        }
+      }
+    }
+    if (!SPLIT && a.amax) {
+#pragma unroll
+      for (int t = 0; t < M; ++t) {
+        const unsigned long long wmax = warp_max_u64(best[t]);
+        if (lane == 0) keys[t * MAXW + warp] = wmax;
+      }
+    }
+  }
+  if (!SPLIT && a.amax) {
+    __syncthreads();
+    if (threadIdx.x < M) {
+      unsigned long long m = 0;
+      for (int w = 0; w < nwc; ++w) m = keys[threadIdx.x * MAXW + w] > m ? keys[threadIdx.x * MAXW + w] : m;
+      a.amax[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
+    }
+  }
+}
+
+
+// Explicit instantiation of every (M, SPLIT, FUSE) kernel of mode Q.
+#define LK_RING_PICK(Q)                                                             \
+  template <>                                                                       \
+  ring_fn ring_pick<Q>(int M, bool split, bool fuse) {                              \
+    if (split) {                                                                    \
+      switch (M) {                                                                  \
+        case 1: return gemv_ring_kernel<Q, 1, true, false>;                         \
+        case 2: return gemv_ring_kernel<Q, 2, true, false>;                         \
+        case 3: return gemv_ring_kernel<Q, 3, true, false>;                         \
+        case 4: return gemv_ring_kernel<Q, 4, true, false>;                         \
+        case 5: return gemv_ring_kernel<Q, 5, true, false>;                         \
+        case 6: return gemv_ring_kernel<Q, 6, true, false>;                         \
+        case 7: return gemv_ring_kernel<Q, 7, true, false>;                         \
+        default: return gemv_ring_kernel<Q, 8, true, false>;                        \
+      }                                                                             \
+    }                                                                               \
+    if (fuse) {                                                                     \
+      switch (M) {                                                                  \
+        case 1: return gemv_ring_kernel<Q, 1, false, true>;                         \
+        case 2: return gemv_ring_kernel<Q, 2, false, true>;                         \
+        case 3: return gemv_ring_kernel<Q, 3, false, true>;                         \
+        case 4: return gemv_ring_kernel<Q, 4, false, true>;                         \
+        case 5: return gemv_ring_kernel<Q, 5, false, true>;                         \
+        case 6: return gemv_ring_kernel<Q, 6, false, true>;                         \
+        case 7: return gemv_ring_kernel<Q, 7, false, true>;                         \
+        default: return gemv_ring_kernel<Q, 8, false, true>;                        \
+      }                                                                             \
+    }                                                                               \
+    switch (M) {                                                                    \
+      case 1: return gemv_ring_kernel<Q, 1, false, false>;                          \
+      case 2: return gemv_ring_kernel<Q, 2, false, false>;                          \
+      case 3: return gemv_ring_kernel<Q, 3, false, false>;                          \
+      case 4: return gemv_ring_kernel<Q, 4, false, false>;                          \
+      case 5: return gemv_ring_kernel<Q, 5, false, false>;                          \
+      case 6: return gemv_ring_kernel<Q, 6, false, false>;                          \
+      case 7: return gemv_ring_kernel<Q, 7, false, false>;                          \
+      default: return gemv_ring_kernel<Q, 8, false, false>;                         \
+    }                                                                               \
+  }
+
+}  // namespace lkring

@@ -1,0 +1,7 @@
+// Ring GEMV kernels of numerics mode 0 (Dequant), compiled in a
+// translation unit of their own so the three modes build in parallel.
+#include "lk_ring_kernel.cuh"
+
+namespace lkring {
+LK_RING_PICK(0)
+}  // namespace lkring

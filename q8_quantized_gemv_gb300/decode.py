@@ -23,7 +23,8 @@ from . import lk, synth
 
 class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
-                 batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6):
+                 batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
+                 fused=True):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
         dev = self.dev
@@ -54,6 +55,12 @@ class DecodeStack:
         self.parts = torch.zeros((B * lk.lk_argmax_parts_max(vocab),), dtype=torch.int64, device=dev)
         self.idx = torch.empty((B,), dtype=torch.int32, device=dev)
         self.n_parts = 0
+        # one launch per projection (norm/quantize prologue inside the GEMV)
+        # wherever the ring kernel takes the shape; else norm/quantize kernels
+        # followed by lk_gemv_q8
+        shapes = dict(self.shapes, lm=(vocab, hidden))
+        self.fused = {n: bool(fused) and lk.lk_gemv_kernel_for(N, K, self.mode, B, 0) == 2
+                      for n, (N, K) in shapes.items()}
 
     def _act_bufs(self, K):
         B = self.B
@@ -87,26 +94,28 @@ class DecodeStack:
         """Launch one token's sequence on the current stream and return the
         device int32 [B] argmax.  ``hook``, if given, is called as
         hook(name, launch) around each GEMV launch (for per-kernel timing)."""
-        def g(name, w, y, a, parts=None):
-            if hook is None:
-                return self._gemv(w, y, a, parts)
-            return hook(name, lambda: self._gemv(w, y, a, parts))
+        def g(name, w, y, x, gain, parts=None):
+            if self.fused[name]:
+                def launch():
+                    return lk.lk_rmsnorm_quant_gemv_q8(w[0], w[1], self.mode, x, y, gain=gain, eps=self.eps,
+                                                       argmax_parts=parts)
+            else:
+                a = self._norm(x, gain) if gain is not None else self._quant(x)
+
+                def launch():
+                    return self._gemv(w, y, a, parts)
+            return launch() if hook is None else hook(name, launch)
 
         x = self.x0 if x_in is None else x_in
         for w in self.layers:
-            a = self._norm(x, w["g_attn"])
-            g("q", w["q"], self.out["q"], a)
-            g("k", w["k"], self.out["k"], a)
-            g("v", w["v"], self.out["v"], a)
-            a = self._quant(w["o_in"])
-            g("o", w["o"], self.out["o"], a)
-            a = self._norm(self.out["o"], w["g_mlp"])
-            g("gu", w["gu"], self.out["gu"], a)
-            a = self._quant(w["d_in"])
-            g("down", w["down"], self.h, a)
+            g("q", w["q"], self.out["q"], x, w["g_attn"])
+            g("k", w["k"], self.out["k"], x, w["g_attn"])
+            g("v", w["v"], self.out["v"], x, w["g_attn"])
+            g("o", w["o"], self.out["o"], w["o_in"], None)
+            g("gu", w["gu"], self.out["gu"], self.out["o"], w["g_mlp"])
+            g("down", w["down"], self.h, w["d_in"], None)
             x = self.h
-        a = self._norm(x, self.g_final)
-        self.n_parts = g("lm", self.lm, self.logits, a, self.parts)
+        self.n_parts = g("lm", self.lm, self.logits, x, self.g_final, self.parts)
         lk.lk_argmax(self.idx, self.B, self.V, parts=self.parts, n_parts=self.n_parts)
         return self.idx
 
@@ -122,7 +131,9 @@ class DecodeStack:
         return self.L * sum(mb(N, K) for N, K in self.shapes.values()) + mb(self.V, self.H)
 
     def launches_per_token(self):
-        norm_quant = 2 * self.L + 1
-        quant = 0 if self.mode == lk.LK_DEQUANT else 2 * self.L
-        gemv = 6 * self.L + 1
-        return norm_quant + quant + gemv + 1  # + argmax reduce
+        n = 1  # argmax reduce
+        f = self.fused
+        per_layer = 6 + (0 if f["q"] else 1) + (0 if f["k"] else 1) + (0 if f["v"] else 1) \
+            + (0 if (f["o"] or self.mode == lk.LK_DEQUANT) else 1) + (0 if f["gu"] else 1) \
+            + (0 if (f["down"] or self.mode == lk.LK_DEQUANT) else 1)
+        return n + self.L * per_layer + 1 + (0 if f["lm"] else 1)

@@ -60,6 +60,8 @@ def _load():
         "lk_get_option": ([ctypes.c_char_p], L),
         "lk_device_error": ([I, ctypes.POINTER(I)], I),
         "lk_selftest_wait_timeout": ([ctypes.c_uint, P], I),
+        "lk_gemv_kernel_for": ([I, I, I, I, I], I),
+        "lk_rmsnorm_quant_gemv_q8": ([P, P, I, I, I, P, P, F, I, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -73,7 +75,8 @@ def exported_symbols():
     return ["lk_status_string", "lk_version", "lk_rmsnorm_quant", "lk_quantize_act", "lk_gemv_q8",
             "lk_splitk_workspace_bytes", "lk_gemv_q8_splitk", "lk_splitk_combine",
             "lk_argmax_parts_max", "lk_argmax_scratch_entries", "lk_argmax", "lk_q8_block_dots",
-            "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout"]
+            "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout", "lk_gemv_kernel_for",
+            "lk_rmsnorm_quant_gemv_q8"]
 
 
 def _ok(st, where):
@@ -148,6 +151,27 @@ def lk_gemv_q8(wq, ws, mode, y, x=None, xq=None, xl=None, xs=None, argmax_parts=
                            _ptr(argmax_parts, torch.int64, "argmax_parts"),
                            ctypes.byref(n) if argmax_parts is not None else None, _stream(stream)),
         "lk_gemv_q8")
+    return n.value
+
+
+def lk_gemv_kernel_for(N, K, mode, M, S=0) -> int:
+    """1 direct kernel, 2 bulk-copy ring kernel, 0 none (see include/lk.h)."""
+    return _load().lk_gemv_kernel_for(N, K, _mode(mode), M, S)
+
+
+def lk_rmsnorm_quant_gemv_q8(wq, ws, mode, x, y, gain=None, eps=1e-6, argmax_parts=None,
+                             stream=None) -> int:
+    """RMSNorm (gain given) or quantize only (gain None) -> GEMV in one launch.
+    Returns the number of argmax partial keys per activation row."""
+    N, K = wq.shape
+    M = x.shape[0]
+    n = ctypes.c_int(0)
+    _ok(_load().lk_rmsnorm_quant_gemv_q8(_ptr(wq, _I8, "wq"), _ptr(ws, _WS, "ws"), N, K, _mode(mode),
+                                         _ptr(x, _F32, "x"), _ptr(gain, _F32, "gain"), eps, M,
+                                         _ptr(y, _F32, "y"),
+                                         _ptr(argmax_parts, torch.int64, "argmax_parts"),
+                                         ctypes.byref(n) if argmax_parts is not None else None,
+                                         _stream(stream)), "lk_rmsnorm_quant_gemv_q8")
     return n.value
 
 

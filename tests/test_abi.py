@@ -107,6 +107,15 @@ def test_norm_quant_argmax_checks(lib):
     assert lk.lk_argmax_parts_max(151936) >= (151936 + 31) // 32
 
 
+def test_kernel_choice_without_gpu(lib):
+    # invalid shapes answer 0 before any device query
+    assert lk.lk_gemv_kernel_for(64, 48, 1, 1, 0) == 0
+    assert lk.lk_gemv_kernel_for(64, 64, 1, 9, 0) == 0
+    lk.lk_set_option("gemv_path", 1)
+    assert lk.lk_gemv_kernel_for(64, 4096, 1, 1, 0) == 1
+    lk.lk_set_option("gemv_path", 0)
+
+
 def test_options(lib):
     assert lk.lk_get_option("gemv_path") == 0
     lk.lk_set_option("gemv_path", 1)

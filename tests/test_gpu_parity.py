@@ -38,10 +38,11 @@ def path(request):
     lk.lk_set_option("gemv_path", 0)
 
 
-def need(path, K):
-    """The bulk-copy ring kernel takes K % 256 == 0 (16-byte aligned scale rows)."""
-    if path == "ring" and (K < 256 or K % 256):
-        pytest.skip("ring kernel needs K % 256 == 0")
+def need(path, K, N=64, mode=1, M=1, S=0):
+    """Skip the ring-path case when the ring kernel does not take the shape
+    (K % 256 != 0, or the activation does not fit in shared memory)."""
+    if path == "ring" and lk.lk_gemv_kernel_for(N, K, mode, M, S) != 2:
+        pytest.skip("shape not taken by the ring kernel")
 
 
 def sync_check():
@@ -143,7 +144,7 @@ SHAPES = [(33, 32), (37, 544), (100, 4096), (1024, 1024), (257, 1056), (33, 256)
 @pytest.mark.parametrize("M", [1, 2, 5, 8])
 @pytest.mark.parametrize("N,K", SHAPES)
 def test_gemv_parity(path, mode, M, N, K):
-    need(path, K)
+    need(path, K, N, mode, M)
     wq, ws = synth.q8_matrix(N, K, 4000 + N + K)
     x = synth.activation(M, K, 4001 + M, outliers=True)
     y_or = oracle.gemv(wq, ws, mode, **oracle_acts(x, mode))
@@ -210,7 +211,7 @@ def test_gemv_k_zero_and_empty():
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("N,K,M", [(37, 544, 1), (64, 5120, 2), (40, 1024, 8), (300, 2304, 3)])
 def test_splitk_parity(path, mode, S, N, K, M):
-    need(path, K)
+    need(path, K, N, mode, M, S)
     wq, ws = synth.q8_matrix(N, K, 5000 + K)
     x = synth.activation(M, K, 5001, outliers=True)
     y_or, ch_or = oracle.gemv_splitk(wq, ws, mode, S, **oracle_acts(x, mode))
@@ -246,7 +247,7 @@ def test_splitk_parity(path, mode, S, N, K, M):
 def test_splitk_combine_fixture_on_gpu(path, mode):
     rec = order_records()["splitk_combine"]
     K, S = int(rec["K"]), int(rec["S"])
-    need(path, K)
+    need(path, K, 1, MODES[mode], 1, S)
     wq, ws, x = block_case(K, rec["blocks"])
     m = MODES[mode]
     part = torch.zeros((S, 1, 1), dtype=torch.float64 if m == DQ else torch.float32, device=DEV)
@@ -321,3 +322,89 @@ def test_bounded_wait_reports_timeout_and_context_survives():
         sync_check()
         assert np.array_equal(bits(host(y)), bits(y_or))
     lk.lk_set_option("gemv_path", 0)
+
+
+# ---- fused RMSNorm -> quantize -> GEMV (one launch) -----------------------------------
+
+@pytest.mark.parametrize("pdl", [0, 1])
+@pytest.mark.parametrize("mode", [DQ, I8, TP])
+@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("N,K,norm", [(300, 1280, True), (1000, 4096, True), (77, 256, False),
+                                      (64, 12288, False), (5, 2048, True)])
+def test_fused_norm_quant_gemv(pdl, mode, M, N, K, norm):
+    if lk.lk_gemv_kernel_for(N, K, mode, M, 0) != 2:
+        pytest.skip("activation area does not fit the ring kernel")
+    lk.lk_set_option("pdl", pdl)
+    try:
+        wq, ws = synth.q8_matrix(N, K, 8000 + N + K)
+        x = synth.activation(M, K, 8001 + M, outliers=True)
+        g = synth.norm_gain(K, 8002) if norm else None
+        xa = oracle.rmsnorm(x, g, mode) if norm else x
+        y_or = oracle.gemv(wq, ws, mode, **oracle_acts(xa, mode))
+        wq_d, ws_d = to_dev(wq), to_dev(ws)
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+        parts = torch.zeros((M * lk.lk_argmax_parts_max(N),), dtype=torch.int64, device=DEV)
+        n = lk.lk_rmsnorm_quant_gemv_q8(wq_d, ws_d, mode, to_dev(x), y, gain=to_dev(g) if norm else None,
+                                        argmax_parts=parts)
+        idx = torch.full((M,), -1, dtype=torch.int32, device=DEV)
+        lk.lk_argmax(idx, M, N, parts=parts, n_parts=n)
+        sync_check()
+        assert_gemv_close(host(y), y_or, wq, ws, xa, mode)
+        assert host(idx).tolist() == [oracle.argmax(y_or[t]) for t in range(M)]
+        # the same bits as the unfused launches
+        if mode != DQ:
+            y2 = torch.zeros_like(y)
+            xq, xl, xs = act_buffers(M, K, mode)
+            if norm:
+                lk.lk_rmsnorm_quant(to_dev(x), to_dev(g), mode, 1e-6, None, xq, xl, xs)
+            else:
+                lk.lk_quantize_act(to_dev(x), mode, xq, xl, xs)
+            lk.lk_gemv_q8(wq_d, ws_d, mode, y2, xq=xq, xl=xl, xs=xs, M=M)
+            sync_check()
+            assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
+    finally:
+        lk.lk_set_option("pdl", 0)
+
+
+def test_fused_pdl_chain_in_a_graph():
+    """A chain of fused launches where each reads the previous one's output,
+    captured in one CUDA graph with programmatic dependent launches, gives the
+    same bits as the same chain launched plainly."""
+    K = N = 1024
+    L = 6
+    mats = [synth.q8_matrix(N, K, 8100 + l) for l in range(L)]
+    gains = [synth.norm_gain(K, 8200 + l) for l in range(L)]
+    x0 = synth.activation(1, K, 8300)
+    dm = [(to_dev(w), to_dev(s)) for w, s in mats]
+    dg = [to_dev(g) for g in gains]
+    bufs = [torch.zeros((1, N), dtype=torch.float32, device=DEV) for _ in range(L + 1)]
+    bufs[0].copy_(to_dev(x0))
+
+    def chain():
+        for l in range(L):
+            lk.lk_rmsnorm_quant_gemv_q8(dm[l][0], dm[l][1], I8, bufs[l], bufs[l + 1], gain=dg[l])
+
+    chain()
+    torch.cuda.synchronize()
+    ref = host(bufs[L]).copy()
+    # oracle of the whole chain
+    v = x0
+    for l in range(L):
+        a = oracle.rmsnorm(v, gains[l], I8)
+        v = oracle.gemv(mats[l][0], mats[l][1], I8, **oracle_acts(a, I8))
+    assert np.array_equal(bits(ref), bits(v))
+    lk.lk_set_option("pdl", 1)
+    try:
+        s = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            chain()
+        for _ in range(3):
+            for b in bufs[1:]:
+                b.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(bits(host(bufs[L])), bits(ref))
+    finally:
+        lk.lk_set_option("pdl", 0)
+    sync_check()
