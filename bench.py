@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--no-pdl", action="store_true",
                     help="no programmatic dependent launches between the fused GEMVs")
     ap.add_argument("--fused", action="store_true", help="gemv workload: RMSNorm->quantize->GEMV in one launch")
+    ap.add_argument("--opt", action="append", default=[],
+                    help="library option name=value (lk_set_option), e.g. ring_kb=110; repeatable")
     return ap.parse_args()
 
 
@@ -269,6 +271,7 @@ def run_ours(a, rank, world):
         dist.init_process_group("nccl", device_id=dev)
 
     lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
+    _apply_opts(lk, a)
     stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=not a.unfused)
     tok_bytes = stack.weight_bytes()
     stream = torch.cuda.Stream(device=dev)
@@ -358,7 +361,7 @@ def run_ours(a, rank, world):
                    "l2": "inputs larger than L2 (8.04 GB of weights per step)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "gemv_path": "auto", "fused_prologue": {k: v for k, v in stack.fused.items()},
-                   "pdl": not a.no_pdl},
+                   "pdl": not a.no_pdl, "options": a.opt},
         "us_per_token": ms_max * 1e3,
         "pct_of_nominal_8TBs": value / world / NOMINAL_HBM_GBS,
         "roofline": roof,
@@ -373,6 +376,12 @@ def run_ours(a, rank, world):
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def _apply_opts(lk, a):
+    for kv in a.opt:
+        k, v = kv.split("=")
+        lk.lk_set_option(k, int(v))
 
 
 def _timing_event(torch, external):
@@ -397,6 +406,7 @@ def run_gemv(a, rank, world):
     build.build()
     lk.lk_set_option("gemv_path", {"auto": 0, "direct": 1, "ring": 2}[a.path])
     lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
+    _apply_opts(lk, a)
     mode = lk.MODES[a.mode]
     N, K, B, S = a.N, a.K, a.batch, a.S
     wbytes = N * K + N * K // 16

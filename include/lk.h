@@ -218,11 +218,13 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  * launches).  Names:
  *   "gemv_path"   0 auto, 1 direct-load kernel, 2 bulk-copy ring kernel
  *   "ring_stages" ring depth of the bulk-copy kernel (0 = as deep as shared
- *                 memory allows, at most 16)
+ *                 memory allows, at most 32)
  *   "grid_ctas"   blocks of the ring kernel (0 = one per SM)
  *   "ring_hint"   1 (default): L2 evict-first hint on the ring's weight
  *                 copies; 0: no hint
- *   "ring_warps"  consumer warps of the ring kernel: 0 auto, 4, 6 or 8
+ *   "ring_warps"  warps per block of the ring kernel: 0 auto, else 1..16
+ *   "ring_kb"     cap on the ring kernel's shared memory per block, KB (0 none)
+ *   "ring_cps"    ring blocks per SM in the grid, 1..4 (default 1)
  *   "pdl"         1: lk_rmsnorm_quant_gemv_q8 launches as a programmatic
  *                 dependent launch (default 0)
  *   "wait_us"     time limit of every device-side wait, microseconds

@@ -16,6 +16,8 @@ long opt_grid_ctas = 0;
 long opt_wait_us = 0;
 long opt_ring_hint = 1;
 long opt_ring_warps = 0;
+long opt_ring_kb = 0;
+long opt_ring_cps = 1;
 long opt_pdl = 0;
 
 static const int kMaxDevices = 64;
@@ -124,14 +126,20 @@ lk_status lk_set_option(const char* name, long value) {
     if (value < 0 || value > 2) return LK_ERR_ARG;
     opt_gemv_path = value;
   } else if (!strcmp(name, "ring_stages")) {
-    if (value < 0 || value > 16) return LK_ERR_ARG;
+    if (value < 0 || value > 32) return LK_ERR_ARG;
     opt_ring_stages = value;
   } else if (!strcmp(name, "grid_ctas")) {
     if (value < 0 || value > (1L << 20)) return LK_ERR_ARG;
     opt_grid_ctas = value;
   } else if (!strcmp(name, "ring_warps")) {
-    if (value != 0 && value != 4 && value != 6 && value != 8) return LK_ERR_ARG;
+    if (value < 0 || value > 16) return LK_ERR_ARG;
     opt_ring_warps = value;
+  } else if (!strcmp(name, "ring_kb")) {
+    if (value < 0 || value > 1024) return LK_ERR_ARG;
+    opt_ring_kb = value;
+  } else if (!strcmp(name, "ring_cps")) {
+    if (value < 1 || value > 4) return LK_ERR_ARG;
+    opt_ring_cps = value;
   } else if (!strcmp(name, "pdl")) {
     if (value < 0 || value > 1) return LK_ERR_ARG;
     opt_pdl = value;
@@ -155,6 +163,8 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "wait_us")) return opt_wait_us;
   if (!strcmp(name, "ring_hint")) return opt_ring_hint;
   if (!strcmp(name, "ring_warps")) return opt_ring_warps;
+  if (!strcmp(name, "ring_kb")) return opt_ring_kb;
+  if (!strcmp(name, "ring_cps")) return opt_ring_cps;
   if (!strcmp(name, "pdl")) return opt_pdl;
   return -1;
 }

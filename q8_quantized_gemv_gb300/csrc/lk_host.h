@@ -23,7 +23,9 @@ const DeviceInfo* device_info(int* dev_out);
 extern long opt_gemv_path;    // 0 auto, 1 direct, 2 ring
 extern long opt_ring_stages;  // 0 default
 extern long opt_grid_ctas;    // 0 default
-extern long opt_ring_warps;   // 0 auto, else 4, 6 or 8 consumer warps
+extern long opt_ring_warps;   // 0 auto, else warps per block of the ring kernel (1..16)
+extern long opt_ring_kb;      // 0: no cap, else shared memory per ring block in KB
+extern long opt_ring_cps;     // ring blocks per SM in the grid (default 1)
 extern long opt_pdl;          // 1: fused ring launches are programmatic dependents
 extern long opt_ring_hint;    // 1: L2 evict-first hint on the weight copies (default)
 extern long opt_wait_us;      // bound of every device-side wait, microseconds (0 = 2 s)

@@ -96,29 +96,25 @@ Layout layout(const lkh::GemvProblem& p, int smem_optin) {
   const int nb = p.K / 32;
   const int S = p.split ? (p.S > 1 ? p.S : 1) : 1;
   L.act_len = 32u * (unsigned)max_chunk_blocks(nb, S);
-  L.tk = p.K <= TKMAX ? (unsigned)p.K : (unsigned)TKMAX;
+  // whole quads (two copies per stage) up to TKMAX; longer rows in 4 KB slices
+  L.tk = p.K <= TKMAX ? (unsigned)p.K : 4096u;
   const bool whole = S == 1 && L.tk >= (unsigned)p.K;
   L.srow = whole ? L.tk / 16u : L.tk / 16u + 16u;
   L.s_off = QR * L.tk;
   L.stage_bytes = (L.s_off + QR * L.srow + 127u) & ~127u;
   L.ring_off = (act_area_rt(p.mode, p.M, L.act_len) + 127u) & ~127u;
-  const long room = (long)smem_optin - (long)L.ring_off - (long)TAIL;
+  long cap = smem_optin;
+  if (lkh::opt_ring_kb > 0 && lkh::opt_ring_kb * 1024 < cap) cap = lkh::opt_ring_kb * 1024;
+  const long room = cap - (long)L.ring_off - (long)TAIL;
   int fit = room > 0 ? (int)(room / L.stage_bytes) : 0;
   if (fit > MAX_STAGES) fit = MAX_STAGES;
   if (lkh::opt_ring_stages > 0 && lkh::opt_ring_stages < fit) fit = (int)lkh::opt_ring_stages;
-  // consumer warps x stages per warp: the most stages in flight, then the most warps
-  L.nwc = 0;
-  L.depth = 0;
-  const int cand[3] = {8, 6, 4};
-  for (int i = 0; i < 3; ++i) {
-    const int w = cand[i];
-    if (lkh::opt_ring_warps > 0 && w != lkh::opt_ring_warps) continue;
-    const int d = fit / w;
-    if (d >= 1 && w * d > L.nwc * L.depth) {
-      L.nwc = w;
-      L.depth = d;
-    }
-  }
+  // warps x stages per warp: as many stages in flight as fit, one warp per
+  // stage up to MAXW warps (each warp streams its own quads)
+  int w = lkh::opt_ring_warps > 0 ? (int)lkh::opt_ring_warps : (fit < MAXW ? fit : MAXW);
+  if (w > fit) w = fit;
+  L.nwc = w;
+  L.depth = w > 0 ? fit / w : 0;
   L.total = L.ring_off + L.nwc * L.depth * L.stage_bytes + TAIL;
   return L;
 }
@@ -145,7 +141,7 @@ bool ring_supports(const GemvProblem& p) {
 
 int ring_max_ctas(long) {
   const DeviceInfo* d = device_info(nullptr);
-  long g = d ? d->sm_count : 1024;
+  long g = d ? 4L * d->sm_count : 4096;  // up to 4 ring blocks per SM ("ring_cps")
   if (opt_grid_ctas > g) g = opt_grid_ctas;
   return (int)g;
 }
@@ -175,13 +171,13 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   ra.err = error_word_ptr();
   if (!ra.err) return LK_ERR_CUDA;
   const int S = p.split && p.S > 1 ? p.S : 1;
-  const int g = opt_grid_ctas > 0 ? (int)opt_grid_ctas : d->sm_count;
+  const int g = opt_grid_ctas > 0 ? (int)opt_grid_ctas : d->sm_count * (opt_ring_cps > 1 ? (int)opt_ring_cps : 1);
   int gx = (g + S - 1) / S;
   if (gx < 1) gx = 1;
   ra.gx = gx;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(gx, S);
-  cfg.blockDim = dim3((L.nwc + 1) * 32);
+  cfg.blockDim = dim3(L.nwc * 32);
   cfg.dynamicSmemBytes = L.total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -11,22 +11,22 @@ namespace lkring {
 
 using namespace lk;
 
-constexpr int MAXW = 8;                // consumer warps at most
-constexpr int THREADS_MAX = (MAXW + 1) * 32;
+constexpr int MAXW = 16;               // warps per block at most
+constexpr int THREADS_MAX = MAXW * 32;
 constexpr int QR = 4;                  // rows per stage (one warp's quad)
-constexpr int TKMAX = 4096;            // bytes of K per stage
-constexpr int MAX_STAGES = 16;
-// barriers (2 per stage + the activation's), abort flag, argmax keys [M][MAXW],
-// norm partial sums [M][32] and norm denominators [M] (8 bytes each)
+constexpr int TKMAX = 8192;            // bytes of K per stage
+constexpr int MAX_STAGES = 32;
+// barriers (one per stage + the activation's), abort flag, argmax keys
+// [M][MAXW], norm partial sums [M][32] and norm denominators [M] (8 B each)
 constexpr unsigned TAIL =
-    8 * (2 * MAX_STAGES + 1) + 16 + 8 * LK_MAX_M * MAXW + 8 * LK_MAX_M * 32 + 8 * LK_MAX_M;
+    8 * (MAX_STAGES + 1) + 16 + 8 * LK_MAX_M * MAXW + 8 * LK_MAX_M * 32 + 8 * LK_MAX_M;
 
 enum : int { ERR_WAIT_FULL = 1, ERR_WAIT_EMPTY = 2, ERR_DRAIN = 4, ERR_SELFTEST = 8, ERR_WAIT_ACT = 16 };
 
 struct RingArgs {
   lkh::GemvProblem p;
-  int nwc;                 // consumer warps; the block is (nwc + 1) warps, the last the producer
-  int depth;               // ring stages owned by each consumer warp
+  int nwc;                 // warps of the block; each streams and computes its own quads
+  int depth;               // ring stages owned by each warp
   int gx;                  // blocks along the rows
   unsigned tk;             // bytes of K per stage (<= TKMAX)
   unsigned srow;           // bytes per row of a stage's scale area
@@ -139,9 +139,7 @@ __device__ __forceinline__ void bulk(void* dst, const void* src, unsigned bytes,
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
-__device__ __forceinline__ void consumers_sync(int nwc) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nwc * 32) : "memory");
-}
+__device__ __forceinline__ void consumers_sync(int) { __syncthreads(); }
 
 // The activation area computed in the block from the raw f32 rows: RMSNorm
 // (when a gain is given) and the quantizer of mode Q, bit for bit what
@@ -210,12 +208,12 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   unsigned char* act = smem;
   unsigned char* ring = smem + ra.ring_off;
   unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
-  volatile int* abort_flag = (volatile int*)(bars + 2 * MAX_STAGES + 1);
-  unsigned long long* keys = (unsigned long long*)(bars + 2 * MAX_STAGES + 3);  // [M][MAXW]
-  double* nred = (double*)(keys + LK_MAX_M * MAXW);                              // [M][32]
-  double* nden = nred + LK_MAX_M * 32;                                           // [M]
-  const unsigned full0 = smem_u32(bars), empty0 = smem_u32(bars + MAX_STAGES);
-  const unsigned act_bar = smem_u32(bars + 2 * MAX_STAGES);
+  volatile int* abort_flag = (volatile int*)(bars + MAX_STAGES + 1);
+  unsigned long long* keys = (unsigned long long*)(bars + MAX_STAGES + 3);  // [M][MAXW]
+  double* nred = (double*)(keys + LK_MAX_M * MAXW);                        // [M][32]
+  double* nden = nred + LK_MAX_M * 32;                                     // [M]
+  const unsigned full0 = smem_u32(bars);
+  const unsigned act_bar = smem_u32(bars + MAX_STAGES);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, nb = K >> 5;
@@ -229,16 +227,16 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   const int k_lo = 32 * b_lo, k_hi = 32 * b_hi;
   const unsigned L = ra.act_len;
   const int tk = (int)ra.tk;
-  const int nsl = (k_hi - k_lo + tk - 1) / tk;  // K slices per quad
+  const int nsl = (k_hi - k_lo + tk - 1) / tk;             // K slices per quad
   const bool whole = (k_lo == 0 && k_hi == K && tk >= K);  // a quad's bytes are contiguous
-  const int per_group = QR * nwc;
-  const long ngroups = (r1 - r0 + per_group - 1) / per_group;
+  const long nquads = (r1 - r0 + QR - 1) / QR;
+  // this warp's quads are warp, warp + nwc, ...; its stages n = (m-th quad, slice c) = m * nsl + c
+  const long myq = warp < nquads ? (nquads - 1 - warp) / nwc + 1 : 0;
+  const long T = myq * nsl;
+  const unsigned long long pol_w = ra.pol_w ? evict_first_policy() : 0ull;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
-    }
+    for (int s = 0; s < NS; ++s) mbar_init(full0 + 8 * s, 1);
     mbar_init(act_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -246,12 +244,50 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   __syncthreads();
   if (ra.pdl && threadIdx.x == 0) griddep_launch();
 
-  if (warp == nwc) {
-    // ------------------------------------------------------------------ producer
-    const unsigned long long pol_a = evict_last_policy();
-    const unsigned long long pol_w = ra.pol_w ? evict_first_policy() : 0ull;
-    if (!FUSE && L > 0) {
-      if (ra.pdl) griddep_wait();  // the activation is the previous kernel's output
+  // Issue stage n of this warp into its slot n % D (all lanes call it).
+  auto issue = [&](long n) {
+    const long qi = warp + (long)nwc * (n / nsl);
+    const int c = (int)(n % nsl);
+    const long row0 = r0 + QR * qi;
+    const int rows = r1 - row0 < QR ? (int)(r1 - row0) : QR;
+    const int k0 = k_lo + c * tk;
+    const int len = (k_hi - k0 < tk) ? k_hi - k0 : tk;
+    const int slot = warp * D + (int)(n % D);
+    const unsigned full = full0 + 8 * slot;
+    unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
+    if (whole) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)K * 17u / 16u);
+        bulk(st, a.wq + row0 * K, rows * K, full, pol_w);
+        bulk(st + ra.s_off, (const unsigned char*)a.ws + row0 * nb * 2, rows * nb * 2, full, pol_w);
+      }
+    } else {
+      const int b0 = k0 >> 5, b1 = b0 + (len >> 5);
+      const unsigned sh = (unsigned)(b0 & 7) * 2u;               // scales' offset in the first 16 B
+      const unsigned slen = ((b1 - b0) * 2u + sh + 15u) & ~15u;  // 16-byte superset of a row's scales
+      if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * (len + slen));
+      __syncwarp();
+      if (lane < rows) {
+        const long row = row0 + lane;
+        bulk(st + lane * tk, a.wq + row * K + k0, len, full, pol_w);
+        bulk(st + ra.s_off + lane * ra.srow, (const unsigned char*)a.ws + ((row * nb + b0) * 2 - sh), slen, full,
+             pol_w);
+      }
+    }
+    __syncwarp();
+  };
+
+  // Weights do not depend on the previous kernel: start streaming at once.
+  long issued = 0;
+  for (; issued < T && issued < D; ++issued) issue(issued);
+
+  if (ra.pdl) griddep_wait();  // from here on: reads of activations, writes of outputs
+  bool ok = true;
+  if (FUSE) {
+    fused_prologue<Q, M>(a, nwc, k_lo, L, act, nred, nden);
+  } else if (L > 0) {
+    if (warp == 0) {
+      const unsigned long long pol_a = evict_last_policy();
       if (lane == 0) mbar_arrive_expect_tx(act_bar, act_area<Q, M>(L));
       __syncwarp();
       if (Q == 0) {
@@ -266,178 +302,102 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
                pol_a);
         }
       }
+      __syncwarp();
     }
-    bool ok = true;
-    for (long gi = 0; ok && gi < ngroups; ++gi) {
-      const long g0 = r0 + gi * per_group;
-      const int rows_g = (int)(r1 - g0 < per_group ? r1 - g0 : per_group);
-      const int nq = (rows_g + QR - 1) / QR;
-      for (int c = 0; ok && c < nsl; ++c) {
-        const int k0 = k_lo + c * tk;
-        const int len = (k_hi - k0 < tk) ? k_hi - k0 : tk;
-        const int b0 = k0 >> 5, b1 = b0 + (len >> 5);
-        const unsigned sh = (unsigned)(b0 & 7) * 2u;               // scales' offset in the first 16 B
-        const unsigned slen = ((b1 - b0) * 2u + sh + 15u) & ~15u;  // 16-byte superset of a row's scales
-        const int n = (int)gi * nsl + c;  // every warp's stage count before this one
-        const unsigned ph = (unsigned)(n / D) & 1u;
-        for (int qd = 0; qd < nq; ++qd) {
-          const int rows = rows_g - QR * qd < QR ? rows_g - QR * qd : QR;
-          const long row0 = g0 + QR * qd;
-          const int slot = qd * D + n % D;  // each warp owns its D slots
-          if (!__all_sync(FULL, mbar_wait(empty0 + 8 * slot, ph ^ 1u, ra.wait_ns, abort_flag))) {
-            if (lane == 0) raise_error(ra.err, ERR_WAIT_EMPTY, abort_flag);
-            ok = false;
-            break;
-          }
-          const unsigned full = full0 + 8 * slot;
-          unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
-          if (whole) {
-            if (lane == 0) {
-              mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)K * 17u / 16u);
-              bulk(st, a.wq + row0 * K, rows * K, full, pol_w);
-              bulk(st + ra.s_off, (const unsigned char*)a.ws + row0 * nb * 2, rows * nb * 2, full, pol_w);
-            }
-          } else {
-            if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * (len + slen));
-            __syncwarp();
-            if (lane < rows) {
-              const long row = row0 + lane;
-              bulk(st + lane * tk, a.wq + row * K + k0, len, full, pol_w);
-              bulk(st + ra.s_off + lane * ra.srow, (const unsigned char*)a.ws + ((row * nb + b0) * 2 - sh), slen,
-                   full, pol_w);
-            }
-          }
-          __syncwarp();
-        }
-      }
-    }
-    // Drain: every copy issued must have landed before this warp lets the
-    // block end.  Warp w's stages are counted as above; its last D stages are
-    // the latest phases of its D slots.
-    if (lane == 0) {
-      const long rows_last = (r1 - r0) - (ngroups - 1) * per_group;
-      const int nq_last = ngroups > 0 ? (int)((rows_last + QR - 1) / QR) : 0;
-      for (int w = 0; w < nwc; ++w) {
-        const long T = ngroups > 0 ? (ngroups - 1) * nsl + (w < nq_last ? nsl : 0) : 0;
-        for (long n = T - D > 0 ? T - D : 0; n < T; ++n) {
-          const unsigned bar = full0 + 8 * (unsigned)(w * D + n % D);
-          const unsigned long long t0 = gtimer();
-          while (!mbar_try(bar, (unsigned)(n / D) & 1u)) {
-            if (gtimer() - t0 > ra.wait_ns) {
-              atomicOr(ra.err, ERR_DRAIN);
-              break;
-            }
-          }
-        }
-      }
-      if (!FUSE && L > 0) {
-        const unsigned long long t0 = gtimer();
-        while (!mbar_try(act_bar, 0)) {
-          if (gtimer() - t0 > ra.wait_ns) {
-            atomicOr(ra.err, ERR_DRAIN);
-            break;
-          }
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp < nwc) {
-    // ------------------------------------------------------------------ consumers
-    const int rr = lane >> 3, j = lane & 7, q = j >> 1;
-    unsigned long long best[M];
+    ok = __all_sync(FULL, mbar_wait(act_bar, 0, ra.wait_ns, abort_flag));
+    if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
+  }
+
+  const int rr = lane >> 3, j = lane & 7, q = j >> 1;
+  const unsigned char* XQ = act;
+  const unsigned char* XL = act + (size_t)M * L;
+  const float* XS = (const float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1));
+  const float* XF = (const float*)act;
+  unsigned long long best[M];
+  P p[M];
 #pragma unroll
-    for (int t = 0; t < M; ++t) best[t] = 0;
-    bool ok = true;
-    if (FUSE) {
-      if (ra.pdl) griddep_wait();  // the raw activation is the previous kernel's output
-      fused_prologue<Q, M>(a, nwc, k_lo, L, act, nred, nden);
-    } else if (L > 0) {
-      ok = __all_sync(FULL, mbar_wait(act_bar, 0, ra.wait_ns, abort_flag));
-      if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
+  for (int t = 0; t < M; ++t) {
+    best[t] = 0;
+    p[t] = (P)0;
+  }
+  long n = 0;
+  for (; ok && n < T; ++n) {
+    const long qi = warp + (long)nwc * (n / nsl);
+    const int c = (int)(n % nsl);
+    const long row0 = r0 + QR * qi;
+    const int k0 = k_lo + c * tk;
+    const int len = (k_hi - k0 < tk) ? k_hi - k0 : tk;
+    const int slot = warp * D + (int)(n % D);
+    if (!__all_sync(FULL, mbar_wait(full0 + 8 * slot, (unsigned)(n / D) & 1u, ra.wait_ns, abort_flag))) {
+      if (lane == 0) raise_error(ra.err, ERR_WAIT_FULL, abort_flag);
+      ok = false;
+      break;
     }
-    if (ra.pdl && !FUSE) griddep_wait();  // before the first write of an output
-    const unsigned char* XQ = act;
-    const unsigned char* XL = act + (size_t)M * L;
-    const float* XS = (const float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1));
-    const float* XF = (const float*)act;
-    for (long gi = 0; ok && gi < ngroups; ++gi) {
-      const long g0 = r0 + gi * per_group;
-      const int rows_g = (int)(r1 - g0 < per_group ? r1 - g0 : per_group);
-      const int nq = (rows_g + QR - 1) / QR;
-      if (warp >= nq) continue;
-      const int rows = rows_g - QR * warp < QR ? rows_g - QR * warp : QR;
-      const bool row_ok = rr < rows;
-      P p[M];
-#pragma unroll
-      for (int t = 0; t < M; ++t) p[t] = (P)0;
-      for (int c = 0; c < nsl; ++c) {
-        const int k0 = k_lo + c * tk;
-        const int len = (k_hi - k0 < tk) ? k_hi - k0 : tk;
-        const int n = (int)gi * nsl + c;
-        const int slot = warp * D + n % D;
-        const unsigned ph = (unsigned)(n / D) & 1u;
-        if (!__all_sync(FULL, mbar_wait(full0 + 8 * slot, ph, ra.wait_ns, abort_flag))) {
-          if (lane == 0) raise_error(ra.err, ERR_WAIT_FULL, abort_flag);
-          ok = false;
-          break;
-        }
-        const unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
-        const int b0 = k0 >> 5;
-        const unsigned sh = whole ? 0u : (unsigned)(b0 & 7) * 2u;
-        const unsigned srow = whole ? (unsigned)nb * 2u : ra.srow;
-        const unsigned wrow = whole ? (unsigned)K : (unsigned)tk;
-        const unsigned char* Wr = st + rr * wrow + 16 * j;
-        const unsigned char* Sr = st + ra.s_off + rr * srow + sh + 2 * q;
-        const int ka = k0 - k_lo;  // offset of this slice in the activation area
-        const int nseg = len >> 7;
+    const unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
+    const int b0 = k0 >> 5;
+    const unsigned sh = whole ? 0u : (unsigned)(b0 & 7) * 2u;
+    const unsigned srow = whole ? (unsigned)nb * 2u : ra.srow;
+    const unsigned wrow = whole ? (unsigned)K : (unsigned)tk;
+    const unsigned char* Wr = st + rr * wrow + 16 * j;
+    const unsigned char* Sr = st + ra.s_off + rr * srow + sh + 2 * q;
+    const int ka = k0 - k_lo;  // offset of this slice in the activation area
+    const int nseg = len >> 7;
 #pragma unroll 4
-        for (int seg = 0; seg < nseg; ++seg) {
-          const int4 w = *(const int4*)(Wr + 128 * seg);
-          const float wsc = __half2float(*(const __half*)(Sr + 8 * seg));
-          const int xo = ka + 128 * seg + 16 * j;
-          const int bi = (ka >> 5) + 4 * seg + q;
+    for (int seg = 0; seg < nseg; ++seg) {
+      const int4 w = *(const int4*)(Wr + 128 * seg);
+      const float wsc = __half2float(*(const __half*)(Sr + 8 * seg));
+      const int xo = ka + 128 * seg + 16 * j;
+      const int bi = (ka >> 5) + 4 * seg + q;
 #pragma unroll
-          for (int t = 0; t < M; ++t) {
-            if constexpr (Q == 0) {
-              const float4* xv = (const float4*)(XF + (size_t)t * L + xo);
-              const int wi[4] = {w.x, w.y, w.z, w.w};
-              float h = 0.f;
+      for (int t = 0; t < M; ++t) {
+        if constexpr (Q == 0) {
+          const float4* xv = (const float4*)(XF + (size_t)t * L + xo);
+          const int wi[4] = {w.x, w.y, w.z, w.w};
+          float h = 0.f;
 #pragma unroll
-              for (int cc = 0; cc < 4; ++cc) {
-                const float4 xx = xv[cc];
-                const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
+          for (int cc = 0; cc < 4; ++cc) {
+            const float4 xx = xv[cc];
+            const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) h = __fmaf_rn((float)(int8_t)(wi[cc] >> (8 * k)), xe[k], h);
-              }
-              const float blk = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
-              p[t] = __fma_rn((double)wsc, (double)blk, (double)p[t]);
-            } else {
-              const int4 hv = *(const int4*)(XQ + (size_t)t * L + xo);
-              int d = dot16(w, hv);
-              d += __shfl_xor_sync(FULL, d, 1);
-              int e = 0;
-              if constexpr (Q == 2) {
-                const int4 lv = *(const int4*)(XL + (size_t)t * L + xo);
-                e = dot16(w, lv);
-                e += __shfl_xor_sync(FULL, e, 1);
-              }
-              const float s = XS[(size_t)t * (L / 32) + bi];
-              p[t] = q8_step<Q>((float)p[t], wsc, s, d, e);
-            }
+            for (int k = 0; k < 4; ++k) h = __fmaf_rn((float)(int8_t)(wi[cc] >> (8 * k)), xe[k], h);
           }
+          const float blk = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
+          p[t] = __fma_rn((double)wsc, (double)blk, (double)p[t]);
+        } else {
+          const int4 hv = *(const int4*)(XQ + (size_t)t * L + xo);
+          int d = dot16(w, hv);
+          d += __shfl_xor_sync(FULL, d, 1);
+          int e = 0;
+          if constexpr (Q == 2) {
+            const int4 lv = *(const int4*)(XL + (size_t)t * L + xo);
+            e = dot16(w, lv);
+            e += __shfl_xor_sync(FULL, e, 1);
+          }
+          const float s = XS[(size_t)t * (L / 32) + bi];
+          p[t] = q8_step<Q>((float)p[t], wsc, s, d, e);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
       }
-      if (!ok) break;
+    }
+    // The slot is free again: refill it with this warp's stage n + D.  The
+    // generic-proxy reads above must be ordered before the bulk copy's
+    // async-proxy writes into the same bytes.
+    __syncwarp();
+    if (issued < T) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(issued);
+      ++issued;
+    }
+    if (c == nsl - 1) {
       // quad done: (p0 + p2) + (p1 + p3) within each row's 8 lanes
+      const int rows = r1 - row0 < QR ? (int)(r1 - row0) : QR;
 #pragma unroll
       for (int t = 0; t < M; ++t) {
         P v = p[t];
         v = v + __shfl_down_sync(FULL, v, 4);
         v = v + __shfl_down_sync(FULL, v, 2);
-        if (j == 0 && row_ok) {
-          const long o = g0 + QR * warp + rr;
+        p[t] = (P)0;
+        if (j == 0 && rr < rows) {
+          const long o = row0 + rr;
           if (SPLIT) {
             const long idx = ((long)blockIdx.y * M + t) * N + o;
             if constexpr (Q == 0) a.part64[idx] = (double)v;
@@ -451,15 +411,37 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
         }
       }
     }
-    if (!SPLIT && a.amax) {
-#pragma unroll
-      for (int t = 0; t < M; ++t) {
-        const unsigned long long wmax = warp_max_u64(best[t]);
-        if (lane == 0) keys[t * MAXW + warp] = wmax;
+  }
+  // Drain: stages this warp issued but did not consume (only after an
+  // abort) must land before the block may end.
+  if (lane == 0) {
+    for (long m = n; m < issued; ++m) {
+      const unsigned bar = full0 + 8 * (unsigned)(warp * D + m % D);
+      const unsigned long long t0 = gtimer();
+      while (!mbar_try(bar, (unsigned)(m / D) & 1u)) {
+        if (gtimer() - t0 > ra.wait_ns) {
+          atomicOr(ra.err, ERR_DRAIN);
+          break;
+        }
+      }
+    }
+    if (!FUSE && L > 0 && warp == 0) {
+      const unsigned long long t0 = gtimer();
+      while (!mbar_try(act_bar, 0)) {
+        if (gtimer() - t0 > ra.wait_ns) {
+          atomicOr(ra.err, ERR_DRAIN);
+          break;
+        }
       }
     }
   }
+  __syncwarp();
   if (!SPLIT && a.amax) {
+#pragma unroll
+    for (int t = 0; t < M; ++t) {
+      const unsigned long long wmax = warp_max_u64(best[t]);
+      if (lane == 0) keys[t * MAXW + warp] = wmax;
+    }
     __syncthreads();
     if (threadIdx.x < M) {
       unsigned long long m = 0;
@@ -468,7 +450,6 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
     }
   }
 }
-
 
 // Explicit instantiation of every (M, SPLIT, FUSE) kernel of mode Q.
 #define LK_RING_PICK(Q)                                                             \
