@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--S", type=int, default=1, help="split-K chunks (gemv workload)")
     ap.add_argument("--argmax", action="store_true", help="argmax epilogue + reduce (gemv workload)")
     ap.add_argument("--path", default="auto", choices=["auto", "direct", "ring"])
+    ap.add_argument("--no-chain", action="store_true",
+                    help="sequence: one launch per projection instead of the whole-token chain kernel")
     ap.add_argument("--unfused", action="store_true",
                     help="sequence: separate norm/quantize launches instead of the fused prologue")
     ap.add_argument("--no-pdl", action="store_true",
@@ -272,7 +274,8 @@ def run_ours(a, rank, world):
 
     lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
     _apply_opts(lk, a)
-    stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=not a.unfused)
+    stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=not a.unfused,
+                        chain=not (a.no_chain or a.unfused))
     tok_bytes = stack.weight_bytes()
     stream = torch.cuda.Stream(device=dev)
 
@@ -291,7 +294,7 @@ def run_ours(a, rank, world):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         stack.run_token()
-    x_in = torch.empty_like(stack.x0)
+    x_in = stack.x_buf  # the token input buffer the launches read
     graph_e2e = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_e2e, stream=stream):
         stack.run_token(x_in=x_in)
@@ -350,8 +353,11 @@ def run_ours(a, rank, world):
            "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": idx_host.numel() * 4,
            "ms_per_step": ms_e2e, "steps": n_e2e}
 
-    # ---- roofline: CUDA events around every GEMV launch, one graph per token -------------
-    roof, per_name = roofline(stack, stream, a, torch)
+    # ---- roofline: CUDA events around every launch of the dominant kernel ---------------
+    if stack.chain is not None:
+        roof, per_name = roofline_chain(stack, stream, a, torch)
+    else:
+        roof, per_name = roofline(stack, stream, a, torch)
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
@@ -361,6 +367,7 @@ def run_ours(a, rank, world):
                    "l2": "inputs larger than L2 (8.04 GB of weights per step)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "gemv_path": "auto", "fused_prologue": {k: v for k, v in stack.fused.items()},
+                   "chain": stack.chain is not None,
                    "pdl": not a.no_pdl, "options": a.opt},
         "us_per_token": ms_max * 1e3,
         "pct_of_nominal_8TBs": value / world / NOMINAL_HBM_GBS,
@@ -503,6 +510,51 @@ def _max_over_ranks(v, dist, dev):
     t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def roofline_chain(stack, stream, a, torch):
+    """The whole-token chain kernel is the only launch per token: time each
+    launch with CUDA events (after the headline region)."""
+    peaks, src = measured_peaks()
+    steps = max(3, min(a.steps, 100))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        stack.run_token()
+        for e0, e1 in evs:
+            e0.record(stream)
+            stack.run_token()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+    B, mode = stack.B, stack.mode
+    act = (lambda K: B * K * 4) if mode == 0 else (lambda K: B * K * (2 if mode == 2 else 1) + B * (K // 32) * 4)
+    alg = stack.weight_bytes()
+    for N, K in list(stack.shapes.values()) * stack.L + [(stack.V, stack.H)]:
+        alg += B * K * 4 + B * N * 4  # raw f32 input read by the prologue, f32 output written
+    achieved = alg / (us * 1e-6) / 1e9
+    return ({"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": achieved / peaks["hbm_gbs"], "traffic": chain_traffic(alg), "peak_source": src,
+             "kernel": "gemv_chain_kernel (one cooperative launch per token)",
+             "algorithmic_bytes_per_launch": alg, "avg_launch_us": us, "launches_timed": steps},
+            {"chain": {"us": us, "GB/s": achieved, "launches": steps}})
+
+
+def chain_traffic(alg):
+    """DRAM bytes per launch from the committed ncu summary of this kernel, if
+    it was taken on the current sources (else None)."""
+    try:
+        from q8_quantized_gemv_gb300 import build
+        rec = {}
+        with open(os.path.join(ROOT, "profiles", "chain_traffic.txt")) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("sources_sha256") != build.sources_digest():
+            return None
+        return float(rec["dram_bytes_per_algorithmic_byte"]) * alg
+    except (OSError, KeyError, ValueError, AttributeError):
+        return None
 
 
 def roofline(stack, stream, a, torch):

@@ -143,6 +143,50 @@ lk_status lk_rmsnorm_quant_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, 
                                    uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream);
 
 /*
+ * One step of a GEMV chain: RMSNorm (gain != NULL) or the quantizer alone
+ * (gain == NULL) of the raw rows x, then y = W x, as lk_rmsnorm_quant_gemv_q8.
+ */
+typedef struct {
+  const int8_t* wq;        /* [N][K] levels, 16-byte aligned                       */
+  const uint16_t* ws;      /* [N][K/32] f16 scales, 16-byte aligned                */
+  int N, K;                /* K % 256 == 0                                          */
+  const float* x;          /* [M][K] raw f32 input rows                             */
+  const float* gain;       /* [K] RMSNorm gain, or NULL                             */
+  float* y;                /* [M][N] output                                         */
+  uint64_t* argmax_parts;  /* optional [M][lk_argmax_parts_max(N)] partial keys     */
+  int32_t* argmax_idx;     /* optional [M]: first index of the max of y (needs parts) */
+  int wait;                /* nonzero: x reads an earlier step's output (the blocks
+                              meet at a grid-wide barrier before this step)          */
+  int reserved;
+} lk_chain_op;
+
+/* Bytes of the sync buffer lk_gemv_chain needs (zeroed once by the caller). */
+size_t lk_chain_sync_bytes(void);
+
+/*
+ * A chain of steps in ONE cooperative launch (one block per SM): the form of
+ * model-as-a-kernel "megakernel.cu" (phases separated by a grid barrier,
+ * the next GEMV's weights streamed during it) for the projection path.  Each
+ * step's result is bit for bit lk_rmsnorm_quant_gemv_q8 of that step.  Steps
+ * run in order; a step with `wait` set starts after every block finished the
+ * steps before it, so its x may be an earlier step's y; a step without it
+ * must not read earlier outputs.  An argmax_idx step is followed by a barrier
+ * and a final reduce.
+ *   ops      HOST array of n_ops steps (validated and sized from it)
+ *   ops_dev  DEVICE copy of the same n_ops entries, read by the kernel
+ *   sync     DEVICE buffer of lk_chain_sync_bytes() bytes, zero before the
+ *            first call and left consistent by every completed call; after
+ *            LK_ERR_DEVICE_TIMEOUT zero it again.  Chains that may run at the
+ *            same time need separate sync buffers.
+ * Every grid-barrier wait is bounded (option "wait_us"); a timeout sets the
+ * device error word (lk_device_error).  LK_ERR_SHAPE if a step's K is not a
+ * multiple of 256 or the largest activation area does not fit in shared
+ * memory next to four weight stages.
+ */
+lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* ops_dev, int n_ops, lk_mode mode, int M,
+                        float eps, uint32_t* sync, cudaStream_t stream);
+
+/*
  * Which GEMV kernel a call of this shape would launch under the current
  * options, for 16-byte aligned operands: 1 the direct-load kernel (any
  * K % 32 == 0), 2 the bulk-copy ring kernel (K % 256 == 0 and the activation

@@ -35,6 +35,17 @@ def _headers():
                   glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
+def sources_digest() -> str:
+    """sha256 over the library's sources and headers (identifies the kernels
+    that a stored profile was taken on)."""
+    import hashlib
+    h = hashlib.sha256()
+    for p in _sources() + _headers():
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
 def _stale(target, deps):
     if not os.path.exists(target):
         return True

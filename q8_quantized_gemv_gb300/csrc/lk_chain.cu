@@ -1,0 +1,303 @@
+// GEMV chain: a sequence of fused RMSNorm/quantize -> Q8_0 GEMV steps (for
+// example one decode token's projections) in ONE cooperative launch.
+//
+// One block per SM runs every step over its balanced row range, with the
+// ring kernel's arrangement (each warp streams and computes its own quads).
+// The warps' weight streams run across step boundaries: when a warp frees a
+// stage it refills it with its next stage, which may belong to a later step,
+// so while the blocks meet at a grid-wide barrier (a step whose input is an
+// earlier step's output), the next step's first stages are already in flight.
+// This is the GB300 form of the whole-model kernel of model-as-a-kernel
+// "megakernel.cu" (phases separated by a grid barrier, the next GEMV's weights
+// prefetched during it), restricted to the projection path.
+//
+// The grid barrier is a counter and a generation word in the caller's sync
+// buffer; every wait on it is bounded by a wall-clock limit, after which the
+// block raises the error word and an abort flag, drains its copies and exits.
+#include "lk_ring_kernel.cuh"
+
+namespace lkring {
+namespace {
+
+constexpr int ERR_BARRIER = 32;
+
+struct ChainArgs {
+  const lk_chain_op* ops;  // device copy
+  int n_ops;
+  int nwc, depth;
+  unsigned stage_bytes, ring_off;
+  float eps;
+  unsigned* sync;           // [0] arrivals, [1] generation
+  unsigned long long wait_ns;
+  unsigned long long pol_w;
+  int* err;
+};
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// All blocks of the grid meet here (bounded).  Writes before it are visible
+// to every block after it.  Returns false after a timeout or an abort.
+__device__ bool grid_sync(unsigned* sync, unsigned nblocks, unsigned long long limit_ns, int* err,
+                          volatile int* abort_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0 && !*abort_flag) {
+    const unsigned gen = ld_acquire_gpu(sync + 1);
+    __threadfence();
+    const unsigned prev = atomicAdd(sync, 1u);
+    if (prev == nblocks - 1) {
+      atomicExch(sync, 0u);
+      __threadfence();
+      atomicAdd(sync + 1, 1u);
+    } else {
+      const unsigned long long t0 = gtimer();
+      unsigned spins = 0;
+      while (ld_acquire_gpu(sync + 1) == gen) {
+        if ((++spins & 63u) == 0 && gtimer() - t0 > limit_ns) {
+          atomicOr(err, ERR_BARRIER);
+          *abort_flag = 1;
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  return __syncthreads_or(*abort_flag) == 0;  // the same answer in every thread
+}
+
+__device__ __forceinline__ int chain_tk(int K) { return K <= TKMAX ? K : 4096; }
+
+__device__ __forceinline__ Geom op_geom(const lk_chain_op& o) {
+  const long N = o.N;
+  return make_geom(o.wq, o.ws, N, o.K, (long)blockIdx.x * N / gridDim.x, (long)(blockIdx.x + 1) * N / gridDim.x, 0,
+                   o.K, chain_tk(o.K));
+}
+
+template <int Q, int M>
+__global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainArgs ca) {
+  typedef typename part_t<Q>::t P;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int nwc = ca.nwc, D = ca.depth, NS = nwc * D;
+  unsigned char* act = smem;
+  unsigned char* ring = smem + ca.ring_off;
+  unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ca.stage_bytes);
+  volatile int* abort_flag = (volatile int*)(bars + MAX_STAGES + 1);
+  unsigned long long* keys = (unsigned long long*)(bars + MAX_STAGES + 3);  // [M][MAXW]
+  double* nred = (double*)(keys + LK_MAX_M * MAXW);                        // [M][32]
+  double* nden = nred + LK_MAX_M * 32;                                     // [M]
+  const unsigned full0 = smem_u32(bars);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned long long pol_w = ca.pol_w ? evict_first_policy() : 0ull;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(full0 + 8 * s, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // The issue cursor walks this warp's stages of every step in order.
+  int iop = 0;
+  Geom gi = op_geom(ca.ops[0]);
+  long in = 0, Ti = geom_stages(gi, warp, nwc), issued = 0;
+  auto issue_next = [&]() {
+    while (in >= Ti) {
+      if (++iop >= ca.n_ops) return;
+      gi = op_geom(ca.ops[iop]);
+      Ti = geom_stages(gi, warp, nwc);
+      in = 0;
+    }
+    const int slot = warp * D + (int)(issued % D);
+    issue_stage(gi, warp, nwc, in, ring + (size_t)slot * ca.stage_bytes, full0 + 8 * slot, pol_w, lane);
+    ++in;
+    ++issued;
+  };
+  for (int d = 0; d < D && iop < ca.n_ops; ++d) issue_next();
+
+  long consumed = 0;
+  bool ok = true;
+  for (int op = 0; ok && op < ca.n_ops; ++op) {
+    const lk_chain_op o = ca.ops[op];
+    if (o.wait && !grid_sync(ca.sync, gridDim.x, ca.wait_ns, ca.err, abort_flag)) {
+      ok = false;
+      break;
+    }
+    // the activation area is rewritten below: every warp is done with the last step
+    __syncthreads();
+    lkh::GemvProblem pr;
+    pr.K = o.K;
+    pr.xraw = o.x;
+    pr.gain = o.gain;
+    pr.eps = ca.eps;
+    fused_prologue<Q, M>(pr, nwc, 0, (unsigned)o.K, act, nred, nden);
+    const Geom g = op_geom(o);
+    const long T = geom_stages(g, warp, nwc);
+    const Act ac{act, (unsigned)o.K};
+    unsigned long long best[M];
+    P p[M];
+#pragma unroll
+    for (int t = 0; t < M; ++t) {
+      best[t] = 0;
+      p[t] = (P)0;
+    }
+    for (long n = 0; n < T; ++n) {
+      const int slot = warp * D + (int)(consumed % D);
+      if (!__all_sync(FULL, mbar_wait(full0 + 8 * slot, (unsigned)(consumed / D) & 1u, ca.wait_ns, abort_flag))) {
+        if (lane == 0) raise_error(ca.err, ERR_WAIT_FULL, abort_flag);
+        ok = false;
+        break;
+      }
+      unsigned char* st = ring + (size_t)slot * ca.stage_bytes;
+      compute_stage<Q, M>(p, g, n, st, ac, lane);
+      __syncwarp();
+      ++consumed;
+      if (iop < ca.n_ops) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_next();
+      }
+      if ((int)(n % g.nsl) == g.nsl - 1) {
+        lkh::GemvProblem dummy;
+        finish_quad<Q, M, false>(p, g, warp, nwc, n, dummy, 0, o.y, best, lane);
+      }
+    }
+    ok = __syncthreads_and(ok) != 0;  // every warp agrees before the next barrier
+    if (!ok) break;
+    if (o.argmax_parts) {
+#pragma unroll
+      for (int t = 0; t < M; ++t) {
+        const unsigned long long wmax = warp_max_u64(best[t]);
+        if (lane == 0) keys[t * MAXW + warp] = wmax;
+      }
+      __syncthreads();
+      if (threadIdx.x < M) {
+        unsigned long long m = 0;
+        for (int w = 0; w < nwc; ++w) m = keys[threadIdx.x * MAXW + w] > m ? keys[threadIdx.x * MAXW + w] : m;
+        o.argmax_parts[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
+      }
+      if (o.argmax_idx) {
+        ok = grid_sync(ca.sync, gridDim.x, ca.wait_ns, ca.err, abort_flag);
+        if (!ok) break;
+        if (blockIdx.x == 0 && warp < M) {
+          unsigned long long m = 0;
+          for (int i = lane; i < (int)gridDim.x; i += 32) {
+            const unsigned long long k = o.argmax_parts[(long)warp * gridDim.x + i];
+            m = k > m ? k : m;
+          }
+          m = warp_max_u64(m);
+          if (lane == 0) o.argmax_idx[warp] = (int)(0xFFFFFFFFu - (unsigned)(m & 0xFFFFFFFFull));
+        }
+      }
+    }
+  }
+  // Drain: stages issued but not consumed (after an abort) must land before
+  // the block may end.
+  if (lane == 0)
+    for (long m = consumed; m < issued; ++m)
+      drain_wait(full0 + 8 * (unsigned)(warp * D + m % D), (unsigned)(m / D) & 1u, ca.wait_ns, ca.err);
+  __syncwarp();
+}
+
+typedef void (*chain_fn)(const ChainArgs);
+
+template <int Q>
+chain_fn pick_m(int M) {
+  switch (M) {
+    case 1: return gemv_chain_kernel<Q, 1>;
+    case 2: return gemv_chain_kernel<Q, 2>;
+    case 3: return gemv_chain_kernel<Q, 3>;
+    case 4: return gemv_chain_kernel<Q, 4>;
+    case 5: return gemv_chain_kernel<Q, 5>;
+    case 6: return gemv_chain_kernel<Q, 6>;
+    case 7: return gemv_chain_kernel<Q, 7>;
+    default: return gemv_chain_kernel<Q, 8>;
+  }
+}
+
+unsigned act_area_rt(int mode, int M, unsigned len) {
+  return mode == 0 ? M * len * 4u : M * len * (mode == 2 ? 2u : 1u) + M * len / 8u;
+}
+
+unsigned stage_bytes_for(int K) {
+  const unsigned tk = K <= TKMAX ? (unsigned)K : 4096u;
+  const bool whole = tk >= (unsigned)K;
+  const unsigned srow = whole ? tk / 16u : tk / 16u + 16u;
+  return (QR * tk + QR * srow + 127u) & ~127u;
+}
+
+}  // namespace
+}  // namespace lkring
+
+using namespace lkring;
+
+extern "C" size_t lk_chain_sync_bytes(void) { return 64; }
+
+extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* ops_dev, int n_ops, lk_mode mode,
+                                   int M, float eps, uint32_t* sync, cudaStream_t stream) {
+  using lkh::aligned;
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+  if (M < 1 || M > LK_MAX_M || n_ops < 0) return LK_ERR_SHAPE;
+  if (n_ops == 0) return LK_OK;
+  if (!ops || !ops_dev || !sync) return LK_ERR_ARG;
+  if (!aligned(ops_dev, 8) || !aligned(sync, 8)) return LK_ERR_ALIGN;
+  unsigned act_cap = 0, sb = 0;
+  for (int i = 0; i < n_ops; ++i) {
+    const lk_chain_op& o = ops[i];
+    if (o.N < 1 || o.K < 256 || o.K % 256) return LK_ERR_SHAPE;
+    if (!o.wq || !o.ws || !o.x || !o.y || (o.argmax_idx && !o.argmax_parts)) return LK_ERR_ARG;
+    if (!aligned(o.wq, 16) || !aligned(o.ws, 16) || !aligned(o.x, 4) || (o.gain && !aligned(o.gain, 4)) ||
+        !aligned(o.y, 4) || (o.argmax_parts && !aligned(o.argmax_parts, 8)) ||
+        (o.argmax_idx && !aligned(o.argmax_idx, 4)))
+      return LK_ERR_ALIGN;
+    const unsigned a = act_area_rt(mode, M, (unsigned)o.K), s = stage_bytes_for(o.K);
+    act_cap = a > act_cap ? a : act_cap;
+    sb = s > sb ? s : sb;
+  }
+  const lkh::DeviceInfo* d = lkh::device_info(nullptr);
+  if (!d) return LK_ERR_CUDA;
+  const unsigned ring_off = (act_cap + 127u) & ~127u;
+  long cap = d->smem_optin;
+  if (lkh::opt_ring_kb > 0 && lkh::opt_ring_kb * 1024 < cap) cap = lkh::opt_ring_kb * 1024;
+  const long room = cap - (long)ring_off - (long)TAIL;
+  int fit = room > 0 ? (int)(room / sb) : 0;
+  if (fit > MAX_STAGES) fit = MAX_STAGES;
+  if (lkh::opt_ring_stages > 0 && lkh::opt_ring_stages < fit) fit = (int)lkh::opt_ring_stages;
+  int w = lkh::opt_ring_warps > 0 ? (int)lkh::opt_ring_warps : (fit < MAXW ? fit : MAXW);
+  if (w > fit) w = fit;
+  const int depth = w > 0 ? fit / w : 0;
+  if (w < 1 || w * depth < 4) return LK_ERR_SHAPE;
+  const unsigned total = ring_off + (unsigned)(w * depth) * sb + TAIL;
+  chain_fn f = mode == 0 ? pick_m<0>(M) : mode == 1 ? pick_m<1>(M) : pick_m<2>(M);
+  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)total) != cudaSuccess)
+    return LK_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, w * 32, total) != cudaSuccess || per_sm < 1)
+    return LK_ERR_SHAPE;
+  ChainArgs ca;
+  ca.ops = ops_dev;
+  ca.n_ops = n_ops;
+  ca.nwc = w;
+  ca.depth = depth;
+  ca.stage_bytes = sb;
+  ca.ring_off = ring_off;
+  ca.eps = eps;
+  ca.sync = sync;
+  ca.wait_ns = lkh::opt_wait_us > 0 ? (unsigned long long)lkh::opt_wait_us * 1000ull : 2000000000ull;
+  ca.pol_w = lkh::opt_ring_hint ? 1ull : 0ull;
+  ca.err = lkh::error_word_ptr();
+  if (!ca.err) return LK_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(d->sm_count);
+  cfg.blockDim = dim3(w * 32);
+  cfg.dynamicSmemBytes = total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, f, ca) != cudaSuccess) return LK_ERR_CUDA;
+  return lkh::launch_status();
+}

@@ -60,6 +60,9 @@ struct GemvProblem {
   float eps;
 };
 
+// Device address of the error word that bounded device waits set (lk_ring.cu).
+int* error_word_ptr();
+
 // Bulk-copy ring kernel (lk_ring.cu).  Returns LK_ERR_SHAPE when the problem
 // is outside what the ring kernel takes (the caller then uses the direct
 // kernel), otherwise the launch status; *n_parts receives the blocks launched.

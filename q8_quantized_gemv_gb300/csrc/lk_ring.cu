@@ -57,9 +57,12 @@ ring_fn pick(int mode, int M, bool split, bool fuse) {
                                                               : ring_pick<2>(M, split, fuse);
 }
 
+}  // namespace
+}  // namespace lkring
+
 // Device address of the error word on the current device, looked up once
 // per device.
-int* error_word_ptr() {
+int* lkh::error_word_ptr() {
   static int* ptr[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
@@ -70,6 +73,9 @@ int* error_word_ptr() {
   }
   return ptr[dev];
 }
+
+namespace lkring {
+namespace {
 
 unsigned act_area_rt(int mode, int M, unsigned len) {
   return mode == 0 ? M * len * 4u : M * len * (mode == 2 ? 2u : 1u) + M * len / 8u;
@@ -168,7 +174,7 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   ra.wait_ns = opt_wait_us > 0 ? (unsigned long long)opt_wait_us * 1000ull : 2000000000ull;
   ra.pol_w = opt_ring_hint ? 1ull : 0ull;
   ra.pdl = opt_pdl ? 1 : 0;
-  ra.err = error_word_ptr();
+  ra.err = lkh::error_word_ptr();
   if (!ra.err) return LK_ERR_CUDA;
   const int S = p.split && p.S > 1 ? p.S : 1;
   const int g = opt_grid_ctas > 0 ? (int)opt_grid_ctas : d->sm_count * (opt_ring_cps > 1 ? (int)opt_ring_cps : 1);
@@ -206,7 +212,7 @@ extern "C" lk_status lk_device_error(int reset, int* code) {
 
 extern "C" lk_status lk_selftest_wait_timeout(unsigned limit_us, cudaStream_t stream) {
   if (limit_us == 0 || limit_us > 10000000u) return LK_ERR_ARG;
-  int* err = lkring::error_word_ptr();
+  int* err = lkh::error_word_ptr();
   if (!err) return LK_ERR_CUDA;
   lkring::wait_selftest_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_us * 1000ull, err);
   return lkh::launch_status();

@@ -139,13 +139,19 @@ __device__ __forceinline__ void bulk(void* dst, const void* src, unsigned bytes,
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
-__device__ __forceinline__ void consumers_sync(int) { __syncthreads(); }
 
 // The activation area computed in the block from the raw f32 rows: RMSNorm
 // (when a gain is given) and the quantizer of mode Q, bit for bit what
 // lk_rmsnorm_quant / lk_quantize_act compute.  The norm's sum of squares
 // follows the block of vt = min(K, 1024) threads of "kernels.rs"
-// lk_rmsnorm_row: the nwc consumer warps play its vt/32 warps in turn.
+// lk_rmsnorm_row: its vt/32 warps are played by the block's nwc warps in turn
+// (warp w plays w, w + nwc, ...), virtual warp v's lane l adding the squares
+// of values 32v + l + vt*u in ascending u.  The same warp then normalizes and
+// quantizes exactly the 32-groups v + (vt/32)*u it loaded, so each row is
+// read from global memory once, all of a warp's loads in flight together.
+constexpr int PRO_VW = 4;  // virtual warps per real warp on the fast path
+constexpr int PRO_KU = 8;  // values per virtual thread on the fast path (K <= 8192)
+
 template <int Q, int M>
 __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, unsigned L, unsigned char* act,
                                void* red_raw, void* den_raw) {
@@ -155,48 +161,315 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
   const int lane = threadIdx.x & 31, cw = threadIdx.x >> 5;
   const int K = a.K;
   const bool norm = a.gain != nullptr;
-  if (norm) {
-    const int vt = K < 1024 ? K : 1024, vw = vt >> 5;
+  const int vt = K < 1024 ? K : 1024, nvw_all = vt >> 5, KU = K / vt;
+  const int nvw = cw < nvw_all ? (nvw_all - 1 - cw) / nwc + 1 : 0;
+  const bool fast = k_lo == 0 && (int)L == K && KU <= PRO_KU && (nvw_all + nwc - 1) / nwc <= PRO_VW &&
+                    K % vt == 0;
+  if (fast) {
+    float gv[PRO_VW][PRO_KU];
+    if (norm) {
+#pragma unroll
+      for (int iv = 0; iv < PRO_VW; ++iv)
+#pragma unroll
+        for (int u = 0; u < PRO_KU; ++u)
+          if (iv < nvw && u < KU) gv[iv][u] = __ldg(a.gain + 32 * (cw + nwc * iv) + lane + vt * u);
+    }
     for (int t = 0; t < M; ++t) {
       const float* xr = a.xraw + (long)t * K;
-      for (int w = cw; w < vw; w += nwc) {
+      float xv[PRO_VW][PRO_KU];
+#pragma unroll
+      for (int iv = 0; iv < PRO_VW; ++iv)
+#pragma unroll
+        for (int u = 0; u < PRO_KU; ++u)
+          if (iv < nvw && u < KU) xv[iv][u] = __ldg(xr + 32 * (cw + nwc * iv) + lane + vt * u);
+      A dn = (A)1;
+      if (norm) {
+#pragma unroll
+        for (int iv = 0; iv < PRO_VW; ++iv) {
+          if (iv < nvw) {
+            A acc = 0;
+#pragma unroll
+            for (int u = 0; u < PRO_KU; ++u)
+              if (u < KU) acc = fma_acc((A)xv[iv][u], acc);
+            acc = warp_tree_sum(acc);
+            if (lane == 0) red[t * 32 + cw + nwc * iv] = acc;
+          }
+        }
+        __syncthreads();
+        if (cw == 0) {
+          A v = lane < nvw_all ? red[t * 32 + lane] : (A)0;
+          v = warp_tree_sum(v);
+          if (lane == 0) den[t] = norm_div_add(v, K, a.eps);
+        }
+        __syncthreads();
+        dn = den[t];
+      }
+#pragma unroll
+      for (int iv = 0; iv < PRO_VW; ++iv)
+#pragma unroll
+        for (int u = 0; u < PRO_KU; ++u)
+          if (iv < nvw && u < KU) {
+            const int g = cw + nwc * iv + nvw_all * u;  // the 32-group holding these values
+            const int i = 32 * g + lane;
+            float v = xv[iv][u];
+            if (norm) v = norm_scale(v, dn, gv[iv][u]);
+            if constexpr (Q == 0) {
+              ((float*)act)[(size_t)t * L + i] = v;
+            } else {
+              int8_t* XQ = (int8_t*)act + (size_t)t * L;
+              int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
+              float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
+              quant_lane<Q>(v, XQ, XL, XS, i, g, lane);
+            }
+          }
+    }
+    __syncthreads();
+    return;
+  }
+  // general path: any K, chunk or warp count.  The sum of squares walks each
+  // virtual thread's values in order (loads unrolled ahead of the chain);
+  // then every warp normalizes and quantizes its groups g = cw + nwc*i, eight
+  // groups' loads in flight at a time.
+  if (norm) {
+    for (int t = 0; t < M; ++t) {
+      const float* xr = a.xraw + (long)t * K;
+      for (int w = cw; w < nvw_all; w += nwc) {
         A acc = 0;
+#pragma unroll 8
         for (int i = 32 * w + lane; i < K; i += vt) acc = fma_acc((A)__ldg(xr + i), acc);
         acc = warp_tree_sum(acc);
         if (lane == 0) red[t * 32 + w] = acc;
       }
     }
-    consumers_sync(nwc);
+    __syncthreads();
     if (cw == 0) {
       for (int t = 0; t < M; ++t) {
-        A v = lane < vw ? red[t * 32 + lane] : (A)0;
+        A v = lane < nvw_all ? red[t * 32 + lane] : (A)0;
         v = warp_tree_sum(v);
         if (lane == 0) den[t] = norm_div_add(v, K, a.eps);
       }
     }
-    consumers_sync(nwc);
+    __syncthreads();
   }
+  constexpr int GB = 8;
   const int ng = (int)(L >> 5);
   for (int t = 0; t < M; ++t) {
     const float* xr = a.xraw + (long)t * K + k_lo;
     const A dn = norm ? den[t] : (A)1;
-    for (int g = cw; g < ng; g += nwc) {
-      const int i = 32 * g + lane;
-      // past the row's end (a chunk narrower than the area) the area keeps zeros
-      const bool in = k_lo + i < K;
-      float v = in ? __ldg(xr + i) : 0.f;
-      if (norm && in) v = norm_scale(v, dn, __ldg(a.gain + k_lo + i));
-      if constexpr (Q == 0) {
-        ((float*)act)[(size_t)t * L + i] = v;
-      } else {
-        int8_t* XQ = (int8_t*)act + (size_t)t * L;
-        int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
-        float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
-        quant_lane<Q>(v, XQ, XL, XS, i, g, lane);
+    for (int g0 = cw; g0 < ng; g0 += GB * nwc) {
+      float xv[GB], gv[GB];
+#pragma unroll
+      for (int b = 0; b < GB; ++b) {
+        const int g = g0 + b * nwc, i = 32 * g + lane;
+        const bool in = g < ng && k_lo + i < K;
+        xv[b] = in ? __ldg(xr + i) : 0.f;
+        gv[b] = (norm && in) ? __ldg(a.gain + k_lo + i) : 1.f;
+      }
+#pragma unroll
+      for (int b = 0; b < GB; ++b) {
+        const int g = g0 + b * nwc, i = 32 * g + lane;
+        if (g >= ng) break;  // warp-uniform
+        float v = xv[b];
+        // past the row's end (a chunk narrower than the area) the area keeps zeros
+        if (norm && k_lo + i < K) v = norm_scale(v, dn, gv[b]);
+        if constexpr (Q == 0) {
+          ((float*)act)[(size_t)t * L + i] = v;
+        } else {
+          int8_t* XQ = (int8_t*)act + (size_t)t * L;
+          int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
+          float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
+          quant_lane<Q>(v, XQ, XL, XS, i, g, lane);
+        }
       }
     }
   }
-  consumers_sync(nwc);
+  __syncthreads();
+}
+
+// ---- one GEMV's stage stream, shared by the ring and the chain kernels -------------
+
+// Where a block's stages come from: rows [r0, r1) of a matrix, K chunk
+// [k_lo, k_hi), cut into quads (4 rows) x slices (tk bytes of K).
+struct Geom {
+  const int8_t* wq;
+  const unsigned char* ws;  // f16 scales, as bytes
+  long N;
+  int K, nb;
+  long r0, r1;
+  int k_lo, k_hi, tk, nsl;
+  bool whole;               // a quad's levels (and its scales) are contiguous: 2 copies a stage
+  unsigned s_off, srow;     // scale area inside a stage, bytes per row there
+};
+
+__device__ __forceinline__ Geom make_geom(const int8_t* wq, const void* ws, long N, int K, long r0, long r1,
+                                          int k_lo, int k_hi, int tk) {
+  Geom g;
+  g.wq = wq;
+  g.ws = (const unsigned char*)ws;
+  g.N = N;
+  g.K = K;
+  g.nb = K >> 5;
+  g.r0 = r0;
+  g.r1 = r1;
+  g.k_lo = k_lo;
+  g.k_hi = k_hi;
+  g.tk = tk;
+  g.nsl = (k_hi - k_lo + tk - 1) / tk;
+  g.whole = (k_lo == 0 && k_hi == K && tk >= K);
+  g.s_off = (unsigned)(QR * tk);
+  g.srow = g.whole ? (unsigned)g.nb * 2u : (unsigned)tk / 16u + 16u;
+  return g;
+}
+
+// Stages of warp `warp` of `nwc`: its quads are warp, warp + nwc, ...
+__device__ __forceinline__ long geom_stages(const Geom& g, int warp, int nwc) {
+  const long nq = (g.r1 - g.r0 + QR - 1) / QR;
+  return warp < nq ? ((nq - 1 - warp) / nwc + 1) * g.nsl : 0;
+}
+
+// Issue this warp's stage n (quad warp + nwc*(n / nsl), slice n % nsl) into
+// the stage buffer `st`, completing on `full`.  All lanes call it.
+__device__ __forceinline__ void issue_stage(const Geom& g, int warp, int nwc, long n, unsigned char* st,
+                                            unsigned full, unsigned long long pol, int lane) {
+  const long qi = warp + (long)nwc * (n / g.nsl);
+  const int c = (int)(n % g.nsl);
+  const long row0 = g.r0 + QR * qi;
+  const int rows = g.r1 - row0 < QR ? (int)(g.r1 - row0) : QR;
+  const int k0 = g.k_lo + c * g.tk;
+  const int len = (g.k_hi - k0 < g.tk) ? g.k_hi - k0 : g.tk;
+  if (g.whole) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)g.K * 17u / 16u);
+      bulk(st, g.wq + row0 * g.K, rows * g.K, full, pol);
+      bulk(st + g.s_off, g.ws + row0 * g.nb * 2, rows * g.nb * 2, full, pol);
+    }
+  } else {
+    const int b0 = k0 >> 5, b1 = b0 + (len >> 5);
+    const unsigned sh = (unsigned)(b0 & 7) * 2u;               // scales' offset in the first 16 B
+    const unsigned slen = ((b1 - b0) * 2u + sh + 15u) & ~15u;  // 16-byte superset of a row's scales
+    if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * (len + slen));
+    __syncwarp();
+    if (lane < rows) {
+      const long row = row0 + lane;
+      bulk(st + lane * g.tk, g.wq + row * g.K + k0, len, full, pol);
+      bulk(st + g.s_off + lane * g.srow, g.ws + ((row * g.nb + b0) * 2 - sh), slen, full, pol);
+    }
+  }
+  __syncwarp();
+}
+
+// The activation area of M rows over `L` bytes of K: int8 words (and low
+// words) and f32 scales, or f32 values under Dequant.
+struct Act {
+  const unsigned char* base;
+  unsigned L;
+};
+
+// Accumulate this warp's stage n (in `st`) into the partials p: 8 lanes per
+// row, lane j reading bytes 16j..16j+15 of each 128-byte segment, lanes 2q and
+// 2q+1 meeting by one xor-shuffle for block q's exact dot, lane 2q chaining
+// partial q = b mod 4 in ascending block order ("kernels.rs" lk_q8_rows_dot,
+// lk_q8_term).
+template <int Q, int M>
+__device__ __forceinline__ void compute_stage(typename part_t<Q>::t (&p)[M], const Geom& g, long n,
+                                              const unsigned char* st, const Act& act, int lane) {
+  const int rr = lane >> 3, j = lane & 7, q = j >> 1;
+  const int c = (int)(n % g.nsl);
+  const int k0 = g.k_lo + c * g.tk;
+  const int len = (g.k_hi - k0 < g.tk) ? g.k_hi - k0 : g.tk;
+  const int b0 = k0 >> 5;
+  const unsigned sh = g.whole ? 0u : (unsigned)(b0 & 7) * 2u;
+  const unsigned wrow = g.whole ? (unsigned)g.K : (unsigned)g.tk;
+  const unsigned char* Wr = st + rr * wrow + 16 * j;
+  const unsigned char* Sr = st + g.s_off + rr * g.srow + sh + 2 * q;
+  const unsigned L = act.L;
+  const unsigned char* XQ = act.base;
+  const unsigned char* XL = act.base + (size_t)M * L;
+  const float* XS = (const float*)(act.base + (size_t)M * L * (Q == 2 ? 2 : 1));
+  const float* XF = (const float*)act.base;
+  const int ka = k0 - g.k_lo;  // offset of this slice in the activation area
+  const int nseg = len >> 7;
+#pragma unroll 4
+  for (int seg = 0; seg < nseg; ++seg) {
+    const int4 w = *(const int4*)(Wr + 128 * seg);
+    const float wsc = __half2float(*(const __half*)(Sr + 8 * seg));
+    const int xo = ka + 128 * seg + 16 * j;
+    const int bi = (ka >> 5) + 4 * seg + q;
+#pragma unroll
+    for (int t = 0; t < M; ++t) {
+      if constexpr (Q == 0) {
+        const float4* xv = (const float4*)(XF + (size_t)t * L + xo);
+        const int wi[4] = {w.x, w.y, w.z, w.w};
+        float h = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const float4 xx = xv[cc];
+          const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) h = __fmaf_rn((float)(int8_t)(wi[cc] >> (8 * k)), xe[k], h);
+        }
+        const float blk = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
+        p[t] = __fma_rn((double)wsc, (double)blk, (double)p[t]);
+      } else {
+        const int4 hv = *(const int4*)(XQ + (size_t)t * L + xo);
+        int d = dot16(w, hv);
+        d += __shfl_xor_sync(FULL, d, 1);
+        int e = 0;
+        if constexpr (Q == 2) {
+          const int4 lv = *(const int4*)(XL + (size_t)t * L + xo);
+          e = dot16(w, lv);
+          e += __shfl_xor_sync(FULL, e, 1);
+        }
+        const float s = XS[(size_t)t * (L / 32) + bi];
+        p[t] = q8_step<Q>((float)p[t], wsc, s, d, e);
+      }
+    }
+  }
+}
+
+// The last slice of a quad: (p0 + p2) + (p1 + p3) within each row's 8 lanes
+// ("kernels.rs" lk_q8_sum4), stored as y (and an argmax key) or as split-K
+// partial `chunk`; p is reset.
+template <int Q, int M, bool SPLIT>
+__device__ __forceinline__ void finish_quad(typename part_t<Q>::t (&p)[M], const Geom& g, int warp, int nwc, long n,
+                                            const lkh::GemvProblem& a, int chunk, float* y,
+                                            unsigned long long (&best)[M], int lane) {
+  typedef typename part_t<Q>::t P;
+  const int rr = lane >> 3, j = lane & 7;
+  const long qi = warp + (long)nwc * (n / g.nsl);
+  const long row0 = g.r0 + QR * qi;
+  const int rows = g.r1 - row0 < QR ? (int)(g.r1 - row0) : QR;
+#pragma unroll
+  for (int t = 0; t < M; ++t) {
+    P v = p[t];
+    v = v + __shfl_down_sync(FULL, v, 4);
+    v = v + __shfl_down_sync(FULL, v, 2);
+    p[t] = (P)0;
+    if (j == 0 && rr < rows) {
+      const long o = row0 + rr;
+      if (SPLIT) {
+        const long idx = ((long)chunk * M + t) * g.N + o;
+        if constexpr (Q == 0) a.part64[idx] = (double)v;
+        else a.y[idx] = (float)v;
+      } else {
+        const float yv = Q == 0 ? __double2float_rn((double)v) : (float)v;
+        y[(long)t * g.N + o] = yv;
+        const unsigned long long kk = amax_key(yv, (unsigned)o);
+        best[t] = kk > best[t] ? kk : best[t];
+      }
+    }
+  }
+}
+
+// Bounded wait on `bar` that ignores the abort flag (used to drain copies).
+__device__ __forceinline__ void drain_wait(unsigned bar, unsigned parity, unsigned long long limit_ns, int* err) {
+  const unsigned long long t0 = gtimer();
+  while (!mbar_try(bar, parity)) {
+    if (gtimer() - t0 > limit_ns) {
+      atomicOr(err, ERR_DRAIN);
+      break;
+    }
+  }
 }
 
 template <int Q, int M, bool SPLIT, bool FUSE>
@@ -218,21 +491,16 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, nb = K >> 5;
   const long N = a.N;
-  const long r0 = (long)blockIdx.x * N / ra.gx, r1 = (long)(blockIdx.x + 1) * N / ra.gx;
   int b_lo = 0, b_hi = nb;
   if (SPLIT) {
     b_lo = splitk_bound(nb, a.S, blockIdx.y);
     b_hi = splitk_bound(nb, a.S, blockIdx.y + 1);
   }
-  const int k_lo = 32 * b_lo, k_hi = 32 * b_hi;
+  const int k_lo = 32 * b_lo;
+  const Geom g = make_geom(a.wq, a.ws, N, K, (long)blockIdx.x * N / ra.gx, (long)(blockIdx.x + 1) * N / ra.gx,
+                           k_lo, 32 * b_hi, (int)ra.tk);
   const unsigned L = ra.act_len;
-  const int tk = (int)ra.tk;
-  const int nsl = (k_hi - k_lo + tk - 1) / tk;             // K slices per quad
-  const bool whole = (k_lo == 0 && k_hi == K && tk >= K);  // a quad's bytes are contiguous
-  const long nquads = (r1 - r0 + QR - 1) / QR;
-  // this warp's quads are warp, warp + nwc, ...; its stages n = (m-th quad, slice c) = m * nsl + c
-  const long myq = warp < nquads ? (nquads - 1 - warp) / nwc + 1 : 0;
-  const long T = myq * nsl;
+  const long T = geom_stages(g, warp, nwc);
   const unsigned long long pol_w = ra.pol_w ? evict_first_policy() : 0ull;
 
   if (threadIdx.x == 0) {
@@ -244,42 +512,11 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   __syncthreads();
   if (ra.pdl && threadIdx.x == 0) griddep_launch();
 
-  // Issue stage n of this warp into its slot n % D (all lanes call it).
-  auto issue = [&](long n) {
-    const long qi = warp + (long)nwc * (n / nsl);
-    const int c = (int)(n % nsl);
-    const long row0 = r0 + QR * qi;
-    const int rows = r1 - row0 < QR ? (int)(r1 - row0) : QR;
-    const int k0 = k_lo + c * tk;
-    const int len = (k_hi - k0 < tk) ? k_hi - k0 : tk;
-    const int slot = warp * D + (int)(n % D);
-    const unsigned full = full0 + 8 * slot;
-    unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
-    if (whole) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)K * 17u / 16u);
-        bulk(st, a.wq + row0 * K, rows * K, full, pol_w);
-        bulk(st + ra.s_off, (const unsigned char*)a.ws + row0 * nb * 2, rows * nb * 2, full, pol_w);
-      }
-    } else {
-      const int b0 = k0 >> 5, b1 = b0 + (len >> 5);
-      const unsigned sh = (unsigned)(b0 & 7) * 2u;               // scales' offset in the first 16 B
-      const unsigned slen = ((b1 - b0) * 2u + sh + 15u) & ~15u;  // 16-byte superset of a row's scales
-      if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * (len + slen));
-      __syncwarp();
-      if (lane < rows) {
-        const long row = row0 + lane;
-        bulk(st + lane * tk, a.wq + row * K + k0, len, full, pol_w);
-        bulk(st + ra.s_off + lane * ra.srow, (const unsigned char*)a.ws + ((row * nb + b0) * 2 - sh), slen, full,
-             pol_w);
-      }
-    }
-    __syncwarp();
-  };
-
   // Weights do not depend on the previous kernel: start streaming at once.
   long issued = 0;
-  for (; issued < T && issued < D; ++issued) issue(issued);
+  for (; issued < T && issued < D; ++issued)
+    issue_stage(g, warp, nwc, issued, ring + (size_t)(warp * D + issued % D) * ra.stage_bytes,
+                full0 + 8 * (warp * D + (int)(issued % D)), pol_w, lane);
 
   if (ra.pdl) griddep_wait();  // from here on: reads of activations, writes of outputs
   bool ok = true;
@@ -308,11 +545,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
     if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
   }
 
-  const int rr = lane >> 3, j = lane & 7, q = j >> 1;
-  const unsigned char* XQ = act;
-  const unsigned char* XL = act + (size_t)M * L;
-  const float* XS = (const float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1));
-  const float* XF = (const float*)act;
+  const Act ac{act, L};
   unsigned long long best[M];
   P p[M];
 #pragma unroll
@@ -322,118 +555,31 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   }
   long n = 0;
   for (; ok && n < T; ++n) {
-    const long qi = warp + (long)nwc * (n / nsl);
-    const int c = (int)(n % nsl);
-    const long row0 = r0 + QR * qi;
-    const int k0 = k_lo + c * tk;
-    const int len = (k_hi - k0 < tk) ? k_hi - k0 : tk;
     const int slot = warp * D + (int)(n % D);
     if (!__all_sync(FULL, mbar_wait(full0 + 8 * slot, (unsigned)(n / D) & 1u, ra.wait_ns, abort_flag))) {
       if (lane == 0) raise_error(ra.err, ERR_WAIT_FULL, abort_flag);
       ok = false;
       break;
     }
-    const unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
-    const int b0 = k0 >> 5;
-    const unsigned sh = whole ? 0u : (unsigned)(b0 & 7) * 2u;
-    const unsigned srow = whole ? (unsigned)nb * 2u : ra.srow;
-    const unsigned wrow = whole ? (unsigned)K : (unsigned)tk;
-    const unsigned char* Wr = st + rr * wrow + 16 * j;
-    const unsigned char* Sr = st + ra.s_off + rr * srow + sh + 2 * q;
-    const int ka = k0 - k_lo;  // offset of this slice in the activation area
-    const int nseg = len >> 7;
-#pragma unroll 4
-    for (int seg = 0; seg < nseg; ++seg) {
-      const int4 w = *(const int4*)(Wr + 128 * seg);
-      const float wsc = __half2float(*(const __half*)(Sr + 8 * seg));
-      const int xo = ka + 128 * seg + 16 * j;
-      const int bi = (ka >> 5) + 4 * seg + q;
-#pragma unroll
-      for (int t = 0; t < M; ++t) {
-        if constexpr (Q == 0) {
-          const float4* xv = (const float4*)(XF + (size_t)t * L + xo);
-          const int wi[4] = {w.x, w.y, w.z, w.w};
-          float h = 0.f;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const float4 xx = xv[cc];
-            const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) h = __fmaf_rn((float)(int8_t)(wi[cc] >> (8 * k)), xe[k], h);
-          }
-          const float blk = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
-          p[t] = __fma_rn((double)wsc, (double)blk, (double)p[t]);
-        } else {
-          const int4 hv = *(const int4*)(XQ + (size_t)t * L + xo);
-          int d = dot16(w, hv);
-          d += __shfl_xor_sync(FULL, d, 1);
-          int e = 0;
-          if constexpr (Q == 2) {
-            const int4 lv = *(const int4*)(XL + (size_t)t * L + xo);
-            e = dot16(w, lv);
-            e += __shfl_xor_sync(FULL, e, 1);
-          }
-          const float s = XS[(size_t)t * (L / 32) + bi];
-          p[t] = q8_step<Q>((float)p[t], wsc, s, d, e);
-        }
-      }
-    }
+    unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
+    compute_stage<Q, M>(p, g, n, st, ac, lane);
     // The slot is free again: refill it with this warp's stage n + D.  The
     // generic-proxy reads above must be ordered before the bulk copy's
     // async-proxy writes into the same bytes.
     __syncwarp();
     if (issued < T) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(issued);
+      issue_stage(g, warp, nwc, issued, st, full0 + 8 * slot, pol_w, lane);
       ++issued;
     }
-    if (c == nsl - 1) {
-      // quad done: (p0 + p2) + (p1 + p3) within each row's 8 lanes
-      const int rows = r1 - row0 < QR ? (int)(r1 - row0) : QR;
-#pragma unroll
-      for (int t = 0; t < M; ++t) {
-        P v = p[t];
-        v = v + __shfl_down_sync(FULL, v, 4);
-        v = v + __shfl_down_sync(FULL, v, 2);
-        p[t] = (P)0;
-        if (j == 0 && rr < rows) {
-          const long o = row0 + rr;
-          if (SPLIT) {
-            const long idx = ((long)blockIdx.y * M + t) * N + o;
-            if constexpr (Q == 0) a.part64[idx] = (double)v;
-            else a.y[idx] = (float)v;
-          } else {
-            const float yv = Q == 0 ? __double2float_rn((double)v) : (float)v;
-            a.y[(long)t * N + o] = yv;
-            const unsigned long long kk = amax_key(yv, (unsigned)o);
-            best[t] = kk > best[t] ? kk : best[t];
-          }
-        }
-      }
-    }
+    if ((int)(n % g.nsl) == g.nsl - 1) finish_quad<Q, M, SPLIT>(p, g, warp, nwc, n, a, blockIdx.y, a.y, best, lane);
   }
   // Drain: stages this warp issued but did not consume (only after an
   // abort) must land before the block may end.
   if (lane == 0) {
-    for (long m = n; m < issued; ++m) {
-      const unsigned bar = full0 + 8 * (unsigned)(warp * D + m % D);
-      const unsigned long long t0 = gtimer();
-      while (!mbar_try(bar, (unsigned)(m / D) & 1u)) {
-        if (gtimer() - t0 > ra.wait_ns) {
-          atomicOr(ra.err, ERR_DRAIN);
-          break;
-        }
-      }
-    }
-    if (!FUSE && L > 0 && warp == 0) {
-      const unsigned long long t0 = gtimer();
-      while (!mbar_try(act_bar, 0)) {
-        if (gtimer() - t0 > ra.wait_ns) {
-          atomicOr(ra.err, ERR_DRAIN);
-          break;
-        }
-      }
-    }
+    for (long m = n; m < issued; ++m)
+      drain_wait(full0 + 8 * (unsigned)(warp * D + m % D), (unsigned)(m / D) & 1u, ra.wait_ns, ra.err);
+    if (!FUSE && L > 0 && warp == 0) drain_wait(act_bar, 0, ra.wait_ns, ra.err);
   }
   __syncwarp();
   if (!SPLIT && a.amax) {

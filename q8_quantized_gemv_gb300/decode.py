@@ -24,7 +24,7 @@ from . import lk, synth
 class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
                  batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
-                 fused=True):
+                 fused=True, chain=True):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
         dev = self.dev
@@ -61,6 +61,11 @@ class DecodeStack:
         shapes = dict(self.shapes, lm=(vocab, hidden))
         self.fused = {n: bool(fused) and lk.lk_gemv_kernel_for(N, K, self.mode, B, 0) == 2
                       for n, (N, K) in shapes.items()}
+        # the whole token as one cooperative chain launch, where every step fits
+        self.x_buf = self.x0.clone()
+        self.chain = None
+        if chain and all(self.fused.values()):
+            self.chain = lk.Chain(self._chain_ops(), dev)
 
     def _act_bufs(self, K):
         B = self.B
@@ -90,10 +95,37 @@ class DecodeStack:
     def _gemv(self, w, y, acts, parts=None):
         return lk.lk_gemv_q8(w[0], w[1], self.mode, y, M=self.B, argmax_parts=parts, **acts)
 
+    def _chain_ops(self):
+        """The token's steps.  A step waits (grid barrier) where a decoder's
+        dataflow has a dependency: the attention output before o, o before
+        gate/up, the gated activation before down, down before the next
+        layer's q/k/v and the lm-head -- including where the synthetic o and
+        down inputs would not need it."""
+        ops = []
+        x = self.x_buf
+        for l, w in enumerate(self.layers):
+            for name in ("q", "k", "v"):
+                ops.append(lk.chain_op(w[name][0], w[name][1], x, self.out[name], gain=w["g_attn"],
+                                       wait=(name == "q" and l > 0)))
+            ops.append(lk.chain_op(w["o"][0], w["o"][1], w["o_in"], self.out["o"], wait=True))
+            ops.append(lk.chain_op(w["gu"][0], w["gu"][1], self.out["o"], self.out["gu"], gain=w["g_mlp"],
+                                   wait=True))
+            ops.append(lk.chain_op(w["down"][0], w["down"][1], w["d_in"], self.h, wait=True))
+            x = self.h
+        ops.append(lk.chain_op(self.lm[0], self.lm[1], x, self.logits, gain=self.g_final,
+                               argmax_parts=self.parts, argmax_idx=self.idx, wait=True))
+        return ops
+
     def run_token(self, x_in=None, hook=None):
         """Launch one token's sequence on the current stream and return the
         device int32 [B] argmax.  ``hook``, if given, is called as
         hook(name, launch) around each GEMV launch (for per-kernel timing)."""
+        if self.chain is not None and hook is None:
+            if x_in is not None and x_in.data_ptr() != self.x_buf.data_ptr():
+                self.x_buf.copy_(x_in)
+            lk.lk_gemv_chain(self.chain, self.mode, self.B, self.eps)
+            return self.idx
+
         def g(name, w, y, x, gain, parts=None):
             if self.fused[name]:
                 def launch():
@@ -131,6 +163,8 @@ class DecodeStack:
         return self.L * sum(mb(N, K) for N, K in self.shapes.values()) + mb(self.V, self.H)
 
     def launches_per_token(self):
+        if self.chain is not None:
+            return 1
         n = 1  # argmax reduce
         f = self.fused
         per_layer = 6 + (0 if f["q"] else 1) + (0 if f["k"] else 1) + (0 if f["v"] else 1) \

@@ -25,6 +25,14 @@ STATUS = {0: "LK_OK", -1: "LK_ERR_ARG", -2: "LK_ERR_ALIGN", -3: "LK_ERR_SHAPE",
           -4: "LK_ERR_WORKSPACE", -5: "LK_ERR_CUDA", -6: "LK_ERR_DEVICE_TIMEOUT"}
 
 
+class LkChainOp(ctypes.Structure):
+    """One step of lk_gemv_chain (the C struct lk_chain_op)."""
+    _fields_ = [("wq", ctypes.c_void_p), ("ws", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int),
+                ("x", ctypes.c_void_p), ("gain", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("argmax_parts", ctypes.c_void_p), ("argmax_idx", ctypes.c_void_p), ("wait", ctypes.c_int),
+                ("reserved", ctypes.c_int)]
+
+
 class LkError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -62,6 +70,8 @@ def _load():
         "lk_selftest_wait_timeout": ([ctypes.c_uint, P], I),
         "lk_gemv_kernel_for": ([I, I, I, I, I], I),
         "lk_rmsnorm_quant_gemv_q8": ([P, P, I, I, I, P, P, F, I, P, P, P, P], I),
+        "lk_chain_sync_bytes": ([], S),
+        "lk_gemv_chain": ([P, P, I, I, I, F, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -76,7 +86,7 @@ def exported_symbols():
             "lk_splitk_workspace_bytes", "lk_gemv_q8_splitk", "lk_splitk_combine",
             "lk_argmax_parts_max", "lk_argmax_scratch_entries", "lk_argmax", "lk_q8_block_dots",
             "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout", "lk_gemv_kernel_for",
-            "lk_rmsnorm_quant_gemv_q8"]
+            "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain"]
 
 
 def _ok(st, where):
@@ -234,3 +244,33 @@ def lk_device_error(reset: bool = True) -> int:
 
 def lk_selftest_wait_timeout(limit_us: int, stream=None):
     _ok(_load().lk_selftest_wait_timeout(int(limit_us), _stream(stream)), "lk_selftest_wait_timeout")
+
+
+def lk_chain_sync_bytes() -> int:
+    return _load().lk_chain_sync_bytes()
+
+
+def chain_op(wq, ws, x, y, gain=None, argmax_parts=None, argmax_idx=None, wait=False) -> LkChainOp:
+    """Marshal one lk_chain_op from device tensors (they must outlive the chain)."""
+    N, K = wq.shape
+    return LkChainOp(_ptr(wq, _I8, "wq"), _ptr(ws, _WS, "ws"), N, K, _ptr(x, _F32, "x"),
+                     _ptr(gain, _F32, "gain"), _ptr(y, _F32, "y"),
+                     _ptr(argmax_parts, torch.int64, "argmax_parts"), _ptr(argmax_idx, torch.int32, "argmax_idx"),
+                     1 if wait else 0, 0)
+
+
+class Chain:
+    """A host array of lk_chain_op, its device copy and a zeroed sync buffer."""
+
+    def __init__(self, ops, device):
+        self.n = len(ops)
+        self.host = (LkChainOp * self.n)(*ops)
+        raw = bytes(self.host)
+        self.dev = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(device)
+        self.sync = torch.zeros((lk_chain_sync_bytes() // 4,), dtype=torch.int32, device=device)
+
+
+def lk_gemv_chain(chain: "Chain", mode, M, eps=1e-6, stream=None):
+    _ok(_load().lk_gemv_chain(ctypes.cast(chain.host, ctypes.c_void_p), _ptr(chain.dev, None, "ops_dev"),
+                              chain.n, _mode(mode), M, eps, _ptr(chain.sync, None, "sync"), _stream(stream)),
+        "lk_gemv_chain")

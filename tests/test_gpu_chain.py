@@ -1,0 +1,118 @@
+"""The GEMV chain (a whole token's projections in one cooperative launch)
+against the per-launch path and the CPU oracle, on a small synthetic decoder
+(3 layers, hidden 1024) under every mode and batch 1 / 3; run-to-run
+identity; and the bounded grid barrier's failure path."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from gpuhelp import bits, host, oracle_acts  # noqa: E402
+from q8_quantized_gemv_gb300 import build, lk  # noqa: E402
+from q8_quantized_gemv_gb300.decode import DecodeStack  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+SMALL = dict(layers=3, hidden=1024, q_dim=1024, kv_dim=256, ffn=1536, vocab=3000)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    yield
+    lk.lk_set_option("wait_us", 0)
+
+
+def oracle_token(st):
+    """The same token through the oracle (host copies of the stack)."""
+    m = st.mode
+    h = lambda t: host(t)  # noqa: E731
+    ws16 = lambda t: host(t).view(np.uint16)  # noqa: E731
+
+    def step(wpair, x, gain):
+        a = oracle.rmsnorm(x, h(gain), m) if gain is not None else x
+        return oracle.gemv(h(wpair[0]), ws16(wpair[1]), m, **oracle_acts(a, m))
+
+    x = h(st.x0)
+    outs = {}
+    for w in st.layers:
+        for n in ("q", "k", "v"):
+            outs[n] = step(w[n], x, w["g_attn"])
+        outs["o"] = step(w["o"], h(w["o_in"]), None)
+        outs["gu"] = step(w["gu"], outs["o"], w["g_mlp"])
+        x = step(w["down"], h(w["d_in"]), None)
+    logits = step(st.lm, x, st.g_final)
+    return outs, x, logits
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("batch", [1, 3])
+def test_chain_matches_launches_and_oracle(mode, batch):
+    a = DecodeStack(**SMALL, batch=batch, mode=mode, chain=True)
+    b = DecodeStack(**SMALL, batch=batch, mode=mode, chain=False)
+    assert a.chain is not None and b.chain is None
+    ia = a.run_token().clone()
+    ib = b.run_token().clone()
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) == 0
+    # the chain is the same arithmetic as the per-launch fused path: same bits
+    for name in ("q", "k", "v", "o", "gu"):
+        assert torch.equal(a.out[name].view(torch.int32), b.out[name].view(torch.int32)), name
+    assert torch.equal(a.h.view(torch.int32), b.h.view(torch.int32))
+    assert torch.equal(a.logits.view(torch.int32), b.logits.view(torch.int32))
+    assert torch.equal(ia, ib)
+    # and the oracle's token
+    outs, hx, logits = oracle_token(a)
+    if mode == 0:
+        assert np.allclose(host(a.logits), logits, rtol=1e-4, atol=1e-3)
+    else:
+        assert np.array_equal(bits(host(a.logits)), bits(logits))
+        assert np.array_equal(bits(host(a.h)), bits(hx))
+    assert host(ia).tolist() == [oracle.argmax(logits[t]) for t in range(batch)]
+    # run to run
+    for _ in range(2):
+        a.run_token()
+        torch.cuda.synchronize()
+        assert torch.equal(a.logits.view(torch.int32), b.logits.view(torch.int32))
+
+
+def test_chain_in_cuda_graph():
+    a = DecodeStack(**SMALL, batch=1, mode=1, chain=True)
+    a.run_token()
+    torch.cuda.synchronize()
+    ref = a.logits.clone()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        a.run_token()
+    for _ in range(3):
+        a.logits.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(a.logits.view(torch.int32), ref.view(torch.int32))
+
+
+def test_chain_barrier_timeout_is_reported_and_recoverable():
+    a = DecodeStack(**SMALL, batch=1, mode=1, chain=True)
+    a.run_token()
+    torch.cuda.synchronize()
+    ref = a.logits.clone()
+    lk.lk_device_error(reset=True)
+    # a sync counter that can never reach "last arrival": every barrier wait
+    # runs out (2 ms), the blocks drain their copies and exit
+    lk.lk_set_option("wait_us", 2000)
+    a.chain.sync.fill_(0x40000000)
+    a.run_token()
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) != 0
+    # zeroed again, the chain runs normally in the same context
+    a.chain.sync.zero_()
+    lk.lk_set_option("wait_us", 0)
+    a.logits.zero_()
+    a.run_token()
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) == 0
+    assert torch.equal(a.logits.view(torch.int32), ref.view(torch.int32))
