@@ -271,6 +271,8 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *   "ring_cps"    ring blocks per SM in the grid, 1..4 (default 1)
  *   "pdl"         1: lk_rmsnorm_quant_gemv_q8 launches as a programmatic
  *                 dependent launch (default 0)
+ *   "trace"       1: the ring and chain kernels write block 0's timestamps
+ *                 to the trace buffer (lk_trace_read)
  *   "wait_us"     time limit of every device-side wait, microseconds
  *                 (0 = default, 2 s)
  * Unknown names or out-of-range values return LK_ERR_ARG.
@@ -285,6 +287,17 @@ long lk_get_option(const char* name);
  * reset != 0 clears the word.
  */
 lk_status lk_device_error(int reset, int* code);
+
+/*
+ * Tracing (cf. the per-phase clock stamps of model-as-a-kernel
+ * "megakernel.cu"): with option "trace" set, block 0 of the last ring or
+ * chain launch records %globaltimer nanoseconds.  Ring kernel: [0] start,
+ * [1] after the dependency wait, [2] activation ready, [3 + w] warp w done.
+ * Chain: [0] start, then per step i: [1 + 3i] step start (after its barrier),
+ * [2 + 3i] activation ready, [3 + 3i] block 0's rows done.  Synchronizes the
+ * device and copies the first n (<= 4096) entries to host_out.
+ */
+lk_status lk_trace_read(uint64_t* host_out, int n);
 
 /*
  * Test hook of the failure path: launches one block that waits, with the

@@ -31,7 +31,12 @@ struct ChainArgs {
   unsigned long long wait_ns;
   unsigned long long pol_w;
   int* err;
+  unsigned long long* trace;  // block 0's timestamps (option "trace"), or NULL
 };
+
+__device__ __forceinline__ void stamp(unsigned long long* trace, int i) {
+  if (trace && blockIdx.x == 0 && threadIdx.x == 0 && i < LK_TRACE_MAX) trace[i] = gtimer();
+}
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
@@ -115,6 +120,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     ++in;
     ++issued;
   };
+  stamp(ca.trace, 0);
   for (int d = 0; d < D && iop < ca.n_ops; ++d) issue_next();
 
   long consumed = 0;
@@ -127,12 +133,14 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     }
     // the activation area is rewritten below: every warp is done with the last step
     __syncthreads();
+    stamp(ca.trace, 1 + 3 * op);
     lkh::GemvProblem pr;
     pr.K = o.K;
     pr.xraw = o.x;
     pr.gain = o.gain;
     pr.eps = ca.eps;
     fused_prologue<Q, M>(pr, nwc, 0, (unsigned)o.K, act, nred, nden);
+    stamp(ca.trace, 2 + 3 * op);
     const Geom g = op_geom(o);
     const long T = geom_stages(g, warp, nwc);
     const Act ac{act, (unsigned)o.K};
@@ -164,6 +172,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
       }
     }
     ok = __syncthreads_and(ok) != 0;  // every warp agrees before the next barrier
+    stamp(ca.trace, 3 + 3 * op);
     if (!ok) break;
     if (o.argmax_parts) {
 #pragma unroll
@@ -288,6 +297,7 @@ extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* op
   ca.pol_w = lkh::opt_ring_hint ? 1ull : 0ull;
   ca.err = lkh::error_word_ptr();
   if (!ca.err) return LK_ERR_CUDA;
+  ca.trace = lkh::opt_trace ? lkh::trace_ptr() : nullptr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->sm_count);
   cfg.blockDim = dim3(w * 32);

@@ -31,6 +31,8 @@
 #include "lk_ring_kernel.cuh"
 
 __device__ int lk_error_word;
+// Block 0's timestamps (%globaltimer, ns) of the last traced launch.
+__device__ unsigned long long lk_trace_buf[lkring::LK_TRACE_MAX];
 
 namespace lkring {
 // A wait on an mbarrier that nothing completes: the bounded wait must give
@@ -70,6 +72,18 @@ int* lkh::error_word_ptr() {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, lk_error_word) != cudaSuccess) return nullptr;
     ptr[dev] = (int*)p;
+  }
+  return ptr[dev];
+}
+
+unsigned long long* lkh::trace_ptr() {
+  static unsigned long long* ptr[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, lk_trace_buf) != cudaSuccess) return nullptr;
+    ptr[dev] = (unsigned long long*)p;
   }
   return ptr[dev];
 }
@@ -176,6 +190,7 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   ra.pdl = opt_pdl ? 1 : 0;
   ra.err = lkh::error_word_ptr();
   if (!ra.err) return LK_ERR_CUDA;
+  ra.trace = opt_trace ? lkh::trace_ptr() : nullptr;
   const int S = p.split && p.S > 1 ? p.S : 1;
   const int g = opt_grid_ctas > 0 ? (int)opt_grid_ctas : d->sm_count * (opt_ring_cps > 1 ? (int)opt_ring_cps : 1);
   int gx = (g + S - 1) / S;
@@ -216,4 +231,12 @@ extern "C" lk_status lk_selftest_wait_timeout(unsigned limit_us, cudaStream_t st
   if (!err) return LK_ERR_CUDA;
   lkring::wait_selftest_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_us * 1000ull, err);
   return lkh::launch_status();
+}
+
+extern "C" lk_status lk_trace_read(uint64_t* host_out, int n) {
+  if (!host_out || n < 0 || n > lkring::LK_TRACE_MAX) return LK_ERR_ARG;
+  if (n == 0) return LK_OK;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LK_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(host_out, lk_trace_buf, (size_t)n * 8) != cudaSuccess) return LK_ERR_CUDA;
+  return LK_OK;
 }

@@ -21,6 +21,8 @@ constexpr int MAX_STAGES = 32;
 constexpr unsigned TAIL =
     8 * (MAX_STAGES + 1) + 16 + 8 * LK_MAX_M * MAXW + 8 * LK_MAX_M * 32 + 8 * LK_MAX_M;
 
+constexpr int LK_TRACE_MAX = 4096;  // timestamps kept by the "trace" option
+
 enum : int { ERR_WAIT_FULL = 1, ERR_WAIT_EMPTY = 2, ERR_DRAIN = 4, ERR_SELFTEST = 8, ERR_WAIT_ACT = 16 };
 
 struct RingArgs {
@@ -38,6 +40,7 @@ struct RingArgs {
   unsigned long long pol_w;  // nonzero: L2 evict-first hint on the weight copies
   int pdl;                 // launched as a programmatic dependent of the previous kernel
   int* err;                // the device error word
+  unsigned long long* trace;  // block 0's timestamps (option "trace"), or NULL
 };
 
 typedef void (*ring_fn)(const RingArgs);
@@ -513,12 +516,14 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   if (ra.pdl && threadIdx.x == 0) griddep_launch();
 
   // Weights do not depend on the previous kernel: start streaming at once.
+  if (ra.trace && blockIdx.x == 0 && threadIdx.x == 0) ra.trace[0] = gtimer();
   long issued = 0;
   for (; issued < T && issued < D; ++issued)
     issue_stage(g, warp, nwc, issued, ring + (size_t)(warp * D + issued % D) * ra.stage_bytes,
                 full0 + 8 * (warp * D + (int)(issued % D)), pol_w, lane);
 
   if (ra.pdl) griddep_wait();  // from here on: reads of activations, writes of outputs
+  if (ra.trace && blockIdx.x == 0 && threadIdx.x == 0) ra.trace[1] = gtimer();
   bool ok = true;
   if (FUSE) {
     fused_prologue<Q, M>(a, nwc, k_lo, L, act, nred, nden);
@@ -546,6 +551,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   }
 
   const Act ac{act, L};
+  if (ra.trace && blockIdx.x == 0 && threadIdx.x == 0) ra.trace[2] = gtimer();
   unsigned long long best[M];
   P p[M];
 #pragma unroll
@@ -574,6 +580,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
     }
     if ((int)(n % g.nsl) == g.nsl - 1) finish_quad<Q, M, SPLIT>(p, g, warp, nwc, n, a, blockIdx.y, a.y, best, lane);
   }
+  if (ra.trace && blockIdx.x == 0 && lane == 0) ra.trace[3 + warp] = gtimer();
   // Drain: stages this warp issued but did not consume (only after an
   // abort) must land before the block may end.
   if (lane == 0) {

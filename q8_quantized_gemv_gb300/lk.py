@@ -71,6 +71,7 @@ def _load():
         "lk_gemv_kernel_for": ([I, I, I, I, I], I),
         "lk_rmsnorm_quant_gemv_q8": ([P, P, I, I, I, P, P, F, I, P, P, P, P], I),
         "lk_chain_sync_bytes": ([], S),
+        "lk_trace_read": ([P, I], I),
         "lk_gemv_chain": ([P, P, I, I, I, F, P, P], I),
     }
     for name, (args, res) in sig.items():
@@ -86,7 +87,7 @@ def exported_symbols():
             "lk_splitk_workspace_bytes", "lk_gemv_q8_splitk", "lk_splitk_combine",
             "lk_argmax_parts_max", "lk_argmax_scratch_entries", "lk_argmax", "lk_q8_block_dots",
             "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout", "lk_gemv_kernel_for",
-            "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain"]
+            "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain", "lk_trace_read"]
 
 
 def _ok(st, where):
@@ -274,3 +275,10 @@ def lk_gemv_chain(chain: "Chain", mode, M, eps=1e-6, stream=None):
     _ok(_load().lk_gemv_chain(ctypes.cast(chain.host, ctypes.c_void_p), _ptr(chain.dev, None, "ops_dev"),
                               chain.n, _mode(mode), M, eps, _ptr(chain.sync, None, "sync"), _stream(stream)),
         "lk_gemv_chain")
+
+
+def lk_trace_read(n: int):
+    """Block 0's timestamps of the last traced launch (ns), as a list."""
+    buf = (ctypes.c_uint64 * n)()
+    _ok(_load().lk_trace_read(ctypes.cast(buf, ctypes.c_void_p), n), "lk_trace_read")
+    return list(buf)
