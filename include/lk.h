@@ -266,7 +266,7 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *   "grid_ctas"   blocks of the ring kernel (0 = one per SM)
  *   "ring_hint"   1 (default): L2 evict-first hint on the ring's weight
  *                 copies; 0: no hint
- *   "ring_warps"  warps per block of the ring kernel: 0 auto, else 1..16
+ *   "ring_warps"  warps per block of the ring kernel: 0 auto, else 1..12
  *   "ring_kb"     cap on the ring kernel's shared memory per block, KB (0 none)
  *   "ring_cps"    ring blocks per SM in the grid, 1..4 (default 1)
  *   "pdl"         1: lk_rmsnorm_quant_gemv_q8 launches as a programmatic

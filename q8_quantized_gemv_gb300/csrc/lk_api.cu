@@ -133,7 +133,7 @@ lk_status lk_set_option(const char* name, long value) {
     if (value < 0 || value > (1L << 20)) return LK_ERR_ARG;
     opt_grid_ctas = value;
   } else if (!strcmp(name, "ring_warps")) {
-    if (value < 0 || value > 16) return LK_ERR_ARG;
+    if (value < 0 || value > 12) return LK_ERR_ARG;
     opt_ring_warps = value;
   } else if (!strcmp(name, "ring_kb")) {
     if (value < 0 || value > 1024) return LK_ERR_ARG;

@@ -11,7 +11,7 @@ namespace lkring {
 
 using namespace lk;
 
-constexpr int MAXW = 16;               // warps per block at most
+constexpr int MAXW = 12;               // warps per block at most (168 registers a thread)
 constexpr int THREADS_MAX = MAXW * 32;
 constexpr int QR = 4;                  // rows per stage (one warp's quad)
 constexpr int TKMAX = 8192;            // bytes of K per stage
@@ -152,8 +152,30 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // of values 32v + l + vt*u in ascending u.  The same warp then normalizes and
 // quantizes exactly the 32-groups v + (vt/32)*u it loaded, so each row is
 // read from global memory once, all of a warp's loads in flight together.
-constexpr int PRO_VW = 4;  // virtual warps per real warp on the fast path
-constexpr int PRO_KU = 8;  // values per virtual thread on the fast path (K <= 8192)
+constexpr int PRO_SLOTS = 16;  // values per lane per row held in registers by the prologue
+
+// A read-only f32 load that the compiler keeps where it is written: the
+// prologue issues all of a lane's loads before using any, so a row costs one
+// round trip to L2 instead of one per 32-group.
+__device__ __forceinline__ float ld_keep(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void compiler_fence() { asm volatile("" ::: "memory"); }
+
+template <int Q, int M>
+__device__ __forceinline__ void store_act(unsigned char* act, unsigned L, int t, int g, int lane, float v) {
+  const int i = 32 * g + lane;
+  if constexpr (Q == 0) {
+    ((float*)act)[(size_t)t * L + i] = v;
+  } else {
+    int8_t* XQ = (int8_t*)act + (size_t)t * L;
+    int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
+    float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
+    quant_lane<Q>(v, XQ, XL, XS, i, g, lane);
+  }
+}
 
 template <int Q, int M>
 __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, unsigned L, unsigned char* act,
@@ -166,80 +188,70 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
   const bool norm = a.gain != nullptr;
   const int vt = K < 1024 ? K : 1024, nvw_all = vt >> 5, KU = K / vt;
   const int nvw = cw < nvw_all ? (nvw_all - 1 - cw) / nwc + 1 : 0;
-  const bool fast = k_lo == 0 && (int)L == K && KU <= PRO_KU && (nvw_all + nwc - 1) / nwc <= PRO_VW &&
-                    K % vt == 0;
-  if (fast) {
-    float gv[PRO_VW][PRO_KU];
-    if (norm) {
+  const int ns = nvw * KU;  // this lane's values per row: slot s -> virtual warp cw + nwc*(s / KU), step s % KU
+  if (norm && k_lo == 0 && (int)L == K && K % vt == 0 && ((nvw_all + nwc - 1) / nwc) * KU <= PRO_SLOTS) {
+    // RMSNorm: the canonical tree from registers, then normalize + quantize
+    // the very groups this warp loaded
+    float gv[PRO_SLOTS];
 #pragma unroll
-      for (int iv = 0; iv < PRO_VW; ++iv)
-#pragma unroll
-        for (int u = 0; u < PRO_KU; ++u)
-          if (iv < nvw && u < KU) gv[iv][u] = __ldg(a.gain + 32 * (cw + nwc * iv) + lane + vt * u);
-    }
+    for (int s = 0; s < PRO_SLOTS; ++s)
+      if (s < ns) gv[s] = ld_keep(a.gain + 32 * (cw + nwc * (s / KU)) + lane + vt * (s % KU));
     for (int t = 0; t < M; ++t) {
       const float* xr = a.xraw + (long)t * K;
-      float xv[PRO_VW][PRO_KU];
+      float xv[PRO_SLOTS];
 #pragma unroll
-      for (int iv = 0; iv < PRO_VW; ++iv)
+      for (int s = 0; s < PRO_SLOTS; ++s)
+        if (s < ns) xv[s] = ld_keep(xr + 32 * (cw + nwc * (s / KU)) + lane + vt * (s % KU));
+      compiler_fence();
+      A acc = 0;
 #pragma unroll
-        for (int u = 0; u < PRO_KU; ++u)
-          if (iv < nvw && u < KU) xv[iv][u] = __ldg(xr + 32 * (cw + nwc * iv) + lane + vt * u);
-      A dn = (A)1;
-      if (norm) {
-#pragma unroll
-        for (int iv = 0; iv < PRO_VW; ++iv) {
-          if (iv < nvw) {
-            A acc = 0;
-#pragma unroll
-            for (int u = 0; u < PRO_KU; ++u)
-              if (u < KU) acc = fma_acc((A)xv[iv][u], acc);
-            acc = warp_tree_sum(acc);
-            if (lane == 0) red[t * 32 + cw + nwc * iv] = acc;
+      for (int s = 0; s < PRO_SLOTS; ++s) {
+        if (s < ns) {
+          acc = fma_acc((A)xv[s], acc);
+          if (s % KU == KU - 1) {  // a virtual thread's values end: its warp's tree
+            const A tot = warp_tree_sum(acc);
+            if (lane == 0) red[t * 32 + cw + nwc * (s / KU)] = tot;
+            acc = 0;
           }
         }
-        __syncthreads();
-        if (cw == 0) {
-          A v = lane < nvw_all ? red[t * 32 + lane] : (A)0;
-          v = warp_tree_sum(v);
-          if (lane == 0) den[t] = norm_div_add(v, K, a.eps);
-        }
-        __syncthreads();
-        dn = den[t];
       }
+      __syncthreads();
+      if (cw == 0) {
+        A v = lane < nvw_all ? red[t * 32 + lane] : (A)0;
+        v = warp_tree_sum(v);
+        if (lane == 0) den[t] = norm_div_add(v, K, a.eps);
+      }
+      __syncthreads();
+      const A dn = den[t];
 #pragma unroll
-      for (int iv = 0; iv < PRO_VW; ++iv)
-#pragma unroll
-        for (int u = 0; u < PRO_KU; ++u)
-          if (iv < nvw && u < KU) {
-            const int g = cw + nwc * iv + nvw_all * u;  // the 32-group holding these values
-            const int i = 32 * g + lane;
-            float v = xv[iv][u];
-            if (norm) v = norm_scale(v, dn, gv[iv][u]);
-            if constexpr (Q == 0) {
-              ((float*)act)[(size_t)t * L + i] = v;
-            } else {
-              int8_t* XQ = (int8_t*)act + (size_t)t * L;
-              int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
-              float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
-              quant_lane<Q>(v, XQ, XL, XS, i, g, lane);
-            }
-          }
+      for (int s = 0; s < PRO_SLOTS; ++s)
+        if (s < ns) {
+          const int g = cw + nwc * (s / KU) + nvw_all * (s % KU);  // the 32-group holding this value
+          store_act<Q, M>(act, L, t, g, lane, norm_scale(xv[s], dn, gv[s]));
+        }
     }
     __syncthreads();
     return;
   }
-  // general path: any K, chunk or warp count.  The sum of squares walks each
-  // virtual thread's values in order (loads unrolled ahead of the chain);
-  // then every warp normalizes and quantizes its groups g = cw + nwc*i, eight
-  // groups' loads in flight at a time.
+  // general path (any K, chunk, warp count; quantizer alone): the sum of
+  // squares walks each virtual thread's values in order, then every warp
+  // normalizes and quantizes its groups g = cw + nwc*i, PRO_SLOTS groups'
+  // loads issued before any is used
   if (norm) {
     for (int t = 0; t < M; ++t) {
       const float* xr = a.xraw + (long)t * K;
       for (int w = cw; w < nvw_all; w += nwc) {
+        float xv[PRO_SLOTS];
         A acc = 0;
-#pragma unroll 8
-        for (int i = 32 * w + lane; i < K; i += vt) acc = fma_acc((A)__ldg(xr + i), acc);
+        for (int i0 = 32 * w + lane; i0 < K; i0 += PRO_SLOTS * vt) {
+#pragma unroll
+          for (int s = 0; s < PRO_SLOTS; ++s)
+            if (i0 + s * vt < K) xv[s] = ld_keep(xr + i0 + s * vt);
+          compiler_fence();
+#pragma unroll
+          for (int s = 0; s < PRO_SLOTS; ++s)
+            if (i0 + s * vt < K) acc = fma_acc((A)xv[s], acc);
+        }
         acc = warp_tree_sum(acc);
         if (lane == 0) red[t * 32 + w] = acc;
       }
@@ -254,35 +266,28 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
     }
     __syncthreads();
   }
-  constexpr int GB = 8;
   const int ng = (int)(L >> 5);
   for (int t = 0; t < M; ++t) {
     const float* xr = a.xraw + (long)t * K + k_lo;
     const A dn = norm ? den[t] : (A)1;
-    for (int g0 = cw; g0 < ng; g0 += GB * nwc) {
-      float xv[GB], gv[GB];
+    for (int g0 = cw; g0 < ng; g0 += PRO_SLOTS * nwc) {
+      float xv[PRO_SLOTS], gv[PRO_SLOTS];
 #pragma unroll
-      for (int b = 0; b < GB; ++b) {
+      for (int b = 0; b < PRO_SLOTS; ++b) {
         const int g = g0 + b * nwc, i = 32 * g + lane;
         const bool in = g < ng && k_lo + i < K;
-        xv[b] = in ? __ldg(xr + i) : 0.f;
-        gv[b] = (norm && in) ? __ldg(a.gain + k_lo + i) : 1.f;
+        xv[b] = in ? ld_keep(xr + i) : 0.f;
+        gv[b] = (norm && in) ? ld_keep(a.gain + k_lo + i) : 1.f;
       }
+      compiler_fence();
 #pragma unroll
-      for (int b = 0; b < GB; ++b) {
-        const int g = g0 + b * nwc, i = 32 * g + lane;
+      for (int b = 0; b < PRO_SLOTS; ++b) {
+        const int g = g0 + b * nwc;
         if (g >= ng) break;  // warp-uniform
         float v = xv[b];
         // past the row's end (a chunk narrower than the area) the area keeps zeros
-        if (norm && k_lo + i < K) v = norm_scale(v, dn, gv[b]);
-        if constexpr (Q == 0) {
-          ((float*)act)[(size_t)t * L + i] = v;
-        } else {
-          int8_t* XQ = (int8_t*)act + (size_t)t * L;
-          int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
-          float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
-          quant_lane<Q>(v, XQ, XL, XS, i, g, lane);
-        }
+        if (norm && k_lo + 32 * g + lane < K) v = norm_scale(v, dn, gv[b]);
+        store_act<Q, M>(act, L, t, g, lane, v);
       }
     }
   }
