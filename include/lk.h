@@ -249,6 +249,27 @@ lk_status lk_argmax(const float* logits, const uint64_t* parts, int n_parts, int
                     int32_t* idx, uint64_t* scratch, cudaStream_t stream);
 
 /*
+ * lk_argmax's logits form without any caller-provided scratch, for callers
+ * that cannot allocate device memory where they call it: code being captured
+ * into a CUDA graph (cudaMalloc is not allowed during stream capture), the
+ * enqueue path of an inference-engine plugin that must not allocate, or a
+ * real-time loop that forbids allocator calls.  The source pages have no
+ * counterpart of this entry point; it computes what lk_argmax(logits, NULL,
+ * ...) computes.
+ *   logits f32 [M][N], idx int32 [M]; 1 <= M <= LK_MAX_M, N >= 1.
+ * The partial keys go to a file-scope device array of LK_MAX_M * 64 keys
+ * (4 KB) that every GPU which loads the library keeps until the process
+ * exits; shapes that would need more return LK_ERR_WORKSPACE (none do within
+ * M <= LK_MAX_M).  The first call on each device looks the array's address up
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  The call allocates and frees nothing.  All
+ * calls share the array: calls that can overlap on the GPU (other streams,
+ * other threads) race and must be serialized by the caller; the array keeps
+ * the last call's keys, which every call overwrites before reading.
+ */
+lk_status lk_argmax_noalloc(const float* logits, int M, int N, int32_t* idx, cudaStream_t stream);
+
+/*
  * Test hook: the exact int32 block dots of one activation row, computed by the
  * same lane arrangement the GEMV uses ("kernels.rs" lk_q8_block_dot).
  *   d[o][b] = sum_k wq[o][32b+k] * xq[32b+k];  e likewise with xl (if both xl

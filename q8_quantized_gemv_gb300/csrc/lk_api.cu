@@ -348,3 +348,42 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free argmax of logits.  The per-block partial keys live in a
+// file-scope device array instead of a caller buffer: LK_MAX_M rows x 64
+// blocks (the most lk_argmax_scratch_entries ever returns) = 512 keys, 4 KB.
+// Every GPU that loads the library holds it until the process exits.
+static __device__ __align__(256) unsigned long long lk_noalloc_argmax_scratch[LK_MAX_M * 64];
+
+// The array's device address on the current device, looked up the first
+// time the entry point runs on that device (cudaGetSymbolAddress with the
+// device current) and cached.
+static unsigned long long* noalloc_scratch_ptr() {
+  static unsigned long long* ptr[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, lk_noalloc_argmax_scratch) != cudaSuccess) return nullptr;
+    ptr[dev] = (unsigned long long*)p;
+  }
+  return ptr[dev];
+}
+
+extern "C" lk_status lk_argmax_noalloc(const float* logits, int M, int N, int32_t* idx, cudaStream_t stream) {
+  if (M < 0 || M > LK_MAX_M) return LK_ERR_SHAPE;
+  if (M == 0) return LK_OK;
+  if (N < 1) return LK_ERR_SHAPE;
+  if (!logits || !idx) return LK_ERR_ARG;
+  if (!aligned(logits, 4) || !aligned(idx, 4)) return LK_ERR_ALIGN;
+  const int nblk = lk_argmax_scratch_entries(N);
+  if ((long)M * nblk > LK_MAX_M * 64) return LK_ERR_WORKSPACE;
+  unsigned long long* scratch = noalloc_scratch_ptr();
+  if (!scratch) return LK_ERR_CUDA;
+  argmax_logits_kernel<<<dim3(nblk, M), 256, 0, stream>>>(logits, N, scratch);
+  lk_status st = launch_status();
+  if (st) return st;
+  argmax_reduce_kernel<<<M, 256, 0, stream>>>(scratch, nblk, idx);
+  return launch_status();
+}

@@ -72,6 +72,7 @@ def _load():
         "lk_rmsnorm_quant_gemv_q8": ([P, P, I, I, I, P, P, F, I, P, P, P, P], I),
         "lk_chain_sync_bytes": ([], S),
         "lk_trace_read": ([P, I], I),
+        "lk_argmax_noalloc": ([P, I, I, P, P], I),
         "lk_gemv_chain": ([P, P, I, I, I, F, P, P], I),
     }
     for name, (args, res) in sig.items():
@@ -87,7 +88,8 @@ def exported_symbols():
             "lk_splitk_workspace_bytes", "lk_gemv_q8_splitk", "lk_splitk_combine",
             "lk_argmax_parts_max", "lk_argmax_scratch_entries", "lk_argmax", "lk_q8_block_dots",
             "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout", "lk_gemv_kernel_for",
-            "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain", "lk_trace_read"]
+            "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain", "lk_trace_read",
+            "lk_argmax_noalloc"]
 
 
 def _ok(st, where):
@@ -282,3 +284,10 @@ def lk_trace_read(n: int):
     buf = (ctypes.c_uint64 * n)()
     _ok(_load().lk_trace_read(ctypes.cast(buf, ctypes.c_void_p), n), "lk_trace_read")
     return list(buf)
+
+
+def lk_argmax_noalloc(logits, idx, stream=None):
+    """Argmax of logits [M, N] into idx [M] with no caller scratch (see lk.h)."""
+    M, N = logits.shape
+    _ok(_load().lk_argmax_noalloc(_ptr(logits, _F32, "logits"), M, N, _ptr(idx, torch.int32, "idx"),
+                                  _stream(stream)), "lk_argmax_noalloc")
