@@ -134,12 +134,18 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     // the activation area is rewritten below: every warp is done with the last step
     __syncthreads();
     stamp(ca.trace, 1 + 3 * op);
-    lkh::GemvProblem pr;
-    pr.K = o.K;
-    pr.xraw = o.x;
-    pr.gain = o.gain;
-    pr.eps = ca.eps;
-    fused_prologue<Q, M>(pr, nwc, 0, (unsigned)o.K, act, nred, nden);
+    // a step that reads the same rows with the same gain as the one before it
+    // (q, k and v of a layer) reuses the activation area as it is
+    const bool same = op > 0 && !o.wait && o.x == ca.ops[op - 1].x && o.gain == ca.ops[op - 1].gain &&
+                      o.K == ca.ops[op - 1].K;
+    if (!same) {
+      lkh::GemvProblem pr;
+      pr.K = o.K;
+      pr.xraw = o.x;
+      pr.gain = o.gain;
+      pr.eps = ca.eps;
+      fused_prologue<Q, M>(pr, nwc, 0, (unsigned)o.K, act, nred, nden);
+    }
     stamp(ca.trace, 2 + 3 * op);
     const Geom g = op_geom(o);
     const long T = geom_stages(g, warp, nwc);

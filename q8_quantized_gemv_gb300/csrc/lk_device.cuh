@@ -39,10 +39,17 @@ __device__ __forceinline__ A warp_tree_sum(A v) {
 // ---- the activation quantizer ("kernels.rs" lk_quant_lane / lk_two_words) ------
 // The calling warp holds one 32-value group, value v in this lane.  Writes
 // the lane's word(s) at index i and (lane 0) the group's scale at g.
+// max|v| over the warp in one instruction: for non-negative floats the IEEE
+// order is the order of their bit patterns, so the integer max of the bits
+// of |v| is the bits of max|v| (exact; NaN inputs are unspecified).
+__device__ __forceinline__ float warp_absmax(float v) {
+  return __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(fabsf(v))));
+}
+
 template <int Q>
 __device__ __forceinline__ void quant_lane(float v, int8_t* __restrict__ hi, int8_t* __restrict__ lo,
                                            float* __restrict__ xs, long i, long g, int lane) {
-  const float a = warp_max_xor(fabsf(v));
+  const float a = warp_absmax(v);
   float s;
   if (Q == 1) {
     s = a > 0.f ? __fdiv_rn(a, 127.0f) : 1.0f;

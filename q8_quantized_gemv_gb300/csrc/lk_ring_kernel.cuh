@@ -181,38 +181,62 @@ template <int Q, int M>
 __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, unsigned L, unsigned char* act,
                                void* red_raw, void* den_raw) {
   typedef typename acc_of<Q>::t A;
+  constexpr int QB = PRO_SLOTS;  // groups a warp quantizes per batch
+  constexpr int KU_MAX = 8;      // values per virtual thread kept in registers (K <= 8192)
   A* red = (A*)red_raw;
   A* den = (A*)den_raw;
   const int lane = threadIdx.x & 31, cw = threadIdx.x >> 5;
   const int K = a.K;
   const bool norm = a.gain != nullptr;
-  const int vt = K < 1024 ? K : 1024, nvw_all = vt >> 5, KU = K / vt;
-  const int nvw = cw < nvw_all ? (nvw_all - 1 - cw) / nwc + 1 : 0;
-  const int ns = nvw * KU;  // this lane's values per row: slot s -> virtual warp cw + nwc*(s / KU), step s % KU
-  if (norm && k_lo == 0 && (int)L == K && K % vt == 0 && ((nvw_all + nwc - 1) / nwc) * KU <= PRO_SLOTS) {
-    // RMSNorm: the canonical tree from registers, then normalize + quantize
-    // the very groups this warp loaded
-    float gv[PRO_SLOTS];
+  const int vt = K < 1024 ? K : 1024, nvw_all = vt >> 5;
+  const int KU = (K + vt - 1) / vt;
+  const int ng = (int)(L >> 5);
+  for (int t = 0; t < M; ++t) {
+    const float* xr = a.xraw + (long)t * K;
+    // (1) the first batch of this warp's groups g = cw + nwc*b: its values and
+    // gains are requested before anything else, so their round trip overlaps
+    // the sum of squares below
+    float qx[QB], qg[QB];
+    auto load_batch = [&](int g0) {
 #pragma unroll
-    for (int s = 0; s < PRO_SLOTS; ++s)
-      if (s < ns) gv[s] = ld_keep(a.gain + 32 * (cw + nwc * (s / KU)) + lane + vt * (s % KU));
-    for (int t = 0; t < M; ++t) {
-      const float* xr = a.xraw + (long)t * K;
-      float xv[PRO_SLOTS];
+      for (int b = 0; b < QB; ++b) {
+        const int g = g0 + b * nwc, i = 32 * g + lane;
+        const bool in = g < ng && k_lo + i < K;
+        qx[b] = in ? ld_keep(xr + k_lo + i) : 0.f;
+        qg[b] = (norm && in) ? ld_keep(a.gain + k_lo + i) : 1.f;
+      }
+    };
+    load_batch(cw);
+    // (2) the norm's sum of squares: virtual warp w (played by warp w mod
+    // nwc), lane l adds the squares of values 32w + l + vt*u in ascending u;
+    // the next virtual warp's values are requested before this one's sum
+    if (norm) {
+      if (KU <= KU_MAX && K % vt == 0) {
+        float cur[KU_MAX], nxt[KU_MAX];
 #pragma unroll
-      for (int s = 0; s < PRO_SLOTS; ++s)
-        if (s < ns) xv[s] = ld_keep(xr + 32 * (cw + nwc * (s / KU)) + lane + vt * (s % KU));
-      compiler_fence();
-      A acc = 0;
+        for (int u = 0; u < KU_MAX; ++u)
+          if (u < KU && cw < nvw_all) cur[u] = ld_keep(xr + 32 * cw + lane + vt * u);
+        for (int w = cw; w < nvw_all; w += nwc) {
+          const int wn = w + nwc;
 #pragma unroll
-      for (int s = 0; s < PRO_SLOTS; ++s) {
-        if (s < ns) {
-          acc = fma_acc((A)xv[s], acc);
-          if (s % KU == KU - 1) {  // a virtual thread's values end: its warp's tree
-            const A tot = warp_tree_sum(acc);
-            if (lane == 0) red[t * 32 + cw + nwc * (s / KU)] = tot;
-            acc = 0;
-          }
+          for (int u = 0; u < KU_MAX; ++u)
+            if (u < KU && wn < nvw_all) nxt[u] = ld_keep(xr + 32 * wn + lane + vt * u);
+          A acc = 0;
+#pragma unroll
+          for (int u = 0; u < KU_MAX; ++u)
+            if (u < KU) acc = fma_acc((A)cur[u], acc);
+          acc = warp_tree_sum(acc);
+          if (lane == 0) red[t * 32 + w] = acc;
+#pragma unroll
+          for (int u = 0; u < KU_MAX; ++u) cur[u] = nxt[u];
+        }
+      } else {
+        for (int w = cw; w < nvw_all; w += nwc) {
+          A acc = 0;
+#pragma unroll 8
+          for (int i = 32 * w + lane; i < K; i += vt) acc = fma_acc((A)__ldg(xr + i), acc);
+          acc = warp_tree_sum(acc);
+          if (lane == 0) red[t * 32 + w] = acc;
         }
       }
       __syncthreads();
@@ -222,71 +246,19 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
         if (lane == 0) den[t] = norm_div_add(v, K, a.eps);
       }
       __syncthreads();
-      const A dn = den[t];
-#pragma unroll
-      for (int s = 0; s < PRO_SLOTS; ++s)
-        if (s < ns) {
-          const int g = cw + nwc * (s / KU) + nvw_all * (s % KU);  // the 32-group holding this value
-          store_act<Q, M>(act, L, t, g, lane, norm_scale(xv[s], dn, gv[s]));
-        }
     }
-    __syncthreads();
-    return;
-  }
-  // general path (any K, chunk, warp count; quantizer alone): the sum of
-  // squares walks each virtual thread's values in order, then every warp
-  // normalizes and quantizes its groups g = cw + nwc*i, PRO_SLOTS groups'
-  // loads issued before any is used
-  if (norm) {
-    for (int t = 0; t < M; ++t) {
-      const float* xr = a.xraw + (long)t * K;
-      for (int w = cw; w < nvw_all; w += nwc) {
-        float xv[PRO_SLOTS];
-        A acc = 0;
-        for (int i0 = 32 * w + lane; i0 < K; i0 += PRO_SLOTS * vt) {
-#pragma unroll
-          for (int s = 0; s < PRO_SLOTS; ++s)
-            if (i0 + s * vt < K) xv[s] = ld_keep(xr + i0 + s * vt);
-          compiler_fence();
-#pragma unroll
-          for (int s = 0; s < PRO_SLOTS; ++s)
-            if (i0 + s * vt < K) acc = fma_acc((A)xv[s], acc);
-        }
-        acc = warp_tree_sum(acc);
-        if (lane == 0) red[t * 32 + w] = acc;
-      }
-    }
-    __syncthreads();
-    if (cw == 0) {
-      for (int t = 0; t < M; ++t) {
-        A v = lane < nvw_all ? red[t * 32 + lane] : (A)0;
-        v = warp_tree_sum(v);
-        if (lane == 0) den[t] = norm_div_add(v, K, a.eps);
-      }
-    }
-    __syncthreads();
-  }
-  const int ng = (int)(L >> 5);
-  for (int t = 0; t < M; ++t) {
-    const float* xr = a.xraw + (long)t * K + k_lo;
     const A dn = norm ? den[t] : (A)1;
-    for (int g0 = cw; g0 < ng; g0 += PRO_SLOTS * nwc) {
-      float xv[PRO_SLOTS], gv[PRO_SLOTS];
-#pragma unroll
-      for (int b = 0; b < PRO_SLOTS; ++b) {
-        const int g = g0 + b * nwc, i = 32 * g + lane;
-        const bool in = g < ng && k_lo + i < K;
-        xv[b] = in ? ld_keep(xr + i) : 0.f;
-        gv[b] = (norm && in) ? ld_keep(a.gain + k_lo + i) : 1.f;
-      }
+    // (3) normalize and quantize, batch by batch
+    for (int g0 = cw; g0 < ng; g0 += QB * nwc) {
+      if (g0 != cw) load_batch(g0);
       compiler_fence();
 #pragma unroll
-      for (int b = 0; b < PRO_SLOTS; ++b) {
+      for (int b = 0; b < QB; ++b) {
         const int g = g0 + b * nwc;
         if (g >= ng) break;  // warp-uniform
-        float v = xv[b];
+        float v = qx[b];
         // past the row's end (a chunk narrower than the area) the area keeps zeros
-        if (norm && k_lo + 32 * g + lane < K) v = norm_scale(v, dn, gv[b]);
+        if (norm && k_lo + 32 * g + lane < K) v = norm_scale(v, dn, qg[b]);
         store_act<Q, M>(act, L, t, g, lane, v);
       }
     }
