@@ -59,13 +59,16 @@ def parse():
     ap.add_argument("--S", type=int, default=1, help="split-K chunks (gemv workload)")
     ap.add_argument("--argmax", action="store_true", help="argmax epilogue + reduce (gemv workload)")
     ap.add_argument("--path", default="auto", choices=["auto", "direct", "ring"])
-    ap.add_argument("--no-chain", action="store_true",
-                    help="sequence: one launch per projection instead of the whole-token chain kernel")
+    ap.add_argument("--chain", action="store_true",
+                    help="sequence: the whole token as one cooperative chain launch (lk_gemv_chain) instead "
+                         "of one fused launch per projection")
     ap.add_argument("--unfused", action="store_true",
                     help="sequence: separate norm/quantize launches instead of the fused prologue")
     ap.add_argument("--no-pdl", action="store_true",
                     help="no programmatic dependent launches between the fused GEMVs")
     ap.add_argument("--fused", action="store_true", help="gemv workload: RMSNorm->quantize->GEMV in one launch")
+    ap.add_argument("--table", default=None,
+                    help="write the per-config single-GEMV table (markdown) to this path")
     ap.add_argument("--opt", action="append", default=[],
                     help="library option name=value (lk_set_option), e.g. ring_kb=110; repeatable")
     return ap.parse_args()
@@ -275,7 +278,7 @@ def run_ours(a, rank, world):
     lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
     _apply_opts(lk, a)
     stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=not a.unfused,
-                        chain=not (a.no_chain or a.unfused))
+                        chain=a.chain and not a.unfused)
     tok_bytes = stack.weight_bytes()
     stream = torch.cuda.Stream(device=dev)
 
@@ -400,7 +403,7 @@ def _timing_event(torch, external):
     return torch.cuda.Event(enable_timing=True)
 
 
-def run_gemv(a, rank, world):
+def run_gemv(a, rank, world, quiet=False):
     """One GEMV shape: per-launch CUDA-event durations over weight copies
     rotated so that every launch streams from HBM (copies x bytes >= 4 x L2)."""
     import torch
@@ -499,8 +502,50 @@ def run_gemv(a, rank, world):
                         "peak_source": src, "algorithmic_bytes_per_launch": alg},
            "clocks": clk, "gpu_launches": a.steps * Rg * (2 if (S > 1 or a.argmax) else 1),
            "kernel": {1: "direct", 2: "ring", 0: "none"}[lk.lk_gemv_kernel_for(N, K, mode, B, S if S > 1 else 0)]}
-    if rank == 0:
+    del mats
+    torch.cuda.empty_cache()
+    if rank == 0 and not quiet:
         print(json.dumps(out), flush=True)
+    return out
+
+
+def run_table(a, path):
+    """The per-config table: every single-GEMV configuration (sizes, modes,
+    split-K) timed as --workload gemv, then the decode sequence at batch 1
+    and 8; markdown rows go to `path`, one JSON line per row to stdout."""
+    import copy
+
+    peaks, _ = measured_peaks()
+    rows = []
+
+    def g(label, **kw):
+        b = copy.copy(a)
+        b.workload, b.steps, b.warmup = "gemv", 20, 3
+        b.S, b.argmax, b.fused, b.batch, b.path = 1, False, False, 1, "auto"
+        for k, v in kw.items():
+            setattr(b, k, v)
+        d = run_gemv(b, 0, 1, quiet=True)
+        print(json.dumps(dict(d, label=label)), flush=True)
+        rows.append((label, b.mode, b.batch, b.S, d["us_per_gemv"], d["value"], d["kernel"]))
+
+    for m in ("dequant", "int8act", "twopass"):
+        g("C0 1024x1024", N=1024, K=1024, mode=m)
+    for m in ("dequant", "int8act", "twopass"):
+        g("C1 q 4096x4096 (norm+quant fused)", N=4096, K=4096, mode=m, fused=True)
+        g("C1 gate/up 24576x4096 (norm+quant fused)", N=24576, K=4096, mode=m, fused=True)
+    for m in ("twopass", "dequant"):
+        for S in (1, 2, 4, 8):
+            g("C2 o 5120x5120 split-K", N=5120, K=5120, mode=m, S=S)
+            g("C2 down 5120x25600 split-K", N=5120, K=25600, mode=m, S=S)
+    for m in ("dequant", "int8act", "twopass"):
+        g("C3 lm-head 151936x4096 + argmax (norm fused)", N=151936, K=4096, mode=m, fused=True, argmax=True)
+    with open(path, "w") as f:
+        f.write("| Config | Mode | M | S | kernel | us/GEMV | weight GB/s | % of 8 TB/s | % of measured %.0f GB/s |\n"
+                % peaks["hbm_gbs"])
+        f.write("|---|---|---|---|---|---|---|---|---|\n")
+        for label, m, B, S, us, gbs, kern in rows:
+            f.write(f"| {label} | {m} | {B} | {S} | {kern} | {us:.2f} | {gbs:.0f} | {100 * gbs / NOMINAL_HBM_GBS:.1f} "
+                    f"| {100 * gbs / peaks['hbm_gbs']:.1f} |\n")
 
 
 def _max_over_ranks(v, dist, dev):
@@ -624,6 +669,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if a.impl == "reference":
         run_reference(a, rank)
+        return
+    if a.table:
+        run_table(a, a.table)
         return
     if a.workload == "gemv":
         run_gemv(a, rank, world)

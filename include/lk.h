@@ -292,8 +292,13 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *   "ring_cps"    ring blocks per SM in the grid, 1..4 (default 1)
  *   "pdl"         1: lk_rmsnorm_quant_gemv_q8 launches as a programmatic
  *                 dependent launch (default 0)
+ *   "l2_prefetch_kb"  lk_gemv_chain: KB of later steps' weights each block
+ *                 keeps requested into L2 ahead of the step it computes
+ *                 (prefetch.global.L2::evict_last by every thread before
+ *                 a barrier; default 0 = off)
  *   "trace"       1: the ring and chain kernels write block 0's timestamps
- *                 to the trace buffer (lk_trace_read)
+ *                 to the trace buffer (lk_trace_read); 2: the chain also
+ *                 records every block's and block 0's warps' step ends
  *   "wait_us"     time limit of every device-side wait, microseconds
  *                 (0 = default, 2 s)
  * Unknown names or out-of-range values return LK_ERR_ARG.
@@ -315,7 +320,10 @@ lk_status lk_device_error(int reset, int* code);
  * chain launch records %globaltimer nanoseconds.  Ring kernel: [0] start,
  * [1] after the dependency wait, [2] activation ready, [3 + w] warp w done.
  * Chain: [0] start, then per step i: [1 + 3i] step start (after its barrier),
- * [2 + 3i] activation ready, [3 + 3i] block 0's rows done.  Synchronizes the
+ * [2 + 3i] activation ready, [3 + 3i] block 0's rows done; with "trace" 2,
+ * from entry 1024 on: [1024 + i*G + b] block b's end of step i (G blocks),
+ * and from entry 1024 + n_ops*G: [.. + i*W + w] warp w of block 0 at the end
+ * of its step-i rows (W warps), while they fit in the buffer.  Synchronizes the
  * device and copies the first n (<= 4096) entries to host_out.
  */
 lk_status lk_trace_read(uint64_t* host_out, int n);

@@ -19,6 +19,7 @@ long opt_ring_warps = 0;
 long opt_ring_kb = 0;
 long opt_ring_cps = 1;
 long opt_trace = 0;
+long opt_l2_prefetch_kb = 0;
 long opt_pdl = 0;
 
 static const int kMaxDevices = 64;
@@ -144,8 +145,11 @@ lk_status lk_set_option(const char* name, long value) {
   } else if (!strcmp(name, "pdl")) {
     if (value < 0 || value > 1) return LK_ERR_ARG;
     opt_pdl = value;
+  } else if (!strcmp(name, "l2_prefetch_kb")) {
+    if (value < 0 || value > 65536) return LK_ERR_ARG;
+    opt_l2_prefetch_kb = value;
   } else if (!strcmp(name, "trace")) {
-    if (value < 0 || value > 1) return LK_ERR_ARG;
+    if (value < 0 || value > 2) return LK_ERR_ARG;
     opt_trace = value;
   } else if (!strcmp(name, "ring_hint")) {
     if (value < 0 || value > 1) return LK_ERR_ARG;
@@ -167,6 +171,7 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "wait_us")) return opt_wait_us;
   if (!strcmp(name, "ring_hint")) return opt_ring_hint;
   if (!strcmp(name, "trace")) return opt_trace;
+  if (!strcmp(name, "l2_prefetch_kb")) return opt_l2_prefetch_kb;
   if (!strcmp(name, "ring_warps")) return opt_ring_warps;
   if (!strcmp(name, "ring_kb")) return opt_ring_kb;
   if (!strcmp(name, "ring_cps")) return opt_ring_cps;

@@ -27,12 +27,32 @@ struct ChainArgs {
   int nwc, depth;
   unsigned stage_bytes, ring_off;
   float eps;
-  unsigned* sync;           // [0] arrivals, [1] generation
+  unsigned* sync;           // [0] arrivals, [32] generation (separate 128-byte lines)
   unsigned long long wait_ns;
   unsigned long long pol_w;
   int* err;
   unsigned long long* trace;  // block 0's timestamps (option "trace"), or NULL
+  int trace_all;              // also every block's and block 0's warps' step ends (trace 2)
+  long long pf_budget;        // bytes of later steps' weights each block keeps requested into L2 ahead
 };
+
+// This block's bytes of step `o` (its rows' levels, then their scales): a
+// contiguous range of each array, since a block's rows are contiguous.
+struct PfRange {
+  const unsigned char* w;
+  long wbytes;
+  const unsigned char* s;
+  long sbytes;
+};
+__device__ __forceinline__ PfRange pf_range(const lk_chain_op& o) {
+  const long N = o.N, r0 = (long)blockIdx.x * N / gridDim.x, r1 = (long)(blockIdx.x + 1) * N / gridDim.x;
+  PfRange r;
+  r.w = (const unsigned char*)o.wq + r0 * o.K;
+  r.wbytes = (r1 - r0) * o.K;
+  r.s = (const unsigned char*)o.ws + r0 * (o.K / 16);
+  r.sbytes = (r1 - r0) * (o.K / 16);
+  return r;
+}
 
 __device__ __forceinline__ void stamp(unsigned long long* trace, int i) {
   if (trace && blockIdx.x == 0 && threadIdx.x == 0 && i < LK_TRACE_MAX) trace[i] = gtimer();
@@ -44,23 +64,40 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void st_relaxed_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // All blocks of the grid meet here (bounded).  Writes before it are visible
-// to every block after it.  Returns false after a timeout or an abort.
-__device__ bool grid_sync(unsigned* sync, unsigned nblocks, unsigned long long limit_ns, int* err,
+// to every block after it: the block's threads meet at a CTA barrier, thread
+// 0 arrives with an acquire-release add on the counter (its release covers
+// the block's writes ordered before it; the last arrival's acquire sees every
+// earlier arrival's), the last arrival resets the counter and releases the
+// next generation, and the others acquire it.  `gen` is the generation this
+// block last saw (read once at kernel start), so an arrival costs one round
+// trip.  No full fence is used, so the block's weight copies still in flight
+// do not delay it.  Returns false after a timeout or an abort.
+__device__ bool grid_sync(unsigned* sync, unsigned& gen, unsigned nblocks, unsigned long long limit_ns, int* err,
                           volatile int* abort_flag) {
   __syncthreads();
   if (threadIdx.x == 0 && !*abort_flag) {
-    const unsigned gen = ld_acquire_gpu(sync + 1);
-    __threadfence();
-    const unsigned prev = atomicAdd(sync, 1u);
+    const unsigned prev = atom_add_acq_rel_gpu(sync, 1u);
     if (prev == nblocks - 1) {
-      atomicExch(sync, 0u);
-      __threadfence();
-      atomicAdd(sync + 1, 1u);
+      st_relaxed_gpu(sync, 0u);
+      red_add_release_gpu(sync + 32, 1u);
     } else {
       const unsigned long long t0 = gtimer();
       unsigned spins = 0;
-      while (ld_acquire_gpu(sync + 1) == gen) {
+      while (ld_acquire_gpu(sync + 32) == gen) {
         if ((++spins & 63u) == 0 && gtimer() - t0 > limit_ns) {
           atomicOr(err, ERR_BARRIER);
           *abort_flag = 1;
@@ -68,8 +105,8 @@ __device__ bool grid_sync(unsigned* sync, unsigned nblocks, unsigned long long l
         }
       }
     }
-    __threadfence();
   }
+  ++gen;  // every thread keeps the count; only thread 0's is used
   return __syncthreads_or(*abort_flag) == 0;  // the same answer in every thread
 }
 
@@ -121,13 +158,53 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     ++issued;
   };
   stamp(ca.trace, 0);
+  // The barrier generation at launch.  No block can complete a barrier of
+  // this launch before every block has read it (completion needs every
+  // block's arrival, and a block arrives only after this read).
+  unsigned gen = threadIdx.x == 0 ? ld_acquire_gpu(ca.sync + 32) : 0u;
   for (int d = 0; d < D && iop < ca.n_ops; ++d) issue_next();
+
+  // L2 prefetch cursor: the block's bytes of later steps (levels, then
+  // scales, step after step) are requested into L2 with per-thread
+  // prefetch.global.L2::evict_last, keeping pf_budget bytes ahead of the step
+  // being computed; it runs while the threads would wait at a barrier anyway.
+  int pf_op = 1;
+  long pf_off = 0;   // bytes of step pf_op already requested
+  auto prefetch_ahead = [&](int cur) {
+    if (ca.pf_budget <= 0) return;
+    if (pf_op <= cur) {
+      pf_op = cur + 1;
+      pf_off = 0;
+    }
+    long ahead = pf_off;  // bytes requested beyond step `cur`
+    for (int k = cur + 1; k < pf_op && k < ca.n_ops; ++k) {
+      const PfRange r = pf_range(ca.ops[k]);
+      ahead += r.wbytes + r.sbytes;
+    }
+    while (pf_op < ca.n_ops && ahead < ca.pf_budget) {
+      const PfRange r = pf_range(ca.ops[pf_op]);
+      const long total = r.wbytes + r.sbytes;
+      const long want = ca.pf_budget - ahead;
+      const long end = pf_off + want < total ? pf_off + want : total;
+      for (long off = pf_off + 128L * threadIdx.x; off < end; off += 128L * blockDim.x) {
+        const unsigned char* ptr = off < r.wbytes ? r.w + off : r.s + (off - r.wbytes);
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(ptr));
+      }
+      ahead += end - pf_off;
+      pf_off = end;
+      if (pf_off >= total) {
+        ++pf_op;
+        pf_off = 0;
+      }
+    }
+  };
 
   long consumed = 0;
   bool ok = true;
   for (int op = 0; ok && op < ca.n_ops; ++op) {
     const lk_chain_op o = ca.ops[op];
-    if (o.wait && !grid_sync(ca.sync, gridDim.x, ca.wait_ns, ca.err, abort_flag)) {
+    if (o.wait) prefetch_ahead(op);
+    if (o.wait && !grid_sync(ca.sync, gen, gridDim.x, ca.wait_ns, ca.err, abort_flag)) {
       ok = false;
       break;
     }
@@ -177,8 +254,16 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
         finish_quad<Q, M, false>(p, g, warp, nwc, n, dummy, 0, o.y, best, lane);
       }
     }
+    if (ca.trace && ca.trace_all && lane == 0 && blockIdx.x == 0) {
+      const long i = 1024 + (long)ca.n_ops * gridDim.x + (long)op * nwc + warp;
+      if (i < LK_TRACE_MAX) ca.trace[i] = gtimer();
+    }
     ok = __syncthreads_and(ok) != 0;  // every warp agrees before the next barrier
     stamp(ca.trace, 3 + 3 * op);
+    if (ca.trace && ca.trace_all && threadIdx.x == 0) {
+      const long i = 1024 + (long)op * gridDim.x + blockIdx.x;
+      if (i < LK_TRACE_MAX) ca.trace[i] = gtimer();
+    }
     if (!ok) break;
     if (o.argmax_parts) {
 #pragma unroll
@@ -193,7 +278,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
         o.argmax_parts[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
       }
       if (o.argmax_idx) {
-        ok = grid_sync(ca.sync, gridDim.x, ca.wait_ns, ca.err, abort_flag);
+        ok = grid_sync(ca.sync, gen, gridDim.x, ca.wait_ns, ca.err, abort_flag);
         if (!ok) break;
         if (blockIdx.x == 0 && warp < M) {
           unsigned long long m = 0;
@@ -247,7 +332,7 @@ unsigned stage_bytes_for(int K) {
 
 using namespace lkring;
 
-extern "C" size_t lk_chain_sync_bytes(void) { return 64; }
+extern "C" size_t lk_chain_sync_bytes(void) { return 256; }
 
 extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* ops_dev, int n_ops, lk_mode mode,
                                    int M, float eps, uint32_t* sync, cudaStream_t stream) {
@@ -304,6 +389,8 @@ extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* op
   ca.err = lkh::error_word_ptr();
   if (!ca.err) return LK_ERR_CUDA;
   ca.trace = lkh::opt_trace ? lkh::trace_ptr() : nullptr;
+  ca.pf_budget = lkh::opt_l2_prefetch_kb * 1024;
+  ca.trace_all = lkh::opt_trace >= 2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->sm_count);
   cfg.blockDim = dim3(w * 32);

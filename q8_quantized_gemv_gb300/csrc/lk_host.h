@@ -27,6 +27,7 @@ extern long opt_ring_warps;   // 0 auto, else warps per block of the ring kernel
 extern long opt_ring_kb;      // 0: no cap, else shared memory per ring block in KB
 extern long opt_ring_cps;     // ring blocks per SM in the grid (default 1)
 extern long opt_pdl;          // 1: fused ring launches are programmatic dependents
+extern long opt_l2_prefetch_kb;  // chain: KB of later steps each block requests into L2 ahead
 extern long opt_trace;        // 1: kernels write block 0 timestamps to the trace buffer
 extern long opt_ring_hint;    // 1: L2 evict-first hint on the weight copies (default)
 extern long opt_wait_us;      // bound of every device-side wait, microseconds (0 = 2 s)

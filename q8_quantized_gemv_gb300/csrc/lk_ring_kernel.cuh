@@ -152,7 +152,7 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // of values 32v + l + vt*u in ascending u.  The same warp then normalizes and
 // quantizes exactly the 32-groups v + (vt/32)*u it loaded, so each row is
 // read from global memory once, all of a warp's loads in flight together.
-constexpr int PRO_SLOTS = 16;  // values per lane per row held in registers by the prologue
+constexpr int PRO_SLOTS = 32;  // groups per warp per batch held in registers by the prologue
 
 // A read-only f32 load that the compiler keeps where it is written: the
 // prologue issues all of a lane's loads before using any, so a row costs one

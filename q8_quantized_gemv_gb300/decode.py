@@ -24,7 +24,7 @@ from . import lk, synth
 class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
                  batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
-                 fused=True, chain=True):
+                 fused=True, chain=False):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
         dev = self.dev

@@ -104,7 +104,7 @@ def test_chain_barrier_timeout_is_reported_and_recoverable():
     # a sync counter that can never reach "last arrival": every barrier wait
     # runs out (2 ms), the blocks drain their copies and exit
     lk.lk_set_option("wait_us", 2000)
-    a.chain.sync.fill_(0x40000000)
+    a.chain.sync[0] = 0x40000000
     a.run_token()
     torch.cuda.synchronize()
     assert lk.lk_device_error(reset=True) != 0
