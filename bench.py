@@ -540,7 +540,7 @@ def run_table(a, path):
     for m in ("dequant", "int8act", "twopass"):
         g("C3 lm-head 151936x4096 + argmax (norm fused)", N=151936, K=4096, mode=m, fused=True, argmax=True)
     with open(path, "w") as f:
-        f.write("| Config | Mode | M | S | kernel | us/GEMV | weight GB/s | % of 8 TB/s | % of measured %.0f GB/s |\n"
+        f.write("| Config | Mode | M | S | kernel | us/GEMV | weight GB/s | %% of 8 TB/s | %% of measured %.0f GB/s |\n"
                 % peaks["hbm_gbs"])
         f.write("|---|---|---|---|---|---|---|---|---|\n")
         for label, m, B, S, us, gbs, kern in rows:
@@ -584,22 +584,27 @@ def roofline_chain(stack, stream, a, torch):
             {"chain": {"us": us, "GB/s": achieved, "launches": steps}})
 
 
-def chain_traffic(alg):
-    """DRAM bytes per launch from the committed ncu summary of this kernel, if
-    it was taken on the current sources (else None)."""
+def profile_traffic(key):
+    """A DRAM-traffic figure from profiles/traffic.txt (one ncu capture), if it
+    was taken on the current library sources (else None)."""
     try:
         from q8_quantized_gemv_gb300 import build
         rec = {}
-        with open(os.path.join(ROOT, "profiles", "chain_traffic.txt")) as f:
+        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             for line in f:
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     rec[k.strip()] = v.strip()
         if rec.get("sources_sha256") != build.sources_digest():
             return None
-        return float(rec["dram_bytes_per_algorithmic_byte"]) * alg
+        return float(rec[key])
     except (OSError, KeyError, ValueError, AttributeError):
         return None
+
+
+def chain_traffic(alg):
+    r = profile_traffic("gemv_chain_2layers_int8act_per_algorithmic_byte")
+    return None if r is None else r * alg
 
 
 def roofline(stack, stream, a, torch):
@@ -653,6 +658,8 @@ def roofline(stack, stream, a, torch):
     gu = per["gu"]
     peak = peaks["hbm_gbs"]
     traffic = None
+    if stack.mode == 1 and stack.B == 1 and stack.fused["gu"]:
+        traffic = profile_traffic("gemv_ring_fused_gateup_24576x4096_int8act")
     roof = {"bound": "hbm", "achieved": gu["GB/s"], "peak": peak, "unit": "GB/s",
             "frac": gu["GB/s"] / peak, "traffic": traffic, "peak_source": src,
             "kernel": "fused gate/up GEMV 24576x4096", "algorithmic_bytes_per_launch": alg_bytes("gu"),
