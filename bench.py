@@ -327,7 +327,7 @@ def run_ours(a, rank, world):
     clk = clocks.summary(tw0, tw1)
     clocks.stop()
     ms_max = _max_over_ranks(ms, dist, dev)
-    value = tok_bytes * world / (ms_max * 1e-3) / 1e9
+    value = replica_value(tok_bytes, world, ms_max)
 
     # ---- e2e: pinned host input -> device, graph, argmax -> pinned host, every step ------
     x_host = stack.x0.cpu().pin_memory()
@@ -546,6 +546,12 @@ def run_table(a, path):
         for label, m, B, S, us, gbs, kern in rows:
             f.write(f"| {label} | {m} | {B} | {S} | {kern} | {us:.2f} | {gbs:.0f} | {100 * gbs / NOMINAL_HBM_GBS:.1f} "
                     f"| {100 * gbs / peaks['hbm_gbs']:.1f} |\n")
+
+
+def replica_value(bytes_per_step, world, ms_max):
+    """Whole-job weight GB/s of `world` replicas: every rank streams its own
+    copy of the weights each step, the slowest rank sets the time."""
+    return bytes_per_step * world / (ms_max * 1e-3) / 1e9
 
 
 def _max_over_ranks(v, dist, dev):
