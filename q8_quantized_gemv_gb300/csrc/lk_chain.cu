@@ -370,7 +370,8 @@ extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* op
   if (w < 1 || w * depth < 4) return LK_ERR_SHAPE;
   const unsigned total = ring_off + (unsigned)(w * depth) * sb + TAIL;
   chain_fn f = mode == 0 ? pick_m<0>(M) : mode == 1 ? pick_m<1>(M) : pick_m<2>(M);
-  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)total) != cudaSuccess)
+  // (the cap is the device's maximum: see ring_gemv)
+  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) != cudaSuccess)
     return LK_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, w * 32, total) != cudaSuccess || per_sm < 1)

@@ -172,8 +172,11 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   const Layout L = layout(p, d->smem_optin);
   if (!layout_ok(L)) return LK_ERR_SHAPE;
   ring_fn f = pick(p.mode, p.M, p.split, p.fuse);
-  // (cheap and idempotent: set on every launch rather than cached per device)
-  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total) != cudaSuccess)
+  // The cap is the device's opt-in maximum, never this launch's size: one
+  // instantiation serves launches of different sizes, and a cap lowered by a
+  // later launch would make an earlier one (e.g. a node of a captured graph,
+  // relaunched on its own by a profiler) exceed it.
+  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) != cudaSuccess)
     return LK_ERR_CUDA;
   RingArgs ra;
   ra.p = p;
