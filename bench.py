@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--K", type=int, default=4096)
     ap.add_argument("--S", type=int, default=1, help="split-K chunks (gemv workload)")
     ap.add_argument("--argmax", action="store_true", help="argmax epilogue + reduce (gemv workload)")
-    ap.add_argument("--path", default="auto", choices=["auto", "direct", "ring"])
+    ap.add_argument("--path", default="auto", choices=["auto", "direct", "ring", "mma"])
     ap.add_argument("--chain", action="store_true",
                     help="sequence: the whole token as one cooperative chain launch (lk_gemv_chain) instead "
                          "of one fused launch per projection")
@@ -370,6 +370,8 @@ def run_ours(a, rank, world):
                    "l2": "inputs larger than L2 (8.04 GB of weights per step)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "gemv_path": "auto", "fused_prologue": {k: v for k, v in stack.fused.items()},
+                   "gemv_kernel": {k: "ring" if stack.fused[k] else {1: "direct", 2: "ring", 3: "mma"}.get(v, "none")
+                                   for k, v in stack.kernel.items()},
                    "chain": stack.chain is not None,
                    "pdl": not a.no_pdl, "options": a.opt},
         "us_per_token": ms_max * 1e3,
@@ -414,7 +416,7 @@ def run_gemv(a, rank, world, quiet=False):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
-    lk.lk_set_option("gemv_path", {"auto": 0, "direct": 1, "ring": 2}[a.path])
+    lk.lk_set_option("gemv_path", {"auto": 0, "direct": 1, "ring": 2, "mma": 3}[a.path])
     lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
     _apply_opts(lk, a)
     mode = lk.MODES[a.mode]
@@ -501,7 +503,8 @@ def run_gemv(a, rank, world, quiet=False):
                         "unit": "GB/s", "frac": alg / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], "traffic": None,
                         "peak_source": src, "algorithmic_bytes_per_launch": alg},
            "clocks": clk, "gpu_launches": a.steps * Rg * (2 if (S > 1 or a.argmax) else 1),
-           "kernel": {1: "direct", 2: "ring", 0: "none"}[lk.lk_gemv_kernel_for(N, K, mode, B, S if S > 1 else 0)]}
+           "kernel": {1: "direct", 2: "ring", 3: "mma", 0: "none"}[lk.lk_gemv_kernel_for(N, K, mode, B,
+                                                                                          S if S > 1 else 0)]}
     del mats
     torch.cuda.empty_cache()
     if rank == 0 and not quiet:
@@ -651,11 +654,13 @@ def roofline(stack, stream, a, torch):
     act_b = B * (1 if stack.mode != 2 else 2)
 
     def alg_bytes(name):
-        if name == "lm":
-            N, K = stack.V, stack.H
-        else:
-            N, K = stack.shapes[name]
-        return N * K + N * K // 16 + (act_b * K + B * (K // 32) * 4 if stack.mode else B * K * 4) + B * N * 4
+        """weights + the activation read once + the outputs; "qkv" is the
+        grouped q/k/v launch (one activation, three matrices)"""
+        mats = [stack.shapes[n] for n in ("q", "k", "v")] if name == "qkv" else \
+            [(stack.V, stack.H)] if name == "lm" else [stack.shapes[name]]
+        K = mats[0][1]
+        act = act_b * K + B * (K // 32) * 4 if stack.mode else B * K * 4
+        return act + sum(N * K + N * K // 16 + B * N * 4 for N, K in mats)
 
     per = {}
     for name, ts in times.items():

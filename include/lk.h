@@ -104,7 +104,10 @@ lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq
  *  b:  Int8Act p = fma(w*s, d, p);  TwoPass p = fma(w, fma(s, d, (s/128)*e), p);
  *  y = (p0 + p2) + (p1 + p3).  Dequant: each block's 32 products are summed
  *  in f32 and the blocks, scaled by the f16 weight scale, in f64; the f64 row
- *  sum is rounded to f32 once.
+ *  sum is rounded to f32 once.  For 2..8 rows of Int8Act / TwoPass the dots
+ *  run on the tensor cores (f16 MMA on the exact int8 levels, f32
+ *  accumulators that hold the exact integer dot); the combine is the same, so
+ *  every kernel gives the same bits.
  *   Dequant reads x; Int8Act reads xq, xs; TwoPass reads xq, xl, xs.
  *   argmax_parts  optional u64 [M][*n_parts_out]: the lm-head epilogue
  *                 (model-as-a-kernel "megakernel.cu" amax_key with
@@ -190,9 +193,11 @@ lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* ops_dev, int 
  * Which GEMV kernel a call of this shape would launch under the current
  * options, for 16-byte aligned operands: 1 the direct-load kernel (any
  * K % 32 == 0), 2 the bulk-copy ring kernel (K % 256 == 0 and the activation
- * fits in shared memory), 0 none (invalid shape, or the ring kernel forced
- * by "gemv_path" 2 but not applicable).  S = 0 asks about lk_gemv_q8,
- * S >= 1 about lk_gemv_q8_splitk.
+ * fits in shared memory), 3 the tensor-core kernel (lk_gemv_q8 only:
+ * LK_INT8ACT or LK_TWOPASS, 2 <= M <= 8 (option "mma_min_m"), K % 256 == 0
+ * and the activation fitting in shared memory next to a weight ring), 0 none
+ * (invalid shape, or a kernel forced by "gemv_path" but not applicable).
+ * S = 0 asks about lk_gemv_q8, S >= 1 about lk_gemv_q8_splitk.
  */
 int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S);
 
@@ -281,7 +286,8 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
 /*
  * Tuning and test options (process-wide; not thread-safe against concurrent
  * launches).  Names:
- *   "gemv_path"   0 auto, 1 direct-load kernel, 2 bulk-copy ring kernel
+ *   "gemv_path"   0 auto, 1 direct-load kernel, 2 bulk-copy ring kernel,
+ *                 3 tensor-core kernel (2..8 rows; LK_ERR_SHAPE elsewhere)
  *   "ring_stages" ring depth of the bulk-copy kernel (0 = as deep as shared
  *                 memory allows, at most 32)
  *   "grid_ctas"   blocks of the ring kernel (0 = one per SM)
@@ -301,6 +307,17 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 records every block's and block 0's warps' step ends
  *   "wait_us"     time limit of every device-side wait, microseconds
  *                 (0 = default, 2 s)
+ *   "mma_min_m"   fewest activation rows lk_gemv_q8 runs on the tensor-core
+ *                 kernel (0 = default 2; 9 = never)
+ *   "mma_tk"      its bytes of K per ring stage: 0 auto (1024, else 512),
+ *                 else a multiple of 256 up to 8192
+ *   "mma_warps"   its warps per block: 0 auto, else 1..16
+ *   "mma_depth"   its ring stages per warp: 0 = 2, else 1..8
+ *   "l2_ahead_kb" ring and tensor-core kernels: KB per block of the stages
+ *                 after the ring's first fill requested into L2 at kernel
+ *                 start (cp.async.bulk.prefetch.L2), so that HBM keeps
+ *                 streaming while the block waits for the previous kernel
+ *                 (default 0 = off)
  * Unknown names or out-of-range values return LK_ERR_ARG.
  */
 lk_status lk_set_option(const char* name, long value);

@@ -21,6 +21,11 @@ long opt_ring_cps = 1;
 long opt_trace = 0;
 long opt_l2_prefetch_kb = 0;
 long opt_pdl = 0;
+long opt_mma_min_m = 0;
+long opt_mma_tk = 0;
+long opt_mma_warps = 0;
+long opt_mma_depth = 0;
+long opt_l2_ahead_kb = 0;
 
 static const int kMaxDevices = 64;
 static DeviceInfo g_info[kMaxDevices];
@@ -62,6 +67,9 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __rest
   typedef typename acc_of<Q>::t A;
   __shared__ A red[32];
   __shared__ A total;
+  // a programmatic dependent (a GEMV launched with "pdl") may start its
+  // weight stream now; it reads these outputs only after this grid completes
+  asm volatile("griddepcontrol.launch_dependents;" :::);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int vt = blockDim.x, nw = vt >> 5;
   const long row = blockIdx.x;
@@ -92,6 +100,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __rest
 template <int Q>
 __global__ void quantize_kernel(const float* __restrict__ x, long groups, int8_t* __restrict__ xq,
                                 int8_t* __restrict__ xl, float* __restrict__ xs) {
+  asm volatile("griddepcontrol.launch_dependents;" :::);  // as in rmsnorm_quant_kernel
   const long g = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (g >= groups) return;  // whole warps exit together
   const int lane = threadIdx.x & 31;
@@ -125,7 +134,7 @@ int lk_version(void) { return 100; }
 lk_status lk_set_option(const char* name, long value) {
   if (!name) return LK_ERR_ARG;
   if (!strcmp(name, "gemv_path")) {
-    if (value < 0 || value > 2) return LK_ERR_ARG;
+    if (value < 0 || value > 3) return LK_ERR_ARG;
     opt_gemv_path = value;
   } else if (!strcmp(name, "ring_stages")) {
     if (value < 0 || value > 32) return LK_ERR_ARG;
@@ -157,6 +166,21 @@ lk_status lk_set_option(const char* name, long value) {
   } else if (!strcmp(name, "wait_us")) {
     if (value < 0 || value > 60000000L) return LK_ERR_ARG;
     opt_wait_us = value;
+  } else if (!strcmp(name, "mma_min_m")) {
+    if (value < 0 || value > LK_MAX_M + 1) return LK_ERR_ARG;
+    opt_mma_min_m = value;
+  } else if (!strcmp(name, "mma_tk")) {
+    if (value < 0 || value > 8192 || value % 256) return LK_ERR_ARG;
+    opt_mma_tk = value;
+  } else if (!strcmp(name, "mma_warps")) {
+    if (value < 0 || value > 16) return LK_ERR_ARG;
+    opt_mma_warps = value;
+  } else if (!strcmp(name, "mma_depth")) {
+    if (value < 0 || value > 8) return LK_ERR_ARG;
+    opt_mma_depth = value;
+  } else if (!strcmp(name, "l2_ahead_kb")) {
+    if (value < 0 || value > 65536) return LK_ERR_ARG;
+    opt_l2_ahead_kb = value;
   } else {
     return LK_ERR_ARG;
   }
@@ -176,6 +200,11 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "ring_kb")) return opt_ring_kb;
   if (!strcmp(name, "ring_cps")) return opt_ring_cps;
   if (!strcmp(name, "pdl")) return opt_pdl;
+  if (!strcmp(name, "mma_min_m")) return opt_mma_min_m;
+  if (!strcmp(name, "mma_tk")) return opt_mma_tk;
+  if (!strcmp(name, "mma_warps")) return opt_mma_warps;
+  if (!strcmp(name, "mma_depth")) return opt_mma_depth;
+  if (!strcmp(name, "l2_ahead_kb")) return opt_l2_ahead_kb;
   return -1;
 }
 

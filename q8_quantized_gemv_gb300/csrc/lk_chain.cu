@@ -34,6 +34,7 @@ struct ChainArgs {
   unsigned long long* trace;  // block 0's timestamps (option "trace"), or NULL
   int trace_all;              // also every block's and block 0's warps' step ends (trace 2)
   long long pf_budget;        // bytes of later steps' weights each block keeps requested into L2 ahead
+  int pdl;                    // launched as a programmatic dependent (a chain without barriers)
 };
 
 // This block's bytes of step `o` (its rows' levels, then their scales): a
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  if (ca.pdl && threadIdx.x == 0) griddep_launch();
 
   // The issue cursor walks this warp's stages of every step in order.
   int iop = 0;
@@ -199,6 +201,8 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     }
   };
 
+  // weights above do not depend on the previous kernel; activations do
+  if (ca.pdl) griddep_wait();
   long consumed = 0;
   bool ok = true;
   for (int op = 0; ok && op < ca.n_ops; ++op) {
@@ -373,6 +377,11 @@ extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* op
   // (the cap is the device's maximum: see ring_gemv)
   if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) != cudaSuccess)
     return LK_ERR_CUDA;
+  // Without a grid barrier (no step waits, no in-kernel argmax reduce) the
+  // chain is an ordinary launch: a grouped GEMV, which may be a programmatic
+  // dependent of the previous kernel.  With one it is a cooperative launch.
+  bool barrier = false;
+  for (int i = 0; i < n_ops; ++i) barrier = barrier || ops[i].wait || ops[i].argmax_idx;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, w * 32, total) != cudaSuccess || per_sm < 1)
     return LK_ERR_SHAPE;
@@ -392,16 +401,22 @@ extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* op
   ca.trace = lkh::opt_trace ? lkh::trace_ptr() : nullptr;
   ca.pf_budget = lkh::opt_l2_prefetch_kb * 1024;
   ca.trace_all = lkh::opt_trace >= 2;
+  ca.pdl = !barrier && lkh::opt_pdl ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->sm_count);
   cfg.blockDim = dim3(w * 32);
   cfg.dynamicSmemBytes = total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (barrier) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (barrier || ca.pdl) ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, f, ca) != cudaSuccess) return LK_ERR_CUDA;
   return lkh::launch_status();
 }

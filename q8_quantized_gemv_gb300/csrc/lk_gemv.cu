@@ -255,10 +255,14 @@ lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode
   p.y = y;
   p.amax = (unsigned long long*)argmax_parts;
   int n_parts = 0;
-  if (opt_gemv_path != 1 && ring_supports(p)) {
+  if ((opt_gemv_path == 0 || opt_gemv_path == 3) && mma_supports(p)) {
+    st = mma_gemv(p, stream, &n_parts);
+  } else if (opt_gemv_path == 3) {
+    return LK_ERR_SHAPE;
+  } else if (opt_gemv_path != 1 && ring_supports(p)) {
     st = ring_gemv(p, stream, &n_parts);
   } else {
-    if (opt_gemv_path == 2 && !ring_supports(p)) return LK_ERR_SHAPE;
+    if (opt_gemv_path == 2) return LK_ERR_SHAPE;
     st = direct_gemv(p, stream, &n_parts);
   }
   if (n_parts_out) *n_parts_out = n_parts;
@@ -276,6 +280,8 @@ int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S) {
   p.split = S > 0;
   p.S = S > 0 ? S : 1;
   if (opt_gemv_path == 1) return 1;
+  if (S == 0 && (opt_gemv_path == 0 || opt_gemv_path == 3) && mma_supports(p)) return 3;
+  if (opt_gemv_path == 3) return S == 0 ? 0 : (ring_supports(p) ? 2 : 1);
   return ring_supports(p) ? 2 : (opt_gemv_path == 2 ? 0 : 1);
 }
 

@@ -20,7 +20,7 @@ struct DeviceInfo {
 const DeviceInfo* device_info(int* dev_out);
 
 // Process-wide options (lk_set_option).
-extern long opt_gemv_path;    // 0 auto, 1 direct, 2 ring
+extern long opt_gemv_path;    // 0 auto, 1 direct, 2 ring, 3 tensor-core (small batch)
 extern long opt_ring_stages;  // 0 default
 extern long opt_grid_ctas;    // 0 default
 extern long opt_ring_warps;   // 0 auto, else warps per block of the ring kernel (1..16)
@@ -31,6 +31,11 @@ extern long opt_l2_prefetch_kb;  // chain: KB of later steps each block requests
 extern long opt_trace;        // 1: kernels write block 0 timestamps to the trace buffer
 extern long opt_ring_hint;    // 1: L2 evict-first hint on the weight copies (default)
 extern long opt_wait_us;      // bound of every device-side wait, microseconds (0 = 2 s)
+extern long opt_mma_min_m;    // fewest activation rows taking the tensor-core kernel (0 = 2)
+extern long opt_mma_tk;       // its bytes of K per stage (0 auto, else a multiple of 256)
+extern long opt_mma_warps;    // its warps per block (0 auto)
+extern long opt_mma_depth;    // its ring stages per warp (0 = 2)
+extern long opt_l2_ahead_kb;  // ring/tensor-core kernels: KB per block of later stages requested into L2 at start
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
@@ -72,6 +77,10 @@ unsigned long long* trace_ptr();
 // kernel), otherwise the launch status; *n_parts receives the blocks launched.
 lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts);
 bool ring_supports(const GemvProblem& p);
+
+// Tensor-core kernel for 2..8 activation rows (lk_mma.cu), same contract.
+lk_status mma_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts);
+bool mma_supports(const GemvProblem& p);
 int ring_max_ctas(long N);
 
 }  // namespace lkh

@@ -1,0 +1,478 @@
+// Small-batch Q8_0 GEMV on the tensor cores (Int8Act and TwoPassInt8, 2..8
+// activation rows), sm_103a.
+//
+// At batch 8 every weight byte meets 8 activation rows: the block dots form a
+// dense int8 contraction [N x K] x [K x 8].  This kernel runs it as
+// mma.sync m16n8k16 with f16 operands and f32 accumulators: the int8 levels
+// (weights and activation hi/lo words) are exact in f16, every product is an
+// integer of magnitude <= 2^14, and one 32-block's dot (two k16 MMAs) stays
+// below 2^20, so the accumulator holds the exact int32 dot d (and e).  The
+// combine is then the same per-block f32 chain as every other path
+// ("kernels.rs" lk_q8_term / lk_q8_acc, partial b mod 4 in ascending block
+// order, (p0 + p2) + (p1 + p3)): the result has the same bits as the M = 1
+// kernels and the oracle.
+//
+// Fragments.  A warp owns a tile of 16 weight rows; its 32 lanes are 8
+// groups g of 4 lanes t.  Inside a 32-block the k order of both operands is
+// permuted the same way so that lane (g, t) reads 8 contiguous bytes:
+// physical bytes 8t..8t+3 are the first MMA's k slots {2t, 2t+1, 2t+8,
+// 2t+9}, bytes 8t+4..8t+7 the second MMA's.  The A fragment (weights) is rows
+// g and g+8, the B fragment (activations) is activation row g, and the
+// accumulator gives rows g, g+8 x activation rows 2t, 2t+1.  Activation rows
+// >= M read as zeros.  The int8 -> f16 step is exact: (0x6400 | (b ^ 0x80))
+// is the f16 1024 + b + 128, minus 1152.
+//
+// Data movement is the ring kernel's: weights stream through per-warp ring
+// slots by 1-D bulk copies (TMA) completing on mbarriers, every wait bounded.
+// A stage is one tile's slice of tk bytes of K: 16 copies of a weight row
+// slice into rows padded to tk + 32 bytes (rows g and g + 4 then fall in
+// different banks, so the warp's 8-byte reads take the minimum two
+// wavefronts) and 16 copies of the matching scale slices.  The activation
+// rows (int8 words, scales) are copied once per block into shared memory, row
+// stride K + 32 bytes for the same reason.  Tiles are dealt to warps across
+// the grid first (tile i -> block i mod grid, then warp), so small matrices
+// still spread over every SM.
+#include "lk_ring_kernel.cuh"
+
+namespace lkmma {
+
+using namespace lk;
+using namespace lkring;
+
+constexpr int TR = 16;          // weight rows per tile (the MMA's M)
+constexpr int TN = 8;           // activation rows per tile (the MMA's N)
+constexpr int MW = 16;          // warps per block at most
+constexpr int MST = 32;         // ring stages per block at most
+// barriers (one per stage + the activation's), abort flag, argmax keys [8][MW]
+constexpr unsigned MTAIL = 8 * (MST + 1) + 16 + 8 * TN * MW;
+
+struct MmaArgs {
+  lkh::GemvProblem p;
+  int nw;                  // warps per block
+  int depth;               // ring stages per warp
+  int gx;                  // blocks
+  long ntiles;             // ceil(N / 16)
+  unsigned tk;             // bytes of K per stage (multiple of 256)
+  unsigned rs;             // stage row stride (tk + 32)
+  unsigned srs;            // stage scale row stride (tk / 16 + 16)
+  unsigned s_off;          // scale area inside a stage (16 * rs)
+  unsigned stage_bytes;
+  unsigned ar;             // activation row stride, bytes (K + 32)
+  unsigned xsr;            // activation scale row stride, floats (K / 32 + 4)
+  unsigned a_lo, a_xs;     // offsets of the low words and the scales in the activation area
+  unsigned ring_off;
+  unsigned long long wait_ns;
+  unsigned long long pol_w;
+  int pdl;
+  int* err;
+  int l2_ahead;            // stages per warp requested into L2 beyond the ring at start
+};
+
+// int8 x 4 (b0 lowest) -> two f16x2: (b0, b1) and (b2, b3), exact.
+__device__ __forceinline__ void i8x4_to_h2(unsigned w, unsigned& lo, unsigned& hi) {
+  const unsigned u = w ^ 0x80808080u;
+  const unsigned a = __byte_perm(u, 0x64646464u, 0x4140);
+  const unsigned b = __byte_perm(u, 0x64646464u, 0x4342);
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+struct Frag8 {   // one 8-byte run of levels as the two MMAs' f16 pairs
+  unsigned m0lo, m0hi, m1lo, m1hi;
+};
+__device__ __forceinline__ Frag8 frag8(uint2 v) {
+  Frag8 f;
+  i8x4_to_h2(v.x, f.m0lo, f.m0hi);
+  i8x4_to_h2(v.y, f.m1lo, f.m1hi);
+  return f;
+}
+
+// d += A(16x16, rows g/g+8) * B(16x8, column g), f32 accumulate
+__device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                         unsigned b0, unsigned b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The block's exact dot for rows (g, g+8) x activation rows (2t, 2t+1).
+__device__ __forceinline__ void block_dot(float (&d)[4], const Frag8& wg, const Frag8& wg8, const Frag8& x) {
+  d[0] = d[1] = d[2] = d[3] = 0.f;
+  mma16816(d, wg.m0lo, wg8.m0lo, wg.m0hi, wg8.m0hi, x.m0lo, x.m0hi);
+  mma16816(d, wg.m1lo, wg8.m1lo, wg.m1hi, wg8.m1hi, x.m1lo, x.m1hi);
+}
+
+struct Tiles {
+  long base, stride, ntiles;
+  int nsl;
+};
+
+// Stage n of the calling warp: tile base + stride * (n / nsl), slice n % nsl.
+__device__ __forceinline__ void issue(const MmaArgs& ra, const Tiles& tl, long n, unsigned char* st, unsigned full,
+                                      unsigned long long pol, int lane) {
+  const lkh::GemvProblem& a = ra.p;
+  const long tile = tl.base + tl.stride * (n / tl.nsl);
+  const int c = (int)(n % tl.nsl);
+  const long row0 = tile * TR;
+  const int rows = a.N - row0 < TR ? (int)(a.N - row0) : TR;
+  const int k0 = c * (int)ra.tk;
+  const int len = a.K - k0 < (int)ra.tk ? a.K - k0 : (int)ra.tk;
+  if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)len * 17u / 16u);
+  __syncwarp();
+  const int r = lane & 15;
+  if (r < rows) {
+    const long row = row0 + r;
+    if (lane < 16)
+      bulk(st + r * ra.rs, a.wq + row * a.K + k0, (unsigned)len, full, pol);
+    else
+      bulk(st + ra.s_off + r * ra.srs, (const unsigned char*)a.ws + (row * (a.K >> 5) + (k0 >> 5)) * 2,
+           (unsigned)len / 16u, full, pol);
+  }
+  __syncwarp();
+}
+
+// Request the calling warp's stage n (the bytes issue() copies) into L2.
+__device__ __forceinline__ void prefetch(const MmaArgs& ra, const Tiles& tl, long n, int lane) {
+  const lkh::GemvProblem& a = ra.p;
+  const long tile = tl.base + tl.stride * (n / tl.nsl);
+  const int c = (int)(n % tl.nsl);
+  const long row0 = tile * TR;
+  const int rows = a.N - row0 < TR ? (int)(a.N - row0) : TR;
+  const int k0 = c * (int)ra.tk;
+  const int len = a.K - k0 < (int)ra.tk ? a.K - k0 : (int)ra.tk;
+  const int r = lane & 15;
+  if (r < rows) {
+    const long row = row0 + r;
+    if (lane < 16)
+      bulk_prefetch_l2(a.wq + row * a.K + k0, (unsigned)len);
+    else
+      bulk_prefetch_l2((const unsigned char*)a.ws + (row * (a.K >> 5) + (k0 >> 5)) * 2, (unsigned)len / 16u);
+  }
+}
+
+template <int Q>
+__global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const lkh::GemvProblem& a = ra.p;
+  const int nw = ra.nw, D = ra.depth, NS = nw * D;
+  const int M = a.M, K = a.K, nb = K >> 5;
+  unsigned char* act = smem;
+  unsigned char* ring = smem + ra.ring_off;
+  unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
+  volatile int* abort_flag = (volatile int*)(bars + MST + 1);
+  unsigned long long* keys = (unsigned long long*)(bars + MST + 3);  // [TN][MW]
+  const unsigned full0 = smem_u32(bars);
+  const unsigned act_bar = smem_u32(bars + MST);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+
+  Tiles tl;
+  tl.base = blockIdx.x + (long)ra.gx * warp;
+  tl.stride = (long)ra.gx * nw;
+  tl.ntiles = ra.ntiles;
+  tl.nsl = (K + (int)ra.tk - 1) / (int)ra.tk;
+  const long my_tiles = tl.base < tl.ntiles ? (tl.ntiles - 1 - tl.base) / tl.stride + 1 : 0;
+  const long T = my_tiles * tl.nsl;
+  const unsigned long long pol_w = ra.pol_w ? evict_first_policy() : 0ull;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(full0 + 8 * s, 1);
+    mbar_init(act_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (ra.pdl && threadIdx.x == 0) griddep_launch();
+
+  // weights do not depend on the previous kernel: start streaming at once
+  long issued = 0;
+  for (; issued < T && issued < D; ++issued)
+    issue(ra, tl, issued, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
+          pol_w, lane);
+  for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m) prefetch(ra, tl, m, lane);
+
+  if (ra.pdl) griddep_wait();
+  // the activation rows: int8 words (and low words) and scales, row-padded
+  if (warp == 0) {
+    const unsigned long long pol_a = evict_last_policy();
+    if (lane == 0)
+      mbar_arrive_expect_tx(act_bar, (unsigned)M * ((unsigned)K * (Q == 2 ? 2u : 1u) + (unsigned)nb * 4u));
+    __syncwarp();
+    if (lane < M) bulk(act + (size_t)lane * ra.ar, a.xq + (long)lane * K, (unsigned)K, act_bar, pol_a);
+    if (Q == 2 && lane >= 8 && lane < 8 + M)
+      bulk(act + ra.a_lo + (size_t)(lane - 8) * ra.ar, a.xl + (long)(lane - 8) * K, (unsigned)K, act_bar, pol_a);
+    if (lane >= 16 && lane < 16 + M)
+      bulk(act + ra.a_xs + (size_t)(lane - 16) * ra.xsr * 4, a.xs + (long)(lane - 16) * nb, (unsigned)nb * 4u,
+           act_bar, pol_a);
+    __syncwarp();
+  }
+  bool ok = __all_sync(FULL, mbar_wait(act_bar, 0, ra.wait_ns, abort_flag));
+  if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
+
+  // activation row g's words and the scales of activation rows 2t, 2t+1
+  const bool gx_ok = g < M;
+  const unsigned char* XH = act + (size_t)g * ra.ar + 8 * t;
+  const unsigned char* XL = act + ra.a_lo + (size_t)g * ra.ar + 8 * t;
+  const float* XS0 = (const float*)(act + ra.a_xs) + (size_t)(2 * t) * ra.xsr;
+  const float* XS1 = XS0 + ra.xsr;
+  const bool s0_ok = 2 * t < M, s1_ok = 2 * t + 1 < M;
+
+  float p[4][4];  // [partial q][element: (g,2t) (g,2t+1) (g+8,2t) (g+8,2t+1)]
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[q][e] = 0.f;
+  unsigned long long best0 = 0, best1 = 0;
+
+  long n = 0;
+  for (; ok && n < T; ++n) {
+    const int slot = warp * D + (int)(n % D);
+    if (!__all_sync(FULL, mbar_wait(full0 + 8 * slot, (unsigned)(n / D) & 1u, ra.wait_ns, abort_flag))) {
+      if (lane == 0) raise_error(ra.err, ERR_WAIT_FULL, abort_flag);
+      ok = false;
+      break;
+    }
+    unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
+    const int c = (int)(n % tl.nsl);
+    const int k0 = c * (int)ra.tk;
+    const int len = K - k0 < (int)ra.tk ? K - k0 : (int)ra.tk;
+    const unsigned char* W0 = st + g * ra.rs + 8 * t;
+    const unsigned char* W8 = W0 + 8 * ra.rs;
+    const unsigned char* S0 = st + ra.s_off + g * ra.srs;
+    const unsigned char* S8 = S0 + 8 * ra.srs;
+    const int b0 = k0 >> 5;
+    const int ngrp = len >> 7;  // groups of 4 blocks (partials 0..3)
+#pragma unroll 2
+    for (int gi = 0; gi < ngrp; ++gi) {
+      // scales of the group's 4 blocks: weight rows g, g+8; activation rows 2t, 2t+1
+      const uint2 sw0 = *(const uint2*)(S0 + 8 * gi);
+      const uint2 sw8 = *(const uint2*)(S8 + 8 * gi);
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 sx0 = s0_ok ? *(const float4*)(XS0 + b0 + 4 * gi) : z4;
+      const float4 sx1 = s1_ok ? *(const float4*)(XS1 + b0 + 4 * gi) : z4;
+      const float wa[4] = {__half2float(__ushort_as_half((unsigned short)(sw0.x & 0xffff))),
+                           __half2float(__ushort_as_half((unsigned short)(sw0.x >> 16))),
+                           __half2float(__ushort_as_half((unsigned short)(sw0.y & 0xffff))),
+                           __half2float(__ushort_as_half((unsigned short)(sw0.y >> 16)))};
+      const float wb[4] = {__half2float(__ushort_as_half((unsigned short)(sw8.x & 0xffff))),
+                           __half2float(__ushort_as_half((unsigned short)(sw8.x >> 16))),
+                           __half2float(__ushort_as_half((unsigned short)(sw8.y & 0xffff))),
+                           __half2float(__ushort_as_half((unsigned short)(sw8.y >> 16)))};
+      const float xa[4] = {sx0.x, sx0.y, sx0.z, sx0.w};
+      const float xb[4] = {sx1.x, sx1.y, sx1.z, sx1.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int bb = 4 * gi + q;  // block within the slice; b0 % 4 == 0, so partial q
+        const Frag8 fw0 = frag8(*(const uint2*)(W0 + 32 * bb));
+        const Frag8 fw8 = frag8(*(const uint2*)(W8 + 32 * bb));
+        const uint2 hv = gx_ok ? *(const uint2*)(XH + k0 + 32 * bb) : make_uint2(0u, 0u);
+        float d[4];
+        block_dot(d, fw0, fw8, frag8(hv));
+        const float ws_[4] = {wa[q], wa[q], wb[q], wb[q]};
+        const float xs_[4] = {xa[q], xb[q], xa[q], xb[q]};
+        if constexpr (Q == 1) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) p[q][e] = __fmaf_rn(__fmul_rn(ws_[e], xs_[e]), d[e], p[q][e]);
+        } else {
+          const uint2 lv = gx_ok ? *(const uint2*)(XL + k0 + 32 * bb) : make_uint2(0u, 0u);
+          float f[4];
+          block_dot(f, fw0, fw8, frag8(lv));
+          // q8_step<2> with the dots already in f32 (exact integers)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float u = __fmaf_rn(xs_[e], d[e], __fmul_rn(__fmul_rn(xs_[e], 0.0078125f), f[e]));
+            p[q][e] = __fmaf_rn(ws_[e], u, p[q][e]);
+          }
+        }
+      }
+    }
+    // the slot is free: refill it with this warp's stage n + D (generic-proxy
+    // reads ordered before the bulk copy's async-proxy writes)
+    __syncwarp();
+    if (issued < T) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(ra, tl, issued, st, full0 + 8 * slot, pol_w, lane);
+      ++issued;
+    }
+    if (c == tl.nsl - 1) {
+      // the tile is done: (p0 + p2) + (p1 + p3) per element ("kernels.rs" lk_q8_sum4)
+      const long tile = tl.base + tl.stride * (n / tl.nsl);
+      const long r0 = tile * TR + g, r8 = r0 + 8;
+      const int t0 = 2 * t, t1 = 2 * t + 1;
+      float yv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        yv[e] = __fadd_rn(__fadd_rn(p[0][e], p[2][e]), __fadd_rn(p[1][e], p[3][e]));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) p[q][e] = 0.f;
+      }
+      if (r0 < a.N) {
+        if (t0 < M) {
+          a.y[(long)t0 * a.N + r0] = yv[0];
+          const unsigned long long k = amax_key(yv[0], (unsigned)r0);
+          best0 = k > best0 ? k : best0;
+        }
+        if (t1 < M) {
+          a.y[(long)t1 * a.N + r0] = yv[1];
+          const unsigned long long k = amax_key(yv[1], (unsigned)r0);
+          best1 = k > best1 ? k : best1;
+        }
+      }
+      if (r8 < a.N) {
+        if (t0 < M) {
+          a.y[(long)t0 * a.N + r8] = yv[2];
+          const unsigned long long k = amax_key(yv[2], (unsigned)r8);
+          best0 = k > best0 ? k : best0;
+        }
+        if (t1 < M) {
+          a.y[(long)t1 * a.N + r8] = yv[3];
+          const unsigned long long k = amax_key(yv[3], (unsigned)r8);
+          best1 = k > best1 ? k : best1;
+        }
+      }
+    }
+  }
+  // drain: stages issued but not consumed (only after an abort) must land
+  // before the block may end
+  if (lane == 0) {
+    for (long m = n; m < issued; ++m)
+      drain_wait(full0 + 8 * (unsigned)(warp * D + m % D), (unsigned)(m / D) & 1u, ra.wait_ns, ra.err);
+    if (warp == 0) drain_wait(act_bar, 0, ra.wait_ns, ra.err);
+  }
+  __syncwarp();
+  if (a.amax) {
+    // per activation row: max over the lanes holding it (same t), then the block
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      const unsigned long long v0 = __shfl_xor_sync(FULL, best0, o);
+      const unsigned long long v1 = __shfl_xor_sync(FULL, best1, o);
+      best0 = v0 > best0 ? v0 : best0;
+      best1 = v1 > best1 ? v1 : best1;
+    }
+    if (g == 0) {
+      keys[(2 * t) * MW + warp] = best0;
+      keys[(2 * t + 1) * MW + warp] = best1;
+    }
+    __syncthreads();
+    if (threadIdx.x < M) {
+      unsigned long long m = 0;
+      for (int w = 0; w < nw; ++w) m = keys[threadIdx.x * MW + w] > m ? keys[threadIdx.x * MW + w] : m;
+      a.amax[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
+    }
+  }
+}
+
+struct MmaLayout {
+  unsigned tk, rs, srs, s_off, stage_bytes, ar, xsr, a_lo, a_xs, ring_off, total;
+  int nw, depth;
+};
+
+unsigned round_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
+
+// Widest tk (1024 or 512 bytes, or the option) that leaves room for >= 2
+// warps x 2 stages next to the activation area.
+MmaLayout mma_layout(const lkh::GemvProblem& p, int smem_optin) {
+  MmaLayout L{};
+  const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)p.M;
+  L.ar = K + 32u;
+  L.xsr = nb + 4u;
+  L.a_lo = round_up(M * L.ar, 128u);
+  L.a_xs = p.mode == LK_TWOPASS ? round_up(L.a_lo + M * L.ar, 128u) : L.a_lo;
+  L.ring_off = round_up(L.a_xs + M * L.xsr * 4u, 128u);
+  const unsigned cands[2] = {1024u, 512u};
+  for (int i = 0; i < 2; ++i) {
+    unsigned tk = lkh::opt_mma_tk > 0 ? (unsigned)lkh::opt_mma_tk : cands[i];
+    if (tk > round_up(K, 256u)) tk = round_up(K, 256u);
+    L.tk = tk;
+    L.rs = tk + 32u;
+    L.srs = tk / 16u + 16u;
+    L.s_off = TR * L.rs;
+    L.stage_bytes = round_up(L.s_off + TR * L.srs, 128u);
+    const long room = (long)smem_optin - (long)L.ring_off - (long)MTAIL;
+    int fit = room > 0 ? (int)(room / L.stage_bytes) : 0;
+    if (fit > MST) fit = MST;
+    int depth = lkh::opt_mma_depth > 0 ? (int)lkh::opt_mma_depth : 2;
+    int w = lkh::opt_mma_warps > 0 ? (int)lkh::opt_mma_warps : fit / depth;
+    if (w > MW) w = MW;
+    if (w * depth > fit) w = fit / depth;
+    L.nw = w;
+    L.depth = depth;
+    L.total = L.ring_off + (unsigned)(w * depth) * L.stage_bytes + MTAIL;
+    if (w >= 2 || lkh::opt_mma_tk > 0) break;
+  }
+  return L;
+}
+
+bool mma_layout_ok(const MmaLayout& L) { return L.nw >= 1 && L.depth >= 1 && L.nw * L.depth >= 2; }
+
+typedef void (*mma_fn)(const MmaArgs);
+
+}  // namespace lkmma
+
+namespace lkh {
+
+using namespace lkmma;
+
+bool mma_supports(const GemvProblem& p) {
+  if (p.mode != LK_INT8ACT && p.mode != LK_TWOPASS) return false;
+  if (p.split || p.fuse) return false;
+  const int min_m = opt_mma_min_m > 0 ? (int)opt_mma_min_m : 2;
+  if (p.M < min_m || p.M > TN) return false;
+  if (p.K < 256 || p.K % 256 || p.N < 1) return false;
+  if (!aligned(p.ws, 16) || !aligned(p.xq, 16) || !aligned(p.xs, 16) || (p.mode == LK_TWOPASS && !aligned(p.xl, 16)))
+    return false;
+  const DeviceInfo* d = device_info(nullptr);
+  if (!d) return false;
+  return mma_layout_ok(mma_layout(p, d->smem_optin));
+}
+
+lk_status mma_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
+  const DeviceInfo* d = device_info(nullptr);
+  if (!d) return LK_ERR_CUDA;
+  const MmaLayout L = mma_layout(p, d->smem_optin);
+  if (!mma_layout_ok(L)) return LK_ERR_SHAPE;
+  mma_fn f = p.mode == LK_TWOPASS ? gemv_mma_kernel<2> : gemv_mma_kernel<1>;
+  // (the cap is the device's maximum: see ring_gemv)
+  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) != cudaSuccess)
+    return LK_ERR_CUDA;
+  MmaArgs ra;
+  ra.p = p;
+  ra.nw = L.nw;
+  ra.depth = L.depth;
+  ra.ntiles = (p.N + TR - 1) / TR;
+  long gx = opt_grid_ctas > 0 ? opt_grid_ctas : d->sm_count;
+  if (gx > ra.ntiles) gx = ra.ntiles;
+  ra.gx = (int)gx;
+  ra.tk = L.tk;
+  ra.rs = L.rs;
+  ra.srs = L.srs;
+  ra.s_off = L.s_off;
+  ra.stage_bytes = L.stage_bytes;
+  ra.ar = L.ar;
+  ra.xsr = L.xsr;
+  ra.a_lo = L.a_lo;
+  ra.a_xs = L.a_xs;
+  ra.ring_off = L.ring_off;
+  ra.wait_ns = opt_wait_us > 0 ? (unsigned long long)opt_wait_us * 1000ull : 2000000000ull;
+  ra.pol_w = opt_ring_hint ? 1ull : 0ull;
+  ra.pdl = opt_pdl ? 1 : 0;
+  ra.err = error_word_ptr();
+  if (!ra.err) return LK_ERR_CUDA;
+  ra.l2_ahead = (int)(opt_l2_ahead_kb * 1024 / ((long)L.nw * L.stage_bytes));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)gx);
+  cfg.blockDim = dim3(L.nw * 32);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ra.pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, f, ra) != cudaSuccess) return LK_ERR_CUDA;
+  if (n_parts) *n_parts = (int)gx;
+  return launch_status();
+}
+
+}  // namespace lkh

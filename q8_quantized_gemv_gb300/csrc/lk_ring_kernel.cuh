@@ -41,6 +41,7 @@ struct RingArgs {
   int pdl;                 // launched as a programmatic dependent of the previous kernel
   int* err;                // the device error word
   unsigned long long* trace;  // block 0's timestamps (option "trace"), or NULL
+  int l2_ahead;            // stages per warp requested into L2 beyond the ring at start
 };
 
 typedef void (*ring_fn)(const RingArgs);
@@ -138,6 +139,12 @@ __device__ __forceinline__ void bulk(void* dst, const void* src, unsigned bytes,
                                      unsigned long long policy) {
   if (policy) bulk_g2s(dst, src, bytes, bar, policy);
   else bulk_g2s_nohint(dst, src, bytes, bar);
+}
+
+// Request `bytes` at `src` into L2 (no completion to wait for).  src 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -338,6 +345,31 @@ __device__ __forceinline__ void issue_stage(const Geom& g, int warp, int nwc, lo
   __syncwarp();
 }
 
+// Request this warp's stage n (the bytes issue_stage copies) into L2.
+__device__ __forceinline__ void prefetch_stage(const Geom& g, int warp, int nwc, long n, int lane) {
+  const long qi = warp + (long)nwc * (n / g.nsl);
+  const int c = (int)(n % g.nsl);
+  const long row0 = g.r0 + QR * qi;
+  const int rows = g.r1 - row0 < QR ? (int)(g.r1 - row0) : QR;
+  const int k0 = g.k_lo + c * g.tk;
+  const int len = (g.k_hi - k0 < g.tk) ? g.k_hi - k0 : g.tk;
+  if (g.whole) {
+    if (lane == 0) {
+      bulk_prefetch_l2(g.wq + row0 * g.K, rows * g.K);
+      bulk_prefetch_l2(g.ws + row0 * g.nb * 2, rows * g.nb * 2);
+    }
+  } else {
+    const int b0 = k0 >> 5, b1 = b0 + (len >> 5);
+    const unsigned sh = (unsigned)(b0 & 7) * 2u;
+    const unsigned slen = ((b1 - b0) * 2u + sh + 15u) & ~15u;
+    if (lane < rows) {
+      const long row = row0 + lane;
+      bulk_prefetch_l2(g.wq + row * g.K + k0, len);
+      bulk_prefetch_l2(g.ws + ((row * g.nb + b0) * 2 - sh), slen);
+    }
+  }
+}
+
 // The activation area of M rows over `L` bytes of K: int8 words (and low
 // words) and f32 scales, or f32 values under Dequant.
 struct Act {
@@ -498,6 +530,9 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   for (; issued < T && issued < D; ++issued)
     issue_stage(g, warp, nwc, issued, ring + (size_t)(warp * D + issued % D) * ra.stage_bytes,
                 full0 + 8 * (warp * D + (int)(issued % D)), pol_w, lane);
+  // the next stages into L2, so that HBM keeps streaming while the block
+  // waits for the previous kernel and runs its prologue
+  for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m) prefetch_stage(g, warp, nwc, m, lane);
 
   if (ra.pdl) griddep_wait();  // from here on: reads of activations, writes of outputs
   if (ra.trace && blockIdx.x == 0 && threadIdx.x == 0) ra.trace[1] = gtimer();

@@ -24,7 +24,7 @@ from . import lk, synth
 class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
                  batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
-                 fused=True, chain=False):
+                 fused=True, chain=False, group_qkv=True):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
         dev = self.dev
@@ -55,17 +55,32 @@ class DecodeStack:
         self.parts = torch.zeros((B * lk.lk_argmax_parts_max(vocab),), dtype=torch.int64, device=dev)
         self.idx = torch.empty((B,), dtype=torch.int32, device=dev)
         self.n_parts = 0
-        # one launch per projection (norm/quantize prologue inside the GEMV)
-        # wherever the ring kernel takes the shape; else norm/quantize kernels
-        # followed by lk_gemv_q8
+        # one launch per projection (norm/quantize prologue inside the ring
+        # GEMV) wherever the ring kernel takes the shape and lk_gemv_q8 would
+        # not pick the tensor-core kernel (2..8 rows); else norm/quantize
+        # kernels followed by lk_gemv_q8
         shapes = dict(self.shapes, lm=(vocab, hidden))
-        self.fused = {n: bool(fused) and lk.lk_gemv_kernel_for(N, K, self.mode, B, 0) == 2
-                      for n, (N, K) in shapes.items()}
-        # the whole token as one cooperative chain launch, where every step fits
-        self.x_buf = self.x0.clone()
+        self.kernel = {n: lk.lk_gemv_kernel_for(N, K, self.mode, B, 0) for n, (N, K) in shapes.items()}
+        prev = lk.lk_get_option("gemv_path")
+        lk.lk_set_option("gemv_path", 2)
+        ring = {n: lk.lk_gemv_kernel_for(N, K, self.mode, B, 0) == 2 for n, (N, K) in shapes.items()}
+        lk.lk_set_option("gemv_path", prev)
+        self.fused = {n: bool(fused) and ring[n] and self.kernel[n] != 3 for n in shapes}
+        # the whole token as one cooperative chain launch (the ring kernel's
+        # fused steps), where every step fits
+        self.x_buf = self.x0.clone()  # the token's input rows
         self.chain = None
-        if chain and all(self.fused.values()):
+        if chain and fused and all(ring.values()):
             self.chain = lk.Chain(self._chain_ops(), dev)
+        # q, k and v of a layer as one grouped launch (a chain without
+        # barriers: one prologue, the three weight streams back to back)
+        self.qkv = None
+        if self.chain is None and group_qkv and all(self.fused[n] for n in ("q", "k", "v")):
+            self.qkv = []
+            for l, w in enumerate(self.layers):
+                x = self.x_buf if l == 0 else self.h
+                self.qkv.append(lk.Chain([lk.chain_op(w[n][0], w[n][1], x, self.out[n], gain=w["g_attn"])
+                                          for n in ("q", "k", "v")], dev))
 
     def _act_bufs(self, K):
         B = self.B
@@ -120,34 +135,43 @@ class DecodeStack:
         """Launch one token's sequence on the current stream and return the
         device int32 [B] argmax.  ``hook``, if given, is called as
         hook(name, launch) around each GEMV launch (for per-kernel timing)."""
+        if x_in is not None and x_in.data_ptr() != self.x_buf.data_ptr():
+            self.x_buf.copy_(x_in)
         if self.chain is not None and hook is None:
-            if x_in is not None and x_in.data_ptr() != self.x_buf.data_ptr():
-                self.x_buf.copy_(x_in)
             lk.lk_gemv_chain(self.chain, self.mode, self.B, self.eps)
             return self.idx
 
-        def g(name, w, y, x, gain, parts=None):
+        def g(name, w, y, x, gain, parts=None, acts=None):
+            """Launch one projection; returns (launch result, the activation
+            arguments it used when not fused)."""
             if self.fused[name]:
                 def launch():
                     return lk.lk_rmsnorm_quant_gemv_q8(w[0], w[1], self.mode, x, y, gain=gain, eps=self.eps,
                                                        argmax_parts=parts)
+                a = None
             else:
-                a = self._norm(x, gain) if gain is not None else self._quant(x)
+                a = acts if acts is not None else (self._norm(x, gain) if gain is not None else self._quant(x))
 
                 def launch():
                     return self._gemv(w, y, a, parts)
-            return launch() if hook is None else hook(name, launch)
+            return (launch() if hook is None else hook(name, launch)), a
 
-        x = self.x0 if x_in is None else x_in
-        for w in self.layers:
-            g("q", w["q"], self.out["q"], x, w["g_attn"])
-            g("k", w["k"], self.out["k"], x, w["g_attn"])
-            g("v", w["v"], self.out["v"], x, w["g_attn"])
+        x = self.x_buf
+        for l, w in enumerate(self.layers):
+            if self.qkv is not None:
+                def launch(c=self.qkv[l]):
+                    return lk.lk_gemv_chain(c, self.mode, self.B, self.eps)
+                launch() if hook is None else hook("qkv", launch)
+            else:
+                # q, k and v read the same normed activation: quantized once
+                _, a = g("q", w["q"], self.out["q"], x, w["g_attn"])
+                g("k", w["k"], self.out["k"], x, w["g_attn"], acts=a if not self.fused["k"] else None)
+                g("v", w["v"], self.out["v"], x, w["g_attn"], acts=a if not self.fused["v"] else None)
             g("o", w["o"], self.out["o"], w["o_in"], None)
             g("gu", w["gu"], self.out["gu"], self.out["o"], w["g_mlp"])
             g("down", w["down"], self.h, w["d_in"], None)
             x = self.h
-        self.n_parts = g("lm", self.lm, self.logits, x, self.g_final, self.parts)
+        self.n_parts, _ = g("lm", self.lm, self.logits, x, self.g_final, self.parts)
         lk.lk_argmax(self.idx, self.B, self.V, parts=self.parts, n_parts=self.n_parts)
         return self.idx
 
@@ -167,7 +191,8 @@ class DecodeStack:
             return 1
         n = 1  # argmax reduce
         f = self.fused
-        per_layer = 6 + (0 if f["q"] else 1) + (0 if f["k"] else 1) + (0 if f["v"] else 1) \
+        qkv_norm = 0 if (f["q"] and f["k"] and f["v"]) else 1  # one shared norm for q, k, v
+        per_layer = (4 if self.qkv is not None else 6) + qkv_norm \
             + (0 if (f["o"] or self.mode == lk.LK_DEQUANT) else 1) + (0 if f["gu"] else 1) \
             + (0 if (f["down"] or self.mode == lk.LK_DEQUANT) else 1)
         return n + self.L * per_layer + 1 + (0 if f["lm"] else 1)

@@ -80,3 +80,14 @@ def assert_gemv_close(y_gpu, y_or, wq, ws, x_np, mode, rows=None, exact_quantize
     mag = oracle.absdot(wq, ws, x_np, rows=rows)
     err = np.abs(y_gpu.astype(np.float64) - y_or.astype(np.float64))
     assert np.all(err <= TOL * mag + 1e-30), float((err / np.maximum(mag, 1e-30)).max())
+
+
+def ring_takes(N, K, mode, M):
+    """Whether the bulk-copy ring kernel (the fused prologue's kernel) takes
+    this shape, whatever kernel lk_gemv_q8 would pick for it."""
+    prev = lk.lk_get_option("gemv_path")
+    lk.lk_set_option("gemv_path", 2)
+    try:
+        return lk.lk_gemv_kernel_for(N, K, mode, M, 0) == 2
+    finally:
+        lk.lk_set_option("gemv_path", prev)

@@ -125,3 +125,16 @@ def test_options(lib):
         lk.lk_set_option("gemv_path", 7)
     with pytest.raises(lk.LkError):
         lk.lk_set_option("no_such_option", 1)
+
+
+@pytest.mark.parametrize("name,good,bad", [("gemv_path", [0, 3], [-1, 4]), ("mma_min_m", [0, 2, 9], [-1, 10]),
+                                           ("mma_tk", [0, 256, 1024, 8192], [100, 8448, -256]),
+                                           ("mma_warps", [0, 1, 16], [17, -1]), ("mma_depth", [0, 1, 8], [9, -1])])
+def test_tensor_core_options(lib, name, good, bad):
+    for v in good:
+        lk.lk_set_option(name, v)
+        assert lk.lk_get_option(name) == v
+    for v in bad:
+        with pytest.raises(lk.LkError):
+            lk.lk_set_option(name, v)
+    lk.lk_set_option(name, 0)

@@ -116,3 +116,31 @@ def test_chain_barrier_timeout_is_reported_and_recoverable():
     torch.cuda.synchronize()
     assert lk.lk_device_error(reset=True) == 0
     assert torch.equal(a.logits.view(torch.int32), ref.view(torch.int32))
+
+
+def test_grouped_qkv_pdl_graph_matches_plain():
+    """The per-launch sequence with q, k, v as one grouped launch: captured
+    with programmatic dependent launches in a graph, it gives the same bits
+    as launched plainly, and the oracle's token."""
+    a = DecodeStack(**SMALL, batch=1, mode=1, chain=False)
+    assert a.qkv is not None
+    lk.lk_set_option("pdl", 0)
+    a.run_token()
+    torch.cuda.synchronize()
+    ref = a.logits.clone()
+    _, hx, logits = oracle_token(a)
+    assert np.array_equal(bits(host(ref)), bits(logits))
+    lk.lk_set_option("pdl", 1)
+    try:
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            a.run_token()
+        for _ in range(3):
+            a.logits.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(a.logits.view(torch.int32), ref.view(torch.int32))
+    finally:
+        lk.lk_set_option("pdl", 0)
+    assert lk.lk_device_error(reset=True) == 0

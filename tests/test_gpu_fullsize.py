@@ -157,3 +157,31 @@ def test_lm_head_argmax_planted_ties(mode):
     lk.lk_argmax(idx, 1, N, parts=parts, n_parts=n)
     torch.cuda.synchronize()
     assert int(host(idx)[0]) == 0 and not host(y).any()
+
+
+@pytest.mark.parametrize("mode", [I8, TP])
+@pytest.mark.parametrize("name,N,K", [("q", 4096, 4096), ("kv", 1024, 4096), ("gate_up", 24576, 4096),
+                                      ("down", 4096, 12288), ("lm_head", 151936, 4096)])
+def test_batch8_sequence_projections(mode, name, N, K):
+    """The 36-layer sequence's projections at batch 8, in the kernel the
+    library picks for 8 rows (the tensor-core kernel where it applies), with
+    the lm-head's argmax epilogue for all 8 rows."""
+    M = 8
+    x = synth.activation(M, K, synth.SEED_BASE + 40 + K, outliers=True)
+    g = synth.norm_gain(K, synth.SEED_BASE + 41)
+    wq_d, ws_d = weights(N, K, synth.SEED_BASE + 400 + N + K)
+    acts, yn = norm_quant(x, g, mode)
+    y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    parts = torch.zeros((M * lk.lk_argmax_parts_max(N),), dtype=torch.int64, device=DEV)
+    n = lk.lk_gemv_q8(wq_d, ws_d, mode, y, M=M, argmax_parts=parts, **acts)
+    idx = torch.full((M,), -1, dtype=torch.int32, device=DEV)
+    lk.lk_argmax(idx, M, N, parts=parts, n_parts=n)
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) == 0
+    check_rows(y, wq_d, ws_d, mode, yn, sample_rows(N, 10 + N))
+    logits = host(y)
+    assert host(idx).tolist() == [oracle.argmax(logits[t]) for t in range(M)]
+    y2 = torch.empty_like(y)
+    lk.lk_gemv_q8(wq_d, ws_d, mode, y2, M=M, **acts)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), y2.view(torch.int32))

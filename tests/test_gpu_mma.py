@@ -1,0 +1,136 @@
+"""The tensor-core GEMV (2..8 activation rows, Int8Act and TwoPassInt8)
+against the CPU oracle, bit for bit: every row count, ragged N (a partial
+last 16-row tile) and ragged K (a partial last stage slice), and every stage
+layout the options allow (bytes of K per stage, warps, stages per warp), so
+that each ring arrangement and tail path is exercised; plus the argmax
+epilogue and the shapes it declines."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from gpuhelp import DEV, bits, dev_acts, gpu_gemv, host, oracle_acts, to_dev  # noqa: E402
+from q8_quantized_gemv_gb300 import build, lk, synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+I8, TP = 1, 2
+OPTS = ("mma_tk", "mma_warps", "mma_depth", "grid_ctas", "gemv_path")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    yield
+    for o in OPTS:
+        lk.lk_set_option(o, 0)
+
+
+@pytest.fixture(autouse=True)
+def _reset():
+    lk.lk_set_option("gemv_path", 3)
+    yield
+    for o in OPTS:
+        lk.lk_set_option(o, 0)
+
+
+def run_case(N, K, M, mode, seed, amax=False):
+    assert lk.lk_gemv_kernel_for(N, K, mode, M, 0) == 3
+    wq, ws = synth.q8_matrix(N, K, seed)
+    x = synth.activation(M, K, seed + 1, outliers=True)
+    y_or = oracle.gemv(wq, ws, mode, **oracle_acts(x, mode))
+    y, parts, n = gpu_gemv(to_dev(wq), to_dev(ws), mode, dev_acts(x, mode), M, amax=amax)
+    idx = None
+    if amax:
+        idx = torch.full((M,), -1, dtype=torch.int32, device=DEV)
+        lk.lk_argmax(idx, M, N, parts=parts, n_parts=n)
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) == 0
+    yg = host(y)
+    bad = np.nonzero(bits(yg) != bits(y_or))
+    assert bad[0].size == 0, f"{bad[0].size} mismatches, first (row, col) {bad[0][0]}, {bad[1][0]}: " \
+                             f"{yg[bad[0][0], bad[1][0]]} vs {y_or[bad[0][0], bad[1][0]]}"
+    if amax:
+        assert host(idx).tolist() == [oracle.argmax(y_or[t]) for t in range(M)]
+    return y
+
+
+@pytest.mark.parametrize("mode", [I8, TP])
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("N,K", [(16, 256), (1000, 1280), (333, 4096), (2500, 2304)])
+def test_mma_rows_and_tails(mode, M, N, K):
+    run_case(N, K, M, mode, 7000 + N + K + M)
+
+
+@pytest.mark.parametrize("mode", [I8, TP])
+@pytest.mark.parametrize("tk,warps,depth", [(256, 0, 0), (512, 0, 0), (1024, 0, 0), (2048, 0, 0),
+                                            (1024, 1, 2), (1024, 3, 1), (512, 16, 1), (256, 4, 4),
+                                            (1024, 2, 3)])
+def test_mma_stage_layouts(mode, tk, warps, depth):
+    lk.lk_set_option("mma_tk", tk)
+    lk.lk_set_option("mma_warps", warps)
+    lk.lk_set_option("mma_depth", depth)
+    run_case(777, 3328, 8, mode, 7100 + tk + warps)
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 152])
+def test_mma_grid_sizes(ctas):
+    lk.lk_set_option("grid_ctas", ctas)
+    run_case(4100, 1024, 5, I8, 7200 + ctas)
+
+
+@pytest.mark.parametrize("mode", [I8, TP])
+def test_mma_argmax_with_ties(mode):
+    N, K, M = 3001, 512, 8
+    wq, ws = synth.q8_matrix(N, K, 7300)
+    x = synth.activation(M, K, 7301)
+    dom = (127 * np.sign(x[3])).astype(np.int8)
+    for i in (15, 16, 2999):   # tile boundary, then the ragged last tile
+        wq[i] = dom
+        ws[i] = np.float16(1.0).view(np.uint16)
+    y_or = oracle.gemv(wq, ws, mode, **oracle_acts(x, mode))
+    y, parts, n = gpu_gemv(to_dev(wq), to_dev(ws), mode, dev_acts(x, mode), M, amax=True)
+    idx = torch.full((M,), -1, dtype=torch.int32, device=DEV)
+    lk.lk_argmax(idx, M, N, parts=parts, n_parts=n)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(y)), bits(y_or))
+    want = [oracle.argmax(y_or[t]) for t in range(M)]
+    assert want[3] == 15
+    assert host(idx).tolist() == want
+
+
+def test_mma_matches_batch1_kernel_bits():
+    """Each of the 8 rows through the batch-1 kernel gives the same bits."""
+    N, K, M = 600, 4096, 8
+    wq, ws = synth.q8_matrix(N, K, 7400)
+    x = synth.activation(M, K, 7401, outliers=True)
+    wq_d, ws_d = to_dev(wq), to_dev(ws)
+    for mode in (I8, TP):
+        lk.lk_set_option("gemv_path", 3)
+        yb, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M)
+        lk.lk_set_option("gemv_path", 0)
+        for t in range(M):
+            y1, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x[t:t + 1], mode), 1)
+            assert np.array_equal(bits(host(y1))[0], bits(host(yb))[t])
+
+
+def test_mma_declines():
+    lk.lk_set_option("gemv_path", 0)
+    assert lk.lk_gemv_kernel_for(4096, 4096, 1, 8, 0) == 3
+    assert lk.lk_gemv_kernel_for(4096, 4096, 0, 8, 0) != 3   # Dequant
+    assert lk.lk_gemv_kernel_for(4096, 4096, 1, 1, 0) != 3   # one row
+    assert lk.lk_gemv_kernel_for(4096, 4128, 1, 8, 0) != 3   # K % 256 != 0
+    assert lk.lk_gemv_kernel_for(4096, 4096, 1, 8, 2) != 3   # split-K
+    # TwoPass activations of 8 rows x 12288 (209 KB) leave room for one warp's
+    # two 512-byte stages: still taken
+    assert lk.lk_gemv_kernel_for(4096, 12288, 2, 8, 0) == 3
+    # ... but not with 4 KB stages forced
+    lk.lk_set_option("mma_tk", 4096)
+    assert lk.lk_gemv_kernel_for(4096, 12288, 2, 8, 0) != 3
+    lk.lk_set_option("mma_tk", 0)
+    lk.lk_set_option("mma_min_m", 9)
+    assert lk.lk_gemv_kernel_for(4096, 4096, 1, 8, 0) != 3
+    lk.lk_set_option("mma_min_m", 0)

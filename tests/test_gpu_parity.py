@@ -12,13 +12,13 @@ import oracle  # noqa: E402
 from casebuild import (MODES, block_case, lo_case, order_records,  # noqa: E402
                        quantizer_records)
 from gpuhelp import (DEV, act_buffers, assert_gemv_close, bits, dev_acts,  # noqa: E402
-                     gpu_gemv, gpu_quantize, host, oracle_acts, to_dev)
+                     gpu_gemv, gpu_quantize, host, oracle_acts, ring_takes, to_dev)
 from q8_quantized_gemv_gb300 import build, lk, synth  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
 DQ, I8, TP = 0, 1, 2
-PATHS = {"direct": 1, "ring": 2}
+PATHS = {"direct": 1, "ring": 2, "mma": 3}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,9 +40,13 @@ def path(request):
 
 def need(path, K, N=64, mode=1, M=1, S=0):
     """Skip the ring-path case when the ring kernel does not take the shape
-    (K % 256 != 0, or the activation does not fit in shared memory)."""
+    (K % 256 != 0, or the activation does not fit in shared memory), and the
+    tensor-core case outside its domain (quantized modes, 2..8 rows, no
+    split-K)."""
     if path == "ring" and lk.lk_gemv_kernel_for(N, K, mode, M, S) != 2:
         pytest.skip("shape not taken by the ring kernel")
+    if path == "mma" and (S > 0 or lk.lk_gemv_kernel_for(N, K, mode, M, 0) != 3):
+        pytest.skip("shape not taken by the tensor-core kernel")
 
 
 def sync_check():
@@ -163,8 +167,11 @@ def test_gemv_batch_invariance(path, mode):
     N, K, M = 300, 2048, 8
     wq, ws = synth.q8_matrix(N, K, 4100)
     x = synth.activation(M, K, 4101, outliers=True)
+    need(path, K, N, mode, M)
     wq_d, ws_d = to_dev(wq), to_dev(ws)
     yb, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M)
+    if path == "mma":  # single rows through the default (batch-1) kernel
+        lk.lk_set_option("gemv_path", 0)
     for t in range(M):
         y1, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x[t:t + 1], mode), 1)
         assert np.array_equal(bits(host(y1))[0], bits(host(yb))[t])
@@ -176,22 +183,34 @@ def test_gemv_batch_invariance(path, mode):
 def test_gemv_order_fixture_on_gpu(path, name, mode):
     rec = order_records()[name]
     K = int(rec["K"])
-    pad = -(-K // 256) * 256 if path == "ring" else None  # zero-weight blocks up to K % 256 == 0
+    pad = -(-K // 256) * 256 if path != "direct" else None  # zero-weight blocks up to K % 256 == 0
     wq, ws, x = block_case(K, rec["blocks"], pad_to=pad)
     m = MODES[mode]
-    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), 1)
+    x, M = fixture_rows(path, m, x)
+    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), M)
     sync_check()
-    assert host(y)[0, 0] == np.float32(rec[f"y_{mode}"])
+    assert host(y)[:, 0].tolist() == [np.float32(rec[f"y_{mode}"])] * M
+
+
+def fixture_rows(path, mode, x):
+    """The tensor-core kernel takes 2..8 rows of quantized activations: the
+    one-row fixtures run there as two equal rows."""
+    if path == "mma":
+        if mode == DQ:
+            pytest.skip("Dequant is not a tensor-core mode")
+        return np.repeat(x, 2, axis=0), 2
+    return x, 1
 
 
 @pytest.mark.parametrize("mode", ["dequant", "int8act", "twopass"])
 def test_gemv_low_word_fixture_on_gpu(path, mode):
     rec = order_records()["gemv_lo"]
-    wq, ws, x = lo_case(rec, pad_to=256 if path == "ring" else None)
+    wq, ws, x = lo_case(rec, pad_to=256 if path != "direct" else None)
     m = MODES[mode]
-    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), 1)
+    x, M = fixture_rows(path, m, x)
+    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), M)
     sync_check()
-    assert host(y)[0, 0] == np.float32(rec[f"y_{mode}"])
+    assert host(y)[:, 0].tolist() == [np.float32(rec[f"y_{mode}"])] * M
 
 
 def test_gemv_k_zero_and_empty():
@@ -283,6 +302,7 @@ def test_argmax_logits(N, M):
 @pytest.mark.parametrize("mode", [DQ, I8, TP])
 def test_gemv_argmax_epilogue_planted_ties(path, mode):
     N, K, M = 5000, 256, 2
+    need(path, K, N, mode, M)
     wq, ws = synth.q8_matrix(N, K, 6000)
     x = synth.activation(M, K, 6001)
     # one dominant row (levels 127*sign of activation row 0, scale 1.0) copied
@@ -332,7 +352,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 @pytest.mark.parametrize("N,K,norm", [(300, 1280, True), (1000, 4096, True), (77, 256, False),
                                       (64, 12288, False), (5, 2048, True)])
 def test_fused_norm_quant_gemv(pdl, mode, M, N, K, norm):
-    if lk.lk_gemv_kernel_for(N, K, mode, M, 0) != 2:
+    if not ring_takes(N, K, mode, M):
         pytest.skip("activation area does not fit the ring kernel")
     lk.lk_set_option("pdl", pdl)
     try:
@@ -351,7 +371,7 @@ def test_fused_norm_quant_gemv(pdl, mode, M, N, K, norm):
         sync_check()
         assert_gemv_close(host(y), y_or, wq, ws, xa, mode)
         assert host(idx).tolist() == [oracle.argmax(y_or[t]) for t in range(M)]
-        # the same bits as the unfused launches
+        # the same bits as the unfused launches (for 2..8 rows: the tensor-core kernel)
         if mode != DQ:
             y2 = torch.zeros_like(y)
             xq, xl, xs = act_buffers(M, K, mode)
