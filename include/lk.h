@@ -56,6 +56,7 @@ typedef int lk_status;
 
 #define LK_MAX_M      8   /* activation rows that share one weight read */
 #define LK_MAX_SPLITK 64  /* split-K chunks */
+#define LK_MAX_GROUP  4   /* matrices of one lk_gemv_q8_group call */
 
 /* A static, human-readable name of a status. */
 const char* lk_status_string(lk_status s);
@@ -122,6 +123,32 @@ lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq
 lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
                      const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
                      float* y, uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream);
+
+/* One matrix of a grouped GEMV. */
+typedef struct {
+  const int8_t* wq;        /* [N][K] levels                                         */
+  const uint16_t* ws;      /* [N][K/32] f16 scales                                  */
+  int N;
+  int reserved;
+  float* y;                /* [M][N] output                                         */
+} lk_gemv_target;
+
+/*
+ * Several GEMVs that read the same activation (the q, k and v projections
+ * of a decoder layer, "kernels.rs" GEMV_Q8 applied per matrix): the same as
+ * calling lk_gemv_q8 for each target in turn, without argmax, and with the
+ * same bits.  Where the tensor-core kernel takes the shape (lk_gemv_kernel_for
+ * of the first target == 3) the group is ONE launch whose 16-row tiles of all
+ * matrices are dealt over the grid together; otherwise one launch per target.
+ * The library extends the pages here; they have no grouped call.
+ *   targets  HOST array of n (1..LK_MAX_GROUP) matrices with the same K;
+ *            read during the call only (a captured graph keeps the values).
+ *   other arguments as lk_gemv_q8.
+ * Errors: LK_ERR_ARG for n out of range or a null target field, and every
+ * error lk_gemv_q8 reports for a target.
+ */
+lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
+                           const int8_t* xq, const int8_t* xl, const float* xs, int M, cudaStream_t stream);
 
 /*
  * RMSNorm -> quantize -> GEMV in one launch: every block of the bulk-copy
@@ -304,15 +331,27 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 a barrier; default 0 = off)
  *   "trace"       1: the ring and chain kernels write block 0's timestamps
  *                 to the trace buffer (lk_trace_read); 2: the chain also
- *                 records every block's and block 0's warps' step ends
+ *                 records every block's and block 0's warps' step ends;
+ *                 3: launch timeline: every ring, chain and tensor-core
+ *                 launch made after the option was set owns a record of 8
+ *                 entries (in launch order, 512 records, wrapping):
+ *                 [0] block 0 start, [1] block 0 past the wait on the
+ *                 previous kernel, [2] block 0's activation ready, [3] the
+ *                 last block's end, [4] block 0's end (all %globaltimer ns),
+ *                 [5] kernel (1 ring, 2 chain, 3 tensor-core), [6] rows
+ *                 (steps, for a chain).  Setting the option restarts the
+ *                 record count.
  *   "wait_us"     time limit of every device-side wait, microseconds
  *                 (0 = default, 2 s)
  *   "mma_min_m"   fewest activation rows lk_gemv_q8 runs on the tensor-core
  *                 kernel (0 = default 2; 9 = never)
- *   "mma_tk"      its bytes of K per ring stage: 0 auto (1024, else 512),
+ *   "mma_tk"      its bytes of K per ring stage: 0 auto (512, else 256),
  *                 else a multiple of 256 up to 8192
  *   "mma_warps"   its warps per block: 0 auto, else 1..16
- *   "mma_depth"   its ring stages per warp: 0 = 2, else 1..8
+ *   "mma_depth"   its ring stages per warp: 0 = 1, else 1..8
+ *   "mma_act16"   its activation rows held in shared memory as f16 (0 auto:
+ *                 where that leaves room for 8 warps; 1 whenever they fit;
+ *                 2 never: int8, converted per use)
  *   "l2_ahead_kb" ring and tensor-core kernels: KB per block of the stages
  *                 after the ring's first fill requested into L2 at kernel
  *                 start (cp.async.bulk.prefetch.L2), so that HBM keeps

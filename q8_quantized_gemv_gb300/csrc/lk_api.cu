@@ -26,6 +26,7 @@ long opt_mma_tk = 0;
 long opt_mma_warps = 0;
 long opt_mma_depth = 0;
 long opt_l2_ahead_kb = 0;
+long opt_mma_act16 = 0;
 
 static const int kMaxDevices = 64;
 static DeviceInfo g_info[kMaxDevices];
@@ -158,8 +159,9 @@ lk_status lk_set_option(const char* name, long value) {
     if (value < 0 || value > 65536) return LK_ERR_ARG;
     opt_l2_prefetch_kb = value;
   } else if (!strcmp(name, "trace")) {
-    if (value < 0 || value > 2) return LK_ERR_ARG;
+    if (value < 0 || value > 3) return LK_ERR_ARG;
     opt_trace = value;
+    trace_reset();
   } else if (!strcmp(name, "ring_hint")) {
     if (value < 0 || value > 1) return LK_ERR_ARG;
     opt_ring_hint = value;
@@ -178,6 +180,9 @@ lk_status lk_set_option(const char* name, long value) {
   } else if (!strcmp(name, "mma_depth")) {
     if (value < 0 || value > 8) return LK_ERR_ARG;
     opt_mma_depth = value;
+  } else if (!strcmp(name, "mma_act16")) {
+    if (value < 0 || value > 2) return LK_ERR_ARG;
+    opt_mma_act16 = value;
   } else if (!strcmp(name, "l2_ahead_kb")) {
     if (value < 0 || value > 65536) return LK_ERR_ARG;
     opt_l2_ahead_kb = value;
@@ -205,6 +210,7 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "mma_warps")) return opt_mma_warps;
   if (!strcmp(name, "mma_depth")) return opt_mma_depth;
   if (!strcmp(name, "l2_ahead_kb")) return opt_l2_ahead_kb;
+  if (!strcmp(name, "mma_act16")) return opt_mma_act16;
   return -1;
 }
 

@@ -35,6 +35,7 @@ struct ChainArgs {
   int trace_all;              // also every block's and block 0's warps' step ends (trace 2)
   long long pf_budget;        // bytes of later steps' weights each block keeps requested into L2 ahead
   int pdl;                    // launched as a programmatic dependent (a chain without barriers)
+  int tslot;                  // trace 3: this launch's record in the timeline, else -1
 };
 
 // This block's bytes of step `o` (its rows' levels, then their scales): a
@@ -58,6 +59,9 @@ __device__ __forceinline__ PfRange pf_range(const lk_chain_op& o) {
 __device__ __forceinline__ void stamp(unsigned long long* trace, int i) {
   if (trace && blockIdx.x == 0 && threadIdx.x == 0 && i < LK_TRACE_MAX) trace[i] = gtimer();
 }
+// step stamps only in the per-launch modes (trace 1, 2)
+#define CHAIN_STAMP(i) \
+  if (ca.tslot < 0) stamp(ca.trace, (i))
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
@@ -159,7 +163,8 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     ++in;
     ++issued;
   };
-  stamp(ca.trace, 0);
+  CHAIN_STAMP(0);
+  tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_START);
   // The barrier generation at launch.  No block can complete a barrier of
   // this launch before every block has read it (completion needs every
   // block's arrival, and a block arrives only after this read).
@@ -203,6 +208,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
 
   // weights above do not depend on the previous kernel; activations do
   if (ca.pdl) griddep_wait();
+  tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_WAITED);
   long consumed = 0;
   bool ok = true;
   for (int op = 0; ok && op < ca.n_ops; ++op) {
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     }
     // the activation area is rewritten below: every warp is done with the last step
     __syncthreads();
-    stamp(ca.trace, 1 + 3 * op);
+    CHAIN_STAMP(1 + 3 * op);
     // a step that reads the same rows with the same gain as the one before it
     // (q, k and v of a layer) reuses the activation area as it is
     const bool same = op > 0 && !o.wait && o.x == ca.ops[op - 1].x && o.gain == ca.ops[op - 1].gain &&
@@ -227,7 +233,8 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
       pr.eps = ca.eps;
       fused_prologue<Q, M>(pr, nwc, 0, (unsigned)o.K, act, nred, nden);
     }
-    stamp(ca.trace, 2 + 3 * op);
+    CHAIN_STAMP(2 + 3 * op);
+    if (op == 0) tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_ACT);
     const Geom g = op_geom(o);
     const long T = geom_stages(g, warp, nwc);
     const Act ac{act, (unsigned)o.K};
@@ -258,13 +265,13 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
         finish_quad<Q, M, false>(p, g, warp, nwc, n, dummy, 0, o.y, best, lane);
       }
     }
-    if (ca.trace && ca.trace_all && lane == 0 && blockIdx.x == 0) {
+    if (ca.trace && ca.trace_all && ca.tslot < 0 && lane == 0 && blockIdx.x == 0) {
       const long i = 1024 + (long)ca.n_ops * gridDim.x + (long)op * nwc + warp;
       if (i < LK_TRACE_MAX) ca.trace[i] = gtimer();
     }
     ok = __syncthreads_and(ok) != 0;  // every warp agrees before the next barrier
-    stamp(ca.trace, 3 + 3 * op);
-    if (ca.trace && ca.trace_all && threadIdx.x == 0) {
+    CHAIN_STAMP(3 + 3 * op);
+    if (ca.trace && ca.trace_all && ca.tslot < 0 && threadIdx.x == 0) {
       const long i = 1024 + (long)op * gridDim.x + blockIdx.x;
       if (i < LK_TRACE_MAX) ca.trace[i] = gtimer();
     }
@@ -302,6 +309,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     for (long m = consumed; m < issued; ++m)
       drain_wait(full0 + 8 * (unsigned)(warp * D + m % D), (unsigned)(m / D) & 1u, ca.wait_ns, ca.err);
   __syncwarp();
+  tend(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, ca.n_ops, 2);
 }
 
 typedef void (*chain_fn)(const ChainArgs);
@@ -400,7 +408,8 @@ extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* op
   if (!ca.err) return LK_ERR_CUDA;
   ca.trace = lkh::opt_trace ? lkh::trace_ptr() : nullptr;
   ca.pf_budget = lkh::opt_l2_prefetch_kb * 1024;
-  ca.trace_all = lkh::opt_trace >= 2;
+  ca.trace_all = lkh::opt_trace == 2;
+  ca.tslot = lkh::opt_trace == 3 ? lkh::trace_next_slot() : -1;
   ca.pdl = !barrier && lkh::opt_pdl ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->sm_count);

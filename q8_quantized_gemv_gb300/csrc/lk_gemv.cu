@@ -269,6 +269,55 @@ lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode
   return st;
 }
 
+lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
+                           const int8_t* xq, const int8_t* xl, const float* xs, int M, cudaStream_t stream) {
+  if (!targets || n < 1 || n > LK_MAX_GROUP) return LK_ERR_ARG;
+  for (int i = 0; i < n; ++i) {
+    const lk_gemv_target& t = targets[i];
+    if (!t.wq || !t.ws || !t.y) return LK_ERR_ARG;
+    lk_status st = check_common(t.wq, t.ws, t.N, K, mode, x, xq, xl, xs, M);
+    if (st) return st;
+    if (t.N < 1) return LK_ERR_SHAPE;
+    if (!aligned(t.y, 4)) return LK_ERR_ALIGN;
+  }
+  if (M == 0 || K == 0) {
+    for (int i = 0; i < n; ++i) {
+      lk_status st = lk_gemv_q8(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M,
+                                targets[i].y, nullptr, nullptr, stream);
+      if (st) return st;
+    }
+    return LK_OK;
+  }
+  GemvProblem p = make_problem(targets[0].wq, targets[0].ws, targets[0].N, K, mode, x, xq, xl, xs, M);
+  bool one = (opt_gemv_path == 0 || opt_gemv_path == 3);
+  for (int i = 0; i < n && one; ++i) {
+    GemvProblem q = p;
+    q.wq = targets[i].wq;
+    q.ws = (const __half*)targets[i].ws;
+    q.N = targets[i].N;
+    one = mma_supports(q);
+  }
+  if (one) {
+    const int8_t* wq[LK_MAX_GROUP];
+    const __half* ws[LK_MAX_GROUP];
+    long N[LK_MAX_GROUP];
+    float* y[LK_MAX_GROUP];
+    for (int i = 0; i < n; ++i) {
+      wq[i] = targets[i].wq;
+      ws[i] = (const __half*)targets[i].ws;
+      N[i] = targets[i].N;
+      y[i] = targets[i].y;
+    }
+    return mma_launch(p, n, wq, ws, N, y, stream, nullptr);
+  }
+  for (int i = 0; i < n; ++i) {
+    lk_status st = lk_gemv_q8(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M, targets[i].y,
+                              nullptr, nullptr, stream);
+    if (st) return st;
+  }
+  return LK_OK;
+}
+
 int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S) {
   if (mode < LK_DEQUANT || mode > LK_TWOPASS || N < 1 || K < 32 || K % 32 || M < 1 || M > LK_MAX_M || S < 0 ||
       S > LK_MAX_SPLITK)

@@ -34,7 +34,8 @@ extern long opt_wait_us;      // bound of every device-side wait, microseconds (
 extern long opt_mma_min_m;    // fewest activation rows taking the tensor-core kernel (0 = 2)
 extern long opt_mma_tk;       // its bytes of K per stage (0 auto, else a multiple of 256)
 extern long opt_mma_warps;    // its warps per block (0 auto)
-extern long opt_mma_depth;    // its ring stages per warp (0 = 2)
+extern long opt_mma_depth;    // its ring stages per warp (0 = 1)
+extern long opt_mma_act16;    // its activations held as f16: 0 auto, 1 force, 2 never
 extern long opt_l2_ahead_kb;  // ring/tensor-core kernels: KB per block of later stages requested into L2 at start
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
@@ -71,6 +72,10 @@ struct GemvProblem {
 int* error_word_ptr();
 // Device address of the trace buffer (option "trace").
 unsigned long long* trace_ptr();
+// Option "trace" 3: the next launch's record index in the timeline (wraps),
+// and its reset (setting the option resets it).
+int trace_next_slot();
+void trace_reset();
 
 // Bulk-copy ring kernel (lk_ring.cu).  Returns LK_ERR_SHAPE when the problem
 // is outside what the ring kernel takes (the caller then uses the direct
@@ -80,6 +85,9 @@ bool ring_supports(const GemvProblem& p);
 
 // Tensor-core kernel for 2..8 activation rows (lk_mma.cu), same contract.
 lk_status mma_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts);
+// The same over nmat matrices sharing p's activation, in one launch.
+lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, const __half* const* ws,
+                     const long* N, float* const* y, cudaStream_t stream, int* n_parts);
 bool mma_supports(const GemvProblem& p);
 int ring_max_ctas(long N);
 

@@ -46,12 +46,20 @@ constexpr int MST = 32;         // ring stages per block at most
 // barriers (one per stage + the activation's), abort flag, argmax keys [8][MW]
 constexpr unsigned MTAIL = 8 * (MST + 1) + 16 + 8 * TN * MW;
 
+constexpr int MG = LK_MAX_GROUP;  // matrices of one grouped launch at most
+
 struct MmaArgs {
-  lkh::GemvProblem p;
+  lkh::GemvProblem p;      // activations, K, M, mode, argmax keys (one matrix only)
+  int nmat;                // matrices sharing the activation (1..MG)
+  const int8_t* wq[MG];
+  const unsigned char* ws[MG];  // f16 scales, as bytes
+  long N[MG];
+  float* y[MG];
+  long tile0[MG + 1];      // first tile of matrix m; tile0[nmat] = all tiles
   int nw;                  // warps per block
   int depth;               // ring stages per warp
   int gx;                  // blocks
-  long ntiles;             // ceil(N / 16)
+  long ntiles;             // sum over the matrices of ceil(N / 16)
   unsigned tk;             // bytes of K per stage (multiple of 256)
   unsigned rs;             // stage row stride (tk + 32)
   unsigned srs;            // stage scale row stride (tk / 16 + 16)
@@ -66,6 +74,8 @@ struct MmaArgs {
   int pdl;
   int* err;
   int l2_ahead;            // stages per warp requested into L2 beyond the ring at start
+  unsigned long long* trace;  // option "trace" 3: the launch timeline, else NULL
+  int tslot;
 };
 
 // int8 x 4 (b0 lowest) -> two f16x2: (b0, b1) and (b2, b3), exact.
@@ -103,55 +113,102 @@ __device__ __forceinline__ void block_dot(float (&d)[4], const Frag8& wg, const 
   mma16816(d, wg.m1lo, wg8.m1lo, wg.m1hi, wg8.m1hi, x.m1lo, x.m1hi);
 }
 
+// The B fragment of activation row g for the 32-block at level offset k:
+// read as f16 (A16) or as int8 and converted; zeros for rows >= M.
+template <bool A16>
+__device__ __forceinline__ Frag8 act_frag(const unsigned char* X, int k, bool ok) {
+  if (A16) {
+    const uint4 v = ok ? *(const uint4*)(X + 2 * k) : make_uint4(0u, 0u, 0u, 0u);
+    return Frag8{v.x, v.y, v.z, v.w};
+  }
+  return frag8(ok ? *(const uint2*)(X + k) : make_uint2(0u, 0u));
+}
+
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
 struct Tiles {
   long base, stride, ntiles;
   int nsl;
 };
 
-// Stage n of the calling warp: tile base + stride * (n / nsl), slice n % nsl.
-__device__ __forceinline__ void issue(const MmaArgs& ra, const Tiles& tl, long n, unsigned char* st, unsigned full,
+// A position in a warp's stage sequence (tile, slice), advanced without
+// divisions: slice c of tile base + stride * r.
+struct Cursor {
+  long tile;
+  int c;
+  __device__ __forceinline__ void next(const Tiles& tl) {
+    if (++c == tl.nsl) {
+      c = 0;
+      tile += tl.stride;
+    }
+  }
+};
+
+// The matrix a tile belongs to, with constant indices into the launch
+// arguments (no local-memory copy of the arrays).
+struct Mat {
+  const int8_t* wq;
+  const unsigned char* ws;
+  long N;
+  float* y;
+  long row0;  // the tile's first row in its matrix
+};
+__device__ __forceinline__ Mat mat_of(const MmaArgs& ra, long tile) {
+  Mat m{ra.wq[0], ra.ws[0], ra.N[0], ra.y[0], tile * TR};
+#pragma unroll
+  for (int i = 1; i < MG; ++i)
+    if (i < ra.nmat && tile >= ra.tile0[i]) m = Mat{ra.wq[i], ra.ws[i], ra.N[i], ra.y[i], (tile - ra.tile0[i]) * TR};
+  return m;
+}
+
+// Slice c of tile `tile` into the stage buffer st, completing on `full`.
+__device__ __forceinline__ void issue(const MmaArgs& ra, long tile, int c, unsigned char* st, unsigned full,
                                       unsigned long long pol, int lane) {
-  const lkh::GemvProblem& a = ra.p;
-  const long tile = tl.base + tl.stride * (n / tl.nsl);
-  const int c = (int)(n % tl.nsl);
-  const long row0 = tile * TR;
-  const int rows = a.N - row0 < TR ? (int)(a.N - row0) : TR;
+  const int K = ra.p.K;
+  const Mat m = mat_of(ra, tile);
+  const int rows = m.N - m.row0 < TR ? (int)(m.N - m.row0) : TR;
   const int k0 = c * (int)ra.tk;
-  const int len = a.K - k0 < (int)ra.tk ? a.K - k0 : (int)ra.tk;
+  const int len = K - k0 < (int)ra.tk ? K - k0 : (int)ra.tk;
   if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)len * 17u / 16u);
   __syncwarp();
   const int r = lane & 15;
   if (r < rows) {
-    const long row = row0 + r;
+    const long row = m.row0 + r;
     if (lane < 16)
-      bulk(st + r * ra.rs, a.wq + row * a.K + k0, (unsigned)len, full, pol);
+      bulk(st + r * ra.rs, m.wq + row * K + k0, (unsigned)len, full, pol);
     else
-      bulk(st + ra.s_off + r * ra.srs, (const unsigned char*)a.ws + (row * (a.K >> 5) + (k0 >> 5)) * 2,
-           (unsigned)len / 16u, full, pol);
+      bulk(st + ra.s_off + r * ra.srs, m.ws + (row * (K >> 5) + (k0 >> 5)) * 2, (unsigned)len / 16u, full, pol);
   }
   __syncwarp();
 }
 
-// Request the calling warp's stage n (the bytes issue() copies) into L2.
-__device__ __forceinline__ void prefetch(const MmaArgs& ra, const Tiles& tl, long n, int lane) {
-  const lkh::GemvProblem& a = ra.p;
-  const long tile = tl.base + tl.stride * (n / tl.nsl);
-  const int c = (int)(n % tl.nsl);
-  const long row0 = tile * TR;
-  const int rows = a.N - row0 < TR ? (int)(a.N - row0) : TR;
+// Request slice c of tile `tile` (the bytes issue() copies) into L2.
+__device__ __forceinline__ void prefetch(const MmaArgs& ra, long tile, int c, int lane) {
+  const int K = ra.p.K;
+  const Mat m = mat_of(ra, tile);
+  const int rows = m.N - m.row0 < TR ? (int)(m.N - m.row0) : TR;
   const int k0 = c * (int)ra.tk;
-  const int len = a.K - k0 < (int)ra.tk ? a.K - k0 : (int)ra.tk;
+  const int len = K - k0 < (int)ra.tk ? K - k0 : (int)ra.tk;
   const int r = lane & 15;
   if (r < rows) {
-    const long row = row0 + r;
+    const long row = m.row0 + r;
     if (lane < 16)
-      bulk_prefetch_l2(a.wq + row * a.K + k0, (unsigned)len);
+      bulk_prefetch_l2(m.wq + row * K + k0, (unsigned)len);
     else
-      bulk_prefetch_l2((const unsigned char*)a.ws + (row * (a.K >> 5) + (k0 >> 5)) * 2, (unsigned)len / 16u);
+      bulk_prefetch_l2(m.ws + (row * (K >> 5) + (k0 >> 5)) * 2, (unsigned)len / 16u);
   }
 }
 
-template <int Q>
+// A16: the activation rows are held in shared memory already converted to
+// f16 (row stride 2K + 64 bytes: a quarter-warp's 16-byte reads of rows g,
+// g+1 then cover 128 distinct bytes), so the B fragment is one 16-byte read
+// per 32-block instead of a read and 10 conversion instructions per warp.
+// Else the int8 words are held (stride K + 32) and converted per use.
+template <int Q, bool A16>
 __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) {
   extern __shared__ __align__(128) unsigned char smem[];
   const lkh::GemvProblem& a = ra.p;
@@ -184,17 +241,46 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   }
   __syncthreads();
   if (ra.pdl && threadIdx.x == 0) griddep_launch();
+  tstamp(ra.trace, ra.tslot, TR_START);
 
   // weights do not depend on the previous kernel: start streaming at once
   long issued = 0;
-  for (; issued < T && issued < D; ++issued)
-    issue(ra, tl, issued, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
+  Cursor ic{tl.base, 0};
+  for (; issued < T && issued < D; ++issued, ic.next(tl))
+    issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
           pol_w, lane);
-  for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m) prefetch(ra, tl, m, lane);
+  {
+    Cursor pc = ic;
+    for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m, pc.next(tl)) prefetch(ra, pc.tile, pc.c, lane);
+  }
 
   if (ra.pdl) griddep_wait();
+  tstamp(ra.trace, ra.tslot, TR_WAITED);
   // the activation rows: int8 words (and low words) and scales, row-padded
-  if (warp == 0) {
+  if (A16) {
+    // every thread converts 16-byte runs of the int8 rows into f16 rows
+    const int runs = K >> 4, nrun = M * runs * (Q == 2 ? 2 : 1);
+    for (int i = threadIdx.x; i < nrun; i += blockDim.x) {
+      const int lo = Q == 2 && i >= M * runs;
+      const int j = lo ? i - M * runs : i;
+      const int row = j / runs, off = (j - row * runs) << 4;
+      const int8_t* src = (lo ? a.xl : a.xq) + (long)row * K + off;
+      const uint4 v = ld_nc16(src);
+      uint4 h0, h1;
+      i8x4_to_h2(v.x, h0.x, h0.y);
+      i8x4_to_h2(v.y, h0.z, h0.w);
+      i8x4_to_h2(v.z, h1.x, h1.y);
+      i8x4_to_h2(v.w, h1.z, h1.w);
+      uint4* dst = (uint4*)(act + (lo ? ra.a_lo : 0u) + (size_t)row * ra.ar + 2 * off);
+      dst[0] = h0;
+      dst[1] = h1;
+    }
+    for (int i = threadIdx.x; i < M * nb; i += blockDim.x) {
+      const int row = i / nb, b = i - row * nb;
+      ((float*)(act + ra.a_xs))[(size_t)row * ra.xsr + b] = __ldg(a.xs + (long)row * nb + b);
+    }
+    __syncthreads();
+  } else if (warp == 0) {
     const unsigned long long pol_a = evict_last_policy();
     if (lane == 0)
       mbar_arrive_expect_tx(act_bar, (unsigned)M * ((unsigned)K * (Q == 2 ? 2u : 1u) + (unsigned)nb * 4u));
@@ -207,13 +293,17 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
            act_bar, pol_a);
     __syncwarp();
   }
-  bool ok = __all_sync(FULL, mbar_wait(act_bar, 0, ra.wait_ns, abort_flag));
-  if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
+  bool ok = true;
+  if (!A16) {
+    ok = __all_sync(FULL, mbar_wait(act_bar, 0, ra.wait_ns, abort_flag));
+    if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
+  }
 
+  tstamp(ra.trace, ra.tslot, TR_ACT);
   // activation row g's words and the scales of activation rows 2t, 2t+1
   const bool gx_ok = g < M;
-  const unsigned char* XH = act + (size_t)g * ra.ar + 8 * t;
-  const unsigned char* XL = act + ra.a_lo + (size_t)g * ra.ar + 8 * t;
+  const unsigned char* XH = act + (size_t)g * ra.ar + (A16 ? 16 : 8) * t;
+  const unsigned char* XL = act + ra.a_lo + (size_t)g * ra.ar + (A16 ? 16 : 8) * t;
   const float* XS0 = (const float*)(act + ra.a_xs) + (size_t)(2 * t) * ra.xsr;
   const float* XS1 = XS0 + ra.xsr;
   const bool s0_ok = 2 * t < M, s1_ok = 2 * t + 1 < M;
@@ -226,15 +316,18 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   unsigned long long best0 = 0, best1 = 0;
 
   long n = 0;
+  Cursor cc{tl.base, 0};
+  int cs = 0;          // slot of stage n within the warp's D
+  unsigned cph = 0;    // its phase parity
   for (; ok && n < T; ++n) {
-    const int slot = warp * D + (int)(n % D);
-    if (!__all_sync(FULL, mbar_wait(full0 + 8 * slot, (unsigned)(n / D) & 1u, ra.wait_ns, abort_flag))) {
+    const int slot = warp * D + cs;
+    if (!__all_sync(FULL, mbar_wait(full0 + 8 * slot, cph, ra.wait_ns, abort_flag))) {
       if (lane == 0) raise_error(ra.err, ERR_WAIT_FULL, abort_flag);
       ok = false;
       break;
     }
     unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
-    const int c = (int)(n % tl.nsl);
+    const int c = cc.c;
     const int k0 = c * (int)ra.tk;
     const int len = K - k0 < (int)ra.tk ? K - k0 : (int)ra.tk;
     const unsigned char* W0 = st + g * ra.rs + 8 * t;
@@ -266,18 +359,16 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
         const int bb = 4 * gi + q;  // block within the slice; b0 % 4 == 0, so partial q
         const Frag8 fw0 = frag8(*(const uint2*)(W0 + 32 * bb));
         const Frag8 fw8 = frag8(*(const uint2*)(W8 + 32 * bb));
-        const uint2 hv = gx_ok ? *(const uint2*)(XH + k0 + 32 * bb) : make_uint2(0u, 0u);
         float d[4];
-        block_dot(d, fw0, fw8, frag8(hv));
+        block_dot(d, fw0, fw8, act_frag<A16>(XH, k0 + 32 * bb, gx_ok));
         const float ws_[4] = {wa[q], wa[q], wb[q], wb[q]};
         const float xs_[4] = {xa[q], xb[q], xa[q], xb[q]};
         if constexpr (Q == 1) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) p[q][e] = __fmaf_rn(__fmul_rn(ws_[e], xs_[e]), d[e], p[q][e]);
         } else {
-          const uint2 lv = gx_ok ? *(const uint2*)(XL + k0 + 32 * bb) : make_uint2(0u, 0u);
           float f[4];
-          block_dot(f, fw0, fw8, frag8(lv));
+          block_dot(f, fw0, fw8, act_frag<A16>(XL, k0 + 32 * bb, gx_ok));
           // q8_step<2> with the dots already in f32 (exact integers)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -292,13 +383,14 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
     __syncwarp();
     if (issued < T) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(ra, tl, issued, st, full0 + 8 * slot, pol_w, lane);
+      issue(ra, ic.tile, ic.c, st, full0 + 8 * slot, pol_w, lane);
+      ic.next(tl);
       ++issued;
     }
     if (c == tl.nsl - 1) {
       // the tile is done: (p0 + p2) + (p1 + p3) per element ("kernels.rs" lk_q8_sum4)
-      const long tile = tl.base + tl.stride * (n / tl.nsl);
-      const long r0 = tile * TR + g, r8 = r0 + 8;
+      const Mat mt = mat_of(ra, cc.tile);
+      const long r0 = mt.row0 + g, r8 = r0 + 8;
       const int t0 = 2 * t, t1 = 2 * t + 1;
       float yv[4];
 #pragma unroll
@@ -307,38 +399,48 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
 #pragma unroll
         for (int q = 0; q < 4; ++q) p[q][e] = 0.f;
       }
-      if (r0 < a.N) {
+      if (r0 < mt.N) {
         if (t0 < M) {
-          a.y[(long)t0 * a.N + r0] = yv[0];
+          mt.y[(long)t0 * mt.N + r0] = yv[0];
           const unsigned long long k = amax_key(yv[0], (unsigned)r0);
           best0 = k > best0 ? k : best0;
         }
         if (t1 < M) {
-          a.y[(long)t1 * a.N + r0] = yv[1];
+          mt.y[(long)t1 * mt.N + r0] = yv[1];
           const unsigned long long k = amax_key(yv[1], (unsigned)r0);
           best1 = k > best1 ? k : best1;
         }
       }
-      if (r8 < a.N) {
+      if (r8 < mt.N) {
         if (t0 < M) {
-          a.y[(long)t0 * a.N + r8] = yv[2];
+          mt.y[(long)t0 * mt.N + r8] = yv[2];
           const unsigned long long k = amax_key(yv[2], (unsigned)r8);
           best0 = k > best0 ? k : best0;
         }
         if (t1 < M) {
-          a.y[(long)t1 * a.N + r8] = yv[3];
+          mt.y[(long)t1 * mt.N + r8] = yv[3];
           const unsigned long long k = amax_key(yv[3], (unsigned)r8);
           best1 = k > best1 ? k : best1;
         }
       }
     }
+    cc.next(tl);
+    if (++cs == D) {
+      cs = 0;
+      cph ^= 1u;
+    }
   }
   // drain: stages issued but not consumed (only after an abort) must land
-  // before the block may end
+  // before the block may end; they occupy the slots from cs on, in order
   if (lane == 0) {
-    for (long m = n; m < issued; ++m)
-      drain_wait(full0 + 8 * (unsigned)(warp * D + m % D), (unsigned)(m / D) & 1u, ra.wait_ns, ra.err);
-    if (warp == 0) drain_wait(act_bar, 0, ra.wait_ns, ra.err);
+    for (long m = n; m < issued; ++m) {
+      drain_wait(full0 + 8 * (unsigned)(warp * D + cs), cph, ra.wait_ns, ra.err);
+      if (++cs == D) {
+        cs = 0;
+        cph ^= 1u;
+      }
+    }
+    if (!A16 && warp == 0) drain_wait(act_bar, 0, ra.wait_ns, ra.err);
   }
   __syncwarp();
   if (a.amax) {
@@ -361,28 +463,41 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
       a.amax[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
     }
   }
+  tend(ra.trace, ra.tslot, ra.ntiles * TR, 3);
 }
 
 struct MmaLayout {
   unsigned tk, rs, srs, s_off, stage_bytes, ar, xsr, a_lo, a_xs, ring_off, total;
   int nw, depth;
+  bool a16;
 };
 
 unsigned round_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
 
-// Widest tk (1024 or 512 bytes, or the option) that leaves room for >= 2
-// warps x 2 stages next to the activation area.
-MmaLayout mma_layout(const lkh::GemvProblem& p, int smem_optin) {
+// Stage layout.  A warp computes its tiles alone, one 32-block after the
+// other, so two regimes (measured, 8 rows):
+//  * many tiles per SM (gate/up 24576 x 4096: 10 per SM): warps beat stages
+//    per warp.  512-byte slices, one stage per warp, as many warps as fit
+//    (16): 29.5-30.8 us; two stages per warp (fewer warps) 44-48 us;
+//    256-byte slices 48 us (too few bytes in flight).
+//  * few tiles per SM (down 4096 x 12288: 1.7 per SM, so ~2 warps per SM
+//    have work): bytes in flight per working warp decide.  1024-byte slices,
+//    two stages per warp: 35.3 us; 512 x 1: 56.4 us; 256 x 1: 94.9 us.
+// Below 4 tiles per SM the second regime's layout is tried first.
+MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int smem_optin, bool a16) {
   MmaLayout L{};
   const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)p.M;
-  L.ar = K + 32u;
+  L.a16 = a16;
+  L.ar = a16 ? 2u * K + 64u : K + 32u;
   L.xsr = nb + 4u;
   L.a_lo = round_up(M * L.ar, 128u);
   L.a_xs = p.mode == LK_TWOPASS ? round_up(L.a_lo + M * L.ar, 128u) : L.a_lo;
   L.ring_off = round_up(L.a_xs + M * L.xsr * 4u, 128u);
-  const unsigned cands[2] = {1024u, 512u};
-  for (int i = 0; i < 2; ++i) {
-    unsigned tk = lkh::opt_mma_tk > 0 ? (unsigned)lkh::opt_mma_tk : cands[i];
+  const bool few = ntiles < 4L * sms;
+  const unsigned cand_tk[4] = {1024u, 512u, 512u, 256u};
+  const int cand_d[4] = {2, 2, 1, 1};
+  for (int i = few ? 0 : 2; i < 4; ++i) {
+    unsigned tk = lkh::opt_mma_tk > 0 ? (unsigned)lkh::opt_mma_tk : cand_tk[i];
     if (tk > round_up(K, 256u)) tk = round_up(K, 256u);
     L.tk = tk;
     L.rs = tk + 32u;
@@ -392,7 +507,7 @@ MmaLayout mma_layout(const lkh::GemvProblem& p, int smem_optin) {
     const long room = (long)smem_optin - (long)L.ring_off - (long)MTAIL;
     int fit = room > 0 ? (int)(room / L.stage_bytes) : 0;
     if (fit > MST) fit = MST;
-    int depth = lkh::opt_mma_depth > 0 ? (int)lkh::opt_mma_depth : 2;
+    int depth = lkh::opt_mma_depth > 0 ? (int)lkh::opt_mma_depth : cand_d[i];
     int w = lkh::opt_mma_warps > 0 ? (int)lkh::opt_mma_warps : fit / depth;
     if (w > MW) w = MW;
     if (w * depth > fit) w = fit / depth;
@@ -404,7 +519,24 @@ MmaLayout mma_layout(const lkh::GemvProblem& p, int smem_optin) {
   return L;
 }
 
+bool mma_layout_ok(const MmaLayout& L);
+
+// f16-held activations where they cost no warps (Int8Act at K = 4096: 16
+// warps either way; TwoPass would drop from 16 to 10: measured 54.9 us
+// against 36.9 us held as int8); option "mma_act16" 1 forces them (if they
+// fit at all), 2 forbids them.
+MmaLayout mma_layout(const lkh::GemvProblem& p, long ntiles, int sms, int smem_optin) {
+  const MmaLayout L8 = mma_layout_for(p, ntiles, sms, smem_optin, false);
+  if (lkh::opt_mma_act16 == 2) return L8;
+  const MmaLayout L16 = mma_layout_for(p, ntiles, sms, smem_optin, true);
+  if (!mma_layout_ok(L16)) return L8;
+  if (lkh::opt_mma_act16 == 1) return L16;
+  return L16.nw >= L8.nw ? L16 : L8;
+}
+
 bool mma_layout_ok(const MmaLayout& L) { return L.nw >= 1 && L.depth >= 1 && L.nw * L.depth >= 2; }
+// (a single-stage ring per warp still overlaps: the warps' copies are in
+// flight while other warps compute)
 
 typedef void (*mma_fn)(const MmaArgs);
 
@@ -424,23 +556,44 @@ bool mma_supports(const GemvProblem& p) {
     return false;
   const DeviceInfo* d = device_info(nullptr);
   if (!d) return false;
-  return mma_layout_ok(mma_layout(p, d->smem_optin));
+  return mma_layout_ok(mma_layout(p, (p.N + TR - 1) / TR, d->sm_count, d->smem_optin));
 }
 
-lk_status mma_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
+// One launch over the matrices (wq[m], ws[m], N[m]) -> y[m], all reading
+// the activation of p.  Argmax keys (p.amax) only for a single matrix.
+lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, const __half* const* ws,
+                     const long* N, float* const* y, cudaStream_t stream, int* n_parts) {
   const DeviceInfo* d = device_info(nullptr);
   if (!d) return LK_ERR_CUDA;
-  const MmaLayout L = mma_layout(p, d->smem_optin);
+  if (nmat < 1 || nmat > MG || (nmat > 1 && p.amax)) return LK_ERR_ARG;
+  long all_tiles = 0;
+  for (int m = 0; m < nmat; ++m) all_tiles += (N[m] + TR - 1) / TR;
+  const MmaLayout L = mma_layout(p, all_tiles, d->sm_count, d->smem_optin);
   if (!mma_layout_ok(L)) return LK_ERR_SHAPE;
-  mma_fn f = p.mode == LK_TWOPASS ? gemv_mma_kernel<2> : gemv_mma_kernel<1>;
+  mma_fn f = p.mode == LK_TWOPASS ? (L.a16 ? gemv_mma_kernel<2, true> : gemv_mma_kernel<2, false>)
+                                  : (L.a16 ? gemv_mma_kernel<1, true> : gemv_mma_kernel<1, false>);
   // (the cap is the device's maximum: see ring_gemv)
   if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) != cudaSuccess)
     return LK_ERR_CUDA;
   MmaArgs ra;
   ra.p = p;
+  ra.nmat = nmat;
+  long tiles = 0;
+  for (int m = 0; m < MG; ++m) {
+    const bool in = m < nmat;
+    ra.wq[m] = in ? wq[m] : wq[0];
+    ra.ws[m] = (const unsigned char*)(in ? ws[m] : ws[0]);
+    ra.N[m] = in ? N[m] : 0;
+    ra.y[m] = in ? y[m] : y[0];
+    ra.tile0[m] = tiles;
+    if (in) tiles += (N[m] + TR - 1) / TR;
+  }
+  ra.tile0[MG] = tiles;
+  for (int m = nmat; m <= MG; ++m) ra.tile0[m] = tiles;
+  ra.ntiles = tiles;
+  if (tiles < 1) return LK_ERR_SHAPE;
   ra.nw = L.nw;
   ra.depth = L.depth;
-  ra.ntiles = (p.N + TR - 1) / TR;
   long gx = opt_grid_ctas > 0 ? opt_grid_ctas : d->sm_count;
   if (gx > ra.ntiles) gx = ra.ntiles;
   ra.gx = (int)gx;
@@ -460,6 +613,8 @@ lk_status mma_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   ra.err = error_word_ptr();
   if (!ra.err) return LK_ERR_CUDA;
   ra.l2_ahead = (int)(opt_l2_ahead_kb * 1024 / ((long)L.nw * L.stage_bytes));
+  ra.trace = opt_trace == 3 ? trace_ptr() : nullptr;
+  ra.tslot = opt_trace == 3 ? trace_next_slot() : -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)gx);
   cfg.blockDim = dim3(L.nw * 32);
@@ -473,6 +628,14 @@ lk_status mma_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   if (cudaLaunchKernelEx(&cfg, f, ra) != cudaSuccess) return LK_ERR_CUDA;
   if (n_parts) *n_parts = (int)gx;
   return launch_status();
+}
+
+lk_status mma_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
+  const int8_t* wq[1] = {p.wq};
+  const __half* ws[1] = {p.ws};
+  const long N[1] = {p.N};
+  float* y[1] = {p.y};
+  return mma_launch(p, 1, wq, ws, N, y, stream, n_parts);
 }
 
 }  // namespace lkh

@@ -76,6 +76,14 @@ int* lkh::error_word_ptr() {
   return ptr[dev];
 }
 
+static int trace_seq = 0;
+void lkh::trace_reset() { trace_seq = 0; }
+int lkh::trace_next_slot() {
+  const int s = trace_seq;
+  trace_seq = (trace_seq + 1) % (lkring::LK_TRACE_MAX / lkring::TREC);
+  return s;
+}
+
 unsigned long long* lkh::trace_ptr() {
   static unsigned long long* ptr[64];
   int dev = 0;
@@ -194,6 +202,7 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   ra.err = lkh::error_word_ptr();
   if (!ra.err) return LK_ERR_CUDA;
   ra.trace = opt_trace ? lkh::trace_ptr() : nullptr;
+  ra.tslot = opt_trace == 3 ? lkh::trace_next_slot() : -1;
   ra.l2_ahead = (int)(opt_l2_ahead_kb * 1024 / ((long)L.nwc * L.stage_bytes));
   const int S = p.split && p.S > 1 ? p.S : 1;
   const int g = opt_grid_ctas > 0 ? (int)opt_grid_ctas : d->sm_count * (opt_ring_cps > 1 ? (int)opt_ring_cps : 1);

@@ -41,6 +41,7 @@ struct RingArgs {
   int pdl;                 // launched as a programmatic dependent of the previous kernel
   int* err;                // the device error word
   unsigned long long* trace;  // block 0's timestamps (option "trace"), or NULL
+  int tslot;               // trace 3: this launch's record in the timeline, else -1
   int l2_ahead;            // stages per warp requested into L2 beyond the ring at start
 };
 
@@ -77,6 +78,7 @@ __device__ __forceinline__ unsigned long long gtimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+__device__ __forceinline__ unsigned long long gtimer_() { return gtimer(); }
 // Bounded wait for the phase of parity `parity` to complete.  Returns false if
 // the limit ran out or another thread raised the abort flag.
 __device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity, unsigned long long limit_ns,
@@ -141,6 +143,31 @@ __device__ __forceinline__ void bulk(void* dst, const void* src, unsigned bytes,
   else bulk_g2s_nohint(dst, src, bytes, bar);
 }
 
+// Trace records.  Options "trace" 1/2: block 0's stamps of the last launch
+// from index 0.  Option 3 (launch timeline): each launch owns record `slot`
+// of TREC entries: [0] block 0 start, [1] block 0 past the dependency wait,
+// [2] block 0's activation ready, [3] the last block's end (max over blocks),
+// [4] block 0's end, [5] kernel kind, [6] rows.
+constexpr int TREC = 8;
+enum : int { TR_START = 0, TR_WAITED = 1, TR_ACT = 2, TR_END_MAX = 3, TR_END0 = 4, TR_KIND = 5, TR_ROWS = 6 };
+__device__ __forceinline__ void tstamp(unsigned long long* tr, int slot, int i) {
+  if (tr && blockIdx.x == 0 && threadIdx.x == 0) tr[(slot < 0 ? 0 : slot * TREC) + i] = gtimer_();
+}
+// every block: the latest end (call after the block's last work, all threads)
+__device__ __forceinline__ void tend(unsigned long long* tr, int slot, long rows, int kind) {
+  if (!tr || slot < 0) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned long long now = gtimer_();
+    atomicMax(tr + slot * TREC + TR_END_MAX, now);
+    if (blockIdx.x == 0) {
+      tr[slot * TREC + TR_END0] = now;
+      tr[slot * TREC + TR_KIND] = (unsigned long long)kind;
+      tr[slot * TREC + TR_ROWS] = (unsigned long long)rows;
+    }
+  }
+}
+
 // Request `bytes` at `src` into L2 (no completion to wait for).  src 16-byte
 // aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
@@ -184,9 +211,15 @@ __device__ __forceinline__ void store_act(unsigned char* act, unsigned L, int t,
   }
 }
 
+// dbg (option "trace" 1, block 0): [0] entry, [1] warp 0's squares summed,
+// [2] denominators ready, [3] warp 0's groups stored, [4] exit.
+__device__ __forceinline__ void pstamp(unsigned long long* dbg, int i) {
+  if (dbg && blockIdx.x == 0 && threadIdx.x == 0) dbg[i] = gtimer();
+}
+
 template <int Q, int M>
 __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, unsigned L, unsigned char* act,
-                               void* red_raw, void* den_raw) {
+                               void* red_raw, void* den_raw, unsigned long long* dbg = nullptr) {
   typedef typename acc_of<Q>::t A;
   constexpr int QB = PRO_SLOTS;  // groups a warp quantizes per batch
   constexpr int KU_MAX = 8;      // values per virtual thread kept in registers (K <= 8192)
@@ -198,6 +231,7 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
   const int vt = K < 1024 ? K : 1024, nvw_all = vt >> 5;
   const int KU = (K + vt - 1) / vt;
   const int ng = (int)(L >> 5);
+  pstamp(dbg, 0);
   for (int t = 0; t < M; ++t) {
     const float* xr = a.xraw + (long)t * K;
     // (1) the first batch of this warp's groups g = cw + nwc*b: its values and
@@ -246,6 +280,7 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
           if (lane == 0) red[t * 32 + w] = acc;
         }
       }
+      pstamp(dbg, 1);
       __syncthreads();
       if (cw == 0) {
         A v = lane < nvw_all ? red[t * 32 + lane] : (A)0;
@@ -253,6 +288,7 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
         if (lane == 0) den[t] = norm_div_add(v, K, a.eps);
       }
       __syncthreads();
+      pstamp(dbg, 2);
     }
     const A dn = norm ? den[t] : (A)1;
     // (3) normalize and quantize, batch by batch
@@ -269,8 +305,10 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
         store_act<Q, M>(act, L, t, g, lane, v);
       }
     }
+    pstamp(dbg, 3);
   }
   __syncthreads();
+  pstamp(dbg, 4);
 }
 
 // ---- one GEMV's stage stream, shared by the ring and the chain kernels -------------
@@ -525,7 +563,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   if (ra.pdl && threadIdx.x == 0) griddep_launch();
 
   // Weights do not depend on the previous kernel: start streaming at once.
-  if (ra.trace && blockIdx.x == 0 && threadIdx.x == 0) ra.trace[0] = gtimer();
+  tstamp(ra.trace, ra.tslot, TR_START);
   long issued = 0;
   for (; issued < T && issued < D; ++issued)
     issue_stage(g, warp, nwc, issued, ring + (size_t)(warp * D + issued % D) * ra.stage_bytes,
@@ -535,10 +573,10 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m) prefetch_stage(g, warp, nwc, m, lane);
 
   if (ra.pdl) griddep_wait();  // from here on: reads of activations, writes of outputs
-  if (ra.trace && blockIdx.x == 0 && threadIdx.x == 0) ra.trace[1] = gtimer();
+  tstamp(ra.trace, ra.tslot, TR_WAITED);
   bool ok = true;
   if (FUSE) {
-    fused_prologue<Q, M>(a, nwc, k_lo, L, act, nred, nden);
+    fused_prologue<Q, M>(a, nwc, k_lo, L, act, nred, nden, ra.trace && ra.tslot < 0 ? ra.trace + 32 : nullptr);
   } else if (L > 0) {
     if (warp == 0) {
       const unsigned long long pol_a = evict_last_policy();
@@ -563,7 +601,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   }
 
   const Act ac{act, L};
-  if (ra.trace && blockIdx.x == 0 && threadIdx.x == 0) ra.trace[2] = gtimer();
+  tstamp(ra.trace, ra.tslot, TR_ACT);
   unsigned long long best[M];
   P p[M];
 #pragma unroll
@@ -592,7 +630,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
     }
     if ((int)(n % g.nsl) == g.nsl - 1) finish_quad<Q, M, SPLIT>(p, g, warp, nwc, n, a, blockIdx.y, a.y, best, lane);
   }
-  if (ra.trace && blockIdx.x == 0 && lane == 0) ra.trace[3 + warp] = gtimer();
+  if (ra.trace && ra.tslot < 0 && blockIdx.x == 0 && lane == 0) ra.trace[3 + warp] = gtimer();
   // Drain: stages this warp issued but did not consume (only after an
   // abort) must land before the block may end.
   if (lane == 0) {
@@ -614,6 +652,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
       a.amax[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
     }
   }
+  tend(ra.trace, ra.tslot, N, 1);
 }
 
 // Explicit instantiation of every (M, SPLIT, FUSE) kernel of mode Q.

@@ -162,6 +162,14 @@ class DecodeStack:
                 def launch(c=self.qkv[l]):
                     return lk.lk_gemv_chain(c, self.mode, self.B, self.eps)
                 launch() if hook is None else hook("qkv", launch)
+            elif not any(self.fused[n] for n in ("q", "k", "v")):
+                # one norm, then q, k and v as one grouped GEMV
+                a = self._norm(x, w["g_attn"])
+
+                def launch(w=w, a=a):
+                    return lk.lk_gemv_q8_group([(w[n][0], w[n][1], self.out[n]) for n in ("q", "k", "v")],
+                                               self.mode, M=self.B, **a)
+                launch() if hook is None else hook("qkv", launch)
             else:
                 # q, k and v read the same normed activation: quantized once
                 _, a = g("q", w["q"], self.out["q"], x, w["g_attn"])
@@ -192,7 +200,8 @@ class DecodeStack:
         n = 1  # argmax reduce
         f = self.fused
         qkv_norm = 0 if (f["q"] and f["k"] and f["v"]) else 1  # one shared norm for q, k, v
-        per_layer = (4 if self.qkv is not None else 6) + qkv_norm \
+        grouped = self.qkv is not None or (qkv_norm and self.kernel["q"] == 3)
+        per_layer = (4 if grouped else 6) + qkv_norm \
             + (0 if (f["o"] or self.mode == lk.LK_DEQUANT) else 1) + (0 if f["gu"] else 1) \
             + (0 if (f["down"] or self.mode == lk.LK_DEQUANT) else 1)
         return n + self.L * per_layer + 1 + (0 if f["lm"] else 1)

@@ -33,6 +33,12 @@ class LkChainOp(ctypes.Structure):
                 ("reserved", ctypes.c_int)]
 
 
+class LkGemvTarget(ctypes.Structure):
+    """One matrix of lk_gemv_q8_group (the C struct lk_gemv_target)."""
+    _fields_ = [("wq", ctypes.c_void_p), ("ws", ctypes.c_void_p), ("N", ctypes.c_int), ("reserved", ctypes.c_int),
+                ("y", ctypes.c_void_p)]
+
+
 class LkError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -74,6 +80,7 @@ def _load():
         "lk_trace_read": ([P, I], I),
         "lk_argmax_noalloc": ([P, I, I, P, P], I),
         "lk_gemv_chain": ([P, P, I, I, I, F, P, P], I),
+        "lk_gemv_q8_group": ([P, I, I, I, P, P, P, P, I, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -89,7 +96,7 @@ def exported_symbols():
             "lk_argmax_parts_max", "lk_argmax_scratch_entries", "lk_argmax", "lk_q8_block_dots",
             "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout", "lk_gemv_kernel_for",
             "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain", "lk_trace_read",
-            "lk_argmax_noalloc"]
+            "lk_argmax_noalloc", "lk_gemv_q8_group"]
 
 
 def _ok(st, where):
@@ -167,8 +174,25 @@ def lk_gemv_q8(wq, ws, mode, y, x=None, xq=None, xl=None, xs=None, argmax_parts=
     return n.value
 
 
+def lk_gemv_q8_group(mats, mode, x=None, xq=None, xl=None, xs=None, M=None, stream=None):
+    """mats: [(wq, ws, y), ...] sharing K and the activation: y = W x for
+    each, in one launch where the tensor-core kernel applies."""
+    K = mats[0][0].shape[1]
+    if M is None:
+        M = (x if x is not None else xq).shape[0]
+    arr = (LkGemvTarget * len(mats))(*[LkGemvTarget(_ptr(wq, _I8, "wq"), _ptr(ws, _WS, "ws"), wq.shape[0], 0,
+                                                    _ptr(y, _F32, "y")) for wq, ws, y in mats])
+    for wq, _, _ in mats:
+        if wq.shape[1] != K:
+            raise ValueError("lk_gemv_q8_group: matrices of one group share K")
+    _ok(_load().lk_gemv_q8_group(ctypes.cast(arr, ctypes.c_void_p), len(mats), K, _mode(mode),
+                                 _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"),
+                                 M, _stream(stream)), "lk_gemv_q8_group")
+
+
 def lk_gemv_kernel_for(N, K, mode, M, S=0) -> int:
-    """1 direct kernel, 2 bulk-copy ring kernel, 0 none (see include/lk.h)."""
+    """1 direct kernel, 2 bulk-copy ring kernel, 3 tensor-core kernel, 0 none
+    (see include/lk.h)."""
     return _load().lk_gemv_kernel_for(N, K, _mode(mode), M, S)
 
 

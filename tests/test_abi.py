@@ -129,7 +129,8 @@ def test_options(lib):
 
 @pytest.mark.parametrize("name,good,bad", [("gemv_path", [0, 3], [-1, 4]), ("mma_min_m", [0, 2, 9], [-1, 10]),
                                            ("mma_tk", [0, 256, 1024, 8192], [100, 8448, -256]),
-                                           ("mma_warps", [0, 1, 16], [17, -1]), ("mma_depth", [0, 1, 8], [9, -1])])
+                                           ("mma_warps", [0, 1, 16], [17, -1]), ("mma_depth", [0, 1, 8], [9, -1]),
+                                           ("mma_act16", [0, 1, 2], [3, -1]), ("l2_ahead_kb", [0, 64], [-1])])
 def test_tensor_core_options(lib, name, good, bad):
     for v in good:
         lk.lk_set_option(name, v)
@@ -138,3 +139,26 @@ def test_tensor_core_options(lib, name, good, bad):
         with pytest.raises(lk.LkError):
             lk.lk_set_option(name, v)
     lk.lk_set_option(name, 0)
+
+
+def test_group_argument_checks(lib):
+    g = lib.lk_gemv_q8_group
+
+    def targets(*specs):
+        arr = (lk.LkGemvTarget * max(1, len(specs)))(*[lk.LkGemvTarget(w, s, n, 0, y) for w, s, n, y in specs])
+        return ctypes.cast(arr, ctypes.c_void_p)
+
+    good = (FAKE, FAKE, 64, FAKE)
+
+    def call(ts, n, K=256, mode=1, M=8, xq=P(FAKE), xl=P(FAKE), xs=P(FAKE)):
+        return g(ts, n, K, mode, None, xq, xl, xs, M, None)
+
+    assert call(None, 1) == -1                            # no targets
+    assert call(targets(good), 0) == -1                   # n out of range
+    assert call(targets(*[good] * 5), 5) == -1
+    assert call(targets(good, (FAKE, FAKE, 64, None)), 2) == -1     # null y
+    assert call(targets(good, (FAKE + 8, FAKE, 64, FAKE)), 2) == -2  # misaligned levels
+    assert call(targets(good, (FAKE, FAKE, 0, FAKE)), 2) == -3       # an empty matrix
+    assert call(targets(good), 1, K=48) == -3             # K % 32
+    assert call(targets(good), 1, M=9) == -3
+    assert call(targets(good), 1, mode=2, xl=None) == -1  # TwoPass needs the low words

@@ -3,7 +3,8 @@ against the CPU oracle, bit for bit: every row count, ragged N (a partial
 last 16-row tile) and ragged K (a partial last stage slice), and every stage
 layout the options allow (bytes of K per stage, warps, stages per warp), so
 that each ring arrangement and tail path is exercised; plus the argmax
-epilogue and the shapes it declines."""
+epilogue, the shapes it declines, and the grouped call (several matrices
+sharing one activation in one launch)."""
 import numpy as np
 import pytest
 
@@ -16,7 +17,7 @@ from q8_quantized_gemv_gb300 import build, lk, synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 I8, TP = 1, 2
-OPTS = ("mma_tk", "mma_warps", "mma_depth", "grid_ctas", "gemv_path")
+OPTS = ("mma_tk", "mma_warps", "mma_depth", "mma_act16", "grid_ctas", "gemv_path")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -58,18 +59,23 @@ def run_case(N, K, M, mode, seed, amax=False):
     return y
 
 
+@pytest.mark.parametrize("act16", [1, 2])
 @pytest.mark.parametrize("mode", [I8, TP])
 @pytest.mark.parametrize("M", [2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("N,K", [(16, 256), (1000, 1280), (333, 4096), (2500, 2304)])
-def test_mma_rows_and_tails(mode, M, N, K):
+def test_mma_rows_and_tails(act16, mode, M, N, K):
+    """act16 1: activations held as f16; 2: held as int8, converted per use."""
+    lk.lk_set_option("mma_act16", act16)
     run_case(N, K, M, mode, 7000 + N + K + M)
 
 
+@pytest.mark.parametrize("act16", [1, 2])
 @pytest.mark.parametrize("mode", [I8, TP])
 @pytest.mark.parametrize("tk,warps,depth", [(256, 0, 0), (512, 0, 0), (1024, 0, 0), (2048, 0, 0),
                                             (1024, 1, 2), (1024, 3, 1), (512, 16, 1), (256, 4, 4),
                                             (1024, 2, 3)])
-def test_mma_stage_layouts(mode, tk, warps, depth):
+def test_mma_stage_layouts(act16, mode, tk, warps, depth):
+    lk.lk_set_option("mma_act16", act16)
     lk.lk_set_option("mma_tk", tk)
     lk.lk_set_option("mma_warps", warps)
     lk.lk_set_option("mma_depth", depth)
@@ -134,3 +140,26 @@ def test_mma_declines():
     lk.lk_set_option("mma_min_m", 9)
     assert lk.lk_gemv_kernel_for(4096, 4096, 1, 8, 0) != 3
     lk.lk_set_option("mma_min_m", 0)
+
+
+@pytest.mark.parametrize("mode", [I8, TP])
+@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("Ns", [(4096, 1024, 1024), (100, 37, 1000, 16), (5,)])
+def test_group_matches_single_calls_and_oracle(mode, M, Ns):
+    """lk_gemv_q8_group over matrices with ragged N: each output has the bits
+    of its own lk_gemv_q8 call and of the oracle (one launch for 2..8 rows,
+    one launch per matrix for a single row)."""
+    lk.lk_set_option("gemv_path", 0)
+    K = 1280
+    mats = [synth.q8_matrix(N, K, 7500 + i + N) for i, N in enumerate(Ns)]
+    x = synth.activation(M, K, 7600 + M, outliers=True)
+    acts = dev_acts(x, mode)
+    dm = [(to_dev(w), to_dev(s), torch.full((M, w.shape[0]), float("nan"), device=DEV)) for w, s in mats]
+    lk.lk_gemv_q8_group(dm, mode, M=M, **acts)
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) == 0
+    for (w, s), (wd, sd, y) in zip(mats, dm):
+        y_or = oracle.gemv(w, s, mode, **oracle_acts(x, mode))
+        assert np.array_equal(bits(host(y)), bits(y_or))
+        y1, _, _ = gpu_gemv(wd, sd, mode, acts, M)
+        assert np.array_equal(bits(host(y1)), bits(host(y)))
