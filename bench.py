@@ -60,10 +60,12 @@ def parse():
     ap.add_argument("--argmax", action="store_true", help="argmax epilogue + reduce (gemv workload)")
     ap.add_argument("--path", default="auto", choices=["auto", "direct", "ring", "mma"])
     ap.add_argument("--chain", action="store_true",
-                    help="sequence: the whole token as one cooperative chain launch (lk_gemv_chain) instead "
-                         "of one fused launch per projection")
-    ap.add_argument("--unfused", action="store_true",
-                    help="sequence: separate norm/quantize launches instead of the fused prologue")
+                    help="sequence: the whole token as one cooperative chain launch (lk_gemv_chain; fused "
+                         "prologues)")
+    ap.add_argument("--fused-prologue", action="store_true",
+                    help="sequence: every GEMV computes RMSNorm/quantize itself (one launch per projection) "
+                         "instead of a separate norm/quantize launch before it (the default, faster on GB300)")
+    ap.add_argument("--unfused", action="store_true", help=argparse.SUPPRESS)  # the default; kept for scripts
     ap.add_argument("--no-pdl", action="store_true",
                     help="no programmatic dependent launches between the fused GEMVs")
     ap.add_argument("--fused", action="store_true", help="gemv workload: RMSNorm->quantize->GEMV in one launch")
@@ -277,8 +279,8 @@ def run_ours(a, rank, world):
 
     lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
     _apply_opts(lk, a)
-    stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=not a.unfused,
-                        chain=a.chain and not a.unfused)
+    fused = (a.fused_prologue or a.chain) and not a.unfused
+    stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=fused, chain=a.chain and fused)
     tok_bytes = stack.weight_bytes()
     stream = torch.cuda.Stream(device=dev)
 

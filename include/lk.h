@@ -323,8 +323,12 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *   "ring_warps"  warps per block of the ring kernel: 0 auto, else 1..12
  *   "ring_kb"     cap on the ring kernel's shared memory per block, KB (0 none)
  *   "ring_cps"    ring blocks per SM in the grid, 1..4 (default 1)
- *   "pdl"         1: lk_rmsnorm_quant_gemv_q8 launches as a programmatic
- *                 dependent launch (default 0)
+ *   "pdl"         1: launches are programmatic dependent launches of the
+ *                 kernel before them on the stream (GEMV kernels, the fused
+ *                 launch, chains without barriers, lk_rmsnorm_quant and
+ *                 lk_quantize_act): each starts while its predecessor
+ *                 finishes (GEMVs stream weights meanwhile) and reads its
+ *                 inputs and writes its outputs only after it (default 0)
  *   "l2_prefetch_kb"  lk_gemv_chain: KB of later steps' weights each block
  *                 keeps requested into L2 ahead of the step it computes
  *                 (prefetch.global.L2::evict_last by every thread before
@@ -336,7 +340,9 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 launch made after the option was set owns a record of 8
  *                 entries (in launch order, 512 records, wrapping):
  *                 [0] block 0 start, [1] block 0 past the wait on the
- *                 previous kernel, [2] block 0's activation ready, [3] the
+ *                 previous kernel (fused launches: the prologue's start; it
+ *                 waits inside, after requesting the norm gains), [2] block
+ *                 0's activation ready, [3] the
  *                 last block's end, [4] block 0's end (all %globaltimer ns),
  *                 [5] kernel (1 ring, 2 chain, 3 tensor-core), [6] rows
  *                 (steps, for a chain).  Setting the option restarts the

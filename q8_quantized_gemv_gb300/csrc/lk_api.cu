@@ -64,13 +64,19 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __rest
                                                              float eps, float* __restrict__ xn,
                                                              int8_t* __restrict__ xq,
                                                              int8_t* __restrict__ xl,
-                                                             float* __restrict__ xs) {
+                                                             float* __restrict__ xs, unsigned long long* tr,
+                                                             int slot) {
   typedef typename acc_of<Q>::t A;
   __shared__ A red[32];
   __shared__ A total;
   // a programmatic dependent (a GEMV launched with "pdl") may start its
-  // weight stream now; it reads these outputs only after this grid completes
+  // weight stream now; it reads these outputs only after this grid completes.
+  // Launched as a dependent itself ("pdl"), this grid reads x and writes its
+  // outputs only after the previous kernel has completed.
   asm volatile("griddepcontrol.launch_dependents;" :::);
+  trec_stamp(tr, slot, TR_START);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  trec_stamp(tr, slot, TR_WAITED);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int vt = blockDim.x, nw = vt >> 5;
   const long row = blockIdx.x;
@@ -96,17 +102,106 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __rest
     if (xn) xn[row * K + i] = yv;
     if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, row * K + i, (row * K + i) >> 5, lane);
   }
+  trec_end(tr, slot, TK_NORM, K);
+}
+
+// The same for K a multiple of the block size vt with KU = K / vt <= 8,
+// spread over KU blocks per row: thread t of every block loads the row's
+// values t + vt*u (u < KU) once, all blocks form the same sum of squares in
+// the same order as rmsnorm_quant_kernel (so the same denominator), and block
+// y normalizes and quantizes only the values t + vt*y it holds: 32-group
+// w + (vt/32)*y per warp w.  The row's divisions are shared by KU blocks.
+template <int Q>
+__global__ void __launch_bounds__(1024) rmsnorm_quant_split_kernel(const float* __restrict__ x,
+                                                                   const float* __restrict__ g, int K, float eps,
+                                                                   float* __restrict__ xn, int8_t* __restrict__ xq,
+                                                                   int8_t* __restrict__ xl, float* __restrict__ xs,
+                                                                   unsigned long long* tr, int slot) {
+  typedef typename acc_of<Q>::t A;
+  constexpr int KU_MAX = 8;
+  __shared__ A red[32];
+  __shared__ A total;
+  asm volatile("griddepcontrol.launch_dependents;" :::);  // as in rmsnorm_quant_kernel
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int vt = blockDim.x, nw = vt >> 5, KU = K / vt, u_mine = blockIdx.y;
+  const long row = blockIdx.x;
+  const float* xr = x + row * K;
+  const float gv = __ldg(g + threadIdx.x + vt * u_mine);  // independent of the previous kernel
+  trec_stamp(tr, slot, TR_START);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  trec_stamp(tr, slot, TR_WAITED);
+  float v[KU_MAX];
+#pragma unroll
+  for (int u = 0; u < KU_MAX; ++u) v[u] = u < KU ? __ldg(xr + threadIdx.x + vt * u) : 0.f;
+  A acc = 0;
+#pragma unroll
+  for (int u = 0; u < KU_MAX; ++u)
+    if (u < KU) acc = fma_acc((A)v[u], acc);
+  acc = warp_tree_sum(acc);
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    A r = lane < nw ? red[lane] : (A)0;
+    r = warp_tree_sum(r);
+    if (lane == 0) total = r;
+  }
+  __syncthreads();
+  const A den = norm_div_add(total, K, eps);
+  float mine = v[0];
+#pragma unroll
+  for (int u = 1; u < KU_MAX; ++u)
+    if (u == u_mine) mine = v[u];
+  const long i = row * K + threadIdx.x + (long)vt * u_mine;
+  const float yv = norm_scale(mine, den, gv);
+  if (xn) xn[i] = yv;
+  if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, i, i >> 5, lane);
+  trec_end(tr, slot, TK_NORM, K);
 }
 
 template <int Q>
 __global__ void quantize_kernel(const float* __restrict__ x, long groups, int8_t* __restrict__ xq,
-                                int8_t* __restrict__ xl, float* __restrict__ xs) {
+                                int8_t* __restrict__ xl, float* __restrict__ xs, unsigned long long* tr, int slot) {
   asm volatile("griddepcontrol.launch_dependents;" :::);  // as in rmsnorm_quant_kernel
+  trec_stamp(tr, slot, TR_START);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  trec_stamp(tr, slot, TR_WAITED);
   const long g = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (g >= groups) return;  // whole warps exit together
-  const int lane = threadIdx.x & 31;
-  const long i = g * 32 + lane;
-  quant_lane<Q>(__ldg(x + i), xq, xl, xs, i, g, lane);
+  if (g < groups) {  // whole warps
+    const int lane = threadIdx.x & 31;
+    const long i = g * 32 + lane;
+    quant_lane<Q>(__ldg(x + i), xq, xl, xs, i, g, lane);
+  }
+  trec_end(tr, slot, TK_QUANT, groups * 32);
+}
+
+// Option "trace" 3: the timeline buffer and this launch's record, else NULL / 0.
+static unsigned long long* tr_ptr() { return opt_trace == 3 ? trace_ptr() : nullptr; }
+static int tr_slot() { return opt_trace == 3 ? trace_next_slot() : 0; }
+
+// The small kernels run with the shared-memory carveout of the GEMV kernels
+// (the largest), so that an SM need not be reconfigured between a norm or
+// quantize launch and the GEMV that depends on it.
+template <typename F>
+static void carveout_max_shared(F f) {
+  cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+}
+
+// Launch as a programmatic dependent of the previous kernel when the option
+// "pdl" is set (the kernels wait for it before their first read of x).
+template <typename... KA, typename... A>
+static void launch_pdl(void (*f)(KA...), dim3 grid, dim3 block, cudaStream_t stream, A... args) {
+  carveout_max_shared(f);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = opt_pdl ? 1 : 0;
+  cudaLaunchKernelEx(&cfg, f, ((KA)args)...);
 }
 
 static lk_status check_act_out(lk_mode mode, const int8_t* xq, const int8_t* xl, const float* xs) {
@@ -222,16 +317,35 @@ lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, floa
   if (!x || !gain) return LK_ERR_ARG;
   if (!aligned(x, 4) || !aligned(gain, 4) || (xn && !aligned(xn, 4))) return LK_ERR_ALIGN;
   const int vt = K < 1024 ? K : 1024;  // K % 32 == 0: roundup32(K) == K
+  if (K % vt == 0 && K / vt <= 8) {
+    const dim3 grid(M, K / vt);
+    if (mode == LK_DEQUANT) {
+      if (!xn) return LK_ERR_ARG;
+      launch_pdl(rmsnorm_quant_split_kernel<0>, grid, dim3(vt), stream, x, gain, K, eps, xn, (int8_t*)nullptr,
+                 (int8_t*)nullptr, (float*)nullptr, tr_ptr(), tr_slot());
+    } else {
+      lk_status st = check_act_out(mode, xq, xl, xs);
+      if (st) return st;
+      if (mode == LK_INT8ACT)
+        launch_pdl(rmsnorm_quant_split_kernel<1>, grid, dim3(vt), stream, x, gain, K, eps, xn, xq,
+                   (int8_t*)nullptr, xs, tr_ptr(), tr_slot());
+      else
+        launch_pdl(rmsnorm_quant_split_kernel<2>, grid, dim3(vt), stream, x, gain, K, eps, xn, xq, xl, xs, tr_ptr(), tr_slot());
+    }
+    return launch_status();
+  }
   if (mode == LK_DEQUANT) {
     if (!xn) return LK_ERR_ARG;
-    rmsnorm_quant_kernel<0><<<M, vt, 0, stream>>>(x, gain, K, eps, xn, nullptr, nullptr, nullptr);
+    launch_pdl(rmsnorm_quant_kernel<0>, dim3(M), dim3(vt), stream, x, gain, K, eps, xn, (int8_t*)nullptr,
+               (int8_t*)nullptr, (float*)nullptr, tr_ptr(), tr_slot());
   } else {
     lk_status st = check_act_out(mode, xq, xl, xs);
     if (st) return st;
     if (mode == LK_INT8ACT)
-      rmsnorm_quant_kernel<1><<<M, vt, 0, stream>>>(x, gain, K, eps, xn, xq, nullptr, xs);
+      launch_pdl(rmsnorm_quant_kernel<1>, dim3(M), dim3(vt), stream, x, gain, K, eps, xn, xq, (int8_t*)nullptr,
+                 xs, tr_ptr(), tr_slot());
     else
-      rmsnorm_quant_kernel<2><<<M, vt, 0, stream>>>(x, gain, K, eps, xn, xq, xl, xs);
+      launch_pdl(rmsnorm_quant_kernel<2>, dim3(M), dim3(vt), stream, x, gain, K, eps, xn, xq, xl, xs, tr_ptr(), tr_slot());
   }
   return launch_status();
 }
@@ -249,9 +363,10 @@ lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq
   const int per_block = 8;
   const long blocks = (groups + per_block - 1) / per_block;
   if (mode == LK_INT8ACT)
-    quantize_kernel<1><<<(unsigned)blocks, 32 * per_block, 0, stream>>>(x, groups, xq, nullptr, xs);
+    launch_pdl(quantize_kernel<1>, dim3((unsigned)blocks), dim3(32 * per_block), stream, x, groups, xq,
+               (int8_t*)nullptr, xs, tr_ptr(), tr_slot());
   else
-    quantize_kernel<2><<<(unsigned)blocks, 32 * per_block, 0, stream>>>(x, groups, xq, xl, xs);
+    launch_pdl(quantize_kernel<2>, dim3((unsigned)blocks), dim3(32 * per_block), stream, x, groups, xq, xl, xs, tr_ptr(), tr_slot());
   return launch_status();
 }
 
@@ -361,6 +476,7 @@ lk_status lk_argmax(const float* logits, const uint64_t* parts, int n_parts, int
   if (parts) {
     if (n_parts < 1) return LK_ERR_SHAPE;
     if (!aligned(parts, 8)) return LK_ERR_ALIGN;
+    carveout_max_shared(argmax_reduce_kernel);
     argmax_reduce_kernel<<<M, 256, 0, stream>>>((const unsigned long long*)parts, n_parts, idx);
     return launch_status();
   }

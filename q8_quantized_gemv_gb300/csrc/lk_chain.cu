@@ -36,7 +36,28 @@ struct ChainArgs {
   long long pf_budget;        // bytes of later steps' weights each block keeps requested into L2 ahead
   int pdl;                    // launched as a programmatic dependent (a chain without barriers)
   int tslot;                  // trace 3: this launch's record in the timeline, else -1
+  // A group of GEMVs over one given activation (lk_gemv_q8_group): the ops
+  // are held here (n_inl of them) and the activation rows are copied once
+  // instead of computed by a prologue.
+  int n_inl;
+  lk_chain_op inl[LK_MAX_GROUP];
+  const float* gx;            // Dequant: f32 rows [M][K]
+  const int8_t* gxq;          // quantized: words, low words, scales
+  const int8_t* gxl;
+  const float* gxs;
 };
+
+// Step i of the chain: from the launch arguments (a group) or the ops array.
+__device__ __forceinline__ lk_chain_op chain_op_at(const ChainArgs& ca, int i) {
+  if (ca.n_inl) {
+    lk_chain_op o = ca.inl[0];
+#pragma unroll
+    for (int k = 1; k < LK_MAX_GROUP; ++k)
+      if (i == k) o = ca.inl[k];
+    return o;
+  }
+  return ca.ops[i];
+}
 
 // This block's bytes of step `o` (its rows' levels, then their scales): a
 // contiguous range of each array, since a block's rows are contiguous.
@@ -149,12 +170,12 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
 
   // The issue cursor walks this warp's stages of every step in order.
   int iop = 0;
-  Geom gi = op_geom(ca.ops[0]);
+  Geom gi = op_geom(chain_op_at(ca, 0));
   long in = 0, Ti = geom_stages(gi, warp, nwc), issued = 0;
   auto issue_next = [&]() {
     while (in >= Ti) {
       if (++iop >= ca.n_ops) return;
-      gi = op_geom(ca.ops[iop]);
+      gi = op_geom(chain_op_at(ca, iop));
       Ti = geom_stages(gi, warp, nwc);
       in = 0;
     }
@@ -168,7 +189,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
   // The barrier generation at launch.  No block can complete a barrier of
   // this launch before every block has read it (completion needs every
   // block's arrival, and a block arrives only after this read).
-  unsigned gen = threadIdx.x == 0 ? ld_acquire_gpu(ca.sync + 32) : 0u;
+  unsigned gen = threadIdx.x == 0 && ca.sync ? ld_acquire_gpu(ca.sync + 32) : 0u;
   for (int d = 0; d < D && iop < ca.n_ops; ++d) issue_next();
 
   // L2 prefetch cursor: the block's bytes of later steps (levels, then
@@ -185,11 +206,11 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     }
     long ahead = pf_off;  // bytes requested beyond step `cur`
     for (int k = cur + 1; k < pf_op && k < ca.n_ops; ++k) {
-      const PfRange r = pf_range(ca.ops[k]);
+      const PfRange r = pf_range(chain_op_at(ca, k));
       ahead += r.wbytes + r.sbytes;
     }
     while (pf_op < ca.n_ops && ahead < ca.pf_budget) {
-      const PfRange r = pf_range(ca.ops[pf_op]);
+      const PfRange r = pf_range(chain_op_at(ca, pf_op));
       const long total = r.wbytes + r.sbytes;
       const long want = ca.pf_budget - ahead;
       const long end = pf_off + want < total ? pf_off + want : total;
@@ -206,32 +227,50 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     }
   };
 
-  // weights above do not depend on the previous kernel; activations do
-  if (ca.pdl) griddep_wait();
+  // weights above do not depend on the previous kernel; activations do (the
+  // first step's prologue waits itself, after requesting its norm gains)
+  bool waited = ca.pdl == 0;
   tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_WAITED);
   long consumed = 0;
   bool ok = true;
   for (int op = 0; ok && op < ca.n_ops; ++op) {
-    const lk_chain_op o = ca.ops[op];
+    const lk_chain_op o = chain_op_at(ca, op);
     if (o.wait) prefetch_ahead(op);
     if (o.wait && !grid_sync(ca.sync, gen, gridDim.x, ca.wait_ns, ca.err, abort_flag)) {
       ok = false;
       break;
     }
-    // the activation area is rewritten below: every warp is done with the last step
-    __syncthreads();
+    // the activation area is rewritten below: every warp is done with the last
+    // step (a group keeps one activation: its warps run on through the steps)
+    if (!ca.n_inl) __syncthreads();
     CHAIN_STAMP(1 + 3 * op);
     // a step that reads the same rows with the same gain as the one before it
     // (q, k and v of a layer) reuses the activation area as it is
-    const bool same = op > 0 && !o.wait && o.x == ca.ops[op - 1].x && o.gain == ca.ops[op - 1].gain &&
-                      o.K == ca.ops[op - 1].K;
-    if (!same) {
+    const lk_chain_op prev = chain_op_at(ca, op > 0 ? op - 1 : 0);
+    const bool same = op > 0 && !o.wait && o.x == prev.x && o.gain == prev.gain && o.K == prev.K;
+    if (ca.n_inl) {
+      // a group: one load of the given activation rows, used by every step
+      if (op == 0) {
+        tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_ISSUED);
+        if (!waited) griddep_wait();
+        waited = true;
+        tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_WAITED);
+        lkh::GemvProblem pa;
+        pa.K = o.K;
+        pa.x = ca.gx;
+        pa.xq = ca.gxq;
+        pa.xl = ca.gxl;
+        pa.xs = ca.gxs;
+        load_act<Q, M>(act, (unsigned)o.K, pa, 0);
+      }
+    } else if (!same) {
       lkh::GemvProblem pr;
       pr.K = o.K;
       pr.xraw = o.x;
       pr.gain = o.gain;
       pr.eps = ca.eps;
-      fused_prologue<Q, M>(pr, nwc, 0, (unsigned)o.K, act, nred, nden);
+      fused_prologue<Q, M>(pr, nwc, 0, (unsigned)o.K, act, nred, nden, nullptr, !waited);
+      waited = true;
     }
     CHAIN_STAMP(2 + 3 * op);
     if (op == 0) tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_ACT);
@@ -269,7 +308,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
       const long i = 1024 + (long)ca.n_ops * gridDim.x + (long)op * nwc + warp;
       if (i < LK_TRACE_MAX) ca.trace[i] = gtimer();
     }
-    ok = __syncthreads_and(ok) != 0;  // every warp agrees before the next barrier
+    if (!ca.n_inl) ok = __syncthreads_and(ok) != 0;  // every warp agrees before the next barrier
     CHAIN_STAMP(3 + 3 * op);
     if (ca.trace && ca.trace_all && ca.tslot < 0 && threadIdx.x == 0) {
       const long i = 1024 + (long)op * gridDim.x + blockIdx.x;
@@ -346,24 +385,13 @@ using namespace lkring;
 
 extern "C" size_t lk_chain_sync_bytes(void) { return 256; }
 
-extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* ops_dev, int n_ops, lk_mode mode,
-                                   int M, float eps, uint32_t* sync, cudaStream_t stream) {
-  using lkh::aligned;
-  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
-  if (M < 1 || M > LK_MAX_M || n_ops < 0) return LK_ERR_SHAPE;
-  if (n_ops == 0) return LK_OK;
-  if (!ops || !ops_dev || !sync) return LK_ERR_ARG;
-  if (!aligned(ops_dev, 8) || !aligned(sync, 8)) return LK_ERR_ALIGN;
+// Launch the chain kernel over `ops` (host copies; ops_dev their device copy,
+// or NULL with the ops carried in the launch arguments: a group).
+static lk_status chain_launch(const lk_chain_op* ops, const lk_chain_op* ops_dev, int n_ops, lk_mode mode, int M,
+                              float eps, uint32_t* sync, const lkh::GemvProblem* given, cudaStream_t stream) {
   unsigned act_cap = 0, sb = 0;
   for (int i = 0; i < n_ops; ++i) {
-    const lk_chain_op& o = ops[i];
-    if (o.N < 1 || o.K < 256 || o.K % 256) return LK_ERR_SHAPE;
-    if (!o.wq || !o.ws || !o.x || !o.y || (o.argmax_idx && !o.argmax_parts)) return LK_ERR_ARG;
-    if (!aligned(o.wq, 16) || !aligned(o.ws, 16) || !aligned(o.x, 4) || (o.gain && !aligned(o.gain, 4)) ||
-        !aligned(o.y, 4) || (o.argmax_parts && !aligned(o.argmax_parts, 8)) ||
-        (o.argmax_idx && !aligned(o.argmax_idx, 4)))
-      return LK_ERR_ALIGN;
-    const unsigned a = act_area_rt(mode, M, (unsigned)o.K), s = stage_bytes_for(o.K);
+    const unsigned a = act_area_rt(mode, M, (unsigned)ops[i].K), s = stage_bytes_for(ops[i].K);
     act_cap = a > act_cap ? a : act_cap;
     sb = s > sb ? s : sb;
   }
@@ -411,6 +439,18 @@ extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* op
   ca.trace_all = lkh::opt_trace == 2;
   ca.tslot = lkh::opt_trace == 3 ? lkh::trace_next_slot() : -1;
   ca.pdl = !barrier && lkh::opt_pdl ? 1 : 0;
+  ca.n_inl = 0;
+  ca.gx = nullptr;
+  ca.gxq = ca.gxl = nullptr;
+  ca.gxs = nullptr;
+  for (int i = 0; i < LK_MAX_GROUP; ++i) ca.inl[i] = ops[i < n_ops ? i : 0];
+  if (given) {
+    ca.n_inl = n_ops;
+    ca.gx = given->x;
+    ca.gxq = given->xq;
+    ca.gxl = given->xl;
+    ca.gxs = given->xs;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d->sm_count);
   cfg.blockDim = dim3(w * 32);
@@ -428,4 +468,40 @@ extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* op
   cfg.numAttrs = (barrier || ca.pdl) ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, f, ca) != cudaSuccess) return LK_ERR_CUDA;
   return lkh::launch_status();
+}
+
+extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* ops_dev, int n_ops, lk_mode mode,
+                                   int M, float eps, uint32_t* sync, cudaStream_t stream) {
+  using lkh::aligned;
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+  if (M < 1 || M > LK_MAX_M || n_ops < 0) return LK_ERR_SHAPE;
+  if (n_ops == 0) return LK_OK;
+  if (!ops || !ops_dev || !sync) return LK_ERR_ARG;
+  if (!aligned(ops_dev, 8) || !aligned(sync, 8)) return LK_ERR_ALIGN;
+  for (int i = 0; i < n_ops; ++i) {
+    const lk_chain_op& o = ops[i];
+    if (o.N < 1 || o.K < 256 || o.K % 256) return LK_ERR_SHAPE;
+    if (!o.wq || !o.ws || !o.x || !o.y || (o.argmax_idx && !o.argmax_parts)) return LK_ERR_ARG;
+    if (!aligned(o.wq, 16) || !aligned(o.ws, 16) || !aligned(o.x, 4) || (o.gain && !aligned(o.gain, 4)) ||
+        !aligned(o.y, 4) || (o.argmax_parts && !aligned(o.argmax_parts, 8)) ||
+        (o.argmax_idx && !aligned(o.argmax_idx, 4)))
+      return LK_ERR_ALIGN;
+  }
+  return chain_launch(ops, ops_dev, n_ops, mode, M, eps, sync, nullptr, stream);
+}
+
+// A group of GEMVs over one given activation (p: K, mode, M and the
+// activation) on the chain kernel, in one launch without barriers.
+// LK_ERR_SHAPE when the chain kernel does not take the shape.
+lk_status lkh::chain_group(const GemvProblem& p, const lk_gemv_target* t, int n, cudaStream_t stream) {
+  if (n < 1 || n > LK_MAX_GROUP || p.K < 256 || p.K % 256 || p.M < 1 || p.M > LK_MAX_M) return LK_ERR_SHAPE;
+  if (p.mode == LK_DEQUANT ? !aligned(p.x, 16)
+                           : (!aligned(p.xq, 16) || !aligned(p.xs, 16) || (p.mode == LK_TWOPASS && !aligned(p.xl, 16))))
+    return LK_ERR_SHAPE;
+  lk_chain_op ops[LK_MAX_GROUP];
+  for (int i = 0; i < n; ++i) {
+    if (!aligned(t[i].wq, 16) || !aligned(t[i].ws, 16)) return LK_ERR_SHAPE;
+    ops[i] = lk_chain_op{t[i].wq, t[i].ws, t[i].N, p.K, nullptr, nullptr, t[i].y, nullptr, nullptr, 0, 0};
+  }
+  return chain_launch(ops, nullptr, n, (lk_mode)p.mode, p.M, 0.f, nullptr, &p, stream);
 }

@@ -27,6 +27,35 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
   return v;
 }
 
+// ---- launch timeline records (option "trace" 3) ---------------------------------
+// Record `slot` holds TREC entries: [0] block 0 start, [1] block 0 past the
+// dependency wait, [2] block 0's activation ready, [3] the last block's end,
+// [4] block 0's end, [5] kernel kind, [6] rows (or K), [7] block 0's first
+// weight stages issued (GEMV kernels).
+constexpr int TREC = 8;
+enum : int { TR_START = 0, TR_WAITED = 1, TR_ACT = 2, TR_END_MAX = 3, TR_END0 = 4, TR_KIND = 5, TR_ROWS = 6,
+             TR_ISSUED = 7 };
+enum : int { TK_RING = 1, TK_CHAIN = 2, TK_MMA = 3, TK_NORM = 4, TK_QUANT = 5 };
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Small kernels' records without a block barrier: thread 0 of every block.
+__device__ __forceinline__ void trec_stamp(unsigned long long* tr, int slot, int i) {
+  if (tr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) tr[slot * TREC + i] = globaltimer_ns();
+}
+__device__ __forceinline__ void trec_end(unsigned long long* tr, int slot, int kind, long rows) {
+  if (!tr || threadIdx.x != 0) return;
+  const unsigned long long now = globaltimer_ns();
+  atomicMax(tr + slot * TREC + TR_END_MAX, now);
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    tr[slot * TREC + TR_END0] = now;
+    tr[slot * TREC + TR_KIND] = (unsigned long long)kind;
+    tr[slot * TREC + TR_ROWS] = (unsigned long long)rows;
+  }
+}
+
 // ---- the canonical sum tree ("kernels.rs" lk_warp_sum) -------------------------
 // Lane l adds lane l+d for d = 16, 8, 4, 2, 1; lane 0 ends with the total.
 template <typename A>
@@ -67,6 +96,50 @@ __device__ __forceinline__ void quant_lane(float v, int8_t* __restrict__ hi, int
     l = l > 127 ? 127 : (l < -128 ? -128 : l);
     hi[i] = (int8_t)h;
     lo[i] = (int8_t)l;
+  }
+}
+
+// quant_lane for four groups at once (groups g + k*step, k < 4, stored where
+// ok[k]): the same operations, written phase by phase so that the four
+// groups' independent chains interleave.  Element i of group G is 32G + lane.
+template <int Q>
+__device__ __forceinline__ void quant_lanes4(const float (&v)[4], const bool (&ok)[4], int8_t* __restrict__ hi,
+                                             int8_t* __restrict__ lo, float* __restrict__ xs, int g, int step,
+                                             int lane) {
+  float a[4], s[4];
+  int h[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) a[k] = warp_absmax(v[k]);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    s[k] = Q == 1 ? (a[k] > 0.f ? __fdiv_rn(a[k], 127.0f) : 1.0f) : __fdiv_rn(a[k] > 1e-30f ? a[k] : 1e-30f, 127.0f);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = __float2int_rn(__fdiv_rn(v[k], s[k]));
+  if (Q == 1) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (ok[k]) {
+        const int G = g + k * step;
+        hi[32 * G + lane] = (int8_t)h[k];
+        if (lane == 0) xs[G] = s[k];
+      }
+  } else {
+    int l[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      h[k] = h[k] > 127 ? 127 : (h[k] < -128 ? -128 : h[k]);
+      const float r = __fmaf_rn(-(float)h[k], s[k], v[k]);
+      l[k] = __float2int_rn(__fdiv_rn(r, __fmul_rn(s[k], 0.0078125f)));
+      l[k] = l[k] > 127 ? 127 : (l[k] < -128 ? -128 : l[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (ok[k]) {
+        const int G = g + k * step;
+        hi[32 * G + lane] = (int8_t)h[k];
+        lo[32 * G + lane] = (int8_t)l[k];
+        if (lane == 0) xs[G] = s[k];
+      }
   }
 }
 

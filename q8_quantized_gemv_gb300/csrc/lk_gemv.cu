@@ -310,6 +310,11 @@ lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode 
     }
     return mma_launch(p, n, wq, ws, N, y, stream, nullptr);
   }
+  // one chain launch (the ring kernel's arrangement) where it takes the shape
+  if (n > 1 && (opt_gemv_path == 0 || opt_gemv_path == 2)) {
+    const lk_status st = chain_group(p, targets, n, stream);
+    if (st != LK_ERR_SHAPE) return st;
+  }
   for (int i = 0; i < n; ++i) {
     lk_status st = lk_gemv_q8(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M, targets[i].y,
                               nullptr, nullptr, stream);

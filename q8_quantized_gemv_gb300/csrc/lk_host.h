@@ -83,6 +83,10 @@ void trace_reset();
 lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts);
 bool ring_supports(const GemvProblem& p);
 
+// Several GEMVs over one given activation on the chain kernel (lk_chain.cu):
+// one launch; LK_ERR_SHAPE when the chain kernel does not take the shape.
+lk_status chain_group(const GemvProblem& p, const lk_gemv_target* t, int n, cudaStream_t stream);
+
 // Tensor-core kernel for 2..8 activation rows (lk_mma.cu), same contract.
 lk_status mma_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts);
 // The same over nmat matrices sharing p's activation, in one launch.

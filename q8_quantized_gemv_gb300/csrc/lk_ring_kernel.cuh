@@ -148,8 +148,6 @@ __device__ __forceinline__ void bulk(void* dst, const void* src, unsigned bytes,
 // of TREC entries: [0] block 0 start, [1] block 0 past the dependency wait,
 // [2] block 0's activation ready, [3] the last block's end (max over blocks),
 // [4] block 0's end, [5] kernel kind, [6] rows.
-constexpr int TREC = 8;
-enum : int { TR_START = 0, TR_WAITED = 1, TR_ACT = 2, TR_END_MAX = 3, TR_END0 = 4, TR_KIND = 5, TR_ROWS = 6 };
 __device__ __forceinline__ void tstamp(unsigned long long* tr, int slot, int i) {
   if (tr && blockIdx.x == 0 && threadIdx.x == 0) tr[(slot < 0 ? 0 : slot * TREC) + i] = gtimer_();
 }
@@ -198,6 +196,23 @@ __device__ __forceinline__ float ld_keep(const float* p) {
 }
 __device__ __forceinline__ void compiler_fence() { asm volatile("" ::: "memory"); }
 
+// store_act for the four groups g, g + step, g + 2 step, g + 3 step (those
+// with ok set), their quantizer steps in lockstep.
+template <int Q, int M>
+__device__ __forceinline__ void store_act4(unsigned char* act, unsigned L, int t, int g, int step, int lane,
+                                           const float (&v)[4], const bool (&ok)[4]) {
+  if constexpr (Q == 0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (ok[k]) ((float*)act)[(size_t)t * L + 32 * (g + k * step) + lane] = v[k];
+  } else {
+    int8_t* XQ = (int8_t*)act + (size_t)t * L;
+    int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
+    float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
+    quant_lanes4<Q>(v, ok, XQ, XL, XS, g, step, lane);
+  }
+}
+
 template <int Q, int M>
 __device__ __forceinline__ void store_act(unsigned char* act, unsigned L, int t, int g, int lane, float v) {
   const int i = 32 * g + lane;
@@ -217,9 +232,13 @@ __device__ __forceinline__ void pstamp(unsigned long long* dbg, int i) {
   if (dbg && blockIdx.x == 0 && threadIdx.x == 0) dbg[i] = gtimer();
 }
 
+// wait_first: the caller has not yet waited for the previous kernel
+// (programmatic dependent launch); the first batch's gains, which do not
+// depend on it, are requested before the wait, the values after it.
 template <int Q, int M>
 __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, unsigned L, unsigned char* act,
-                               void* red_raw, void* den_raw, unsigned long long* dbg = nullptr) {
+                               void* red_raw, void* den_raw, unsigned long long* dbg = nullptr,
+                               bool wait_first = false) {
   typedef typename acc_of<Q>::t A;
   constexpr int QB = PRO_SLOTS;  // groups a warp quantizes per batch
   constexpr int KU_MAX = 8;      // values per virtual thread kept in registers (K <= 8192)
@@ -238,16 +257,29 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
     // gains are requested before anything else, so their round trip overlaps
     // the sum of squares below
     float qx[QB], qg[QB];
-    auto load_batch = [&](int g0) {
+    auto load_gains = [&](int g0) {
+#pragma unroll
+      for (int b = 0; b < QB; ++b) {
+        const int g = g0 + b * nwc, i = 32 * g + lane;
+        const bool in = g < ng && k_lo + i < K;
+        qg[b] = (norm && in) ? ld_keep(a.gain + k_lo + i) : 1.f;
+      }
+    };
+    auto load_values = [&](int g0) {
 #pragma unroll
       for (int b = 0; b < QB; ++b) {
         const int g = g0 + b * nwc, i = 32 * g + lane;
         const bool in = g < ng && k_lo + i < K;
         qx[b] = in ? ld_keep(xr + k_lo + i) : 0.f;
-        qg[b] = (norm && in) ? ld_keep(a.gain + k_lo + i) : 1.f;
       }
     };
-    load_batch(cw);
+    auto load_batch = [&](int g0) {
+      load_gains(g0);
+      load_values(g0);
+    };
+    load_gains(cw);
+    if (t == 0 && wait_first) griddep_wait();
+    load_values(cw);
     // (2) the norm's sum of squares: virtual warp w (played by warp w mod
     // nwc), lane l adds the squares of values 32w + l + vt*u in ascending u;
     // the next virtual warp's values are requested before this one's sum
@@ -291,18 +323,25 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
       pstamp(dbg, 2);
     }
     const A dn = norm ? den[t] : (A)1;
-    // (3) normalize and quantize, batch by batch
+    // (3) normalize and quantize, batch by batch, four groups at a time in
+    // lockstep (their division chains interleave)
     for (int g0 = cw; g0 < ng; g0 += QB * nwc) {
       if (g0 != cw) load_batch(g0);
       compiler_fence();
 #pragma unroll
-      for (int b = 0; b < QB; ++b) {
-        const int g = g0 + b * nwc;
-        if (g >= ng) break;  // warp-uniform
-        float v = qx[b];
-        // past the row's end (a chunk narrower than the area) the area keeps zeros
-        if (norm && k_lo + 32 * g + lane < K) v = norm_scale(v, dn, qg[b]);
-        store_act<Q, M>(act, L, t, g, lane, v);
+      for (int b0 = 0; b0 < QB; b0 += 4) {
+        if (g0 + b0 * nwc >= ng) break;  // warp-uniform: the chunk is empty
+        float v[4];
+        bool ok[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int g = g0 + (b0 + k) * nwc;
+          ok[k] = g < ng;
+          v[k] = qx[b0 + k];
+          // past the row's end (a chunk narrower than the area) the area keeps zeros
+          if (norm && k_lo + 32 * g + lane < K) v[k] = norm_scale(v[k], dn, qg[b0 + k]);
+        }
+        store_act4<Q, M>(act, L, t, g0 + b0 * nwc, nwc, lane, v, ok);
       }
     }
     pstamp(dbg, 3);
@@ -406,6 +445,49 @@ __device__ __forceinline__ void prefetch_stage(const Geom& g, int warp, int nwc,
       bulk_prefetch_l2(g.ws + ((row * g.nb + b0) * 2 - sh), slen);
     }
   }
+}
+
+// 16-byte load from L2 (not L1): for data an earlier kernel wrote.
+__device__ __forceinline__ uint4 ld_cg16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// The activation area of M rows over [k_lo, k_lo + L) (L a multiple of 128,
+// k_lo of 128) loaded by every thread of the block with 16-byte L2 loads:
+// int8 words (and low words) and f32 scales, or f32 values under Dequant, in
+// the layout Act describes.  Plain loads rather than a bulk copy: a bulk copy
+// issued after the block's weight stages completes only after them (the
+// copy engine serves a block's copies in order), which held the activation
+// back by the whole ring fill, several microseconds.
+template <int Q, int M>
+__device__ __forceinline__ void load_act(unsigned char* act, unsigned L, const lkh::GemvProblem& a, int k_lo) {
+  const int K = a.K, nb = K >> 5, b_lo = k_lo >> 5;
+  if constexpr (Q == 0) {
+    const int per = (int)L / 4;  // 16-byte runs per row
+    for (int i = threadIdx.x; i < M * per; i += blockDim.x) {
+      const int t = i / per, c = i - t * per;
+      *(uint4*)(act + ((size_t)t * L + 4 * c) * 4) = ld_cg16(a.x + (long)t * K + k_lo + 4 * c);
+    }
+  } else {
+    const int per = (int)L / 16, pers = (int)L / 128;
+    const int nw = M * per * (Q == 2 ? 2 : 1);
+    for (int i = threadIdx.x; i < nw + M * pers; i += blockDim.x) {
+      if (i < nw) {
+        const int lo = Q == 2 && i >= M * per;
+        const int j = lo ? i - M * per : i;
+        const int t = j / per, c = j - t * per;
+        *(uint4*)(act + (lo ? (size_t)M * L : 0) + (size_t)t * L + 16 * c) =
+            ld_cg16((lo ? a.xl : a.xq) + (long)t * K + k_lo + 16 * c);
+      } else {
+        const int j = i - nw, t = j / pers, c = j - t * pers;
+        *(uint4*)(act + (size_t)M * L * (Q == 2 ? 2 : 1) + (size_t)t * (L / 8) + 16 * c) =
+            ld_cg16(a.xs + (long)t * nb + b_lo + 4 * c);
+      }
+    }
+  }
+  __syncthreads();
 }
 
 // The activation area of M rows over `L` bytes of K: int8 words (and low
@@ -536,7 +618,6 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   double* nred = (double*)(keys + LK_MAX_M * MAXW);                        // [M][32]
   double* nden = nred + LK_MAX_M * 32;                                     // [M]
   const unsigned full0 = smem_u32(bars);
-  const unsigned act_bar = smem_u32(bars + MAX_STAGES);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int K = a.K, nb = K >> 5;
@@ -555,7 +636,6 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(full0 + 8 * s, 1);
-    mbar_init(act_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -571,33 +651,18 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   // the next stages into L2, so that HBM keeps streaming while the block
   // waits for the previous kernel and runs its prologue
   for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m) prefetch_stage(g, warp, nwc, m, lane);
+  tstamp(ra.trace, ra.tslot, TR_ISSUED);
 
-  if (ra.pdl) griddep_wait();  // from here on: reads of activations, writes of outputs
+  // from the dependency wait on: reads of activations, writes of outputs (the
+  // fused prologue waits itself, after requesting the norm gains)
+  if (ra.pdl && !FUSE) griddep_wait();
   tstamp(ra.trace, ra.tslot, TR_WAITED);
   bool ok = true;
   if (FUSE) {
-    fused_prologue<Q, M>(a, nwc, k_lo, L, act, nred, nden, ra.trace && ra.tslot < 0 ? ra.trace + 32 : nullptr);
+    fused_prologue<Q, M>(a, nwc, k_lo, L, act, nred, nden, ra.trace && ra.tslot < 0 ? ra.trace + 32 : nullptr,
+                         ra.pdl != 0);
   } else if (L > 0) {
-    if (warp == 0) {
-      const unsigned long long pol_a = evict_last_policy();
-      if (lane == 0) mbar_arrive_expect_tx(act_bar, act_area<Q, M>(L));
-      __syncwarp();
-      if (Q == 0) {
-        if (lane < M) bulk(act + (size_t)lane * L * 4, a.x + (long)lane * K + k_lo, L * 4, act_bar, pol_a);
-      } else {
-        if (lane < M) bulk(act + (size_t)lane * L, a.xq + (long)lane * K + k_lo, L, act_bar, pol_a);
-        if (Q == 2 && lane >= 8 && lane < 8 + M)
-          bulk(act + (size_t)M * L + (lane - 8) * L, a.xl + (long)(lane - 8) * K + k_lo, L, act_bar, pol_a);
-        if (lane >= 16 && lane < 16 + M) {
-          const int t = lane - 16;
-          bulk(act + (size_t)M * L * (Q == 2 ? 2 : 1) + t * (L / 8), a.xs + (long)t * nb + b_lo, L / 8, act_bar,
-               pol_a);
-        }
-      }
-      __syncwarp();
-    }
-    ok = __all_sync(FULL, mbar_wait(act_bar, 0, ra.wait_ns, abort_flag));
-    if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
+    load_act<Q, M>(act, L, a, k_lo);
   }
 
   const Act ac{act, L};
@@ -636,7 +701,6 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   if (lane == 0) {
     for (long m = n; m < issued; ++m)
       drain_wait(full0 + 8 * (unsigned)(warp * D + m % D), (unsigned)(m / D) & 1u, ra.wait_ns, ra.err);
-    if (!FUSE && L > 0 && warp == 0) drain_wait(act_bar, 0, ra.wait_ns, ra.err);
   }
   __syncwarp();
   if (!SPLIT && a.amax) {

@@ -24,7 +24,7 @@ from . import lk, synth
 class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
                  batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
-                 fused=True, chain=False, group_qkv=True):
+                 fused=False, chain=False, group_qkv=True):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
         dev = self.dev
@@ -70,7 +70,7 @@ class DecodeStack:
         # fused steps), where every step fits
         self.x_buf = self.x0.clone()  # the token's input rows
         self.chain = None
-        if chain and fused and all(ring.values()):
+        if chain and all(ring.values()):
             self.chain = lk.Chain(self._chain_ops(), dev)
         # q, k and v of a layer as one grouped launch (a chain without
         # barriers: one prologue, the three weight streams back to back)

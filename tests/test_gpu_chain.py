@@ -48,11 +48,14 @@ def oracle_token(st):
     return outs, x, logits
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("batch", [1, 3])
-def test_chain_matches_launches_and_oracle(mode, batch):
+def test_chain_matches_launches_and_oracle(mode, batch, fused):
+    """The chain against the per-launch sequence, with separate norm/quantize
+    launches (fused False) or the GEMVs' own prologue (True)."""
     a = DecodeStack(**SMALL, batch=batch, mode=mode, chain=True)
-    b = DecodeStack(**SMALL, batch=batch, mode=mode, chain=False)
+    b = DecodeStack(**SMALL, batch=batch, mode=mode, chain=False, fused=fused)
     assert a.chain is not None and b.chain is None
     ia = a.run_token().clone()
     ib = b.run_token().clone()
@@ -118,12 +121,14 @@ def test_chain_barrier_timeout_is_reported_and_recoverable():
     assert torch.equal(a.logits.view(torch.int32), ref.view(torch.int32))
 
 
-def test_grouped_qkv_pdl_graph_matches_plain():
-    """The per-launch sequence with q, k, v as one grouped launch: captured
-    with programmatic dependent launches in a graph, it gives the same bits
-    as launched plainly, and the oracle's token."""
-    a = DecodeStack(**SMALL, batch=1, mode=1, chain=False)
-    assert a.qkv is not None
+@pytest.mark.parametrize("fused", [False, True])
+def test_grouped_qkv_pdl_graph_matches_plain(fused):
+    """The per-launch sequence with q, k, v as one grouped launch (after one
+    norm launch, or with the fused prologue): captured with programmatic
+    dependent launches in a graph, it gives the same bits as launched plainly,
+    and the oracle's token."""
+    a = DecodeStack(**SMALL, batch=1, mode=1, chain=False, fused=fused)
+    assert (a.qkv is not None) == fused
     lk.lk_set_option("pdl", 0)
     a.run_token()
     torch.cuda.synchronize()
