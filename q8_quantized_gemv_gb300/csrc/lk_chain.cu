@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
         pa.xq = ca.gxq;
         pa.xl = ca.gxl;
         pa.xs = ca.gxs;
-        load_act<Q, M>(act, (unsigned)o.K, pa, 0);
+        load_act<Q, M, 2>(act, (unsigned)o.K, pa, 0);
       }
     } else if (!same) {
       lkh::GemvProblem pr;

@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   volatile int* abort_flag = (volatile int*)(bars + MST + 1);
   unsigned long long* keys = (unsigned long long*)(bars + MST + 3);  // [TN][MW]
   const unsigned full0 = smem_u32(bars);
+  const unsigned act_bar = smem_u32(bars + MST);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
 
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(full0 + 8 * s, 1);
+    mbar_init(act_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -258,44 +260,63 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   if (A16) {
     // every thread converts 16-byte runs of the int8 rows into f16 rows
     const int runs = K >> 4, nrun = M * runs * (Q == 2 ? 2 : 1);
-    for (int i = threadIdx.x; i < nrun; i += blockDim.x) {
-      const int lo = Q == 2 && i >= M * runs;
-      const int j = lo ? i - M * runs : i;
-      const int row = j / runs, off = (j - row * runs) << 4;
-      const int8_t* src = (lo ? a.xl : a.xq) + (long)row * K + off;
-      const uint4 v = ld_nc16(src);
-      uint4 h0, h1;
-      i8x4_to_h2(v.x, h0.x, h0.y);
-      i8x4_to_h2(v.y, h0.z, h0.w);
-      i8x4_to_h2(v.z, h1.x, h1.y);
-      i8x4_to_h2(v.w, h1.z, h1.w);
-      uint4* dst = (uint4*)(act + (lo ? ra.a_lo : 0u) + (size_t)row * ra.ar + 2 * off);
-      dst[0] = h0;
-      dst[1] = h1;
+    constexpr int U = 4;  // loads in flight per thread
+    for (int i0 = threadIdx.x; i0 < nrun; i0 += U * blockDim.x) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < nrun) {
+          const int lo = Q == 2 && i >= M * runs;
+          const int j = lo ? i - M * runs : i;
+          const int row = j / runs, off = (j - row * runs) << 4;
+          v[u] = ld_cg16((lo ? a.xl : a.xq) + (long)row * K + off);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < nrun) {
+          const int lo = Q == 2 && i >= M * runs;
+          const int j = lo ? i - M * runs : i;
+          const int row = j / runs, off = (j - row * runs) << 4;
+          uint4 h0, h1;
+          i8x4_to_h2(v[u].x, h0.x, h0.y);
+          i8x4_to_h2(v[u].y, h0.z, h0.w);
+          i8x4_to_h2(v[u].z, h1.x, h1.y);
+          i8x4_to_h2(v[u].w, h1.z, h1.w);
+          uint4* dst = (uint4*)(act + (lo ? ra.a_lo : 0u) + (size_t)row * ra.ar + 2 * off);
+          dst[0] = h0;
+          dst[1] = h1;
+        }
+      }
     }
     for (int i = threadIdx.x; i < M * nb; i += blockDim.x) {
       const int row = i / nb, b = i - row * nb;
       ((float*)(act + ra.a_xs))[(size_t)row * ra.xsr + b] = __ldg(a.xs + (long)row * nb + b);
     }
     __syncthreads();
-  } else {
-    // int8 rows as they are, by 16-byte L2 loads (a bulk copy would complete
-    // only after the weight stages issued before it)
-    const int runs = K >> 4, nrun = M * runs * (Q == 2 ? 2 : 1);
-    for (int i = threadIdx.x; i < nrun; i += blockDim.x) {
-      const int lo = Q == 2 && i >= M * runs;
-      const int j = lo ? i - M * runs : i;
-      const int row = j / runs, off = (j - row * runs) << 4;
-      *(uint4*)(act + (lo ? ra.a_lo : 0u) + (size_t)row * ra.ar + off) = ld_cg16((lo ? a.xl : a.xq) + (long)row * K + off);
-    }
-    const int sruns = nb >> 2;
-    for (int i = threadIdx.x; i < M * sruns; i += blockDim.x) {
-      const int row = i / sruns, c = i - row * sruns;
-      *(uint4*)(act + ra.a_xs + (size_t)row * ra.xsr * 4 + 16 * c) = ld_cg16(a.xs + (long)row * nb + 4 * c);
-    }
-    __syncthreads();
+  } else if (warp == 0) {
+    // int8 rows as they are, by bulk copies: with few warps (long K, few
+    // tiles) plain loads of up to 200 KB take several round trips, while
+    // the copies' wait behind the weight stages issued before them is short
+    const unsigned long long pol_a = evict_last_policy();
+    if (lane == 0)
+      mbar_arrive_expect_tx(act_bar, (unsigned)M * ((unsigned)K * (Q == 2 ? 2u : 1u) + (unsigned)nb * 4u));
+    __syncwarp();
+    if (lane < M) bulk(act + (size_t)lane * ra.ar, a.xq + (long)lane * K, (unsigned)K, act_bar, pol_a);
+    if (Q == 2 && lane >= 8 && lane < 8 + M)
+      bulk(act + ra.a_lo + (size_t)(lane - 8) * ra.ar, a.xl + (long)(lane - 8) * K, (unsigned)K, act_bar, pol_a);
+    if (lane >= 16 && lane < 16 + M)
+      bulk(act + ra.a_xs + (size_t)(lane - 16) * ra.xsr * 4, a.xs + (long)(lane - 16) * nb, (unsigned)nb * 4u,
+           act_bar, pol_a);
+    __syncwarp();
   }
   bool ok = true;
+  if (!A16) {
+    ok = __all_sync(FULL, mbar_wait(act_bar, 0, ra.wait_ns, abort_flag));
+    if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
+  }
 
   tstamp(ra.trace, ra.tslot, TR_ACT);
   // activation row g's words and the scales of activation rows 2t, 2t+1
@@ -438,6 +459,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
         cph ^= 1u;
       }
     }
+    if (!A16 && warp == 0) drain_wait(act_bar, 0, ra.wait_ns, ra.err);
   }
   __syncwarp();
   if (a.amax) {

@@ -461,29 +461,52 @@ __device__ __forceinline__ uint4 ld_cg16(const void* p) {
 // issued after the block's weight stages completes only after them (the
 // copy engine serves a block's copies in order), which held the activation
 // back by the whole ring fill, several microseconds.
-template <int Q, int M>
+template <int Q, int M, int U = (M >= 4 ? 8 : 2)>  // U: loads in flight per thread
 __device__ __forceinline__ void load_act(unsigned char* act, unsigned L, const lkh::GemvProblem& a, int k_lo) {
   const int K = a.K, nb = K >> 5, b_lo = k_lo >> 5;
-  if constexpr (Q == 0) {
-    const int per = (int)L / 4;  // 16-byte runs per row
-    for (int i = threadIdx.x; i < M * per; i += blockDim.x) {
+  // 16-byte run i: its source and its place in the area
+  auto run = [&](int i, const void*& src, unsigned char*& dst) {
+    if constexpr (Q == 0) {
+      const int per = (int)L / 4;
       const int t = i / per, c = i - t * per;
-      *(uint4*)(act + ((size_t)t * L + 4 * c) * 4) = ld_cg16(a.x + (long)t * K + k_lo + 4 * c);
-    }
-  } else {
-    const int per = (int)L / 16, pers = (int)L / 128;
-    const int nw = M * per * (Q == 2 ? 2 : 1);
-    for (int i = threadIdx.x; i < nw + M * pers; i += blockDim.x) {
+      src = a.x + (long)t * K + k_lo + 4 * c;
+      dst = act + ((size_t)t * L + 4 * c) * 4;
+    } else {
+      const int per = (int)L / 16, pers = (int)L / 128, nw = M * per * (Q == 2 ? 2 : 1);
       if (i < nw) {
         const int lo = Q == 2 && i >= M * per;
         const int j = lo ? i - M * per : i;
         const int t = j / per, c = j - t * per;
-        *(uint4*)(act + (lo ? (size_t)M * L : 0) + (size_t)t * L + 16 * c) =
-            ld_cg16((lo ? a.xl : a.xq) + (long)t * K + k_lo + 16 * c);
+        src = (lo ? a.xl : a.xq) + (long)t * K + k_lo + 16 * c;
+        dst = act + (lo ? (size_t)M * L : 0) + (size_t)t * L + 16 * c;
       } else {
         const int j = i - nw, t = j / pers, c = j - t * pers;
-        *(uint4*)(act + (size_t)M * L * (Q == 2 ? 2 : 1) + (size_t)t * (L / 8) + 16 * c) =
-            ld_cg16(a.xs + (long)t * nb + b_lo + 4 * c);
+        src = a.xs + (long)t * nb + b_lo + 4 * c;
+        dst = act + (size_t)M * L * (Q == 2 ? 2 : 1) + (size_t)t * (L / 8) + 16 * c;
+      }
+    }
+  };
+  const int nrun = Q == 0 ? M * (int)L / 4 : M * (int)L / 16 * (Q == 2 ? 2 : 1) + M * (int)L / 128;
+  for (int i0 = threadIdx.x; i0 < nrun; i0 += U * blockDim.x) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * blockDim.x;
+      const void* src;
+      unsigned char* dst;
+      if (i < nrun) {
+        run(i, src, dst);
+        v[u] = ld_cg16(src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * blockDim.x;
+      const void* src;
+      unsigned char* dst;
+      if (i < nrun) {
+        run(i, src, dst);
+        *(uint4*)dst = v[u];
       }
     }
   }
