@@ -13,8 +13,8 @@ argmax reduce), about 8.04 GB of Q8_0 weights per token, batch 1 (or
                   HBM, nothing fits the 129 MB L2)
   e2e             the same metric with the token input copied from pinned
                   host memory and the argmax read back to the host every step
-  roofline        the fused gate/up GEMV launches (the largest share of the
-                  token's bytes), timed with CUDA events around each launch
+  roofline        the gate/up GEMV launches (the largest share of a layer's
+                  bytes), timed with CUDA events around each launch
   cpu_baseline    the CPU oracle on a bounded sample of the same sequence
 
 ``--impl reference`` times the CPU oracle (the reference arm of this
@@ -595,26 +595,31 @@ def roofline_chain(stack, stream, a, torch):
             {"chain": {"us": us, "GB/s": achieved, "launches": steps}})
 
 
-def profile_traffic(key):
-    """A DRAM-traffic figure from profiles/traffic.txt (one ncu capture), if it
-    was taken on the current library sources (else None)."""
+def profile_traffic(key, kind):
+    """A DRAM-traffic figure (bytes per launch) from profiles/traffic.txt (one
+    ncu capture), if it was taken on the current sources of that kernel
+    family (else None).  Lines: "<key>: <bytes> <family>=<sha256>"."""
     try:
         from q8_quantized_gemv_gb300 import build
-        rec = {}
         with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             for line in f:
-                if ":" in line and not line.startswith("#"):
-                    k, v = line.split(":", 1)
-                    rec[k.strip()] = v.strip()
-        if rec.get("sources_sha256") != build.sources_digest():
-            return None
-        return float(rec[key])
+                if line.startswith("#") or ":" not in line:
+                    continue
+                k, v = line.split(":", 1)
+                if k.strip() != key:
+                    continue
+                val, tag = v.split()
+                fam, sha = tag.split("=")
+                if fam != kind or sha != build.sources_digest(kind):
+                    return None
+                return float(val)
     except (OSError, KeyError, ValueError, AttributeError):
         return None
+    return None
 
 
 def chain_traffic(alg):
-    r = profile_traffic("gemv_chain_2layers_int8act_per_algorithmic_byte")
+    r = profile_traffic("gemv_chain_2layers_int8act_per_algorithmic_byte", "chain")
     return None if r is None else r * alg
 
 
@@ -670,12 +675,15 @@ def roofline(stack, stream, a, torch):
         per[name] = {"us": avg * 1e3, "GB/s": alg_bytes(name) / (avg * 1e-3) / 1e9, "launches": len(ts)}
     gu = per["gu"]
     peak = peaks["hbm_gbs"]
-    traffic = None
-    if stack.mode == 1 and stack.B == 1 and stack.fused["gu"]:
-        traffic = profile_traffic("gemv_ring_fused_gateup_24576x4096_int8act")
+    kname = "ring_fused" if stack.fused["gu"] else {1: "direct", 2: "ring", 3: "mma"}.get(stack.kernel["gu"], "none")
+    mname = {0: "dequant", 1: "int8act", 2: "twopass"}[stack.mode]
+    # DRAM bytes per launch from one ncu capture of this kernel and shape, if
+    # taken on the current sources (profiles/traffic.txt), else null
+    traffic = profile_traffic(f"gemv_{kname}_gateup_24576x4096_{mname}_b{stack.B}",
+                              "mma" if kname == "mma" else "ring")
     roof = {"bound": "hbm", "achieved": gu["GB/s"], "peak": peak, "unit": "GB/s",
             "frac": gu["GB/s"] / peak, "traffic": traffic, "peak_source": src,
-            "kernel": "fused gate/up GEMV 24576x4096", "algorithmic_bytes_per_launch": alg_bytes("gu"),
+            "kernel": f"gate/up GEMV 24576x4096 ({kname} kernel)", "algorithmic_bytes_per_launch": alg_bytes("gu"),
             "avg_launch_us": gu["us"], "launches_timed": gu["launches"]}
     tot_b = sum(alg_bytes(n) * len(ts) for n, ts in times.items())
     tot_t = sum(sum(ts) for ts in times.values())

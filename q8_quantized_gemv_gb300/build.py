@@ -35,12 +35,27 @@ def _headers():
                   glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def sources_digest() -> str:
-    """sha256 over the library's sources and headers (identifies the kernels
-    that a stored profile was taken on)."""
+# The files that make each kernel family (a stored profile of one stays valid
+# while these are unchanged).
+KERNEL_FILES = {
+    "ring": ["lk_ring_kernel.cuh", "lk_ring.cu", "lk_ring_q0.cu", "lk_ring_q1.cu", "lk_ring_q2.cu"],
+    "mma": ["lk_mma.cu", "lk_ring_kernel.cuh"],
+    "chain": ["lk_chain.cu", "lk_ring_kernel.cuh"],
+}
+COMMON_FILES = ["lk_device.cuh", "lk_host.h"]
+
+
+def sources_digest(kind: str | None = None) -> str:
+    """sha256 over the sources and headers of one kernel family (or of the
+    whole library): identifies the kernels a stored profile was taken on."""
     import hashlib
     h = hashlib.sha256()
-    for p in _sources() + _headers():
+    if kind is None:
+        files = _sources() + _headers()
+    else:
+        files = [os.path.join(CSRC, f) for f in KERNEL_FILES[kind] + COMMON_FILES] + \
+            [os.path.join(INCLUDE, "lk.h")]
+    for p in files:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode() + b"\0" + f.read())
     return h.hexdigest()

@@ -138,6 +138,8 @@ __device__ bool grid_sync(unsigned* sync, unsigned& gen, unsigned nblocks, unsig
 
 __device__ __forceinline__ int chain_tk(int K) { return K <= TKMAX ? K : 4096; }
 
+__device__ __forceinline__ int quads_of(const Geom& g) { return (int)((g.r1 - g.r0 + QR - 1) / QR); }
+
 __device__ __forceinline__ Geom op_geom(const lk_chain_op& o) {
   const long N = o.N;
   return make_geom(o.wq, o.ws, N, o.K, (long)blockIdx.x * N / gridDim.x, (long)(blockIdx.x + 1) * N / gridDim.x, 0,
@@ -168,19 +170,25 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
   __syncthreads();
   if (ca.pdl && threadIdx.x == 0) griddep_launch();
 
-  // The issue cursor walks this warp's stages of every step in order.
-  int iop = 0;
+  // The issue cursor walks this warp's stages of every step in order.  A
+  // step's quads are dealt to the warps starting where the step before
+  // stopped (rotation), so that steps of a few quads each (q, k, v of a
+  // layer) spread over all warps instead of piling onto the first ones.
+  int iop = 0, irot = 0;
   Geom gi = op_geom(chain_op_at(ca, 0));
   long in = 0, Ti = geom_stages(gi, warp, nwc), issued = 0;
+  int ilw = warp;  // this warp's place in the step's deal
   auto issue_next = [&]() {
     while (in >= Ti) {
       if (++iop >= ca.n_ops) return;
+      irot = (irot + quads_of(gi)) % nwc;
       gi = op_geom(chain_op_at(ca, iop));
-      Ti = geom_stages(gi, warp, nwc);
+      ilw = (warp - irot + nwc) % nwc;
+      Ti = geom_stages(gi, ilw, nwc);
       in = 0;
     }
     const int slot = warp * D + (int)(issued % D);
-    issue_stage(gi, warp, nwc, in, ring + (size_t)slot * ca.stage_bytes, full0 + 8 * slot, pol_w, lane);
+    issue_stage(gi, ilw, nwc, in, ring + (size_t)slot * ca.stage_bytes, full0 + 8 * slot, pol_w, lane);
     ++in;
     ++issued;
   };
@@ -232,6 +240,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
   bool waited = ca.pdl == 0;
   tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_WAITED);
   long consumed = 0;
+  int crot = 0;  // the consume side's deal rotation (as irot)
   bool ok = true;
   for (int op = 0; ok && op < ca.n_ops; ++op) {
     const lk_chain_op o = chain_op_at(ca, op);
@@ -275,7 +284,9 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
     CHAIN_STAMP(2 + 3 * op);
     if (op == 0) tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_ACT);
     const Geom g = op_geom(o);
-    const long T = geom_stages(g, warp, nwc);
+    const int lw = (warp - crot + nwc) % nwc;  // as the issue cursor dealt this step
+    crot = (crot + quads_of(g)) % nwc;
+    const long T = geom_stages(g, lw, nwc);
     const Act ac{act, (unsigned)o.K};
     unsigned long long best[M];
     P p[M];
@@ -301,7 +312,7 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
       }
       if ((int)(n % g.nsl) == g.nsl - 1) {
         lkh::GemvProblem dummy;
-        finish_quad<Q, M, false>(p, g, warp, nwc, n, dummy, 0, o.y, best, lane);
+        finish_quad<Q, M, false>(p, g, lw, nwc, n, dummy, 0, o.y, best, lane);
       }
     }
     if (ca.trace && ca.trace_all && ca.tslot < 0 && lane == 0 && blockIdx.x == 0) {
