@@ -358,6 +358,10 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *   "mma_act16"   its activation rows held in shared memory as f16 (0 auto:
  *                 where that leaves room for 8 warps; 1 whenever they fit;
  *                 2 never: int8, converted per use)
+ *   "ring_prefill" GEMV kernels: warps of a block that issue their first
+ *                 weight stages before the wait on the previous kernel; the
+ *                 others issue theirs once the activation is loaded (0 =
+ *                 half of the warps, the default; 12 or 16 = all)
  *   "l2_ahead_kb" ring and tensor-core kernels: KB per block of the stages
  *                 after the ring's first fill requested into L2 at kernel
  *                 start (cp.async.bulk.prefetch.L2), so that HBM keeps

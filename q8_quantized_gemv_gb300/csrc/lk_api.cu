@@ -26,6 +26,7 @@ long opt_mma_tk = 0;
 long opt_mma_warps = 0;
 long opt_mma_depth = 0;
 long opt_l2_ahead_kb = 0;
+long opt_ring_prefill = 0;
 long opt_mma_act16 = 0;
 
 static const int kMaxDevices = 64;
@@ -158,6 +159,67 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_split_kernel(const float* 
   trec_end(tr, slot, TK_NORM, K);
 }
 
+// The same for K a multiple of 1024 (the norm's 1024 virtual threads): 256
+// real threads per block play the 32 virtual warps (warp w plays w, w + 8,
+// w + 16, w + 24), so a block needs few registers and can share an SM with a
+// GEMV block of the neighbouring launches (a 1024-thread block cannot).
+template <int Q>
+__global__ void __launch_bounds__(256) rmsnorm_quant_split256_kernel(const float* __restrict__ x,
+                                                                     const float* __restrict__ g, int K, float eps,
+                                                                     float* __restrict__ xn, int8_t* __restrict__ xq,
+                                                                     int8_t* __restrict__ xl, float* __restrict__ xs,
+                                                                     unsigned long long* tr, int slot) {
+  typedef typename acc_of<Q>::t A;
+  constexpr int KU_MAX = 8, VT = 1024, NJ = 4;  // virtual warps per real warp
+  __shared__ A red[32];
+  __shared__ A total;
+  asm volatile("griddepcontrol.launch_dependents;" :::);  // as in rmsnorm_quant_kernel
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int KU = K / VT, u_mine = blockIdx.y;
+  const long row = blockIdx.x;
+  const float* xr = x + row * K;
+  float gv[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) gv[j] = __ldg(g + 32 * (warp + 8 * j) + lane + VT * u_mine);
+  trec_stamp(tr, slot, TR_START);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  trec_stamp(tr, slot, TR_WAITED);
+  float v[NJ][KU_MAX];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+#pragma unroll
+    for (int u = 0; u < KU_MAX; ++u) v[j][u] = u < KU ? __ldg(xr + 32 * (warp + 8 * j) + lane + VT * u) : 0.f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    A acc = 0;
+#pragma unroll
+    for (int u = 0; u < KU_MAX; ++u)
+      if (u < KU) acc = fma_acc((A)v[j][u], acc);
+    acc = warp_tree_sum(acc);
+    if (lane == 0) red[warp + 8 * j] = acc;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    A r = red[lane];
+    r = warp_tree_sum(r);
+    if (lane == 0) total = r;
+  }
+  __syncthreads();
+  const A den = norm_div_add(total, K, eps);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    float mine = v[j][0];
+#pragma unroll
+    for (int u = 1; u < KU_MAX; ++u)
+      if (u == u_mine) mine = v[j][u];
+    const long i = row * K + 32 * (warp + 8 * j) + lane + (long)VT * u_mine;
+    const float yv = norm_scale(mine, den, gv[j]);
+    if (xn) xn[i] = yv;
+    if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, i, i >> 5, lane);
+  }
+  trec_end(tr, slot, TK_NORM, K);
+}
+
 template <int Q>
 __global__ void quantize_kernel(const float* __restrict__ x, long groups, int8_t* __restrict__ xq,
                                 int8_t* __restrict__ xl, float* __restrict__ xs, unsigned long long* tr, int slot) {
@@ -278,6 +340,9 @@ lk_status lk_set_option(const char* name, long value) {
   } else if (!strcmp(name, "mma_act16")) {
     if (value < 0 || value > 2) return LK_ERR_ARG;
     opt_mma_act16 = value;
+  } else if (!strcmp(name, "ring_prefill")) {
+    if (value < 0 || value > 12) return LK_ERR_ARG;
+    opt_ring_prefill = value;
   } else if (!strcmp(name, "l2_ahead_kb")) {
     if (value < 0 || value > 65536) return LK_ERR_ARG;
     opt_l2_ahead_kb = value;
@@ -305,6 +370,7 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "mma_warps")) return opt_mma_warps;
   if (!strcmp(name, "mma_depth")) return opt_mma_depth;
   if (!strcmp(name, "l2_ahead_kb")) return opt_l2_ahead_kb;
+  if (!strcmp(name, "ring_prefill")) return opt_ring_prefill;
   if (!strcmp(name, "mma_act16")) return opt_mma_act16;
   return -1;
 }
@@ -317,6 +383,24 @@ lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, floa
   if (!x || !gain) return LK_ERR_ARG;
   if (!aligned(x, 4) || !aligned(gain, 4) || (xn && !aligned(xn, 4))) return LK_ERR_ALIGN;
   const int vt = K < 1024 ? K : 1024;  // K % 32 == 0: roundup32(K) == K
+  if (K % 1024 == 0 && K / 1024 <= 8) {
+    const dim3 grid(M, K / 1024);
+    if (mode == LK_DEQUANT) {
+      if (!xn) return LK_ERR_ARG;
+      launch_pdl(rmsnorm_quant_split256_kernel<0>, grid, dim3(256), stream, x, gain, K, eps, xn, (int8_t*)nullptr,
+                 (int8_t*)nullptr, (float*)nullptr, tr_ptr(), tr_slot());
+    } else {
+      lk_status st = check_act_out(mode, xq, xl, xs);
+      if (st) return st;
+      if (mode == LK_INT8ACT)
+        launch_pdl(rmsnorm_quant_split256_kernel<1>, grid, dim3(256), stream, x, gain, K, eps, xn, xq,
+                   (int8_t*)nullptr, xs, tr_ptr(), tr_slot());
+      else
+        launch_pdl(rmsnorm_quant_split256_kernel<2>, grid, dim3(256), stream, x, gain, K, eps, xn, xq, xl, xs,
+                   tr_ptr(), tr_slot());
+    }
+    return launch_status();
+  }
   if (K % vt == 0 && K / vt <= 8) {
     const dim3 grid(M, K / vt);
     if (mode == LK_DEQUANT) {

@@ -36,6 +36,7 @@ struct ChainArgs {
   long long pf_budget;        // bytes of later steps' weights each block keeps requested into L2 ahead
   int pdl;                    // launched as a programmatic dependent (a chain without barriers)
   int tslot;                  // trace 3: this launch's record in the timeline, else -1
+  int prefill;                // warps that fill their stages before the dependency wait
   // A group of GEMVs over one given activation (lk_gemv_q8_group): the ops
   // are held here (n_inl of them) and the activation rows are copied once
   // instead of computed by a prologue.
@@ -198,7 +199,9 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
   // this launch before every block has read it (completion needs every
   // block's arrival, and a block arrives only after this read).
   unsigned gen = threadIdx.x == 0 && ca.sync ? ld_acquire_gpu(ca.sync + 32) : 0u;
-  for (int d = 0; d < D && iop < ca.n_ops; ++d) issue_next();
+  // (warps >= prefill fill their stages after the first step's activation)
+  const bool early = warp < ca.prefill;
+  for (int d = 0; early && d < D && iop < ca.n_ops; ++d) issue_next();
 
   // L2 prefetch cursor: the block's bytes of later steps (levels, then
   // scales, step after step) are requested into L2 with per-thread
@@ -282,7 +285,10 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
       waited = true;
     }
     CHAIN_STAMP(2 + 3 * op);
-    if (op == 0) tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_ACT);
+    if (op == 0) {
+      tstamp(ca.tslot >= 0 ? ca.trace : nullptr, ca.tslot, TR_ACT);
+      for (int d = 0; !early && d < D && iop < ca.n_ops; ++d) issue_next();
+    }
     const Geom g = op_geom(o);
     const int lw = (warp - crot + nwc) % nwc;  // as the issue cursor dealt this step
     crot = (crot + quads_of(g)) % nwc;
@@ -450,6 +456,7 @@ static lk_status chain_launch(const lk_chain_op* ops, const lk_chain_op* ops_dev
   ca.trace_all = lkh::opt_trace == 2;
   ca.tslot = lkh::opt_trace == 3 ? lkh::trace_next_slot() : -1;
   ca.pdl = !barrier && lkh::opt_pdl ? 1 : 0;
+  ca.prefill = lkh::prefill_warps(w);
   ca.n_inl = 0;
   ca.gx = nullptr;
   ca.gxq = ca.gxl = nullptr;

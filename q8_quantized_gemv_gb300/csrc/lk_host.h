@@ -36,6 +36,7 @@ extern long opt_mma_tk;       // its bytes of K per stage (0 auto, else a multip
 extern long opt_mma_warps;    // its warps per block (0 auto)
 extern long opt_mma_depth;    // its ring stages per warp (0 = 1)
 extern long opt_mma_act16;    // its activations held as f16: 0 auto, 1 force, 2 never
+extern long opt_ring_prefill; // warps that issue their first weight stages before the dependency wait (0: half)
 extern long opt_l2_ahead_kb;  // ring/tensor-core kernels: KB per block of later stages requested into L2 at start
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
@@ -67,6 +68,15 @@ struct GemvProblem {
   const float* gain;             // fused: RMSNorm gain [K], or NULL for quantize only
   float eps;
 };
+
+// Warps of a block of nw that fill their ring stages before the dependency
+// wait (the others after the activation is loaded): option "ring_prefill",
+// 0 = half of them (measured best: a full ring of requests ahead of the
+// wait slowed the activation loads and the wait itself).
+inline int prefill_warps(int nw) {
+  const int p = opt_ring_prefill > 0 ? (int)opt_ring_prefill : (nw + 1) / 2;
+  return p < nw ? p : nw;
+}
 
 // Device address of the error word that bounded device waits set (lk_ring.cu).
 int* error_word_ptr();

@@ -76,6 +76,7 @@ struct MmaArgs {
   int l2_ahead;            // stages per warp requested into L2 beyond the ring at start
   unsigned long long* trace;  // option "trace" 3: the launch timeline, else NULL
   int tslot;
+  int prefill;             // warps that fill their stages before the dependency wait
 };
 
 // int8 x 4 (b0 lowest) -> two f16x2: (b0, b1) and (b2, b3), exact.
@@ -246,7 +247,9 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   // weights do not depend on the previous kernel: start streaming at once
   long issued = 0;
   Cursor ic{tl.base, 0};
-  for (; issued < T && issued < D; ++issued, ic.next(tl))
+  // (warps >= prefill fill their stages once the activation is loaded)
+  const bool early = warp < ra.prefill;
+  for (; early && issued < T && issued < D; ++issued, ic.next(tl))
     issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
           pol_w, lane);
   {
@@ -319,6 +322,9 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   }
 
   tstamp(ra.trace, ra.tslot, TR_ACT);
+  for (; !early && issued < T && issued < D; ++issued, ic.next(tl))
+    issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
+          pol_w, lane);
   // activation row g's words and the scales of activation rows 2t, 2t+1
   const bool gx_ok = g < M;
   const unsigned char* XH = act + (size_t)g * ra.ar + (A16 ? 16 : 8) * t;
@@ -634,6 +640,7 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   ra.l2_ahead = (int)(opt_l2_ahead_kb * 1024 / ((long)L.nw * L.stage_bytes));
   ra.trace = opt_trace == 3 ? trace_ptr() : nullptr;
   ra.tslot = opt_trace == 3 ? trace_next_slot() : -1;
+  ra.prefill = prefill_warps(L.nw);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)gx);
   cfg.blockDim = dim3(L.nw * 32);

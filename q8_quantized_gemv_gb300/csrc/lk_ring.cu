@@ -204,6 +204,7 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   ra.trace = opt_trace ? lkh::trace_ptr() : nullptr;
   ra.tslot = opt_trace == 3 ? lkh::trace_next_slot() : -1;
   ra.l2_ahead = (int)(opt_l2_ahead_kb * 1024 / ((long)L.nwc * L.stage_bytes));
+  ra.prefill = lkh::prefill_warps(L.nwc);
   const int S = p.split && p.S > 1 ? p.S : 1;
   const int g = opt_grid_ctas > 0 ? (int)opt_grid_ctas : d->sm_count * (opt_ring_cps > 1 ? (int)opt_ring_cps : 1);
   int gx = (g + S - 1) / S;

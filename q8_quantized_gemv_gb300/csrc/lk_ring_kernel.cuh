@@ -43,6 +43,7 @@ struct RingArgs {
   unsigned long long* trace;  // block 0's timestamps (option "trace"), or NULL
   int tslot;               // trace 3: this launch's record in the timeline, else -1
   int l2_ahead;            // stages per warp requested into L2 beyond the ring at start
+  int prefill;             // warps that fill their stages before the dependency wait
 };
 
 typedef void (*ring_fn)(const RingArgs);
@@ -667,8 +668,12 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
 
   // Weights do not depend on the previous kernel: start streaming at once.
   tstamp(ra.trace, ra.tslot, TR_START);
+  // (warps >= prefill issue their first stages only once the activation is
+  // ready: a full ring's requests ahead of the dependency wait slow the
+  // activation's own loads)
   long issued = 0;
-  for (; issued < T && issued < D; ++issued)
+  const bool early = warp < ra.prefill;
+  for (; early && issued < T && issued < D; ++issued)
     issue_stage(g, warp, nwc, issued, ring + (size_t)(warp * D + issued % D) * ra.stage_bytes,
                 full0 + 8 * (warp * D + (int)(issued % D)), pol_w, lane);
   // the next stages into L2, so that HBM keeps streaming while the block
@@ -687,6 +692,9 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   } else if (L > 0) {
     load_act<Q, M>(act, L, a, k_lo);
   }
+  for (; !early && issued < T && issued < D; ++issued)
+    issue_stage(g, warp, nwc, issued, ring + (size_t)(warp * D + issued % D) * ra.stage_bytes,
+                full0 + 8 * (warp * D + (int)(issued % D)), pol_w, lane);
 
   const Act ac{act, L};
   tstamp(ra.trace, ra.tslot, TR_ACT);
