@@ -355,6 +355,9 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 else a multiple of 256 up to 8192
  *   "mma_warps"   its warps per block: 0 auto, else 1..16
  *   "mma_depth"   its ring stages per warp: 0 = 1, else 1..8
+ *   "mma_group"   its warps per 16-row tile: 0 auto, 1 one warp per tile, 4
+ *                 four warps per tile (each one partial b mod 4; for
+ *                 launches with few tiles per SM)
  *   "mma_act16"   its activation rows held in shared memory as f16 (0 auto:
  *                 where that leaves room for 8 warps; 1 whenever they fit;
  *                 2 never: int8, converted per use)

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(256) gemv_direct_kernel(GemvProblem a) {
           for (int c = 0; c < 4; ++c) {
             const float xe[4] = {xx[c].x, xx[c].y, xx[c].z, xx[c].w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) h = __fmaf_rn((float)(int8_t)(wi[c] >> (8 * k)), xe[k], h);
+            for (int k = 0; k < 4; ++k) h = __fmaf_rn(i8_as_f32((unsigned)wi[c] ^ 0x80808080u, k), xe[k], h);
           }
           const float blk = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
           if (bok) p[t] = __fma_rn((double)wsv[u], (double)blk, (double)p[t]);

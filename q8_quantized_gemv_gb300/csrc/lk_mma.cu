@@ -204,61 +204,16 @@ __device__ __forceinline__ void prefetch(const MmaArgs& ra, long tile, int c, in
   }
 }
 
-// A16: the activation rows are held in shared memory already converted to
-// f16 (row stride 2K + 64 bytes: a quarter-warp's 16-byte reads of rows g,
-// g+1 then cover 128 distinct bytes), so the B fragment is one 16-byte read
-// per 32-block instead of a read and 10 conversion instructions per warp.
-// Else the int8 words are held (stride K + 32) and converted per use.
+// The activation rows into shared memory (all threads call it, after the
+// dependency wait): f16 rows converted by every thread (A16), or the int8
+// rows by warp 0's bulk copies completing on act_bar (bounded wait).
+// Returns false when that wait gave up.
 template <int Q, bool A16>
-__global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__device__ __forceinline__ bool load_rows(const MmaArgs& ra, unsigned char* act, unsigned act_bar,
+                                          volatile int* abort_flag) {
   const lkh::GemvProblem& a = ra.p;
-  const int nw = ra.nw, D = ra.depth, NS = nw * D;
   const int M = a.M, K = a.K, nb = K >> 5;
-  unsigned char* act = smem;
-  unsigned char* ring = smem + ra.ring_off;
-  unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
-  volatile int* abort_flag = (volatile int*)(bars + MST + 1);
-  unsigned long long* keys = (unsigned long long*)(bars + MST + 3);  // [TN][MW]
-  const unsigned full0 = smem_u32(bars);
-  const unsigned act_bar = smem_u32(bars + MST);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-
-  Tiles tl;
-  tl.base = blockIdx.x + (long)ra.gx * warp;
-  tl.stride = (long)ra.gx * nw;
-  tl.ntiles = ra.ntiles;
-  tl.nsl = (K + (int)ra.tk - 1) / (int)ra.tk;
-  const long my_tiles = tl.base < tl.ntiles ? (tl.ntiles - 1 - tl.base) / tl.stride + 1 : 0;
-  const long T = my_tiles * tl.nsl;
-  const unsigned long long pol_w = ra.pol_w ? evict_first_policy() : 0ull;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(full0 + 8 * s, 1);
-    mbar_init(act_bar, 1);
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  if (ra.pdl && threadIdx.x == 0) griddep_launch();
-  tstamp(ra.trace, ra.tslot, TR_START);
-
-  // weights do not depend on the previous kernel: start streaming at once
-  long issued = 0;
-  Cursor ic{tl.base, 0};
-  // (warps >= prefill fill their stages once the activation is loaded)
-  const bool early = warp < ra.prefill;
-  for (; early && issued < T && issued < D; ++issued, ic.next(tl))
-    issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
-          pol_w, lane);
-  {
-    Cursor pc = ic;
-    for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m, pc.next(tl)) prefetch(ra, pc.tile, pc.c, lane);
-  }
-
-  if (ra.pdl) griddep_wait();
-  tstamp(ra.trace, ra.tslot, TR_WAITED);
   // the activation rows: int8 words (and low words) and scales, row-padded
   if (A16) {
     // every thread converts 16-byte runs of the int8 rows into f16 rows
@@ -321,6 +276,65 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
     if (!ok && lane == 0) raise_error(ra.err, ERR_WAIT_ACT, abort_flag);
   }
 
+  return ok;
+}
+
+// A16: the activation rows are held in shared memory already converted to
+// f16 (row stride 2K + 64 bytes: a quarter-warp's 16-byte reads of rows g,
+// g+1 then cover 128 distinct bytes), so the B fragment is one 16-byte read
+// per 32-block instead of a read and 10 conversion instructions per warp.
+// Else the int8 words are held (stride K + 32) and converted per use.
+template <int Q, bool A16>
+__global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const lkh::GemvProblem& a = ra.p;
+  const int nw = ra.nw, D = ra.depth, NS = nw * D;
+  const int M = a.M, K = a.K;
+  unsigned char* act = smem;
+  unsigned char* ring = smem + ra.ring_off;
+  unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
+  volatile int* abort_flag = (volatile int*)(bars + MST + 1);
+  unsigned long long* keys = (unsigned long long*)(bars + MST + 3);  // [TN][MW]
+  const unsigned full0 = smem_u32(bars);
+  const unsigned act_bar = smem_u32(bars + MST);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+
+  Tiles tl;
+  tl.base = blockIdx.x + (long)ra.gx * warp;
+  tl.stride = (long)ra.gx * nw;
+  tl.ntiles = ra.ntiles;
+  tl.nsl = (K + (int)ra.tk - 1) / (int)ra.tk;
+  const long my_tiles = tl.base < tl.ntiles ? (tl.ntiles - 1 - tl.base) / tl.stride + 1 : 0;
+  const long T = my_tiles * tl.nsl;
+  const unsigned long long pol_w = ra.pol_w ? evict_first_policy() : 0ull;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(full0 + 8 * s, 1);
+    mbar_init(act_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (ra.pdl && threadIdx.x == 0) griddep_launch();
+  tstamp(ra.trace, ra.tslot, TR_START);
+
+  // weights do not depend on the previous kernel: start streaming at once
+  long issued = 0;
+  Cursor ic{tl.base, 0};
+  // (warps >= prefill fill their stages once the activation is loaded)
+  const bool early = warp < ra.prefill;
+  for (; early && issued < T && issued < D; ++issued, ic.next(tl))
+    issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
+          pol_w, lane);
+  {
+    Cursor pc = ic;
+    for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m, pc.next(tl)) prefetch(ra, pc.tile, pc.c, lane);
+  }
+
+  if (ra.pdl) griddep_wait();
+  tstamp(ra.trace, ra.tslot, TR_WAITED);
+  bool ok = load_rows<Q, A16>(ra, act, act_bar, abort_flag);
   tstamp(ra.trace, ra.tslot, TR_ACT);
   for (; !early && issued < T && issued < D; ++issued, ic.next(tl))
     issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
@@ -491,10 +505,259 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   tend(ra.trace, ra.tslot, ra.ntiles * TR, 3);
 }
 
+// ---- four warps per tile --------------------------------------------------------------
+//
+// Where a launch has few tiles per SM (down 4096 x 12288 at 8 rows: 1.7), one
+// warp per tile leaves most warps idle and serializes a tile's 32-blocks on
+// one warp.  Here a group of four warps shares each 16-row tile: warp q of
+// the group computes the blocks b = q mod 4 of every stage, i.e. exactly
+// partial q of the combine ("kernels.rs" lk_q8_rows_dot), and at the end of
+// the tile the group's leader (q = 0) adds (p0 + p2) + (p1 + p3) from the
+// other three warps' partials in shared memory: the same operations in the
+// same order, so the same bits.  A group's stages are filled by its leader
+// and released by all four warps (an "empty" mbarrier of 4 arrivals); the
+// partials go through a per-group buffer guarded by two mbarriers (written,
+// read).  Every wait is bounded.
+constexpr int G4 = 4;                          // warps per group
+constexpr int MGRP = MW / G4;                  // groups per block at most
+constexpr unsigned G4_CBUF = MGRP * 3 * 4 * 32 * 4;  // partials of warps 1..3, [grp][q-1][elem][lane]
+constexpr unsigned MTAIL4 = MTAIL + 8 * MST + 8 * 2 * MGRP + G4_CBUF;
+
+template <int Q, bool A16>
+__global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs ra) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const lkh::GemvProblem& a = ra.p;
+  const int nw = ra.nw, NG = nw / G4, D = ra.depth, NS = NG * D;
+  const int M = a.M, K = a.K;
+  unsigned char* act = smem;
+  unsigned char* ring = smem + ra.ring_off;
+  unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
+  volatile int* abort_flag = (volatile int*)(bars + MST + 1);
+  unsigned long long* keys = (unsigned long long*)(bars + MST + 3);  // [TN][MW]
+  unsigned long long* ebars = keys + TN * MW;                          // empty, [MST]
+  unsigned long long* cbars = ebars + MST;                             // written [MGRP], read [MGRP]
+  float* cbuf = (float*)(cbars + 2 * MGRP);
+  const unsigned full0 = smem_u32(bars), empty0 = smem_u32(ebars), act_bar = smem_u32(bars + MST);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp = warp / G4, q = warp % G4;
+  const bool leader = q == 0;
+  const int g = lane >> 2, t = lane & 3;
+  const unsigned cw_bar = smem_u32(cbars + grp), cr_bar = smem_u32(cbars + MGRP + grp);
+
+  Tiles tl;
+  tl.base = blockIdx.x + (long)ra.gx * grp;
+  tl.stride = (long)ra.gx * NG;
+  tl.ntiles = ra.ntiles;
+  tl.nsl = (K + (int)ra.tk - 1) / (int)ra.tk;
+  const long my_tiles = tl.base < tl.ntiles ? (tl.ntiles - 1 - tl.base) / tl.stride + 1 : 0;
+  const long T = my_tiles * tl.nsl;
+  const unsigned long long pol_w = ra.pol_w ? evict_first_policy() : 0ull;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, G4);
+    }
+    mbar_init(act_bar, 1);
+    for (int gi = 0; gi < NG; ++gi) {
+      mbar_init(smem_u32(cbars + gi), 32 * (G4 - 1));  // every lane of warps 1..3 has written
+      mbar_init(smem_u32(cbars + MGRP + gi), 32);       // every lane of the leader has read
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (ra.pdl && threadIdx.x == 0) griddep_launch();
+  tstamp(ra.trace, ra.tslot, TR_START);
+
+  long issued = 0;
+  Cursor ic{tl.base, 0};
+  const bool early = grp < ra.prefill;  // groups that fill before the dependency wait
+  if (leader)
+    for (; early && issued < T && issued < D; ++issued, ic.next(tl))
+      issue(ra, ic.tile, ic.c, ring + (size_t)(grp * D + issued) * ra.stage_bytes, full0 + 8 * (grp * D + (int)issued),
+            pol_w, lane);
+  if (ra.pdl) griddep_wait();
+  tstamp(ra.trace, ra.tslot, TR_WAITED);
+  bool ok = load_rows<Q, A16>(ra, act, act_bar, abort_flag);
+  tstamp(ra.trace, ra.tslot, TR_ACT);
+  if (leader)
+    for (; !early && issued < T && issued < D; ++issued, ic.next(tl))
+      issue(ra, ic.tile, ic.c, ring + (size_t)(grp * D + issued) * ra.stage_bytes, full0 + 8 * (grp * D + (int)issued),
+            pol_w, lane);
+
+  const bool gx_ok = g < M;
+  const unsigned char* XH = act + (size_t)g * ra.ar + (A16 ? 16 : 8) * t;
+  const unsigned char* XL = act + ra.a_lo + (size_t)g * ra.ar + (A16 ? 16 : 8) * t;
+  const float* XS0 = (const float*)(act + ra.a_xs) + (size_t)(2 * t) * ra.xsr;
+  const float* XS1 = XS0 + ra.xsr;
+  const bool s0_ok = 2 * t < M, s1_ok = 2 * t + 1 < M;
+
+  float p[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's partial q: (g,2t) (g,2t+1) (g+8,2t) (g+8,2t+1)
+  unsigned long long best0 = 0, best1 = 0;
+  long n = 0;
+  Cursor cc{tl.base, 0};
+  int cs = 0;
+  unsigned cph = 0, jt = 0;  // phase parity of the current slot round; tiles finished
+  for (; ok && n < T; ++n) {
+    const int slot = grp * D + cs;
+    if (!__all_sync(FULL, mbar_wait(full0 + 8 * slot, cph, ra.wait_ns, abort_flag))) {
+      if (lane == 0) raise_error(ra.err, ERR_WAIT_FULL, abort_flag);
+      ok = false;
+      break;
+    }
+    unsigned char* st = ring + (size_t)slot * ra.stage_bytes;
+    const int c = cc.c;
+    const int k0 = c * (int)ra.tk;
+    const int len = K - k0 < (int)ra.tk ? K - k0 : (int)ra.tk;
+    const unsigned char* W0 = st + g * ra.rs + 8 * t;
+    const unsigned char* W8 = W0 + 8 * ra.rs;
+    const unsigned char* S0 = st + ra.s_off + g * ra.srs;
+    const unsigned char* S8 = S0 + 8 * ra.srs;
+    const int b0 = k0 >> 5, nblk = len >> 5;
+#pragma unroll 4
+    for (int bb = q; bb < nblk; bb += G4) {  // b0 % 4 == 0: block b0 + bb is in partial q
+      const float wa = __half2float(*(const __half*)(S0 + 2 * bb));
+      const float wb = __half2float(*(const __half*)(S8 + 2 * bb));
+      const float xa = s0_ok ? XS0[b0 + bb] : 0.f;
+      const float xb = s1_ok ? XS1[b0 + bb] : 0.f;
+      const Frag8 fw0 = frag8(*(const uint2*)(W0 + 32 * bb));
+      const Frag8 fw8 = frag8(*(const uint2*)(W8 + 32 * bb));
+      float d[4];
+      block_dot(d, fw0, fw8, act_frag<A16>(XH, k0 + 32 * bb, gx_ok));
+      const float ws_[4] = {wa, wa, wb, wb};
+      const float xs_[4] = {xa, xb, xa, xb};
+      if constexpr (Q == 1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[e] = __fmaf_rn(__fmul_rn(ws_[e], xs_[e]), d[e], p[e]);
+      } else {
+        float f[4];
+        block_dot(f, fw0, fw8, act_frag<A16>(XL, k0 + 32 * bb, gx_ok));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float u = __fmaf_rn(xs_[e], d[e], __fmul_rn(__fmul_rn(xs_[e], 0.0078125f), f[e]));
+          p[e] = __fmaf_rn(ws_[e], u, p[e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * slot);  // this warp is done with the stage
+    if (c == tl.nsl - 1) {
+      // the tile is done: (p0 + p2) + (p1 + p3) across the group ("kernels.rs" lk_q8_sum4)
+      float* buf = cbuf + (size_t)grp * 3 * 4 * 32;
+      if (!leader) {
+        // the leader has read the previous tile's partials before these are written
+        if (jt > 0 && !__all_sync(FULL, mbar_wait(cr_bar, (jt - 1) & 1u, ra.wait_ns, abort_flag))) {
+          if (lane == 0) raise_error(ra.err, ERR_WAIT_FULL, abort_flag);
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) buf[((q - 1) * 4 + e) * 32 + lane] = p[e];
+        mbar_arrive(cw_bar);
+      } else {
+        if (!__all_sync(FULL, mbar_wait(cw_bar, jt & 1u, ra.wait_ns, abort_flag))) {
+          if (lane == 0) raise_error(ra.err, ERR_WAIT_FULL, abort_flag);
+          ok = false;
+          break;
+        }
+        float yv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p1 = buf[(0 * 4 + e) * 32 + lane], p2 = buf[(1 * 4 + e) * 32 + lane],
+                      p3 = buf[(2 * 4 + e) * 32 + lane];
+          yv[e] = __fadd_rn(__fadd_rn(p[e], p2), __fadd_rn(p1, p3));
+        }
+        mbar_arrive(cr_bar);
+        const Mat mt = mat_of(ra, cc.tile);
+        const long r0 = mt.row0 + g, r8 = r0 + 8;
+        const int t0 = 2 * t, t1 = 2 * t + 1;
+        if (r0 < mt.N) {
+          if (t0 < M) {
+            mt.y[(long)t0 * mt.N + r0] = yv[0];
+            const unsigned long long k = amax_key(yv[0], (unsigned)r0);
+            best0 = k > best0 ? k : best0;
+          }
+          if (t1 < M) {
+            mt.y[(long)t1 * mt.N + r0] = yv[1];
+            const unsigned long long k = amax_key(yv[1], (unsigned)r0);
+            best1 = k > best1 ? k : best1;
+          }
+        }
+        if (r8 < mt.N) {
+          if (t0 < M) {
+            mt.y[(long)t0 * mt.N + r8] = yv[2];
+            const unsigned long long k = amax_key(yv[2], (unsigned)r8);
+            best0 = k > best0 ? k : best0;
+          }
+          if (t1 < M) {
+            mt.y[(long)t1 * mt.N + r8] = yv[3];
+            const unsigned long long k = amax_key(yv[3], (unsigned)r8);
+            best1 = k > best1 ? k : best1;
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p[e] = 0.f;
+      ++jt;
+    }
+    // the leader refills the slot once all four warps are done with it
+    if (leader && issued < T) {
+      if (!__all_sync(FULL, mbar_wait(empty0 + 8 * slot, cph, ra.wait_ns, abort_flag))) {
+        if (lane == 0) raise_error(ra.err, ERR_WAIT_EMPTY, abort_flag);
+        ok = false;
+        break;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(ra, ic.tile, ic.c, st, full0 + 8 * slot, pol_w, lane);
+      ic.next(tl);
+      ++issued;
+    }
+    cc.next(tl);
+    if (++cs == D) {
+      cs = 0;
+      cph ^= 1u;
+    }
+  }
+  // drain: the leader's stages issued but not consumed (only after an abort)
+  // must land before the block may end; they occupy the slots from cs on
+  if (leader && lane == 0) {
+    for (long m = n; m < issued; ++m) {
+      drain_wait(full0 + 8 * (unsigned)(grp * D + cs), cph, ra.wait_ns, ra.err);
+      if (++cs == D) {
+        cs = 0;
+        cph ^= 1u;
+      }
+    }
+  }
+  if (!A16 && warp == 0 && lane == 0) drain_wait(act_bar, 0, ra.wait_ns, ra.err);
+  __syncwarp();
+  if (a.amax) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      const unsigned long long v0 = __shfl_xor_sync(FULL, best0, o);
+      const unsigned long long v1 = __shfl_xor_sync(FULL, best1, o);
+      best0 = v0 > best0 ? v0 : best0;
+      best1 = v1 > best1 ? v1 : best1;
+    }
+    if (g == 0) {
+      keys[(2 * t) * MW + warp] = best0;
+      keys[(2 * t + 1) * MW + warp] = best1;
+    }
+    __syncthreads();
+    if (threadIdx.x < M) {
+      unsigned long long m = 0;
+      for (int w = 0; w < nw; ++w) m = keys[threadIdx.x * MW + w] > m ? keys[threadIdx.x * MW + w] : m;
+      a.amax[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
+    }
+  }
+  tend(ra.trace, ra.tslot, ra.ntiles * TR, 3);
+}
+
 struct MmaLayout {
   unsigned tk, rs, srs, s_off, stage_bytes, ar, xsr, a_lo, a_xs, ring_off, total;
-  int nw, depth;
-  bool a16;
+  int nw, depth;  // g4: warps (4 per group) and stages per group
+  bool a16, g4;
 };
 
 unsigned round_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
@@ -544,6 +807,43 @@ MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int sm
   return L;
 }
 
+// Four warps per tile: 512-byte slices (256 when they do not fit), groups of
+// four warps with at least three stages each (the group consumes a stage four
+// times faster than one warp), as many groups as fit, up to four.
+MmaLayout mma_layout_g4(const lkh::GemvProblem& p, int smem_optin, bool a16) {
+  MmaLayout L{};
+  const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)p.M;
+  L.a16 = a16;
+  L.g4 = true;
+  L.ar = a16 ? 2u * K + 64u : K + 32u;
+  L.xsr = nb + 4u;
+  L.a_lo = round_up(M * L.ar, 128u);
+  L.a_xs = p.mode == LK_TWOPASS ? round_up(L.a_lo + M * L.ar, 128u) : L.a_lo;
+  L.ring_off = round_up(L.a_xs + M * L.xsr * 4u, 128u);
+  const unsigned cand_tk[2] = {512u, 256u};
+  for (int i = 0; i < 2; ++i) {
+    unsigned tk = lkh::opt_mma_tk > 0 ? (unsigned)lkh::opt_mma_tk : cand_tk[i];
+    if (tk > round_up(K, 256u)) tk = round_up(K, 256u);
+    L.tk = tk;
+    L.rs = tk + 32u;
+    L.srs = tk / 16u + 16u;
+    L.s_off = TR * L.rs;
+    L.stage_bytes = round_up(L.s_off + TR * L.srs, 128u);
+    const long room = (long)smem_optin - (long)L.ring_off - (long)MTAIL4;
+    int fit = room > 0 ? (int)(room / L.stage_bytes) : 0;
+    if (fit > MST) fit = MST;
+    int ng = lkh::opt_mma_warps > 0 ? (int)lkh::opt_mma_warps / G4 : fit / 3;
+    if (ng > MGRP) ng = MGRP;
+    int depth = lkh::opt_mma_depth > 0 ? (int)lkh::opt_mma_depth : (ng > 0 ? fit / ng : 0);
+    if (ng * depth > fit) ng = depth > 0 ? fit / depth : 0;
+    L.nw = G4 * ng;
+    L.depth = depth;
+    L.total = L.ring_off + (unsigned)(ng * depth) * L.stage_bytes + MTAIL4;
+    if (ng >= 1 || lkh::opt_mma_tk > 0) break;
+  }
+  return L;
+}
+
 bool mma_layout_ok(const MmaLayout& L);
 
 // f16-held activations where they cost no warps (Int8Act at K = 4096: 16
@@ -551,6 +851,14 @@ bool mma_layout_ok(const MmaLayout& L);
 // against 36.9 us held as int8); option "mma_act16" 1 forces them (if they
 // fit at all), 2 forbids them.
 MmaLayout mma_layout(const lkh::GemvProblem& p, long ntiles, int sms, int smem_optin) {
+  if (lkh::opt_mma_group == 4) {
+    const MmaLayout G8 = mma_layout_g4(p, smem_optin, false);
+    if (lkh::opt_mma_act16 == 2) return G8;
+    const MmaLayout G16 = mma_layout_g4(p, smem_optin, true);
+    if (!mma_layout_ok(G16)) return G8;
+    if (lkh::opt_mma_act16 == 1) return G16;
+    return G16.nw >= G8.nw ? G16 : G8;
+  }
   const MmaLayout L8 = mma_layout_for(p, ntiles, sms, smem_optin, false);
   if (lkh::opt_mma_act16 == 2) return L8;
   const MmaLayout L16 = mma_layout_for(p, ntiles, sms, smem_optin, true);
@@ -559,7 +867,9 @@ MmaLayout mma_layout(const lkh::GemvProblem& p, long ntiles, int sms, int smem_o
   return L16.nw >= L8.nw ? L16 : L8;
 }
 
-bool mma_layout_ok(const MmaLayout& L) { return L.nw >= 1 && L.depth >= 1 && L.nw * L.depth >= 2; }
+bool mma_layout_ok(const MmaLayout& L) {
+  return L.g4 ? (L.nw >= G4 && L.depth >= 2) : (L.nw >= 1 && L.depth >= 1 && L.nw * L.depth >= 2);
+}
 // (a single-stage ring per warp still overlaps: the warps' copies are in
 // flight while other warps compute)
 
@@ -595,8 +905,10 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   for (int m = 0; m < nmat; ++m) all_tiles += (N[m] + TR - 1) / TR;
   const MmaLayout L = mma_layout(p, all_tiles, d->sm_count, d->smem_optin);
   if (!mma_layout_ok(L)) return LK_ERR_SHAPE;
-  mma_fn f = p.mode == LK_TWOPASS ? (L.a16 ? gemv_mma_kernel<2, true> : gemv_mma_kernel<2, false>)
-                                  : (L.a16 ? gemv_mma_kernel<1, true> : gemv_mma_kernel<1, false>);
+  mma_fn f = L.g4 ? (p.mode == LK_TWOPASS ? (L.a16 ? gemv_mma_g4_kernel<2, true> : gemv_mma_g4_kernel<2, false>)
+                                          : (L.a16 ? gemv_mma_g4_kernel<1, true> : gemv_mma_g4_kernel<1, false>))
+                  : (p.mode == LK_TWOPASS ? (L.a16 ? gemv_mma_kernel<2, true> : gemv_mma_kernel<2, false>)
+                                          : (L.a16 ? gemv_mma_kernel<1, true> : gemv_mma_kernel<1, false>));
   // (the cap is the device's maximum: see ring_gemv)
   if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) != cudaSuccess)
     return LK_ERR_CUDA;
@@ -640,7 +952,7 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   ra.l2_ahead = (int)(opt_l2_ahead_kb * 1024 / ((long)L.nw * L.stage_bytes));
   ra.trace = opt_trace == 3 ? trace_ptr() : nullptr;
   ra.tslot = opt_trace == 3 ? trace_next_slot() : -1;
-  ra.prefill = prefill_warps(L.nw);
+  ra.prefill = L.g4 ? prefill_warps(L.nw / G4) : prefill_warps(L.nw);  // groups, or warps
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)gx);
   cfg.blockDim = dim3(L.nw * 32);

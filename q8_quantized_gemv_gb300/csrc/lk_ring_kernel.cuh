@@ -562,7 +562,7 @@ __device__ __forceinline__ void compute_stage(typename part_t<Q>::t (&p)[M], con
           const float4 xx = xv[cc];
           const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) h = __fmaf_rn((float)(int8_t)(wi[cc] >> (8 * k)), xe[k], h);
+          for (int k = 0; k < 4; ++k) h = __fmaf_rn(i8_as_f32((unsigned)wi[cc] ^ 0x80808080u, k), xe[k], h);
         }
         const float blk = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
         p[t] = __fma_rn((double)wsc, (double)blk, (double)p[t]);

@@ -17,7 +17,7 @@ from q8_quantized_gemv_gb300 import build, lk, synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 I8, TP = 1, 2
-OPTS = ("mma_tk", "mma_warps", "mma_depth", "mma_act16", "grid_ctas", "gemv_path")
+OPTS = ("mma_tk", "mma_warps", "mma_depth", "mma_act16", "mma_group", "grid_ctas", "gemv_path")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,22 +59,30 @@ def run_case(N, K, M, mode, seed, amax=False):
     return y
 
 
+@pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("act16", [1, 2])
 @pytest.mark.parametrize("mode", [I8, TP])
 @pytest.mark.parametrize("M", [2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("N,K", [(16, 256), (1000, 1280), (333, 4096), (2500, 2304)])
-def test_mma_rows_and_tails(act16, mode, M, N, K):
-    """act16 1: activations held as f16; 2: held as int8, converted per use."""
+def test_mma_rows_and_tails(group, act16, mode, M, N, K):
+    """act16 1: activations held as f16; 2: held as int8, converted per use.
+    group 1: one warp per 16-row tile; 4: four warps per tile (one partial
+    each, combined through shared memory)."""
+    lk.lk_set_option("mma_group", group)
     lk.lk_set_option("mma_act16", act16)
     run_case(N, K, M, mode, 7000 + N + K + M)
 
 
+@pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("act16", [1, 2])
 @pytest.mark.parametrize("mode", [I8, TP])
 @pytest.mark.parametrize("tk,warps,depth", [(256, 0, 0), (512, 0, 0), (1024, 0, 0), (2048, 0, 0),
                                             (1024, 1, 2), (1024, 3, 1), (512, 16, 1), (256, 4, 4),
                                             (1024, 2, 3)])
-def test_mma_stage_layouts(act16, mode, tk, warps, depth):
+def test_mma_stage_layouts(group, act16, mode, tk, warps, depth):
+    if group == 4 and (warps % 4 or (depth and depth < 2)):
+        pytest.skip("four-warp tiles take warps in fours and two or more stages per group")
+    lk.lk_set_option("mma_group", group)
     lk.lk_set_option("mma_act16", act16)
     lk.lk_set_option("mma_tk", tk)
     lk.lk_set_option("mma_warps", warps)
@@ -82,14 +90,18 @@ def test_mma_stage_layouts(act16, mode, tk, warps, depth):
     run_case(777, 3328, 8, mode, 7100 + tk + warps)
 
 
+@pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("ctas", [1, 7, 152])
-def test_mma_grid_sizes(ctas):
+def test_mma_grid_sizes(ctas, group):
+    lk.lk_set_option("mma_group", group)
     lk.lk_set_option("grid_ctas", ctas)
     run_case(4100, 1024, 5, I8, 7200 + ctas)
 
 
+@pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("mode", [I8, TP])
-def test_mma_argmax_with_ties(mode):
+def test_mma_argmax_with_ties(mode, group):
+    lk.lk_set_option("mma_group", group)
     N, K, M = 3001, 512, 8
     wq, ws = synth.q8_matrix(N, K, 7300)
     x = synth.activation(M, K, 7301)
@@ -142,14 +154,16 @@ def test_mma_declines():
     lk.lk_set_option("mma_min_m", 0)
 
 
+@pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("mode", [I8, TP])
 @pytest.mark.parametrize("M", [1, 3, 8])
 @pytest.mark.parametrize("Ns", [(4096, 1024, 1024), (100, 37, 1000, 16), (5,)])
-def test_group_matches_single_calls_and_oracle(mode, M, Ns):
+def test_group_matches_single_calls_and_oracle(mode, M, Ns, group):
     """lk_gemv_q8_group over matrices with ragged N: each output has the bits
     of its own lk_gemv_q8 call and of the oracle (one launch for 2..8 rows,
     one launch per matrix for a single row)."""
     lk.lk_set_option("gemv_path", 0)
+    lk.lk_set_option("mma_group", group)
     K = 1280
     mats = [synth.q8_matrix(N, K, 7500 + i + N) for i, N in enumerate(Ns)]
     x = synth.activation(M, K, 7600 + M, outliers=True)
