@@ -355,6 +355,10 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 else a multiple of 256 up to 8192
  *   "mma_warps"   its warps per block: 0 auto, else 1..16
  *   "mma_depth"   its ring stages per warp: 0 = 1, else 1..8
+ *   "mma_i8"      its dots on the int8 tensor path (mma m16n8k32 s8, the
+ *                 levels as they are) instead of f16 MMAs on converted
+ *                 levels: 0 auto (Int8Act with 8+ tiles of 16 rows per
+ *                 SM), 1 always, 2 never
  *   "mma_group"   its warps per 16-row tile: 0 auto, 1 one warp per tile, 4
  *                 four warps per tile (each one partial b mod 4; for
  *                 launches with few tiles per SM)

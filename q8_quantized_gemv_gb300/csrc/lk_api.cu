@@ -29,6 +29,7 @@ long opt_l2_ahead_kb = 0;
 long opt_ring_prefill = 0;
 long opt_mma_act16 = 0;
 long opt_mma_group = 0;
+long opt_mma_i8 = 0;
 
 static const int kMaxDevices = 64;
 static DeviceInfo g_info[kMaxDevices];
@@ -338,6 +339,9 @@ lk_status lk_set_option(const char* name, long value) {
   } else if (!strcmp(name, "mma_depth")) {
     if (value < 0 || value > 8) return LK_ERR_ARG;
     opt_mma_depth = value;
+  } else if (!strcmp(name, "mma_i8")) {
+    if (value < 0 || value > 2) return LK_ERR_ARG;
+    opt_mma_i8 = value;
   } else if (!strcmp(name, "mma_group")) {
     if (value != 0 && value != 1 && value != 4) return LK_ERR_ARG;
     opt_mma_group = value;
@@ -377,6 +381,7 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "ring_prefill")) return opt_ring_prefill;
   if (!strcmp(name, "mma_act16")) return opt_mma_act16;
   if (!strcmp(name, "mma_group")) return opt_mma_group;
+  if (!strcmp(name, "mma_i8")) return opt_mma_i8;
   return -1;
 }
 

@@ -35,6 +35,7 @@ extern long opt_mma_min_m;    // fewest activation rows taking the tensor-core k
 extern long opt_mma_tk;       // its bytes of K per stage (0 auto, else a multiple of 256)
 extern long opt_mma_warps;    // its warps per block (0 auto)
 extern long opt_mma_depth;    // its ring stages per warp (0 = 1)
+extern long opt_mma_i8;       // its dots on the int8 tensor path: 0 auto (Int8Act), 1 always, 2 never
 extern long opt_mma_group;    // its tiles per warp: 0 auto, 1 one warp per tile, 4 four warps per tile
 extern long opt_mma_act16;    // its activations held as f16: 0 auto, 1 force, 2 never
 extern long opt_ring_prefill; // warps that issue their first weight stages before the dependency wait (0: half)

@@ -107,6 +107,27 @@ __device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d += A(16x32 int8, rows g/g+8) * B(32x8 int8, column g), exact int32
+// (m16n8k32: a0/a2 row g, a1/a3 row g+8, each 4 consecutive k; b0/b1 4 k each)
+__device__ __forceinline__ void imma16832(int (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                          unsigned b0, unsigned b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The block's exact dot on the int8 tensor path: lane (g, t)'s 8 bytes of
+// each operand are the k slots {4t..4t+3} (first word) and {4t+16..4t+19}
+// (second word) of one m16n8k32, the same permutation for A and B.  The
+// int32 result (|d| < 2^20) becomes an f32 by the magic-number add: its bits
+// added to those of 1.5 * 2^23, minus 1.5 * 2^23, exactly.
+__device__ __forceinline__ void block_dot_i8(float (&d)[4], uint2 w0, uint2 w8, uint2 x) {
+  int di[4] = {0, 0, 0, 0};
+  imma16832(di, w0.x, w8.x, w0.y, w8.y, x.x, x.y);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = __fadd_rn(__int_as_float(di[e] + 0x4B400000), -12582912.0f);
+}
+
 // The block's exact dot for rows (g, g+8) x activation rows (2t, 2t+1).
 __device__ __forceinline__ void block_dot(float (&d)[4], const Frag8& wg, const Frag8& wg8, const Frag8& x) {
   d[0] = d[1] = d[2] = d[3] = 0.f;
@@ -284,7 +305,9 @@ __device__ __forceinline__ bool load_rows(const MmaArgs& ra, unsigned char* act,
 // g+1 then cover 128 distinct bytes), so the B fragment is one 16-byte read
 // per 32-block instead of a read and 10 conversion instructions per warp.
 // Else the int8 words are held (stride K + 32) and converted per use.
-template <int Q, bool A16>
+// I8: the dots on the int8 tensor path (mma m16n8k32 s8, no level
+// conversions; activation rows held as int8), else on the f16 path.
+template <int Q, bool A16, bool I8 = false>
 __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) {
   extern __shared__ __align__(128) unsigned char smem[];
   const lkh::GemvProblem& a = ra.p;
@@ -396,18 +419,23 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int bb = 4 * gi + q;  // block within the slice; b0 % 4 == 0, so partial q
-        const Frag8 fw0 = frag8(*(const uint2*)(W0 + 32 * bb));
-        const Frag8 fw8 = frag8(*(const uint2*)(W8 + 32 * bb));
-        float d[4];
-        block_dot(d, fw0, fw8, act_frag<A16>(XH, k0 + 32 * bb, gx_ok));
+        const uint2 rw0 = *(const uint2*)(W0 + 32 * bb), rw8 = *(const uint2*)(W8 + 32 * bb);
+        float d[4], f[4];
+        if constexpr (I8) {
+          const uint2 z = make_uint2(0u, 0u);
+          block_dot_i8(d, rw0, rw8, gx_ok ? *(const uint2*)(XH + k0 + 32 * bb) : z);
+          if (Q == 2) block_dot_i8(f, rw0, rw8, gx_ok ? *(const uint2*)(XL + k0 + 32 * bb) : z);
+        } else {
+          const Frag8 fw0 = frag8(rw0), fw8 = frag8(rw8);
+          block_dot(d, fw0, fw8, act_frag<A16>(XH, k0 + 32 * bb, gx_ok));
+          if (Q == 2) block_dot(f, fw0, fw8, act_frag<A16>(XL, k0 + 32 * bb, gx_ok));
+        }
         const float ws_[4] = {wa[q], wa[q], wb[q], wb[q]};
         const float xs_[4] = {xa[q], xb[q], xa[q], xb[q]};
         if constexpr (Q == 1) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) p[q][e] = __fmaf_rn(__fmul_rn(ws_[e], xs_[e]), d[e], p[q][e]);
         } else {
-          float f[4];
-          block_dot(f, fw0, fw8, act_frag<A16>(XL, k0 + 32 * bb, gx_ok));
           // q8_step<2> with the dots already in f32 (exact integers)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -757,7 +785,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
 struct MmaLayout {
   unsigned tk, rs, srs, s_off, stage_bytes, ar, xsr, a_lo, a_xs, ring_off, total;
   int nw, depth;  // g4: warps (4 per group) and stages per group
-  bool a16, g4;
+  bool a16, g4, i8;
 };
 
 unsigned round_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
@@ -846,11 +874,29 @@ MmaLayout mma_layout_g4(const lkh::GemvProblem& p, int smem_optin, bool a16) {
 
 bool mma_layout_ok(const MmaLayout& L);
 
+// The int8 tensor path (option "mma_i8": 0 auto, 1 always, 2 never).  An
+// int8 MMA is a single instruction per 32-block with no level conversions,
+// but on this GPU a long-latency one: it won where the tiles are many (8
+// rows, Int8Act: gate/up 28.9 against 29.7 us, lm-head 127.9 against
+// 133.2 us) and lost where a warp's chain of blocks is the critical path
+// (4096x4096: 17.0 against 13.5 us; 4096x12288: 46.3 against 35.4 us; and
+// TwoPass, two per block, everywhere).
+bool use_i8(const lkh::GemvProblem& p, long ntiles, int sms) {
+  if (lkh::opt_mma_i8 == 2) return false;
+  if (lkh::opt_mma_i8 == 1) return true;
+  return p.mode == LK_INT8ACT && ntiles >= 8L * sms;
+}
+
 // f16-held activations where they cost no warps (Int8Act at K = 4096: 16
 // warps either way; TwoPass would drop from 16 to 10: measured 54.9 us
 // against 36.9 us held as int8); option "mma_act16" 1 forces them (if they
 // fit at all), 2 forbids them.
 MmaLayout mma_layout(const lkh::GemvProblem& p, long ntiles, int sms, int smem_optin) {
+  if (use_i8(p, ntiles, sms)) {
+    MmaLayout L = mma_layout_for(p, ntiles, sms, smem_optin, false);
+    L.i8 = true;
+    return L;
+  }
   if (lkh::opt_mma_group == 4) {
     const MmaLayout G8 = mma_layout_g4(p, smem_optin, false);
     if (lkh::opt_mma_act16 == 2) return G8;
@@ -905,7 +951,8 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   for (int m = 0; m < nmat; ++m) all_tiles += (N[m] + TR - 1) / TR;
   const MmaLayout L = mma_layout(p, all_tiles, d->sm_count, d->smem_optin);
   if (!mma_layout_ok(L)) return LK_ERR_SHAPE;
-  mma_fn f = L.g4 ? (p.mode == LK_TWOPASS ? (L.a16 ? gemv_mma_g4_kernel<2, true> : gemv_mma_g4_kernel<2, false>)
+  mma_fn f = L.i8 ? (p.mode == LK_TWOPASS ? gemv_mma_kernel<2, false, true> : gemv_mma_kernel<1, false, true>)
+           : L.g4 ? (p.mode == LK_TWOPASS ? (L.a16 ? gemv_mma_g4_kernel<2, true> : gemv_mma_g4_kernel<2, false>)
                                           : (L.a16 ? gemv_mma_g4_kernel<1, true> : gemv_mma_g4_kernel<1, false>))
                   : (p.mode == LK_TWOPASS ? (L.a16 ? gemv_mma_kernel<2, true> : gemv_mma_kernel<2, false>)
                                           : (L.a16 ? gemv_mma_kernel<1, true> : gemv_mma_kernel<1, false>));

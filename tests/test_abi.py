@@ -132,7 +132,8 @@ def test_options(lib):
                                            ("mma_warps", [0, 1, 16], [17, -1]), ("mma_depth", [0, 1, 8], [9, -1]),
                                            ("mma_act16", [0, 1, 2], [3, -1]), ("l2_ahead_kb", [0, 64], [-1]),
                                            ("ring_prefill", [0, 1, 12], [13, -1]),
-                                           ("mma_group", [0, 1, 4], [2, 3, 5, -1])])
+                                           ("mma_group", [0, 1, 4], [2, 3, 5, -1]),
+                                           ("mma_i8", [0, 1, 2], [3, -1])])
 def test_tensor_core_options(lib, name, good, bad):
     for v in good:
         lk.lk_set_option(name, v)

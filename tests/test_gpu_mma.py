@@ -17,7 +17,7 @@ from q8_quantized_gemv_gb300 import build, lk, synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 I8, TP = 1, 2
-OPTS = ("mma_tk", "mma_warps", "mma_depth", "mma_act16", "mma_group", "grid_ctas", "gemv_path")
+OPTS = ("mma_tk", "mma_warps", "mma_depth", "mma_act16", "mma_group", "mma_i8", "grid_ctas", "gemv_path")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,29 +59,33 @@ def run_case(N, K, M, mode, seed, amax=False):
     return y
 
 
-@pytest.mark.parametrize("group", [1, 4])
-@pytest.mark.parametrize("act16", [1, 2])
+@pytest.mark.parametrize("path", ["f16", "f16-act16", "f16-g4", "f16-g4-act16", "i8"])
 @pytest.mark.parametrize("mode", [I8, TP])
 @pytest.mark.parametrize("M", [2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("N,K", [(16, 256), (1000, 1280), (333, 4096), (2500, 2304)])
-def test_mma_rows_and_tails(group, act16, mode, M, N, K):
-    """act16 1: activations held as f16; 2: held as int8, converted per use.
-    group 1: one warp per 16-row tile; 4: four warps per tile (one partial
-    each, combined through shared memory)."""
-    lk.lk_set_option("mma_group", group)
-    lk.lk_set_option("mma_act16", act16)
+def test_mma_rows_and_tails(path, mode, M, N, K):
+    """f16: the dots as f16 MMAs on converted levels, activations held as int8
+    (or f16: act16); g4: four warps per 16-row tile (one partial each,
+    combined through shared memory); i8: the dots as int8 MMAs."""
+    lk.lk_set_option("mma_i8", 1 if path == "i8" else 2)
+    lk.lk_set_option("mma_group", 4 if "g4" in path else 1)
+    lk.lk_set_option("mma_act16", 1 if "act16" in path else 2)
     run_case(N, K, M, mode, 7000 + N + K + M)
 
 
+@pytest.mark.parametrize("i8", [1, 2])
 @pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("act16", [1, 2])
 @pytest.mark.parametrize("mode", [I8, TP])
 @pytest.mark.parametrize("tk,warps,depth", [(256, 0, 0), (512, 0, 0), (1024, 0, 0), (2048, 0, 0),
                                             (1024, 1, 2), (1024, 3, 1), (512, 16, 1), (256, 4, 4),
                                             (1024, 2, 3)])
-def test_mma_stage_layouts(group, act16, mode, tk, warps, depth):
+def test_mma_stage_layouts(i8, group, act16, mode, tk, warps, depth):
     if group == 4 and (warps % 4 or (depth and depth < 2)):
         pytest.skip("four-warp tiles take warps in fours and two or more stages per group")
+    if i8 == 1 and (group == 4 or act16 == 1):
+        pytest.skip("the int8 path is one warp per tile on int8 activation rows")
+    lk.lk_set_option("mma_i8", i8)
     lk.lk_set_option("mma_group", group)
     lk.lk_set_option("mma_act16", act16)
     lk.lk_set_option("mma_tk", tk)
@@ -99,9 +103,11 @@ def test_mma_grid_sizes(ctas, group):
 
 
 @pytest.mark.parametrize("group", [1, 4])
+@pytest.mark.parametrize("i8", [1, 2])
 @pytest.mark.parametrize("mode", [I8, TP])
-def test_mma_argmax_with_ties(mode, group):
+def test_mma_argmax_with_ties(mode, group, i8):
     lk.lk_set_option("mma_group", group)
+    lk.lk_set_option("mma_i8", i8)
     N, K, M = 3001, 512, 8
     wq, ws = synth.q8_matrix(N, K, 7300)
     x = synth.activation(M, K, 7301)
