@@ -66,6 +66,8 @@ def parse():
                     help="sequence: every GEMV computes RMSNorm/quantize itself (one launch per projection) "
                          "instead of a separate norm/quantize launch before it (the default, faster on GB300)")
     ap.add_argument("--unfused", action="store_true", help=argparse.SUPPRESS)  # the default; kept for scripts
+    ap.add_argument("--fuse", default="", help="sequence: comma-separated projections (q,k,v,o,gu,down,lm) "
+                                               "that compute their own norm/quantize prologue")
     ap.add_argument("--no-pdl", action="store_true",
                     help="no programmatic dependent launches between the fused GEMVs")
     ap.add_argument("--fused", action="store_true", help="gemv workload: RMSNorm->quantize->GEMV in one launch")
@@ -280,6 +282,8 @@ def run_ours(a, rank, world):
     lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
     _apply_opts(lk, a)
     fused = (a.fused_prologue or a.chain) and not a.unfused
+    if a.fuse and not fused:
+        fused = [n for n in a.fuse.split(",") if n]
     stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=fused, chain=a.chain and fused)
     tok_bytes = stack.weight_bytes()
     stream = torch.cuda.Stream(device=dev)

@@ -65,7 +65,10 @@ class DecodeStack:
         lk.lk_set_option("gemv_path", 2)
         ring = {n: lk.lk_gemv_kernel_for(N, K, self.mode, B, 0) == 2 for n, (N, K) in shapes.items()}
         lk.lk_set_option("gemv_path", prev)
-        self.fused = {n: bool(fused) and ring[n] and self.kernel[n] != 3 for n in shapes}
+        # fused: True / False for every projection, or the names of those
+        # that compute their own norm/quantize prologue
+        want = set(shapes) if fused is True else set() if not fused else set(fused)
+        self.fused = {n: n in want and ring[n] and self.kernel[n] != 3 for n in shapes}
         # the whole token as one cooperative chain launch (the ring kernel's
         # fused steps), where every step fits
         self.x_buf = self.x0.clone()  # the token's input rows
@@ -200,7 +203,9 @@ class DecodeStack:
         n = 1  # argmax reduce
         f = self.fused
         qkv_norm = 0 if (f["q"] and f["k"] and f["v"]) else 1  # one shared norm for q, k, v
-        grouped = self.qkv is not None or (qkv_norm and self.kernel["q"] == 3)
+        # q, k, v in one launch: the fused chain, or lk_gemv_q8_group on the
+        # tensor-core or chain kernel (both take the shape where the ring does)
+        grouped = self.qkv is not None or (not any(f[n] for n in ("q", "k", "v")) and self.kernel["q"] in (2, 3))
         per_layer = (4 if grouped else 6) + qkv_norm \
             + (0 if (f["o"] or self.mode == lk.LK_DEQUANT) else 1) + (0 if f["gu"] else 1) \
             + (0 if (f["down"] or self.mode == lk.LK_DEQUANT) else 1)
