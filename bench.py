@@ -71,6 +71,8 @@ def parse():
     ap.add_argument("--no-pdl", action="store_true",
                     help="no programmatic dependent launches between the fused GEMVs")
     ap.add_argument("--fused", action="store_true", help="gemv workload: RMSNorm->quantize->GEMV in one launch")
+    ap.add_argument("--norm", action="store_true",
+                    help="gemv workload: an RMSNorm->quantize launch before every GEMV (the separate form)")
     ap.add_argument("--table", default=None,
                     help="write the per-config single-GEMV table (markdown) to this path")
     ap.add_argument("--opt", action="append", default=[],
@@ -449,8 +451,15 @@ def run_gemv(a, rank, world, quiet=False):
 
     gain = synth.norm_gain_torch(K, synth.SEED_BASE + 48, dev)
 
+    xn = torch.empty((B, K), dtype=torch.float32, device=dev) if mode == lk.LK_DEQUANT else None
+
     def launch(r):
         wq, ws = mats[r % R]
+        if a.norm and not a.fused:
+            if mode == lk.LK_DEQUANT:
+                lk.lk_rmsnorm_quant(x, gain, mode, 1e-6, xn)
+            else:
+                lk.lk_rmsnorm_quant(x, gain, mode, 1e-6, None, acts["xq"], acts["xl"], acts["xs"])
         if a.fused:
             n = lk.lk_rmsnorm_quant_gemv_q8(wq, ws, mode, x, y, gain=gain, argmax_parts=parts)
             if a.argmax:
@@ -459,7 +468,8 @@ def run_gemv(a, rank, world, quiet=False):
             lk.lk_gemv_q8_splitk(wq, ws, mode, S, part, M=B, **acts)
             lk.lk_splitk_combine(mode, part, S, B, N, y)
         else:
-            n = lk.lk_gemv_q8(wq, ws, mode, y, M=B, argmax_parts=parts, **acts)
+            n = lk.lk_gemv_q8(wq, ws, mode, y, M=B, argmax_parts=parts, **({"x": xn} if xn is not None and a.norm
+                                                                            else acts))
             if a.argmax:
                 lk.lk_argmax(idx, B, N, parts=parts, n_parts=n)
 
@@ -501,14 +511,16 @@ def run_gemv(a, rank, world, quiet=False):
            "steps": a.steps, "warmup": a.warmup, "ms_per_step": us * 1e-3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": _dtype(a.mode), "data": "synthetic",
            "config": {"workload": f"Q8_0 GEMV N={N} K={K} batch {B} {a.mode} S={S}"
-                                  + (" + argmax" if a.argmax else "") + (" fused norm+quant" if a.fused else ""),
+                                  + (" + argmax" if a.argmax else "") + (" fused norm+quant" if a.fused else "")
+                                  + (" after a norm+quant launch" if a.norm and not a.fused else ""),
                       "rotation": f"{R} weight copies ({R * wbytes} bytes >= 4x L2), {max(R, 8)} launches per graph",
                       "path": a.path},
            "us_per_gemv": us, "pct_of_nominal_8TBs": gbs / NOMINAL_HBM_GBS,
            "roofline": {"bound": "hbm", "achieved": alg / (us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": alg / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], "traffic": None,
                         "peak_source": src, "algorithmic_bytes_per_launch": alg},
-           "clocks": clk, "gpu_launches": a.steps * Rg * (2 if (S > 1 or a.argmax) else 1),
+           "clocks": clk,
+           "gpu_launches": a.steps * Rg * (1 + (1 if (S > 1 or a.argmax) else 0) + (1 if a.norm and not a.fused else 0)),
            "kernel": {1: "direct", 2: "ring", 3: "mma", 0: "none"}[lk.lk_gemv_kernel_for(N, K, mode, B,
                                                                                           S if S > 1 else 0)]}
     del mats
@@ -530,7 +542,7 @@ def run_table(a, path):
     def g(label, **kw):
         b = copy.copy(a)
         b.workload, b.steps, b.warmup = "gemv", 20, 3
-        b.S, b.argmax, b.fused, b.batch, b.path = 1, False, False, 1, "auto"
+        b.S, b.argmax, b.fused, b.norm, b.batch, b.path = 1, False, False, False, 1, "auto"
         for k, v in kw.items():
             setattr(b, k, v)
         d = run_gemv(b, 0, 1, quiet=True)
@@ -542,12 +554,16 @@ def run_table(a, path):
     for m in ("dequant", "int8act", "twopass"):
         g("C1 q 4096x4096 (norm+quant fused)", N=4096, K=4096, mode=m, fused=True)
         g("C1 gate/up 24576x4096 (norm+quant fused)", N=24576, K=4096, mode=m, fused=True)
+        g("C1 q 4096x4096 (norm+quant launch, then GEMV)", N=4096, K=4096, mode=m, norm=True)
+        g("C1 gate/up 24576x4096 (norm+quant launch, then GEMV)", N=24576, K=4096, mode=m, norm=True)
     for m in ("twopass", "dequant"):
         for S in (1, 2, 4, 8):
             g("C2 o 5120x5120 split-K", N=5120, K=5120, mode=m, S=S)
             g("C2 down 5120x25600 split-K", N=5120, K=25600, mode=m, S=S)
     for m in ("dequant", "int8act", "twopass"):
         g("C3 lm-head 151936x4096 + argmax (norm fused)", N=151936, K=4096, mode=m, fused=True, argmax=True)
+        g("C3 lm-head 151936x4096 + argmax (norm launch, then GEMV)", N=151936, K=4096, mode=m, norm=True,
+          argmax=True)
     with open(path, "w") as f:
         f.write("| Config | Mode | M | S | kernel | us/GEMV | weight GB/s | %% of 8 TB/s | %% of measured %.0f GB/s |\n"
                 % peaks["hbm_gbs"])

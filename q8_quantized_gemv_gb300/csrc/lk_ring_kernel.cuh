@@ -545,6 +545,47 @@ __device__ __forceinline__ void compute_stage(typename part_t<Q>::t (&p)[M], con
   const float* XF = (const float*)act.base;
   const int ka = k0 - g.k_lo;  // offset of this slice in the activation area
   const int nseg = len >> 7;
+  if constexpr (Q == 0) {
+    // Dequant: the pair's f32 block sum is the same on both lanes; the f64
+    // step (GB300's FP64 rate is low) is split between them, lane 2q taking
+    // the even segments and lane 2q+1 the odd ones, so each warp issues one
+    // f64 step per two segments; finish_quad adds the two halves.  (The f64
+    // sum's order differs from the plain ascending one; Dequant is held to
+    // the tolerance, not to bits.)
+    const int hf = j & 1;
+#pragma unroll 2
+    for (int seg = 0; seg < nseg; seg += 2) {
+      const bool two = seg + 1 < nseg;
+      const int4 wA = *(const int4*)(Wr + 128 * seg);
+      const int4 wB = two ? *(const int4*)(Wr + 128 * (seg + 1)) : make_int4(0, 0, 0, 0);
+      const float wsA = __half2float(*(const __half*)(Sr + 8 * seg));
+      const float wsB = two ? __half2float(*(const __half*)(Sr + 8 * (seg + 1))) : 0.f;
+#pragma unroll
+      for (int t = 0; t < M; ++t) {
+        float blk[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int4 w = u ? wB : wA;
+          const float4* xv = (const float4*)(XF + (size_t)t * L + ka + 128 * (seg + u) + 16 * j);
+          const int wi[4] = {w.x, w.y, w.z, w.w};
+          float h = 0.f;
+          if (u == 0 || two) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const float4 xx = xv[cc];
+              const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) h = __fmaf_rn(i8_as_f32((unsigned)wi[cc] ^ 0x80808080u, k), xe[k], h);
+            }
+          }
+          blk[u] = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
+        }
+        const float wsel = hf ? wsB : wsA, bsel = hf ? blk[1] : blk[0];
+        p[t] = __fma_rn((double)wsel, (double)bsel, (double)p[t]);
+      }
+    }
+    return;
+  }
 #pragma unroll 4
   for (int seg = 0; seg < nseg; ++seg) {
     const int4 w = *(const int4*)(Wr + 128 * seg);
@@ -598,6 +639,7 @@ __device__ __forceinline__ void finish_quad(typename part_t<Q>::t (&p)[M], const
 #pragma unroll
   for (int t = 0; t < M; ++t) {
     P v = p[t];
+    if constexpr (Q == 0) v = v + __shfl_xor_sync(FULL, v, 1);  // the pair's two halves (compute_stage)
     v = v + __shfl_down_sync(FULL, v, 4);
     v = v + __shfl_down_sync(FULL, v, 2);
     p[t] = (P)0;
