@@ -335,7 +335,9 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 a barrier; default 0 = off)
  *   "trace"       1: the ring and chain kernels write block 0's timestamps
  *                 to the trace buffer (lk_trace_read); 2: the chain also
- *                 records every block's and block 0's warps' step ends;
+ *                 records every block's and block 0's warps' step ends, and
+ *                 when block 0's warps' first stage of each step was there
+ *                 and computed (from index 2048);
  *                 3: launch timeline: every ring, chain and tensor-core
  *                 launch made after the option was set owns a record of 8
  *                 entries (in launch order, 512 records, wrapping):

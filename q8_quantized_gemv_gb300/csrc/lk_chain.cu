@@ -309,7 +309,12 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
         break;
       }
       unsigned char* st = ring + (size_t)slot * ca.stage_bytes;
+      // trace 2: block 0's warps' first stage of each step: data there, computed
+      const bool tr2 = ca.trace && ca.trace_all && ca.tslot < 0 && n == 0 && blockIdx.x == 0 && lane == 0 &&
+                       2048 + 2 * ((long)op * nwc + warp) + 1 < LK_TRACE_MAX;
+      if (tr2) ca.trace[2048 + 2 * ((long)op * nwc + warp)] = gtimer();
       compute_stage<Q, M>(p, g, n, st, ac, lane);
+      if (tr2) ca.trace[2048 + 2 * ((long)op * nwc + warp) + 1] = gtimer();
       __syncwarp();
       ++consumed;
       if (iop < ca.n_ops) {

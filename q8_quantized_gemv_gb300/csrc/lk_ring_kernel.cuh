@@ -586,7 +586,7 @@ __device__ __forceinline__ void compute_stage(typename part_t<Q>::t (&p)[M], con
     }
     return;
   }
-#pragma unroll 4
+#pragma unroll 8
   for (int seg = 0; seg < nseg; ++seg) {
     const int4 w = *(const int4*)(Wr + 128 * seg);
     const float wsc = __half2float(*(const __half*)(Sr + 8 * seg));
