@@ -371,6 +371,11 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 weight stages before the wait on the previous kernel; the
  *                 others issue theirs once the activation is loaded (0 =
  *                 half of the warps, the default; 12 or 16 = all)
+ *   "ring_tk"     ring kernel: bytes of K per stage for rows longer than
+ *                 that, a multiple of 1024 up to 8192 (0 = auto: whole rows
+ *                 up to 8192, else 4096)
+ *   "group_prefill" the same for a grouped launch (lk_gemv_q8_group on the
+ *                 ring path): 0 = as "ring_prefill", else that many warps
  *   "l2_ahead_kb" ring and tensor-core kernels: KB per block of the stages
  *                 after the ring's first fill requested into L2 at kernel
  *                 start (cp.async.bulk.prefetch.L2), so that HBM keeps

@@ -27,6 +27,8 @@ long opt_mma_warps = 0;
 long opt_mma_depth = 0;
 long opt_l2_ahead_kb = 0;
 long opt_ring_prefill = 0;
+long opt_group_prefill = 0;
+long opt_ring_tk = 0;
 long opt_mma_act16 = 0;
 long opt_mma_group = 0;
 long opt_mma_i8 = 0;
@@ -351,6 +353,12 @@ lk_status lk_set_option(const char* name, long value) {
   } else if (!strcmp(name, "ring_prefill")) {
     if (value < 0 || value > 12) return LK_ERR_ARG;
     opt_ring_prefill = value;
+  } else if (!strcmp(name, "ring_tk")) {
+    if (value < 0 || value > 8192 || value % 1024) return LK_ERR_ARG;
+    opt_ring_tk = value;
+  } else if (!strcmp(name, "group_prefill")) {
+    if (value < 0 || value > 16) return LK_ERR_ARG;
+    opt_group_prefill = value;
   } else if (!strcmp(name, "l2_ahead_kb")) {
     if (value < 0 || value > 65536) return LK_ERR_ARG;
     opt_l2_ahead_kb = value;
@@ -379,6 +387,8 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "mma_depth")) return opt_mma_depth;
   if (!strcmp(name, "l2_ahead_kb")) return opt_l2_ahead_kb;
   if (!strcmp(name, "ring_prefill")) return opt_ring_prefill;
+  if (!strcmp(name, "group_prefill")) return opt_group_prefill;
+  if (!strcmp(name, "ring_tk")) return opt_ring_tk;
   if (!strcmp(name, "mma_act16")) return opt_mma_act16;
   if (!strcmp(name, "mma_group")) return opt_mma_group;
   if (!strcmp(name, "mma_i8")) return opt_mma_i8;

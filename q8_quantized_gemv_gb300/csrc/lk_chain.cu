@@ -395,8 +395,7 @@ unsigned act_area_rt(int mode, int M, unsigned len) {
 
 unsigned stage_bytes_for(int K) {
   const unsigned tk = K <= TKMAX ? (unsigned)K : 4096u;
-  const bool whole = tk >= (unsigned)K;
-  const unsigned srow = whole ? tk / 16u : tk / 16u + 16u;
+  const unsigned srow = tk / 16u + 16u;  // as make_geom (padded rows)
   return (QR * tk + QR * srow + 127u) & ~127u;
 }
 
@@ -468,6 +467,7 @@ static lk_status chain_launch(const lk_chain_op* ops, const lk_chain_op* ops_dev
   ca.gxs = nullptr;
   for (int i = 0; i < LK_MAX_GROUP; ++i) ca.inl[i] = ops[i < n_ops ? i : 0];
   if (given) {
+    if (lkh::opt_group_prefill > 0) ca.prefill = (int)lkh::opt_group_prefill;
     ca.n_inl = n_ops;
     ca.gx = given->x;
     ca.gxq = given->xq;

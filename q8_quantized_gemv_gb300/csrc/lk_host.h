@@ -38,6 +38,8 @@ extern long opt_mma_depth;    // its ring stages per warp (0 = 1)
 extern long opt_mma_i8;       // its dots on the int8 tensor path: 0 auto (Int8Act), 1 always, 2 never
 extern long opt_mma_group;    // its tiles per warp: 0 auto, 1 one warp per tile, 4 four warps per tile
 extern long opt_mma_act16;    // its activations held as f16: 0 auto, 1 force, 2 never
+extern long opt_group_prefill; // the same for a grouped launch over one given activation (0: as ring_prefill)
+extern long opt_ring_tk;       // ring kernel: bytes of K per stage for rows longer than that (0: auto)
 extern long opt_ring_prefill; // warps that issue their first weight stages before the dependency wait (0: half)
 extern long opt_l2_ahead_kb;  // ring/tensor-core kernels: KB per block of later stages requested into L2 at start
 

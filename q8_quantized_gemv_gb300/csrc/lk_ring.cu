@@ -124,10 +124,11 @@ Layout layout(const lkh::GemvProblem& p, int smem_optin) {
   const int nb = p.K / 32;
   const int S = p.split ? (p.S > 1 ? p.S : 1) : 1;
   L.act_len = 32u * (unsigned)max_chunk_blocks(nb, S);
-  // whole quads (two copies per stage) up to TKMAX; longer rows in 4 KB slices
+  // whole quads (one copy of the levels, one per row of scales) up to TKMAX;
+  // longer rows in 4 KB slices
   L.tk = p.K <= TKMAX ? (unsigned)p.K : 4096u;
-  const bool whole = S == 1 && L.tk >= (unsigned)p.K;
-  L.srow = whole ? L.tk / 16u : L.tk / 16u + 16u;
+  if (lkh::opt_ring_tk > 0 && lkh::opt_ring_tk < p.K) L.tk = (unsigned)lkh::opt_ring_tk;
+  L.srow = L.tk / 16u + 16u;  // as make_geom (padded rows)
   L.s_off = QR * L.tk;
   L.stage_bytes = (L.s_off + QR * L.srow + 127u) & ~127u;
   L.ring_off = (act_area_rt(p.mode, p.M, L.act_len) + 127u) & ~127u;

@@ -382,7 +382,9 @@ __device__ __forceinline__ Geom make_geom(const int8_t* wq, const void* ws, long
   g.nsl = (k_hi - k_lo + tk - 1) / tk;
   g.whole = (k_lo == 0 && k_hi == K && tk >= K);
   g.s_off = (unsigned)(QR * tk);
-  g.srow = g.whole ? (unsigned)g.nb * 2u : (unsigned)tk / 16u + 16u;
+  // 16 bytes of padding per row: the four rows' scales of a stage start in
+  // different banks (a step's scale loads, one per row, need one wavefront)
+  g.srow = (unsigned)tk / 16u + 16u;
   return g;
 }
 
@@ -406,8 +408,9 @@ __device__ __forceinline__ void issue_stage(const Geom& g, int warp, int nwc, lo
     if (lane == 0) {
       mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)g.K * 17u / 16u);
       bulk(st, g.wq + row0 * g.K, rows * g.K, full, pol);
-      bulk(st + g.s_off, g.ws + row0 * g.nb * 2, rows * g.nb * 2, full, pol);
     }
+    __syncwarp();
+    if (lane < rows) bulk(st + g.s_off + lane * g.srow, g.ws + (row0 + lane) * g.nb * 2, g.nb * 2, full, pol);
   } else {
     const int b0 = k0 >> 5, b1 = b0 + (len >> 5);
     const unsigned sh = (unsigned)(b0 & 7) * 2u;               // scales' offset in the first 16 B
@@ -546,13 +549,22 @@ __device__ __forceinline__ void compute_stage(typename part_t<Q>::t (&p)[M], con
   const int ka = k0 - g.k_lo;  // offset of this slice in the activation area
   const int nseg = len >> 7;
   if constexpr (Q == 0) {
-    // Dequant: the pair's f32 block sum is the same on both lanes; the f64
-    // step (GB300's FP64 rate is low) is split between them, lane 2q taking
-    // the even segments and lane 2q+1 the odd ones, so each warp issues one
-    // f64 step per two segments; finish_quad adds the two halves.  (The f64
-    // sum's order differs from the plain ascending one; Dequant is held to
-    // the tolerance, not to bits.)
+    // Dequant: the pair's f32 block sum is the same on both lanes; lane 2q
+    // takes the even segments' blocks and lane 2q+1 the odd ones (finish_quad
+    // adds the two halves).  The running sum across blocks is an f64 value
+    // carried through the stage as an unevaluated pair of f32 (hi + lo): each
+    // block's scaled sum w*b enters exactly as the pair (w*b, fma(w, b, -w*b))
+    // (Dekker's product) and is added to hi by Knuth's two-sum, the rounding
+    // errors collected in lo.  GB300's FP64 rate is low: this keeps the f64
+    // pipe to a few conversions per stage.  The pair's error is ~2^-44 of the
+    // sum of magnitudes; Dequant is held to the tolerance, not to bits.
     const int hf = j & 1;
+    float ah[M], al[M];
+#pragma unroll
+    for (int t = 0; t < M; ++t) {
+      ah[t] = __double2float_rn((double)p[t]);
+      al[t] = __double2float_rn(__dsub_rn((double)p[t], (double)ah[t]));
+    }
 #pragma unroll 2
     for (int seg = 0; seg < nseg; seg += 2) {
       const bool two = seg + 1 < nseg;
@@ -567,12 +579,20 @@ __device__ __forceinline__ void compute_stage(typename part_t<Q>::t (&p)[M], con
         for (int u = 0; u < 2; ++u) {
           const int4 w = u ? wB : wA;
           const float4* xv = (const float4*)(XF + (size_t)t * L + ka + 128 * (seg + u) + 16 * j);
-          const int wi[4] = {w.x, w.y, w.z, w.w};
+          // lane j's 16 values are 64 bytes apart from lane j+1's: read in
+          // the same order, lanes j and j+2 would hit the same banks.  Each
+          // lane pair starts at its own 16-byte word (word (cc + q) mod 4 in
+          // turn), which makes a quarter-warp's loads conflict-free; the
+          // weight words are rotated to match (the block sum's order is free
+          // under Dequant's tolerance).
+          const int a0 = (q & 1) ? w.y : w.x, a1 = (q & 1) ? w.z : w.y, a2 = (q & 1) ? w.w : w.z,
+                    a3 = (q & 1) ? w.x : w.w;
+          const int wi[4] = {(q & 2) ? a2 : a0, (q & 2) ? a3 : a1, (q & 2) ? a0 : a2, (q & 2) ? a1 : a3};
           float h = 0.f;
           if (u == 0 || two) {
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-              const float4 xx = xv[cc];
+              const float4 xx = xv[(cc + q) & 3];
               const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
 #pragma unroll
               for (int k = 0; k < 4; ++k) h = __fmaf_rn(i8_as_f32((unsigned)wi[cc] ^ 0x80808080u, k), xe[k], h);
@@ -581,9 +601,15 @@ __device__ __forceinline__ void compute_stage(typename part_t<Q>::t (&p)[M], con
           blk[u] = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
         }
         const float wsel = hf ? wsB : wsA, bsel = hf ? blk[1] : blk[0];
-        p[t] = __fma_rn((double)wsel, (double)bsel, (double)p[t]);
+        const float ph = __fmul_rn(wsel, bsel), pl = __fmaf_rn(wsel, bsel, -ph);
+        const float sh2 = __fadd_rn(ah[t], ph), bv = __fsub_rn(sh2, ah[t]);
+        const float er = __fadd_rn(__fsub_rn(ah[t], __fsub_rn(sh2, bv)), __fsub_rn(ph, bv));
+        ah[t] = sh2;
+        al[t] = __fadd_rn(al[t], __fadd_rn(er, pl));
       }
     }
+#pragma unroll
+    for (int t = 0; t < M; ++t) p[t] = __dadd_rn((double)ah[t], (double)al[t]);
     return;
   }
 #pragma unroll 8
@@ -594,32 +620,17 @@ __device__ __forceinline__ void compute_stage(typename part_t<Q>::t (&p)[M], con
     const int bi = (ka >> 5) + 4 * seg + q;
 #pragma unroll
     for (int t = 0; t < M; ++t) {
-      if constexpr (Q == 0) {
-        const float4* xv = (const float4*)(XF + (size_t)t * L + xo);
-        const int wi[4] = {w.x, w.y, w.z, w.w};
-        float h = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const float4 xx = xv[cc];
-          const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) h = __fmaf_rn(i8_as_f32((unsigned)wi[cc] ^ 0x80808080u, k), xe[k], h);
-        }
-        const float blk = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
-        p[t] = __fma_rn((double)wsc, (double)blk, (double)p[t]);
-      } else {
-        const int4 hv = *(const int4*)(XQ + (size_t)t * L + xo);
-        int d = dot16(w, hv);
-        d += __shfl_xor_sync(FULL, d, 1);
-        int e = 0;
-        if constexpr (Q == 2) {
-          const int4 lv = *(const int4*)(XL + (size_t)t * L + xo);
-          e = dot16(w, lv);
-          e += __shfl_xor_sync(FULL, e, 1);
-        }
-        const float s = XS[(size_t)t * (L / 32) + bi];
-        p[t] = q8_step<Q>((float)p[t], wsc, s, d, e);
+      const int4 hv = *(const int4*)(XQ + (size_t)t * L + xo);
+      int d = dot16(w, hv);
+      d += __shfl_xor_sync(FULL, d, 1);
+      int e = 0;
+      if constexpr (Q == 2) {
+        const int4 lv = *(const int4*)(XL + (size_t)t * L + xo);
+        e = dot16(w, lv);
+        e += __shfl_xor_sync(FULL, e, 1);
       }
+      const float s = XS[(size_t)t * (L / 32) + bi];
+      p[t] = q8_step<Q>((float)p[t], wsc, s, d, e);
     }
   }
 }

@@ -133,7 +133,9 @@ def test_options(lib):
                                            ("mma_act16", [0, 1, 2], [3, -1]), ("l2_ahead_kb", [0, 64], [-1]),
                                            ("ring_prefill", [0, 1, 12], [13, -1]),
                                            ("mma_group", [0, 1, 4], [2, 3, 5, -1]),
-                                           ("mma_i8", [0, 1, 2], [3, -1])])
+                                           ("mma_i8", [0, 1, 2], [3, -1]),
+                                           ("ring_tk", [0, 1024, 8192], [512, 9216, -1024]),
+                                           ("group_prefill", [0, 1, 16], [17, -1])])
 def test_tensor_core_options(lib, name, good, bad):
     for v in good:
         lk.lk_set_option(name, v)
