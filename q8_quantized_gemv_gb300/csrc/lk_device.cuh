@@ -193,6 +193,39 @@ __device__ __forceinline__ float i8_as_f32(unsigned u, int k) {
   return __fadd_rn(__uint_as_float(bits), -8388736.0f);
 }
 
+// The float 2^23 + 128 + b for byte k of u = w ^ 0x80808080 (i8_as_f32
+// before its subtraction).
+__device__ __forceinline__ float i8_bits_f32(unsigned u, int k) {
+  return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440u | (unsigned)k));
+}
+
+// Packed pairs of f32 (sm_100 and later: one instruction for both halves,
+// each rounded to nearest like its scalar form).
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2_pack(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f32x2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 __device__ __forceinline__ int dot16(int4 w, int4 x) {
   int d = __dp4a(w.x, x.x, 0);
   d = __dp4a(w.y, x.y, d);

@@ -549,67 +549,58 @@ __device__ __forceinline__ void compute_stage(typename part_t<Q>::t (&p)[M], con
   const int ka = k0 - g.k_lo;  // offset of this slice in the activation area
   const int nseg = len >> 7;
   if constexpr (Q == 0) {
-    // Dequant: the pair's f32 block sum is the same on both lanes; lane 2q
-    // takes the even segments' blocks and lane 2q+1 the odd ones (finish_quad
-    // adds the two halves).  The running sum across blocks is an f64 value
-    // carried through the stage as an unevaluated pair of f32 (hi + lo): each
-    // block's scaled sum w*b enters exactly as the pair (w*b, fma(w, b, -w*b))
-    // (Dekker's product) and is added to hi by Knuth's two-sum, the rounding
-    // errors collected in lo.  GB300's FP64 rate is low: this keeps the f64
-    // pipe to a few conversions per stage.  The pair's error is ~2^-44 of the
-    // sum of magnitudes; Dequant is held to the tolerance, not to bits.
-    const int hf = j & 1;
-    float ah[M], al[M];
+    // Dequant: lane l takes values 4l..4l+3 of every 128-value segment, of
+    // all four rows, so each f32 activation word is read from shared memory
+    // once per warp (not once per row): its 4-value sums, scaled by the
+    // block's weight scale, accumulate per lane and row in f32 over the
+    // stage; at the stage's end each row's 32 lane sums are added by a
+    // butterfly and lane 8r adds row r's total to its f64 partial (the
+    // other lanes keep 0; finish_quad's reduction then only moves it).  The
+    // order differs from a plain ascending sum; Dequant is held to the
+    // tolerance (a stage of at most 64 segments adds at most ~75 f32
+    // roundings of its sum of magnitudes, under 5e-6 of it).
+    // The arithmetic runs on packed f32 pairs (values k and k+2 of the four
+    // in the two halves): one instruction for two conversions, products or
+    // sums.
+    const unsigned char* W0 = st + 4 * lane;
+    const unsigned char* S0 = st + g.s_off + sh + 2 * (lane >> 3);
+    const f32x2 neg = f2_pack(-8388736.0f, -8388736.0f);  // 2^23 + 128, as in i8_as_f32
+    f32x2 acc[M][QR];
 #pragma unroll
-    for (int t = 0; t < M; ++t) {
-      ah[t] = __double2float_rn((double)p[t]);
-      al[t] = __double2float_rn(__dsub_rn((double)p[t], (double)ah[t]));
-    }
-#pragma unroll 2
-    for (int seg = 0; seg < nseg; seg += 2) {
-      const bool two = seg + 1 < nseg;
-      const int4 wA = *(const int4*)(Wr + 128 * seg);
-      const int4 wB = two ? *(const int4*)(Wr + 128 * (seg + 1)) : make_int4(0, 0, 0, 0);
-      const float wsA = __half2float(*(const __half*)(Sr + 8 * seg));
-      const float wsB = two ? __half2float(*(const __half*)(Sr + 8 * (seg + 1))) : 0.f;
+    for (int t = 0; t < M; ++t)
+#pragma unroll
+      for (int r = 0; r < QR; ++r) acc[t][r] = f2_pack(0.f, 0.f);
+#pragma unroll(M >= 4 ? 1 : 4)
+    for (int seg = 0; seg < nseg; ++seg) {
+      f32x2 w01[QR], w23[QR], ws2[QR];
+#pragma unroll
+      for (int r = 0; r < QR; ++r) {
+        const unsigned u = *(const unsigned*)(W0 + r * wrow + 128 * seg) ^ 0x80808080u;
+        const float wsr = __half2float(*(const __half*)(S0 + r * g.srow + 8 * seg));
+        w01[r] = f2_add(f2_pack(i8_bits_f32(u, 0), i8_bits_f32(u, 1)), neg);
+        w23[r] = f2_add(f2_pack(i8_bits_f32(u, 2), i8_bits_f32(u, 3)), neg);
+        ws2[r] = f2_pack(wsr, wsr);
+      }
 #pragma unroll
       for (int t = 0; t < M; ++t) {
-        float blk[2];
+        const float4 xx = *(const float4*)(XF + (size_t)t * L + ka + 128 * seg + 4 * lane);
+        const f32x2 x01 = f2_pack(xx.x, xx.y), x23 = f2_pack(xx.z, xx.w);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int4 w = u ? wB : wA;
-          const float4* xv = (const float4*)(XF + (size_t)t * L + ka + 128 * (seg + u) + 16 * j);
-          // lane j's 16 values are 64 bytes apart from lane j+1's: read in
-          // the same order, lanes j and j+2 would hit the same banks.  Each
-          // lane pair starts at its own 16-byte word (word (cc + q) mod 4 in
-          // turn), which makes a quarter-warp's loads conflict-free; the
-          // weight words are rotated to match (the block sum's order is free
-          // under Dequant's tolerance).
-          const int a0 = (q & 1) ? w.y : w.x, a1 = (q & 1) ? w.z : w.y, a2 = (q & 1) ? w.w : w.z,
-                    a3 = (q & 1) ? w.x : w.w;
-          const int wi[4] = {(q & 2) ? a2 : a0, (q & 2) ? a3 : a1, (q & 2) ? a0 : a2, (q & 2) ? a1 : a3};
-          float h = 0.f;
-          if (u == 0 || two) {
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const float4 xx = xv[(cc + q) & 3];
-              const float xe[4] = {xx.x, xx.y, xx.z, xx.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) h = __fmaf_rn(i8_as_f32((unsigned)wi[cc] ^ 0x80808080u, k), xe[k], h);
-            }
-          }
-          blk[u] = __fadd_rn(h, __shfl_xor_sync(FULL, h, 1));
-        }
-        const float wsel = hf ? wsB : wsA, bsel = hf ? blk[1] : blk[0];
-        const float ph = __fmul_rn(wsel, bsel), pl = __fmaf_rn(wsel, bsel, -ph);
-        const float sh2 = __fadd_rn(ah[t], ph), bv = __fsub_rn(sh2, ah[t]);
-        const float er = __fadd_rn(__fsub_rn(ah[t], __fsub_rn(sh2, bv)), __fsub_rn(ph, bv));
-        ah[t] = sh2;
-        al[t] = __fadd_rn(al[t], __fadd_rn(er, pl));
+        for (int r = 0; r < QR; ++r) acc[t][r] = f2_fma(ws2[r], f2_fma(w23[r], x23, f2_mul(w01[r], x01)), acc[t][r]);
       }
     }
 #pragma unroll
-    for (int t = 0; t < M; ++t) p[t] = __dadd_rn((double)ah[t], (double)al[t]);
+    for (int t = 0; t < M; ++t) {
+#pragma unroll
+      for (int r = 0; r < QR; ++r) {
+        float a0, a1;
+        f2_unpack(acc[t][r], a0, a1);
+        float v = __fadd_rn(a0, a1);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(FULL, v, o));
+        if (lane == 8 * r) p[t] = __dadd_rn((double)p[t], (double)v);
+      }
+    }
     return;
   }
 #pragma unroll 8
@@ -650,7 +641,6 @@ __device__ __forceinline__ void finish_quad(typename part_t<Q>::t (&p)[M], const
 #pragma unroll
   for (int t = 0; t < M; ++t) {
     P v = p[t];
-    if constexpr (Q == 0) v = v + __shfl_xor_sync(FULL, v, 1);  // the pair's two halves (compute_stage)
     v = v + __shfl_down_sync(FULL, v, 4);
     v = v + __shfl_down_sync(FULL, v, 2);
     p[t] = (P)0;
