@@ -68,6 +68,7 @@ def parse():
     ap.add_argument("--unfused", action="store_true", help=argparse.SUPPRESS)  # the default; kept for scripts
     ap.add_argument("--fuse", default="", help="sequence: comma-separated projections (q,k,v,o,gu,down,lm) "
                                                "that compute their own norm/quantize prologue")
+    ap.add_argument("--prefill", action="append", default=[], help=argparse.SUPPRESS)  # name=warps
     ap.add_argument("--no-pdl", action="store_true",
                     help="no programmatic dependent launches between the fused GEMVs")
     ap.add_argument("--fused", action="store_true", help="gemv workload: RMSNorm->quantize->GEMV in one launch")
@@ -286,7 +287,9 @@ def run_ours(a, rank, world):
     fused = (a.fused_prologue or a.chain) and not a.unfused
     if a.fuse and not fused:
         fused = [n for n in a.fuse.split(",") if n]
-    stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=fused, chain=a.chain and fused)
+    prefill = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in a.prefill}
+    stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=fused, chain=a.chain and fused,
+                        prefill=prefill)
     tok_bytes = stack.weight_bytes()
     stream = torch.cuda.Stream(device=dev)
 
@@ -381,6 +384,7 @@ def run_ours(a, rank, world):
                    "gemv_kernel": {k: "ring" if stack.fused[k] else {1: "direct", 2: "ring", 3: "mma"}.get(v, "none")
                                    for k, v in stack.kernel.items()},
                    "chain": stack.chain is not None,
+                   "ring_prefill": stack.prefill or "half of the warps",
                    "pdl": not a.no_pdl, "options": a.opt},
         "us_per_token": ms_max * 1e3,
         "pct_of_nominal_8TBs": value / world / NOMINAL_HBM_GBS,

@@ -24,9 +24,12 @@ from . import lk, synth
 class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
                  batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
-                 fused=False, chain=False, group_qkv=True):
+                 fused=False, chain=False, group_qkv=True, prefill=None):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
+        # per projection: warps of a ring GEMV block that fill their stages
+        # before the dependency wait (option "ring_prefill" for that launch)
+        self.prefill = dict(prefill or {})
         dev = self.dev
         s = seed
         self.shapes = {"q": (q_dim, hidden), "k": (kv_dim, hidden), "v": (kv_dim, hidden),
@@ -110,6 +113,17 @@ class DecodeStack:
         lk.lk_quantize_act(x, self.mode, a["xq"], a.get("xl"), a["xs"])
         return a
 
+    def _with_prefill(self, name, launch):
+        v = self.prefill.get(name)
+        if v is None:
+            return launch()
+        old = lk.lk_get_option("ring_prefill")
+        lk.lk_set_option("ring_prefill", v)
+        try:
+            return launch()
+        finally:
+            lk.lk_set_option("ring_prefill", old)
+
     def _gemv(self, w, y, acts, parts=None):
         return lk.lk_gemv_q8(w[0], w[1], self.mode, y, M=self.B, argmax_parts=parts, **acts)
 
@@ -156,7 +170,7 @@ class DecodeStack:
                 a = acts if acts is not None else (self._norm(x, gain) if gain is not None else self._quant(x))
 
                 def launch():
-                    return self._gemv(w, y, a, parts)
+                    return self._with_prefill(name, lambda: self._gemv(w, y, a, parts))
             return (launch() if hook is None else hook(name, launch)), a
 
         x = self.x_buf
