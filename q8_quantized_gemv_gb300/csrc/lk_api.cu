@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __rest
   const float* xr = x + row * K;
 
   A acc = 0;
-  for (int i = threadIdx.x; i < K; i += vt) acc = fma_acc((A)__ldg(xr + i), acc);
+  for (int i = threadIdx.x; i < K; i += vt) acc = fma_acc((A)__ldcg(xr + i), acc);
   acc = warp_tree_sum(acc);
   if (lane == 0) red[warp] = acc;
   __syncthreads();
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __rest
   // warp w holds the 32-groups starting at 32w, 32w + vt, ... (vt % 32 == 0)
   for (int base = warp * 32; base < K; base += vt) {
     const int i = base + lane;
-    const float yv = norm_scale(__ldg(xr + i), den, __ldg(g + i));
+    const float yv = norm_scale(__ldcg(xr + i), den, __ldg(g + i));
     if (xn) xn[row * K + i] = yv;
     if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, row * K + i, (row * K + i) >> 5, lane);
   }
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_split_kernel(const float* 
   trec_stamp(tr, slot, TR_WAITED);
   float v[KU_MAX];
 #pragma unroll
-  for (int u = 0; u < KU_MAX; ++u) v[u] = u < KU ? __ldg(xr + threadIdx.x + vt * u) : 0.f;
+  for (int u = 0; u < KU_MAX; ++u) v[u] = u < KU ? __ldcg(xr + threadIdx.x + vt * u) : 0.f;
   A acc = 0;
 #pragma unroll
   for (int u = 0; u < KU_MAX; ++u)
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(256) rmsnorm_quant_split256_kernel(const float
 #pragma unroll
   for (int j = 0; j < NJ; ++j)
 #pragma unroll
-    for (int u = 0; u < KU_MAX; ++u) v[j][u] = u < KU ? __ldg(xr + 32 * (warp + 8 * j) + lane + VT * u) : 0.f;
+    for (int u = 0; u < KU_MAX; ++u) v[j][u] = u < KU ? __ldcg(xr + 32 * (warp + 8 * j) + lane + VT * u) : 0.f;
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     A acc = 0;
@@ -235,7 +235,7 @@ __global__ void quantize_kernel(const float* __restrict__ x, long groups, int8_t
   if (g < groups) {  // whole warps
     const int lane = threadIdx.x & 31;
     const long i = g * 32 + lane;
-    quant_lane<Q>(__ldg(x + i), xq, xl, xs, i, g, lane);
+    quant_lane<Q>(__ldcg(x + i), xq, xl, xs, i, g, lane);
   }
   trec_end(tr, slot, TK_QUANT, groups * 32);
 }
@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(256) argmax_logits_kernel(const float* __restr
   const long i0 = (long)blockIdx.x * per, i1 = i0 + per < N ? i0 + per : N;
   unsigned long long best = 0;
   for (long i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
-    const unsigned long long k = amax_key(__ldg(logits + t * N + i), (unsigned)i);
+    const unsigned long long k = amax_key(__ldcg(logits + t * N + i), (unsigned)i);
     best = k > best ? k : best;
   }
   best = block_max_u64(best, sh);

@@ -146,11 +146,6 @@ __device__ __forceinline__ Frag8 act_frag(const unsigned char* X, int k, bool ok
   return frag8(ok ? *(const uint2*)(X + k) : make_uint2(0u, 0u));
 }
 
-__device__ __forceinline__ uint4 ld_nc16(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
-}
 
 struct Tiles {
   long base, stride, ntiles;
@@ -272,7 +267,7 @@ __device__ __forceinline__ bool load_rows(const MmaArgs& ra, unsigned char* act,
     }
     for (int i = threadIdx.x; i < M * nb; i += blockDim.x) {
       const int row = i / nb, b = i - row * nb;
-      ((float*)(act + ra.a_xs))[(size_t)row * ra.xsr + b] = __ldg(a.xs + (long)row * nb + b);
+      ((float*)(act + ra.a_xs))[(size_t)row * ra.xsr + b] = __ldcg(a.xs + (long)row * nb + b);
     }
     __syncthreads();
   } else if (warp == 0) {
@@ -838,7 +833,7 @@ MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int sm
 // Four warps per tile: 512-byte slices (256 when they do not fit), groups of
 // four warps with at least three stages each (the group consumes a stage four
 // times faster than one warp), as many groups as fit, up to four.
-MmaLayout mma_layout_g4(const lkh::GemvProblem& p, int smem_optin, bool a16) {
+MmaLayout mma_layout_g4(const lkh::GemvProblem& p, int smem_optin, bool a16, unsigned tk_pref = 0) {
   MmaLayout L{};
   const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)p.M;
   L.a16 = a16;
@@ -848,7 +843,7 @@ MmaLayout mma_layout_g4(const lkh::GemvProblem& p, int smem_optin, bool a16) {
   L.a_lo = round_up(M * L.ar, 128u);
   L.a_xs = p.mode == LK_TWOPASS ? round_up(L.a_lo + M * L.ar, 128u) : L.a_lo;
   L.ring_off = round_up(L.a_xs + M * L.xsr * 4u, 128u);
-  const unsigned cand_tk[2] = {512u, 256u};
+  const unsigned cand_tk[2] = {tk_pref ? tk_pref : 512u, tk_pref ? tk_pref : 256u};
   for (int i = 0; i < 2; ++i) {
     unsigned tk = lkh::opt_mma_tk > 0 ? (unsigned)lkh::opt_mma_tk : cand_tk[i];
     if (tk > round_up(K, 256u)) tk = round_up(K, 256u);
@@ -896,6 +891,17 @@ MmaLayout mma_layout(const lkh::GemvProblem& p, long ntiles, int sms, int smem_o
     MmaLayout L = mma_layout_for(p, ntiles, sms, smem_optin, false);
     L.i8 = true;
     return L;
+  }
+  // Int8Act launches with few tiles per SM (the narrow projections at 8
+  // rows: q, k, v, o, down): four warps per tile with 1 KB slices (2 KB for
+  // rows longer than 8192), where such a layout fits.  Measured at 8 rows
+  // against one warp per tile: down 4096x12288 35.4 -> 27.5 us, 4096x4096
+  // 13.4 -> 10.7 us, 1024x4096 10.6 -> 5.9 us.  (TwoPass keeps one warp per
+  // tile: its doubled activation area leaves four-warp groups too few
+  // stages, down 64.2 -> 130.1 us.)
+  if (lkh::opt_mma_group == 0 && p.mode == LK_INT8ACT && ntiles < 4L * sms) {
+    const MmaLayout G = mma_layout_g4(p, smem_optin, false, p.K > 8192 ? 2048u : 1024u);
+    if (mma_layout_ok(G)) return G;
   }
   if (lkh::opt_mma_group == 4) {
     const MmaLayout G8 = mma_layout_g4(p, smem_optin, false);

@@ -187,12 +187,23 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // read from global memory once, all of a warp's loads in flight together.
 constexpr int PRO_SLOTS = 32;  // groups per warp per batch held in registers by the prologue
 
-// A read-only f32 load that the compiler keeps where it is written: the
-// prologue issues all of a lane's loads before using any, so a row costs one
-// round trip to L2 instead of one per 32-group.
+// f32 loads that the compiler keeps where they are written: the prologue
+// issues all of a lane's loads before using any, so a row costs one round
+// trip to L2 instead of one per 32-group.  ld_keep (read-only path) is for
+// data no kernel writes (the norm gains); ld_keep_cg (L2 only) for the raw
+// activation, which the previous kernel writes: under a programmatic
+// dependent launch this kernel starts while that kernel still runs, and the
+// read-only path is only valid for data that stays unchanged over the
+// reading kernel's whole lifetime (measured: ld.global.nc here gave stale
+// values in a few replays in a hundred of a captured token).
 __device__ __forceinline__ float ld_keep(const float* p) {
   float v;
   asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_keep_cg(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
 __device__ __forceinline__ void compiler_fence() { asm volatile("" ::: "memory"); }
@@ -271,7 +282,7 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
       for (int b = 0; b < QB; ++b) {
         const int g = g0 + b * nwc, i = 32 * g + lane;
         const bool in = g < ng && k_lo + i < K;
-        qx[b] = in ? ld_keep(xr + k_lo + i) : 0.f;
+        qx[b] = in ? ld_keep_cg(xr + k_lo + i) : 0.f;
       }
     };
     auto load_batch = [&](int g0) {
@@ -289,12 +300,12 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
         float cur[KU_MAX], nxt[KU_MAX];
 #pragma unroll
         for (int u = 0; u < KU_MAX; ++u)
-          if (u < KU && cw < nvw_all) cur[u] = ld_keep(xr + 32 * cw + lane + vt * u);
+          if (u < KU && cw < nvw_all) cur[u] = ld_keep_cg(xr + 32 * cw + lane + vt * u);
         for (int w = cw; w < nvw_all; w += nwc) {
           const int wn = w + nwc;
 #pragma unroll
           for (int u = 0; u < KU_MAX; ++u)
-            if (u < KU && wn < nvw_all) nxt[u] = ld_keep(xr + 32 * wn + lane + vt * u);
+            if (u < KU && wn < nvw_all) nxt[u] = ld_keep_cg(xr + 32 * wn + lane + vt * u);
           A acc = 0;
 #pragma unroll
           for (int u = 0; u < KU_MAX; ++u)
@@ -308,7 +319,7 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
         for (int w = cw; w < nvw_all; w += nwc) {
           A acc = 0;
 #pragma unroll 8
-          for (int i = 32 * w + lane; i < K; i += vt) acc = fma_acc((A)__ldg(xr + i), acc);
+          for (int i = 32 * w + lane; i < K; i += vt) acc = fma_acc((A)__ldcg(xr + i), acc);
           acc = warp_tree_sum(acc);
           if (lane == 0) red[t * 32 + w] = acc;
         }

@@ -121,6 +121,41 @@ def test_chain_barrier_timeout_is_reported_and_recoverable():
     assert torch.equal(a.logits.view(torch.int32), ref.view(torch.int32))
 
 
+@pytest.mark.parametrize("prefill", [0, 1, 12])
+@pytest.mark.parametrize("fused", [False, True])
+def test_pdl_graph_replays_identical(fused, prefill):
+    """A captured token with programmatic dependent launches, replayed many
+    times, gives the bits of the plain launches every time, with any number
+    of warps filling before the dependency wait: every kernel's reads of what
+    the kernel before it wrote come after that kernel is complete (the
+    dependent starts early and must not read such data through a cache that
+    can hold lines from before)."""
+    a = DecodeStack(**SMALL, batch=1, mode=1, chain=False, fused=fused)
+    lk.lk_set_option("pdl", 0)
+    a.run_token()
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in list(a.out.items()) + [("h", a.h), ("logits", a.logits)]}
+    lk.lk_set_option("pdl", 1)
+    lk.lk_set_option("ring_prefill", prefill)
+    try:
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            a.run_token()
+        for r in range(60):
+            a.logits.zero_()
+            a.h.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            got = {k: v for k, v in list(a.out.items()) + [("h", a.h), ("logits", a.logits)]}
+            for k in ref:
+                assert torch.equal(got[k].view(torch.int32), ref[k].view(torch.int32)), (r, k)
+    finally:
+        lk.lk_set_option("pdl", 0)
+        lk.lk_set_option("ring_prefill", 0)
+    assert lk.lk_device_error(reset=True) == 0
+
+
 @pytest.mark.parametrize("fused", [False, True])
 def test_grouped_qkv_pdl_graph_matches_plain(fused):
     """The per-launch sequence with q, k, v as one grouped launch (after one

@@ -94,6 +94,16 @@ def test_mma_stage_layouts(i8, group, act16, mode, tk, warps, depth):
     run_case(777, 3328, 8, mode, 7100 + tk + warps)
 
 
+@pytest.mark.parametrize("M", [2, 8])
+@pytest.mark.parametrize("N,K", [(1024, 4096), (300, 12288), (4096, 4096)])
+def test_mma_auto_layout_few_tiles(N, K, M):
+    """The automatic choice for Int8Act launches with few tiles per SM (four
+    warps per tile, 1 KB or 2 KB slices): bit for bit the oracle."""
+    lk.lk_set_option("gemv_path", 0)
+    assert lk.lk_gemv_kernel_for(N, K, I8, M, 0) == 3
+    run_case(N, K, M, I8, 7250 + N + M)
+
+
 @pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("ctas", [1, 7, 152])
 def test_mma_grid_sizes(ctas, group):
