@@ -162,6 +162,23 @@ def test_gemv_parity(path, mode, M, N, K):
     assert np.array_equal(bits(host(y2)), bits(host(y)))
 
 
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("K", [8192, 12288, 25600])
+def test_dequant_long_rows_same_sign(path, M, K):
+    """Dequant where every product w*x is positive (no cancellation to hide
+    rounding): the longest whole-row stages (K = 8192, 64 segments summed in
+    f32 per lane) and sliced rows stay within 1e-5 of sum|W x|."""
+    need(path, K, 64, DQ, M)
+    rng = np.random.default_rng(4200 + K + M)
+    wq = rng.integers(1, 128, size=(64, K), dtype=np.int16).astype(np.int8)
+    _, ws = synth.q8_matrix(64, K, 4201 + K)
+    x = np.abs(synth.activation(M, K, 4202 + K + M, outliers=True)).astype(np.float32)
+    y_or = oracle.gemv(wq, ws, DQ, x=x)
+    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), DQ, dev_acts(x, DQ), M)
+    sync_check()
+    assert_gemv_close(host(y), y_or, wq, ws, x, DQ)
+
+
 @pytest.mark.parametrize("mode", [DQ, I8, TP])
 def test_gemv_batch_invariance(path, mode):
     N, K, M = 300, 2048, 8
