@@ -373,7 +373,7 @@ struct Geom {
   int K, nb;
   long r0, r1;
   int k_lo, k_hi, tk, nsl;
-  bool whole;               // a quad's levels (and its scales) are contiguous: 2 copies a stage
+  bool whole;               // a stage is a whole quad: one copy of its levels, one per row of scales
   unsigned s_off, srow;     // scale area inside a stage, bytes per row there
 };
 
