@@ -137,9 +137,12 @@ typedef struct {
  * Several GEMVs that read the same activation (the q, k and v projections
  * of a decoder layer, "kernels.rs" GEMV_Q8 applied per matrix): the same as
  * calling lk_gemv_q8 for each target in turn, without argmax, and with the
- * same bits.  Where the tensor-core kernel takes the shape (lk_gemv_kernel_for
- * of the first target == 3) the group is ONE launch whose 16-row tiles of all
- * matrices are dealt over the grid together; otherwise one launch per target.
+ * same bits.  Where the tensor-core kernel takes every matrix (2..8 rows,
+ * lk_gemv_kernel_for == 3) the group is ONE launch whose 16-row tiles of all
+ * matrices are dealt over the grid together.  Otherwise two or more matrices
+ * that the bulk-copy ring arrangement takes run as ONE launch of the chain
+ * kernel without barriers (each matrix's quads dealt on from where the
+ * previous matrix's stopped); anything else is one launch per target.
  * The library extends the pages here; they have no grouped call.
  *   targets  HOST array of n (1..LK_MAX_GROUP) matrices with the same K;
  *            read during the call only (a captured graph keeps the values).
