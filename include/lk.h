@@ -103,11 +103,12 @@ lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq
  *  lk_q8_sum4).  Quantized modes: each 32-block's int8 dot d (and e of the
  *  low words) is exact; block b's step goes into partial b mod 4 in ascending
  *  b:  Int8Act p = fma(w*s, d, p);  TwoPass p = fma(w, fma(s, d, (s/128)*e), p);
- *  y = (p0 + p2) + (p1 + p3).  Dequant: the products scaled by the f16 weight
- *  scale are summed in f32 over a stretch of the row (a 32-block in the
- *  direct kernel, a stage of at most 8192 values in the bulk-copy ring
- *  kernel) and the stretches in f64; the f64 row sum is rounded to f32 once
- *  (within 1e-5 of sum|W x| of the exact value, not bit-fixed).  For 2..8
+ *  y = (p0 + p2) + (p1 + p3).  Dequant: the products are summed in f32 over
+ *  a stretch of the row -- a 32-block in the direct kernel (scaled by the
+ *  f16 weight scale in f64), a stage of at most 8192 values in the bulk-copy
+ *  ring kernel (each block's part scaled in f32) -- and the stretches are
+ *  added in f64; the f64 row sum is rounded to f32 once (within 1e-5 of
+ *  sum|W x| of the exact value, not bit-fixed).  For 2..8
  *  rows of Int8Act / TwoPass the dots run on the tensor cores (f16 MMA on
  *  the exact int8 levels, or int8 MMA; accumulators that hold the exact
  *  integer dot); the combine is the same, so every kernel gives the same
