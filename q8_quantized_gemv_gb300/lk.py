@@ -176,7 +176,9 @@ def lk_gemv_q8(wq, ws, mode, y, x=None, xq=None, xl=None, xs=None, argmax_parts=
 
 def lk_gemv_q8_group(mats, mode, x=None, xq=None, xl=None, xs=None, M=None, stream=None):
     """mats: [(wq, ws, y), ...] sharing K and the activation: y = W x for
-    each, in one launch where the tensor-core kernel applies."""
+    each, with the bits of one lk_gemv_q8 call per matrix; one launch where
+    the tensor-core kernel (2..8 rows) or, for two or more matrices, the
+    chain kernel's ring arrangement (one row) takes the shapes."""
     K = mats[0][0].shape[1]
     if M is None:
         M = (x if x is not None else xq).shape[0]
