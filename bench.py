@@ -198,6 +198,22 @@ def host_layer(stack_or_none, l, B, mode_seed=0):
     return out
 
 
+def host_info():
+    """The host the CPU timings ran on: logical CPUs, architecture, model."""
+    import platform
+    info = {"nproc": os.cpu_count(), "machine": platform.machine()}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip() in ("model name", "Model", "Hardware", "CPU part") and v.strip():
+                    info["model"] = v.strip()
+                    break
+    except OSError:
+        pass
+    return info
+
+
 def cpu_baseline(stack, a, budget_s):
     import oracle
 
@@ -217,7 +233,7 @@ def cpu_baseline(stack, a, budget_s):
     return {"value": tot_b / tot_t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"layers 0..{layers - 1} of the sequence (full matrices, norm + quantize + "
                       f"6 GEMVs each, batch {a.batch}, {a.mode}), single-threaded C oracle",
-            "seconds": tot_t}
+            "seconds": tot_t, "host": host_info()}
 
 
 # ---- reference arm: the CPU oracle -----------------------------------------------------
@@ -255,7 +271,7 @@ def run_reference(a, rank):
                                         "sample": "2 of the layers per step, on the host"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "each step: layers 0-1 of the sequence (full matrices) in the "
-                                   "single-threaded C oracle"},
+                                   "single-threaded C oracle", "host": host_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

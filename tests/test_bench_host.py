@@ -67,3 +67,8 @@ def test_peaks_and_defaults():
 def test_replica_value():
     assert bench.replica_value(8_041_103_360, 1, 2.0) == pytest.approx(8_041_103_360 / 2e-3 / 1e9)
     assert bench.replica_value(1e9, 4, 1.0) == pytest.approx(4000.0)
+
+
+def test_host_info():
+    h = bench.host_info()
+    assert isinstance(h["nproc"], int) and h["nproc"] >= 1 and h["machine"]
