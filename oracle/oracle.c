@@ -35,8 +35,8 @@
 /* IEEE binary16 -> binary32, from the format's definition: sign, 5-bit
  * exponent biased by 15, 10-bit fraction; exponent 0 is subnormal
  * (fraction * 2^-24), exponent 31 is inf/NaN.  The Q8_0 block scale is an f16
- * ([lane] module doc: "A Q8_0 matrix is uploaded split"; the scale array holds
- * one half per 32 weights).  The value is exact in f32. */
+ * ([lane] module doc: a Q8_0 matrix reaches the device as two arrays, the int8
+ * levels and one f16 scale for every 32 weights).  The value is exact in f32. */
 float oracle_half_to_float(uint16_t h)
 {
     int sign = (h >> 15) & 1;
@@ -53,9 +53,15 @@ float oracle_half_to_float(uint16_t h)
 }
 
 /* Round to nearest, ties to even (the pages' __float2int_rn).  The distance
- * to the floor is taken in f64, where it is exact for any f32 input. */
+ * to the floor is taken in f64, where it is exact for any f32 input.  Values
+ * outside the int range saturate and NaN gives 0, as the GPU's conversion
+ * does; the quantizer below never produces either (its quotients stay within
+ * about +-128), so this only keeps the function defined everywhere. */
 static int round_half_even(float v)
 {
+    if (v != v) return 0;
+    if (v >= 2147483648.0f) return 2147483647;
+    if (v < -2147483648.0f) return -2147483647 - 1;
     double fl = floor((double)v);
     double diff = (double)v - fl;
     long n = (long)fl;
@@ -69,12 +75,22 @@ static int clamp8(int v) { return v > 127 ? 127 : (v < -128 ? -128 : v); }
 /* ---- activation quantizer ------------------------------------------------
  * [lane] module doc and PRELUDE (lk_quant_lane, lk_two_scale, lk_two_words):
  * a group of 32 values shares one scale from its largest magnitude a.
- *   Int8Act:  s = a > 0 ? a/127 : 1;   hi = rn(v/s)   (no clamp: |v/s| <= 127)
+ *   Int8Act:  s = a/127 (1 for an all-zero group);  hi = rn(v/s)
  *   TwoPass:  s = max(a, 1e-30)/127;   hi = clamp(rn(v/s));
  *             r = fma(-hi, s, v);      lo = clamp(rn(r / (s * 2^-7)))
  * The quotient form is the definition (the reciprocal variant lk_two_words_r is
  * a kernel shortcut and is not used).  Dequant keeps f32 and quantizes nothing.
+ *
+ * Reading for Int8Act groups whose largest magnitude is tiny: the pages give
+ * the scale 1 only to a = 0, but for 0 < a < 127 * 2^-126 the scale a/127 is
+ * subnormal or zero, loses bits, and v/s then leaves [-127, 127] (even inf or
+ * NaN), so hi would not fit its int8.  Such a group is treated as the all-zero
+ * group (s = 1, every hi = 0): then |v - hi*s| = |v| < 2^-119 <= s/2 still
+ * holds, and for every a >= 127 * 2^-126 the scale is a normal float and
+ * |v/s| <= 127 (1 + 2^-24), so rn(v/s) is within [-127, 127] without a clamp.
+ * TwoPass needs no such rule: its scale is at least 1e-30/127, a normal float.
  * v has K values, K a multiple of 32; hi/lo have K entries, s has K/32. */
+#define OR_INT8ACT_MIN_MAX 0x1.fcp-120f /* 127 * 2^-126 */
 void oracle_quantize_row(const float* v, int K, int mode, int8_t* hi, int8_t* lo, float* s)
 {
     for (int g = 0; g < K / 32; ++g) {
@@ -86,7 +102,7 @@ void oracle_quantize_row(const float* v, int K, int mode, int8_t* hi, int8_t* lo
         }
         float sc;
         if (mode == OR_INT8ACT)
-            sc = a > 0.0f ? a / 127.0f : 1.0f;
+            sc = a >= OR_INT8ACT_MIN_MAX ? a / 127.0f : 1.0f;
         else
             sc = (a > 1e-30f ? a : 1e-30f) / 127.0f;
         s[g] = sc;
@@ -106,9 +122,10 @@ void oracle_quantize_row(const float* v, int K, int mode, int8_t* hi, int8_t* lo
 }
 
 /* ---- RMSNorm ---------------------------------------------------------------
- * [lane] module doc: "an RMSNorm divides by sqrt(mean + 1e-6) then scales";
- * RMSNORM (lk_rmsnorm_row): y_i = v_i / sqrt(sum(v^2)/K + eps) * g_i, the sum
- * in the accumulator of the mode (f64 under Dequant, f32 otherwise: lk_acc).
+ * [lane] module doc: the norm divides each value by the square root of the
+ * mean square plus 1e-6, then multiplies by the gain; RMSNORM
+ * (lk_rmsnorm_row): y_i = v_i / sqrt(sum(v^2)/K + eps) * g_i, the sum in the
+ * accumulator of the mode (f64 under Dequant, f32 otherwise: lk_acc).
  *
  * The f32 sum of squares is not associative, so its order is part of the
  * definition.  The pages' block is norm_threads(K) = min(roundup32(K), 1024)
@@ -254,8 +271,8 @@ static float q8_row_range(const int8_t* wq, const uint16_t* ws, int K, int mode,
 
 /* Dequant value of row o over columns [k0, k1): the plain definition, W = f16
  * scale * level (exact in f32), each product (double)W*(double)x exact in f64,
- * summed in ascending k in f64 ([lane] module doc: "the dot accumulates in
- * f64").  Returned unrounded. */
+ * summed in ascending k in f64 ([lane] module doc: Dequant's dot is an f64
+ * sum).  Returned unrounded. */
 static double deq_row_range(const int8_t* wq, const uint16_t* ws, int K, long o, const float* x,
                             int k0, int k1)
 {
@@ -348,7 +365,7 @@ void oracle_absdot_rows(const int8_t* wq, const uint16_t* ws, int K, const float
 }
 
 /* ---- argmax ------------------------------------------------------------------
- * [lane] module doc: "an arg-max keeps the first of equal maxima"; [mak]
+ * [lane] module doc: of equal maxima the arg-max returns the first; [mak]
  * ph_argmax_part: lowest index on ties.  A linear scan with a strict `>` over
  * the logits as stored in f32 (so -0 == +0).  n >= 1.  NaN is unspecified. */
 long oracle_argmax(const float* v, long n)

@@ -14,6 +14,9 @@ from q8_quantized_gemv_gb300 import synth
 
 DQ, I8, TP = oracle.DEQUANT, oracle.INT8ACT, oracle.TWOPASS
 U32 = 2.0 ** -24
+# Int8Act: groups with max|v| below 127 * 2^-126 (a/127 not a normal float)
+# are quantized as the all-zero group (the reading for tiny groups)
+INT8ACT_MIN_MAX = 127.0 * 2.0 ** -126
 
 
 # ---- f16 scales -----------------------------------------------------------
@@ -49,6 +52,13 @@ def _groups(seed, n=400):
     g[::17, 5] = 0.0          # zeros inside groups
     g[::29, :] = 0.0          # all-zero groups
     g[::31, :] = np.float32(0.5)  # all equal
+    # groups whose largest magnitude is tiny: subnormal, and straddling the
+    # Int8Act threshold 127 * 2^-126 below which a group is quantized as zero
+    g[3::37, :] = (g[3::37, :] * np.float32(2.0 ** -140)).astype(np.float32)
+    g[7::41, :] = (g[7::41, :] / np.abs(g[7::41, :]).max(axis=1, keepdims=True)
+                   * np.float32(INT8ACT_MIN_MAX) * np.float32(1.5)).astype(np.float32)
+    g[11::43, :] = (g[11::43, :] / np.abs(g[11::43, :]).max(axis=1, keepdims=True)
+                    * np.float32(INT8ACT_MIN_MAX) * np.float32(0.75)).astype(np.float32)
     return g.reshape(1, -1)
 
 
@@ -61,7 +71,8 @@ def test_quantizer_invariants(mode):
     a = np.abs(v.reshape(-1, 32)).max(axis=1)
     # the scale: max|v|/127 as one IEEE f32 division (numpy), with the per-mode floor
     if mode == I8:
-        want = np.where(a > 0, a / np.float32(127.0), np.float32(1.0)).astype(np.float32)
+        want = np.where(a >= INT8ACT_MIN_MAX, a / np.float32(127.0), np.float32(1.0)).astype(np.float32)
+        assert (a < INT8ACT_MIN_MAX).sum() > (a == 0).sum()  # tiny groups are present
     else:
         want = (np.maximum(a, np.float32(1e-30)) / np.float32(127.0)).astype(np.float32)
     assert np.array_equal(s[0].view(np.uint32), want.view(np.uint32))
