@@ -67,7 +67,8 @@ int lk_version(void);
 /*
  * RMSNorm of M rows, then the activation quantizer of `mode`.
  * ("kernels.rs" RMSNORM lk_rmsnorm / lk_rmsnorm_row with lk_quant_lane;
- *  module doc: "an RMSNorm divides by sqrt(mean + 1e-6) then scales".)
+ *  its module doc: each value over the root of the mean square plus eps,
+ *  times the gain.)
  *   y[t][i] = x[t][i] / sqrt(sum_k x[t][k]^2 / K + eps) * gain[i]
  * The sum of squares is accumulated in f64 under LK_DEQUANT and in f32
  * otherwise, in the fixed order of a block of min(roundup32(K), 1024)
@@ -88,7 +89,9 @@ lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, floa
  * The activation quantizer alone ("kernels.rs" QUANT lk_quant, PRELUDE
  * lk_quant_lane / lk_two_scale / lk_two_words).  Per 32-value group with
  * a = max|v|:
- *   LK_INT8ACT: s = a > 0 ? a/127 : 1; hi = rn(v/s)
+ *   LK_INT8ACT: s = a/127, hi = rn(v/s); a group with a < 127 * 2^-126
+ *               (a/127 not a normal float, a = 0 included) gets s = 1 and
+ *               hi = 0, so hi always lies in [-127, 127]
  *   LK_TWOPASS: s = max(a, 1e-30)/127; hi = clamp(rn(v/s));
  *               lo = clamp(rn(fma(-hi, s, v) / (s/128)))
  * rn rounds to nearest even; divisions are IEEE.  mode LK_DEQUANT is an
@@ -274,9 +277,9 @@ int lk_argmax_parts_max(int N);
 int lk_argmax_scratch_entries(int N);
 
 /*
- * First index of the maximum of each of M rows ("kernels.rs" module doc: the
- * arg-max keeps the first of equal maxima; "megakernel.cu" ph_argmax_part /
- * ph_argmax_fin).  Two forms:
+ * First index of the maximum of each of M rows ("kernels.rs" module doc on
+ * the arg-max: the lowest index among equal maxima; "megakernel.cu"
+ * ph_argmax_part / ph_argmax_fin).  Two forms:
  *   parts != NULL: reduce the n_parts keys per row that lk_gemv_q8 wrote
  *                  (logits and scratch are ignored);
  *   parts == NULL: reduce logits f32 [M][N] in two kernels through scratch
@@ -301,7 +304,11 @@ lk_status lk_argmax(const float* logits, const uint64_t* parts, int n_parts, int
  * exits; shapes that would need more return LK_ERR_WORKSPACE (none do within
  * M <= LK_MAX_M).  The first call on each device looks the array's address up
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  The call allocates and frees nothing.  All
+ * before any stream capture.  Host threads may make first calls at the same
+ * time (the per-device address cache is atomic).  The address belongs to the
+ * device's context: after cudaDeviceReset() of a device it is stale, as are
+ * the library's other per-device addresses, so do not call the library on a
+ * device after resetting it.  The call allocates and frees nothing.  All
  * calls share the array: calls that can overlap on the GPU (other streams,
  * other threads) race and must be serialized by the caller; the array keeps
  * the last call's keys, which every call overwrites before reading.

@@ -3,6 +3,8 @@
 // reductions and the block-dot test hook.
 #include <string.h>
 
+#include <mutex>
+
 #include "lk_device.cuh"
 #include "lk_host.h"
 
@@ -33,23 +35,28 @@ long opt_mma_act16 = 0;
 long opt_mma_group = 0;
 long opt_mma_i8 = 0;
 
-static const int kMaxDevices = 64;
+// Per-device attributes, queried once per device under a lock (concurrent
+// first calls are safe).
 static DeviceInfo g_info[kMaxDevices];
-static int g_info_ok[kMaxDevices];
+static std::atomic<int> g_info_ok[kMaxDevices];
+static std::mutex g_info_lock;
 
 const DeviceInfo* device_info(int* dev_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   if (dev_out) *dev_out = dev;
-  if (!g_info_ok[dev]) {
-    DeviceInfo d;
-    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
-      return nullptr;
-    g_info[dev] = d;
-    g_info_ok[dev] = 1;
+  if (!g_info_ok[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> hold(g_info_lock);
+    if (!g_info_ok[dev].load(std::memory_order_relaxed)) {
+      DeviceInfo d;
+      if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+        return nullptr;
+      g_info[dev] = d;
+      g_info_ok[dev].store(1, std::memory_order_release);
+    }
   }
   return &g_info[dev];
 }
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __rest
     const int i = base + lane;
     const float yv = norm_scale(__ldcg(xr + i), den, __ldg(g + i));
     if (xn) xn[row * K + i] = yv;
-    if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, row * K + i, (row * K + i) >> 5, lane);
+    if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, (row * K + i) >> 5, lane);
   }
   trec_end(tr, slot, TK_NORM, K);
 }
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_quant_split_kernel(const float* 
   const long i = row * K + threadIdx.x + (long)vt * u_mine;
   const float yv = norm_scale(mine, den, gv);
   if (xn) xn[i] = yv;
-  if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, i, i >> 5, lane);
+  if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, i >> 5, lane);
   trec_end(tr, slot, TK_NORM, K);
 }
 
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(256) rmsnorm_quant_split256_kernel(const float
     const long i = row * K + 32 * (warp + 8 * j) + lane + (long)VT * u_mine;
     const float yv = norm_scale(mine, den, gv[j]);
     if (xn) xn[i] = yv;
-    if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, i, i >> 5, lane);
+    if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, i >> 5, lane);
   }
   trec_end(tr, slot, TK_NORM, K);
 }
@@ -235,7 +242,7 @@ __global__ void quantize_kernel(const float* __restrict__ x, long groups, int8_t
   if (g < groups) {  // whole warps
     const int lane = threadIdx.x & 31;
     const long i = g * 32 + lane;
-    quant_lane<Q>(__ldcg(x + i), xq, xl, xs, i, g, lane);
+    quant_lane<Q>(__ldcg(x + i), xq, xl, xs, g, lane);
   }
   trec_end(tr, slot, TK_QUANT, groups * 32);
 }
@@ -618,17 +625,10 @@ static __device__ __align__(256) unsigned long long lk_noalloc_argmax_scratch[LK
 
 // The array's device address on the current device, looked up the first
 // time the entry point runs on that device (cudaGetSymbolAddress with the
-// device current) and cached.
+// device current) and kept per device; concurrent first calls are safe.
 static unsigned long long* noalloc_scratch_ptr() {
-  static unsigned long long* ptr[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, lk_noalloc_argmax_scratch) != cudaSuccess) return nullptr;
-    ptr[dev] = (unsigned long long*)p;
-  }
-  return ptr[dev];
+  static std::atomic<unsigned long long*> cache[kMaxDevices];
+  return device_symbol(cache, (const void*)lk_noalloc_argmax_scratch);
 }
 
 extern "C" lk_status lk_argmax_noalloc(const float* logits, int M, int N, int32_t* idx, cudaStream_t stream) {

@@ -65,9 +65,20 @@ __device__ __forceinline__ A warp_tree_sum(A v) {
   return v;
 }
 
-// ---- the activation quantizer ("kernels.rs" lk_quant_lane / lk_two_words) ------
-// The calling warp holds one 32-value group, value v in this lane.  Writes
-// the lane's word(s) at index i and (lane 0) the group's scale at g.
+// ---- the activation quantizer ("kernels.rs" PRELUDE: lk_quant_lane,
+// lk_two_scale, lk_two_words) ------------------------------------------------
+// A warp quantizes NG 32-value groups at once, one value of each per lane;
+// the groups' steps are written phase by phase, so their independent chains
+// (the IEEE divisions above all) interleave.  Per group, a = max|v|:
+//   Int8Act (Q 1): s = a/127; a group with a < 127 * 2^-126 (a/127 not a
+//                  normal float, the all-zero group included) gets s = 1 and
+//                  hi = 0; otherwise |v/s| <= 127 (1 + 2^-24) and
+//                  hi = rn(v/s) needs no clamp.
+//   TwoPass (Q 2): s = max(a, 1e-30)/127; hi = clamp(rn(v/s)) and
+//                  lo = clamp(rn(fma(-hi, s, v) / (s/128))).
+// rn rounds to nearest even; every division is the IEEE one.
+constexpr float kInt8ActMinMax = 0x1.fcp-120f;  // 127 * 2^-126
+
 // max|v| over the warp in one instruction: for non-negative floats the IEEE
 // order is the order of their bit patterns, so the integer max of the bits
 // of |v| is the bits of max|v| (exact; NaN inputs are unspecified).
@@ -76,71 +87,51 @@ __device__ __forceinline__ float warp_absmax(float v) {
 }
 
 template <int Q>
-__device__ __forceinline__ void quant_lane(float v, int8_t* __restrict__ hi, int8_t* __restrict__ lo,
-                                           float* __restrict__ xs, long i, long g, int lane) {
-  const float a = warp_absmax(v);
-  float s;
-  if (Q == 1) {
-    s = a > 0.f ? __fdiv_rn(a, 127.0f) : 1.0f;
-  } else {
-    s = __fdiv_rn(a > 1e-30f ? a : 1e-30f, 127.0f);
+__device__ __forceinline__ float act_scale(float a) {
+  if constexpr (Q == 1) return a >= kInt8ActMinMax ? __fdiv_rn(a, 127.0f) : 1.0f;
+  return __fdiv_rn(fmaxf(a, 1e-30f), 127.0f);
+}
+
+__device__ __forceinline__ int sat_i8(int v) { return min(max(v, -128), 127); }
+
+// Groups G_k = g + k * step (k < NG) of one activation row: lane `lane`
+// holds v[k], element 32 G_k + lane of the row; groups with ok[k] false are
+// computed but not stored.  hi, lo (TwoPass only) and xs point at the row.
+template <int Q, int NG>
+__device__ __forceinline__ void quant_groups(const float (&v)[NG], const bool (&ok)[NG], int8_t* __restrict__ hi,
+                                             int8_t* __restrict__ lo, float* __restrict__ xs, long g, long step,
+                                             int lane) {
+  float s[NG];
+  int h[NG], l[NG];
+#pragma unroll
+  for (int k = 0; k < NG; ++k) s[k] = act_scale<Q>(warp_absmax(v[k]));
+#pragma unroll
+  for (int k = 0; k < NG; ++k) h[k] = __float2int_rn(__fdiv_rn(v[k], s[k]));  // a tiny group: |v| / 1 rounds to 0
+  if constexpr (Q == 2) {
+#pragma unroll
+    for (int k = 0; k < NG; ++k) {
+      h[k] = sat_i8(h[k]);
+      const float res = __fmaf_rn(-(float)h[k], s[k], v[k]);
+      l[k] = sat_i8(__float2int_rn(__fdiv_rn(res, __fmul_rn(s[k], 0.0078125f))));
+    }
   }
-  if (lane == 0) xs[g] = s;
-  int h = __float2int_rn(__fdiv_rn(v, s));
-  if (Q == 1) {
-    hi[i] = (int8_t)h;
-  } else {
-    h = h > 127 ? 127 : (h < -128 ? -128 : h);
-    const float r = __fmaf_rn(-(float)h, s, v);
-    int l = __float2int_rn(__fdiv_rn(r, __fmul_rn(s, 0.0078125f)));
-    l = l > 127 ? 127 : (l < -128 ? -128 : l);
-    hi[i] = (int8_t)h;
-    lo[i] = (int8_t)l;
+#pragma unroll
+  for (int k = 0; k < NG; ++k) {
+    if (!ok[k]) continue;
+    const long e = 32 * (g + k * step) + lane;
+    hi[e] = (int8_t)h[k];
+    if constexpr (Q == 2) lo[e] = (int8_t)l[k];
+    if (lane == 0) xs[g + k * step] = s[k];
   }
 }
 
-// quant_lane for four groups at once (groups g + k*step, k < 4, stored where
-// ok[k]): the same operations, written phase by phase so that the four
-// groups' independent chains interleave.  Element i of group G is 32G + lane.
+// One group: lane `lane` holds v, element 32 g + lane.
 template <int Q>
-__device__ __forceinline__ void quant_lanes4(const float (&v)[4], const bool (&ok)[4], int8_t* __restrict__ hi,
-                                             int8_t* __restrict__ lo, float* __restrict__ xs, int g, int step,
-                                             int lane) {
-  float a[4], s[4];
-  int h[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) a[k] = warp_absmax(v[k]);
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    s[k] = Q == 1 ? (a[k] > 0.f ? __fdiv_rn(a[k], 127.0f) : 1.0f) : __fdiv_rn(a[k] > 1e-30f ? a[k] : 1e-30f, 127.0f);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) h[k] = __float2int_rn(__fdiv_rn(v[k], s[k]));
-  if (Q == 1) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (ok[k]) {
-        const int G = g + k * step;
-        hi[32 * G + lane] = (int8_t)h[k];
-        if (lane == 0) xs[G] = s[k];
-      }
-  } else {
-    int l[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      h[k] = h[k] > 127 ? 127 : (h[k] < -128 ? -128 : h[k]);
-      const float r = __fmaf_rn(-(float)h[k], s[k], v[k]);
-      l[k] = __float2int_rn(__fdiv_rn(r, __fmul_rn(s[k], 0.0078125f)));
-      l[k] = l[k] > 127 ? 127 : (l[k] < -128 ? -128 : l[k]);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (ok[k]) {
-        const int G = g + k * step;
-        hi[32 * G + lane] = (int8_t)h[k];
-        lo[32 * G + lane] = (int8_t)l[k];
-        if (lane == 0) xs[G] = s[k];
-      }
-  }
+__device__ __forceinline__ void quant_lane(float v, int8_t* __restrict__ hi, int8_t* __restrict__ lo,
+                                           float* __restrict__ xs, long g, int lane) {
+  const float vv[1] = {v};
+  const bool ok[1] = {true};
+  quant_groups<Q, 1>(vv, ok, hi, lo, xs, g, 0, lane);
 }
 
 // ---- RMSNorm arithmetic ("kernels.rs" lk_rmsnorm_row: accumulator f64 under

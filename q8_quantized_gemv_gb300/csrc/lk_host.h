@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "lk.h"
 
 namespace lkh {
@@ -44,6 +46,27 @@ extern long opt_ring_prefill; // warps that issue their first weight stages befo
 extern long opt_l2_ahead_kb;  // ring/tensor-core kernels: KB per block of later stages requested into L2 at start
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// Device address of a file-scope __device__ variable on the current device,
+// looked up (cudaGetSymbolAddress, with that device current) the first time
+// and kept per device.  `symbol` is the variable's host-side stand-in, which
+// is not a device address.  Threads that race on a first lookup each store
+// the same address (atomics, no data race).  The cached address belongs to
+// the device's current context: it is stale after cudaDeviceReset().
+constexpr int kMaxDevices = 64;
+template <typename T>
+inline T* device_symbol(std::atomic<T*> (&cache)[kMaxDevices], const void* symbol) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  T* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&q, symbol) != cudaSuccess || !q) return nullptr;
+    p = (T*)q;
+    cache[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
 
 inline lk_status launch_status() {
   cudaError_t e = cudaGetLastError();

@@ -65,35 +65,17 @@ ring_fn pick(int mode, int M, bool split, bool fuse) {
 // Device address of the error word on the current device, looked up once
 // per device.
 int* lkh::error_word_ptr() {
-  static int* ptr[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, lk_error_word) != cudaSuccess) return nullptr;
-    ptr[dev] = (int*)p;
-  }
-  return ptr[dev];
+  static std::atomic<int*> cache[kMaxDevices];
+  return device_symbol(cache, (const void*)&lk_error_word);
 }
 
-static int trace_seq = 0;
-void lkh::trace_reset() { trace_seq = 0; }
-int lkh::trace_next_slot() {
-  const int s = trace_seq;
-  trace_seq = (trace_seq + 1) % (lkring::LK_TRACE_MAX / lkring::TREC);
-  return s;
-}
+static std::atomic<int> trace_seq{0};
+void lkh::trace_reset() { trace_seq.store(0); }
+int lkh::trace_next_slot() { return trace_seq.fetch_add(1) % (lkring::LK_TRACE_MAX / lkring::TREC); }
 
 unsigned long long* lkh::trace_ptr() {
-  static unsigned long long* ptr[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, lk_trace_buf) != cudaSuccess) return nullptr;
-    ptr[dev] = (unsigned long long*)p;
-  }
-  return ptr[dev];
+  static std::atomic<unsigned long long*> cache[kMaxDevices];
+  return device_symbol(cache, (const void*)lk_trace_buf);
 }
 
 namespace lkring {

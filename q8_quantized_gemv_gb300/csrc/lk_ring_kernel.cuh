@@ -208,8 +208,9 @@ __device__ __forceinline__ float ld_keep_cg(const float* p) {
 }
 __device__ __forceinline__ void compiler_fence() { asm volatile("" ::: "memory"); }
 
-// store_act for the four groups g, g + step, g + 2 step, g + 3 step (those
-// with ok set), their quantizer steps in lockstep.
+// The activation of four groups g, g + step, g + 2 step, g + 3 step of row t
+// (those with ok set) into the area: f32 values under Dequant, else their
+// quantized words and scales.
 template <int Q, int M>
 __device__ __forceinline__ void store_act4(unsigned char* act, unsigned L, int t, int g, int step, int lane,
                                            const float (&v)[4], const bool (&ok)[4]) {
@@ -221,20 +222,7 @@ __device__ __forceinline__ void store_act4(unsigned char* act, unsigned L, int t
     int8_t* XQ = (int8_t*)act + (size_t)t * L;
     int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
     float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
-    quant_lanes4<Q>(v, ok, XQ, XL, XS, g, step, lane);
-  }
-}
-
-template <int Q, int M>
-__device__ __forceinline__ void store_act(unsigned char* act, unsigned L, int t, int g, int lane, float v) {
-  const int i = 32 * g + lane;
-  if constexpr (Q == 0) {
-    ((float*)act)[(size_t)t * L + i] = v;
-  } else {
-    int8_t* XQ = (int8_t*)act + (size_t)t * L;
-    int8_t* XL = (int8_t*)act + (size_t)M * L + (size_t)t * L;
-    float* XS = (float*)(act + (size_t)M * L * (Q == 2 ? 2 : 1)) + (size_t)t * (L >> 5);
-    quant_lane<Q>(v, XQ, XL, XS, i, g, lane);
+    quant_groups<Q, 4>(v, ok, XQ, XL, XS, g, step, lane);
   }
 }
 
