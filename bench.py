@@ -635,13 +635,13 @@ def roofline_chain(stack, stream, a, torch):
             {"chain": {"us": us, "GB/s": achieved, "launches": steps}})
 
 
-def profile_traffic(key, kind):
+def profile_traffic(key, kind, path=None):
     """A DRAM-traffic figure (bytes per launch) from profiles/traffic.txt (one
     ncu capture), if it was taken on the current sources of that kernel
     family (else None).  Lines: "<key>: <bytes> <family>=<sha256>"."""
     try:
         from q8_quantized_gemv_gb300 import build
-        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
+        with open(path or os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             for line in f:
                 if line.startswith("#") or ":" not in line:
                     continue

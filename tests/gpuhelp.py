@@ -91,3 +91,71 @@ def ring_takes(N, K, mode, M):
         return lk.lk_gemv_kernel_for(N, K, mode, M, 0) == 2
     finally:
         lk.lk_set_option("gemv_path", prev)
+
+
+# ---- whole decode tokens ------------------------------------------------------------
+
+def run_token_capture(st):
+    """One token of a DecodeStack through its per-launch path, recording after
+    every GEMV launch (synchronized) host copies of what it wrote: a list with
+    one dict per layer (q, k, v, o, gu, h) and the final logits and argmax."""
+    layers, final = [], {}
+
+    def hook(name, launch):
+        r = launch()
+        torch.cuda.synchronize()
+        if name in ("qkv", "q"):
+            layers.append({})
+        if name == "qkv":
+            for n in ("q", "k", "v"):
+                layers[-1][n] = host(st.out[n]).copy()
+        elif name in ("q", "k", "v", "o", "gu"):
+            layers[-1][name] = host(st.out[name]).copy()
+        elif name == "down":
+            layers[-1]["h"] = host(st.h).copy()
+        elif name == "lm":
+            final["logits"] = host(st.logits).copy()
+        return r
+
+    idx = st.run_token(hook=hook)
+    torch.cuda.synchronize()
+    final["idx"] = host(idx).copy()
+    assert len(layers) == st.L and all(len(r) == 6 for r in layers)
+    return layers, final
+
+
+def _host_w(pair):
+    return host(pair[0]), host(pair[1]).view(np.uint16)
+
+
+def check_token(st, layers, final):
+    """Every GEMV of a captured token against the oracle on that GEMV's own
+    input (the GPU's previous outputs, copied back): RMSNorm -> quantize ->
+    GEMV in the oracle, then bit-exact (Int8Act, TwoPass) or within
+    TOL * sum|W x| per row (Dequant).  Bit-exact steps chained from the same
+    first input make the GPU token the oracle's own token.  The argmax must be
+    the oracle's first index of the maximum of the GPU's logits (and, for the
+    quantized modes, the logits are the oracle's bit for bit)."""
+    m = st.mode
+    eps = st.eps
+
+    def step(wpair, x, gain, y_gpu, what):
+        a = oracle.rmsnorm(x, host(gain), m, eps) if gain is not None else x
+        wq, ws = wpair
+        y_or = oracle.gemv(wq, ws, m, **oracle_acts(a, m))
+        try:
+            assert_gemv_close(y_gpu, y_or, wq, ws, a, m)
+        except AssertionError as e:
+            raise AssertionError(f"{what}: {e}") from None
+
+    x = host(st.x_buf)
+    for l, w in enumerate(st.layers):
+        rec = layers[l]
+        for n in ("q", "k", "v"):
+            step(_host_w(w[n]), x, w["g_attn"], rec[n], f"layer {l} {n}")
+        step(_host_w(w["o"]), host(w["o_in"]), None, rec["o"], f"layer {l} o")
+        step(_host_w(w["gu"]), rec["o"], w["g_mlp"], rec["gu"], f"layer {l} gate/up")
+        step(_host_w(w["down"]), host(w["d_in"]), None, rec["h"], f"layer {l} down")
+        x = rec["h"]
+    step(_host_w(st.lm), x, st.g_final, final["logits"], "lm-head")
+    assert final["idx"].tolist() == [oracle.argmax(final["logits"][t]) for t in range(st.B)]

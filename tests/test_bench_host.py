@@ -40,15 +40,32 @@ def test_clock_summary_without_samples():
     assert s == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
 
 
-def test_traffic_lookup_follows_the_kernel_sources(monkeypatch):
+def test_traffic_lookup_follows_the_kernel_sources(monkeypatch, tmp_path):
     from q8_quantized_gemv_gb300 import build
     key = "gemv_ring_gateup_24576x4096_int8act_b1"
-    got = bench.profile_traffic(key, "ring")
-    assert got is not None and 1.0e8 < got < 1.2e8  # ~ the 107 MB of weights it streams
-    assert bench.profile_traffic("no_such_capture", "ring") is None
-    assert bench.profile_traffic(key, "mma") is None  # another family's key
+    f = tmp_path / "traffic.txt"
+    f.write_text("# comment\n"
+                 f"{key}: 109848576 ring={build.sources_digest('ring')}\n"
+                 f"other_key: 5 mma={build.sources_digest('mma')}\n")
+    got = bench.profile_traffic(key, "ring", str(f))
+    assert got == 109848576.0
+    assert bench.profile_traffic("no_such_capture", "ring", str(f)) is None
+    assert bench.profile_traffic(key, "mma", str(f)) is None  # another family's key
     monkeypatch.setattr(build, "sources_digest", lambda kind=None: "0" * 64)
-    assert bench.profile_traffic(key, "ring") is None  # sources changed since the capture
+    assert bench.profile_traffic(key, "ring", str(f)) is None  # sources changed since the capture
+
+
+def test_committed_traffic_file_parses():
+    """profiles/traffic.txt: every line a key, a byte count and a family digest."""
+    import os
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.txt")) as fh:
+        for line in fh:
+            if line.startswith("#") or not line.strip():
+                continue
+            k, v = line.split(":", 1)
+            val, tag = v.split()
+            fam, sha = tag.split("=")
+            assert float(val) > 0 and fam in ("ring", "mma", "chain") and len(sha) == 64
 
 
 def test_peaks_and_defaults():
