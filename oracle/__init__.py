@@ -9,8 +9,10 @@ lives in ``oracle.c`` (plain C, single-threaded, built with
 Sources, by page:
   * "kernels.rs" (logicaffeine_compile codegen_cuda lane kernel library):
     the numerics modes, the activation quantizer, the quantized block step and
-    its four-partial order, RMSNorm and its reduction tree, the balanced split.
-  * the QWEN38_EXTRA_KERNELS constant: "SPLIT-K FOR THE NARROW PROJECTIONS".
+    its four-partial order, RMSNorm and its reduction tree (with the residual
+    add), the gated projection pair (SwiGLU), the balanced split.
+  * the QWEN38_EXTRA_KERNELS constant: "SPLIT-K FOR THE NARROW PROJECTIONS",
+    the fused add + norm + quantize kernels and the SwiGLU + requantize one.
   * model-as-a-kernel "megakernel.cu": the argmax's first index of equal maxima.
 """
 from __future__ import annotations
@@ -65,6 +67,9 @@ def _load():
     lib.oracle_splitk_bound.restype = i32
     lib.oracle_gemv_splitk_rows.argtypes = [P, P, i32, i32, P, P, P, P, i32, i64, i64, P, P, P]
     lib.oracle_absdot_rows.argtypes = [P, P, i32, P, i64, i64, P]
+    lib.oracle_add_rmsnorm_row.argtypes = [P, P, P, i32, f32, i32, P, P]
+    lib.oracle_add_rmsnorm_row.restype = i32
+    lib.oracle_swiglu.argtypes = [P, P, i64, P]
     lib.oracle_argmax.argtypes = [P, i64]
     lib.oracle_argmax.restype = i64
     _lib = lib
@@ -129,6 +134,44 @@ def rmsnorm(x, g, mode: int, eps: float = 1e-6) -> np.ndarray:
     for t in range(M):
         lib.oracle_rmsnorm_row(_p(x[t]), _p(g), K, eps, mode, _p(y[t]))
     return y
+
+
+def add_rmsnorm(x, r, g, mode: int, eps: float = 1e-6):
+    """Residual add, then RMSNorm: s = x + r (f32), y = RMSNorm(s) * g.
+    x, r: [M, K] f32.  Returns (s, y)."""
+    lib = _load()
+    x = _c(np.atleast_2d(x), np.float32)
+    r = _c(np.atleast_2d(r), np.float32)
+    g = _c(g, np.float32)
+    M, K = x.shape
+    assert r.shape == (M, K)
+    s = np.zeros((M, K), np.float32)
+    y = np.zeros((M, K), np.float32)
+    for t in range(M):
+        assert lib.oracle_add_rmsnorm_row(_p(x[t]), _p(r[t]), _p(g), K, eps, mode, _p(s[t]), _p(y[t])) == 0
+    return s, y
+
+
+def swiglu(g, u) -> np.ndarray:
+    """h = silu(g) * u = g / (1 + e^-g) * u, elementwise (f64, one rounding)."""
+    lib = _load()
+    g = _c(g, np.float32)
+    u = _c(u, np.float32)
+    assert g.shape == u.shape
+    h = np.zeros(g.shape, np.float32)
+    lib.oracle_swiglu(_p(g), _p(u), g.size, _p(h))
+    return h
+
+
+def glu(wg, wsg, wu, wsu, mode: int, x=None, hi=None, lo=None, s=None):
+    """The gated projection pair of a decoder's MLP: g = Wg x and u = Wu x by
+    gemv(), then h = swiglu(g, u), and h quantized by quantize() for the
+    quantized modes.  Returns (g, u, h, (hq, hl, hs) or None)."""
+    acts = dict(x=x, hi=hi, lo=lo, s=s)
+    g = gemv(wg, wsg, mode, **acts)
+    u = gemv(wu, wsu, mode, **acts)
+    h = swiglu(g, u)
+    return g, u, h, (quantize(h, mode) if mode != DEQUANT else None)
 
 
 def block_dots(wq, hi, lo=None):

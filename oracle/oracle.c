@@ -26,6 +26,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define OR_DEQUANT 0
@@ -204,6 +205,45 @@ void oracle_rmsnorm_row(const float* v, const float* g, int K, float eps, int mo
     } else {
         float den = sqrtf(oracle_sumsq_f32(v, K) / (float)K + eps);
         for (int i = 0; i < K; ++i) y[i] = v[i] / den * g[i];
+    }
+}
+
+/* ---- residual add + RMSNorm ------------------------------------------------
+ * [lane] RMSNORM lk_rmsnorm_row with ADD (and SUM): the residual r is added to
+ * the row first, v_i = x_i + r_i as one f32 addition, the sum v is the
+ * residual stream the next block reads (written to s when s != NULL), and v is
+ * what the norm sees; [extra] gk_add_rmsnorm_q8_hl is the same step (x += y,
+ * then the norm and the quantizer).  The norm is oracle_rmsnorm_row's, on v.
+ * Returns 0, or -1 if the scratch row cannot be allocated. */
+int oracle_add_rmsnorm_row(const float* x, const float* r, const float* g, int K, float eps, int mode,
+                           float* s, float* y)
+{
+    if (K <= 0) return 0;
+    float* v = (float*)malloc(sizeof(float) * (size_t)K);
+    if (!v) return -1;
+    for (int i = 0; i < K; ++i) {
+        v[i] = x[i] + r[i];
+        if (s) s[i] = v[i];
+    }
+    oracle_rmsnorm_row(v, g, K, eps, mode, y);
+    free(v);
+    return 0;
+}
+
+/* ---- SwiGLU ------------------------------------------------------------------
+ * [lane] GLU (lk_gemv_glu with ACT -1, lk_swiglu) and [extra] gk_silu_had_q8:
+ * the gated activation of a gate value g and an up value u is
+ *   h = silu(g) * u = g / (1 + e^-g) * u.
+ * The pages evaluate it in f32 with the GPU's expf; the oracle takes the
+ * definition in f64 from the f32 inputs and rounds h to f32 once (for
+ * g < -709 the f64 e^-g overflows and h is a signed zero, as the f32 form
+ * gives below g = -88.7).  h feeds the activation quantizer of the down
+ * projection (oracle_quantize_row). */
+void oracle_swiglu(const float* g, const float* u, long n, float* h)
+{
+    for (long i = 0; i < n; ++i) {
+        double gv = (double)g[i];
+        h[i] = (float)(gv / (1.0 + exp(-gv)) * (double)u[i]);
     }
 }
 

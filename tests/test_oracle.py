@@ -361,3 +361,94 @@ def test_argmax_first_of_equal_maxima():
     assert oracle.argmax(v) == 1
     assert oracle.argmax(np.zeros(100, np.float32)) == 0
     assert oracle.argmax(np.full(5, -np.inf, np.float32)) == 0
+
+
+# ---- residual add + RMSNorm ------------------------------------------------
+
+@pytest.mark.parametrize("mode", [DQ, I8])
+def test_add_rmsnorm_sum_is_the_f32_sum(mode):
+    r = np.random.default_rng(21)
+    x = r.standard_normal((2, 1024)).astype(np.float32)
+    res = (r.standard_normal((2, 1024)) * 3).astype(np.float32)
+    g = synth.norm_gain(1024, 22)
+    s, y = oracle.add_rmsnorm(x, res, g, mode)
+    assert np.array_equal(s.view(np.uint32), (x + res).view(np.uint32))  # numpy's IEEE f32 add
+    # the norm sees the sum: within a few ulp of the long-double definition
+    v = s.astype(np.longdouble)
+    den = np.sqrt((v * v).sum(axis=1, keepdims=True) / 1024 + np.longdouble(np.float32(1e-6)))
+    want = v / den * g.astype(np.longdouble)
+    assert np.all(np.abs(y - want) <= 4 * np.spacing(np.abs(want).astype(np.float32)))
+
+
+@pytest.mark.parametrize("mode", [DQ, I8])
+@pytest.mark.parametrize("K", [32, 1024, 4096])
+def test_add_rmsnorm_constant_sum_closed_form(mode, K):
+    # x + r = c exactly in every element (x = c - r with few significant bits):
+    # y_i = g_i c / sqrt(c^2 + eps), which a norm of x alone (or of r) misses
+    r = np.random.default_rng(K)
+    res = r.integers(-64, 64, size=(1, K)).astype(np.float32) / np.float32(8)
+    c = np.float32(0.375)
+    x = (c - res).astype(np.float32)
+    assert np.all(x + res == c)
+    g = synth.norm_gain(K, 23)
+    s, y = oracle.add_rmsnorm(x, res, g, mode)
+    assert np.all(s == c)
+    eps = np.float32(1e-6)
+    want = g.astype(np.float64) * float(c) / np.sqrt(float(c) ** 2 + float(eps))
+    assert np.allclose(y[0], want, rtol=4 * U32, atol=0)
+
+
+# ---- SwiGLU ---------------------------------------------------------------------
+
+def test_swiglu_closed_forms():
+    u = np.array([1.0, -2.0, 0.5, 3.0, 96.0, -0.25], np.float32)
+    # silu(0) = 0; for g tiny the slope is 1/2: h = g u / 2 exactly
+    assert not oracle.swiglu(np.zeros_like(u), u).any()
+    t = np.float32(2.0 ** -30)
+    assert np.array_equal(oracle.swiglu(np.full_like(u, t), u), (t * u / 2).astype(np.float32))
+    # sigma(50) = 1 - 2e-22: h = 50 u (representable) exactly; sigma(-50) ~ 2e-22
+    assert np.array_equal(oracle.swiglu(np.full_like(u, 50.0), u), (50 * u).astype(np.float32))
+    h = oracle.swiglu(np.full_like(u, -50.0), u)
+    assert np.allclose(h, -50.0 * np.exp(-50.0) * u.astype(np.float64), rtol=1e-6)
+    # far beyond the f64 range of e^-g: a signed zero for g -> -inf, g u for g -> +inf
+    assert not oracle.swiglu(np.full_like(u, -1000.0), u).any()
+    assert np.array_equal(oracle.swiglu(np.full_like(u, 1000.0), u), (1000 * u).astype(np.float32))
+
+
+def test_swiglu_identities():
+    r = np.random.default_rng(31)
+    g = (r.standard_normal(4096) * 4).astype(np.float32)
+    u = r.standard_normal(4096).astype(np.float32)
+    h = oracle.swiglu(g, u).astype(np.float64)
+    # silu(g) - silu(-g) = g (sigma(g) + sigma(-g) = 1): catches e^g for e^-g,
+    # a dropped sign, or the gate and up operands exchanged
+    d = h - oracle.swiglu(-g, u).astype(np.float64)
+    gu = g.astype(np.float64) * u
+    assert np.all(np.abs(d - gu) <= 2 * np.spacing(np.abs(gu).astype(np.float32)) + 1e-38)
+    # linear in u: doubling u doubles h exactly
+    assert np.array_equal(oracle.swiglu(g, 2 * u), 2 * oracle.swiglu(g, u))
+    # |silu(g)| <= |g| and silu(g) >= min over g (about -0.2785)
+    s1 = oracle.swiglu(g, np.ones_like(g)).astype(np.float64)
+    assert np.all(np.abs(s1) <= np.abs(g) + 1e-30) and s1.min() > -0.2785
+
+
+def test_glu_composition():
+    # gate and up are two GEMVs of one activation; h their SwiGLU, then quantized
+    wg, wsg = synth.q8_matrix(64, 256, 41)
+    wu, wsu = synth.q8_matrix(64, 256, 42)
+    x = synth.activation(2, 256, 43, outliers=True)
+    for mode in (DQ, I8, TP):
+        if mode == DQ:
+            acts = dict(x=x)
+        else:
+            hi, lo, s = oracle.quantize(x, mode)
+            acts = dict(hi=hi, lo=lo, s=s)
+        g, u, h, q = oracle.glu(wg, wsg, wu, wsu, mode, **acts)
+        assert np.array_equal(g, oracle.gemv(wg, wsg, mode, **acts))
+        assert np.array_equal(u, oracle.gemv(wu, wsu, mode, **acts))
+        assert np.array_equal(h, oracle.swiglu(g, u))
+        if mode == DQ:
+            assert q is None
+        else:
+            for a, b in zip(q, oracle.quantize(h, mode)):
+                assert np.array_equal(a, b)
