@@ -3,8 +3,9 @@
 TEST INFRASTRUCTURE ONLY.  The tests, the package smoke check and the
 benchmark's CPU-baseline leg call it; the library (``q8_quantized_gemv_gb300``)
 never imports it, and it imports nothing from the library.  The arithmetic
-lives in ``oracle.c`` (plain C, single-threaded, built with
-``-ffp-contract=off``); this module builds it and wraps it for numpy arrays.
+lives in ``oracle.c`` (plain C built with ``-ffp-contract=off``, one thread
+by default; its GEMV row loops can be spread over host threads without
+changing any bit); this module builds it and wraps it for numpy arrays.
 
 Sources, by page:
   * "kernels.rs" (logicaffeine_compile codegen_cuda lane kernel library):
@@ -37,7 +38,7 @@ def build(force: bool = False) -> str:
     if force or stale:
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.run(
-            ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+            ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
             check=True,
         )
         os.replace(tmp, _LIB)
@@ -70,6 +71,8 @@ def _load():
     lib.oracle_add_rmsnorm_row.argtypes = [P, P, P, i32, f32, i32, P, P]
     lib.oracle_add_rmsnorm_row.restype = i32
     lib.oracle_swiglu.argtypes = [P, P, i64, P]
+    lib.oracle_set_threads.argtypes = [i32]
+    lib.oracle_set_threads.restype = i32
     lib.oracle_argmax.argtypes = [P, i64]
     lib.oracle_argmax.restype = i64
     _lib = lib
@@ -83,6 +86,13 @@ def _c(a, dtype):
 
 def _p(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def set_threads(n: int) -> int:
+    """Host threads of the GEMV row loops (1, the default, is the plain
+    single-threaded oracle; any count gives the same bits).  Returns the
+    count in effect."""
+    return _load().oracle_set_threads(int(n))
 
 
 def half_to_float(h) -> np.ndarray:

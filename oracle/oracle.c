@@ -5,10 +5,13 @@
  * the library never does.  It shares no code, header or table with the CUDA
  * path.
  *
- * Build: gcc -O2 -ffp-contract=off -fPIC -shared oracle.c -lm
+ * Build: gcc -O2 -ffp-contract=off -fopenmp -fPIC -shared oracle.c -lm
  * (-ffp-contract=off: every fused multiply-add below is written out with
  * fmaf/fma; every other product and sum is rounded on its own, in IEEE
- * single or double precision as stated.)
+ * single or double precision as stated.)  The GEMV row loops may run on
+ * several host threads (oracle_set_threads; 1 by default): each output row
+ * is computed by one thread exactly as written, so any thread count gives
+ * the same bits.
  *
  * Sources (three web pages on the subject):
  *   [lane]   "kernels.rs" of logicaffeine_compile::codegen_cuda::lane: the
@@ -28,6 +31,23 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Host threads of the GEMV row loops (1 = the plain single-threaded oracle). */
+static int or_threads = 1;
+int oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    or_threads = n < 1 ? 1 : n;
+#else
+    (void)n;
+    or_threads = 1;
+#endif
+    return or_threads;
+}
 
 #define OR_DEQUANT 0
 #define OR_INT8ACT 1
@@ -331,6 +351,7 @@ void oracle_gemv_rows(const int8_t* wq, const uint16_t* ws, int K, int mode, con
                       const int8_t* hi, const int8_t* lo, const float* s, long r0, long r1,
                       float* y)
 {
+#pragma omp parallel for schedule(static) num_threads(or_threads) if (or_threads > 1)
     for (long o = r0; o < r1; ++o) {
         if (mode == OR_DEQUANT)
             y[o - r0] = (float)deq_row_range(wq, ws, K, o, x, 0, K);
@@ -365,6 +386,7 @@ void oracle_gemv_splitk_rows(const int8_t* wq, const uint16_t* ws, int K, int mo
 {
     int nb = K / 32;
     long n = r1 - r0;
+#pragma omp parallel for schedule(static) num_threads(or_threads) if (or_threads > 1)
     for (long o = r0; o < r1; ++o) {
         if (mode == OR_DEQUANT) {
             double acc = 0.0;
@@ -394,6 +416,7 @@ void oracle_absdot_rows(const int8_t* wq, const uint16_t* ws, int K, const float
                         long r1, double* out)
 {
     int nb = K / 32;
+#pragma omp parallel for schedule(static) num_threads(or_threads) if (or_threads > 1)
     for (long o = r0; o < r1; ++o) {
         double acc = 0.0;
         for (int k = 0; k < K; ++k) {

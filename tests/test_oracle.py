@@ -452,3 +452,25 @@ def test_glu_composition():
         else:
             for a, b in zip(q, oracle.quantize(h, mode)):
                 assert np.array_equal(a, b)
+
+
+def test_threads_give_the_same_bits():
+    """The all-cores oracle (rows spread over host threads) is bit-identical
+    to the single-threaded one, in every mode and in split-K."""
+    wq, ws = synth.q8_matrix(301, 512, 51)
+    x = synth.activation(2, 512, 52, outliers=True)
+    outs = {}
+    for n in (1, 4):
+        assert oracle.set_threads(n) == n
+        try:
+            r = []
+            for mode in (DQ, I8, TP):
+                a = dict(x=x) if mode == DQ else dict(zip(("hi", "lo", "s"), oracle.quantize(x, mode)))
+                r.append(oracle.gemv(wq, ws, mode, **a))
+                r.extend(oracle.gemv_splitk(wq, ws, mode, 3, **a))
+            r.append(oracle.absdot(wq, ws, x))
+        finally:
+            oracle.set_threads(1)
+        outs[n] = r
+    for a, b in zip(outs[1], outs[4]):
+        assert a.dtype == b.dtype and np.array_equal(a.view(np.uint8), b.view(np.uint8))
