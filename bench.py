@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=36)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration GEMV table and the other sequence forms")
     ap.add_argument("--workload", default="sequence", choices=["sequence", "gemv"],
                     help="sequence: the per-token decode projections (default); gemv: one "
                          "GEMV shape, launched back to back over rotated weight copies")
@@ -69,6 +71,9 @@ def parse():
     ap.add_argument("--fuse", default="", help="sequence: comma-separated projections (q,k,v,o,gu,down,lm) "
                                                "that compute their own norm/quantize prologue")
     ap.add_argument("--prefill", action="append", default=[], help=argparse.SUPPRESS)  # name=warps
+    ap.add_argument("--decoder", action="store_true",
+                    help="sequence: the decoder-layer dataflow (residual add + norm + quantize launches, the gate/up "
+                         "pair with its SwiGLU epilogue feeding down) instead of the projections alone")
     ap.add_argument("--no-pdl", action="store_true",
                     help="no programmatic dependent launches between the fused GEMVs")
     ap.add_argument("--fused", action="store_true", help="gemv workload: RMSNorm->quantize->GEMV in one launch")
@@ -90,9 +95,11 @@ def measured_peaks():
 
 
 def workload_name(a):
+    flow = ("decoder layers: residual add + RMSNorm + quantize, SwiGLU + quantize in the gate/up launch"
+            if getattr(a, "decoder", False) else "projections alone")
     return (f"decode projections: {a.layers} layers, hidden 4096, q 4096x4096, k/v 1024x4096, "
-            f"o 4096x4096, gate/up 24576x4096, down 4096x12288, lm-head 151936x4096 + argmax, "
-            f"batch {a.batch}, {a.mode}")
+            f"o 4096x4096, gate/up 24576x4096 (a 2 x 12288x4096 pair), down 4096x12288, lm-head 151936x4096 + "
+            f"argmax, batch {a.batch}, {a.mode}; {flow}")
 
 
 # ---- clocks ------------------------------------------------------------------------
@@ -151,7 +158,10 @@ class Clocks:
 # ---- CPU oracle sample ---------------------------------------------------------------
 
 def oracle_layer(oracle, w, mode, x, eps=1e-6):
-    """One layer of the sequence on the CPU oracle; returns (y_down, bytes)."""
+    """One layer of the sequence on the CPU oracle; returns (the next layer's
+    input, weight bytes).  With gate/up as a pair ("gate", "up": the decoder
+    dataflow) x is the residual stream entering the layer; otherwise the
+    projections-alone dataflow (down's input a fixed vector)."""
     def acts(v):
         if mode == oracle.DEQUANT:
             return dict(x=v)
@@ -165,6 +175,13 @@ def oracle_layer(oracle, w, mode, x, eps=1e-6):
         nbytes += w[n][0].size * 17 // 16
     o = oracle.gemv(w["o"][0], w["o"][1], mode, **acts(w["o_in"]))
     nbytes += w["o"][0].size * 17 // 16
+    if "gate" in w:
+        h_mid, y = oracle.add_rmsnorm(o, x, w["g_mlp"], mode, eps)
+        _, _, hg, _ = oracle.glu(w["gate"][0], w["gate"][1], w["up"][0], w["up"][1], mode, **acts(y))
+        nbytes += 2 * w["gate"][0].size * 17 // 16
+        d = oracle.gemv(w["down"][0], w["down"][1], mode, **acts(hg))
+        nbytes += w["down"][0].size * 17 // 16
+        return (h_mid + d).astype("float32"), nbytes
     a = acts(oracle.rmsnorm(o, w["g_mlp"], mode, eps))
     oracle.gemv(w["gu"][0], w["gu"][1], mode, **a)
     nbytes += w["gu"][0].size * 17 // 16
@@ -182,13 +199,14 @@ def host_layer(stack_or_none, l, B, mode_seed=0):
     if stack_or_none is not None:
         w = stack_or_none.layers[l]
         out = {}
-        for n in ("q", "k", "v", "o", "gu", "down"):
-            out[n] = (w[n][0].cpu().numpy(), w[n][1].cpu().numpy().view(np.uint16))
+        for n in ("q", "k", "v", "o", "gu", "gate", "up", "down"):
+            if n in w:
+                out[n] = (w[n][0].cpu().numpy(), w[n][1].cpu().numpy().view(np.uint16))
         for n in ("g_attn", "g_mlp", "o_in", "d_in"):
             out[n] = w[n].cpu().numpy()
         return out
     shapes = {"q": (4096, 4096), "k": (1024, 4096), "v": (1024, 4096), "o": (4096, 4096),
-              "gu": (24576, 4096), "down": (4096, 12288)}
+              "gate": (12288, 4096), "up": (12288, 4096), "down": (4096, 12288)}
     s = synth.SEED_BASE + 4 + 1000 * l + mode_seed
     out = {n: synth.q8_matrix(N, K, s + i) for i, (n, (N, K)) in enumerate(shapes.items())}
     out["g_attn"] = synth.norm_gain(4096, s + 10)
@@ -214,26 +232,46 @@ def host_info():
     return info
 
 
-def cpu_baseline(stack, a, budget_s):
-    import oracle
-
-    mode = {"dequant": 0, "int8act": 1, "twopass": 2}[a.mode]
+def _time_oracle_layers(oracle, stack, a, mode, budget_s, first_layer=0):
+    """Oracle layers of the sequence, in order from `first_layer`, until
+    `budget_s` seconds of oracle time; returns (bytes, seconds, layers)."""
     import numpy as np
     x = stack.x0.cpu().numpy() if stack is not None else np.ones((a.batch, 4096), np.float32)
-    tot_b, tot_t, layers = 0, 0.0, 0
-    for l in range(a.layers):
+    tot_b, tot_t, n = 0, 0.0, 0
+    for l in range(first_layer, a.layers):
         w = host_layer(stack, l, a.batch)
         t0 = time.perf_counter()
         x, nb = oracle_layer(oracle, w, mode, x)
         tot_t += time.perf_counter() - t0
         tot_b += nb
-        layers += 1
+        n += 1
         if tot_t >= budget_s:
             break
-    return {"value": tot_b / tot_t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"layers 0..{layers - 1} of the sequence (full matrices, norm + quantize + "
-                      f"6 GEMVs each, batch {a.batch}, {a.mode}), single-threaded C oracle",
-            "seconds": tot_t, "host": host_info()}
+    return tot_b, tot_t, n
+
+
+def cpu_baseline(stack, a, budget_s):
+    """The oracle on the host cores: all of them (its GEMV row loops over
+    every logical CPU, bit-identical to one thread) for the reported value,
+    and one thread beside it, each on a bounded sample of the sequence."""
+    import oracle
+
+    mode = {"dequant": 0, "int8act": 1, "twopass": 2}[a.mode]
+    cores = os.cpu_count() or 1
+    oracle.set_threads(1)
+    b1, t1, n1 = _time_oracle_layers(oracle, stack, a, mode, budget_s / 3)
+    used = oracle.set_threads(cores)
+    try:
+        bn, tn, nn = _time_oracle_layers(oracle, stack, a, mode, 2 * budget_s / 3)
+    finally:
+        oracle.set_threads(1)
+    what = f"(full matrices, norm + quantize + 6 GEMVs each, batch {a.batch}, {a.mode}), C oracle"
+    return {"value": bn / tn / 1e9, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"layers 0..{nn - 1} of the sequence {what}, GEMV rows over {used} threads",
+            "seconds": tn, "host": host_info(),
+            "single_thread": {"value": b1 / t1 / 1e9, "unit": UNIT, "cores": 1,
+                              "sample": f"layers 0..{n1 - 1} of the sequence {what}, one thread",
+                              "seconds": t1}}
 
 
 # ---- reference arm: the CPU oracle -----------------------------------------------------
@@ -245,6 +283,7 @@ def run_reference(a, rank):
     oracle.build()
     mode = {"dequant": 0, "int8act": 1, "twopass": 2}[a.mode]
     import numpy as np
+    cores = oracle.set_threads(os.cpu_count() or 1)
     layers = [host_layer(None, l, a.batch) for l in range(2)]
     x0 = np.ones((a.batch, 4096), np.float32)
 
@@ -269,9 +308,9 @@ def run_reference(a, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": _dtype(a.mode),
         "data": "synthetic", "config": {"workload": workload_name(a),
                                         "sample": "2 of the layers per step, on the host"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "each step: layers 0-1 of the sequence (full matrices) in the "
-                                   "single-threaded C oracle", "host": host_info()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: layers 0-1 of the sequence (full matrices) in the C oracle, "
+                                   f"GEMV rows over {cores} threads", "host": host_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -305,7 +344,7 @@ def run_ours(a, rank, world):
         fused = [n for n in a.fuse.split(",") if n]
     prefill = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in a.prefill}
     stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=fused, chain=a.chain and fused,
-                        prefill=prefill)
+                        prefill=prefill, glu=a.decoder)
     tok_bytes = stack.weight_bytes()
     stream = torch.cuda.Stream(device=dev)
 
@@ -401,6 +440,7 @@ def run_ours(a, rank, world):
                                    for k, v in stack.kernel.items()},
                    "chain": stack.chain is not None,
                    "ring_prefill": stack.prefill or "half of the warps",
+                   "dataflow": "decoder (glu)" if stack.glu else "projections alone",
                    "pdl": not a.no_pdl, "options": a.opt},
         "us_per_token": ms_max * 1e3,
         "pct_of_nominal_8TBs": value / world / NOMINAL_HBM_GBS,
@@ -412,6 +452,17 @@ def run_ours(a, rank, world):
     }
     if rank == 0 and not a.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(stack, a, a.cpu_seconds)
+    if rank == 0 and not a.no_configs:
+        # after every timed region of the headline: the other configurations
+        del graph, graph_e2e
+        lk.lk_set_option("pdl", 1)
+        forms = [(1, "int8act"), (1, "twopass"), (1, "dequant"), (8, "int8act"), (8, "twopass"),
+                 (16, "int8act"), (64, "int8act")]
+        forms = [(b, m, False) for b, m in forms if (b, m) != (a.batch, a.mode) or a.decoder] + \
+                [(b, m, True) for b, m in ((1, "int8act"), (1, "twopass"), (8, "int8act"))
+                 if (b, m) != (a.batch, a.mode) or not a.decoder]
+        out["sequences"] = measure_sequences(a, forms, dev)
+        out["configs"] = measure_configs(a)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist is not None:
@@ -433,7 +484,7 @@ def _timing_event(torch, external):
     return torch.cuda.Event(enable_timing=True)
 
 
-def run_gemv(a, rank, world, quiet=False):
+def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
     """One GEMV shape: per-launch CUDA-event durations over weight copies
     rotated so that every launch streams from HBM (copies x bytes >= 4 x L2)."""
     import torch
@@ -509,8 +560,9 @@ def run_gemv(a, rank, world, quiet=False):
             graph.replay()
     torch.cuda.synchronize()
     clocks = Clocks(local)
-    clocks.start()
-    time.sleep(0.3)
+    if sample_clocks:
+        clocks.start()
+        time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     tw0 = time.time()
     with torch.cuda.stream(stream):
@@ -550,47 +602,107 @@ def run_gemv(a, rank, world, quiet=False):
     return out
 
 
-def run_table(a, path):
-    """The per-config table: every single-GEMV configuration (sizes, modes,
-    split-K) timed as --workload gemv, then the decode sequence at batch 1
-    and 8; markdown rows go to `path`, one JSON line per row to stdout."""
-    import copy
-
-    peaks, _ = measured_peaks()
-    rows = []
-
-    def g(label, **kw):
-        b = copy.copy(a)
-        b.workload, b.steps, b.warmup = "gemv", 20, 3
-        b.S, b.argmax, b.fused, b.norm, b.batch, b.path = 1, False, False, False, 1, "auto"
-        for k, v in kw.items():
-            setattr(b, k, v)
-        d = run_gemv(b, 0, 1, quiet=True)
-        print(json.dumps(dict(d, label=label)), flush=True)
-        rows.append((label, b.mode, b.batch, b.S, d["us_per_gemv"], d["value"], d["kernel"]))
-
+# The single-GEMV configurations of the workload: (label, keyword settings
+# of run_gemv).  C1 and C3 in both forms: an RMSNorm -> quantize launch
+# before the GEMV (the sequence's form) and the one-launch fused prologue.
+def gemv_configs():
+    out = []
     for m in ("dequant", "int8act", "twopass"):
-        g("C0 1024x1024", N=1024, K=1024, mode=m)
+        out.append(("C0 1024x1024", dict(N=1024, K=1024, mode=m)))
     for m in ("dequant", "int8act", "twopass"):
-        g("C1 q 4096x4096 (norm+quant fused)", N=4096, K=4096, mode=m, fused=True)
-        g("C1 gate/up 24576x4096 (norm+quant fused)", N=24576, K=4096, mode=m, fused=True)
-        g("C1 q 4096x4096 (norm+quant launch, then GEMV)", N=4096, K=4096, mode=m, norm=True)
-        g("C1 gate/up 24576x4096 (norm+quant launch, then GEMV)", N=24576, K=4096, mode=m, norm=True)
+        out.append(("C1 q 4096x4096 (norm+quant launch, then GEMV)", dict(N=4096, K=4096, mode=m, norm=True)))
+        out.append(("C1 gate/up 24576x4096 (norm+quant launch, then GEMV)", dict(N=24576, K=4096, mode=m, norm=True)))
+        out.append(("C1 q 4096x4096 (norm+quant fused)", dict(N=4096, K=4096, mode=m, fused=True)))
+        out.append(("C1 gate/up 24576x4096 (norm+quant fused)", dict(N=24576, K=4096, mode=m, fused=True)))
     for m in ("twopass", "dequant"):
         for S in (1, 2, 4, 8):
-            g("C2 o 5120x5120 split-K", N=5120, K=5120, mode=m, S=S)
-            g("C2 down 5120x25600 split-K", N=5120, K=25600, mode=m, S=S)
+            out.append(("C2 o 5120x5120 split-K", dict(N=5120, K=5120, mode=m, S=S)))
+            out.append(("C2 down 5120x25600 split-K", dict(N=5120, K=25600, mode=m, S=S)))
     for m in ("dequant", "int8act", "twopass"):
-        g("C3 lm-head 151936x4096 + argmax (norm fused)", N=151936, K=4096, mode=m, fused=True, argmax=True)
-        g("C3 lm-head 151936x4096 + argmax (norm launch, then GEMV)", N=151936, K=4096, mode=m, norm=True,
-          argmax=True)
+        out.append(("C3 lm-head 151936x4096 + argmax (norm launch, then GEMV)",
+                    dict(N=151936, K=4096, mode=m, norm=True, argmax=True)))
+        out.append(("C3 lm-head 151936x4096 + argmax (norm+quant fused)",
+                    dict(N=151936, K=4096, mode=m, fused=True, argmax=True)))
+    return out
+
+
+def measure_configs(a):
+    """Every single-GEMV configuration, timed as --workload gemv (back-to-back
+    launches in a graph over rotated weight copies, CUDA events), at 1 GPU.
+    Returns one dict per configuration."""
+    import copy
+
+    peaks, src = measured_peaks()
+    rows = []
+    for label, kw in gemv_configs():
+        b = copy.copy(a)
+        b.workload, b.steps, b.warmup = "gemv", 20, 3
+        b.S, b.argmax, b.fused, b.norm, b.batch, b.path, b.no_pdl = 1, False, False, False, 1, "auto", False
+        for k, v in kw.items():
+            setattr(b, k, v)
+        d = run_gemv(b, 0, 1, quiet=True, sample_clocks=False)
+        rows.append({"config": label, "mode": b.mode, "M": b.batch, "S": b.S, "kernel": d["kernel"],
+                     "us_per_gemv": d["us_per_gemv"], "weight_GBs": d["value"],
+                     "frac_of_measured_hbm": d["value"] / peaks["hbm_gbs"],
+                     "pct_of_nominal_8TBs": 100 * d["value"] / NOMINAL_HBM_GBS,
+                     "roofline_frac": d["roofline"]["frac"]})
+    return rows
+
+
+def measure_sequences(a, forms, dev):
+    """The per-token sequence in other forms (batch, mode, decoder dataflow):
+    us per token and weight GB/s, one CUDA graph per token, `a.steps` tokens
+    after warm-up."""
+    import torch
+
+    from q8_quantized_gemv_gb300.decode import DecodeStack
+    peaks, _ = measured_peaks()
+    out = []
+    for batch, mode, glu in forms:
+        st = DecodeStack(layers=a.layers, batch=batch, mode=mode, device=dev, glu=glu)
+        s = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(s):
+            st.run_token()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            st.run_token()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        steps = max(1, min(a.steps, 50))
+        with torch.cuda.stream(s):
+            for _ in range(max(3, a.warmup)):
+                g.replay()
+            e0.record(s)
+            for _ in range(steps):
+                g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        gbs = st.weight_bytes() / (us * 1e-6) / 1e9
+        out.append({"batch": batch, "mode": mode, "dataflow": "decoder" if glu else "projections alone",
+                    "us_per_token": us, "weight_GBs": gbs,
+                    "frac_of_measured_hbm": gbs / peaks["hbm_gbs"], "pct_of_nominal_8TBs": 100 * gbs / NOMINAL_HBM_GBS,
+                    "launches_per_token": st.launches_per_token()})
+        del g, st
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_table(a, path):
+    """The per-config table (measure_configs) as markdown rows in `path`, one
+    JSON line per row to stdout."""
+    peaks, _ = measured_peaks()
+    rows = measure_configs(a)
+    for r in rows:
+        print(json.dumps(r), flush=True)
     with open(path, "w") as f:
         f.write("| Config | Mode | M | S | kernel | us/GEMV | weight GB/s | %% of 8 TB/s | %% of measured %.0f GB/s |\n"
                 % peaks["hbm_gbs"])
         f.write("|---|---|---|---|---|---|---|---|---|\n")
-        for label, m, B, S, us, gbs, kern in rows:
-            f.write(f"| {label} | {m} | {B} | {S} | {kern} | {us:.2f} | {gbs:.0f} | {100 * gbs / NOMINAL_HBM_GBS:.1f} "
-                    f"| {100 * gbs / peaks['hbm_gbs']:.1f} |\n")
+        for r in rows:
+            f.write(f"| {r['config']} | {r['mode']} | {r['M']} | {r['S']} | {r['kernel']} | {r['us_per_gemv']:.2f} "
+                    f"| {r['weight_GBs']:.0f} | {r['pct_of_nominal_8TBs']:.1f} "
+                    f"| {100 * r['frac_of_measured_hbm']:.1f} |\n")
 
 
 def replica_value(bytes_per_step, world, ms_max):

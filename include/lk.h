@@ -54,9 +54,30 @@ typedef int lk_status;
 #define LK_ERR_CUDA            -5  /* the CUDA runtime reported an error     */
 #define LK_ERR_DEVICE_TIMEOUT  -6  /* a device-side bounded wait gave up     */
 
-#define LK_MAX_M      8   /* activation rows that share one weight read */
+#define LK_MAX_M      8   /* activation rows that share one weight read (every kernel) */
+#define LK_MAX_BATCH  64  /* activation rows of the tensor-core GEMV path and of the
+                             norm / quantize / SwiGLU / argmax calls */
 #define LK_MAX_SPLITK 64  /* split-K chunks */
 #define LK_MAX_GROUP  4   /* matrices of one lk_gemv_q8_group call */
+
+/*
+ * Per-call launch settings of the GEMV entry points with an `_ex` suffix
+ * (NULL: the process options, lk_set_option).  The library's own design,
+ * with no counterpart on the pages.
+ *   pdl      -1: the option "pdl"; 0: an ordinary launch; 1: a programmatic
+ *            dependent launch of the kernel before it on the stream (it starts
+ *            while that kernel finishes, streams weights meanwhile and reads
+ *            its activation and writes its outputs only after it)
+ *   prefill  warps (four-warp groups in the tensor-core kernel's four-warp
+ *            layout) of a block that issue their first weight stages before
+ *            the dependency wait (0: the option "ring_prefill", whose default
+ *            is half of them)
+ * Errors: LK_ERR_ARG for pdl outside -1..1 or a negative prefill.
+ */
+typedef struct {
+  int pdl;
+  int prefill;
+} lk_launch_cfg;
 
 /* A static, human-readable name of a status. */
 const char* lk_status_string(lk_status s);
@@ -84,6 +105,40 @@ int lk_version(void);
 lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, float eps,
                            lk_mode mode, float* xn, int8_t* xq, int8_t* xl, float* xs,
                            cudaStream_t stream);
+
+/*
+ * Residual add, then lk_rmsnorm_quant of the sum: the step between a
+ * decoder's projection and the next norm ("kernels.rs" RMSNORM lk_rmsnorm_row
+ * with ADD and SUM; QWEN38_EXTRA_KERNELS gk_add_rmsnorm_q8_hl).
+ *   v[t][i] = x[t][i] + r[t][i]   (one f32 addition)
+ *   s = v (optional), then the RMSNorm of v and the quantizer of `mode`,
+ *   bit for bit lk_rmsnorm_quant(v, gain, ...).
+ *   x, r  f32 [M][K]   the projection output and the residual stream
+ *   s     f32 [M][K]   optional (NULL): the new residual stream v; must not
+ *                      overlap x or r (LK_ERR_ARG), since every block of a row
+ *                      reads the whole row
+ *   gain, xn, xq, xl, xs and the errors as lk_rmsnorm_quant.
+ */
+lk_status lk_add_rmsnorm_quant(const float* x, const float* r, const float* gain, int M, int K, float eps,
+                               lk_mode mode, float* s, float* xn, int8_t* xq, int8_t* xl, float* xs,
+                               cudaStream_t stream);
+
+/*
+ * The gated activation between a decoder's gate/up and down projections,
+ * quantized for the down projection ("kernels.rs" GLU lk_gemv_glu with ACT -1;
+ * QWEN38_EXTRA_KERNELS gk_silu_had_q8 / gk_silu_had_q8_hl):
+ *   h[t][j] = (g / (1 + expf(-g))) * u,  g = gate[t*ld + j], u = up[t*ld + j]
+ * each operation rounded to f32 as written (expf is the CUDA math library's,
+ * within 2 ulp), then the activation quantizer of `mode` on h per 32 values.
+ *   gate, up  f32 rows of F values at a row pitch of ld >= F floats (for a
+ *             fused gate/up output [M][2F]: gate = y, up = y + F, ld = 2F)
+ *   h         f32 [M][F]: required under LK_DEQUANT (the down projection's
+ *             activation), optional otherwise
+ *   hq, hl, hs  [M][F], [M][F], [M][F/32] as lk_quantize_act's outputs
+ * F must be a multiple of 32 (LK_ERR_SHAPE); 0 <= M <= LK_MAX_M.
+ */
+lk_status lk_swiglu_quant(const float* gate, const float* up, int M, int F, long ld, lk_mode mode, float* h,
+                          int8_t* hq, int8_t* hl, float* hs, cudaStream_t stream);
 
 /*
  * The activation quantizer alone ("kernels.rs" QUANT lk_quant, PRELUDE
@@ -131,6 +186,12 @@ lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode
                      const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
                      float* y, uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream);
 
+/* lk_gemv_q8 with per-call launch settings (cfg may be NULL). */
+lk_status lk_gemv_q8_ex(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
+                        const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
+                        float* y, uint64_t* argmax_parts, int* n_parts_out, const lk_launch_cfg* cfg,
+                        cudaStream_t stream);
+
 /* One matrix of a grouped GEMV. */
 typedef struct {
   const int8_t* wq;        /* [N][K] levels                                         */
@@ -159,6 +220,49 @@ typedef struct {
  */
 lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
                            const int8_t* xq, const int8_t* xl, const float* xs, int M, cudaStream_t stream);
+
+/* lk_gemv_q8_group with per-call launch settings (cfg may be NULL). */
+lk_status lk_gemv_q8_group_ex(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
+                              const int8_t* xq, const int8_t* xl, const float* xs, int M, const lk_launch_cfg* cfg,
+                              cudaStream_t stream);
+
+/*
+ * The gated projection pair of a decoder's MLP with the SwiGLU and the
+ * down projection's quantizer in its epilogue ("kernels.rs" GLU lk_gemv_glu
+ * with ACT -1 and a quantized output; QWEN38_EXTRA_KERNELS gk_silu_had_q8):
+ *   g = Wg x, u = Wu x (each exactly lk_gemv_q8's value for its matrix),
+ *   h = (g / (1 + expf(-g))) * u as lk_swiglu_quant computes it, and h
+ *   quantized per 32 outputs by the quantizer of `mode`.
+ *   wg, wsg / wu, wsu  the gate and up matrices, F rows of K each
+ *   x, xq, xl, xs, M   the activation, as lk_gemv_q8
+ *   gu     f32 [2][M][F]: receives the gate values gu[0][t][o] and the up
+ *          values gu[1][t][o] (always written: the epilogue reads them back)
+ *   h      f32 [M][F]: required under LK_DEQUANT (the down projection's
+ *          activation), optional otherwise
+ *   hq, hl, hs  [M][F], [M][F], [M][F/32]: the quantized h (LK_INT8ACT,
+ *          LK_TWOPASS), as lk_quantize_act writes them
+ *   cnt    int32 [F/32] zeroed by the caller before the first call; every
+ *          completed call leaves it zeroed (after LK_ERR_DEVICE_TIMEOUT zero it
+ *          again).  Calls that may run at the same time need separate ones.
+ *          May be NULL: then the two launches below are used.
+ * With one activation row (M = 1), K % 256 == 0 and cnt given, this is ONE
+ * launch of the bulk-copy ring kernel over the 2F rows of both matrices
+ * (interleaved in 32-row tiles, so most groups of 32 outputs are finished by
+ * the block that computed them; a group split between two blocks is finished
+ * by the one whose count completes it).  Otherwise the two GEMVs run as
+ * lk_gemv_q8_group and the SwiGLU as lk_swiglu_quant.  Same bits either way.
+ * F must be a multiple of 32 (LK_ERR_SHAPE).  The library extends the pages
+ * here only in fusing the pair's two matrices into one launch.
+ */
+lk_status lk_gemv_q8_glu(const int8_t* wg, const uint16_t* wsg, const int8_t* wu, const uint16_t* wsu, int F, int K,
+                         lk_mode mode, const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
+                         float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt, cudaStream_t stream);
+
+/* lk_gemv_q8_glu with per-call launch settings (cfg may be NULL). */
+lk_status lk_gemv_q8_glu_ex(const int8_t* wg, const uint16_t* wsg, const int8_t* wu, const uint16_t* wsu, int F,
+                            int K, lk_mode mode, const float* x, const int8_t* xq, const int8_t* xl, const float* xs,
+                            int M, float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt,
+                            const lk_launch_cfg* cfg, cudaStream_t stream);
 
 /*
  * RMSNorm -> quantize -> GEMV in one launch: every block of the bulk-copy
@@ -343,10 +447,6 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 lk_quantize_act): each starts while its predecessor
  *                 finishes (GEMVs stream weights meanwhile) and reads its
  *                 inputs and writes its outputs only after it (default 0)
- *   "l2_prefetch_kb"  lk_gemv_chain: KB of later steps' weights each block
- *                 keeps requested into L2 ahead of the step it computes
- *                 (prefetch.global.L2::evict_last by every thread before
- *                 a barrier; default 0 = off)
  *   "trace"       1: the ring and chain kernels write block 0's timestamps
  *                 to the trace buffer (lk_trace_read); 2: the chain also
  *                 records every block's and block 0's warps' step ends, and
@@ -390,11 +490,6 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 up to 8192, else 4096)
  *   "group_prefill" the same for a grouped launch (lk_gemv_q8_group on the
  *                 ring path): 0 = as "ring_prefill", else that many warps
- *   "l2_ahead_kb" ring and tensor-core kernels: KB per block of the stages
- *                 after the ring's first fill requested into L2 at kernel
- *                 start (cp.async.bulk.prefetch.L2), so that HBM keeps
- *                 streaming while the block waits for the previous kernel
- *                 (default 0 = off)
  * Unknown names or out-of-range values return LK_ERR_ARG.
  */
 lk_status lk_set_option(const char* name, long value);

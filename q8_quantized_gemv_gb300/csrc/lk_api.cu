@@ -21,13 +21,11 @@ long opt_ring_warps = 0;
 long opt_ring_kb = 0;
 long opt_ring_cps = 1;
 long opt_trace = 0;
-long opt_l2_prefetch_kb = 0;
 long opt_pdl = 0;
 long opt_mma_min_m = 0;
 long opt_mma_tk = 0;
 long opt_mma_warps = 0;
 long opt_mma_depth = 0;
-long opt_l2_ahead_kb = 0;
 long opt_ring_prefill = 0;
 long opt_group_prefill = 0;
 long opt_ring_tk = 0;
@@ -61,175 +59,15 @@ const DeviceInfo* device_info(int* dev_out) {
   return &g_info[dev];
 }
 
+lk_status check_launch_cfg(const lk_launch_cfg* cfg) {
+  if (!cfg) return LK_OK;
+  if (cfg->pdl < -1 || cfg->pdl > 1 || cfg->prefill < 0) return LK_ERR_ARG;
+  return LK_OK;
+}
+
 }  // namespace lkh
 
 using namespace lkh;
-
-// ---------------------------------------------------------------------------
-// RMSNorm (+ quantize).  One block per activation row, blockDim.x =
-// min(roundup32(K), 1024) ("kernels.rs" norm_threads): that block size fixes
-// the order of the f32 sum of squares.  Q 0 (Dequant) accumulates in f64 and
-// writes only the normed row.
-template <int Q>
-__global__ void __launch_bounds__(1024) rmsnorm_quant_kernel(const float* __restrict__ x,
-                                                             const float* __restrict__ g, int K,
-                                                             float eps, float* __restrict__ xn,
-                                                             int8_t* __restrict__ xq,
-                                                             int8_t* __restrict__ xl,
-                                                             float* __restrict__ xs, unsigned long long* tr,
-                                                             int slot) {
-  typedef typename acc_of<Q>::t A;
-  __shared__ A red[32];
-  __shared__ A total;
-  // a programmatic dependent (a GEMV launched with "pdl") may start its
-  // weight stream now; it reads these outputs only after this grid completes.
-  // Launched as a dependent itself ("pdl"), this grid reads x and writes its
-  // outputs only after the previous kernel has completed.
-  asm volatile("griddepcontrol.launch_dependents;" :::);
-  trec_stamp(tr, slot, TR_START);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  trec_stamp(tr, slot, TR_WAITED);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int vt = blockDim.x, nw = vt >> 5;
-  const long row = blockIdx.x;
-  const float* xr = x + row * K;
-
-  A acc = 0;
-  for (int i = threadIdx.x; i < K; i += vt) acc = fma_acc((A)__ldcg(xr + i), acc);
-  acc = warp_tree_sum(acc);
-  if (lane == 0) red[warp] = acc;
-  __syncthreads();
-  if (warp == 0) {
-    A v = lane < nw ? red[lane] : (A)0;
-    v = warp_tree_sum(v);
-    if (lane == 0) total = v;
-  }
-  __syncthreads();
-  const A den = norm_div_add(total, K, eps);
-
-  // warp w holds the 32-groups starting at 32w, 32w + vt, ... (vt % 32 == 0)
-  for (int base = warp * 32; base < K; base += vt) {
-    const int i = base + lane;
-    const float yv = norm_scale(__ldcg(xr + i), den, __ldg(g + i));
-    if (xn) xn[row * K + i] = yv;
-    if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, (row * K + i) >> 5, lane);
-  }
-  trec_end(tr, slot, TK_NORM, K);
-}
-
-// The same for K a multiple of the block size vt with KU = K / vt <= 8,
-// spread over KU blocks per row: thread t of every block loads the row's
-// values t + vt*u (u < KU) once, all blocks form the same sum of squares in
-// the same order as rmsnorm_quant_kernel (so the same denominator), and block
-// y normalizes and quantizes only the values t + vt*y it holds: 32-group
-// w + (vt/32)*y per warp w.  The row's divisions are shared by KU blocks.
-template <int Q>
-__global__ void __launch_bounds__(1024) rmsnorm_quant_split_kernel(const float* __restrict__ x,
-                                                                   const float* __restrict__ g, int K, float eps,
-                                                                   float* __restrict__ xn, int8_t* __restrict__ xq,
-                                                                   int8_t* __restrict__ xl, float* __restrict__ xs,
-                                                                   unsigned long long* tr, int slot) {
-  typedef typename acc_of<Q>::t A;
-  constexpr int KU_MAX = 8;
-  __shared__ A red[32];
-  __shared__ A total;
-  asm volatile("griddepcontrol.launch_dependents;" :::);  // as in rmsnorm_quant_kernel
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int vt = blockDim.x, nw = vt >> 5, KU = K / vt, u_mine = blockIdx.y;
-  const long row = blockIdx.x;
-  const float* xr = x + row * K;
-  const float gv = __ldg(g + threadIdx.x + vt * u_mine);  // independent of the previous kernel
-  trec_stamp(tr, slot, TR_START);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  trec_stamp(tr, slot, TR_WAITED);
-  float v[KU_MAX];
-#pragma unroll
-  for (int u = 0; u < KU_MAX; ++u) v[u] = u < KU ? __ldcg(xr + threadIdx.x + vt * u) : 0.f;
-  A acc = 0;
-#pragma unroll
-  for (int u = 0; u < KU_MAX; ++u)
-    if (u < KU) acc = fma_acc((A)v[u], acc);
-  acc = warp_tree_sum(acc);
-  if (lane == 0) red[warp] = acc;
-  __syncthreads();
-  if (warp == 0) {
-    A r = lane < nw ? red[lane] : (A)0;
-    r = warp_tree_sum(r);
-    if (lane == 0) total = r;
-  }
-  __syncthreads();
-  const A den = norm_div_add(total, K, eps);
-  float mine = v[0];
-#pragma unroll
-  for (int u = 1; u < KU_MAX; ++u)
-    if (u == u_mine) mine = v[u];
-  const long i = row * K + threadIdx.x + (long)vt * u_mine;
-  const float yv = norm_scale(mine, den, gv);
-  if (xn) xn[i] = yv;
-  if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, i >> 5, lane);
-  trec_end(tr, slot, TK_NORM, K);
-}
-
-// The same for K a multiple of 1024 (the norm's 1024 virtual threads): 256
-// real threads per block play the 32 virtual warps (warp w plays w, w + 8,
-// w + 16, w + 24), so a block needs few registers and can share an SM with a
-// GEMV block of the neighbouring launches (a 1024-thread block cannot).
-template <int Q>
-__global__ void __launch_bounds__(256) rmsnorm_quant_split256_kernel(const float* __restrict__ x,
-                                                                     const float* __restrict__ g, int K, float eps,
-                                                                     float* __restrict__ xn, int8_t* __restrict__ xq,
-                                                                     int8_t* __restrict__ xl, float* __restrict__ xs,
-                                                                     unsigned long long* tr, int slot) {
-  typedef typename acc_of<Q>::t A;
-  constexpr int KU_MAX = 8, VT = 1024, NJ = 4;  // virtual warps per real warp
-  __shared__ A red[32];
-  __shared__ A total;
-  asm volatile("griddepcontrol.launch_dependents;" :::);  // as in rmsnorm_quant_kernel
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int KU = K / VT, u_mine = blockIdx.y;
-  const long row = blockIdx.x;
-  const float* xr = x + row * K;
-  float gv[NJ];
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) gv[j] = __ldg(g + 32 * (warp + 8 * j) + lane + VT * u_mine);
-  trec_stamp(tr, slot, TR_START);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  trec_stamp(tr, slot, TR_WAITED);
-  float v[NJ][KU_MAX];
-#pragma unroll
-  for (int j = 0; j < NJ; ++j)
-#pragma unroll
-    for (int u = 0; u < KU_MAX; ++u) v[j][u] = u < KU ? __ldcg(xr + 32 * (warp + 8 * j) + lane + VT * u) : 0.f;
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    A acc = 0;
-#pragma unroll
-    for (int u = 0; u < KU_MAX; ++u)
-      if (u < KU) acc = fma_acc((A)v[j][u], acc);
-    acc = warp_tree_sum(acc);
-    if (lane == 0) red[warp + 8 * j] = acc;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    A r = red[lane];
-    r = warp_tree_sum(r);
-    if (lane == 0) total = r;
-  }
-  __syncthreads();
-  const A den = norm_div_add(total, K, eps);
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    float mine = v[j][0];
-#pragma unroll
-    for (int u = 1; u < KU_MAX; ++u)
-      if (u == u_mine) mine = v[j][u];
-    const long i = row * K + 32 * (warp + 8 * j) + lane + (long)VT * u_mine;
-    const float yv = norm_scale(mine, den, gv[j]);
-    if (xn) xn[i] = yv;
-    if (Q > 0) quant_lane<Q>(yv, xq, xl, xs, i >> 5, lane);
-  }
-  trec_end(tr, slot, TK_NORM, K);
-}
 
 template <int Q>
 __global__ void quantize_kernel(const float* __restrict__ x, long groups, int8_t* __restrict__ xq,
@@ -247,41 +85,6 @@ __global__ void quantize_kernel(const float* __restrict__ x, long groups, int8_t
   trec_end(tr, slot, TK_QUANT, groups * 32);
 }
 
-// Option "trace" 3: the timeline buffer and this launch's record, else NULL / 0.
-static unsigned long long* tr_ptr() { return opt_trace == 3 ? trace_ptr() : nullptr; }
-static int tr_slot() { return opt_trace == 3 ? trace_next_slot() : 0; }
-
-// The small kernels run with the shared-memory carveout of the GEMV kernels
-// (the largest), so that an SM need not be reconfigured between a norm or
-// quantize launch and the GEMV that depends on it.
-template <typename F>
-static void carveout_max_shared(F f) {
-  cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-}
-
-// Launch as a programmatic dependent of the previous kernel when the option
-// "pdl" is set (the kernels wait for it before their first read of x).
-template <typename... KA, typename... A>
-static void launch_pdl(void (*f)(KA...), dim3 grid, dim3 block, cudaStream_t stream, A... args) {
-  carveout_max_shared(f);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = opt_pdl ? 1 : 0;
-  cudaLaunchKernelEx(&cfg, f, ((KA)args)...);
-}
-
-static lk_status check_act_out(lk_mode mode, const int8_t* xq, const int8_t* xl, const float* xs) {
-  if (!xq || !xs || (mode == LK_TWOPASS && !xl)) return LK_ERR_ARG;
-  if (!aligned(xs, 4)) return LK_ERR_ALIGN;
-  return LK_OK;
-}
 
 extern "C" {
 
@@ -323,9 +126,6 @@ lk_status lk_set_option(const char* name, long value) {
   } else if (!strcmp(name, "pdl")) {
     if (value < 0 || value > 1) return LK_ERR_ARG;
     opt_pdl = value;
-  } else if (!strcmp(name, "l2_prefetch_kb")) {
-    if (value < 0 || value > 65536) return LK_ERR_ARG;
-    opt_l2_prefetch_kb = value;
   } else if (!strcmp(name, "trace")) {
     if (value < 0 || value > 3) return LK_ERR_ARG;
     opt_trace = value;
@@ -366,9 +166,6 @@ lk_status lk_set_option(const char* name, long value) {
   } else if (!strcmp(name, "group_prefill")) {
     if (value < 0 || value > 16) return LK_ERR_ARG;
     opt_group_prefill = value;
-  } else if (!strcmp(name, "l2_ahead_kb")) {
-    if (value < 0 || value > 65536) return LK_ERR_ARG;
-    opt_l2_ahead_kb = value;
   } else {
     return LK_ERR_ARG;
   }
@@ -383,7 +180,6 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "wait_us")) return opt_wait_us;
   if (!strcmp(name, "ring_hint")) return opt_ring_hint;
   if (!strcmp(name, "trace")) return opt_trace;
-  if (!strcmp(name, "l2_prefetch_kb")) return opt_l2_prefetch_kb;
   if (!strcmp(name, "ring_warps")) return opt_ring_warps;
   if (!strcmp(name, "ring_kb")) return opt_ring_kb;
   if (!strcmp(name, "ring_cps")) return opt_ring_cps;
@@ -392,7 +188,6 @@ long lk_get_option(const char* name) {
   if (!strcmp(name, "mma_tk")) return opt_mma_tk;
   if (!strcmp(name, "mma_warps")) return opt_mma_warps;
   if (!strcmp(name, "mma_depth")) return opt_mma_depth;
-  if (!strcmp(name, "l2_ahead_kb")) return opt_l2_ahead_kb;
   if (!strcmp(name, "ring_prefill")) return opt_ring_prefill;
   if (!strcmp(name, "group_prefill")) return opt_group_prefill;
   if (!strcmp(name, "ring_tk")) return opt_ring_tk;
@@ -402,69 +197,10 @@ long lk_get_option(const char* name) {
   return -1;
 }
 
-lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, float eps, lk_mode mode,
-                           float* xn, int8_t* xq, int8_t* xl, float* xs, cudaStream_t stream) {
-  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
-  if (M < 0 || M > LK_MAX_M || K < 0 || K % 32) return LK_ERR_SHAPE;
-  if (M == 0 || K == 0) return LK_OK;
-  if (!x || !gain) return LK_ERR_ARG;
-  if (!aligned(x, 4) || !aligned(gain, 4) || (xn && !aligned(xn, 4))) return LK_ERR_ALIGN;
-  const int vt = K < 1024 ? K : 1024;  // K % 32 == 0: roundup32(K) == K
-  if (K % 1024 == 0 && K / 1024 <= 8) {
-    const dim3 grid(M, K / 1024);
-    if (mode == LK_DEQUANT) {
-      if (!xn) return LK_ERR_ARG;
-      launch_pdl(rmsnorm_quant_split256_kernel<0>, grid, dim3(256), stream, x, gain, K, eps, xn, (int8_t*)nullptr,
-                 (int8_t*)nullptr, (float*)nullptr, tr_ptr(), tr_slot());
-    } else {
-      lk_status st = check_act_out(mode, xq, xl, xs);
-      if (st) return st;
-      if (mode == LK_INT8ACT)
-        launch_pdl(rmsnorm_quant_split256_kernel<1>, grid, dim3(256), stream, x, gain, K, eps, xn, xq,
-                   (int8_t*)nullptr, xs, tr_ptr(), tr_slot());
-      else
-        launch_pdl(rmsnorm_quant_split256_kernel<2>, grid, dim3(256), stream, x, gain, K, eps, xn, xq, xl, xs,
-                   tr_ptr(), tr_slot());
-    }
-    return launch_status();
-  }
-  if (K % vt == 0 && K / vt <= 8) {
-    const dim3 grid(M, K / vt);
-    if (mode == LK_DEQUANT) {
-      if (!xn) return LK_ERR_ARG;
-      launch_pdl(rmsnorm_quant_split_kernel<0>, grid, dim3(vt), stream, x, gain, K, eps, xn, (int8_t*)nullptr,
-                 (int8_t*)nullptr, (float*)nullptr, tr_ptr(), tr_slot());
-    } else {
-      lk_status st = check_act_out(mode, xq, xl, xs);
-      if (st) return st;
-      if (mode == LK_INT8ACT)
-        launch_pdl(rmsnorm_quant_split_kernel<1>, grid, dim3(vt), stream, x, gain, K, eps, xn, xq,
-                   (int8_t*)nullptr, xs, tr_ptr(), tr_slot());
-      else
-        launch_pdl(rmsnorm_quant_split_kernel<2>, grid, dim3(vt), stream, x, gain, K, eps, xn, xq, xl, xs, tr_ptr(), tr_slot());
-    }
-    return launch_status();
-  }
-  if (mode == LK_DEQUANT) {
-    if (!xn) return LK_ERR_ARG;
-    launch_pdl(rmsnorm_quant_kernel<0>, dim3(M), dim3(vt), stream, x, gain, K, eps, xn, (int8_t*)nullptr,
-               (int8_t*)nullptr, (float*)nullptr, tr_ptr(), tr_slot());
-  } else {
-    lk_status st = check_act_out(mode, xq, xl, xs);
-    if (st) return st;
-    if (mode == LK_INT8ACT)
-      launch_pdl(rmsnorm_quant_kernel<1>, dim3(M), dim3(vt), stream, x, gain, K, eps, xn, xq, (int8_t*)nullptr,
-                 xs, tr_ptr(), tr_slot());
-    else
-      launch_pdl(rmsnorm_quant_kernel<2>, dim3(M), dim3(vt), stream, x, gain, K, eps, xn, xq, xl, xs, tr_ptr(), tr_slot());
-  }
-  return launch_status();
-}
-
 lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq, int8_t* xl,
                           float* xs, cudaStream_t stream) {
   if (mode != LK_INT8ACT && mode != LK_TWOPASS) return LK_ERR_ARG;
-  if (M < 0 || M > LK_MAX_M || K < 0 || K % 32) return LK_ERR_SHAPE;
+  if (M < 0 || M > LK_MAX_BATCH || K < 0 || K % 32) return LK_ERR_SHAPE;
   if (M == 0 || K == 0) return LK_OK;
   if (!x) return LK_ERR_ARG;
   if (!aligned(x, 4)) return LK_ERR_ALIGN;
@@ -579,7 +315,7 @@ int lk_argmax_scratch_entries(int N) {
 
 lk_status lk_argmax(const float* logits, const uint64_t* parts, int n_parts, int M, int N,
                     int32_t* idx, uint64_t* scratch, cudaStream_t stream) {
-  if (M < 0 || M > LK_MAX_M) return LK_ERR_SHAPE;
+  if (M < 0 || M > LK_MAX_BATCH) return LK_ERR_SHAPE;
   if (M == 0) return LK_OK;
   if (N < 1) return LK_ERR_SHAPE;
   if (!idx) return LK_ERR_ARG;

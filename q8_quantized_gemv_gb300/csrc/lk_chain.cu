@@ -33,7 +33,6 @@ struct ChainArgs {
   int* err;
   unsigned long long* trace;  // block 0's timestamps (option "trace"), or NULL
   int trace_all;              // also every block's and block 0's warps' step ends (trace 2)
-  long long pf_budget;        // bytes of later steps' weights each block keeps requested into L2 ahead
   int pdl;                    // launched as a programmatic dependent (a chain without barriers)
   int tslot;                  // trace 3: this launch's record in the timeline, else -1
   int prefill;                // warps that fill their stages before the dependency wait
@@ -58,24 +57,6 @@ __device__ __forceinline__ lk_chain_op chain_op_at(const ChainArgs& ca, int i) {
     return o;
   }
   return ca.ops[i];
-}
-
-// This block's bytes of step `o` (its rows' levels, then their scales): a
-// contiguous range of each array, since a block's rows are contiguous.
-struct PfRange {
-  const unsigned char* w;
-  long wbytes;
-  const unsigned char* s;
-  long sbytes;
-};
-__device__ __forceinline__ PfRange pf_range(const lk_chain_op& o) {
-  const long N = o.N, r0 = (long)blockIdx.x * N / gridDim.x, r1 = (long)(blockIdx.x + 1) * N / gridDim.x;
-  PfRange r;
-  r.w = (const unsigned char*)o.wq + r0 * o.K;
-  r.wbytes = (r1 - r0) * o.K;
-  r.s = (const unsigned char*)o.ws + r0 * (o.K / 16);
-  r.sbytes = (r1 - r0) * (o.K / 16);
-  return r;
 }
 
 __device__ __forceinline__ void stamp(unsigned long long* trace, int i) {
@@ -203,41 +184,6 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
   const bool early = warp < ca.prefill;
   for (int d = 0; early && d < D && iop < ca.n_ops; ++d) issue_next();
 
-  // L2 prefetch cursor: the block's bytes of later steps (levels, then
-  // scales, step after step) are requested into L2 with per-thread
-  // prefetch.global.L2::evict_last, keeping pf_budget bytes ahead of the step
-  // being computed; it runs while the threads would wait at a barrier anyway.
-  int pf_op = 1;
-  long pf_off = 0;   // bytes of step pf_op already requested
-  auto prefetch_ahead = [&](int cur) {
-    if (ca.pf_budget <= 0) return;
-    if (pf_op <= cur) {
-      pf_op = cur + 1;
-      pf_off = 0;
-    }
-    long ahead = pf_off;  // bytes requested beyond step `cur`
-    for (int k = cur + 1; k < pf_op && k < ca.n_ops; ++k) {
-      const PfRange r = pf_range(chain_op_at(ca, k));
-      ahead += r.wbytes + r.sbytes;
-    }
-    while (pf_op < ca.n_ops && ahead < ca.pf_budget) {
-      const PfRange r = pf_range(chain_op_at(ca, pf_op));
-      const long total = r.wbytes + r.sbytes;
-      const long want = ca.pf_budget - ahead;
-      const long end = pf_off + want < total ? pf_off + want : total;
-      for (long off = pf_off + 128L * threadIdx.x; off < end; off += 128L * blockDim.x) {
-        const unsigned char* ptr = off < r.wbytes ? r.w + off : r.s + (off - r.wbytes);
-        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(ptr));
-      }
-      ahead += end - pf_off;
-      pf_off = end;
-      if (pf_off >= total) {
-        ++pf_op;
-        pf_off = 0;
-      }
-    }
-  };
-
   // weights above do not depend on the previous kernel; activations do (the
   // first step's prologue waits itself, after requesting its norm gains)
   bool waited = ca.pdl == 0;
@@ -247,7 +193,6 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_chain_kernel(const ChainA
   bool ok = true;
   for (int op = 0; ok && op < ca.n_ops; ++op) {
     const lk_chain_op o = chain_op_at(ca, op);
-    if (o.wait) prefetch_ahead(op);
     if (o.wait && !grid_sync(ca.sync, gen, gridDim.x, ca.wait_ns, ca.err, abort_flag)) {
       ok = false;
       break;
@@ -456,18 +401,17 @@ static lk_status chain_launch(const lk_chain_op* ops, const lk_chain_op* ops_dev
   ca.err = lkh::error_word_ptr();
   if (!ca.err) return LK_ERR_CUDA;
   ca.trace = lkh::opt_trace ? lkh::trace_ptr() : nullptr;
-  ca.pf_budget = lkh::opt_l2_prefetch_kb * 1024;
   ca.trace_all = lkh::opt_trace == 2;
   ca.tslot = lkh::opt_trace == 3 ? lkh::trace_next_slot() : -1;
-  ca.pdl = !barrier && lkh::opt_pdl ? 1 : 0;
-  ca.prefill = lkh::prefill_warps(w);
+  ca.pdl = !barrier && (given ? given->pdl : (int)lkh::opt_pdl) ? 1 : 0;
+  ca.prefill = lkh::prefill_warps(w, given ? given->prefill : 0);
   ca.n_inl = 0;
   ca.gx = nullptr;
   ca.gxq = ca.gxl = nullptr;
   ca.gxs = nullptr;
   for (int i = 0; i < LK_MAX_GROUP; ++i) ca.inl[i] = ops[i < n_ops ? i : 0];
   if (given) {
-    if (lkh::opt_group_prefill > 0) ca.prefill = (int)lkh::opt_group_prefill;
+    if (lkh::opt_group_prefill > 0 && given->prefill == 0) ca.prefill = (int)lkh::opt_group_prefill;
     ca.n_inl = n_ops;
     ca.gx = given->x;
     ca.gxq = given->xq;

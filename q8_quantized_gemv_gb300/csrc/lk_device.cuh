@@ -134,6 +134,12 @@ __device__ __forceinline__ void quant_lane(float v, int8_t* __restrict__ hi, int
   quant_groups<Q, 1>(vv, ok, hi, lo, xs, g, 0, lane);
 }
 
+// ---- SwiGLU ("kernels.rs" lk_gemv_glu with ACT -1): h = g / (1 + e^-g) * u,
+// each operation rounded to f32 as written (expf is the CUDA library's).
+__device__ __forceinline__ float swiglu(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
 // ---- RMSNorm arithmetic ("kernels.rs" lk_rmsnorm_row: accumulator f64 under
 // Dequant (Q 0), f32 otherwise; y = v / sqrt(sum/K + eps) * g)
 template <int Q>
@@ -151,9 +157,6 @@ __device__ __forceinline__ double norm_div_add(double sum, int K, float eps) {
 }
 __device__ __forceinline__ float norm_scale(float v, float den, float g) {
   return __fmul_rn(__fdiv_rn(v, den), g);
-}
-__device__ __forceinline__ float norm_scale(float v, double den, float g) {
-  return __double2float_rn(__dmul_rn(__ddiv_rn((double)v, den), (double)g));
 }
 
 // ---- argmax key ("megakernel.cu" amax_key) --------------------------------------

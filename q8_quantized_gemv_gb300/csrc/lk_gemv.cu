@@ -180,7 +180,7 @@ lk_status direct_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
 lk_status check_common(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
                        const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M) {
   if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
-  if (N < 0 || K < 0 || K % 32 || M < 0 || M > LK_MAX_M) return LK_ERR_SHAPE;
+  if (N < 0 || K < 0 || K % 32 || M < 0 || M > LK_MAX_BATCH) return LK_ERR_SHAPE;
   if (K == 0) return LK_OK;  // nothing is read: every output is 0
   if (!wq || !ws) return LK_ERR_ARG;
   if (mode == LK_DEQUANT ? !x : (!xq || !xs || (mode == LK_TWOPASS && !xl))) return LK_ERR_ARG;
@@ -213,6 +213,15 @@ GemvProblem make_problem(const int8_t* wq, const uint16_t* ws, int N, int K, lk_
   p.xraw = nullptr;
   p.gain = nullptr;
   p.eps = 0.f;
+  p.F = 0;
+  p.wq2 = nullptr;
+  p.ws2 = nullptr;
+  p.glu_cnt = nullptr;
+  p.h = nullptr;
+  p.hq = nullptr;
+  p.hl = nullptr;
+  p.hs = nullptr;
+  apply_cfg(p, nullptr);
   return p;
 }
 
@@ -242,7 +251,15 @@ extern "C" {
 lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode, const float* x,
                      const int8_t* xq, const int8_t* xl, const float* xs, int M, float* y,
                      uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream) {
+  return lk_gemv_q8_ex(wq, ws, N, K, mode, x, xq, xl, xs, M, y, argmax_parts, n_parts_out, nullptr, stream);
+}
+
+lk_status lk_gemv_q8_ex(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode, const float* x,
+                        const int8_t* xq, const int8_t* xl, const float* xs, int M, float* y,
+                        uint64_t* argmax_parts, int* n_parts_out, const lk_launch_cfg* cfg, cudaStream_t stream) {
   lk_status st = check_common(wq, ws, N, K, mode, x, xq, xl, xs, M);
+  if (st) return st;
+  st = check_launch_cfg(cfg);
   if (st) return st;
   if (argmax_parts && !n_parts_out) return LK_ERR_ARG;
   if (N == 0 || M == 0) {
@@ -252,13 +269,14 @@ lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode
   if (!y) return LK_ERR_ARG;
   if (!aligned(y, 4) || (argmax_parts && !aligned(argmax_parts, 8))) return LK_ERR_ALIGN;
   GemvProblem p = make_problem(wq, ws, N, K, mode, x, xq, xl, xs, M);
+  apply_cfg(p, cfg);
   p.y = y;
   p.amax = (unsigned long long*)argmax_parts;
   int n_parts = 0;
   if ((opt_gemv_path == 0 || opt_gemv_path == 3) && mma_supports(p)) {
     st = mma_gemv(p, stream, &n_parts);
-  } else if (opt_gemv_path == 3) {
-    return LK_ERR_SHAPE;
+  } else if (opt_gemv_path == 3 || M > LK_MAX_M) {
+    return LK_ERR_SHAPE;  // past 8 rows: the tensor-core kernel only
   } else if (opt_gemv_path != 1 && ring_supports(p)) {
     st = ring_gemv(p, stream, &n_parts);
   } else {
@@ -271,7 +289,17 @@ lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode
 
 lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
                            const int8_t* xq, const int8_t* xl, const float* xs, int M, cudaStream_t stream) {
+  return lk_gemv_q8_group_ex(targets, n, K, mode, x, xq, xl, xs, M, nullptr, stream);
+}
+
+lk_status lk_gemv_q8_group_ex(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
+                              const int8_t* xq, const int8_t* xl, const float* xs, int M, const lk_launch_cfg* cfg,
+                              cudaStream_t stream) {
   if (!targets || n < 1 || n > LK_MAX_GROUP) return LK_ERR_ARG;
+  {
+    const lk_status st = check_launch_cfg(cfg);
+    if (st) return st;
+  }
   for (int i = 0; i < n; ++i) {
     const lk_gemv_target& t = targets[i];
     if (!t.wq || !t.ws || !t.y) return LK_ERR_ARG;
@@ -282,13 +310,14 @@ lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode 
   }
   if (M == 0 || K == 0) {
     for (int i = 0; i < n; ++i) {
-      lk_status st = lk_gemv_q8(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M,
-                                targets[i].y, nullptr, nullptr, stream);
+      lk_status st = lk_gemv_q8_ex(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M,
+                                   targets[i].y, nullptr, nullptr, cfg, stream);
       if (st) return st;
     }
     return LK_OK;
   }
   GemvProblem p = make_problem(targets[0].wq, targets[0].ws, targets[0].N, K, mode, x, xq, xl, xs, M);
+  apply_cfg(p, cfg);
   bool one = (opt_gemv_path == 0 || opt_gemv_path == 3);
   for (int i = 0; i < n && one; ++i) {
     GemvProblem q = p;
@@ -316,16 +345,16 @@ lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode 
     if (st != LK_ERR_SHAPE) return st;
   }
   for (int i = 0; i < n; ++i) {
-    lk_status st = lk_gemv_q8(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M, targets[i].y,
-                              nullptr, nullptr, stream);
+    lk_status st = lk_gemv_q8_ex(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M, targets[i].y,
+                                 nullptr, nullptr, cfg, stream);
     if (st) return st;
   }
   return LK_OK;
 }
 
 int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S) {
-  if (mode < LK_DEQUANT || mode > LK_TWOPASS || N < 1 || K < 32 || K % 32 || M < 1 || M > LK_MAX_M || S < 0 ||
-      S > LK_MAX_SPLITK)
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS || N < 1 || K < 32 || K % 32 || M < 1 || M > LK_MAX_BATCH || S < 0 ||
+      S > LK_MAX_SPLITK || (M > LK_MAX_M && S > 0))
     return 0;
   // 16-byte aligned stand-in pointers: only the shape decides
   const void* a16 = (const void*)(uintptr_t)256;
@@ -333,8 +362,9 @@ int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S) {
                                (const int8_t*)a16, (const int8_t*)a16, (const float*)a16, M);
   p.split = S > 0;
   p.S = S > 0 ? S : 1;
-  if (opt_gemv_path == 1) return 1;
   if (S == 0 && (opt_gemv_path == 0 || opt_gemv_path == 3) && mma_supports(p)) return 3;
+  if (M > LK_MAX_M) return 0;
+  if (opt_gemv_path == 1) return 1;
   if (opt_gemv_path == 3) return S == 0 ? 0 : (ring_supports(p) ? 2 : 1);
   return ring_supports(p) ? 2 : (opt_gemv_path == 2 ? 0 : 1);
 }
@@ -367,6 +397,54 @@ lk_status lk_rmsnorm_quant_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, 
   return st;
 }
 
+lk_status lk_gemv_q8_glu(const int8_t* wg, const uint16_t* wsg, const int8_t* wu, const uint16_t* wsu, int F, int K,
+                         lk_mode mode, const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
+                         float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt, cudaStream_t stream) {
+  return lk_gemv_q8_glu_ex(wg, wsg, wu, wsu, F, K, mode, x, xq, xl, xs, M, gu, h, hq, hl, hs, cnt, nullptr, stream);
+}
+
+lk_status lk_gemv_q8_glu_ex(const int8_t* wg, const uint16_t* wsg, const int8_t* wu, const uint16_t* wsu, int F,
+                            int K, lk_mode mode, const float* x, const int8_t* xq, const int8_t* xl, const float* xs,
+                            int M, float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt,
+                            const lk_launch_cfg* cfg, cudaStream_t stream) {
+  lk_status st = check_common(wg, wsg, F, K, mode, x, xq, xl, xs, M);
+  if (st) return st;
+  st = check_launch_cfg(cfg);
+  if (st) return st;
+  st = check_common(wu, wsu, F, K, mode, x, xq, xl, xs, M);
+  if (st) return st;
+  if (F % 32) return LK_ERR_SHAPE;
+  if (F == 0 || M == 0) return LK_OK;
+  if (!gu) return LK_ERR_ARG;
+  if (!aligned(gu, 4) || (h && !aligned(h, 4))) return LK_ERR_ALIGN;
+  if (mode == LK_DEQUANT) {
+    if (!h) return LK_ERR_ARG;
+  } else {
+    st = check_act_out(mode, hq, hl, hs);
+    if (st) return st;
+  }
+  if (K > 0 && opt_gemv_path == 0) {
+    GemvProblem p = make_problem(wg, wsg, 2 * F, K, mode, x, xq, xl, xs, M);
+    apply_cfg(p, cfg);
+    p.y = gu;
+    p.F = F;
+    p.wq2 = wu;
+    p.ws2 = (const __half*)wsu;
+    p.glu_cnt = cnt;
+    p.h = h;
+    p.hq = mode == LK_DEQUANT ? nullptr : hq;
+    p.hl = mode == LK_TWOPASS ? hl : nullptr;
+    p.hs = mode == LK_DEQUANT ? nullptr : hs;
+    if (cnt && aligned(cnt, 4) && ring_supports(p)) return ring_gemv(p, stream, nullptr);
+  }
+  // two launches: both GEMVs (one grouped launch where the kernels allow),
+  // then the SwiGLU -> quantize step over their outputs
+  const lk_gemv_target t[2] = {{wg, wsg, F, 0, gu}, {wu, wsu, F, 0, gu + (long)M * F}};
+  st = lk_gemv_q8_group_ex(t, 2, K, mode, x, xq, xl, xs, M, cfg, stream);
+  if (st) return st;
+  return lk_swiglu_quant(gu, gu + (long)M * F, M, F, F, mode, h, hq, hl, hs, stream);
+}
+
 size_t lk_splitk_workspace_bytes(lk_mode mode, int S, int M, int N) {
   if (S < 1 || M < 0 || N < 0) return 0;
   return (size_t)S * (size_t)M * (size_t)N * (mode == LK_DEQUANT ? 8 : 4);
@@ -377,7 +455,7 @@ lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, 
                             int S, void* part, size_t part_bytes, cudaStream_t stream) {
   lk_status st = check_common(wq, ws, N, K, mode, x, xq, xl, xs, M);
   if (st) return st;
-  if (S < 1 || S > LK_MAX_SPLITK) return LK_ERR_SHAPE;
+  if (S < 1 || S > LK_MAX_SPLITK || M > LK_MAX_M) return LK_ERR_SHAPE;
   if (N == 0 || M == 0) return LK_OK;
   if (!part) return LK_ERR_ARG;
   if (!aligned(part, mode == LK_DEQUANT ? 8 : 4)) return LK_ERR_ALIGN;

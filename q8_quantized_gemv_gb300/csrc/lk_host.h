@@ -29,7 +29,6 @@ extern long opt_ring_warps;   // 0 auto, else warps per block of the ring kernel
 extern long opt_ring_kb;      // 0: no cap, else shared memory per ring block in KB
 extern long opt_ring_cps;     // ring blocks per SM in the grid (default 1)
 extern long opt_pdl;          // 1: fused ring launches are programmatic dependents
-extern long opt_l2_prefetch_kb;  // chain: KB of later steps each block requests into L2 ahead
 extern long opt_trace;        // 1: kernels write block 0 timestamps to the trace buffer
 extern long opt_ring_hint;    // 1: L2 evict-first hint on the weight copies (default)
 extern long opt_wait_us;      // bound of every device-side wait, microseconds (0 = 2 s)
@@ -43,7 +42,6 @@ extern long opt_mma_act16;    // its activations held as f16: 0 auto, 1 force, 2
 extern long opt_group_prefill; // the same for a grouped launch over one given activation (0: as ring_prefill)
 extern long opt_ring_tk;       // ring kernel: bytes of K per stage for rows longer than that (0: auto)
 extern long opt_ring_prefill; // warps that issue their first weight stages before the dependency wait (0: half)
-extern long opt_l2_ahead_kb;  // ring/tensor-core kernels: KB per block of later stages requested into L2 at start
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
@@ -73,6 +71,9 @@ inline lk_status launch_status() {
   return e == cudaSuccess ? LK_OK : LK_ERR_CUDA;
 }
 
+// Checks of a caller's launch settings: LK_ERR_ARG, else LK_OK.
+lk_status check_launch_cfg(const lk_launch_cfg* cfg);
+
 // Everything one GEMV launch needs (plain, split-K partial, argmax epilogue).
 struct GemvProblem {
   const int8_t* wq;
@@ -94,24 +95,83 @@ struct GemvProblem {
   const float* xraw;             // fused: raw f32 rows [M][K]
   const float* gain;             // fused: RMSNorm gain [K], or NULL for quantize only
   float eps;
+  // The gated pair (lk_gemv_q8_glu; F > 0): wq/ws are the gate matrix,
+  // wq2/ws2 the up matrix, F rows each, N = 2F; y receives the gate values
+  // [M][F] followed by the up values [M][F]; the epilogue writes the SwiGLU
+  // h (optional f32 [M][F]) and its quantized words hq/hl/hs, completing each
+  // 32-output group once through the counters glu_cnt [F/32].
+  long F;
+  const int8_t* wq2;
+  const __half* ws2;
+  int* glu_cnt;
+  float* h;
+  int8_t* hq;
+  int8_t* hl;
+  float* hs;
+  // per-call launch settings (lk_launch_cfg, or the process options)
+  int pdl;
+  int prefill;                 // 0: the default
 };
+
+// GemvProblem's launch settings from cfg (NULL: the process options).
+inline void apply_cfg(GemvProblem& p, const lk_launch_cfg* cfg) {
+  p.pdl = (cfg && cfg->pdl >= 0) ? cfg->pdl : (opt_pdl ? 1 : 0);
+  p.prefill = cfg ? cfg->prefill : 0;
+}
 
 // Warps of a block of nw that fill their ring stages before the dependency
 // wait (the others after the activation is loaded): option "ring_prefill",
 // 0 = half of them (measured best: a full ring of requests ahead of the
 // wait slowed the activation loads and the wait itself).
-inline int prefill_warps(int nw) {
-  const int p = opt_ring_prefill > 0 ? (int)opt_ring_prefill : (nw + 1) / 2;
+inline int prefill_warps(int nw, int want = 0) {
+  const int p = want > 0 ? want : opt_ring_prefill > 0 ? (int)opt_ring_prefill : (nw + 1) / 2;
   return p < nw ? p : nw;
+}
+
+// Option "trace" 3: the timeline buffer and this launch's record, else NULL / 0.
+unsigned long long* trace_ptr();
+int trace_next_slot();
+inline unsigned long long* tr_ptr() { return opt_trace == 3 ? trace_ptr() : nullptr; }
+inline int tr_slot() { return opt_trace == 3 ? trace_next_slot() : 0; }
+
+// The small kernels run with the shared-memory carveout of the GEMV kernels
+// (the largest), so that an SM need not be reconfigured between a norm or
+// quantize launch and the GEMV that depends on it.
+template <typename F>
+inline void carveout_max_shared(F f) {
+  cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+}
+
+// Launch as a programmatic dependent of the previous kernel when the option
+// "pdl" is set (the kernels wait for it before their first read of data
+// that kernel writes).
+template <typename... KA, typename... A>
+inline void launch_pdl(void (*f)(KA...), dim3 grid, dim3 block, cudaStream_t stream, A... args) {
+  carveout_max_shared(f);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = opt_pdl ? 1 : 0;
+  cudaLaunchKernelEx(&cfg, f, ((KA)args)...);
+}
+
+// Output buffers of an activation quantizer: present for the mode, aligned.
+inline lk_status check_act_out(lk_mode mode, const int8_t* xq, const int8_t* xl, const float* xs) {
+  if (!xq || !xs || (mode == LK_TWOPASS && !xl)) return LK_ERR_ARG;
+  if (!aligned(xs, 4)) return LK_ERR_ALIGN;
+  return LK_OK;
 }
 
 // Device address of the error word that bounded device waits set (lk_ring.cu).
 int* error_word_ptr();
-// Device address of the trace buffer (option "trace").
-unsigned long long* trace_ptr();
-// Option "trace" 3: the next launch's record index in the timeline (wraps),
-// and its reset (setting the option resets it).
-int trace_next_slot();
+// Option "trace" 3: resets the record index of the timeline (setting the
+// option does it).
 void trace_reset();
 
 // Bulk-copy ring kernel (lk_ring.cu).  Returns LK_ERR_SHAPE when the problem

@@ -22,6 +22,13 @@
 // >= M read as zeros.  The int8 -> f16 step is exact: (0x6400 | (b ^ 0x80))
 // is the f16 1024 + b + 128, minus 1152.
 //
+// More than 8 activation rows (up to LK_MAX_BATCH): the rows form groups of
+// 8 (blockIdx.y), each group with its own share of the SMs (gridDim.x blocks
+// per group) running the 8-row arithmetic above over every tile.  All groups
+// run at once, so a tile is read from HBM once and from L2 by the other
+// groups at about the same time; each (row, activation) value is computed
+// exactly as at 8 rows.
+//
 // Data movement is the ring kernel's: weights stream through per-warp ring
 // slots by 1-D bulk copies (TMA) completing on mbarriers, every wait bounded.
 // A stage is one tile's slice of tk bytes of K: 16 copies of a weight row
@@ -58,7 +65,7 @@ struct MmaArgs {
   long tile0[MG + 1];      // first tile of matrix m; tile0[nmat] = all tiles
   int nw;                  // warps per block
   int depth;               // ring stages per warp
-  int gx;                  // blocks
+  int gx;                  // blocks per activation-row group (gridDim.x)
   long ntiles;             // sum over the matrices of ceil(N / 16)
   unsigned tk;             // bytes of K per stage (multiple of 256)
   unsigned rs;             // stage row stride (tk + 32)
@@ -73,7 +80,6 @@ struct MmaArgs {
   unsigned long long pol_w;
   int pdl;
   int* err;
-  int l2_ahead;            // stages per warp requested into L2 beyond the ring at start
   unsigned long long* trace;  // option "trace" 3: the launch timeline, else NULL
   int tslot;
   int prefill;             // warps that fill their stages before the dependency wait
@@ -203,32 +209,19 @@ __device__ __forceinline__ void issue(const MmaArgs& ra, long tile, int c, unsig
   __syncwarp();
 }
 
-// Request slice c of tile `tile` (the bytes issue() copies) into L2.
-__device__ __forceinline__ void prefetch(const MmaArgs& ra, long tile, int c, int lane) {
-  const int K = ra.p.K;
-  const Mat m = mat_of(ra, tile);
-  const int rows = m.N - m.row0 < TR ? (int)(m.N - m.row0) : TR;
-  const int k0 = c * (int)ra.tk;
-  const int len = K - k0 < (int)ra.tk ? K - k0 : (int)ra.tk;
-  const int r = lane & 15;
-  if (r < rows) {
-    const long row = m.row0 + r;
-    if (lane < 16)
-      bulk_prefetch_l2(m.wq + row * K + k0, (unsigned)len);
-    else
-      bulk_prefetch_l2(m.ws + (row * (K >> 5) + (k0 >> 5)) * 2, (unsigned)len / 16u);
-  }
-}
-
 // The activation rows into shared memory (all threads call it, after the
 // dependency wait): f16 rows converted by every thread (A16), or the int8
 // rows by warp 0's bulk copies completing on act_bar (bounded wait).
 // Returns false when that wait gave up.
 template <int Q, bool A16>
-__device__ __forceinline__ bool load_rows(const MmaArgs& ra, unsigned char* act, unsigned act_bar,
+__device__ __forceinline__ bool load_rows(const MmaArgs& ra, int M, int row0, unsigned char* act, unsigned act_bar,
                                           volatile int* abort_flag) {
   const lkh::GemvProblem& a = ra.p;
-  const int M = a.M, K = a.K, nb = K >> 5;
+  const int K = a.K, nb = K >> 5;
+  // this block's group of activation rows: rows row0 .. row0 + M - 1
+  const int8_t* gxq = a.xq + (long)row0 * K;
+  const int8_t* gxl = Q == 2 ? a.xl + (long)row0 * K : nullptr;
+  const float* gxs = a.xs + (long)row0 * nb;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // the activation rows: int8 words (and low words) and scales, row-padded
   if (A16) {
@@ -244,7 +237,7 @@ __device__ __forceinline__ bool load_rows(const MmaArgs& ra, unsigned char* act,
           const int lo = Q == 2 && i >= M * runs;
           const int j = lo ? i - M * runs : i;
           const int row = j / runs, off = (j - row * runs) << 4;
-          v[u] = ld_cg16((lo ? a.xl : a.xq) + (long)row * K + off);
+          v[u] = ld_cg16((lo ? gxl : gxq) + (long)row * K + off);
         }
       }
 #pragma unroll
@@ -267,7 +260,7 @@ __device__ __forceinline__ bool load_rows(const MmaArgs& ra, unsigned char* act,
     }
     for (int i = threadIdx.x; i < M * nb; i += blockDim.x) {
       const int row = i / nb, b = i - row * nb;
-      ((float*)(act + ra.a_xs))[(size_t)row * ra.xsr + b] = __ldcg(a.xs + (long)row * nb + b);
+      ((float*)(act + ra.a_xs))[(size_t)row * ra.xsr + b] = __ldcg(gxs + (long)row * nb + b);
     }
     __syncthreads();
   } else if (warp == 0) {
@@ -278,11 +271,11 @@ __device__ __forceinline__ bool load_rows(const MmaArgs& ra, unsigned char* act,
     if (lane == 0)
       mbar_arrive_expect_tx(act_bar, (unsigned)M * ((unsigned)K * (Q == 2 ? 2u : 1u) + (unsigned)nb * 4u));
     __syncwarp();
-    if (lane < M) bulk(act + (size_t)lane * ra.ar, a.xq + (long)lane * K, (unsigned)K, act_bar, pol_a);
+    if (lane < M) bulk(act + (size_t)lane * ra.ar, gxq + (long)lane * K, (unsigned)K, act_bar, pol_a);
     if (Q == 2 && lane >= 8 && lane < 8 + M)
-      bulk(act + ra.a_lo + (size_t)(lane - 8) * ra.ar, a.xl + (long)(lane - 8) * K, (unsigned)K, act_bar, pol_a);
+      bulk(act + ra.a_lo + (size_t)(lane - 8) * ra.ar, gxl + (long)(lane - 8) * K, (unsigned)K, act_bar, pol_a);
     if (lane >= 16 && lane < 16 + M)
-      bulk(act + ra.a_xs + (size_t)(lane - 16) * ra.xsr * 4, a.xs + (long)(lane - 16) * nb, (unsigned)nb * 4u,
+      bulk(act + ra.a_xs + (size_t)(lane - 16) * ra.xsr * 4, gxs + (long)(lane - 16) * nb, (unsigned)nb * 4u,
            act_bar, pol_a);
     __syncwarp();
   }
@@ -307,7 +300,8 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   extern __shared__ __align__(128) unsigned char smem[];
   const lkh::GemvProblem& a = ra.p;
   const int nw = ra.nw, D = ra.depth, NS = nw * D;
-  const int M = a.M, K = a.K;
+  const int row0 = TN * (int)blockIdx.y;                  // this block's group of activation rows
+  const int M = a.M - row0 < TN ? a.M - row0 : TN, K = a.K;
   unsigned char* act = smem;
   unsigned char* ring = smem + ra.ring_off;
   unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
@@ -345,14 +339,10 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   for (; early && issued < T && issued < D; ++issued, ic.next(tl))
     issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
           pol_w, lane);
-  {
-    Cursor pc = ic;
-    for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m, pc.next(tl)) prefetch(ra, pc.tile, pc.c, lane);
-  }
 
   if (ra.pdl) griddep_wait();
   tstamp(ra.trace, ra.tslot, TR_WAITED);
-  bool ok = load_rows<Q, A16>(ra, act, act_bar, abort_flag);
+  bool ok = load_rows<Q, A16>(ra, M, row0, act, act_bar, abort_flag);
   tstamp(ra.trace, ra.tslot, TR_ACT);
   for (; !early && issued < T && issued < D; ++issued, ic.next(tl))
     issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
@@ -463,24 +453,24 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
       }
       if (r0 < mt.N) {
         if (t0 < M) {
-          mt.y[(long)t0 * mt.N + r0] = yv[0];
+          mt.y[(long)(row0 + t0) * mt.N + r0] = yv[0];
           const unsigned long long k = amax_key(yv[0], (unsigned)r0);
           best0 = k > best0 ? k : best0;
         }
         if (t1 < M) {
-          mt.y[(long)t1 * mt.N + r0] = yv[1];
+          mt.y[(long)(row0 + t1) * mt.N + r0] = yv[1];
           const unsigned long long k = amax_key(yv[1], (unsigned)r0);
           best1 = k > best1 ? k : best1;
         }
       }
       if (r8 < mt.N) {
         if (t0 < M) {
-          mt.y[(long)t0 * mt.N + r8] = yv[2];
+          mt.y[(long)(row0 + t0) * mt.N + r8] = yv[2];
           const unsigned long long k = amax_key(yv[2], (unsigned)r8);
           best0 = k > best0 ? k : best0;
         }
         if (t1 < M) {
-          mt.y[(long)t1 * mt.N + r8] = yv[3];
+          mt.y[(long)(row0 + t1) * mt.N + r8] = yv[3];
           const unsigned long long k = amax_key(yv[3], (unsigned)r8);
           best1 = k > best1 ? k : best1;
         }
@@ -522,7 +512,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
     if (threadIdx.x < M) {
       unsigned long long m = 0;
       for (int w = 0; w < nw; ++w) m = keys[threadIdx.x * MW + w] > m ? keys[threadIdx.x * MW + w] : m;
-      a.amax[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
+      a.amax[(long)(row0 + threadIdx.x) * gridDim.x + blockIdx.x] = m;
     }
   }
   tend(ra.trace, ra.tslot, ra.ntiles * TR, 3);
@@ -551,7 +541,8 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
   extern __shared__ __align__(128) unsigned char smem[];
   const lkh::GemvProblem& a = ra.p;
   const int nw = ra.nw, NG = nw / G4, D = ra.depth, NS = NG * D;
-  const int M = a.M, K = a.K;
+  const int row0 = TN * (int)blockIdx.y;                  // this block's group of activation rows
+  const int M = a.M - row0 < TN ? a.M - row0 : TN, K = a.K;
   unsigned char* act = smem;
   unsigned char* ring = smem + ra.ring_off;
   unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
@@ -602,7 +593,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
             pol_w, lane);
   if (ra.pdl) griddep_wait();
   tstamp(ra.trace, ra.tslot, TR_WAITED);
-  bool ok = load_rows<Q, A16>(ra, act, act_bar, abort_flag);
+  bool ok = load_rows<Q, A16>(ra, M, row0, act, act_bar, abort_flag);
   tstamp(ra.trace, ra.tslot, TR_ACT);
   if (leader)
     for (; !early && issued < T && issued < D; ++issued, ic.next(tl))
@@ -697,24 +688,24 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
         const int t0 = 2 * t, t1 = 2 * t + 1;
         if (r0 < mt.N) {
           if (t0 < M) {
-            mt.y[(long)t0 * mt.N + r0] = yv[0];
+            mt.y[(long)(row0 + t0) * mt.N + r0] = yv[0];
             const unsigned long long k = amax_key(yv[0], (unsigned)r0);
             best0 = k > best0 ? k : best0;
           }
           if (t1 < M) {
-            mt.y[(long)t1 * mt.N + r0] = yv[1];
+            mt.y[(long)(row0 + t1) * mt.N + r0] = yv[1];
             const unsigned long long k = amax_key(yv[1], (unsigned)r0);
             best1 = k > best1 ? k : best1;
           }
         }
         if (r8 < mt.N) {
           if (t0 < M) {
-            mt.y[(long)t0 * mt.N + r8] = yv[2];
+            mt.y[(long)(row0 + t0) * mt.N + r8] = yv[2];
             const unsigned long long k = amax_key(yv[2], (unsigned)r8);
             best0 = k > best0 ? k : best0;
           }
           if (t1 < M) {
-            mt.y[(long)t1 * mt.N + r8] = yv[3];
+            mt.y[(long)(row0 + t1) * mt.N + r8] = yv[3];
             const unsigned long long k = amax_key(yv[3], (unsigned)r8);
             best1 = k > best1 ? k : best1;
           }
@@ -771,7 +762,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
     if (threadIdx.x < M) {
       unsigned long long m = 0;
       for (int w = 0; w < nw; ++w) m = keys[threadIdx.x * MW + w] > m ? keys[threadIdx.x * MW + w] : m;
-      a.amax[(long)threadIdx.x * gridDim.x + blockIdx.x] = m;
+      a.amax[(long)(row0 + threadIdx.x) * gridDim.x + blockIdx.x] = m;
     }
   }
   tend(ra.trace, ra.tslot, ra.ntiles * TR, 3);
@@ -797,7 +788,7 @@ unsigned round_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
 // Below 4 tiles per SM the second regime's layout is tried first.
 MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int smem_optin, bool a16) {
   MmaLayout L{};
-  const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)p.M;
+  const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)(p.M < TN ? p.M : TN);  // a block's rows
   L.a16 = a16;
   L.ar = a16 ? 2u * K + 64u : K + 32u;
   L.xsr = nb + 4u;
@@ -835,7 +826,7 @@ MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int sm
 // times faster than one warp), as many groups as fit, up to four.
 MmaLayout mma_layout_g4(const lkh::GemvProblem& p, int smem_optin, bool a16, unsigned tk_pref = 0) {
   MmaLayout L{};
-  const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)p.M;
+  const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)(p.M < TN ? p.M : TN);  // a block's rows
   L.a16 = a16;
   L.g4 = true;
   L.ar = a16 ? 2u * K + 64u : K + 32u;
@@ -933,17 +924,26 @@ namespace lkh {
 
 using namespace lkmma;
 
+// Activation-row groups of a launch of M rows, and the blocks (SMs) each
+// group gets: every group runs at once, one block per SM.
+int mma_groups(int M) { return (M + TN - 1) / TN; }
+int mma_group_blocks(int M, int sms) {
+  const int g = sms / mma_groups(M);
+  return g > 0 ? g : 1;
+}
+
 bool mma_supports(const GemvProblem& p) {
   if (p.mode != LK_INT8ACT && p.mode != LK_TWOPASS) return false;
-  if (p.split || p.fuse) return false;
+  if (p.split || p.fuse || p.F > 0) return false;
   const int min_m = opt_mma_min_m > 0 ? (int)opt_mma_min_m : 2;
-  if (p.M < min_m || p.M > TN) return false;
+  if (p.M < min_m || p.M > LK_MAX_BATCH) return false;
   if (p.K < 256 || p.K % 256 || p.N < 1) return false;
   if (!aligned(p.ws, 16) || !aligned(p.xq, 16) || !aligned(p.xs, 16) || (p.mode == LK_TWOPASS && !aligned(p.xl, 16)))
     return false;
+  // each group's rows start 16-byte aligned (K % 256 == 0) and its scales too
   const DeviceInfo* d = device_info(nullptr);
   if (!d) return false;
-  return mma_layout_ok(mma_layout(p, (p.N + TR - 1) / TR, d->sm_count, d->smem_optin));
+  return mma_layout_ok(mma_layout(p, (p.N + TR - 1) / TR, mma_group_blocks(p.M, d->sm_count), d->smem_optin));
 }
 
 // One launch over the matrices (wq[m], ws[m], N[m]) -> y[m], all reading
@@ -955,7 +955,8 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   if (nmat < 1 || nmat > MG || (nmat > 1 && p.amax)) return LK_ERR_ARG;
   long all_tiles = 0;
   for (int m = 0; m < nmat; ++m) all_tiles += (N[m] + TR - 1) / TR;
-  const MmaLayout L = mma_layout(p, all_tiles, d->sm_count, d->smem_optin);
+  const int ngrp = mma_groups(p.M), gsms = mma_group_blocks(p.M, d->sm_count);
+  const MmaLayout L = mma_layout(p, all_tiles, gsms, d->smem_optin);
   if (!mma_layout_ok(L)) return LK_ERR_SHAPE;
   mma_fn f = L.i8 ? (p.mode == LK_TWOPASS ? gemv_mma_kernel<2, false, true> : gemv_mma_kernel<1, false, true>)
            : L.g4 ? (p.mode == LK_TWOPASS ? (L.a16 ? gemv_mma_g4_kernel<2, true> : gemv_mma_g4_kernel<2, false>)
@@ -984,7 +985,7 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   if (tiles < 1) return LK_ERR_SHAPE;
   ra.nw = L.nw;
   ra.depth = L.depth;
-  long gx = opt_grid_ctas > 0 ? opt_grid_ctas : d->sm_count;
+  long gx = opt_grid_ctas > 0 ? opt_grid_ctas : gsms;
   if (gx > ra.ntiles) gx = ra.ntiles;
   ra.gx = (int)gx;
   ra.tk = L.tk;
@@ -999,15 +1000,14 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   ra.ring_off = L.ring_off;
   ra.wait_ns = opt_wait_us > 0 ? (unsigned long long)opt_wait_us * 1000ull : 2000000000ull;
   ra.pol_w = opt_ring_hint ? 1ull : 0ull;
-  ra.pdl = opt_pdl ? 1 : 0;
+  ra.pdl = p.pdl;
   ra.err = error_word_ptr();
   if (!ra.err) return LK_ERR_CUDA;
-  ra.l2_ahead = (int)(opt_l2_ahead_kb * 1024 / ((long)L.nw * L.stage_bytes));
   ra.trace = opt_trace == 3 ? trace_ptr() : nullptr;
   ra.tslot = opt_trace == 3 ? trace_next_slot() : -1;
-  ra.prefill = L.g4 ? prefill_warps(L.nw / G4) : prefill_warps(L.nw);  // groups, or warps
+  ra.prefill = L.g4 ? prefill_warps(L.nw / G4, p.prefill) : prefill_warps(L.nw, p.prefill);  // groups, or warps
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)gx);
+  cfg.gridDim = dim3((unsigned)gx, (unsigned)ngrp);
   cfg.blockDim = dim3(L.nw * 32);
   cfg.dynamicSmemBytes = L.total;
   cfg.stream = stream;

@@ -53,10 +53,10 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns, int* err) {
 
 
 namespace {
-ring_fn pick(int mode, int M, bool split, bool fuse) {
+ring_fn pick(int mode, int M, bool split, bool fuse, bool glu) {
   if (split) fuse = false;  // the fused prologue is for whole rows only
-  return mode == 0 ? ring_pick<0>(M, split, fuse) : mode == 1 ? ring_pick<1>(M, split, fuse)
-                                                              : ring_pick<2>(M, split, fuse);
+  return mode == 0 ? ring_pick<0>(M, split, fuse, glu) : mode == 1 ? ring_pick<1>(M, split, fuse, glu)
+                                                                  : ring_pick<2>(M, split, fuse, glu);
 }
 
 }  // namespace
@@ -141,6 +141,8 @@ using namespace lkring;
 
 bool ring_supports(const GemvProblem& p) {
   if (p.K < 256 || p.K % 256 || p.N < 1 || p.M < 1 || p.M > LK_MAX_M) return false;
+  // the gated pair's epilogue kernel: one activation row, whole rows
+  if (p.F > 0 && (p.M != 1 || p.split || p.fuse || p.N != 2 * p.F || p.F % 32 || !aligned(p.ws2, 16))) return false;
   if (!aligned(p.ws, 16)) return false;
   if (!p.fuse && (p.mode == 0 ? !aligned(p.x, 16)
                               : (!aligned(p.xq, 16) || !aligned(p.xs, 16) || (p.mode == 2 && !aligned(p.xl, 16)))))
@@ -162,7 +164,7 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   if (!d) return LK_ERR_CUDA;
   const Layout L = layout(p, d->smem_optin);
   if (!layout_ok(L)) return LK_ERR_SHAPE;
-  ring_fn f = pick(p.mode, p.M, p.split, p.fuse);
+  ring_fn f = pick(p.mode, p.M, p.split, p.fuse, p.F > 0);
   // The cap is the device's opt-in maximum, never this launch's size: one
   // instantiation serves launches of different sizes, and a cap lowered by a
   // later launch would make an earlier one (e.g. a node of a captured graph,
@@ -181,13 +183,12 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   ra.ring_off = L.ring_off;
   ra.wait_ns = opt_wait_us > 0 ? (unsigned long long)opt_wait_us * 1000ull : 2000000000ull;
   ra.pol_w = opt_ring_hint ? 1ull : 0ull;
-  ra.pdl = opt_pdl ? 1 : 0;
+  ra.pdl = p.pdl;
   ra.err = lkh::error_word_ptr();
   if (!ra.err) return LK_ERR_CUDA;
   ra.trace = opt_trace ? lkh::trace_ptr() : nullptr;
   ra.tslot = opt_trace == 3 ? lkh::trace_next_slot() : -1;
-  ra.l2_ahead = (int)(opt_l2_ahead_kb * 1024 / ((long)L.nwc * L.stage_bytes));
-  ra.prefill = lkh::prefill_warps(L.nwc);
+  ra.prefill = lkh::prefill_warps(L.nwc, p.prefill);
   const int S = p.split && p.S > 1 ? p.S : 1;
   const int g = opt_grid_ctas > 0 ? (int)opt_grid_ctas : d->sm_count * (opt_ring_cps > 1 ? (int)opt_ring_cps : 1);
   int gx = (g + S - 1) / S;

@@ -42,13 +42,12 @@ struct RingArgs {
   int* err;                // the device error word
   unsigned long long* trace;  // block 0's timestamps (option "trace"), or NULL
   int tslot;               // trace 3: this launch's record in the timeline, else -1
-  int l2_ahead;            // stages per warp requested into L2 beyond the ring at start
   int prefill;             // warps that fill their stages before the dependency wait
 };
 
 typedef void (*ring_fn)(const RingArgs);
 template <int Q>
-ring_fn ring_pick(int M, bool split, bool fuse);
+ring_fn ring_pick(int M, bool split, bool fuse, bool glu);
 
 // ---- PTX wrappers -------------------------------------------------------------------------
 __device__ __forceinline__ unsigned smem_u32(const void* p) {
@@ -165,12 +164,6 @@ __device__ __forceinline__ void tend(unsigned long long* tr, int slot, long rows
       tr[slot * TREC + TR_ROWS] = (unsigned long long)rows;
     }
   }
-}
-
-// Request `bytes` at `src` into L2 (no completion to wait for).  src 16-byte
-// aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -357,6 +350,15 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
 struct Geom {
   const int8_t* wq;
   const unsigned char* ws;  // f16 scales, as bytes
+  // The gated pair (F > 0): N = 2F logical rows interleaving the gate matrix
+  // (wq, ws) and the up matrix (wq2, ws2) in 32-row tiles -- logical row L is
+  // row 32 (L >> 6) + (L & 31) of the up matrix if bit 5 of L is set, else of
+  // the gate matrix -- so a group of 32 outputs' gate and up rows are 64
+  // neighbouring logical rows.  Quads are aligned to 4 rows, so a quad's rows
+  // are consecutive rows of one matrix.
+  const int8_t* wq2;
+  const unsigned char* ws2;
+  long F;
   long N;
   int K, nb;
   long r0, r1;
@@ -370,6 +372,9 @@ __device__ __forceinline__ Geom make_geom(const int8_t* wq, const void* ws, long
   Geom g;
   g.wq = wq;
   g.ws = (const unsigned char*)ws;
+  g.wq2 = nullptr;
+  g.ws2 = nullptr;
+  g.F = 0;
   g.N = N;
   g.K = K;
   g.nb = K >> 5;
@@ -385,6 +390,22 @@ __device__ __forceinline__ Geom make_geom(const int8_t* wq, const void* ws, long
   // different banks (a step's scale loads, one per row, need one wavefront)
   g.srow = (unsigned)tk / 16u + 16u;
   return g;
+}
+
+// Where logical row `row` lives: its matrix's levels and scales, and its row
+// there (the row itself unless the geometry is a gated pair).
+__device__ __forceinline__ void row_src(const Geom& g, long row, const int8_t*& wq, const unsigned char*& ws,
+                                        long& prow) {
+  if (g.F > 0) {
+    const bool up = (row >> 5) & 1;
+    wq = up ? g.wq2 : g.wq;
+    ws = up ? g.ws2 : g.ws;
+    prow = ((row >> 6) << 5) | (row & 31);
+  } else {
+    wq = g.wq;
+    ws = g.ws;
+    prow = row;
+  }
 }
 
 // Stages of warp `warp` of `nwc`: its quads are warp, warp + nwc, ...
@@ -403,13 +424,17 @@ __device__ __forceinline__ void issue_stage(const Geom& g, int warp, int nwc, lo
   const int rows = g.r1 - row0 < QR ? (int)(g.r1 - row0) : QR;
   const int k0 = g.k_lo + c * g.tk;
   const int len = (g.k_hi - k0 < g.tk) ? g.k_hi - k0 : g.tk;
+  const int8_t* wq;
+  const unsigned char* ws;
+  long prow0;
+  row_src(g, row0, wq, ws, prow0);  // the quad's rows are prow0.. of one matrix
   if (g.whole) {
     if (lane == 0) {
       mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)g.K * 17u / 16u);
-      bulk(st, g.wq + row0 * g.K, rows * g.K, full, pol);
+      bulk(st, wq + prow0 * g.K, rows * g.K, full, pol);
     }
     __syncwarp();
-    if (lane < rows) bulk(st + g.s_off + lane * g.srow, g.ws + (row0 + lane) * g.nb * 2, g.nb * 2, full, pol);
+    if (lane < rows) bulk(st + g.s_off + lane * g.srow, ws + (prow0 + lane) * g.nb * 2, g.nb * 2, full, pol);
   } else {
     const int b0 = k0 >> 5, b1 = b0 + (len >> 5);
     const unsigned sh = (unsigned)(b0 & 7) * 2u;               // scales' offset in the first 16 B
@@ -417,37 +442,12 @@ __device__ __forceinline__ void issue_stage(const Geom& g, int warp, int nwc, lo
     if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * (len + slen));
     __syncwarp();
     if (lane < rows) {
-      const long row = row0 + lane;
-      bulk(st + lane * g.tk, g.wq + row * g.K + k0, len, full, pol);
-      bulk(st + g.s_off + lane * g.srow, g.ws + ((row * g.nb + b0) * 2 - sh), slen, full, pol);
+      const long row = prow0 + lane;
+      bulk(st + lane * g.tk, wq + row * g.K + k0, len, full, pol);
+      bulk(st + g.s_off + lane * g.srow, ws + ((row * g.nb + b0) * 2 - sh), slen, full, pol);
     }
   }
   __syncwarp();
-}
-
-// Request this warp's stage n (the bytes issue_stage copies) into L2.
-__device__ __forceinline__ void prefetch_stage(const Geom& g, int warp, int nwc, long n, int lane) {
-  const long qi = warp + (long)nwc * (n / g.nsl);
-  const int c = (int)(n % g.nsl);
-  const long row0 = g.r0 + QR * qi;
-  const int rows = g.r1 - row0 < QR ? (int)(g.r1 - row0) : QR;
-  const int k0 = g.k_lo + c * g.tk;
-  const int len = (g.k_hi - k0 < g.tk) ? g.k_hi - k0 : g.tk;
-  if (g.whole) {
-    if (lane == 0) {
-      bulk_prefetch_l2(g.wq + row0 * g.K, rows * g.K);
-      bulk_prefetch_l2(g.ws + row0 * g.nb * 2, rows * g.nb * 2);
-    }
-  } else {
-    const int b0 = k0 >> 5, b1 = b0 + (len >> 5);
-    const unsigned sh = (unsigned)(b0 & 7) * 2u;
-    const unsigned slen = ((b1 - b0) * 2u + sh + 15u) & ~15u;
-    if (lane < rows) {
-      const long row = row0 + lane;
-      bulk_prefetch_l2(g.wq + row * g.K + k0, len);
-      bulk_prefetch_l2(g.ws + ((row * g.nb + b0) * 2 - sh), slen);
-    }
-  }
 }
 
 // 16-byte load from L2 (not L1): for data an earlier kernel wrote.
@@ -649,6 +649,10 @@ __device__ __forceinline__ void finish_quad(typename part_t<Q>::t (&p)[M], const
         const long idx = ((long)chunk * M + t) * g.N + o;
         if constexpr (Q == 0) a.part64[idx] = (double)v;
         else a.y[idx] = (float)v;
+      } else if (g.F > 0) {
+        // the gated pair: gate values [M][F], then up values [M][F]
+        const long prow = ((o >> 6) << 5) | (o & 31);
+        y[(((o >> 5) & 1) * M + t) * g.F + prow] = Q == 0 ? __double2float_rn((double)v) : (float)v;
       } else {
         const float yv = Q == 0 ? __double2float_rn((double)v) : (float)v;
         y[(long)t * g.N + o] = yv;
@@ -670,7 +674,46 @@ __device__ __forceinline__ void drain_wait(unsigned bar, unsigned parity, unsign
   }
 }
 
-template <int Q, int M, bool SPLIT, bool FUSE>
+// The SwiGLU epilogue of a gated pair ("kernels.rs" lk_gemv_glu with a
+// quantized output): output group j (32 outputs) needs the 64 logical rows
+// [64 j, 64 j + 64), its 32 gate and 32 up values.  A block whose rows hold
+// the whole group finishes it; a group split between two blocks is finished
+// by the one that completes its count: each adds the rows it wrote to
+// glu_cnt[j] after a fence, and the one whose add reaches 64 reads the other's
+// values back through L2 and resets the count for the next launch.  A warp
+// per group: lane l computes h = swiglu(gate, up) of output 32 j + l for every
+// activation row and quantizes the 32 values as one group.
+template <int Q, int M>
+__device__ __forceinline__ void glu_epilogue(const lkh::GemvProblem& a, const Geom& g, int nwc, int warp, int lane) {
+  __threadfence();  // this block's gate/up values before any of its counts
+  __syncthreads();
+  if (g.r1 <= g.r0) return;
+  const long F = a.F;
+  const long j0 = g.r0 >> 6, j1 = (g.r1 - 1) >> 6;
+  for (long j = j0 + warp; j <= j1; j += nwc) {
+    const long lo = g.r0 > 64 * j ? g.r0 : 64 * j, hi = g.r1 < 64 * j + 64 ? g.r1 : 64 * j + 64;
+    const int c = (int)(hi - lo);
+    if (c < 64) {
+      int old = 0;
+      if (lane == 0) old = atomicAdd(a.glu_cnt + j, c);
+      old = __shfl_sync(FULL, old, 0);
+      if (old + c != 64) continue;  // the other block finishes the group
+      if (lane == 0) a.glu_cnt[j] = 0;
+      __threadfence();  // the other block's values after its count
+    }
+#pragma unroll
+    for (int t = 0; t < M; ++t) {
+      const long i = (long)t * F + 32 * j + lane;
+      const float hv = swiglu(__ldcg(a.y + i), __ldcg(a.y + (long)M * F + i));
+      if (a.h) a.h[i] = hv;
+      if constexpr (Q > 0)
+        quant_lane<Q>(hv, a.hq + (long)t * F, Q == 2 ? a.hl + (long)t * F : nullptr, a.hs + (long)t * (F >> 5), j,
+                      lane);
+    }
+  }
+}
+
+template <int Q, int M, bool SPLIT, bool FUSE, bool GLU = false>
 __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArgs ra) {
   typedef typename part_t<Q>::t P;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -694,8 +737,16 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
     b_hi = splitk_bound(nb, a.S, blockIdx.y + 1);
   }
   const int k_lo = 32 * b_lo;
-  const Geom g = make_geom(a.wq, a.ws, N, K, (long)blockIdx.x * N / ra.gx, (long)(blockIdx.x + 1) * N / ra.gx,
-                           k_lo, 32 * b_hi, (int)ra.tk);
+  // a gated pair's rows are split in whole quads (a quad never straddles
+  // the 32-row tiles of its matrices)
+  const long q_lo = GLU ? 4 * ((long)blockIdx.x * (N >> 2) / ra.gx) : (long)blockIdx.x * N / ra.gx;
+  const long q_hi = GLU ? 4 * ((long)(blockIdx.x + 1) * (N >> 2) / ra.gx) : (long)(blockIdx.x + 1) * N / ra.gx;
+  Geom g = make_geom(a.wq, a.ws, N, K, q_lo, q_hi, k_lo, 32 * b_hi, (int)ra.tk);
+  if (GLU) {
+    g.wq2 = a.wq2;
+    g.ws2 = (const unsigned char*)a.ws2;
+    g.F = a.F;
+  }
   const unsigned L = ra.act_len;
   const long T = geom_stages(g, warp, nwc);
   const unsigned long long pol_w = ra.pol_w ? evict_first_policy() : 0ull;
@@ -718,9 +769,6 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
   for (; early && issued < T && issued < D; ++issued)
     issue_stage(g, warp, nwc, issued, ring + (size_t)(warp * D + issued % D) * ra.stage_bytes,
                 full0 + 8 * (warp * D + (int)(issued % D)), pol_w, lane);
-  // the next stages into L2, so that HBM keeps streaming while the block
-  // waits for the previous kernel and runs its prologue
-  for (long m = issued; m < T && m < issued + ra.l2_ahead; ++m) prefetch_stage(g, warp, nwc, m, lane);
   tstamp(ra.trace, ra.tslot, TR_ISSUED);
 
   // from the dependency wait on: reads of activations, writes of outputs (the
@@ -776,7 +824,11 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
       drain_wait(full0 + 8 * (unsigned)(warp * D + m % D), (unsigned)(m / D) & 1u, ra.wait_ns, ra.err);
   }
   __syncwarp();
-  if (!SPLIT && a.amax) {
+  if constexpr (GLU) {
+    __syncthreads();
+    if (!*abort_flag) glu_epilogue<Q, M>(a, g, nwc, warp, lane);
+  }
+  if (!SPLIT && !GLU && a.amax) {
 #pragma unroll
     for (int t = 0; t < M; ++t) {
       const unsigned long long wmax = warp_max_u64(best[t]);
@@ -795,7 +847,8 @@ __global__ void __launch_bounds__(THREADS_MAX, 1) gemv_ring_kernel(const RingArg
 // Explicit instantiation of every (M, SPLIT, FUSE) kernel of mode Q.
 #define LK_RING_PICK(Q)                                                             \
   template <>                                                                       \
-  ring_fn ring_pick<Q>(int M, bool split, bool fuse) {                              \
+  ring_fn ring_pick<Q>(int M, bool split, bool fuse, bool glu) {                    \
+    if (glu) return gemv_ring_kernel<Q, 1, false, false, true>;                     \
     if (split) {                                                                    \
       switch (M) {                                                                  \
         case 1: return gemv_ring_kernel<Q, 1, true, false>;                         \

@@ -1,14 +1,23 @@
 """The per-token projection sequence of a synthetic decoder, run through the
-C ABI: per layer RMSNorm -> quantize -> q, k, v; quantize -> o; RMSNorm ->
-quantize -> fused gate/up; quantize -> down; then RMSNorm -> quantize ->
-lm-head with the argmax epilogue -> argmax.
+C ABI.  Two dataflows:
 
-Attention and the gated activation are not part of the projection path, so
-the inputs they would produce are fixed seeded vectors: the o-projection's and
-the down-projection's inputs are N(0,1) with 1% x20 outliers, one per layer,
-quantized every token.  The residual stream is the chain of projection
-outputs: the o output feeds the MLP norm and the down output feeds the next
-layer's attention norm.
+glu=True (a pre-norm decoder layer):
+    x = norm(h) -> q, k, v;  quantize(o_in) -> o;
+    h' = h + o, x = norm(h') -> gate/up -> SwiGLU -> quantize -> down;
+    h'' = h' + down, x = norm(h'') -> next layer (the last: the lm-head norm)
+  the residual add, norm and quantizer run as one launch
+  (lk_add_rmsnorm_quant) and the SwiGLU with its quantizer runs in the
+  gate/up launch's epilogue (lk_gemv_q8_glu);
+glu=False (the default: the projections alone):
+    norm -> quantize -> q, k, v; quantize -> o; norm -> quantize -> fused
+    gate/up; quantize -> down; the o output feeds the MLP norm and the down
+    output the next layer's norm, with no residual add.
+Then RMSNorm -> quantize -> lm-head with the argmax epilogue -> argmax.
+
+Attention is not part of the projection path, so the input it would produce
+for the o projection is a fixed seeded vector (N(0,1) with 1% x20 outliers,
+one per layer) quantized every token; with glu=False the down projection's
+input is such a vector too.
 
 Weights live on the device for the life of the object (about 8 GB for the
 36-layer, hidden-4096 configuration); every buffer is allocated once here and
@@ -24,7 +33,7 @@ from . import lk, synth
 class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
                  batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
-                 fused=False, chain=False, group_qkv=True, prefill=None):
+                 fused=False, chain=False, group_qkv=True, prefill=None, glu=False):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
         # per projection: warps of a ring GEMV block that fill their stages
@@ -32,12 +41,20 @@ class DecodeStack:
         self.prefill = dict(prefill or {})
         dev = self.dev
         s = seed
+        # the gated pair runs as one fused launch; the chain and fused-prologue
+        # forms keep the projections-alone dataflow
+        self.glu = bool(glu) and not chain and not fused
         self.shapes = {"q": (q_dim, hidden), "k": (kv_dim, hidden), "v": (kv_dim, hidden),
                        "o": (hidden, q_dim), "gu": (2 * ffn, hidden), "down": (hidden, ffn)}
         self.layers = []
         for l in range(layers):
             w = {}
             for i, (name, (N, K)) in enumerate(self.shapes.items()):
+                if name == "gu" and self.glu:
+                    # the gate and up matrices of the pair (ffn rows each)
+                    w["gate"] = synth.q8_matrix_torch(ffn, hidden, s + 1000 * l + i, dev)
+                    w["up"] = synth.q8_matrix_torch(ffn, hidden, s + 1000 * l + 20 + i, dev)
+                    continue
                 w[name] = synth.q8_matrix_torch(N, K, s + 1000 * l + i, dev)
             w["g_attn"] = synth.norm_gain_torch(hidden, s + 1000 * l + 10, dev)
             w["g_mlp"] = synth.norm_gain_torch(hidden, s + 1000 * l + 11, dev)
@@ -54,6 +71,11 @@ class DecodeStack:
         self.xn = torch.empty((B, hidden), dtype=f32, device=dev)       # normed (Dequant GEMV input)
         self.acts = {K: self._act_bufs(K) for K in {hidden, q_dim, ffn}}
         self.out = {name: torch.empty((B, N), dtype=f32, device=dev) for name, (N, _) in self.shapes.items()}
+        if self.glu:
+            self.hbuf = [torch.empty((B, hidden), dtype=f32, device=dev) for _ in range(2)]  # residual stream
+            self.gu_buf = torch.empty((2, B, ffn), dtype=f32, device=dev)   # gate and up values
+            self.hglu = torch.empty((B, ffn), dtype=f32, device=dev)        # SwiGLU output (Dequant input)
+            self.glu_cnt = torch.zeros((ffn // 32,), dtype=torch.int32, device=dev)
         self.logits = torch.empty((B, vocab), dtype=f32, device=dev)
         self.parts = torch.zeros((B * lk.lk_argmax_parts_max(vocab),), dtype=torch.int64, device=dev)
         self.idx = torch.empty((B,), dtype=torch.int32, device=dev)
@@ -106,6 +128,16 @@ class DecodeStack:
         lk.lk_rmsnorm_quant(x, g, self.mode, self.eps, None, a["xq"], a.get("xl"), a["xs"])
         return a
 
+    def _add_norm(self, x, r, s, g):
+        """s = x + r, then RMSNorm -> quantize of s (one launch); returns the
+        GEMV activation arguments."""
+        if self.mode == lk.LK_DEQUANT:
+            lk.lk_add_rmsnorm_quant(x, r, g, self.mode, self.eps, s=s, xn=self.xn)
+            return {"x": self.xn}
+        a = self.acts[x.shape[1]]
+        lk.lk_add_rmsnorm_quant(x, r, g, self.mode, self.eps, s=s, xq=a["xq"], xl=a.get("xl"), xs=a["xs"])
+        return a
+
     def _quant(self, x):
         if self.mode == lk.LK_DEQUANT:
             return {"x": x}
@@ -148,12 +180,42 @@ class DecodeStack:
                                argmax_parts=self.parts, argmax_idx=self.idx, wait=True))
         return ops
 
+    def _run_token_glu(self, hook):
+        """The pre-norm decoder layer dataflow (glu=True)."""
+        def launch(name, fn):
+            return fn() if hook is None else hook(name, fn)
+
+        m, B, L = self.mode, self.B, self.L
+        a_h = self._norm(self.x_buf, self.layers[0]["g_attn"])
+        h_cur = self.x_buf
+        for l, w in enumerate(self.layers):
+            launch("qkv", lambda w=w, a=a_h: lk.lk_gemv_q8_group(
+                [(w[n][0], w[n][1], self.out[n]) for n in ("q", "k", "v")], m, M=B, **a))
+            a_o = self._quant(w["o_in"])
+            launch("o", lambda w=w, a=a_o: self._gemv(w["o"], self.out["o"], a))
+            h_mid = self.hbuf[0]
+            a_m = self._add_norm(self.out["o"], h_cur, h_mid, w["g_mlp"])
+            a_d = {"x": self.hglu} if m == lk.LK_DEQUANT else self.acts[self.F]
+            launch("gu", lambda w=w, a=a_m, d=a_d: lk.lk_gemv_q8_glu(
+                w["gate"][0], w["gate"][1], w["up"][0], w["up"][1], m, self.gu_buf, h=self.hglu,
+                hq=d.get("xq"), hl=d.get("xl"), hs=d.get("xs"), cnt=self.glu_cnt, M=B, **a))
+            launch("down", lambda w=w, d=a_d: self._gemv(w["down"], self.out["down"], d))
+            h_next = self.hbuf[1]
+            g_next = self.layers[l + 1]["g_attn"] if l + 1 < L else self.g_final
+            a_h = self._add_norm(self.out["down"], h_mid, h_next, g_next)
+            h_cur = h_next
+        self.n_parts = launch("lm", lambda: self._gemv(self.lm, self.logits, a_h, self.parts))
+        lk.lk_argmax(self.idx, B, self.V, parts=self.parts, n_parts=self.n_parts)
+        return self.idx
+
     def run_token(self, x_in=None, hook=None):
         """Launch one token's sequence on the current stream and return the
         device int32 [B] argmax.  ``hook``, if given, is called as
         hook(name, launch) around each GEMV launch (for per-kernel timing)."""
         if x_in is not None and x_in.data_ptr() != self.x_buf.data_ptr():
             self.x_buf.copy_(x_in)
+        if self.glu:
+            return self._run_token_glu(hook)
         if self.chain is not None and hook is None:
             lk.lk_gemv_chain(self.chain, self.mode, self.B, self.eps)
             return self.idx
@@ -208,12 +270,27 @@ class DecodeStack:
         if name == "lm":
             return mb(self.V, self.H)
         if name is not None:
-            return mb(*self.shapes[name])
+            return mb(*self.shapes[name])  # "gu": the gate/up pair together
         return self.L * sum(mb(N, K) for N, K in self.shapes.values()) + mb(self.V, self.H)
+
+    def glu_launches(self):
+        """Launches of the gate/up pair: one (the ring kernel's SwiGLU
+        epilogue) at one activation row where the ring kernel takes the
+        shape, else the grouped GEMVs and the SwiGLU kernel."""
+        prev = lk.lk_get_option("gemv_path")
+        lk.lk_set_option("gemv_path", 2)
+        ring = lk.lk_gemv_kernel_for(2 * self.F, self.H, self.mode, 1, 0) == 2
+        lk.lk_set_option("gemv_path", prev)
+        return 1 if (self.B == 1 and ring and prev == 0) else 2
 
     def launches_per_token(self):
         if self.chain is not None:
             return 1
+        if self.glu:
+            # first norm; per layer q/k/v, [quantize], o, add+norm, gate/up
+            # pair, down, add+norm; lm-head, argmax
+            per_layer = 5 + (0 if self.mode == lk.LK_DEQUANT else 1) + self.glu_launches()
+            return 1 + self.L * per_layer + 2
         n = 1  # argmax reduce
         f = self.fused
         qkv_norm = 0 if (f["q"] and f["k"] and f["v"]) else 1  # one shared norm for q, k, v

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "liblk.so")
 LK_DEQUANT, LK_INT8ACT, LK_TWOPASS = 0, 1, 2
 MODES = {"dequant": LK_DEQUANT, "int8act": LK_INT8ACT, "twopass": LK_TWOPASS}
 LK_MAX_M = 8
+LK_MAX_BATCH = 64
 LK_MAX_SPLITK = 64
 
 STATUS = {0: "LK_OK", -1: "LK_ERR_ARG", -2: "LK_ERR_ALIGN", -3: "LK_ERR_SHAPE",
@@ -37,6 +38,21 @@ class LkGemvTarget(ctypes.Structure):
     """One matrix of lk_gemv_q8_group (the C struct lk_gemv_target)."""
     _fields_ = [("wq", ctypes.c_void_p), ("ws", ctypes.c_void_p), ("N", ctypes.c_int), ("reserved", ctypes.c_int),
                 ("y", ctypes.c_void_p)]
+
+
+class LkLaunchCfg(ctypes.Structure):
+    """Per-call launch settings (the C struct lk_launch_cfg)."""
+    _fields_ = [("pdl", ctypes.c_int), ("prefill", ctypes.c_int)]
+
+
+def launch_cfg(pdl=-1, prefill=0) -> LkLaunchCfg:
+    """lk_launch_cfg: pdl -1 (the process option) / 0 / 1; prefill 0 (the
+    default) or the warps that fill their stages before the dependency wait."""
+    return LkLaunchCfg(int(pdl), int(prefill))
+
+
+def _cfg(cfg):
+    return None if cfg is None else ctypes.byref(cfg)
 
 
 class LkError(RuntimeError):
@@ -81,6 +97,12 @@ def _load():
         "lk_argmax_noalloc": ([P, I, I, P, P], I),
         "lk_gemv_chain": ([P, P, I, I, I, F, P, P], I),
         "lk_gemv_q8_group": ([P, I, I, I, P, P, P, P, I, P], I),
+        "lk_add_rmsnorm_quant": ([P, P, P, I, I, F, I, P, P, P, P, P, P], I),
+        "lk_swiglu_quant": ([P, P, I, I, L, I, P, P, P, P, P], I),
+        "lk_gemv_q8_glu": ([P, P, P, P, I, I, I, P, P, P, P, I, P, P, P, P, P, P, P], I),
+        "lk_gemv_q8_ex": ([P, P, I, I, I, P, P, P, P, I, P, P, P, P, P], I),
+        "lk_gemv_q8_group_ex": ([P, I, I, I, P, P, P, P, I, P, P], I),
+        "lk_gemv_q8_glu_ex": ([P, P, P, P, I, I, I, P, P, P, P, I, P, P, P, P, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -96,7 +118,8 @@ def exported_symbols():
             "lk_argmax_parts_max", "lk_argmax_scratch_entries", "lk_argmax", "lk_q8_block_dots",
             "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout", "lk_gemv_kernel_for",
             "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain", "lk_trace_read",
-            "lk_argmax_noalloc", "lk_gemv_q8_group"]
+            "lk_argmax_noalloc", "lk_gemv_q8_group", "lk_add_rmsnorm_quant", "lk_swiglu_quant",
+            "lk_gemv_q8_glu", "lk_gemv_q8_ex", "lk_gemv_q8_group_ex", "lk_gemv_q8_glu_ex"]
 
 
 def _ok(st, where):
@@ -150,6 +173,42 @@ def lk_rmsnorm_quant(x, gain, mode, eps=1e-6, xn=None, xq=None, xl=None, xs=None
                                  _ptr(xs, _F32, "xs"), _stream(stream)), "lk_rmsnorm_quant")
 
 
+def lk_add_rmsnorm_quant(x, r, gain, mode, eps=1e-6, s=None, xn=None, xq=None, xl=None, xs=None, stream=None):
+    """s = x + r (optional output), then lk_rmsnorm_quant of the sum."""
+    M, K = x.shape
+    if tuple(r.shape) != (M, K):
+        raise ValueError("r must have the shape of x")
+    _ok(_load().lk_add_rmsnorm_quant(_ptr(x, _F32, "x"), _ptr(r, _F32, "r"), _ptr(gain, _F32, "gain"), M, K, eps,
+                                     _mode(mode), _ptr(s, _F32, "s"), _ptr(xn, _F32, "xn"), _ptr(xq, _I8, "xq"),
+                                     _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), _stream(stream)),
+        "lk_add_rmsnorm_quant")
+
+
+def _pitched_rows(t, name):
+    """Pointer and row pitch (elements) of a 2-D f32 CUDA tensor whose rows
+    are contiguous (a column slice of a wider row-major tensor is fine)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != _F32 or t.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D float32 CUDA tensor")
+    if t.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()), t.stride(0)
+
+
+def lk_swiglu_quant(gate, up, mode, h=None, hq=None, hl=None, hs=None, stream=None):
+    """h = silu(gate) * up, quantized for the next GEMV.  gate and up are
+    [M, F] f32 with contiguous rows and the same row pitch (e.g. the two
+    halves gu[:, :F], gu[:, F:] of a fused gate/up output)."""
+    M, F = gate.shape
+    if tuple(up.shape) != (M, F):
+        raise ValueError("up must have the shape of gate")
+    pg, ldg = _pitched_rows(gate, "gate")
+    pu, ldu = _pitched_rows(up, "up")
+    if ldg != ldu:
+        raise ValueError("gate and up must have the same row pitch")
+    _ok(_load().lk_swiglu_quant(pg, pu, M, F, ldg, _mode(mode), _ptr(h, _F32, "h"), _ptr(hq, _I8, "hq"),
+                                _ptr(hl, _I8, "hl"), _ptr(hs, _F32, "hs"), _stream(stream)), "lk_swiglu_quant")
+
+
 def lk_quantize_act(x, mode, xq, xl, xs, stream=None):
     M, K = x.shape
     _ok(_load().lk_quantize_act(_ptr(x, _F32, "x"), M, K, _mode(mode), _ptr(xq, _I8, "xq"),
@@ -158,23 +217,25 @@ def lk_quantize_act(x, mode, xq, xl, xs, stream=None):
 
 
 def lk_gemv_q8(wq, ws, mode, y, x=None, xq=None, xl=None, xs=None, argmax_parts=None, M=None,
-               stream=None) -> int:
+               stream=None, cfg=None) -> int:
     """y[M, N] = W x.  Returns the number of argmax partial keys written per
-    activation row (0 when argmax_parts is None)."""
+    activation row (0 when argmax_parts is None).  cfg: launch_cfg(...) for
+    lk_gemv_q8_ex."""
     N, K = wq.shape
     if M is None:
         M = (x if x is not None else xq).shape[0]
     n = ctypes.c_int(0)
-    _ok(_load().lk_gemv_q8(_ptr(wq, _I8, "wq"), _ptr(ws, _WS, "ws"), N, K, _mode(mode),
-                           _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"),
-                           _ptr(xs, _F32, "xs"), M, _ptr(y, _F32, "y"),
-                           _ptr(argmax_parts, torch.int64, "argmax_parts"),
-                           ctypes.byref(n) if argmax_parts is not None else None, _stream(stream)),
-        "lk_gemv_q8")
+    args = [_ptr(wq, _I8, "wq"), _ptr(ws, _WS, "ws"), N, K, _mode(mode), _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"),
+            _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), M, _ptr(y, _F32, "y"),
+            _ptr(argmax_parts, torch.int64, "argmax_parts"), ctypes.byref(n) if argmax_parts is not None else None]
+    if cfg is None:
+        _ok(_load().lk_gemv_q8(*args, _stream(stream)), "lk_gemv_q8")
+    else:
+        _ok(_load().lk_gemv_q8_ex(*args, _cfg(cfg), _stream(stream)), "lk_gemv_q8_ex")
     return n.value
 
 
-def lk_gemv_q8_group(mats, mode, x=None, xq=None, xl=None, xs=None, M=None, stream=None):
+def lk_gemv_q8_group(mats, mode, x=None, xq=None, xl=None, xs=None, M=None, stream=None, cfg=None):
     """mats: [(wq, ws, y), ...] sharing K and the activation: y = W x for
     each, with the bits of one lk_gemv_q8 call per matrix; one launch where
     the tensor-core kernel (2..8 rows) or, for two or more matrices, the
@@ -187,9 +248,34 @@ def lk_gemv_q8_group(mats, mode, x=None, xq=None, xl=None, xs=None, M=None, stre
     for wq, _, _ in mats:
         if wq.shape[1] != K:
             raise ValueError("lk_gemv_q8_group: matrices of one group share K")
-    _ok(_load().lk_gemv_q8_group(ctypes.cast(arr, ctypes.c_void_p), len(mats), K, _mode(mode),
-                                 _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"),
-                                 M, _stream(stream)), "lk_gemv_q8_group")
+    args = [ctypes.cast(arr, ctypes.c_void_p), len(mats), K, _mode(mode), _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"),
+            _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), M]
+    if cfg is None:
+        _ok(_load().lk_gemv_q8_group(*args, _stream(stream)), "lk_gemv_q8_group")
+    else:
+        _ok(_load().lk_gemv_q8_group_ex(*args, _cfg(cfg), _stream(stream)), "lk_gemv_q8_group_ex")
+
+
+def lk_gemv_q8_glu(wg, wsg, wu, wsu, mode, gu, x=None, xq=None, xl=None, xs=None, h=None, hq=None, hl=None,
+                   hs=None, cnt=None, M=None, stream=None, cfg=None):
+    """g = Wg x, u = Wu x into gu [2, M, F]; h = silu(g) * u (optional f32
+    [M, F]) and its quantized words hq/hl/hs for the next GEMV.  cnt: int32
+    [F/32] zeroed counters (enables the one-launch kernel at M = 1)."""
+    F, K = wg.shape
+    if tuple(wu.shape) != (F, K):
+        raise ValueError("the gate and up matrices must have the same shape")
+    if M is None:
+        M = (x if x is not None else xq).shape[0]
+    if tuple(gu.shape) != (2, M, F):
+        raise ValueError("gu must be [2, M, F]")
+    args = [_ptr(wg, _I8, "wg"), _ptr(wsg, _WS, "wsg"), _ptr(wu, _I8, "wu"), _ptr(wsu, _WS, "wsu"), F, K,
+            _mode(mode), _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), M,
+            _ptr(gu, _F32, "gu"), _ptr(h, _F32, "h"), _ptr(hq, _I8, "hq"), _ptr(hl, _I8, "hl"), _ptr(hs, _F32, "hs"),
+            _ptr(cnt, torch.int32, "cnt")]
+    if cfg is None:
+        _ok(_load().lk_gemv_q8_glu(*args, _stream(stream)), "lk_gemv_q8_glu")
+    else:
+        _ok(_load().lk_gemv_q8_glu_ex(*args, _cfg(cfg), _stream(stream)), "lk_gemv_q8_glu_ex")
 
 
 def lk_gemv_kernel_for(N, K, mode, M, S=0) -> int:

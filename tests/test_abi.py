@@ -98,7 +98,7 @@ def test_norm_quant_argmax_checks(lib):
     assert r(P(FAKE), P(FAKE), 1, 64, 1e-6, 2, None, P(FAKE), None, P(FAKE), None) == -1
     q = lib.lk_quantize_act
     assert q(P(FAKE), 1, 64, 0, P(FAKE), None, P(FAKE), None) == -1  # nothing to quantize
-    assert q(P(FAKE), 9, 64, 1, P(FAKE), None, P(FAKE), None) == -3
+    assert q(P(FAKE), 65, 64, 1, P(FAKE), None, P(FAKE), None) == -3  # M <= LK_MAX_BATCH
     a = lib.lk_argmax
     assert a(P(FAKE), None, 0, 1, 0, P(FAKE), P(FAKE), None) == -3  # N >= 1
     assert a(P(FAKE), None, 0, 1, 10, P(FAKE), None, None) == -1    # logits form needs scratch
@@ -110,7 +110,8 @@ def test_norm_quant_argmax_checks(lib):
 def test_kernel_choice_without_gpu(lib):
     # invalid shapes answer 0 before any device query
     assert lk.lk_gemv_kernel_for(64, 48, 1, 1, 0) == 0
-    assert lk.lk_gemv_kernel_for(64, 64, 1, 9, 0) == 0
+    assert lk.lk_gemv_kernel_for(64, 64, 1, 9, 0) == 0      # past 8 rows: the tensor-core path only
+    assert lk.lk_gemv_kernel_for(4096, 4096, 1, 65, 0) == 0  # past LK_MAX_BATCH
     lk.lk_set_option("gemv_path", 1)
     assert lk.lk_gemv_kernel_for(64, 4096, 1, 1, 0) == 1
     lk.lk_set_option("gemv_path", 0)
@@ -130,7 +131,7 @@ def test_options(lib):
 @pytest.mark.parametrize("name,good,bad", [("gemv_path", [0, 3], [-1, 4]), ("mma_min_m", [0, 2, 9], [-1, 10]),
                                            ("mma_tk", [0, 256, 1024, 8192], [100, 8448, -256]),
                                            ("mma_warps", [0, 1, 16], [17, -1]), ("mma_depth", [0, 1, 8], [9, -1]),
-                                           ("mma_act16", [0, 1, 2], [3, -1]), ("l2_ahead_kb", [0, 64], [-1]),
+                                           ("mma_act16", [0, 1, 2], [3, -1]),
                                            ("ring_prefill", [0, 1, 12], [13, -1]),
                                            ("mma_group", [0, 1, 4], [2, 3, 5, -1]),
                                            ("mma_i8", [0, 1, 2], [3, -1]),
@@ -167,3 +168,48 @@ def test_group_argument_checks(lib):
     assert call(targets(good), 1, K=48) == -3             # K % 32
     assert call(targets(good), 1, M=9) == -3
     assert call(targets(good), 1, mode=2, xl=None) == -1  # TwoPass needs the low words
+
+
+def test_add_rmsnorm_quant_checks(lib):
+    f = lib.lk_add_rmsnorm_quant
+    n = 4 * 256  # M x K floats
+
+    def call(x=FAKE, r=FAKE + 16 * n, g=FAKE + 32 * n, M=4, K=256, mode=1, s=FAKE + 48 * n, xn=None,
+             xq=FAKE + 64 * n, xl=None, xs=FAKE + 80 * n):
+        return f(P(x), P(r) if r else None, P(g) if g else None, M, K, 1e-6, mode, P(s) if s else None,
+                 P(xn) if xn else None, P(xq) if xq else None, P(xl) if xl else None, P(xs) if xs else None, None)
+
+    assert call(K=48) == -3
+    assert call(M=65) == -3
+    assert call(mode=3) == -1
+    assert call(r=None) == -1 and call(g=None) == -1
+    assert call(xq=None) == -1                  # the quantized output is required
+    assert call(mode=2) == -1                   # TwoPass needs the low words
+    assert call(mode=0) == -1                   # Dequant needs the normed rows
+    assert call(x=FAKE + 2) == -2
+    assert call(s=FAKE + 2) == -2
+    # the new residual stream may not overlap either operand
+    assert call(s=FAKE) == -1
+    assert call(s=FAKE + 4 * n - 4) == -1       # last element of x
+    assert call(s=FAKE + 16 * n + 8) == -1      # inside r
+    assert call(M=0) == 0 and call(K=0) == 0
+
+
+def test_swiglu_quant_checks(lib):
+    f = lib.lk_swiglu_quant
+
+    def call(gate=FAKE, up=FAKE + 4096, M=2, F=1024, ld=2048, mode=1, h=None, hq=FAKE + 65536, hl=None,
+             hs=FAKE + 131072):
+        return f(P(gate) if gate else None, P(up) if up else None, M, F, ld, mode, P(h) if h else None,
+                 P(hq) if hq else None, P(hl) if hl else None, P(hs) if hs else None, None)
+
+    assert call(F=48) == -3                     # F % 32
+    assert call(ld=512) == -3                   # pitch below the row length
+    assert call(M=65) == -3
+    assert call(mode=5) == -1
+    assert call(gate=None) == -1
+    assert call(mode=0) == -1                   # Dequant needs h
+    assert call(mode=2) == -1                   # TwoPass needs the low words
+    assert call(hq=None) == -1
+    assert call(hs=FAKE + 2) == -2
+    assert call(M=0) == 0 and call(F=0) == 0

@@ -193,3 +193,60 @@ def test_group_matches_single_calls_and_oracle(mode, M, Ns, group):
         assert np.array_equal(bits(host(y)), bits(y_or))
         y1, _, _ = gpu_gemv(wd, sd, mode, acts, M)
         assert np.array_equal(bits(host(y1)), bits(host(y)))
+
+
+# ---- more than 8 activation rows -------------------------------------------------------
+
+@pytest.mark.parametrize("path", ["f16", "f16-g4", "i8"])
+@pytest.mark.parametrize("mode", [I8, TP])
+@pytest.mark.parametrize("M", [9, 16, 33, 64])
+@pytest.mark.parametrize("N,K", [(16, 256), (1000, 1280), (2500, 4096)])
+def test_mma_batches_past_eight_rows(path, mode, M, N, K):
+    """Groups of 8 activation rows side by side on the SMs: every value bit for
+    bit the oracle's (the 8-row arithmetic), the argmax of every row, with
+    ragged row groups (9, 33) and ragged tiles."""
+    lk.lk_set_option("mma_i8", 1 if path == "i8" else 2)
+    lk.lk_set_option("mma_group", 4 if "g4" in path else 1)
+    run_case(N, K, M, mode, 9100 + N + K + M, amax=True)
+
+
+@pytest.mark.parametrize("mode", [I8, TP])
+def test_batch_past_eight_matches_groups_of_eight(mode):
+    """M = 24 in one launch equals three launches of 8 rows, bit for bit, and
+    the grouped call (q, k, v) at 24 rows equals per-matrix calls."""
+    lk.lk_set_option("gemv_path", 0)
+    N, K, M = 2048, 4096, 24
+    wq, ws = synth.q8_matrix(N, K, 91)
+    x = synth.activation(M, K, 92, outliers=True)
+    acts = dev_acts(x, mode)
+    wq_d, ws_d = to_dev(wq), to_dev(ws)
+    y, _, _ = gpu_gemv(wq_d, ws_d, mode, acts, M)
+    parts = []
+    for r in range(0, M, 8):
+        sub = {k: (v[r:r + 8].contiguous() if v is not None else None) for k, v in acts.items()}
+        yy, _, _ = gpu_gemv(wq_d, ws_d, mode, sub, 8)
+        parts.append(yy)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), torch.cat(parts).view(torch.int32))
+    mats = [(wq_d, ws_d, torch.empty((M, N), dtype=torch.float32, device=DEV)),
+            (wq_d[:1024], ws_d[:1024], torch.empty((M, 1024), dtype=torch.float32, device=DEV))]
+    lk.lk_gemv_q8_group(mats, mode, M=M, **acts)
+    torch.cuda.synchronize()
+    assert torch.equal(mats[0][2].view(torch.int32), y.view(torch.int32))
+    assert torch.equal(mats[1][2].view(torch.int32), y[:, :1024].contiguous().view(torch.int32))
+
+
+def test_past_eight_rows_needs_the_tensor_core_path():
+    """Past 8 rows only the tensor-core kernel runs: Dequant, split-K and
+    K % 256 != 0 are shape errors, not silent fallbacks."""
+    lk.lk_set_option("gemv_path", 0)
+    assert lk.lk_gemv_kernel_for(4096, 4096, I8, 64, 0) == 3
+    assert lk.lk_gemv_kernel_for(4096, 4096, I8, 65, 0) == 0
+    assert lk.lk_gemv_kernel_for(4096, 4096, 0, 16, 0) == 0
+    assert lk.lk_gemv_kernel_for(4096, 1056, I8, 16, 0) == 0
+    assert lk.lk_gemv_kernel_for(4096, 4096, I8, 16, 2) == 0
+    wq, ws = to_dev(np.zeros((64, 1056), np.int8)), to_dev(np.zeros((64, 33), np.uint16))
+    x = to_dev(np.zeros((16, 1056), np.float32))
+    y = torch.empty((16, 64), dtype=torch.float32, device=DEV)
+    with pytest.raises(lk.LkError):
+        lk.lk_gemv_q8(wq, ws, 0, y, x=x, M=16)

@@ -25,7 +25,7 @@ def _lib():
 
 @pytest.mark.parametrize("batch", [1, 8])
 def test_timeline_records(batch):
-    st = DecodeStack(**SMALL, batch=batch, mode=1)
+    st = DecodeStack(**SMALL, batch=batch, mode=1, glu=False)
     st.run_token()
     torch.cuda.synchronize()
     ref = st.logits.clone()
@@ -55,3 +55,25 @@ def test_timeline_records(batch):
     ends = [r[3] for r in used]
     # launch order: each launch ends no earlier than its predecessor starts
     assert all(ends[i] >= starts[i - 1] for i in range(1, len(used)))
+
+
+def test_timeline_records_glu_token():
+    """The decoder dataflow at batch 1: first norm, then per layer q/k/v,
+    quantize, o, add+norm, the gate/up pair with its SwiGLU epilogue (one ring
+    launch), down, add+norm; then the lm-head."""
+    st = DecodeStack(**SMALL, batch=1, mode=1, glu=True)
+    assert st.glu and st.glu_launches() == 1
+    st.run_token()
+    torch.cuda.synchronize()
+    ref = st.logits.clone()
+    lk.lk_set_option("trace", 3)
+    try:
+        st.run_token()
+        torch.cuda.synchronize()
+    finally:
+        lk.lk_set_option("trace", 0)
+    assert torch.equal(st.logits.view(torch.int32), ref.view(torch.int32))
+    raw = lk.lk_trace_read(4096)
+    n = st.launches_per_token() - 1
+    kinds = [raw[i * 8 + 5] for i in range(n)]
+    assert kinds == [4] + [2, 5, 1, 4, 1, 1, 4] * SMALL["layers"] + [1]
