@@ -73,6 +73,8 @@ def _load():
     lib.oracle_swiglu.argtypes = [P, P, i64, P]
     lib.oracle_set_threads.argtypes = [i32]
     lib.oracle_set_threads.restype = i32
+    lib.oracle_get_threads.argtypes = []
+    lib.oracle_get_threads.restype = i32
     lib.oracle_argmax.argtypes = [P, i64]
     lib.oracle_argmax.restype = i64
     _lib = lib
@@ -93,6 +95,11 @@ def set_threads(n: int) -> int:
     single-threaded oracle; any count gives the same bits).  Returns the
     count in effect."""
     return _load().oracle_set_threads(int(n))
+
+
+def get_threads() -> int:
+    """Host threads the GEMV row loops use now."""
+    return _load().oracle_get_threads()
 
 
 def half_to_float(h) -> np.ndarray:

@@ -48,6 +48,7 @@ int oracle_set_threads(int n)
 #endif
     return or_threads;
 }
+int oracle_get_threads(void) { return or_threads; }
 
 #define OR_DEQUANT 0
 #define OR_INT8ACT 1

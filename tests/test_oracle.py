@@ -460,6 +460,7 @@ def test_threads_give_the_same_bits():
     wq, ws = synth.q8_matrix(301, 512, 51)
     x = synth.activation(2, 512, 52, outliers=True)
     outs = {}
+    prev = oracle.get_threads()
     for n in (1, 4):
         assert oracle.set_threads(n) == n
         try:
@@ -470,7 +471,7 @@ def test_threads_give_the_same_bits():
                 r.extend(oracle.gemv_splitk(wq, ws, mode, 3, **a))
             r.append(oracle.absdot(wq, ws, x))
         finally:
-            oracle.set_threads(1)
+            oracle.set_threads(prev)
         outs[n] = r
     for a, b in zip(outs[1], outs[4]):
         assert a.dtype == b.dtype and np.array_equal(a.view(np.uint8), b.view(np.uint8))
