@@ -86,10 +86,40 @@ __device__ __forceinline__ float warp_absmax(float v) {
   return __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(fabsf(v))));
 }
 
+// ---- IEEE quotients of the quantizer without the division sequence --------
+// a / 127 for finite a >= 0, correctly rounded: Markstein's correction step
+// (P. Markstein, IBM J. Res. Develop. 34(1), 1990) from r = RN(1/127):
+// q0 = RN(a r), rem = fma(-q0, 127, a), q = fma(rem, r, q0).  Checked equal to
+// the IEEE quotient for every finite non-negative binary32 on the host
+// (tests/csrc/div127_check.c), with the same IEEE binary32 operations.
+__device__ __forceinline__ float div127(float a) {
+  const float r = 0x1.020408p-7f;
+  const float q0 = __fmul_rn(a, r);
+  return __fmaf_rn(__fmaf_rn(-q0, 127.0f, a), r, q0);
+}
+
+// rn(v / s) as an integer, |v / s| < 129, with rs an approximate 1/s (the
+// hardware reciprocal, relative error below 2^-22): qa = RN(v rs) is within
+// 129 (2^-22 + 2^-24) < 2^-14 of v / s, and RN(v / s) within 2^-18 of it, so
+// unless qa lies within 2^-12 of a half-integer both round to the same
+// integer; near one (a tie or close: about 1 value in 2000) the IEEE
+// quotient decides.
+__device__ __forceinline__ float approx_rcp(float s) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+__device__ __forceinline__ int rn_quot(float v, float s, float rs) {
+  const float qa = __fmul_rn(v, rs);
+  const float m = fabsf(qa);
+  if (fabsf(__fsub_rn(__fsub_rn(m, floorf(m)), 0.5f)) < 0x1p-12f) return __float2int_rn(__fdiv_rn(v, s));
+  return __float2int_rn(qa);
+}
+
 template <int Q>
 __device__ __forceinline__ float act_scale(float a) {
-  if constexpr (Q == 1) return a >= kInt8ActMinMax ? __fdiv_rn(a, 127.0f) : 1.0f;
-  return __fdiv_rn(fmaxf(a, 1e-30f), 127.0f);
+  if constexpr (Q == 1) return a >= kInt8ActMinMax ? div127(a) : 1.0f;
+  return div127(fmaxf(a, 1e-30f));
 }
 
 __device__ __forceinline__ int sat_i8(int v) { return min(max(v, -128), 127); }
@@ -101,18 +131,24 @@ template <int Q, int NG>
 __device__ __forceinline__ void quant_groups(const float (&v)[NG], const bool (&ok)[NG], int8_t* __restrict__ hi,
                                              int8_t* __restrict__ lo, float* __restrict__ xs, long g, long step,
                                              int lane) {
-  float s[NG];
+  float s[NG], rs[NG];
   int h[NG], l[NG];
 #pragma unroll
-  for (int k = 0; k < NG; ++k) s[k] = act_scale<Q>(warp_absmax(v[k]));
+  for (int k = 0; k < NG; ++k) {
+    s[k] = act_scale<Q>(warp_absmax(v[k]));
+    rs[k] = approx_rcp(s[k]);
+  }
+  // |v / s| <= 127 (1 + 2^-24): rn_quot applies (a tiny group: |v| / 1 rounds to 0)
 #pragma unroll
-  for (int k = 0; k < NG; ++k) h[k] = __float2int_rn(__fdiv_rn(v[k], s[k]));  // a tiny group: |v| / 1 rounds to 0
+  for (int k = 0; k < NG; ++k) h[k] = rn_quot(v[k], s[k], rs[k]);
   if constexpr (Q == 2) {
 #pragma unroll
     for (int k = 0; k < NG; ++k) {
       h[k] = sat_i8(h[k]);
+      // the low word's quotient res / (s/128) = 128 res / s, |.| <= 65: s/128
+      // is exact (s is a normal float at least 1e-30/127), so is 128 res
       const float res = __fmaf_rn(-(float)h[k], s[k], v[k]);
-      l[k] = sat_i8(__float2int_rn(__fdiv_rn(res, __fmul_rn(s[k], 0.0078125f))));
+      l[k] = sat_i8(rn_quot(__fmul_rn(res, 128.0f), s[k], rs[k]));
     }
   }
 #pragma unroll
@@ -157,6 +193,33 @@ __device__ __forceinline__ double norm_div_add(double sum, int K, float eps) {
 }
 __device__ __forceinline__ float norm_scale(float v, float den, float g) {
   return __fmul_rn(__fdiv_rn(v, den), g);
+}
+
+// RN(v / d) for finite v and a normal d > 0, given yd = RN(1/d) (__frcp_rn,
+// once per row): Markstein's correction q = fma(fma(-q0, d, v), yd, q0) with
+// q0 = RN(v yd), accepted only where it is provably the correctly rounded
+// quotient: for 2^-60 <= |q| < 2^64 with q not a power of two (its two
+// neighbours one ulp away), the residual rem = fma(-q, d, v) is exact
+// (q within an ulp of v/d), and |rem| < ulp(q)/2 * d (a power of two times d:
+// exact) means |v/d - q| < ulp(q)/2 strictly, so q = RN(v/d) and no tie.
+// Anything else (zero, a tie or near one, tiny or huge quotients) takes the
+// IEEE division.  The same bits as __fdiv_rn(v, d) in every case.
+__device__ __forceinline__ float div_row(float v, float d, float yd) {
+  const float q0 = __fmul_rn(v, yd);
+  const float q = __fmaf_rn(__fmaf_rn(-q0, d, v), yd, q0);
+  const unsigned b = __float_as_uint(q), e = b & 0x7F800000u;
+  if (e >= (67u << 23) && e < (191u << 23) && (b & 0x007FFFFFu) != 0u) {
+    const float rem = __fmaf_rn(-q, d, v);
+    const float half = __uint_as_float(e - (24u << 23));  // ulp(q) / 2 = 2^(E - 127 - 24)
+    if (fabsf(rem) < __fmul_rn(half, d)) return q;
+  }
+  return __fdiv_rn(v, d);
+}
+__device__ __forceinline__ float norm_scale_r(float v, float den, float yd, float g) {
+  return __fmul_rn(div_row(v, den, yd), g);
+}
+__device__ __forceinline__ float norm_scale(float v, double den, float g) {
+  return __double2float_rn(__dmul_rn(__ddiv_rn((double)v, den), (double)g));
 }
 
 // ---- argmax key ("megakernel.cu" amax_key) --------------------------------------

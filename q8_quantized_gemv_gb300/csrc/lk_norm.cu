@@ -46,10 +46,25 @@ __device__ __forceinline__ float row_value(const NormArgs& a, long i) {
 
 // Normalize value v (element i of the [M][K] layout) and store what the mode
 // asks for; with ADD also the sum itself.
+// The row's divisor and, for an f32 norm, its correctly rounded reciprocal
+// (the quotients then take div_row's checked shortcut).
+template <typename A>
+struct Den {
+  A d;
+  float r;
+};
+template <typename A>
+__device__ __forceinline__ Den<A> make_den(A d) {
+  if constexpr (sizeof(A) == 4) return Den<A>{d, __frcp_rn(d)};
+  return Den<A>{d, 0.f};
+}
+
 template <int Q, bool ADD, typename A>
-__device__ __forceinline__ void finish_value(const NormArgs& a, long i, float v, A den, float gv, int lane) {
+__device__ __forceinline__ void finish_value(const NormArgs& a, long i, float v, Den<A> den, float gv, int lane) {
   if (ADD && a.s) a.s[i] = v;
-  const float yv = norm_scale(v, den, gv);
+  float yv;
+  if constexpr (sizeof(A) == 4) yv = norm_scale_r(v, den.d, den.r, gv);
+  else yv = norm_scale(v, den.d, gv);
   if (a.xn) a.xn[i] = yv;
   if constexpr (Q > 0) quant_lane<Q>(yv, a.xq, a.xl, a.xs, i >> 5, lane);
 }
@@ -82,7 +97,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(const NormArgs a) {
     if (lane == 0) total = v;
   }
   __syncthreads();
-  const A den = norm_div_add(total, K, a.eps);
+  const Den<A> den = make_den<A>(norm_div_add(total, K, a.eps));
   // warp w holds the 32-groups starting at 32w, 32w + vt, ... (vt % 32 == 0)
   for (int b = warp * 32; b < K; b += vt)
     finish_value<Q, ADD>(a, base + b + lane, row_value<ADD>(a, base + b + lane), den, __ldg(a.g + b + lane), lane);
@@ -122,7 +137,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_split_kernel(const NormArgs a) {
     if (lane == 0) total = t;
   }
   __syncthreads();
-  const A den = norm_div_add(total, K, a.eps);
+  const Den<A> den = make_den<A>(norm_div_add(total, K, a.eps));
   float mine = v[0];
 #pragma unroll
   for (int u = 1; u < KU_MAX; ++u)
@@ -173,7 +188,7 @@ __global__ void __launch_bounds__(256) rmsnorm_split256_kernel(const NormArgs a)
     if (lane == 0) total = t;
   }
   __syncthreads();
-  const A den = norm_div_add(total, K, a.eps);
+  const Den<A> den = make_den<A>(norm_div_add(total, K, a.eps));
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     float mine = v[j][0];

@@ -316,6 +316,7 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
       pstamp(dbg, 2);
     }
     const A dn = norm ? den[t] : (A)1;
+    const float rdn = sizeof(A) == 4 ? __frcp_rn((float)dn) : 0.f;  // for div_row (f32 norms)
     // (3) normalize and quantize, batch by batch, four groups at a time in
     // lockstep (their division chains interleave)
     for (int g0 = cw; g0 < ng; g0 += QB * nwc) {
@@ -332,7 +333,10 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
           ok[k] = g < ng;
           v[k] = qx[b0 + k];
           // past the row's end (a chunk narrower than the area) the area keeps zeros
-          if (norm && k_lo + 32 * g + lane < K) v[k] = norm_scale(v[k], dn, qg[b0 + k]);
+          if (norm && k_lo + 32 * g + lane < K) {
+            if constexpr (sizeof(A) == 4) v[k] = norm_scale_r(v[k], (float)dn, rdn, qg[b0 + k]);
+            else v[k] = norm_scale(v[k], dn, qg[b0 + k]);
+          }
         }
         store_act4<Q, M>(act, L, t, g0 + b0 * nwc, nwc, lane, v, ok);
       }
