@@ -244,6 +244,72 @@ __device__ void fused_prologue(const lkh::GemvProblem& a, int nwc, int k_lo, uns
   const int KU = (K + vt - 1) / vt;
   const int ng = (int)(L >> 5);
   pstamp(dbg, 0);
+  // One round trip per row where the layouts agree (K = 1024 u, u <= 4, the
+  // whole row, at least 11 warps): virtual warp w's values 32w + l + 1024u
+  // are element l of the 32-groups w + 32u, so the values a warp loads for
+  // the sum of squares are whole groups of the quantizer too -- loaded once,
+  // kept in registers through the sum, the norm and the quantizer.
+  if (norm && K % 1024 == 0 && KU <= 4 && k_lo == 0 && (int)L == K && nwc >= 11) {
+    for (int t = 0; t < M; ++t) {
+      const float* xr = a.xraw + (long)t * K;
+      float xv[3][4], gv[3][4];
+#pragma unroll
+      for (int j = 0; j < 3; ++j)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int w = cw + j * nwc;
+          gv[j][u] = (w < 32 && u < KU) ? ld_keep(a.gain + 32 * w + lane + 1024 * u) : 1.f;
+        }
+      if (t == 0 && wait_first) griddep_wait();
+#pragma unroll
+      for (int j = 0; j < 3; ++j)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int w = cw + j * nwc;
+          xv[j][u] = (w < 32 && u < KU) ? ld_keep_cg(xr + 32 * w + lane + 1024 * u) : 0.f;
+        }
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int w = cw + j * nwc;
+        if (w >= 32) break;  // warp-uniform
+        A acc = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (u < KU) acc = fma_acc((A)xv[j][u], acc);
+        acc = warp_tree_sum(acc);
+        if (lane == 0) red[t * 32 + w] = acc;
+      }
+      pstamp(dbg, 1);
+      __syncthreads();
+      if (cw == 0) {
+        A v = red[t * 32 + lane];
+        v = warp_tree_sum(v);
+        if (lane == 0) den[t] = norm_div_add(v, K, a.eps);
+      }
+      __syncthreads();
+      pstamp(dbg, 2);
+      const A dn = den[t];
+      const float rdn = sizeof(A) == 4 ? __frcp_rn((float)dn) : 0.f;  // for div_row (f32 norms)
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int w = cw + j * nwc;
+        if (w >= 32) break;
+        float v[4];
+        bool ok[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          ok[u] = u < KU;
+          if constexpr (sizeof(A) == 4) v[u] = norm_scale_r(xv[j][u], (float)dn, rdn, gv[j][u]);
+          else v[u] = norm_scale(xv[j][u], dn, gv[j][u]);
+        }
+        store_act4<Q, M>(act, L, t, w, 32, lane, v, ok);  // groups w + 32 u
+      }
+      pstamp(dbg, 3);
+    }
+    __syncthreads();
+    pstamp(dbg, 4);
+    return;
+  }
   for (int t = 0; t < M; ++t) {
     const float* xr = a.xraw + (long)t * K;
     // (1) the first batch of this warp's groups g = cw + nwc*b: its values and

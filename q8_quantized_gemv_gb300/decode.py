@@ -33,7 +33,7 @@ from . import lk, synth
 class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
                  batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
-                 fused=False, chain=False, group_qkv=True, prefill=None, glu=False):
+                 fused=False, chain=False, group_qkv=True, prefill=None, glu=False, fused_qkv=True):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
         # per projection: warps of a ring GEMV block that fill their stages
@@ -46,10 +46,21 @@ class DecodeStack:
         self.glu = bool(glu) and not chain and not fused
         self.shapes = {"q": (q_dim, hidden), "k": (kv_dim, hidden), "v": (kv_dim, hidden),
                        "o": (hidden, q_dim), "gu": (2 * ffn, hidden), "down": (hidden, ffn)}
+        # fused_qkv: q, k and v are row ranges of one [q + 2 kv, hidden]
+        # matrix (the usual fused attention projection); the per-launch
+        # sequence then runs them as ONE GEMV over its rows
+        self.fused_qkv = bool(fused_qkv)
         self.layers = []
         for l in range(layers):
             w = {}
+            if self.fused_qkv:
+                w["qkv"] = synth.q8_matrix_torch(q_dim + 2 * kv_dim, hidden, s + 1000 * l + 30, dev)
+                bounds = {"q": (0, q_dim), "k": (q_dim, q_dim + kv_dim), "v": (q_dim + kv_dim, q_dim + 2 * kv_dim)}
+                for n, (r0, r1) in bounds.items():
+                    w[n] = (w["qkv"][0][r0:r1], w["qkv"][1][r0:r1])
             for i, (name, (N, K)) in enumerate(self.shapes.items()):
+                if name in ("q", "k", "v") and self.fused_qkv:
+                    continue
                 if name == "gu" and self.glu:
                     # the gate and up matrices of the pair (ffn rows each)
                     w["gate"] = synth.q8_matrix_torch(ffn, hidden, s + 1000 * l + i, dev)
@@ -71,6 +82,11 @@ class DecodeStack:
         self.xn = torch.empty((B, hidden), dtype=f32, device=dev)       # normed (Dequant GEMV input)
         self.acts = {K: self._act_bufs(K) for K in {hidden, q_dim, ffn}}
         self.out = {name: torch.empty((B, N), dtype=f32, device=dev) for name, (N, _) in self.shapes.items()}
+        if self.fused_qkv:
+            # one output for the fused matrix; q, k, v are its column ranges
+            self.out_qkv = torch.empty((B, q_dim + 2 * kv_dim), dtype=f32, device=dev)
+            self.qkv_views = {"q": self.out_qkv[:, :q_dim], "k": self.out_qkv[:, q_dim:q_dim + kv_dim],
+                              "v": self.out_qkv[:, q_dim + kv_dim:]}
         if self.glu:
             self.hbuf = [torch.empty((B, hidden), dtype=f32, device=dev) for _ in range(2)]  # residual stream
             self.gu_buf = torch.empty((2, B, ffn), dtype=f32, device=dev)   # gate and up values
@@ -103,12 +119,17 @@ class DecodeStack:
         # q, k and v of a layer as one grouped launch (a chain without
         # barriers: one prologue, the three weight streams back to back)
         self.qkv = None
-        if self.chain is None and group_qkv and all(self.fused[n] for n in ("q", "k", "v")):
+        if self.chain is None and group_qkv and all(self.fused[n] for n in ("q", "k", "v")) and not self.fused_qkv:
             self.qkv = []
             for l, w in enumerate(self.layers):
                 x = self.x_buf if l == 0 else self.h
                 self.qkv.append(lk.Chain([lk.chain_op(w[n][0], w[n][1], x, self.out[n], gain=w["g_attn"])
                                           for n in ("q", "k", "v")], dev))
+
+        fq = [self.fused[n] for n in ("q", "k", "v")]
+        self.qkv_one = self.fused_qkv and self.chain is None and (all(fq) or not any(fq))
+        if self.qkv_one:
+            self.out.update(self.qkv_views)
 
     def _act_bufs(self, K):
         B = self.B
@@ -180,6 +201,14 @@ class DecodeStack:
                                argmax_parts=self.parts, argmax_idx=self.idx, wait=True))
         return ops
 
+    def _qkv_launch(self, w, a):
+        """The attention projections of layer weights w on activation a: one
+        GEMV over the fused q|k|v matrix, or one grouped GEMV over three."""
+        if self.fused_qkv:
+            return lambda: lk.lk_gemv_q8(w["qkv"][0], w["qkv"][1], self.mode, self.out_qkv, M=self.B, **a)
+        return lambda: lk.lk_gemv_q8_group([(w[n][0], w[n][1], self.out[n]) for n in ("q", "k", "v")], self.mode,
+                                           M=self.B, **a)
+
     def _run_token_glu(self, hook):
         """The pre-norm decoder layer dataflow (glu=True)."""
         def launch(name, fn):
@@ -189,8 +218,7 @@ class DecodeStack:
         a_h = self._norm(self.x_buf, self.layers[0]["g_attn"])
         h_cur = self.x_buf
         for l, w in enumerate(self.layers):
-            launch("qkv", lambda w=w, a=a_h: lk.lk_gemv_q8_group(
-                [(w[n][0], w[n][1], self.out[n]) for n in ("q", "k", "v")], m, M=B, **a))
+            launch("qkv", self._qkv_launch(w, a_h))
             a_o = self._quant(w["o_in"])
             launch("o", lambda w=w, a=a_o: self._gemv(w["o"], self.out["o"], a))
             h_mid = self.hbuf[0]
@@ -241,13 +269,17 @@ class DecodeStack:
                 def launch(c=self.qkv[l]):
                     return lk.lk_gemv_chain(c, self.mode, self.B, self.eps)
                 launch() if hook is None else hook("qkv", launch)
+            elif self.qkv_one and self.fused["q"]:
+                # one launch: norm -> quantize prologue, the fused q|k|v matrix
+                def launch(w=w, x=x):
+                    return lk.lk_rmsnorm_quant_gemv_q8(w["qkv"][0], w["qkv"][1], self.mode, x, self.out_qkv,
+                                                       gain=w["g_attn"], eps=self.eps)
+                launch() if hook is None else hook("qkv", launch)
             elif not any(self.fused[n] for n in ("q", "k", "v")):
-                # one norm, then q, k and v as one grouped GEMV
+                # one norm, then q, k and v as one GEMV over the fused matrix
+                # (or one grouped GEMV over the three)
                 a = self._norm(x, w["g_attn"])
-
-                def launch(w=w, a=a):
-                    return lk.lk_gemv_q8_group([(w[n][0], w[n][1], self.out[n]) for n in ("q", "k", "v")],
-                                               self.mode, M=self.B, **a)
+                launch = self._qkv_launch(w, a)
                 launch() if hook is None else hook("qkv", launch)
             else:
                 # q, k and v read the same normed activation: quantized once
@@ -296,7 +328,8 @@ class DecodeStack:
         qkv_norm = 0 if (f["q"] and f["k"] and f["v"]) else 1  # one shared norm for q, k, v
         # q, k, v in one launch: the fused chain, or lk_gemv_q8_group on the
         # tensor-core or chain kernel (both take the shape where the ring does)
-        grouped = self.qkv is not None or (not any(f[n] for n in ("q", "k", "v")) and self.kernel["q"] in (2, 3))
+        grouped = self.qkv is not None or self.qkv_one or \
+            (not any(f[n] for n in ("q", "k", "v")) and self.kernel["q"] in (2, 3))
         per_layer = (4 if grouped else 6) + qkv_norm \
             + (0 if (f["o"] or self.mode == lk.LK_DEQUANT) else 1) + (0 if f["gu"] else 1) \
             + (0 if (f["down"] or self.mode == lk.LK_DEQUANT) else 1)

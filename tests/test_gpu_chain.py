@@ -128,14 +128,16 @@ def test_pdl_graph_replays_identical(fused, prefill):
     assert lk.lk_device_error(reset=True) == 0
 
 
+@pytest.mark.parametrize("fused_qkv", [False, True])
 @pytest.mark.parametrize("fused", [False, True])
-def test_grouped_qkv_pdl_graph_matches_plain(fused):
-    """The per-launch sequence with q, k, v as one grouped launch (after one
-    norm launch, or with the fused prologue): captured with programmatic
+def test_grouped_qkv_pdl_graph_matches_plain(fused, fused_qkv):
+    """The per-launch sequence with q, k, v in one launch -- one GEMV over the
+    fused q|k|v matrix, or one grouped launch over three matrices -- after one
+    norm launch or with the fused prologue: captured with programmatic
     dependent launches in a graph, it gives the same bits as launched plainly,
     and the oracle's token."""
-    a = DecodeStack(**SMALL, batch=1, mode=1, chain=False, fused=fused)
-    assert (a.qkv is not None) == fused
+    a = DecodeStack(**SMALL, batch=1, mode=1, chain=False, fused=fused, fused_qkv=fused_qkv)
+    assert (a.qkv is not None) == (fused and not fused_qkv) and a.qkv_one == fused_qkv
     lk.lk_set_option("pdl", 0)
     layers, final = run_token_capture(a)
     check_token(a, layers, final)

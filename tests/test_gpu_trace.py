@@ -41,7 +41,7 @@ def test_timeline_records(batch):
     n = st.launches_per_token() - 1
     used = [raw[i * 8:(i + 1) * 8] for i in range(n)]
     gemv = 1 if batch == 1 else 3
-    qkv = 2 if batch == 1 else 3
+    qkv = gemv  # one GEMV over the fused q|k|v matrix
     want = [4, qkv, 5, gemv, 4, gemv, 5, gemv] * SMALL["layers"] + [4, gemv]
     assert [r[5] for r in used] == want
     assert [r[6] for r in used if r[5] == 4] == [SMALL["hidden"]] * (2 * SMALL["layers"] + 1)
@@ -76,4 +76,4 @@ def test_timeline_records_glu_token():
     raw = lk.lk_trace_read(4096)
     n = st.launches_per_token() - 1
     kinds = [raw[i * 8 + 5] for i in range(n)]
-    assert kinds == [4] + [2, 5, 1, 4, 1, 1, 4] * SMALL["layers"] + [1]
+    assert kinds == [4] + [1, 5, 1, 4, 1, 1, 4] * SMALL["layers"] + [1]
