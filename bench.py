@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--K", type=int, default=4096)
     ap.add_argument("--S", type=int, default=1, help="split-K chunks (gemv workload)")
     ap.add_argument("--argmax", action="store_true", help="argmax epilogue + reduce (gemv workload)")
+    ap.add_argument("--glu", action="store_true",
+                    help="gemv workload: the gate/up pair (two N/2-row matrices) with the SwiGLU + quantize epilogue")
     ap.add_argument("--path", default="auto", choices=["auto", "direct", "ring", "mma"])
     ap.add_argument("--chain", action="store_true",
                     help="sequence: the whole token as one cooperative chain launch (lk_gemv_chain; fused "
@@ -524,8 +526,21 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
 
     xn = torch.empty((B, K), dtype=torch.float32, device=dev) if mode == lk.LK_DEQUANT else None
 
+    F = N // 2
+    gu_buf = torch.empty((2, B, F), dtype=torch.float32, device=dev) if a.glu else None
+    h_glu = torch.empty((B, F), dtype=torch.float32, device=dev) if a.glu else None
+    hact = ({"hq": torch.empty((B, F), dtype=torch.int8, device=dev),
+             "hl": torch.empty((B, F), dtype=torch.int8, device=dev) if mode == lk.LK_TWOPASS else None,
+             "hs": torch.empty((B, F // 32), dtype=torch.float32, device=dev)} if a.glu and mode else {})
+    cnt = torch.zeros((F // 32,), dtype=torch.int32, device=dev) if a.glu else None
+
     def launch(r):
         wq, ws = mats[r % R]
+        if a.glu:
+            # the two halves of the copy as the gate and the up matrix
+            lk.lk_gemv_q8_glu(wq[:F], ws[:F], wq[F:], ws[F:], mode, gu_buf, h=h_glu, cnt=cnt, M=B, **hact,
+                              **({"x": xn if xn is not None and a.norm else x} if mode == lk.LK_DEQUANT else acts))
+            return
         if a.norm and not a.fused:
             if mode == lk.LK_DEQUANT:
                 lk.lk_rmsnorm_quant(x, gain, mode, 1e-6, xn)
@@ -583,6 +598,7 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
            "steps": a.steps, "warmup": a.warmup, "ms_per_step": us * 1e-3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": _dtype(a.mode), "data": "synthetic",
            "config": {"workload": f"Q8_0 GEMV N={N} K={K} batch {B} {a.mode} S={S}"
+                                  + (" gate/up pair + SwiGLU + quantize" if a.glu else "")
                                   + (" + argmax" if a.argmax else "") + (" fused norm+quant" if a.fused else "")
                                   + (" after a norm+quant launch" if a.norm and not a.fused else ""),
                       "rotation": f"{R} weight copies ({R * wbytes} bytes >= 4x L2), {max(R, 8)} launches per graph",

@@ -59,6 +59,7 @@ typedef int lk_status;
                              norm / quantize / SwiGLU / argmax calls */
 #define LK_MAX_SPLITK 64  /* split-K chunks */
 #define LK_MAX_GROUP  4   /* matrices of one lk_gemv_q8_group call */
+#define LK_TRACE_REC  8   /* entries of one launch record of option "trace" 3 */
 
 /*
  * Per-call launch settings of the GEMV entry points with an `_ex` suffix
@@ -453,16 +454,18 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 when block 0's warps' first stage of each step was there
  *                 and computed (from index 2048);
  *                 3: launch timeline: every ring, chain and tensor-core
- *                 launch made after the option was set owns a record of 8
- *                 entries (in launch order, 512 records, wrapping):
+ *                 launch made after the option was set owns a record of
+ *                 LK_TRACE_REC entries (in launch order, 512 records,
+ *                 wrapping):
  *                 [0] block 0 start, [1] block 0 past the wait on the
  *                 previous kernel (fused launches: the prologue's start; it
  *                 waits inside, after requesting the norm gains), [2] block
  *                 0's activation ready, [3] the
  *                 last block's end, [4] block 0's end (all %globaltimer ns),
- *                 [5] kernel (1 ring, 2 chain, 3 tensor-core), [6] rows
- *                 (steps, for a chain).  Setting the option restarts the
- *                 record count.
+ *                 [5] kernel (1 ring, 2 chain, 3 tensor-core, 4 norm,
+ *                 5 quantize), [6] rows (steps, for a chain), [7] block 0's
+ *                 first weight stages issued.  Setting the option restarts
+ *                 the record count.
  *   "wait_us"     time limit of every device-side wait, microseconds
  *                 (0 = default, 2 s)
  *   "mma_min_m"   fewest activation rows lk_gemv_q8 runs on the tensor-core

@@ -1,34 +1,25 @@
-// Bulk-copy ring GEMV for sm_103a (host side), and the device-side error word that every
-// bounded wait sets when it gives up.
+// Bulk-copy ring GEMV for sm_103a (host side: layout and launch), and the
+// device-side error word that every bounded wait sets when it gives up.
 //
 // One block per SM, persistent over a contiguous, balanced range of rows
-// [r0, r1) (and one split-K chunk).  The block first copies the activation
-// slice it needs (words and scales of all M rows) into shared memory, where
-// it stays for the whole kernel.  Warp 8 then streams the weights through a
-// ring of shared-memory stages with 1-D bulk copies (TMA: cp.async.bulk ...
-// mbarrier::complete_tx::bytes, L2 evict-first).  A stage is one "quad": four
-// consecutive rows times up to 4 KB of K, so for K <= 4096 a stage is two
-// copies (the quad's levels and its scales are contiguous in global memory);
-// for longer K each row's slice and its scale slice are copied separately.
-// Quads are dealt to the 8 consumer warps in groups of 8 (warp w takes quad
-// w of each group, all its K slices in order), so consecutive stages belong
-// to different warps and the ring overlaps 8 quads' compute with up to 16
-// stages of copies in flight.  Each stage has a "full" mbarrier (expect-tx
-// arrival + the copies' bytes) and an "empty" one (one arrival: the warp
-// that consumed it).
-//
-// The consumer arithmetic is the direct kernel's: 8 lanes per row, lane j
-// reading bytes 16j..16j+15 of each 128-byte segment, lanes 2q, 2q+1 meeting
-// by one xor-shuffle for block q's exact dot, lane 2q carrying partial
-// q = b mod 4 in ascending block order, then (p0 + p2) + (p1 + p3).  Both
-// kernels give the same bits.
+// (and one split-K chunk).  The block loads the activation slice it needs
+// (words and scales of all M rows) into shared memory once.  Every warp then
+// streams its own "quads" (4 consecutive rows; warp w takes quads w, w + W,
+// ...) through its own ring stages with 1-D bulk copies (TMA:
+// cp.async.bulk ... mbarrier::complete_tx::bytes, L2 evict-first), refilling
+// a stage as soon as it has consumed it: a stage is a whole quad for rows up
+// to 8 KB, else a 4 KB slice of it; each warp owns one stage where they fit
+// (12 warps).  The consumer arithmetic is the direct kernel's (lk_gemv.cu),
+// with the same bits.
 //
 // Every wait on an mbarrier is bounded by a wall-clock limit (%globaltimer).
 // A wait that runs out sets the error word and an abort flag in shared
-// memory; every thread then leaves its loops, and the producer, before it
-// exits, waits (again bounded) for the copies it issued, so that no copy is
-// still in flight into the block's shared memory when the block ends.
+// memory; every thread then leaves its loops, and each warp waits (again
+// bounded) for the copies it issued, so that no copy is still in flight into
+// the block's shared memory when the block ends.
 #include "lk_ring_kernel.cuh"
+
+static_assert(lkring::TREC == LK_TRACE_REC, "trace record size of the public header");
 
 __device__ int lk_error_word;
 // Block 0's timestamps (%globaltimer, ns) of the last traced launch.
@@ -101,7 +92,16 @@ int max_chunk_blocks(int nb, int S) {
   return m;
 }
 
-Layout layout(const lkh::GemvProblem& p, int smem_optin) {
+// Blocks of a ring launch along the rows (per split-K chunk).
+int ring_gx(const lkh::GemvProblem& p, int sm_count) {
+  const int S = p.split && p.S > 1 ? p.S : 1;
+  const int g = lkh::opt_grid_ctas > 0 ? (int)lkh::opt_grid_ctas
+                                       : sm_count * (lkh::opt_ring_cps > 1 ? (int)lkh::opt_ring_cps : 1);
+  const int gx = (g + S - 1) / S;
+  return gx < 1 ? 1 : gx;
+}
+
+Layout layout(const lkh::GemvProblem& p, int smem_optin, int /*sm_count*/) {
   Layout L;
   const int nb = p.K / 32;
   const int S = p.split ? (p.S > 1 ? p.S : 1) : 1;
@@ -121,7 +121,10 @@ Layout layout(const lkh::GemvProblem& p, int smem_optin) {
   if (fit > MAX_STAGES) fit = MAX_STAGES;
   if (lkh::opt_ring_stages > 0 && lkh::opt_ring_stages < fit) fit = (int)lkh::opt_ring_stages;
   // warps x stages per warp: as many stages in flight as fit, one warp per
-  // stage up to MAXW warps (each warp streams its own quads)
+  // stage up to MAXW warps (each warp streams its own quads).  Measured: for
+  // rows in slices with few quads per block (down 4096 x 12288, 6.7 quads of
+  // 3 slices), 6 warps of 2 stages lost to 12 of 1 (in the sequence: body
+  // 10.2 against 9.7 us, 1815 against 1789 us per token)
   int w = lkh::opt_ring_warps > 0 ? (int)lkh::opt_ring_warps : (fit < MAXW ? fit : MAXW);
   if (w > fit) w = fit;
   L.nwc = w;
@@ -149,7 +152,7 @@ bool ring_supports(const GemvProblem& p) {
     return false;
   const DeviceInfo* d = device_info(nullptr);
   if (!d) return false;
-  return layout_ok(layout(p, d->smem_optin));
+  return layout_ok(layout(p, d->smem_optin, d->sm_count));
 }
 
 int ring_max_ctas(long) {
@@ -162,7 +165,7 @@ int ring_max_ctas(long) {
 lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   const DeviceInfo* d = device_info(nullptr);
   if (!d) return LK_ERR_CUDA;
-  const Layout L = layout(p, d->smem_optin);
+  const Layout L = layout(p, d->smem_optin, d->sm_count);
   if (!layout_ok(L)) return LK_ERR_SHAPE;
   ring_fn f = pick(p.mode, p.M, p.split, p.fuse, p.F > 0);
   // The cap is the device's opt-in maximum, never this launch's size: one
@@ -190,9 +193,7 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   ra.tslot = opt_trace == 3 ? lkh::trace_next_slot() : -1;
   ra.prefill = lkh::prefill_warps(L.nwc, p.prefill);
   const int S = p.split && p.S > 1 ? p.S : 1;
-  const int g = opt_grid_ctas > 0 ? (int)opt_grid_ctas : d->sm_count * (opt_ring_cps > 1 ? (int)opt_ring_cps : 1);
-  int gx = (g + S - 1) / S;
-  if (gx < 1) gx = 1;
+  const int gx = ring_gx(p, d->sm_count);
   ra.gx = gx;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(gx, S);

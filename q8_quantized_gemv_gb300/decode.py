@@ -36,8 +36,8 @@ class DecodeStack:
                  fused=False, chain=False, group_qkv=True, prefill=None, glu=False, fused_qkv=True):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
-        # per projection: warps of a ring GEMV block that fill their stages
-        # before the dependency wait (option "ring_prefill" for that launch)
+        # per projection (qkv, o, gu, down, lm): warps of a GEMV block that
+        # fill their stages before the dependency wait (lk_launch_cfg.prefill)
         self.prefill = dict(prefill or {})
         dev = self.dev
         s = seed
@@ -166,19 +166,14 @@ class DecodeStack:
         lk.lk_quantize_act(x, self.mode, a["xq"], a.get("xl"), a["xs"])
         return a
 
-    def _with_prefill(self, name, launch):
+    def _cfg(self, name):
+        """Per-call launch settings of projection `name`: the warps filling
+        before the dependency wait, where set (None: the defaults)."""
         v = self.prefill.get(name)
-        if v is None:
-            return launch()
-        old = lk.lk_get_option("ring_prefill")
-        lk.lk_set_option("ring_prefill", v)
-        try:
-            return launch()
-        finally:
-            lk.lk_set_option("ring_prefill", old)
+        return None if v is None else lk.launch_cfg(prefill=v)
 
-    def _gemv(self, w, y, acts, parts=None):
-        return lk.lk_gemv_q8(w[0], w[1], self.mode, y, M=self.B, argmax_parts=parts, **acts)
+    def _gemv(self, w, y, acts, parts=None, name=None):
+        return lk.lk_gemv_q8(w[0], w[1], self.mode, y, M=self.B, argmax_parts=parts, cfg=self._cfg(name), **acts)
 
     def _chain_ops(self):
         """The token's steps.  A step waits (grid barrier) where a decoder's
@@ -204,10 +199,11 @@ class DecodeStack:
     def _qkv_launch(self, w, a):
         """The attention projections of layer weights w on activation a: one
         GEMV over the fused q|k|v matrix, or one grouped GEMV over three."""
+        c = self._cfg("qkv")
         if self.fused_qkv:
-            return lambda: lk.lk_gemv_q8(w["qkv"][0], w["qkv"][1], self.mode, self.out_qkv, M=self.B, **a)
+            return lambda: lk.lk_gemv_q8(w["qkv"][0], w["qkv"][1], self.mode, self.out_qkv, M=self.B, cfg=c, **a)
         return lambda: lk.lk_gemv_q8_group([(w[n][0], w[n][1], self.out[n]) for n in ("q", "k", "v")], self.mode,
-                                           M=self.B, **a)
+                                           M=self.B, cfg=c, **a)
 
     def _run_token_glu(self, hook):
         """The pre-norm decoder layer dataflow (glu=True)."""
@@ -220,19 +216,19 @@ class DecodeStack:
         for l, w in enumerate(self.layers):
             launch("qkv", self._qkv_launch(w, a_h))
             a_o = self._quant(w["o_in"])
-            launch("o", lambda w=w, a=a_o: self._gemv(w["o"], self.out["o"], a))
+            launch("o", lambda w=w, a=a_o: self._gemv(w["o"], self.out["o"], a, name="o"))
             h_mid = self.hbuf[0]
             a_m = self._add_norm(self.out["o"], h_cur, h_mid, w["g_mlp"])
             a_d = {"x": self.hglu} if m == lk.LK_DEQUANT else self.acts[self.F]
             launch("gu", lambda w=w, a=a_m, d=a_d: lk.lk_gemv_q8_glu(
                 w["gate"][0], w["gate"][1], w["up"][0], w["up"][1], m, self.gu_buf, h=self.hglu,
-                hq=d.get("xq"), hl=d.get("xl"), hs=d.get("xs"), cnt=self.glu_cnt, M=B, **a))
-            launch("down", lambda w=w, d=a_d: self._gemv(w["down"], self.out["down"], d))
+                hq=d.get("xq"), hl=d.get("xl"), hs=d.get("xs"), cnt=self.glu_cnt, M=B, cfg=self._cfg("gu"), **a))
+            launch("down", lambda w=w, d=a_d: self._gemv(w["down"], self.out["down"], d, name="down"))
             h_next = self.hbuf[1]
             g_next = self.layers[l + 1]["g_attn"] if l + 1 < L else self.g_final
             a_h = self._add_norm(self.out["down"], h_mid, h_next, g_next)
             h_cur = h_next
-        self.n_parts = launch("lm", lambda: self._gemv(self.lm, self.logits, a_h, self.parts))
+        self.n_parts = launch("lm", lambda: self._gemv(self.lm, self.logits, a_h, self.parts, name="lm"))
         lk.lk_argmax(self.idx, B, self.V, parts=self.parts, n_parts=self.n_parts)
         return self.idx
 
@@ -260,7 +256,7 @@ class DecodeStack:
                 a = acts if acts is not None else (self._norm(x, gain) if gain is not None else self._quant(x))
 
                 def launch():
-                    return self._with_prefill(name, lambda: self._gemv(w, y, a, parts))
+                    return self._gemv(w, y, a, parts, name)
             return (launch() if hook is None else hook(name, launch)), a
 
         x = self.x_buf

@@ -39,7 +39,8 @@ def test_timeline_records(batch):
     raw = lk.lk_trace_read(4096)
     # one record per traced launch (all but the argmax reduce), in launch order
     n = st.launches_per_token() - 1
-    used = [raw[i * 8:(i + 1) * 8] for i in range(n)]
+    R = lk.LK_TRACE_REC
+    used = [raw[i * R:(i + 1) * R] for i in range(n)]
     gemv = 1 if batch == 1 else 3
     qkv = gemv  # one GEMV over the fused q|k|v matrix
     want = [4, qkv, 5, gemv, 4, gemv, 5, gemv] * SMALL["layers"] + [4, gemv]
@@ -75,5 +76,5 @@ def test_timeline_records_glu_token():
     assert torch.equal(st.logits.view(torch.int32), ref.view(torch.int32))
     raw = lk.lk_trace_read(4096)
     n = st.launches_per_token() - 1
-    kinds = [raw[i * 8 + 5] for i in range(n)]
+    kinds = [raw[i * lk.LK_TRACE_REC + 5] for i in range(n)]
     assert kinds == [4] + [1, 5, 1, 4, 1, 1, 4] * SMALL["layers"] + [1]
