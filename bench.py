@@ -83,8 +83,9 @@ def parse():
                     help="gemv workload: an RMSNorm->quantize launch before every GEMV (the separate form)")
     ap.add_argument("--table", default=None,
                     help="write the per-config single-GEMV table (markdown) to this path")
-    ap.add_argument("--opt", action="append", default=[],
-                    help="library option name=value (lk_set_option), e.g. ring_kb=110; repeatable")
+    ap.add_argument("--cfg", action="append", default=[],
+                    help="a launch setting name=value (a field of lk_launch_cfg, e.g. mma_tk=1024) for every "
+                         "call; repeatable")
     return ap.parse_args()
 
 
@@ -339,14 +340,12 @@ def run_ours(a, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
-    _apply_opts(lk, a)
     fused = (a.fused_prologue or a.chain) and not a.unfused
     if a.fuse and not fused:
         fused = [n for n in a.fuse.split(",") if n]
     prefill = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in a.prefill}
     stack = DecodeStack(layers=a.layers, batch=a.batch, mode=a.mode, device=dev, fused=fused, chain=a.chain and fused,
-                        prefill=prefill, glu=a.decoder)
+                        prefill=prefill, glu=a.decoder, pdl=not a.no_pdl, tune=_tune(a))
     tok_bytes = stack.weight_bytes()
     stream = torch.cuda.Stream(device=dev)
 
@@ -437,13 +436,13 @@ def run_ours(a, rank, world):
         "config": {"workload": workload_name(a), "weight_bytes_per_step": tok_bytes,
                    "l2": "inputs larger than L2 (8.04 GB of weights per step)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "gemv_path": "auto", "fused_prologue": {k: v for k, v in stack.fused.items()},
+                   "path": "auto", "fused_prologue": {k: v for k, v in stack.fused.items()},
                    "gemv_kernel": {k: "ring" if stack.fused[k] else {1: "direct", 2: "ring", 3: "mma"}.get(v, "none")
                                    for k, v in stack.kernel.items()},
                    "chain": stack.chain is not None,
-                   "ring_prefill": stack.prefill or "half of the warps",
+                   "prefill": stack.prefill or "half of the warps",
                    "dataflow": "decoder (glu)" if stack.glu else "projections alone",
-                   "pdl": not a.no_pdl, "options": a.opt},
+                   "pdl": not a.no_pdl, "launch_cfg": a.cfg},
         "us_per_token": ms_max * 1e3,
         "pct_of_nominal_8TBs": value / world / NOMINAL_HBM_GBS,
         "roofline": roof,
@@ -457,7 +456,6 @@ def run_ours(a, rank, world):
     if rank == 0 and not a.no_configs:
         # after every timed region of the headline: the other configurations
         del graph, graph_e2e
-        lk.lk_set_option("pdl", 1)
         forms = [(1, "int8act"), (1, "twopass"), (1, "dequant"), (8, "int8act"), (8, "twopass"),
                  (16, "int8act"), (64, "int8act")]
         forms = [(b, m, False) for b, m in forms if (b, m) != (a.batch, a.mode) or a.decoder] + \
@@ -471,10 +469,9 @@ def run_ours(a, rank, world):
         dist.destroy_process_group()
 
 
-def _apply_opts(lk, a):
-    for kv in a.opt:
-        k, v = kv.split("=")
-        lk.lk_set_option(k, int(v))
+def _tune(a):
+    """The --cfg launch settings as a dict of lk_launch_cfg fields."""
+    return {kv.split("=")[0]: int(kv.split("=")[1]) for kv in a.cfg}
 
 
 def _timing_event(torch, external):
@@ -497,9 +494,7 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
-    lk.lk_set_option("gemv_path", {"auto": 0, "direct": 1, "ring": 2, "mma": 3}[a.path])
-    lk.lk_set_option("pdl", 0 if a.no_pdl else 1)
-    _apply_opts(lk, a)
+    cfg = lk.launch_cfg(**dict(_tune(a), path=a.path, pdl=0 if a.no_pdl else 1))
     mode = lk.MODES[a.mode]
     N, K, B, S = a.N, a.K, a.batch, a.S
     wbytes = N * K + N * K // 16
@@ -538,24 +533,24 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
         wq, ws = mats[r % R]
         if a.glu:
             # the two halves of the copy as the gate and the up matrix
-            lk.lk_gemv_q8_glu(wq[:F], ws[:F], wq[F:], ws[F:], mode, gu_buf, h=h_glu, cnt=cnt, M=B, **hact,
+            lk.lk_gemv_q8_glu(wq[:F], ws[:F], wq[F:], ws[F:], mode, gu_buf, h=h_glu, cnt=cnt, M=B, cfg=cfg, **hact,
                               **({"x": xn if xn is not None and a.norm else x} if mode == lk.LK_DEQUANT else acts))
             return
         if a.norm and not a.fused:
             if mode == lk.LK_DEQUANT:
-                lk.lk_rmsnorm_quant(x, gain, mode, 1e-6, xn)
+                lk.lk_rmsnorm_quant(x, gain, mode, 1e-6, xn, cfg=cfg)
             else:
-                lk.lk_rmsnorm_quant(x, gain, mode, 1e-6, None, acts["xq"], acts["xl"], acts["xs"])
+                lk.lk_rmsnorm_quant(x, gain, mode, 1e-6, None, acts["xq"], acts["xl"], acts["xs"], cfg=cfg)
         if a.fused:
-            n = lk.lk_rmsnorm_quant_gemv_q8(wq, ws, mode, x, y, gain=gain, argmax_parts=parts)
+            n = lk.lk_rmsnorm_quant_gemv_q8(wq, ws, mode, x, y, gain=gain, argmax_parts=parts, cfg=cfg)
             if a.argmax:
                 lk.lk_argmax(idx, B, N, parts=parts, n_parts=n)
         elif S > 1:
-            lk.lk_gemv_q8_splitk(wq, ws, mode, S, part, M=B, **acts)
+            lk.lk_gemv_q8_splitk(wq, ws, mode, S, part, M=B, cfg=cfg, **acts)
             lk.lk_splitk_combine(mode, part, S, B, N, y)
         else:
-            n = lk.lk_gemv_q8(wq, ws, mode, y, M=B, argmax_parts=parts, **({"x": xn} if xn is not None and a.norm
-                                                                            else acts))
+            n = lk.lk_gemv_q8(wq, ws, mode, y, M=B, argmax_parts=parts, cfg=cfg,
+                              **({"x": xn} if xn is not None and a.norm else acts))
             if a.argmax:
                 lk.lk_argmax(idx, B, N, parts=parts, n_parts=n)
 
@@ -610,7 +605,8 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
            "clocks": clk,
            "gpu_launches": a.steps * Rg * (1 + (1 if (S > 1 or a.argmax) else 0) + (1 if a.norm and not a.fused else 0)),
            "kernel": {1: "direct", 2: "ring", 3: "mma", 0: "none"}[lk.lk_gemv_kernel_for(N, K, mode, B,
-                                                                                          S if S > 1 else 0)]}
+                                                                                          S if S > 1 else 0,
+                                                                                          cfg=cfg)]}
     del mats
     torch.cuda.empty_cache()
     if rank == 0 and not quiet:
@@ -675,7 +671,7 @@ def measure_sequences(a, forms, dev):
     peaks, _ = measured_peaks()
     out = []
     for batch, mode, glu in forms:
-        st = DecodeStack(layers=a.layers, batch=batch, mode=mode, device=dev, glu=glu)
+        st = DecodeStack(layers=a.layers, batch=batch, mode=mode, device=dev, glu=glu, pdl=True)
         s = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(s):
             st.run_token()

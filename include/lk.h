@@ -13,13 +13,20 @@
  *     keeps only a small per-device cache of device attributes.
  *   - Every call is asynchronous on the given stream (0 = the legacy default
  *     stream) and never synchronizes, except lk_device_error.
+ *   - Every call that launches a configurable kernel takes its launch
+ *     settings as `const lk_launch_cfg* cfg`, just before the stream (NULL:
+ *     the defaults).  Kernel choice and launch form depend only on the
+ *     call's arguments and cfg: the library keeps no setting between calls
+ *     apart from the two diagnostic options of lk_set_option, which change
+ *     neither.
  *   - Arguments are validated before anything is launched; a failed check
  *     returns a negative status and launches nothing.  A launch failure
  *     reported by the CUDA runtime returns LK_ERR_CUDA.
  *   - Layouts are row-major and dense:
  *       wq  int8   [N][K]       weight levels of a Q8_0 matrix
  *       ws  uint16 [N][K/32]    f16 bit patterns, one scale per 32 weights
- *       x   f32    [M][K]       activation rows (M <= LK_MAX_M)
+ *       x   f32    [M][K]       activation rows (M <= LK_MAX_BATCH; per call
+ *                               below: most kernels take M <= LK_MAX_M)
  *       xq  int8   [M][K]       high words of the quantized activation
  *       xl  int8   [M][K]       low words (TwoPassInt8 only)
  *       xs  f32    [M][K/32]    one activation scale per 32 values
@@ -62,22 +69,57 @@ typedef int lk_status;
 #define LK_TRACE_REC  8   /* entries of one launch record of option "trace" 3 */
 
 /*
- * Per-call launch settings of the GEMV entry points with an `_ex` suffix
- * (NULL: the process options, lk_set_option).  The library's own design,
- * with no counterpart on the pages.
- *   pdl      -1: the option "pdl"; 0: an ordinary launch; 1: a programmatic
- *            dependent launch of the kernel before it on the stream (it starts
- *            while that kernel finishes, streams weights meanwhile and reads
- *            its activation and writes its outputs only after it)
- *   prefill  warps (four-warp groups in the tensor-core kernel's four-warp
- *            layout) of a block that issue their first weight stages before
- *            the dependency wait (0: the option "ring_prefill", whose default
- *            is half of them)
- * Errors: LK_ERR_ARG for pdl outside -1..1 or a negative prefill.
+ * Per-call launch settings (the library's own design, with no counterpart on
+ * the pages).  Zero in every field is the default; NULL means all defaults.
+ *   pdl        0: an ordinary launch; 1: a programmatic dependent launch of
+ *              the kernel before it on the stream (it starts while that kernel
+ *              finishes; GEMVs stream weights meanwhile; every kernel reads
+ *              its inputs and writes its outputs only after that kernel)
+ *   prefill    warps (four-warp groups in the tensor-core kernel's four-warp
+ *              layout) of a GEMV block that issue their first weight stages
+ *              before the dependency wait (0: half of them)
+ *   path       GEMV kernel: 0 the library's choice, 1 the direct-load kernel,
+ *              2 the bulk-copy ring kernel, 3 the tensor-core kernel (2 to
+ *              LK_MAX_BATCH rows); a forced kernel that does not take the
+ *              shape gives LK_ERR_SHAPE
+ *   grid_ctas  blocks of a ring or tensor-core launch along the rows
+ *              (0: one per SM; a launch that writes argmax keys takes at most
+ *              lk_argmax_parts_max(N), else LK_ERR_ARG)
+ *   ring_tk    ring kernel: bytes of K per stage for rows longer than that, a
+ *              multiple of 1024 up to 8192 (0: whole rows up to 8192, else
+ *              4096)
+ *   mma_min_m  fewest activation rows that take the tensor-core kernel under
+ *              path 0 (0: 2; LK_MAX_BATCH + 1: never)
+ *   mma_tk     tensor-core kernel: bytes of K per ring stage (0 auto, else a
+ *              multiple of 256 up to 8192)
+ *   mma_warps  its warps per block (0 auto, else 1..16)
+ *   mma_depth  its ring stages per warp (0: 1, else 1..8)
+ *   mma_i8     its dots on the int8 tensor path (mma m16n8k32 s8 on the
+ *              levels as they are) or the f16 path (f16 MMAs on converted
+ *              levels): 0 auto (int8 for Int8Act with 8+ tiles of 16 rows per
+ *              SM), 1 int8, 2 f16
+ *   mma_group  its warps per 16-row tile: 0 auto, 1 one warp per tile, 4 four
+ *              warps per tile (each one partial b mod 4; for launches with few
+ *              tiles per SM)
+ *   mma_act16  its activation rows held in shared memory as f16 (0 auto:
+ *              where that leaves room for 8 warps; 1 whenever they fit; 2
+ *              never: int8, converted per use)
+ * Errors: LK_ERR_ARG for a field outside its range.  Every setting gives the
+ * same bits: only speed depends on them.
  */
 typedef struct {
   int pdl;
   int prefill;
+  int path;
+  int grid_ctas;
+  int ring_tk;
+  int mma_min_m;
+  int mma_tk;
+  int mma_warps;
+  int mma_depth;
+  int mma_i8;
+  int mma_group;
+  int mma_act16;
 } lk_launch_cfg;
 
 /* A static, human-readable name of a status. */
@@ -105,7 +147,7 @@ int lk_version(void);
  */
 lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, float eps,
                            lk_mode mode, float* xn, int8_t* xq, int8_t* xl, float* xs,
-                           cudaStream_t stream);
+                           const lk_launch_cfg* cfg, cudaStream_t stream);
 
 /*
  * Residual add, then lk_rmsnorm_quant of the sum: the step between a
@@ -122,7 +164,7 @@ lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, floa
  */
 lk_status lk_add_rmsnorm_quant(const float* x, const float* r, const float* gain, int M, int K, float eps,
                                lk_mode mode, float* s, float* xn, int8_t* xq, int8_t* xl, float* xs,
-                               cudaStream_t stream);
+                               const lk_launch_cfg* cfg, cudaStream_t stream);
 
 /*
  * The gated activation between a decoder's gate/up and down projections,
@@ -139,7 +181,7 @@ lk_status lk_add_rmsnorm_quant(const float* x, const float* r, const float* gain
  * F must be a multiple of 32 (LK_ERR_SHAPE); 0 <= M <= LK_MAX_M.
  */
 lk_status lk_swiglu_quant(const float* gate, const float* up, int M, int F, long ld, lk_mode mode, float* h,
-                          int8_t* hq, int8_t* hl, float* hs, cudaStream_t stream);
+                          int8_t* hq, int8_t* hl, float* hs, const lk_launch_cfg* cfg, cudaStream_t stream);
 
 /*
  * The activation quantizer alone ("kernels.rs" QUANT lk_quant, PRELUDE
@@ -154,7 +196,7 @@ lk_status lk_swiglu_quant(const float* gate, const float* up, int M, int F, long
  * argument error (nothing to quantize).
  */
 lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq, int8_t* xl,
-                          float* xs, cudaStream_t stream);
+                          float* xs, const lk_launch_cfg* cfg, cudaStream_t stream);
 
 /*
  * y = W x for M <= 8 activation rows that share each weight read
@@ -185,13 +227,8 @@ lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq
  */
 lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
                      const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
-                     float* y, uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream);
-
-/* lk_gemv_q8 with per-call launch settings (cfg may be NULL). */
-lk_status lk_gemv_q8_ex(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
-                        const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
-                        float* y, uint64_t* argmax_parts, int* n_parts_out, const lk_launch_cfg* cfg,
-                        cudaStream_t stream);
+                     float* y, uint64_t* argmax_parts, int* n_parts_out, const lk_launch_cfg* cfg,
+                     cudaStream_t stream);
 
 /* One matrix of a grouped GEMV. */
 typedef struct {
@@ -220,12 +257,8 @@ typedef struct {
  * error lk_gemv_q8 reports for a target.
  */
 lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
-                           const int8_t* xq, const int8_t* xl, const float* xs, int M, cudaStream_t stream);
-
-/* lk_gemv_q8_group with per-call launch settings (cfg may be NULL). */
-lk_status lk_gemv_q8_group_ex(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
-                              const int8_t* xq, const int8_t* xl, const float* xs, int M, const lk_launch_cfg* cfg,
-                              cudaStream_t stream);
+                           const int8_t* xq, const int8_t* xl, const float* xs, int M, const lk_launch_cfg* cfg,
+                           cudaStream_t stream);
 
 /*
  * The gated projection pair of a decoder's MLP with the SwiGLU and the
@@ -257,13 +290,8 @@ lk_status lk_gemv_q8_group_ex(const lk_gemv_target* targets, int n, int K, lk_mo
  */
 lk_status lk_gemv_q8_glu(const int8_t* wg, const uint16_t* wsg, const int8_t* wu, const uint16_t* wsu, int F, int K,
                          lk_mode mode, const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
-                         float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt, cudaStream_t stream);
-
-/* lk_gemv_q8_glu with per-call launch settings (cfg may be NULL). */
-lk_status lk_gemv_q8_glu_ex(const int8_t* wg, const uint16_t* wsg, const int8_t* wu, const uint16_t* wsu, int F,
-                            int K, lk_mode mode, const float* x, const int8_t* xq, const int8_t* xl, const float* xs,
-                            int M, float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt,
-                            const lk_launch_cfg* cfg, cudaStream_t stream);
+                         float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt, const lk_launch_cfg* cfg,
+                         cudaStream_t stream);
 
 /*
  * RMSNorm -> quantize -> GEMV in one launch: every block of the bulk-copy
@@ -279,13 +307,14 @@ lk_status lk_gemv_q8_glu_ex(const int8_t* wg, const uint16_t* wsg, const int8_t*
  *   y, argmax_parts, n_parts_out   as lk_gemv_q8
  * Needs the ring kernel: K % 256 == 0 and the activation area fitting in
  * shared memory (lk_gemv_kernel_for(...) == 2); otherwise LK_ERR_SHAPE.  With
- * the option "pdl" set, the launch is a programmatic dependent launch: its
- * weight stream starts while the previous kernel on the stream finishes, and
- * it reads x only after that kernel has completed.
+ * cfg->pdl set, the launch is a programmatic dependent launch: its weight
+ * stream starts while the previous kernel on the stream finishes, and it
+ * reads x only after that kernel has completed.  cfg->path must be 0 or 2.
  */
 lk_status lk_rmsnorm_quant_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
                                    const float* x, const float* gain, float eps, int M, float* y,
-                                   uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream);
+                                   uint64_t* argmax_parts, int* n_parts_out, const lk_launch_cfg* cfg,
+                                   cudaStream_t stream);
 
 /*
  * One step of a GEMV chain: RMSNorm (gain != NULL) or the quantizer alone
@@ -326,22 +355,25 @@ size_t lk_chain_sync_bytes(void);
  * Every grid-barrier wait is bounded (option "wait_us"); a timeout sets the
  * device error word (lk_device_error).  LK_ERR_SHAPE if a step's K is not a
  * multiple of 256 or the largest activation area does not fit in shared
- * memory next to four weight stages.
+ * memory next to four weight stages.  cfg: pdl applies to a chain without
+ * barriers (a chain with barriers is always a cooperative launch), prefill
+ * as for the ring kernel; the other fields do not apply (one block per SM).
  */
 lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* ops_dev, int n_ops, lk_mode mode, int M,
-                        float eps, uint32_t* sync, cudaStream_t stream);
+                        float eps, uint32_t* sync, const lk_launch_cfg* cfg, cudaStream_t stream);
 
 /*
- * Which GEMV kernel a call of this shape would launch under the current
- * options, for 16-byte aligned operands: 1 the direct-load kernel (any
- * K % 32 == 0), 2 the bulk-copy ring kernel (K % 256 == 0 and the activation
- * fits in shared memory), 3 the tensor-core kernel (lk_gemv_q8 only:
- * LK_INT8ACT or LK_TWOPASS, 2 <= M <= 8 (option "mma_min_m"), K % 256 == 0
- * and the activation fitting in shared memory next to a weight ring), 0 none
- * (invalid shape, or a kernel forced by "gemv_path" but not applicable).
- * S = 0 asks about lk_gemv_q8, S >= 1 about lk_gemv_q8_splitk.
+ * Which GEMV kernel a call of this shape would launch with these settings,
+ * for 16-byte aligned operands: 1 the direct-load kernel (any K % 32 == 0,
+ * M <= LK_MAX_M), 2 the bulk-copy ring kernel (K % 256 == 0 and the
+ * activation fits in shared memory), 3 the tensor-core kernel (lk_gemv_q8
+ * only: LK_INT8ACT or LK_TWOPASS, cfg->mma_min_m (default 2) <= M <=
+ * LK_MAX_BATCH, K % 256 == 0 and the activation fitting in shared memory
+ * next to a weight ring), 0 none (invalid shape or settings, or a kernel
+ * forced by cfg->path but not applicable).  S = 0 asks about lk_gemv_q8,
+ * S >= 1 about lk_gemv_q8_splitk.  cfg may be NULL (the defaults).
  */
-int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S);
+int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S, const lk_launch_cfg* cfg);
 
 /*
  * Bytes of the split-K partial buffer for (mode, S, M, N): S*M*N values,
@@ -361,7 +393,8 @@ size_t lk_splitk_workspace_bytes(lk_mode mode, int S, int M, int N);
  */
 lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
                             const float* x, const int8_t* xq, const int8_t* xl, const float* xs,
-                            int M, int S, void* part, size_t part_bytes, cudaStream_t stream);
+                            int M, int S, void* part, size_t part_bytes, const lk_launch_cfg* cfg,
+                            cudaStream_t stream);
 
 /*
  * The split-K combine (QWEN38_EXTRA_KERNELS gk_sk_combine): a separate
@@ -430,70 +463,30 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
                            int32_t* d, int32_t* e, cudaStream_t stream);
 
 /*
- * Tuning and test options (process-wide; not thread-safe against concurrent
- * launches).  Names:
- *   "gemv_path"   0 auto, 1 direct-load kernel, 2 bulk-copy ring kernel,
- *                 3 tensor-core kernel (2..8 rows; LK_ERR_SHAPE elsewhere)
- *   "ring_stages" ring depth of the bulk-copy kernel (0 = as deep as shared
- *                 memory allows, at most 32)
- *   "grid_ctas"   blocks of the ring kernel (0 = one per SM)
- *   "ring_hint"   1 (default): L2 evict-first hint on the ring's weight
- *                 copies; 0: no hint
- *   "ring_warps"  warps per block of the ring kernel: 0 auto, else 1..12
- *   "ring_kb"     cap on the ring kernel's shared memory per block, KB (0 none)
- *   "ring_cps"    ring blocks per SM in the grid, 1..4 (default 1)
- *   "pdl"         1: launches are programmatic dependent launches of the
- *                 kernel before them on the stream (GEMV kernels, the fused
- *                 launch, chains without barriers, lk_rmsnorm_quant and
- *                 lk_quantize_act): each starts while its predecessor
- *                 finishes (GEMVs stream weights meanwhile) and reads its
- *                 inputs and writes its outputs only after it (default 0)
+ * The two diagnostic options (process-wide).  Neither changes which kernel a
+ * call launches, how it is launched or any result; launch settings are per
+ * call (lk_launch_cfg).  Names:
  *   "trace"       1: the ring and chain kernels write block 0's timestamps
  *                 to the trace buffer (lk_trace_read); 2: the chain also
  *                 records every block's and block 0's warps' step ends, and
  *                 when block 0's warps' first stage of each step was there
  *                 and computed (from index 2048);
- *                 3: launch timeline: every ring, chain and tensor-core
- *                 launch made after the option was set owns a record of
- *                 LK_TRACE_REC entries (in launch order, 512 records,
- *                 wrapping):
+ *                 3: launch timeline: every ring, chain, tensor-core, norm
+ *                 and quantize launch made after the option was set owns a
+ *                 record of LK_TRACE_REC entries (in launch order, 512
+ *                 records, wrapping):
  *                 [0] block 0 start, [1] block 0 past the wait on the
  *                 previous kernel (fused launches: the prologue's start; it
  *                 waits inside, after requesting the norm gains), [2] block
- *                 0's activation ready, [3] the
- *                 last block's end, [4] block 0's end (all %globaltimer ns),
- *                 [5] kernel (1 ring, 2 chain, 3 tensor-core, 4 norm,
- *                 5 quantize), [6] rows (steps, for a chain), [7] block 0's
- *                 first weight stages issued.  Setting the option restarts
- *                 the record count.
+ *                 0's activation ready, [3] the last block's end, [4] block
+ *                 0's end (all %globaltimer ns), [5] kernel (1 ring, 2 chain,
+ *                 3 tensor-core, 4 norm, 5 quantize), [6] rows (steps, for a
+ *                 chain), [7] block 0's first weight stages issued.  Setting
+ *                 the option restarts the record count.
  *   "wait_us"     time limit of every device-side wait, microseconds
- *                 (0 = default, 2 s)
- *   "mma_min_m"   fewest activation rows lk_gemv_q8 runs on the tensor-core
- *                 kernel (0 = default 2; 9 = never)
- *   "mma_tk"      its bytes of K per ring stage: 0 auto (512, else 256),
- *                 else a multiple of 256 up to 8192
- *   "mma_warps"   its warps per block: 0 auto, else 1..16
- *   "mma_depth"   its ring stages per warp: 0 = 1, else 1..8
- *   "mma_i8"      its dots on the int8 tensor path (mma m16n8k32 s8, the
- *                 levels as they are) instead of f16 MMAs on converted
- *                 levels: 0 auto (Int8Act with 8+ tiles of 16 rows per
- *                 SM), 1 always, 2 never
- *   "mma_group"   its warps per 16-row tile: 0 auto, 1 one warp per tile, 4
- *                 four warps per tile (each one partial b mod 4; for
- *                 launches with few tiles per SM)
- *   "mma_act16"   its activation rows held in shared memory as f16 (0 auto:
- *                 where that leaves room for 8 warps; 1 whenever they fit;
- *                 2 never: int8, converted per use)
- *   "ring_prefill" GEMV kernels: warps of a block that issue their first
- *                 weight stages before the wait on the previous kernel; the
- *                 others issue theirs once the activation is loaded (0 =
- *                 half of the warps, the default; 12 or 16 = all)
- *   "ring_tk"     ring kernel: bytes of K per stage for rows longer than
- *                 that, a multiple of 1024 up to 8192 (0 = auto: whole rows
- *                 up to 8192, else 4096)
- *   "group_prefill" the same for a grouped launch (lk_gemv_q8_group on the
- *                 ring path): 0 = as "ring_prefill", else that many warps
- * Unknown names or out-of-range values return LK_ERR_ARG.
+ *                 (0 = default, 2 s; at most 6 * 10^7)
+ * Unknown names or out-of-range values return LK_ERR_ARG; lk_get_option
+ * returns -1 for an unknown name.
  */
 lk_status lk_set_option(const char* name, long value);
 long lk_get_option(const char* name);

@@ -12,26 +12,8 @@ using namespace lk;
 
 namespace lkh {
 
-long opt_gemv_path = 0;
-long opt_ring_stages = 0;
-long opt_grid_ctas = 0;
 long opt_wait_us = 0;
-long opt_ring_hint = 1;
-long opt_ring_warps = 0;
-long opt_ring_kb = 0;
-long opt_ring_cps = 1;
 long opt_trace = 0;
-long opt_pdl = 0;
-long opt_mma_min_m = 0;
-long opt_mma_tk = 0;
-long opt_mma_warps = 0;
-long opt_mma_depth = 0;
-long opt_ring_prefill = 0;
-long opt_group_prefill = 0;
-long opt_ring_tk = 0;
-long opt_mma_act16 = 0;
-long opt_mma_group = 0;
-long opt_mma_i8 = 0;
 
 // Per-device attributes, queried once per device under a lock (concurrent
 // first calls are safe).
@@ -61,7 +43,15 @@ const DeviceInfo* device_info(int* dev_out) {
 
 lk_status check_launch_cfg(const lk_launch_cfg* cfg) {
   if (!cfg) return LK_OK;
-  if (cfg->pdl < -1 || cfg->pdl > 1 || cfg->prefill < 0) return LK_ERR_ARG;
+  const lk_launch_cfg& c = *cfg;
+  if (c.pdl < 0 || c.pdl > 1 || c.prefill < 0 || c.prefill > 16 || c.path < 0 || c.path > 3) return LK_ERR_ARG;
+  if (c.grid_ctas < 0 || c.grid_ctas > (1 << 20)) return LK_ERR_ARG;
+  if (c.ring_tk < 0 || c.ring_tk > 8192 || c.ring_tk % 1024) return LK_ERR_ARG;
+  if (c.mma_min_m < 0 || c.mma_min_m > LK_MAX_BATCH + 1) return LK_ERR_ARG;
+  if (c.mma_tk < 0 || c.mma_tk > 8192 || c.mma_tk % 256) return LK_ERR_ARG;
+  if (c.mma_warps < 0 || c.mma_warps > 16 || c.mma_depth < 0 || c.mma_depth > 8) return LK_ERR_ARG;
+  if (c.mma_i8 < 0 || c.mma_i8 > 2 || c.mma_act16 < 0 || c.mma_act16 > 2) return LK_ERR_ARG;
+  if (c.mma_group != 0 && c.mma_group != 1 && c.mma_group != 4) return LK_ERR_ARG;
   return LK_OK;
 }
 
@@ -105,67 +95,13 @@ int lk_version(void) { return 100; }
 
 lk_status lk_set_option(const char* name, long value) {
   if (!name) return LK_ERR_ARG;
-  if (!strcmp(name, "gemv_path")) {
-    if (value < 0 || value > 3) return LK_ERR_ARG;
-    opt_gemv_path = value;
-  } else if (!strcmp(name, "ring_stages")) {
-    if (value < 0 || value > 32) return LK_ERR_ARG;
-    opt_ring_stages = value;
-  } else if (!strcmp(name, "grid_ctas")) {
-    if (value < 0 || value > (1L << 20)) return LK_ERR_ARG;
-    opt_grid_ctas = value;
-  } else if (!strcmp(name, "ring_warps")) {
-    if (value < 0 || value > 12) return LK_ERR_ARG;
-    opt_ring_warps = value;
-  } else if (!strcmp(name, "ring_kb")) {
-    if (value < 0 || value > 1024) return LK_ERR_ARG;
-    opt_ring_kb = value;
-  } else if (!strcmp(name, "ring_cps")) {
-    if (value < 1 || value > 4) return LK_ERR_ARG;
-    opt_ring_cps = value;
-  } else if (!strcmp(name, "pdl")) {
-    if (value < 0 || value > 1) return LK_ERR_ARG;
-    opt_pdl = value;
-  } else if (!strcmp(name, "trace")) {
+  if (!strcmp(name, "trace")) {
     if (value < 0 || value > 3) return LK_ERR_ARG;
     opt_trace = value;
     trace_reset();
-  } else if (!strcmp(name, "ring_hint")) {
-    if (value < 0 || value > 1) return LK_ERR_ARG;
-    opt_ring_hint = value;
   } else if (!strcmp(name, "wait_us")) {
     if (value < 0 || value > 60000000L) return LK_ERR_ARG;
     opt_wait_us = value;
-  } else if (!strcmp(name, "mma_min_m")) {
-    if (value < 0 || value > LK_MAX_M + 1) return LK_ERR_ARG;
-    opt_mma_min_m = value;
-  } else if (!strcmp(name, "mma_tk")) {
-    if (value < 0 || value > 8192 || value % 256) return LK_ERR_ARG;
-    opt_mma_tk = value;
-  } else if (!strcmp(name, "mma_warps")) {
-    if (value < 0 || value > 16) return LK_ERR_ARG;
-    opt_mma_warps = value;
-  } else if (!strcmp(name, "mma_depth")) {
-    if (value < 0 || value > 8) return LK_ERR_ARG;
-    opt_mma_depth = value;
-  } else if (!strcmp(name, "mma_i8")) {
-    if (value < 0 || value > 2) return LK_ERR_ARG;
-    opt_mma_i8 = value;
-  } else if (!strcmp(name, "mma_group")) {
-    if (value != 0 && value != 1 && value != 4) return LK_ERR_ARG;
-    opt_mma_group = value;
-  } else if (!strcmp(name, "mma_act16")) {
-    if (value < 0 || value > 2) return LK_ERR_ARG;
-    opt_mma_act16 = value;
-  } else if (!strcmp(name, "ring_prefill")) {
-    if (value < 0 || value > 12) return LK_ERR_ARG;
-    opt_ring_prefill = value;
-  } else if (!strcmp(name, "ring_tk")) {
-    if (value < 0 || value > 8192 || value % 1024) return LK_ERR_ARG;
-    opt_ring_tk = value;
-  } else if (!strcmp(name, "group_prefill")) {
-    if (value < 0 || value > 16) return LK_ERR_ARG;
-    opt_group_prefill = value;
   } else {
     return LK_ERR_ARG;
   }
@@ -174,32 +110,15 @@ lk_status lk_set_option(const char* name, long value) {
 
 long lk_get_option(const char* name) {
   if (!name) return -1;
-  if (!strcmp(name, "gemv_path")) return opt_gemv_path;
-  if (!strcmp(name, "ring_stages")) return opt_ring_stages;
-  if (!strcmp(name, "grid_ctas")) return opt_grid_ctas;
-  if (!strcmp(name, "wait_us")) return opt_wait_us;
-  if (!strcmp(name, "ring_hint")) return opt_ring_hint;
   if (!strcmp(name, "trace")) return opt_trace;
-  if (!strcmp(name, "ring_warps")) return opt_ring_warps;
-  if (!strcmp(name, "ring_kb")) return opt_ring_kb;
-  if (!strcmp(name, "ring_cps")) return opt_ring_cps;
-  if (!strcmp(name, "pdl")) return opt_pdl;
-  if (!strcmp(name, "mma_min_m")) return opt_mma_min_m;
-  if (!strcmp(name, "mma_tk")) return opt_mma_tk;
-  if (!strcmp(name, "mma_warps")) return opt_mma_warps;
-  if (!strcmp(name, "mma_depth")) return opt_mma_depth;
-  if (!strcmp(name, "ring_prefill")) return opt_ring_prefill;
-  if (!strcmp(name, "group_prefill")) return opt_group_prefill;
-  if (!strcmp(name, "ring_tk")) return opt_ring_tk;
-  if (!strcmp(name, "mma_act16")) return opt_mma_act16;
-  if (!strcmp(name, "mma_group")) return opt_mma_group;
-  if (!strcmp(name, "mma_i8")) return opt_mma_i8;
+  if (!strcmp(name, "wait_us")) return opt_wait_us;
   return -1;
 }
 
 lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq, int8_t* xl,
-                          float* xs, cudaStream_t stream) {
+                          float* xs, const lk_launch_cfg* cfg, cudaStream_t stream) {
   if (mode != LK_INT8ACT && mode != LK_TWOPASS) return LK_ERR_ARG;
+  if (check_launch_cfg(cfg)) return LK_ERR_ARG;
   if (M < 0 || M > LK_MAX_BATCH || K < 0 || K % 32) return LK_ERR_SHAPE;
   if (M == 0 || K == 0) return LK_OK;
   if (!x) return LK_ERR_ARG;
@@ -210,10 +129,11 @@ lk_status lk_quantize_act(const float* x, int M, int K, lk_mode mode, int8_t* xq
   const int per_block = 8;
   const long blocks = (groups + per_block - 1) / per_block;
   if (mode == LK_INT8ACT)
-    launch_pdl(quantize_kernel<1>, dim3((unsigned)blocks), dim3(32 * per_block), stream, x, groups, xq,
-               (int8_t*)nullptr, xs, tr_ptr(), tr_slot());
+    launch_pdl(quantize_kernel<1>, dim3((unsigned)blocks), dim3(32 * per_block), stream, cfg_pdl(cfg), x, groups,
+               xq, (int8_t*)nullptr, xs, tr_ptr(), tr_slot());
   else
-    launch_pdl(quantize_kernel<2>, dim3((unsigned)blocks), dim3(32 * per_block), stream, x, groups, xq, xl, xs, tr_ptr(), tr_slot());
+    launch_pdl(quantize_kernel<2>, dim3((unsigned)blocks), dim3(32 * per_block), stream, cfg_pdl(cfg), x, groups,
+               xq, xl, xs, tr_ptr(), tr_slot());
   return launch_status();
 }
 

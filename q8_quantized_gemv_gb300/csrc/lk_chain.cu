@@ -354,7 +354,8 @@ extern "C" size_t lk_chain_sync_bytes(void) { return 256; }
 // Launch the chain kernel over `ops` (host copies; ops_dev their device copy,
 // or NULL with the ops carried in the launch arguments: a group).
 static lk_status chain_launch(const lk_chain_op* ops, const lk_chain_op* ops_dev, int n_ops, lk_mode mode, int M,
-                              float eps, uint32_t* sync, const lkh::GemvProblem* given, cudaStream_t stream) {
+                              float eps, uint32_t* sync, const lkh::GemvProblem* given, const lk_launch_cfg& lc,
+                              cudaStream_t stream) {
   unsigned act_cap = 0, sb = 0;
   for (int i = 0; i < n_ops; ++i) {
     const unsigned a = act_area_rt(mode, M, (unsigned)ops[i].K), s = stage_bytes_for(ops[i].K);
@@ -364,14 +365,10 @@ static lk_status chain_launch(const lk_chain_op* ops, const lk_chain_op* ops_dev
   const lkh::DeviceInfo* d = lkh::device_info(nullptr);
   if (!d) return LK_ERR_CUDA;
   const unsigned ring_off = (act_cap + 127u) & ~127u;
-  long cap = d->smem_optin;
-  if (lkh::opt_ring_kb > 0 && lkh::opt_ring_kb * 1024 < cap) cap = lkh::opt_ring_kb * 1024;
-  const long room = cap - (long)ring_off - (long)TAIL;
+  const long room = (long)d->smem_optin - (long)ring_off - (long)TAIL;
   int fit = room > 0 ? (int)(room / sb) : 0;
   if (fit > MAX_STAGES) fit = MAX_STAGES;
-  if (lkh::opt_ring_stages > 0 && lkh::opt_ring_stages < fit) fit = (int)lkh::opt_ring_stages;
-  int w = lkh::opt_ring_warps > 0 ? (int)lkh::opt_ring_warps : (fit < MAXW ? fit : MAXW);
-  if (w > fit) w = fit;
+  const int w = fit < MAXW ? fit : MAXW;
   const int depth = w > 0 ? fit / w : 0;
   if (w < 1 || w * depth < 4) return LK_ERR_SHAPE;
   const unsigned total = ring_off + (unsigned)(w * depth) * sb + TAIL;
@@ -397,21 +394,20 @@ static lk_status chain_launch(const lk_chain_op* ops, const lk_chain_op* ops_dev
   ca.eps = eps;
   ca.sync = sync;
   ca.wait_ns = lkh::opt_wait_us > 0 ? (unsigned long long)lkh::opt_wait_us * 1000ull : 2000000000ull;
-  ca.pol_w = lkh::opt_ring_hint ? 1ull : 0ull;
+  ca.pol_w = 1ull;  // L2 evict-first on the weight copies
   ca.err = lkh::error_word_ptr();
   if (!ca.err) return LK_ERR_CUDA;
   ca.trace = lkh::opt_trace ? lkh::trace_ptr() : nullptr;
   ca.trace_all = lkh::opt_trace == 2;
   ca.tslot = lkh::opt_trace == 3 ? lkh::trace_next_slot() : -1;
-  ca.pdl = !barrier && (given ? given->pdl : (int)lkh::opt_pdl) ? 1 : 0;
-  ca.prefill = lkh::prefill_warps(w, given ? given->prefill : 0);
+  ca.pdl = !barrier && lc.pdl ? 1 : 0;
+  ca.prefill = lkh::prefill_warps(w, lc.prefill);
   ca.n_inl = 0;
   ca.gx = nullptr;
   ca.gxq = ca.gxl = nullptr;
   ca.gxs = nullptr;
   for (int i = 0; i < LK_MAX_GROUP; ++i) ca.inl[i] = ops[i < n_ops ? i : 0];
   if (given) {
-    if (lkh::opt_group_prefill > 0 && given->prefill == 0) ca.prefill = (int)lkh::opt_group_prefill;
     ca.n_inl = n_ops;
     ca.gx = given->x;
     ca.gxq = given->xq;
@@ -438,9 +434,9 @@ static lk_status chain_launch(const lk_chain_op* ops, const lk_chain_op* ops_dev
 }
 
 extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* ops_dev, int n_ops, lk_mode mode,
-                                   int M, float eps, uint32_t* sync, cudaStream_t stream) {
+                                   int M, float eps, uint32_t* sync, const lk_launch_cfg* cfg, cudaStream_t stream) {
   using lkh::aligned;
-  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS || lkh::check_launch_cfg(cfg)) return LK_ERR_ARG;
   if (M < 1 || M > LK_MAX_M || n_ops < 0) return LK_ERR_SHAPE;
   if (n_ops == 0) return LK_OK;
   if (!ops || !ops_dev || !sync) return LK_ERR_ARG;
@@ -454,7 +450,7 @@ extern "C" lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* op
         (o.argmax_idx && !aligned(o.argmax_idx, 4)))
       return LK_ERR_ALIGN;
   }
-  return chain_launch(ops, ops_dev, n_ops, mode, M, eps, sync, nullptr, stream);
+  return chain_launch(ops, ops_dev, n_ops, mode, M, eps, sync, nullptr, cfg ? *cfg : lk_launch_cfg{}, stream);
 }
 
 // A group of GEMVs over one given activation (p: K, mode, M and the
@@ -470,5 +466,5 @@ lk_status lkh::chain_group(const GemvProblem& p, const lk_gemv_target* t, int n,
     if (!aligned(t[i].wq, 16) || !aligned(t[i].ws, 16)) return LK_ERR_SHAPE;
     ops[i] = lk_chain_op{t[i].wq, t[i].ws, t[i].N, p.K, nullptr, nullptr, t[i].y, nullptr, nullptr, 0, 0};
   }
-  return chain_launch(ops, nullptr, n, (lk_mode)p.mode, p.M, 0.f, nullptr, &p, stream);
+  return chain_launch(ops, nullptr, n, (lk_mode)p.mode, p.M, 0.f, nullptr, &p, p.cfg, stream);
 }

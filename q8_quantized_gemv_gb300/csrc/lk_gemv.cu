@@ -250,13 +250,7 @@ extern "C" {
 
 lk_status lk_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode, const float* x,
                      const int8_t* xq, const int8_t* xl, const float* xs, int M, float* y,
-                     uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream) {
-  return lk_gemv_q8_ex(wq, ws, N, K, mode, x, xq, xl, xs, M, y, argmax_parts, n_parts_out, nullptr, stream);
-}
-
-lk_status lk_gemv_q8_ex(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode, const float* x,
-                        const int8_t* xq, const int8_t* xl, const float* xs, int M, float* y,
-                        uint64_t* argmax_parts, int* n_parts_out, const lk_launch_cfg* cfg, cudaStream_t stream) {
+                     uint64_t* argmax_parts, int* n_parts_out, const lk_launch_cfg* cfg, cudaStream_t stream) {
   lk_status st = check_common(wq, ws, N, K, mode, x, xq, xl, xs, M);
   if (st) return st;
   st = check_launch_cfg(cfg);
@@ -268,19 +262,22 @@ lk_status lk_gemv_q8_ex(const int8_t* wq, const uint16_t* ws, int N, int K, lk_m
   }
   if (!y) return LK_ERR_ARG;
   if (!aligned(y, 4) || (argmax_parts && !aligned(argmax_parts, 8))) return LK_ERR_ALIGN;
+  // the argmax keys are sized by lk_argmax_parts_max: no more blocks than that
+  if (argmax_parts && cfg && cfg->grid_ctas > lk_argmax_parts_max(N)) return LK_ERR_ARG;
   GemvProblem p = make_problem(wq, ws, N, K, mode, x, xq, xl, xs, M);
   apply_cfg(p, cfg);
   p.y = y;
   p.amax = (unsigned long long*)argmax_parts;
   int n_parts = 0;
-  if ((opt_gemv_path == 0 || opt_gemv_path == 3) && mma_supports(p)) {
+  const int path = p.cfg.path;
+  if ((path == 0 || path == 3) && mma_supports(p)) {
     st = mma_gemv(p, stream, &n_parts);
-  } else if (opt_gemv_path == 3 || M > LK_MAX_M) {
+  } else if (path == 3 || M > LK_MAX_M) {
     return LK_ERR_SHAPE;  // past 8 rows: the tensor-core kernel only
-  } else if (opt_gemv_path != 1 && ring_supports(p)) {
+  } else if (path != 1 && ring_supports(p)) {
     st = ring_gemv(p, stream, &n_parts);
   } else {
-    if (opt_gemv_path == 2) return LK_ERR_SHAPE;
+    if (path == 2) return LK_ERR_SHAPE;
     st = direct_gemv(p, stream, &n_parts);
   }
   if (n_parts_out) *n_parts_out = n_parts;
@@ -288,13 +285,8 @@ lk_status lk_gemv_q8_ex(const int8_t* wq, const uint16_t* ws, int N, int K, lk_m
 }
 
 lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
-                           const int8_t* xq, const int8_t* xl, const float* xs, int M, cudaStream_t stream) {
-  return lk_gemv_q8_group_ex(targets, n, K, mode, x, xq, xl, xs, M, nullptr, stream);
-}
-
-lk_status lk_gemv_q8_group_ex(const lk_gemv_target* targets, int n, int K, lk_mode mode, const float* x,
-                              const int8_t* xq, const int8_t* xl, const float* xs, int M, const lk_launch_cfg* cfg,
-                              cudaStream_t stream) {
+                           const int8_t* xq, const int8_t* xl, const float* xs, int M, const lk_launch_cfg* cfg,
+                           cudaStream_t stream) {
   if (!targets || n < 1 || n > LK_MAX_GROUP) return LK_ERR_ARG;
   {
     const lk_status st = check_launch_cfg(cfg);
@@ -310,15 +302,16 @@ lk_status lk_gemv_q8_group_ex(const lk_gemv_target* targets, int n, int K, lk_mo
   }
   if (M == 0 || K == 0) {
     for (int i = 0; i < n; ++i) {
-      lk_status st = lk_gemv_q8_ex(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M,
-                                   targets[i].y, nullptr, nullptr, cfg, stream);
+      lk_status st = lk_gemv_q8(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M,
+                                targets[i].y, nullptr, nullptr, cfg, stream);
       if (st) return st;
     }
     return LK_OK;
   }
   GemvProblem p = make_problem(targets[0].wq, targets[0].ws, targets[0].N, K, mode, x, xq, xl, xs, M);
   apply_cfg(p, cfg);
-  bool one = (opt_gemv_path == 0 || opt_gemv_path == 3);
+  const int path = p.cfg.path;
+  bool one = (path == 0 || path == 3);
   for (int i = 0; i < n && one; ++i) {
     GemvProblem q = p;
     q.wq = targets[i].wq;
@@ -340,21 +333,21 @@ lk_status lk_gemv_q8_group_ex(const lk_gemv_target* targets, int n, int K, lk_mo
     return mma_launch(p, n, wq, ws, N, y, stream, nullptr);
   }
   // one chain launch (the ring kernel's arrangement) where it takes the shape
-  if (n > 1 && (opt_gemv_path == 0 || opt_gemv_path == 2)) {
+  if (n > 1 && (path == 0 || path == 2)) {
     const lk_status st = chain_group(p, targets, n, stream);
     if (st != LK_ERR_SHAPE) return st;
   }
   for (int i = 0; i < n; ++i) {
-    lk_status st = lk_gemv_q8_ex(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M, targets[i].y,
-                                 nullptr, nullptr, cfg, stream);
+    lk_status st = lk_gemv_q8(targets[i].wq, targets[i].ws, targets[i].N, K, mode, x, xq, xl, xs, M, targets[i].y,
+                              nullptr, nullptr, cfg, stream);
     if (st) return st;
   }
   return LK_OK;
 }
 
-int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S) {
+int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S, const lk_launch_cfg* cfg) {
   if (mode < LK_DEQUANT || mode > LK_TWOPASS || N < 1 || K < 32 || K % 32 || M < 1 || M > LK_MAX_BATCH || S < 0 ||
-      S > LK_MAX_SPLITK || (M > LK_MAX_M && S > 0))
+      S > LK_MAX_SPLITK || (M > LK_MAX_M && S > 0) || check_launch_cfg(cfg))
     return 0;
   // 16-byte aligned stand-in pointers: only the shape decides
   const void* a16 = (const void*)(uintptr_t)256;
@@ -362,17 +355,21 @@ int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S) {
                                (const int8_t*)a16, (const int8_t*)a16, (const float*)a16, M);
   p.split = S > 0;
   p.S = S > 0 ? S : 1;
-  if (S == 0 && (opt_gemv_path == 0 || opt_gemv_path == 3) && mma_supports(p)) return 3;
+  apply_cfg(p, cfg);
+  const int path = p.cfg.path;
+  if (S == 0 && (path == 0 || path == 3) && mma_supports(p)) return 3;
   if (M > LK_MAX_M) return 0;
-  if (opt_gemv_path == 1) return 1;
-  if (opt_gemv_path == 3) return S == 0 ? 0 : (ring_supports(p) ? 2 : 1);
-  return ring_supports(p) ? 2 : (opt_gemv_path == 2 ? 0 : 1);
+  if (path == 1) return 1;
+  if (path == 3) return S == 0 ? 0 : (ring_supports(p) ? 2 : 1);
+  return ring_supports(p) ? 2 : (path == 2 ? 0 : 1);
 }
 
 lk_status lk_rmsnorm_quant_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
                                    const float* x, const float* gain, float eps, int M, float* y,
-                                   uint64_t* argmax_parts, int* n_parts_out, cudaStream_t stream) {
-  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+                                   uint64_t* argmax_parts, int* n_parts_out, const lk_launch_cfg* cfg,
+                                   cudaStream_t stream) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS || check_launch_cfg(cfg)) return LK_ERR_ARG;
+  if (cfg && cfg->path != 0 && cfg->path != 2) return LK_ERR_SHAPE;
   if (N < 0 || K < 0 || K % 32 || M < 0 || M > LK_MAX_M) return LK_ERR_SHAPE;
   if (argmax_parts && !n_parts_out) return LK_ERR_ARG;
   if (N == 0 || M == 0) {
@@ -383,7 +380,9 @@ lk_status lk_rmsnorm_quant_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, 
   if (!aligned(wq, 16) || !aligned(ws, 2) || !aligned(x, 4) || (gain && !aligned(gain, 4)) || !aligned(y, 4) ||
       (argmax_parts && !aligned(argmax_parts, 8)))
     return LK_ERR_ALIGN;
+  if (argmax_parts && cfg && cfg->grid_ctas > lk_argmax_parts_max(N)) return LK_ERR_ARG;
   GemvProblem p = make_problem(wq, ws, N, K, mode, nullptr, nullptr, nullptr, nullptr, M);
+  apply_cfg(p, cfg);
   p.fuse = true;
   p.xraw = x;
   p.gain = gain;
@@ -399,14 +398,8 @@ lk_status lk_rmsnorm_quant_gemv_q8(const int8_t* wq, const uint16_t* ws, int N, 
 
 lk_status lk_gemv_q8_glu(const int8_t* wg, const uint16_t* wsg, const int8_t* wu, const uint16_t* wsu, int F, int K,
                          lk_mode mode, const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
-                         float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt, cudaStream_t stream) {
-  return lk_gemv_q8_glu_ex(wg, wsg, wu, wsu, F, K, mode, x, xq, xl, xs, M, gu, h, hq, hl, hs, cnt, nullptr, stream);
-}
-
-lk_status lk_gemv_q8_glu_ex(const int8_t* wg, const uint16_t* wsg, const int8_t* wu, const uint16_t* wsu, int F,
-                            int K, lk_mode mode, const float* x, const int8_t* xq, const int8_t* xl, const float* xs,
-                            int M, float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt,
-                            const lk_launch_cfg* cfg, cudaStream_t stream) {
+                         float* gu, float* h, int8_t* hq, int8_t* hl, float* hs, int* cnt, const lk_launch_cfg* cfg,
+                         cudaStream_t stream) {
   lk_status st = check_common(wg, wsg, F, K, mode, x, xq, xl, xs, M);
   if (st) return st;
   st = check_launch_cfg(cfg);
@@ -423,7 +416,7 @@ lk_status lk_gemv_q8_glu_ex(const int8_t* wg, const uint16_t* wsg, const int8_t*
     st = check_act_out(mode, hq, hl, hs);
     if (st) return st;
   }
-  if (K > 0 && opt_gemv_path == 0) {
+  if (K > 0 && (!cfg || cfg->path == 0)) {
     GemvProblem p = make_problem(wg, wsg, 2 * F, K, mode, x, xq, xl, xs, M);
     apply_cfg(p, cfg);
     p.y = gu;
@@ -440,9 +433,9 @@ lk_status lk_gemv_q8_glu_ex(const int8_t* wg, const uint16_t* wsg, const int8_t*
   // two launches: both GEMVs (one grouped launch where the kernels allow),
   // then the SwiGLU -> quantize step over their outputs
   const lk_gemv_target t[2] = {{wg, wsg, F, 0, gu}, {wu, wsu, F, 0, gu + (long)M * F}};
-  st = lk_gemv_q8_group_ex(t, 2, K, mode, x, xq, xl, xs, M, cfg, stream);
+  st = lk_gemv_q8_group(t, 2, K, mode, x, xq, xl, xs, M, cfg, stream);
   if (st) return st;
-  return lk_swiglu_quant(gu, gu + (long)M * F, M, F, F, mode, h, hq, hl, hs, stream);
+  return lk_swiglu_quant(gu, gu + (long)M * F, M, F, F, mode, h, hq, hl, hs, cfg, stream);
 }
 
 size_t lk_splitk_workspace_bytes(lk_mode mode, int S, int M, int N) {
@@ -452,8 +445,11 @@ size_t lk_splitk_workspace_bytes(lk_mode mode, int S, int M, int N) {
 
 lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
                             const float* x, const int8_t* xq, const int8_t* xl, const float* xs, int M,
-                            int S, void* part, size_t part_bytes, cudaStream_t stream) {
+                            int S, void* part, size_t part_bytes, const lk_launch_cfg* cfg,
+                            cudaStream_t stream) {
   lk_status st = check_common(wq, ws, N, K, mode, x, xq, xl, xs, M);
+  if (st) return st;
+  st = check_launch_cfg(cfg);
   if (st) return st;
   if (S < 1 || S > LK_MAX_SPLITK || M > LK_MAX_M) return LK_ERR_SHAPE;
   if (N == 0 || M == 0) return LK_OK;
@@ -461,12 +457,13 @@ lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, 
   if (!aligned(part, mode == LK_DEQUANT ? 8 : 4)) return LK_ERR_ALIGN;
   if (part_bytes < lk_splitk_workspace_bytes(mode, S, M, N)) return LK_ERR_WORKSPACE;
   GemvProblem p = make_problem(wq, ws, N, K, mode, x, xq, xl, xs, M);
+  apply_cfg(p, cfg);
   p.S = S;
   p.split = true;
   if (mode == LK_DEQUANT) p.part64 = (double*)part;
   else p.y = (float*)part;
-  if (opt_gemv_path != 1 && ring_supports(p)) return ring_gemv(p, stream, nullptr);
-  if (opt_gemv_path == 2) return LK_ERR_SHAPE;
+  if (p.cfg.path != 1 && ring_supports(p)) return ring_gemv(p, stream, nullptr);
+  if (p.cfg.path == 2) return LK_ERR_SHAPE;
   const long blocks = (p.N + kRowsPerBlock - 1) / kRowsPerBlock;
   kernel_fn f = pick(p.mode, p.M, true);
   f<<<dim3((unsigned)blocks, S), kWarps * 32, 0, stream>>>(p);

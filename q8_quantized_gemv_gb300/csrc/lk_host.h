@@ -21,27 +21,10 @@ struct DeviceInfo {
 };
 const DeviceInfo* device_info(int* dev_out);
 
-// Process-wide options (lk_set_option).
-extern long opt_gemv_path;    // 0 auto, 1 direct, 2 ring, 3 tensor-core (small batch)
-extern long opt_ring_stages;  // 0 default
-extern long opt_grid_ctas;    // 0 default
-extern long opt_ring_warps;   // 0 auto, else warps per block of the ring kernel (1..16)
-extern long opt_ring_kb;      // 0: no cap, else shared memory per ring block in KB
-extern long opt_ring_cps;     // ring blocks per SM in the grid (default 1)
-extern long opt_pdl;          // 1: fused ring launches are programmatic dependents
-extern long opt_trace;        // 1: kernels write block 0 timestamps to the trace buffer
-extern long opt_ring_hint;    // 1: L2 evict-first hint on the weight copies (default)
+// The two process-wide diagnostic options (lk_set_option).  Neither
+// changes which kernel runs, how it is launched or any result.
+extern long opt_trace;        // 1..3: kernels write timestamps to the trace buffer
 extern long opt_wait_us;      // bound of every device-side wait, microseconds (0 = 2 s)
-extern long opt_mma_min_m;    // fewest activation rows taking the tensor-core kernel (0 = 2)
-extern long opt_mma_tk;       // its bytes of K per stage (0 auto, else a multiple of 256)
-extern long opt_mma_warps;    // its warps per block (0 auto)
-extern long opt_mma_depth;    // its ring stages per warp (0 = 1)
-extern long opt_mma_i8;       // its dots on the int8 tensor path: 0 auto (Int8Act), 1 always, 2 never
-extern long opt_mma_group;    // its tiles per warp: 0 auto, 1 one warp per tile, 4 four warps per tile
-extern long opt_mma_act16;    // its activations held as f16: 0 auto, 1 force, 2 never
-extern long opt_group_prefill; // the same for a grouped launch over one given activation (0: as ring_prefill)
-extern long opt_ring_tk;       // ring kernel: bytes of K per stage for rows longer than that (0: auto)
-extern long opt_ring_prefill; // warps that issue their first weight stages before the dependency wait (0: half)
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
@@ -73,6 +56,8 @@ inline lk_status launch_status() {
 
 // Checks of a caller's launch settings: LK_ERR_ARG, else LK_OK.
 lk_status check_launch_cfg(const lk_launch_cfg* cfg);
+// The pdl flag of cfg (NULL: 0).
+inline int cfg_pdl(const lk_launch_cfg* cfg) { return cfg && cfg->pdl ? 1 : 0; }
 
 // Everything one GEMV launch needs (plain, split-K partial, argmax epilogue).
 struct GemvProblem {
@@ -108,23 +93,21 @@ struct GemvProblem {
   int8_t* hq;
   int8_t* hl;
   float* hs;
-  // per-call launch settings (lk_launch_cfg, or the process options)
-  int pdl;
-  int prefill;                 // 0: the default
+  // the caller's per-call launch settings (all zero: the defaults)
+  lk_launch_cfg cfg;
 };
 
-// GemvProblem's launch settings from cfg (NULL: the process options).
+// GemvProblem's launch settings from cfg (NULL: the defaults).
 inline void apply_cfg(GemvProblem& p, const lk_launch_cfg* cfg) {
-  p.pdl = (cfg && cfg->pdl >= 0) ? cfg->pdl : (opt_pdl ? 1 : 0);
-  p.prefill = cfg ? cfg->prefill : 0;
+  p.cfg = cfg ? *cfg : lk_launch_cfg{};
 }
 
 // Warps of a block of nw that fill their ring stages before the dependency
-// wait (the others after the activation is loaded): option "ring_prefill",
-// 0 = half of them (measured best: a full ring of requests ahead of the
-// wait slowed the activation loads and the wait itself).
+// wait (the others after the activation is loaded): `want`, 0 = half of
+// them (measured best: a full ring of requests ahead of the wait slowed the
+// activation loads and the wait itself).
 inline int prefill_warps(int nw, int want = 0) {
-  const int p = want > 0 ? want : opt_ring_prefill > 0 ? (int)opt_ring_prefill : (nw + 1) / 2;
+  const int p = want > 0 ? want : (nw + 1) / 2;
   return p < nw ? p : nw;
 }
 
@@ -142,11 +125,11 @@ inline void carveout_max_shared(F f) {
   cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
 }
 
-// Launch as a programmatic dependent of the previous kernel when the option
-// "pdl" is set (the kernels wait for it before their first read of data
-// that kernel writes).
+// Launch as a programmatic dependent of the previous kernel when pdl is set
+// (lk_launch_cfg.pdl; the kernels wait for it before their first read of
+// data that kernel writes and before their first write).
 template <typename... KA, typename... A>
-inline void launch_pdl(void (*f)(KA...), dim3 grid, dim3 block, cudaStream_t stream, A... args) {
+inline void launch_pdl(void (*f)(KA...), dim3 grid, dim3 block, cudaStream_t stream, int pdl, A... args) {
   carveout_max_shared(f);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -157,7 +140,7 @@ inline void launch_pdl(void (*f)(KA...), dim3 grid, dim3 block, cudaStream_t str
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = opt_pdl ? 1 : 0;
+  cfg.numAttrs = pdl ? 1 : 0;
   cudaLaunchKernelEx(&cfg, f, ((KA)args)...);
 }
 

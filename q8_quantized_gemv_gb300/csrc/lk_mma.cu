@@ -799,7 +799,7 @@ MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int sm
   const unsigned cand_tk[4] = {1024u, 512u, 512u, 256u};
   const int cand_d[4] = {2, 2, 1, 1};
   for (int i = few ? 0 : 2; i < 4; ++i) {
-    unsigned tk = lkh::opt_mma_tk > 0 ? (unsigned)lkh::opt_mma_tk : cand_tk[i];
+    unsigned tk = p.cfg.mma_tk > 0 ? (unsigned)p.cfg.mma_tk : cand_tk[i];
     if (tk > round_up(K, 256u)) tk = round_up(K, 256u);
     L.tk = tk;
     L.rs = tk + 32u;
@@ -809,14 +809,14 @@ MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int sm
     const long room = (long)smem_optin - (long)L.ring_off - (long)MTAIL;
     int fit = room > 0 ? (int)(room / L.stage_bytes) : 0;
     if (fit > MST) fit = MST;
-    int depth = lkh::opt_mma_depth > 0 ? (int)lkh::opt_mma_depth : cand_d[i];
-    int w = lkh::opt_mma_warps > 0 ? (int)lkh::opt_mma_warps : fit / depth;
+    int depth = p.cfg.mma_depth > 0 ? (int)p.cfg.mma_depth : cand_d[i];
+    int w = p.cfg.mma_warps > 0 ? (int)p.cfg.mma_warps : fit / depth;
     if (w > MW) w = MW;
     if (w * depth > fit) w = fit / depth;
     L.nw = w;
     L.depth = depth;
     L.total = L.ring_off + (unsigned)(w * depth) * L.stage_bytes + MTAIL;
-    if (w >= 2 || lkh::opt_mma_tk > 0) break;
+    if (w >= 2 || p.cfg.mma_tk > 0) break;
   }
   return L;
 }
@@ -836,7 +836,7 @@ MmaLayout mma_layout_g4(const lkh::GemvProblem& p, int smem_optin, bool a16, uns
   L.ring_off = round_up(L.a_xs + M * L.xsr * 4u, 128u);
   const unsigned cand_tk[2] = {tk_pref ? tk_pref : 512u, tk_pref ? tk_pref : 256u};
   for (int i = 0; i < 2; ++i) {
-    unsigned tk = lkh::opt_mma_tk > 0 ? (unsigned)lkh::opt_mma_tk : cand_tk[i];
+    unsigned tk = p.cfg.mma_tk > 0 ? (unsigned)p.cfg.mma_tk : cand_tk[i];
     if (tk > round_up(K, 256u)) tk = round_up(K, 256u);
     L.tk = tk;
     L.rs = tk + 32u;
@@ -846,21 +846,21 @@ MmaLayout mma_layout_g4(const lkh::GemvProblem& p, int smem_optin, bool a16, uns
     const long room = (long)smem_optin - (long)L.ring_off - (long)MTAIL4;
     int fit = room > 0 ? (int)(room / L.stage_bytes) : 0;
     if (fit > MST) fit = MST;
-    int ng = lkh::opt_mma_warps > 0 ? (int)lkh::opt_mma_warps / G4 : fit / 3;
+    int ng = p.cfg.mma_warps > 0 ? (int)p.cfg.mma_warps / G4 : fit / 3;
     if (ng > MGRP) ng = MGRP;
-    int depth = lkh::opt_mma_depth > 0 ? (int)lkh::opt_mma_depth : (ng > 0 ? fit / ng : 0);
+    int depth = p.cfg.mma_depth > 0 ? (int)p.cfg.mma_depth : (ng > 0 ? fit / ng : 0);
     if (ng * depth > fit) ng = depth > 0 ? fit / depth : 0;
     L.nw = G4 * ng;
     L.depth = depth;
     L.total = L.ring_off + (unsigned)(ng * depth) * L.stage_bytes + MTAIL4;
-    if (ng >= 1 || lkh::opt_mma_tk > 0) break;
+    if (ng >= 1 || p.cfg.mma_tk > 0) break;
   }
   return L;
 }
 
 bool mma_layout_ok(const MmaLayout& L);
 
-// The int8 tensor path (option "mma_i8": 0 auto, 1 always, 2 never).  An
+// The int8 tensor path (lk_launch_cfg.mma_i8: 0 auto, 1 always, 2 never).  An
 // int8 MMA is a single instruction per 32-block with no level conversions,
 // but on this GPU a long-latency one: it won where the tiles are many (8
 // rows, Int8Act: gate/up 28.9 against 29.7 us, lm-head 127.9 against
@@ -868,15 +868,15 @@ bool mma_layout_ok(const MmaLayout& L);
 // (4096x4096: 17.0 against 13.5 us; 4096x12288: 46.3 against 35.4 us; and
 // TwoPass, two per block, everywhere).
 bool use_i8(const lkh::GemvProblem& p, long ntiles, int sms) {
-  if (lkh::opt_mma_i8 == 2) return false;
-  if (lkh::opt_mma_i8 == 1) return true;
+  if (p.cfg.mma_i8 == 2) return false;
+  if (p.cfg.mma_i8 == 1) return true;
   return p.mode == LK_INT8ACT && ntiles >= 8L * sms;
 }
 
 // f16-held activations where they cost no warps (Int8Act at K = 4096: 16
 // warps either way; TwoPass would drop from 16 to 10: measured 54.9 us
-// against 36.9 us held as int8); option "mma_act16" 1 forces them (if they
-// fit at all), 2 forbids them.
+// against 36.9 us held as int8); lk_launch_cfg.mma_act16 1 forces them (if
+// they fit at all), 2 forbids them.
 MmaLayout mma_layout(const lkh::GemvProblem& p, long ntiles, int sms, int smem_optin) {
   if (use_i8(p, ntiles, sms)) {
     MmaLayout L = mma_layout_for(p, ntiles, sms, smem_optin, false);
@@ -890,23 +890,23 @@ MmaLayout mma_layout(const lkh::GemvProblem& p, long ntiles, int sms, int smem_o
   // 13.4 -> 10.7 us, 1024x4096 10.6 -> 5.9 us.  (TwoPass keeps one warp per
   // tile: its doubled activation area leaves four-warp groups too few
   // stages, down 64.2 -> 130.1 us.)
-  if (lkh::opt_mma_group == 0 && p.mode == LK_INT8ACT && ntiles < 4L * sms) {
+  if (p.cfg.mma_group == 0 && p.mode == LK_INT8ACT && ntiles < 4L * sms) {
     const MmaLayout G = mma_layout_g4(p, smem_optin, false, p.K > 8192 ? 2048u : 1024u);
     if (mma_layout_ok(G)) return G;
   }
-  if (lkh::opt_mma_group == 4) {
+  if (p.cfg.mma_group == 4) {
     const MmaLayout G8 = mma_layout_g4(p, smem_optin, false);
-    if (lkh::opt_mma_act16 == 2) return G8;
+    if (p.cfg.mma_act16 == 2) return G8;
     const MmaLayout G16 = mma_layout_g4(p, smem_optin, true);
     if (!mma_layout_ok(G16)) return G8;
-    if (lkh::opt_mma_act16 == 1) return G16;
+    if (p.cfg.mma_act16 == 1) return G16;
     return G16.nw >= G8.nw ? G16 : G8;
   }
   const MmaLayout L8 = mma_layout_for(p, ntiles, sms, smem_optin, false);
-  if (lkh::opt_mma_act16 == 2) return L8;
+  if (p.cfg.mma_act16 == 2) return L8;
   const MmaLayout L16 = mma_layout_for(p, ntiles, sms, smem_optin, true);
   if (!mma_layout_ok(L16)) return L8;
-  if (lkh::opt_mma_act16 == 1) return L16;
+  if (p.cfg.mma_act16 == 1) return L16;
   return L16.nw >= L8.nw ? L16 : L8;
 }
 
@@ -935,7 +935,7 @@ int mma_group_blocks(int M, int sms) {
 bool mma_supports(const GemvProblem& p) {
   if (p.mode != LK_INT8ACT && p.mode != LK_TWOPASS) return false;
   if (p.split || p.fuse || p.F > 0) return false;
-  const int min_m = opt_mma_min_m > 0 ? (int)opt_mma_min_m : 2;
+  const int min_m = p.cfg.mma_min_m > 0 ? p.cfg.mma_min_m : 2;
   if (p.M < min_m || p.M > LK_MAX_BATCH) return false;
   if (p.K < 256 || p.K % 256 || p.N < 1) return false;
   if (!aligned(p.ws, 16) || !aligned(p.xq, 16) || !aligned(p.xs, 16) || (p.mode == LK_TWOPASS && !aligned(p.xl, 16)))
@@ -985,7 +985,7 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   if (tiles < 1) return LK_ERR_SHAPE;
   ra.nw = L.nw;
   ra.depth = L.depth;
-  long gx = opt_grid_ctas > 0 ? opt_grid_ctas : gsms;
+  long gx = p.cfg.grid_ctas > 0 ? p.cfg.grid_ctas : gsms;
   if (gx > ra.ntiles) gx = ra.ntiles;
   ra.gx = (int)gx;
   ra.tk = L.tk;
@@ -999,13 +999,13 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   ra.a_xs = L.a_xs;
   ra.ring_off = L.ring_off;
   ra.wait_ns = opt_wait_us > 0 ? (unsigned long long)opt_wait_us * 1000ull : 2000000000ull;
-  ra.pol_w = opt_ring_hint ? 1ull : 0ull;
-  ra.pdl = p.pdl;
+  ra.pol_w = 1ull;  // L2 evict-first on the weight copies
+  ra.pdl = p.cfg.pdl;
   ra.err = error_word_ptr();
   if (!ra.err) return LK_ERR_CUDA;
   ra.trace = opt_trace == 3 ? trace_ptr() : nullptr;
   ra.tslot = opt_trace == 3 ? trace_next_slot() : -1;
-  ra.prefill = L.g4 ? prefill_warps(L.nw / G4, p.prefill) : prefill_warps(L.nw, p.prefill);  // groups, or warps
+  ra.prefill = L.g4 ? prefill_warps(L.nw / G4, p.cfg.prefill) : prefill_warps(L.nw, p.cfg.prefill);  // groups, or warps
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)gx, (unsigned)ngrp);
   cfg.blockDim = dim3(L.nw * 32);

@@ -75,9 +75,9 @@ __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(const NormArgs a) {
   typedef typename acc_of<Q>::t A;
   __shared__ A red[32];
   __shared__ A total;
-  // a programmatic dependent (a GEMV launched with "pdl") may start its
+  // a programmatic dependent (a GEMV launched with lk_launch_cfg.pdl) may start its
   // weight stream now; it reads these outputs only after this grid completes.
-  // Launched as a dependent itself ("pdl"), this grid reads its inputs and
+  // Launched as a dependent itself (pdl), this grid reads its inputs and
   // writes its outputs only after the previous kernel has completed.
   asm volatile("griddepcontrol.launch_dependents;" :::);
   trec_stamp(a.tr, a.slot, TR_START);
@@ -201,26 +201,26 @@ __global__ void __launch_bounds__(256) rmsnorm_split256_kernel(const NormArgs a)
 }
 
 template <int Q, bool ADD>
-void launch_norm(const NormArgs& a, int M, cudaStream_t stream) {
+void launch_norm(const NormArgs& a, int M, int pdl, cudaStream_t stream) {
   const int K = a.K, vt = K < 1024 ? K : 1024;  // K % 32 == 0: roundup32(K) == K
   if (K % 1024 == 0 && K / 1024 <= 8)
-    launch_pdl(rmsnorm_split256_kernel<Q, ADD>, dim3(M, K / 1024), dim3(256), stream, a);
+    launch_pdl(rmsnorm_split256_kernel<Q, ADD>, dim3(M, K / 1024), dim3(256), stream, pdl, a);
   else if (K % vt == 0 && K / vt <= 8)
-    launch_pdl(rmsnorm_split_kernel<Q, ADD>, dim3(M, K / vt), dim3(vt), stream, a);
+    launch_pdl(rmsnorm_split_kernel<Q, ADD>, dim3(M, K / vt), dim3(vt), stream, pdl, a);
   else
-    launch_pdl(rmsnorm_row_kernel<Q, ADD>, dim3(M), dim3(vt), stream, a);
+    launch_pdl(rmsnorm_row_kernel<Q, ADD>, dim3(M), dim3(vt), stream, pdl, a);
 }
 
 template <bool ADD>
-lk_status norm_entry(const NormArgs& a, int M, lk_mode mode, cudaStream_t stream) {
+lk_status norm_entry(const NormArgs& a, int M, lk_mode mode, int pdl, cudaStream_t stream) {
   if (mode == LK_DEQUANT) {
     if (!a.xn) return LK_ERR_ARG;
-    launch_norm<0, ADD>(a, M, stream);
+    launch_norm<0, ADD>(a, M, pdl, stream);
   } else {
     const lk_status st = check_act_out(mode, a.xq, a.xl, a.xs);
     if (st) return st;
-    if (mode == LK_INT8ACT) launch_norm<1, ADD>(a, M, stream);
-    else launch_norm<2, ADD>(a, M, stream);
+    if (mode == LK_INT8ACT) launch_norm<1, ADD>(a, M, pdl, stream);
+    else launch_norm<2, ADD>(a, M, pdl, stream);
   }
   return launch_status();
 }
@@ -277,19 +277,20 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(const float* __restri
 extern "C" {
 
 lk_status lk_rmsnorm_quant(const float* x, const float* gain, int M, int K, float eps, lk_mode mode, float* xn,
-                           int8_t* xq, int8_t* xl, float* xs, cudaStream_t stream) {
-  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+                           int8_t* xq, int8_t* xl, float* xs, const lk_launch_cfg* cfg, cudaStream_t stream) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS || check_launch_cfg(cfg)) return LK_ERR_ARG;
   if (M < 0 || M > LK_MAX_BATCH || K < 0 || K % 32) return LK_ERR_SHAPE;
   if (M == 0 || K == 0) return LK_OK;
   if (!x || !gain) return LK_ERR_ARG;
   if (!aligned(x, 4) || !aligned(gain, 4) || (xn && !aligned(xn, 4))) return LK_ERR_ALIGN;
-  return norm_entry<false>(norm_args(x, nullptr, nullptr, gain, K, eps, mode, xn, xq, xl, xs), M, mode, stream);
+  return norm_entry<false>(norm_args(x, nullptr, nullptr, gain, K, eps, mode, xn, xq, xl, xs), M, mode,
+                           cfg_pdl(cfg), stream);
 }
 
 lk_status lk_add_rmsnorm_quant(const float* x, const float* r, const float* gain, int M, int K, float eps,
                                lk_mode mode, float* s, float* xn, int8_t* xq, int8_t* xl, float* xs,
-                               cudaStream_t stream) {
-  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+                               const lk_launch_cfg* cfg, cudaStream_t stream) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS || check_launch_cfg(cfg)) return LK_ERR_ARG;
   if (M < 0 || M > LK_MAX_BATCH || K < 0 || K % 32) return LK_ERR_SHAPE;
   if (M == 0 || K == 0) return LK_OK;
   if (!x || !r || !gain) return LK_ERR_ARG;
@@ -297,12 +298,12 @@ lk_status lk_add_rmsnorm_quant(const float* x, const float* r, const float* gain
     return LK_ERR_ALIGN;
   const long n = (long)M * K;
   if (s && (overlap(s, x, n) || overlap(s, r, n))) return LK_ERR_ARG;
-  return norm_entry<true>(norm_args(x, r, s, gain, K, eps, mode, xn, xq, xl, xs), M, mode, stream);
+  return norm_entry<true>(norm_args(x, r, s, gain, K, eps, mode, xn, xq, xl, xs), M, mode, cfg_pdl(cfg), stream);
 }
 
 lk_status lk_swiglu_quant(const float* gate, const float* up, int M, int F, long ld, lk_mode mode, float* h,
-                          int8_t* hq, int8_t* hl, float* hs, cudaStream_t stream) {
-  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+                          int8_t* hq, int8_t* hl, float* hs, const lk_launch_cfg* cfg, cudaStream_t stream) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS || check_launch_cfg(cfg)) return LK_ERR_ARG;
   if (M < 0 || M > LK_MAX_BATCH || F < 0 || F % 32 || ld < F) return LK_ERR_SHAPE;
   if (M == 0 || F == 0) return LK_OK;
   if (!gate || !up) return LK_ERR_ARG;
@@ -315,14 +316,15 @@ lk_status lk_swiglu_quant(const float* gate, const float* up, int M, int F, long
   const long groups = (long)M * (F / 32);
   const int per_block = 8;
   const dim3 grid((unsigned)((groups + per_block - 1) / per_block)), block(32 * per_block);
+  const int pdl = cfg_pdl(cfg);
   if (mode == LK_DEQUANT)
-    launch_pdl(swiglu_quant_kernel<0>, grid, block, stream, gate, up, ld, F, groups, h, (int8_t*)nullptr,
+    launch_pdl(swiglu_quant_kernel<0>, grid, block, stream, pdl, gate, up, ld, F, groups, h, (int8_t*)nullptr,
                (int8_t*)nullptr, (float*)nullptr, tr_ptr(), tr_slot());
   else if (mode == LK_INT8ACT)
-    launch_pdl(swiglu_quant_kernel<1>, grid, block, stream, gate, up, ld, F, groups, h, hq, (int8_t*)nullptr, hs,
+    launch_pdl(swiglu_quant_kernel<1>, grid, block, stream, pdl, gate, up, ld, F, groups, h, hq, (int8_t*)nullptr, hs,
                tr_ptr(), tr_slot());
   else
-    launch_pdl(swiglu_quant_kernel<2>, grid, block, stream, gate, up, ld, F, groups, h, hq, hl, hs, tr_ptr(),
+    launch_pdl(swiglu_quant_kernel<2>, grid, block, stream, pdl, gate, up, ld, F, groups, h, hq, hl, hs, tr_ptr(),
                tr_slot());
   return launch_status();
 }

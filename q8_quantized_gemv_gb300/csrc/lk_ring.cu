@@ -95,8 +95,7 @@ int max_chunk_blocks(int nb, int S) {
 // Blocks of a ring launch along the rows (per split-K chunk).
 int ring_gx(const lkh::GemvProblem& p, int sm_count) {
   const int S = p.split && p.S > 1 ? p.S : 1;
-  const int g = lkh::opt_grid_ctas > 0 ? (int)lkh::opt_grid_ctas
-                                       : sm_count * (lkh::opt_ring_cps > 1 ? (int)lkh::opt_ring_cps : 1);
+  const int g = p.cfg.grid_ctas > 0 ? p.cfg.grid_ctas : sm_count;
   const int gx = (g + S - 1) / S;
   return gx < 1 ? 1 : gx;
 }
@@ -109,24 +108,20 @@ Layout layout(const lkh::GemvProblem& p, int smem_optin, int /*sm_count*/) {
   // whole quads (one copy of the levels, one per row of scales) up to TKMAX;
   // longer rows in 4 KB slices
   L.tk = p.K <= TKMAX ? (unsigned)p.K : 4096u;
-  if (lkh::opt_ring_tk > 0 && lkh::opt_ring_tk < p.K) L.tk = (unsigned)lkh::opt_ring_tk;
+  if (p.cfg.ring_tk > 0 && p.cfg.ring_tk < p.K) L.tk = (unsigned)p.cfg.ring_tk;
   L.srow = L.tk / 16u + 16u;  // as make_geom (padded rows)
   L.s_off = QR * L.tk;
   L.stage_bytes = (L.s_off + QR * L.srow + 127u) & ~127u;
   L.ring_off = (act_area_rt(p.mode, p.M, L.act_len) + 127u) & ~127u;
-  long cap = smem_optin;
-  if (lkh::opt_ring_kb > 0 && lkh::opt_ring_kb * 1024 < cap) cap = lkh::opt_ring_kb * 1024;
-  const long room = cap - (long)L.ring_off - (long)TAIL;
+  const long room = (long)smem_optin - (long)L.ring_off - (long)TAIL;
   int fit = room > 0 ? (int)(room / L.stage_bytes) : 0;
   if (fit > MAX_STAGES) fit = MAX_STAGES;
-  if (lkh::opt_ring_stages > 0 && lkh::opt_ring_stages < fit) fit = (int)lkh::opt_ring_stages;
   // warps x stages per warp: as many stages in flight as fit, one warp per
   // stage up to MAXW warps (each warp streams its own quads).  Measured: for
   // rows in slices with few quads per block (down 4096 x 12288, 6.7 quads of
   // 3 slices), 6 warps of 2 stages lost to 12 of 1 (in the sequence: body
   // 10.2 against 9.7 us, 1815 against 1789 us per token)
-  int w = lkh::opt_ring_warps > 0 ? (int)lkh::opt_ring_warps : (fit < MAXW ? fit : MAXW);
-  if (w > fit) w = fit;
+  const int w = fit < MAXW ? fit : MAXW;
   L.nwc = w;
   L.depth = w > 0 ? fit / w : 0;
   L.total = L.ring_off + L.nwc * L.depth * L.stage_bytes + TAIL;
@@ -156,10 +151,10 @@ bool ring_supports(const GemvProblem& p) {
 }
 
 int ring_max_ctas(long) {
+  // one block per SM by default; lk_launch_cfg.grid_ctas up to four per SM
+  // where the launch writes argmax keys
   const DeviceInfo* d = device_info(nullptr);
-  long g = d ? 4L * d->sm_count : 4096;  // up to 4 ring blocks per SM ("ring_cps")
-  if (opt_grid_ctas > g) g = opt_grid_ctas;
-  return (int)g;
+  return d ? 4 * d->sm_count : 4096;
 }
 
 lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
@@ -185,13 +180,13 @@ lk_status ring_gemv(const GemvProblem& p, cudaStream_t stream, int* n_parts) {
   ra.act_len = L.act_len;
   ra.ring_off = L.ring_off;
   ra.wait_ns = opt_wait_us > 0 ? (unsigned long long)opt_wait_us * 1000ull : 2000000000ull;
-  ra.pol_w = opt_ring_hint ? 1ull : 0ull;
-  ra.pdl = p.pdl;
+  ra.pol_w = 1ull;  // L2 evict-first on the weight copies
+  ra.pdl = p.cfg.pdl;
   ra.err = lkh::error_word_ptr();
   if (!ra.err) return LK_ERR_CUDA;
   ra.trace = opt_trace ? lkh::trace_ptr() : nullptr;
   ra.tslot = opt_trace == 3 ? lkh::trace_next_slot() : -1;
-  ra.prefill = lkh::prefill_warps(L.nwc, p.prefill);
+  ra.prefill = lkh::prefill_warps(L.nwc, p.cfg.prefill);
   const int S = p.split && p.S > 1 ? p.S : 1;
   const int gx = ring_gx(p, d->sm_count);
   ra.gx = gx;

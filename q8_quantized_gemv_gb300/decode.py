@@ -33,12 +33,19 @@ from . import lk, synth
 class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
                  batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
-                 fused=False, chain=False, group_qkv=True, prefill=None, glu=False, fused_qkv=True):
+                 fused=False, chain=False, group_qkv=True, prefill=None, glu=False, fused_qkv=True, pdl=False,
+                 path=0, tune=None):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
         # per projection (qkv, o, gu, down, lm): warps of a GEMV block that
         # fill their stages before the dependency wait (lk_launch_cfg.prefill)
         self.prefill = dict(prefill or {})
+        # every launch a programmatic dependent of the one before (may be
+        # changed between tokens); the GEMV kernel (lk_launch_cfg.path)
+        self.pdl = bool(pdl)
+        self.path = lk.PATHS[path] if isinstance(path, str) else int(path)
+        # further lk_launch_cfg fields for every call (tensor-core layouts ...)
+        self.tune = dict(tune or {})
         dev = self.dev
         s = seed
         # the gated pair runs as one fused launch; the chain and fused-prologue
@@ -101,11 +108,10 @@ class DecodeStack:
         # not pick the tensor-core kernel (2..8 rows); else norm/quantize
         # kernels followed by lk_gemv_q8
         shapes = dict(self.shapes, lm=(vocab, hidden))
-        self.kernel = {n: lk.lk_gemv_kernel_for(N, K, self.mode, B, 0) for n, (N, K) in shapes.items()}
-        prev = lk.lk_get_option("gemv_path")
-        lk.lk_set_option("gemv_path", 2)
-        ring = {n: lk.lk_gemv_kernel_for(N, K, self.mode, B, 0) == 2 for n, (N, K) in shapes.items()}
-        lk.lk_set_option("gemv_path", prev)
+        self.kernel = {n: lk.lk_gemv_kernel_for(N, K, self.mode, B, 0, cfg=self._cfg())
+                       for n, (N, K) in shapes.items()}
+        ring_cfg = lk.launch_cfg(path=2)
+        ring = {n: lk.lk_gemv_kernel_for(N, K, self.mode, B, 0, cfg=ring_cfg) == 2 for n, (N, K) in shapes.items()}
         # fused: True / False for every projection, or the names of those
         # that compute their own norm/quantize prologue
         want = set(shapes) if fused is True else set() if not fused else set(fused)
@@ -143,34 +149,36 @@ class DecodeStack:
     def _norm(self, x, g):
         """RMSNorm -> quantize; returns the GEMV activation arguments."""
         if self.mode == lk.LK_DEQUANT:
-            lk.lk_rmsnorm_quant(x, g, self.mode, self.eps, self.xn)
+            lk.lk_rmsnorm_quant(x, g, self.mode, self.eps, self.xn, cfg=self._cfg())
             return {"x": self.xn}
         a = self.acts[x.shape[1]]
-        lk.lk_rmsnorm_quant(x, g, self.mode, self.eps, None, a["xq"], a.get("xl"), a["xs"])
+        lk.lk_rmsnorm_quant(x, g, self.mode, self.eps, None, a["xq"], a.get("xl"), a["xs"], cfg=self._cfg())
         return a
 
     def _add_norm(self, x, r, s, g):
         """s = x + r, then RMSNorm -> quantize of s (one launch); returns the
         GEMV activation arguments."""
         if self.mode == lk.LK_DEQUANT:
-            lk.lk_add_rmsnorm_quant(x, r, g, self.mode, self.eps, s=s, xn=self.xn)
+            lk.lk_add_rmsnorm_quant(x, r, g, self.mode, self.eps, s=s, xn=self.xn, cfg=self._cfg())
             return {"x": self.xn}
         a = self.acts[x.shape[1]]
-        lk.lk_add_rmsnorm_quant(x, r, g, self.mode, self.eps, s=s, xq=a["xq"], xl=a.get("xl"), xs=a["xs"])
+        lk.lk_add_rmsnorm_quant(x, r, g, self.mode, self.eps, s=s, xq=a["xq"], xl=a.get("xl"), xs=a["xs"],
+                                cfg=self._cfg())
         return a
 
     def _quant(self, x):
         if self.mode == lk.LK_DEQUANT:
             return {"x": x}
         a = self.acts[x.shape[1]]
-        lk.lk_quantize_act(x, self.mode, a["xq"], a.get("xl"), a["xs"])
+        lk.lk_quantize_act(x, self.mode, a["xq"], a.get("xl"), a["xs"], cfg=self._cfg())
         return a
 
-    def _cfg(self, name):
-        """Per-call launch settings of projection `name`: the warps filling
-        before the dependency wait, where set (None: the defaults)."""
-        v = self.prefill.get(name)
-        return None if v is None else lk.launch_cfg(prefill=v)
+    def _cfg(self, name=None):
+        """Launch settings of one call: pdl and the GEMV kernel of the stack,
+        and for projection `name` the warps filling before the dependency
+        wait, where set."""
+        return lk.launch_cfg(**dict(self.tune, pdl=self.pdl, path=self.path,
+                                    prefill=self.prefill.get(name, 0) if name else 0))
 
     def _gemv(self, w, y, acts, parts=None, name=None):
         return lk.lk_gemv_q8(w[0], w[1], self.mode, y, M=self.B, argmax_parts=parts, cfg=self._cfg(name), **acts)
@@ -241,7 +249,7 @@ class DecodeStack:
         if self.glu:
             return self._run_token_glu(hook)
         if self.chain is not None and hook is None:
-            lk.lk_gemv_chain(self.chain, self.mode, self.B, self.eps)
+            lk.lk_gemv_chain(self.chain, self.mode, self.B, self.eps, cfg=self._cfg())
             return self.idx
 
         def g(name, w, y, x, gain, parts=None, acts=None):
@@ -250,7 +258,7 @@ class DecodeStack:
             if self.fused[name]:
                 def launch():
                     return lk.lk_rmsnorm_quant_gemv_q8(w[0], w[1], self.mode, x, y, gain=gain, eps=self.eps,
-                                                       argmax_parts=parts)
+                                                       argmax_parts=parts, cfg=self._cfg(name))
                 a = None
             else:
                 a = acts if acts is not None else (self._norm(x, gain) if gain is not None else self._quant(x))
@@ -263,13 +271,13 @@ class DecodeStack:
         for l, w in enumerate(self.layers):
             if self.qkv is not None:
                 def launch(c=self.qkv[l]):
-                    return lk.lk_gemv_chain(c, self.mode, self.B, self.eps)
+                    return lk.lk_gemv_chain(c, self.mode, self.B, self.eps, cfg=self._cfg("qkv"))
                 launch() if hook is None else hook("qkv", launch)
             elif self.qkv_one and self.fused["q"]:
                 # one launch: norm -> quantize prologue, the fused q|k|v matrix
                 def launch(w=w, x=x):
                     return lk.lk_rmsnorm_quant_gemv_q8(w["qkv"][0], w["qkv"][1], self.mode, x, self.out_qkv,
-                                                       gain=w["g_attn"], eps=self.eps)
+                                                       gain=w["g_attn"], eps=self.eps, cfg=self._cfg("qkv"))
                 launch() if hook is None else hook("qkv", launch)
             elif not any(self.fused[n] for n in ("q", "k", "v")):
                 # one norm, then q, k and v as one GEMV over the fused matrix
@@ -305,11 +313,8 @@ class DecodeStack:
         """Launches of the gate/up pair: one (the ring kernel's SwiGLU
         epilogue) at one activation row where the ring kernel takes the
         shape, else the grouped GEMVs and the SwiGLU kernel."""
-        prev = lk.lk_get_option("gemv_path")
-        lk.lk_set_option("gemv_path", 2)
-        ring = lk.lk_gemv_kernel_for(2 * self.F, self.H, self.mode, 1, 0) == 2
-        lk.lk_set_option("gemv_path", prev)
-        return 1 if (self.B == 1 and ring and prev == 0) else 2
+        ring = lk.lk_gemv_kernel_for(2 * self.F, self.H, self.mode, 1, 0, cfg=lk.launch_cfg(path=2)) == 2
+        return 1 if (self.B == 1 and ring and self.path == 0) else 2
 
     def launches_per_token(self):
         if self.chain is not None:

@@ -41,15 +41,27 @@ class LkGemvTarget(ctypes.Structure):
                 ("y", ctypes.c_void_p)]
 
 
+CFG_FIELDS = ("pdl", "prefill", "path", "grid_ctas", "ring_tk", "mma_min_m", "mma_tk", "mma_warps", "mma_depth",
+              "mma_i8", "mma_group", "mma_act16")
+PATHS = {"auto": 0, "direct": 1, "ring": 2, "mma": 3}
+
+
 class LkLaunchCfg(ctypes.Structure):
-    """Per-call launch settings (the C struct lk_launch_cfg)."""
-    _fields_ = [("pdl", ctypes.c_int), ("prefill", ctypes.c_int)]
+    """Per-call launch settings (the C struct lk_launch_cfg; see include/lk.h)."""
+    _fields_ = [(f, ctypes.c_int) for f in CFG_FIELDS]
 
 
-def launch_cfg(pdl=-1, prefill=0) -> LkLaunchCfg:
-    """lk_launch_cfg: pdl -1 (the process option) / 0 / 1; prefill 0 (the
-    default) or the warps that fill their stages before the dependency wait."""
-    return LkLaunchCfg(int(pdl), int(prefill))
+def launch_cfg(**kw) -> LkLaunchCfg:
+    """lk_launch_cfg from keyword fields (every other field 0, the default):
+    pdl, prefill, path (0..3 or "auto"/"direct"/"ring"/"mma"), grid_ctas,
+    ring_tk, mma_min_m, mma_tk, mma_warps, mma_depth, mma_i8, mma_group,
+    mma_act16."""
+    bad = set(kw) - set(CFG_FIELDS)
+    if bad:
+        raise TypeError(f"launch_cfg: unknown fields {sorted(bad)}")
+    if isinstance(kw.get("path"), str):
+        kw["path"] = PATHS[kw["path"]]
+    return LkLaunchCfg(*[int(kw.get(f, 0)) for f in CFG_FIELDS])
 
 
 def _cfg(cfg):
@@ -77,11 +89,11 @@ def _load():
     sig = {
         "lk_status_string": ([I], ctypes.c_char_p),
         "lk_version": ([], I),
-        "lk_rmsnorm_quant": ([P, P, I, I, F, I, P, P, P, P, P], I),
-        "lk_quantize_act": ([P, I, I, I, P, P, P, P], I),
-        "lk_gemv_q8": ([P, P, I, I, I, P, P, P, P, I, P, P, P, P], I),
+        "lk_rmsnorm_quant": ([P, P, I, I, F, I, P, P, P, P, P, P], I),
+        "lk_quantize_act": ([P, I, I, I, P, P, P, P, P], I),
+        "lk_gemv_q8": ([P, P, I, I, I, P, P, P, P, I, P, P, P, P, P], I),
         "lk_splitk_workspace_bytes": ([I, I, I, I], S),
-        "lk_gemv_q8_splitk": ([P, P, I, I, I, P, P, P, P, I, I, P, S, P], I),
+        "lk_gemv_q8_splitk": ([P, P, I, I, I, P, P, P, P, I, I, P, S, P, P], I),
         "lk_splitk_combine": ([I, P, I, I, I, P, P], I),
         "lk_argmax_parts_max": ([I], I),
         "lk_argmax_scratch_entries": ([I], I),
@@ -91,19 +103,16 @@ def _load():
         "lk_get_option": ([ctypes.c_char_p], L),
         "lk_device_error": ([I, ctypes.POINTER(I)], I),
         "lk_selftest_wait_timeout": ([ctypes.c_uint, P], I),
-        "lk_gemv_kernel_for": ([I, I, I, I, I], I),
-        "lk_rmsnorm_quant_gemv_q8": ([P, P, I, I, I, P, P, F, I, P, P, P, P], I),
+        "lk_gemv_kernel_for": ([I, I, I, I, I, P], I),
+        "lk_rmsnorm_quant_gemv_q8": ([P, P, I, I, I, P, P, F, I, P, P, P, P, P], I),
         "lk_chain_sync_bytes": ([], S),
         "lk_trace_read": ([P, I], I),
         "lk_argmax_noalloc": ([P, I, I, P, P], I),
-        "lk_gemv_chain": ([P, P, I, I, I, F, P, P], I),
-        "lk_gemv_q8_group": ([P, I, I, I, P, P, P, P, I, P], I),
-        "lk_add_rmsnorm_quant": ([P, P, P, I, I, F, I, P, P, P, P, P, P], I),
-        "lk_swiglu_quant": ([P, P, I, I, L, I, P, P, P, P, P], I),
-        "lk_gemv_q8_glu": ([P, P, P, P, I, I, I, P, P, P, P, I, P, P, P, P, P, P, P], I),
-        "lk_gemv_q8_ex": ([P, P, I, I, I, P, P, P, P, I, P, P, P, P, P], I),
-        "lk_gemv_q8_group_ex": ([P, I, I, I, P, P, P, P, I, P, P], I),
-        "lk_gemv_q8_glu_ex": ([P, P, P, P, I, I, I, P, P, P, P, I, P, P, P, P, P, P, P, P], I),
+        "lk_gemv_chain": ([P, P, I, I, I, F, P, P, P], I),
+        "lk_gemv_q8_group": ([P, I, I, I, P, P, P, P, I, P, P], I),
+        "lk_add_rmsnorm_quant": ([P, P, P, I, I, F, I, P, P, P, P, P, P, P], I),
+        "lk_swiglu_quant": ([P, P, I, I, L, I, P, P, P, P, P, P], I),
+        "lk_gemv_q8_glu": ([P, P, P, P, I, I, I, P, P, P, P, I, P, P, P, P, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -120,7 +129,7 @@ def exported_symbols():
             "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout", "lk_gemv_kernel_for",
             "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain", "lk_trace_read",
             "lk_argmax_noalloc", "lk_gemv_q8_group", "lk_add_rmsnorm_quant", "lk_swiglu_quant",
-            "lk_gemv_q8_glu", "lk_gemv_q8_ex", "lk_gemv_q8_group_ex", "lk_gemv_q8_glu_ex"]
+            "lk_gemv_q8_glu"]
 
 
 def _ok(st, where):
@@ -167,21 +176,22 @@ def lk_version() -> int:
     return _load().lk_version()
 
 
-def lk_rmsnorm_quant(x, gain, mode, eps=1e-6, xn=None, xq=None, xl=None, xs=None, stream=None):
+def lk_rmsnorm_quant(x, gain, mode, eps=1e-6, xn=None, xq=None, xl=None, xs=None, stream=None, cfg=None):
     M, K = x.shape
     _ok(_load().lk_rmsnorm_quant(_ptr(x, _F32, "x"), _ptr(gain, _F32, "gain"), M, K, eps, _mode(mode),
                                  _ptr(xn, _F32, "xn"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"),
-                                 _ptr(xs, _F32, "xs"), _stream(stream)), "lk_rmsnorm_quant")
+                                 _ptr(xs, _F32, "xs"), _cfg(cfg), _stream(stream)), "lk_rmsnorm_quant")
 
 
-def lk_add_rmsnorm_quant(x, r, gain, mode, eps=1e-6, s=None, xn=None, xq=None, xl=None, xs=None, stream=None):
+def lk_add_rmsnorm_quant(x, r, gain, mode, eps=1e-6, s=None, xn=None, xq=None, xl=None, xs=None, stream=None,
+                         cfg=None):
     """s = x + r (optional output), then lk_rmsnorm_quant of the sum."""
     M, K = x.shape
     if tuple(r.shape) != (M, K):
         raise ValueError("r must have the shape of x")
     _ok(_load().lk_add_rmsnorm_quant(_ptr(x, _F32, "x"), _ptr(r, _F32, "r"), _ptr(gain, _F32, "gain"), M, K, eps,
                                      _mode(mode), _ptr(s, _F32, "s"), _ptr(xn, _F32, "xn"), _ptr(xq, _I8, "xq"),
-                                     _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), _stream(stream)),
+                                     _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), _cfg(cfg), _stream(stream)),
         "lk_add_rmsnorm_quant")
 
 
@@ -195,7 +205,7 @@ def _pitched_rows(t, name):
     return ctypes.c_void_p(t.data_ptr()), t.stride(0)
 
 
-def lk_swiglu_quant(gate, up, mode, h=None, hq=None, hl=None, hs=None, stream=None):
+def lk_swiglu_quant(gate, up, mode, h=None, hq=None, hl=None, hs=None, stream=None, cfg=None):
     """h = silu(gate) * up, quantized for the next GEMV.  gate and up are
     [M, F] f32 with contiguous rows and the same row pitch (e.g. the two
     halves gu[:, :F], gu[:, F:] of a fused gate/up output)."""
@@ -207,21 +217,22 @@ def lk_swiglu_quant(gate, up, mode, h=None, hq=None, hl=None, hs=None, stream=No
     if ldg != ldu:
         raise ValueError("gate and up must have the same row pitch")
     _ok(_load().lk_swiglu_quant(pg, pu, M, F, ldg, _mode(mode), _ptr(h, _F32, "h"), _ptr(hq, _I8, "hq"),
-                                _ptr(hl, _I8, "hl"), _ptr(hs, _F32, "hs"), _stream(stream)), "lk_swiglu_quant")
+                                _ptr(hl, _I8, "hl"), _ptr(hs, _F32, "hs"), _cfg(cfg), _stream(stream)),
+        "lk_swiglu_quant")
 
 
-def lk_quantize_act(x, mode, xq, xl, xs, stream=None):
+def lk_quantize_act(x, mode, xq, xl, xs, stream=None, cfg=None):
     M, K = x.shape
     _ok(_load().lk_quantize_act(_ptr(x, _F32, "x"), M, K, _mode(mode), _ptr(xq, _I8, "xq"),
-                                _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), _stream(stream)),
+                                _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), _cfg(cfg), _stream(stream)),
         "lk_quantize_act")
 
 
 def lk_gemv_q8(wq, ws, mode, y, x=None, xq=None, xl=None, xs=None, argmax_parts=None, M=None,
                stream=None, cfg=None) -> int:
     """y[M, N] = W x.  Returns the number of argmax partial keys written per
-    activation row (0 when argmax_parts is None).  cfg: launch_cfg(...) for
-    lk_gemv_q8_ex."""
+    activation row (0 when argmax_parts is None).  cfg: launch_cfg(...) or
+    None (the defaults)."""
     N, K = wq.shape
     if M is None:
         M = (x if x is not None else xq).shape[0]
@@ -229,10 +240,7 @@ def lk_gemv_q8(wq, ws, mode, y, x=None, xq=None, xl=None, xs=None, argmax_parts=
     args = [_ptr(wq, _I8, "wq"), _ptr(ws, _WS, "ws"), N, K, _mode(mode), _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"),
             _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), M, _ptr(y, _F32, "y"),
             _ptr(argmax_parts, torch.int64, "argmax_parts"), ctypes.byref(n) if argmax_parts is not None else None]
-    if cfg is None:
-        _ok(_load().lk_gemv_q8(*args, _stream(stream)), "lk_gemv_q8")
-    else:
-        _ok(_load().lk_gemv_q8_ex(*args, _cfg(cfg), _stream(stream)), "lk_gemv_q8_ex")
+    _ok(_load().lk_gemv_q8(*args, _cfg(cfg), _stream(stream)), "lk_gemv_q8")
     return n.value
 
 
@@ -251,10 +259,7 @@ def lk_gemv_q8_group(mats, mode, x=None, xq=None, xl=None, xs=None, M=None, stre
             raise ValueError("lk_gemv_q8_group: matrices of one group share K")
     args = [ctypes.cast(arr, ctypes.c_void_p), len(mats), K, _mode(mode), _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"),
             _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), M]
-    if cfg is None:
-        _ok(_load().lk_gemv_q8_group(*args, _stream(stream)), "lk_gemv_q8_group")
-    else:
-        _ok(_load().lk_gemv_q8_group_ex(*args, _cfg(cfg), _stream(stream)), "lk_gemv_q8_group_ex")
+    _ok(_load().lk_gemv_q8_group(*args, _cfg(cfg), _stream(stream)), "lk_gemv_q8_group")
 
 
 def lk_gemv_q8_glu(wg, wsg, wu, wsu, mode, gu, x=None, xq=None, xl=None, xs=None, h=None, hq=None, hl=None,
@@ -273,20 +278,17 @@ def lk_gemv_q8_glu(wg, wsg, wu, wsu, mode, gu, x=None, xq=None, xl=None, xs=None
             _mode(mode), _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), M,
             _ptr(gu, _F32, "gu"), _ptr(h, _F32, "h"), _ptr(hq, _I8, "hq"), _ptr(hl, _I8, "hl"), _ptr(hs, _F32, "hs"),
             _ptr(cnt, torch.int32, "cnt")]
-    if cfg is None:
-        _ok(_load().lk_gemv_q8_glu(*args, _stream(stream)), "lk_gemv_q8_glu")
-    else:
-        _ok(_load().lk_gemv_q8_glu_ex(*args, _cfg(cfg), _stream(stream)), "lk_gemv_q8_glu_ex")
+    _ok(_load().lk_gemv_q8_glu(*args, _cfg(cfg), _stream(stream)), "lk_gemv_q8_glu")
 
 
-def lk_gemv_kernel_for(N, K, mode, M, S=0) -> int:
+def lk_gemv_kernel_for(N, K, mode, M, S=0, cfg=None) -> int:
     """1 direct kernel, 2 bulk-copy ring kernel, 3 tensor-core kernel, 0 none
     (see include/lk.h)."""
-    return _load().lk_gemv_kernel_for(N, K, _mode(mode), M, S)
+    return _load().lk_gemv_kernel_for(N, K, _mode(mode), M, S, _cfg(cfg))
 
 
 def lk_rmsnorm_quant_gemv_q8(wq, ws, mode, x, y, gain=None, eps=1e-6, argmax_parts=None,
-                             stream=None) -> int:
+                             stream=None, cfg=None) -> int:
     """RMSNorm (gain given) or quantize only (gain None) -> GEMV in one launch.
     Returns the number of argmax partial keys per activation row."""
     N, K = wq.shape
@@ -297,7 +299,7 @@ def lk_rmsnorm_quant_gemv_q8(wq, ws, mode, x, y, gain=None, eps=1e-6, argmax_par
                                          _ptr(y, _F32, "y"),
                                          _ptr(argmax_parts, torch.int64, "argmax_parts"),
                                          ctypes.byref(n) if argmax_parts is not None else None,
-                                         _stream(stream)), "lk_rmsnorm_quant_gemv_q8")
+                                         _cfg(cfg), _stream(stream)), "lk_rmsnorm_quant_gemv_q8")
     return n.value
 
 
@@ -305,14 +307,14 @@ def lk_splitk_workspace_bytes(mode, S, M, N) -> int:
     return _load().lk_splitk_workspace_bytes(_mode(mode), S, M, N)
 
 
-def lk_gemv_q8_splitk(wq, ws, mode, S, part, x=None, xq=None, xl=None, xs=None, M=None, stream=None):
+def lk_gemv_q8_splitk(wq, ws, mode, S, part, x=None, xq=None, xl=None, xs=None, M=None, stream=None, cfg=None):
     N, K = wq.shape
     if M is None:
         M = (x if x is not None else xq).shape[0]
     _ok(_load().lk_gemv_q8_splitk(_ptr(wq, _I8, "wq"), _ptr(ws, _WS, "ws"), N, K, _mode(mode),
                                   _ptr(x, _F32, "x"), _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"),
                                   _ptr(xs, _F32, "xs"), M, S, _ptr(part, None, "part"),
-                                  part.numel() * part.element_size(), _stream(stream)),
+                                  part.numel() * part.element_size(), _cfg(cfg), _stream(stream)),
         "lk_gemv_q8_splitk")
 
 
@@ -386,10 +388,10 @@ class Chain:
         self.sync = torch.zeros((lk_chain_sync_bytes() // 4,), dtype=torch.int32, device=device)
 
 
-def lk_gemv_chain(chain: "Chain", mode, M, eps=1e-6, stream=None):
+def lk_gemv_chain(chain: "Chain", mode, M, eps=1e-6, stream=None, cfg=None):
     _ok(_load().lk_gemv_chain(ctypes.cast(chain.host, ctypes.c_void_p), _ptr(chain.dev, None, "ops_dev"),
-                              chain.n, _mode(mode), M, eps, _ptr(chain.sync, None, "sync"), _stream(stream)),
-        "lk_gemv_chain")
+                              chain.n, _mode(mode), M, eps, _ptr(chain.sync, None, "sync"), _cfg(cfg),
+                              _stream(stream)), "lk_gemv_chain")
 
 
 def lk_trace_read(n: int):

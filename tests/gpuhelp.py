@@ -46,14 +46,15 @@ def gpu_quantize(x_dev, mode):
     return xq, xl, xs
 
 
-def gpu_gemv(wq_d, ws_d, mode, acts, M, amax=False):
-    """acts: dict with x (Dequant) or xq/xl/xs.  Returns (y, parts, n_parts)."""
+def gpu_gemv(wq_d, ws_d, mode, acts, M, amax=False, cfg=None):
+    """acts: dict with x (Dequant) or xq/xl/xs; cfg: lk.launch_cfg(...) or
+    None.  Returns (y, parts, n_parts)."""
     N = wq_d.shape[0]
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
     parts = None
     if amax:
         parts = torch.zeros((M * lk.lk_argmax_parts_max(N),), dtype=torch.int64, device=DEV)
-    n = lk.lk_gemv_q8(wq_d, ws_d, mode, y, M=M, argmax_parts=parts, **acts)
+    n = lk.lk_gemv_q8(wq_d, ws_d, mode, y, M=M, argmax_parts=parts, cfg=cfg, **acts)
     return y, parts, n
 
 
@@ -91,12 +92,7 @@ def assert_gemv_close(y_gpu, y_or, wq, ws, x_np, mode, rows=None, exact_quantize
 def ring_takes(N, K, mode, M):
     """Whether the bulk-copy ring kernel (the fused prologue's kernel) takes
     this shape, whatever kernel lk_gemv_q8 would pick for it."""
-    prev = lk.lk_get_option("gemv_path")
-    lk.lk_set_option("gemv_path", 2)
-    try:
-        return lk.lk_gemv_kernel_for(N, K, mode, M, 0) == 2
-    finally:
-        lk.lk_set_option("gemv_path", prev)
+    return lk.lk_gemv_kernel_for(N, K, mode, M, 0, cfg=lk.launch_cfg(path=2)) == 2
 
 
 # ---- whole decode tokens ------------------------------------------------------------

@@ -102,29 +102,25 @@ def test_pdl_graph_replays_identical(fused, prefill):
     the kernel before it wrote come after that kernel is complete (the
     dependent starts early and must not read such data through a cache that
     can hold lines from before)."""
-    a = DecodeStack(**SMALL, batch=1, mode=1, chain=False, fused=fused)
-    lk.lk_set_option("pdl", 0)
+    every = ("q", "k", "v", "qkv", "o", "gu", "down", "lm")
+    a = DecodeStack(**SMALL, batch=1, mode=1, chain=False, fused=fused, pdl=False,
+                    prefill={n: prefill for n in every} if prefill else None)
     a.run_token()
     torch.cuda.synchronize()
     ref = {k: v.clone() for k, v in list(a.out.items()) + [("h", a.h), ("logits", a.logits)]}
-    lk.lk_set_option("pdl", 1)
-    lk.lk_set_option("ring_prefill", prefill)
-    try:
-        s = torch.cuda.Stream()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            a.run_token()
-        for r in range(60):
-            a.logits.zero_()
-            a.h.zero_()
-            g.replay()
-            torch.cuda.synchronize()
-            got = {k: v for k, v in list(a.out.items()) + [("h", a.h), ("logits", a.logits)]}
-            for k in ref:
-                assert torch.equal(got[k].view(torch.int32), ref[k].view(torch.int32)), (r, k)
-    finally:
-        lk.lk_set_option("pdl", 0)
-        lk.lk_set_option("ring_prefill", 0)
+    a.pdl = True
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        a.run_token()
+    for r in range(60):
+        a.logits.zero_()
+        a.h.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        got = {k: v for k, v in list(a.out.items()) + [("h", a.h), ("logits", a.logits)]}
+        for k in ref:
+            assert torch.equal(got[k].view(torch.int32), ref[k].view(torch.int32)), (r, k)
     assert lk.lk_device_error(reset=True) == 0
 
 
@@ -138,21 +134,17 @@ def test_grouped_qkv_pdl_graph_matches_plain(fused, fused_qkv):
     and the oracle's token."""
     a = DecodeStack(**SMALL, batch=1, mode=1, chain=False, fused=fused, fused_qkv=fused_qkv)
     assert (a.qkv is not None) == (fused and not fused_qkv) and a.qkv_one == fused_qkv
-    lk.lk_set_option("pdl", 0)
     layers, final = run_token_capture(a)
     check_token(a, layers, final)
     ref = a.logits.clone()
-    lk.lk_set_option("pdl", 1)
-    try:
-        s = torch.cuda.Stream()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            a.run_token()
-        for _ in range(3):
-            a.logits.zero_()
-            g.replay()
-            torch.cuda.synchronize()
-            assert torch.equal(a.logits.view(torch.int32), ref.view(torch.int32))
-    finally:
-        lk.lk_set_option("pdl", 0)
+    a.pdl = True
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        a.run_token()
+    for _ in range(3):
+        a.logits.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(a.logits.view(torch.int32), ref.view(torch.int32))
     assert lk.lk_device_error(reset=True) == 0

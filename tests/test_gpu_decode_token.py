@@ -27,9 +27,7 @@ def _lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     build.build()
-    lk.lk_set_option("gemv_path", 0)
     yield
-    lk.lk_set_option("pdl", 0)
     torch.cuda.empty_cache()
 
 
@@ -49,7 +47,6 @@ def _final_bits(st):
                          ids=["int8act-b1", "twopass-b1", "dequant-b1", "int8act-b8", "twopass-b8",
                               "int8act-b1-projections", "twopass-b8-projections"])
 def test_full_decode_token_matches_oracle(mode, batch, glu):
-    lk.lk_set_option("pdl", 0)
     st = DecodeStack(batch=batch, mode=mode, glu=glu)  # the benchmark's 36-layer configuration
     try:
         layers, final = run_token_capture(st)
@@ -58,7 +55,7 @@ def test_full_decode_token_matches_oracle(mode, batch, glu):
         plain = _final_bits(st)
         # the benchmark's form: one graph per token, every launch a
         # programmatic dependent of the one before
-        lk.lk_set_option("pdl", 1)
+        st.pdl = True
         s = torch.cuda.Stream()
         with torch.cuda.stream(s):
             st.run_token()
@@ -76,6 +73,5 @@ def test_full_decode_token_matches_oracle(mode, batch, glu):
                 assert np.array_equal(got[k], plain[k]), k
         assert lk.lk_device_error(reset=True) == 0
     finally:
-        lk.lk_set_option("pdl", 0)
         del st
         torch.cuda.empty_cache()

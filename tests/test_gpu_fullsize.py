@@ -24,7 +24,6 @@ def _lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     build.build()
-    lk.lk_set_option("gemv_path", 0)
     yield
     torch.cuda.empty_cache()
 

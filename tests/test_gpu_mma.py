@@ -17,7 +17,6 @@ from q8_quantized_gemv_gb300 import build, lk, synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 I8, TP = 1, 2
-OPTS = ("mma_tk", "mma_warps", "mma_depth", "mma_act16", "mma_group", "mma_i8", "grid_ctas", "gemv_path")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -26,24 +25,20 @@ def _lib():
         pytest.skip("no CUDA device")
     build.build()
     yield
-    for o in OPTS:
-        lk.lk_set_option(o, 0)
 
 
-@pytest.fixture(autouse=True)
-def _reset():
-    lk.lk_set_option("gemv_path", 3)
-    yield
-    for o in OPTS:
-        lk.lk_set_option(o, 0)
+def mma(**kw):
+    """Launch settings forcing the tensor-core kernel (and the given fields)."""
+    return lk.launch_cfg(path=kw.pop("path", 3), **kw)
 
 
-def run_case(N, K, M, mode, seed, amax=False):
-    assert lk.lk_gemv_kernel_for(N, K, mode, M, 0) == 3
+def run_case(N, K, M, mode, seed, amax=False, cfg=None):
+    cfg = cfg if cfg is not None else mma()
+    assert lk.lk_gemv_kernel_for(N, K, mode, M, 0, cfg=cfg) == 3
     wq, ws = synth.q8_matrix(N, K, seed)
     x = synth.activation(M, K, seed + 1, outliers=True)
     y_or = oracle.gemv(wq, ws, mode, **oracle_acts(x, mode))
-    y, parts, n = gpu_gemv(to_dev(wq), to_dev(ws), mode, dev_acts(x, mode), M, amax=amax)
+    y, parts, n = gpu_gemv(to_dev(wq), to_dev(ws), mode, dev_acts(x, mode), M, amax=amax, cfg=cfg)
     idx = None
     if amax:
         idx = torch.full((M,), -1, dtype=torch.int32, device=DEV)
@@ -67,10 +62,9 @@ def test_mma_rows_and_tails(path, mode, M, N, K):
     """f16: the dots as f16 MMAs on converted levels, activations held as int8
     (or f16: act16); g4: four warps per 16-row tile (one partial each,
     combined through shared memory); i8: the dots as int8 MMAs."""
-    lk.lk_set_option("mma_i8", 1 if path == "i8" else 2)
-    lk.lk_set_option("mma_group", 4 if "g4" in path else 1)
-    lk.lk_set_option("mma_act16", 1 if "act16" in path else 2)
-    run_case(N, K, M, mode, 7000 + N + K + M)
+    cfg = mma(mma_i8=1 if path == "i8" else 2, mma_group=4 if "g4" in path else 1,
+              mma_act16=1 if "act16" in path else 2)
+    run_case(N, K, M, mode, 7000 + N + K + M, cfg=cfg)
 
 
 @pytest.mark.parametrize("i8", [1, 2])
@@ -85,13 +79,8 @@ def test_mma_stage_layouts(i8, group, act16, mode, tk, warps, depth):
         pytest.skip("four-warp tiles take warps in fours and two or more stages per group")
     if i8 == 1 and (group == 4 or act16 == 1):
         pytest.skip("the int8 path is one warp per tile on int8 activation rows")
-    lk.lk_set_option("mma_i8", i8)
-    lk.lk_set_option("mma_group", group)
-    lk.lk_set_option("mma_act16", act16)
-    lk.lk_set_option("mma_tk", tk)
-    lk.lk_set_option("mma_warps", warps)
-    lk.lk_set_option("mma_depth", depth)
-    run_case(777, 3328, 8, mode, 7100 + tk + warps)
+    cfg = mma(mma_i8=i8, mma_group=group, mma_act16=act16, mma_tk=tk, mma_warps=warps, mma_depth=depth)
+    run_case(777, 3328, 8, mode, 7100 + tk + warps, cfg=cfg)
 
 
 @pytest.mark.parametrize("M", [2, 8])
@@ -99,25 +88,21 @@ def test_mma_stage_layouts(i8, group, act16, mode, tk, warps, depth):
 def test_mma_auto_layout_few_tiles(N, K, M):
     """The automatic choice for Int8Act launches with few tiles per SM (four
     warps per tile, 1 KB or 2 KB slices): bit for bit the oracle."""
-    lk.lk_set_option("gemv_path", 0)
     assert lk.lk_gemv_kernel_for(N, K, I8, M, 0) == 3
-    run_case(N, K, M, I8, 7250 + N + M)
+    run_case(N, K, M, I8, 7250 + N + M, cfg=lk.launch_cfg())
 
 
 @pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("ctas", [1, 7, 152])
 def test_mma_grid_sizes(ctas, group):
-    lk.lk_set_option("mma_group", group)
-    lk.lk_set_option("grid_ctas", ctas)
-    run_case(4100, 1024, 5, I8, 7200 + ctas)
+    run_case(4100, 1024, 5, I8, 7200 + ctas, cfg=mma(mma_group=group, grid_ctas=ctas))
 
 
 @pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("i8", [1, 2])
 @pytest.mark.parametrize("mode", [I8, TP])
 def test_mma_argmax_with_ties(mode, group, i8):
-    lk.lk_set_option("mma_group", group)
-    lk.lk_set_option("mma_i8", i8)
+    cfg = mma(mma_group=group, mma_i8=i8)
     N, K, M = 3001, 512, 8
     wq, ws = synth.q8_matrix(N, K, 7300)
     x = synth.activation(M, K, 7301)
@@ -126,7 +111,7 @@ def test_mma_argmax_with_ties(mode, group, i8):
         wq[i] = dom
         ws[i] = np.float16(1.0).view(np.uint16)
     y_or = oracle.gemv(wq, ws, mode, **oracle_acts(x, mode))
-    y, parts, n = gpu_gemv(to_dev(wq), to_dev(ws), mode, dev_acts(x, mode), M, amax=True)
+    y, parts, n = gpu_gemv(to_dev(wq), to_dev(ws), mode, dev_acts(x, mode), M, amax=True, cfg=cfg)
     idx = torch.full((M,), -1, dtype=torch.int32, device=DEV)
     lk.lk_argmax(idx, M, N, parts=parts, n_parts=n)
     torch.cuda.synchronize()
@@ -143,16 +128,13 @@ def test_mma_matches_batch1_kernel_bits():
     x = synth.activation(M, K, 7401, outliers=True)
     wq_d, ws_d = to_dev(wq), to_dev(ws)
     for mode in (I8, TP):
-        lk.lk_set_option("gemv_path", 3)
-        yb, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M)
-        lk.lk_set_option("gemv_path", 0)
+        yb, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M, cfg=mma())
         for t in range(M):
             y1, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x[t:t + 1], mode), 1)
             assert np.array_equal(bits(host(y1))[0], bits(host(yb))[t])
 
 
 def test_mma_declines():
-    lk.lk_set_option("gemv_path", 0)
     assert lk.lk_gemv_kernel_for(4096, 4096, 1, 8, 0) == 3
     assert lk.lk_gemv_kernel_for(4096, 4096, 0, 8, 0) != 3   # Dequant
     assert lk.lk_gemv_kernel_for(4096, 4096, 1, 1, 0) != 3   # one row
@@ -162,12 +144,8 @@ def test_mma_declines():
     # two 512-byte stages: still taken
     assert lk.lk_gemv_kernel_for(4096, 12288, 2, 8, 0) == 3
     # ... but not with 4 KB stages forced
-    lk.lk_set_option("mma_tk", 4096)
-    assert lk.lk_gemv_kernel_for(4096, 12288, 2, 8, 0) != 3
-    lk.lk_set_option("mma_tk", 0)
-    lk.lk_set_option("mma_min_m", 9)
-    assert lk.lk_gemv_kernel_for(4096, 4096, 1, 8, 0) != 3
-    lk.lk_set_option("mma_min_m", 0)
+    assert lk.lk_gemv_kernel_for(4096, 12288, 2, 8, 0, cfg=lk.launch_cfg(mma_tk=4096)) != 3
+    assert lk.lk_gemv_kernel_for(4096, 4096, 1, 8, 0, cfg=lk.launch_cfg(mma_min_m=9)) != 3
 
 
 @pytest.mark.parametrize("group", [1, 4])
@@ -178,20 +156,19 @@ def test_group_matches_single_calls_and_oracle(mode, M, Ns, group):
     """lk_gemv_q8_group over matrices with ragged N: each output has the bits
     of its own lk_gemv_q8 call and of the oracle (one launch for 2..8 rows,
     one launch per matrix for a single row)."""
-    lk.lk_set_option("gemv_path", 0)
-    lk.lk_set_option("mma_group", group)
+    cfg = lk.launch_cfg(mma_group=group)
     K = 1280
     mats = [synth.q8_matrix(N, K, 7500 + i + N) for i, N in enumerate(Ns)]
     x = synth.activation(M, K, 7600 + M, outliers=True)
     acts = dev_acts(x, mode)
     dm = [(to_dev(w), to_dev(s), torch.full((M, w.shape[0]), float("nan"), device=DEV)) for w, s in mats]
-    lk.lk_gemv_q8_group(dm, mode, M=M, **acts)
+    lk.lk_gemv_q8_group(dm, mode, M=M, cfg=cfg, **acts)
     torch.cuda.synchronize()
     assert lk.lk_device_error(reset=True) == 0
     for (w, s), (wd, sd, y) in zip(mats, dm):
         y_or = oracle.gemv(w, s, mode, **oracle_acts(x, mode))
         assert np.array_equal(bits(host(y)), bits(y_or))
-        y1, _, _ = gpu_gemv(wd, sd, mode, acts, M)
+        y1, _, _ = gpu_gemv(wd, sd, mode, acts, M, cfg=cfg)
         assert np.array_equal(bits(host(y1)), bits(host(y)))
 
 
@@ -205,16 +182,14 @@ def test_mma_batches_past_eight_rows(path, mode, M, N, K):
     """Groups of 8 activation rows side by side on the SMs: every value bit for
     bit the oracle's (the 8-row arithmetic), the argmax of every row, with
     ragged row groups (9, 33) and ragged tiles."""
-    lk.lk_set_option("mma_i8", 1 if path == "i8" else 2)
-    lk.lk_set_option("mma_group", 4 if "g4" in path else 1)
-    run_case(N, K, M, mode, 9100 + N + K + M, amax=True)
+    cfg = mma(mma_i8=1 if path == "i8" else 2, mma_group=4 if "g4" in path else 1)
+    run_case(N, K, M, mode, 9100 + N + K + M, amax=True, cfg=cfg)
 
 
 @pytest.mark.parametrize("mode", [I8, TP])
 def test_batch_past_eight_matches_groups_of_eight(mode):
     """M = 24 in one launch equals three launches of 8 rows, bit for bit, and
     the grouped call (q, k, v) at 24 rows equals per-matrix calls."""
-    lk.lk_set_option("gemv_path", 0)
     N, K, M = 2048, 4096, 24
     wq, ws = synth.q8_matrix(N, K, 91)
     x = synth.activation(M, K, 92, outliers=True)
@@ -239,7 +214,6 @@ def test_batch_past_eight_matches_groups_of_eight(mode):
 def test_past_eight_rows_needs_the_tensor_core_path():
     """Past 8 rows only the tensor-core kernel runs: Dequant, split-K and
     K % 256 != 0 are shape errors, not silent fallbacks."""
-    lk.lk_set_option("gemv_path", 0)
     assert lk.lk_gemv_kernel_for(4096, 4096, I8, 64, 0) == 3
     assert lk.lk_gemv_kernel_for(4096, 4096, I8, 65, 0) == 0
     assert lk.lk_gemv_kernel_for(4096, 4096, 0, 16, 0) == 0

@@ -28,14 +28,16 @@ def _lib():
     build.build()
     lk._load()
     yield
-    lk.lk_set_option("gemv_path", 0)
 
 
 @pytest.fixture(params=sorted(PATHS))
 def path(request):
-    lk.lk_set_option("gemv_path", PATHS[request.param])
-    yield request.param
-    lk.lk_set_option("gemv_path", 0)
+    return request.param
+
+
+def cfgp(path):
+    """Launch settings forcing the GEMV kernel of `path`."""
+    return lk.launch_cfg(path=PATHS[path])
 
 
 def need(path, K, N=64, mode=1, M=1, S=0):
@@ -43,9 +45,9 @@ def need(path, K, N=64, mode=1, M=1, S=0):
     (K % 256 != 0, or the activation does not fit in shared memory), and the
     tensor-core case outside its domain (quantized modes, 2..8 rows, no
     split-K)."""
-    if path == "ring" and lk.lk_gemv_kernel_for(N, K, mode, M, S) != 2:
+    if path == "ring" and lk.lk_gemv_kernel_for(N, K, mode, M, S, cfg=cfgp(path)) != 2:
         pytest.skip("shape not taken by the ring kernel")
-    if path == "mma" and (S > 0 or lk.lk_gemv_kernel_for(N, K, mode, M, 0) != 3):
+    if path == "mma" and (S > 0 or lk.lk_gemv_kernel_for(N, K, mode, M, 0, cfg=cfgp(path)) != 3):
         pytest.skip("shape not taken by the tensor-core kernel")
 
 
@@ -153,11 +155,11 @@ def test_gemv_parity(path, mode, M, N, K):
     x = synth.activation(M, K, 4001 + M, outliers=True)
     y_or = oracle.gemv(wq, ws, mode, **oracle_acts(x, mode))
     wq_d, ws_d = to_dev(wq), to_dev(ws)
-    y, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M)
+    y, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M, cfg=cfgp(path))
     sync_check()
     assert_gemv_close(host(y), y_or, wq, ws, x, mode)
     # run to run: the same bytes
-    y2, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M)
+    y2, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M, cfg=cfgp(path))
     sync_check()
     assert np.array_equal(bits(host(y2)), bits(host(y)))
 
@@ -174,7 +176,7 @@ def test_dequant_long_rows_same_sign(path, M, K):
     _, ws = synth.q8_matrix(64, K, 4201 + K)
     x = np.abs(synth.activation(M, K, 4202 + K + M, outliers=True)).astype(np.float32)
     y_or = oracle.gemv(wq, ws, DQ, x=x)
-    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), DQ, dev_acts(x, DQ), M)
+    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), DQ, dev_acts(x, DQ), M, cfg=cfgp(path))
     sync_check()
     assert_gemv_close(host(y), y_or, wq, ws, x, DQ)
 
@@ -186,11 +188,10 @@ def test_gemv_batch_invariance(path, mode):
     x = synth.activation(M, K, 4101, outliers=True)
     need(path, K, N, mode, M)
     wq_d, ws_d = to_dev(wq), to_dev(ws)
-    yb, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M)
-    if path == "mma":  # single rows through the default (batch-1) kernel
-        lk.lk_set_option("gemv_path", 0)
+    yb, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x, mode), M, cfg=cfgp(path))
+    one = None if path == "mma" else cfgp(path)  # mma: single rows through the default (batch-1) kernel
     for t in range(M):
-        y1, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x[t:t + 1], mode), 1)
+        y1, _, _ = gpu_gemv(wq_d, ws_d, mode, dev_acts(x[t:t + 1], mode), 1, cfg=one)
         assert np.array_equal(bits(host(y1))[0], bits(host(yb))[t])
     sync_check()
 
@@ -204,7 +205,7 @@ def test_gemv_order_fixture_on_gpu(path, name, mode):
     wq, ws, x = block_case(K, rec["blocks"], pad_to=pad)
     m = MODES[mode]
     x, M = fixture_rows(path, m, x)
-    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), M)
+    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), M, cfg=cfgp(path))
     sync_check()
     assert host(y)[:, 0].tolist() == [np.float32(rec[f"y_{mode}"])] * M
 
@@ -225,7 +226,7 @@ def test_gemv_low_word_fixture_on_gpu(path, mode):
     wq, ws, x = lo_case(rec, pad_to=256 if path != "direct" else None)
     m = MODES[mode]
     x, M = fixture_rows(path, m, x)
-    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), M)
+    y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), M, cfg=cfgp(path))
     sync_check()
     assert host(y)[:, 0].tolist() == [np.float32(rec[f"y_{mode}"])] * M
 
@@ -255,7 +256,7 @@ def test_splitk_parity(path, mode, S, N, K, M):
     dt = torch.float64 if mode == DQ else torch.float32
     part = torch.full((S, M, N), float("nan"), dtype=dt, device=DEV)
     acts = dev_acts(x, mode)
-    lk.lk_gemv_q8_splitk(wq_d, ws_d, mode, S, part, M=M, **acts)
+    lk.lk_gemv_q8_splitk(wq_d, ws_d, mode, S, part, M=M, cfg=cfgp(path), **acts)
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
     lk.lk_splitk_combine(mode, part, S, M, N, y)
     sync_check()
@@ -266,11 +267,11 @@ def test_splitk_parity(path, mode, S, N, K, M):
         assert np.array_equal(bits(host(part)), bits(ch_or))
     assert_gemv_close(host(y), y_or, wq, ws, x, mode)
     if S == 1 and mode != DQ:
-        y1, _, _ = gpu_gemv(wq_d, ws_d, mode, acts, M)
+        y1, _, _ = gpu_gemv(wq_d, ws_d, mode, acts, M, cfg=cfgp(path))
         assert np.array_equal(host(y1), host(y))
     # run to run
     part2 = torch.zeros_like(part)
-    lk.lk_gemv_q8_splitk(wq_d, ws_d, mode, S, part2, M=M, **acts)
+    lk.lk_gemv_q8_splitk(wq_d, ws_d, mode, S, part2, M=M, cfg=cfgp(path), **acts)
     y2 = torch.zeros_like(y)
     lk.lk_splitk_combine(mode, part2, S, M, N, y2)
     sync_check()
@@ -287,10 +288,10 @@ def test_splitk_combine_fixture_on_gpu(path, mode):
     wq, ws, x = block_case(K, rec["blocks"])
     m = MODES[mode]
     part = torch.zeros((S, 1, 1), dtype=torch.float64 if m == DQ else torch.float32, device=DEV)
-    lk.lk_gemv_q8_splitk(to_dev(wq), to_dev(ws), m, S, part, M=1, **dev_acts(x, m))
+    lk.lk_gemv_q8_splitk(to_dev(wq), to_dev(ws), m, S, part, M=1, cfg=cfgp(path), **dev_acts(x, m))
     y = torch.zeros((1, 1), device=DEV)
     lk.lk_splitk_combine(m, part, S, 1, 1, y)
-    yp, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), 1)
+    yp, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), m, dev_acts(x, m), 1, cfg=cfgp(path))
     sync_check()
     assert host(y)[0, 0] == np.float32(rec[f"y_split_{mode}"])
     assert host(yp)[0, 0] == np.float32(rec[f"y_plain_{mode}"])
@@ -330,7 +331,7 @@ def test_gemv_argmax_epilogue_planted_ties(path, mode):
         wq[i] = dom
         ws[i] = np.float16(1.0).view(np.uint16)
     y_or = oracle.gemv(wq, ws, mode, **oracle_acts(x, mode))
-    y, parts, n = gpu_gemv(to_dev(wq), to_dev(ws), mode, dev_acts(x, mode), M, amax=True)
+    y, parts, n = gpu_gemv(to_dev(wq), to_dev(ws), mode, dev_acts(x, mode), M, amax=True, cfg=cfgp(path))
     idx = torch.full((M,), -1, dtype=torch.int32, device=DEV)
     lk.lk_argmax(idx, M, N, parts=parts, n_parts=n)
     sync_check()
@@ -354,11 +355,9 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     x = synth.activation(1, K, 7001)
     y_or = oracle.gemv(wq, ws, I8, **oracle_acts(x, I8))
     for p in (1, 2):
-        lk.lk_set_option("gemv_path", p)
-        y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), I8, dev_acts(x, I8), 1)
+        y, _, _ = gpu_gemv(to_dev(wq), to_dev(ws), I8, dev_acts(x, I8), 1, cfg=lk.launch_cfg(path=p))
         sync_check()
         assert np.array_equal(bits(host(y)), bits(y_or))
-    lk.lk_set_option("gemv_path", 0)
 
 
 # ---- fused RMSNorm -> quantize -> GEMV (one launch) -----------------------------------
@@ -371,36 +370,33 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 def test_fused_norm_quant_gemv(pdl, mode, M, N, K, norm):
     if not ring_takes(N, K, mode, M):
         pytest.skip("activation area does not fit the ring kernel")
-    lk.lk_set_option("pdl", pdl)
-    try:
-        wq, ws = synth.q8_matrix(N, K, 8000 + N + K)
-        x = synth.activation(M, K, 8001 + M, outliers=True)
-        g = synth.norm_gain(K, 8002) if norm else None
-        xa = oracle.rmsnorm(x, g, mode) if norm else x
-        y_or = oracle.gemv(wq, ws, mode, **oracle_acts(xa, mode))
-        wq_d, ws_d = to_dev(wq), to_dev(ws)
-        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
-        parts = torch.zeros((M * lk.lk_argmax_parts_max(N),), dtype=torch.int64, device=DEV)
-        n = lk.lk_rmsnorm_quant_gemv_q8(wq_d, ws_d, mode, to_dev(x), y, gain=to_dev(g) if norm else None,
-                                        argmax_parts=parts)
-        idx = torch.full((M,), -1, dtype=torch.int32, device=DEV)
-        lk.lk_argmax(idx, M, N, parts=parts, n_parts=n)
+    cfg = lk.launch_cfg(pdl=pdl)
+    wq, ws = synth.q8_matrix(N, K, 8000 + N + K)
+    x = synth.activation(M, K, 8001 + M, outliers=True)
+    g = synth.norm_gain(K, 8002) if norm else None
+    xa = oracle.rmsnorm(x, g, mode) if norm else x
+    y_or = oracle.gemv(wq, ws, mode, **oracle_acts(xa, mode))
+    wq_d, ws_d = to_dev(wq), to_dev(ws)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    parts = torch.zeros((M * lk.lk_argmax_parts_max(N),), dtype=torch.int64, device=DEV)
+    n = lk.lk_rmsnorm_quant_gemv_q8(wq_d, ws_d, mode, to_dev(x), y, gain=to_dev(g) if norm else None,
+                                    argmax_parts=parts, cfg=cfg)
+    idx = torch.full((M,), -1, dtype=torch.int32, device=DEV)
+    lk.lk_argmax(idx, M, N, parts=parts, n_parts=n)
+    sync_check()
+    assert_gemv_close(host(y), y_or, wq, ws, xa, mode)
+    assert host(idx).tolist() == [oracle.argmax(y_or[t]) for t in range(M)]
+    # the same bits as the unfused launches (for 2..8 rows: the tensor-core kernel)
+    if mode != DQ:
+        y2 = torch.zeros_like(y)
+        xq, xl, xs = act_buffers(M, K, mode)
+        if norm:
+            lk.lk_rmsnorm_quant(to_dev(x), to_dev(g), mode, 1e-6, None, xq, xl, xs, cfg=cfg)
+        else:
+            lk.lk_quantize_act(to_dev(x), mode, xq, xl, xs, cfg=cfg)
+        lk.lk_gemv_q8(wq_d, ws_d, mode, y2, xq=xq, xl=xl, xs=xs, M=M, cfg=cfg)
         sync_check()
-        assert_gemv_close(host(y), y_or, wq, ws, xa, mode)
-        assert host(idx).tolist() == [oracle.argmax(y_or[t]) for t in range(M)]
-        # the same bits as the unfused launches (for 2..8 rows: the tensor-core kernel)
-        if mode != DQ:
-            y2 = torch.zeros_like(y)
-            xq, xl, xs = act_buffers(M, K, mode)
-            if norm:
-                lk.lk_rmsnorm_quant(to_dev(x), to_dev(g), mode, 1e-6, None, xq, xl, xs)
-            else:
-                lk.lk_quantize_act(to_dev(x), mode, xq, xl, xs)
-            lk.lk_gemv_q8(wq_d, ws_d, mode, y2, xq=xq, xl=xl, xs=xs, M=M)
-            sync_check()
-            assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
-    finally:
-        lk.lk_set_option("pdl", 0)
+        assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
 
 
 def test_fused_pdl_chain_in_a_graph():
@@ -417,9 +413,9 @@ def test_fused_pdl_chain_in_a_graph():
     bufs = [torch.zeros((1, N), dtype=torch.float32, device=DEV) for _ in range(L + 1)]
     bufs[0].copy_(to_dev(x0))
 
-    def chain():
+    def chain(cfg=None):
         for l in range(L):
-            lk.lk_rmsnorm_quant_gemv_q8(dm[l][0], dm[l][1], I8, bufs[l], bufs[l + 1], gain=dg[l])
+            lk.lk_rmsnorm_quant_gemv_q8(dm[l][0], dm[l][1], I8, bufs[l], bufs[l + 1], gain=dg[l], cfg=cfg)
 
     chain()
     torch.cuda.synchronize()
@@ -430,18 +426,14 @@ def test_fused_pdl_chain_in_a_graph():
         a = oracle.rmsnorm(v, gains[l], I8)
         v = oracle.gemv(mats[l][0], mats[l][1], I8, **oracle_acts(a, I8))
     assert np.array_equal(bits(ref), bits(v))
-    lk.lk_set_option("pdl", 1)
-    try:
-        s = torch.cuda.Stream()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=s):
-            chain()
-        for _ in range(3):
-            for b in bufs[1:]:
-                b.zero_()
-            graph.replay()
-            torch.cuda.synchronize()
-            assert np.array_equal(bits(host(bufs[L])), bits(ref))
-    finally:
-        lk.lk_set_option("pdl", 0)
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        chain(lk.launch_cfg(pdl=1))
+    for _ in range(3):
+        for b in bufs[1:]:
+            b.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(host(bufs[L])), bits(ref))
     sync_check()
