@@ -347,7 +347,7 @@ lk_status lk_gemv_q8_group(const lk_gemv_target* targets, int n, int K, lk_mode 
 
 int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S, const lk_launch_cfg* cfg) {
   if (mode < LK_DEQUANT || mode > LK_TWOPASS || N < 1 || K < 32 || K % 32 || M < 1 || M > LK_MAX_BATCH || S < 0 ||
-      S > LK_MAX_SPLITK || (M > LK_MAX_M && S > 0) || check_launch_cfg(cfg))
+      S > LK_MAX_SPLITK || check_launch_cfg(cfg))
     return 0;
   // 16-byte aligned stand-in pointers: only the shape decides
   const void* a16 = (const void*)(uintptr_t)256;
@@ -357,10 +357,9 @@ int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S, const lk_launch
   p.S = S > 0 ? S : 1;
   apply_cfg(p, cfg);
   const int path = p.cfg.path;
-  if (S == 0 && (path == 0 || path == 3) && mma_supports(p)) return 3;
-  if (M > LK_MAX_M) return 0;
+  if ((path == 0 || path == 3) && mma_supports(p)) return 3;
+  if (M > LK_MAX_M || path == 3) return 0;
   if (path == 1) return 1;
-  if (path == 3) return S == 0 ? 0 : (ring_supports(p) ? 2 : 1);
   return ring_supports(p) ? 2 : (path == 2 ? 0 : 1);
 }
 
@@ -451,7 +450,7 @@ lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, 
   if (st) return st;
   st = check_launch_cfg(cfg);
   if (st) return st;
-  if (S < 1 || S > LK_MAX_SPLITK || M > LK_MAX_M) return LK_ERR_SHAPE;
+  if (S < 1 || S > LK_MAX_SPLITK) return LK_ERR_SHAPE;
   if (N == 0 || M == 0) return LK_OK;
   if (!part) return LK_ERR_ARG;
   if (!aligned(part, mode == LK_DEQUANT ? 8 : 4)) return LK_ERR_ALIGN;
@@ -462,8 +461,12 @@ lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, 
   p.split = true;
   if (mode == LK_DEQUANT) p.part64 = (double*)part;
   else p.y = (float*)part;
-  if (p.cfg.path != 1 && ring_supports(p)) return ring_gemv(p, stream, nullptr);
-  if (p.cfg.path == 2) return LK_ERR_SHAPE;
+  const int path = p.cfg.path;
+  // 2.. LK_MAX_BATCH rows: the tensor-core kernel (past 8 rows the only one)
+  if ((path == 0 || path == 3) && mma_supports(p)) return mma_gemv(p, stream, nullptr);
+  if (path == 3 || M > LK_MAX_M) return LK_ERR_SHAPE;
+  if (path != 1 && ring_supports(p)) return ring_gemv(p, stream, nullptr);
+  if (path == 2) return LK_ERR_SHAPE;
   const long blocks = (p.N + kRowsPerBlock - 1) / kRowsPerBlock;
   kernel_fn f = pick(p.mode, p.M, true);
   f<<<dim3((unsigned)blocks, S), kWarps * 32, 0, stream>>>(p);
@@ -473,7 +476,7 @@ lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, 
 lk_status lk_splitk_combine(lk_mode mode, const void* part, int S, int M, int N, float* y,
                             cudaStream_t stream) {
   if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
-  if (S < 1 || S > LK_MAX_SPLITK || M < 0 || M > LK_MAX_M || N < 0) return LK_ERR_SHAPE;
+  if (S < 1 || S > LK_MAX_SPLITK || M < 0 || M > LK_MAX_BATCH || N < 0) return LK_ERR_SHAPE;
   if (N == 0 || M == 0) return LK_OK;
   if (!part || !y) return LK_ERR_ARG;
   if (!aligned(part, mode == LK_DEQUANT ? 8 : 4) || !aligned(y, 4)) return LK_ERR_ALIGN;

@@ -39,6 +39,15 @@
 // stride K + 32 bytes for the same reason.  Tiles are dealt to warps across
 // the grid first (tile i -> block i mod grid, then warp), so small matrices
 // still spread over every SM.
+//
+// Split-K (lk_gemv_q8_splitk, S chunks): blockIdx.z is the chunk.  A block
+// holds only its chunk's columns of the activation rows (so long rows leave
+// room for more stages) and runs every tile over the chunk's blocks
+// [4 floor(c G / S), 4 floor((c + 1) G / S)) (G = K / 128, the last chunk
+// ending at K / 32): partial index = global block index mod 4 (chunks start
+// on a multiple of 4 blocks), and the chunk's (p0 + p2) + (p1 + p3) goes to
+// part[c][t][o].  The blocks of a row group are split evenly over the
+// chunks, so the tiles x chunks work units still spread over every SM.
 #include "lk_ring_kernel.cuh"
 
 namespace lkmma {
@@ -83,7 +92,21 @@ struct MmaArgs {
   unsigned long long* trace;  // option "trace" 3: the launch timeline, else NULL
   int tslot;
   int prefill;             // warps that fill their stages before the dependency wait
+  int S;                   // split-K chunks (gridDim.z), 1: the plain GEMV
+  long part_stride;        // split-K: elements of one chunk's partials (M * N)
 };
+
+// This block's split-K chunk: its first 32-block and its length in bytes of
+// K (the whole row when S == 1).
+struct Chunk {
+  int k_lo, kc;
+};
+__device__ __forceinline__ Chunk chunk_of(const MmaArgs& ra) {
+  const int nb = ra.p.K >> 5;
+  if (ra.S <= 1) return Chunk{0, ra.p.K};
+  const int b_lo = splitk_bound(nb, ra.S, blockIdx.z), b_hi = splitk_bound(nb, ra.S, blockIdx.z + 1);
+  return Chunk{32 * b_lo, 32 * (b_hi - b_lo)};
+}
 
 // int8 x 4 (b0 lowest) -> two f16x2: (b0, b1) and (b2, b3), exact.
 __device__ __forceinline__ void i8x4_to_h2(unsigned w, unsigned& lo, unsigned& hi) {
@@ -188,15 +211,25 @@ __device__ __forceinline__ Mat mat_of(const MmaArgs& ra, long tile) {
   return m;
 }
 
-// Slice c of tile `tile` into the stage buffer st, completing on `full`.
-__device__ __forceinline__ void issue(const MmaArgs& ra, long tile, int c, unsigned char* st, unsigned full,
-                                      unsigned long long pol, int lane) {
+// Bytes between a stage's scale row start (a 16-byte boundary) and the
+// scale of level offset k0 (a multiple of 128): 0 or 8.
+__device__ __forceinline__ unsigned scale_shift(int k0) { return (unsigned)((k0 >> 5) & 7) * 2u; }
+
+// Slice c of tile `tile` (of the chunk ch) into the stage buffer st,
+// completing on `full`.
+__device__ __forceinline__ void issue(const MmaArgs& ra, const Chunk& ch, long tile, int c, unsigned char* st,
+                                      unsigned full, unsigned long long pol, int lane) {
   const int K = ra.p.K;
   const Mat m = mat_of(ra, tile);
   const int rows = m.N - m.row0 < TR ? (int)(m.N - m.row0) : TR;
-  const int k0 = c * (int)ra.tk;
-  const int len = K - k0 < (int)ra.tk ? K - k0 : (int)ra.tk;
-  if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * (unsigned)len * 17u / 16u);
+  const int kl = c * (int)ra.tk;
+  const int len = ch.kc - kl < (int)ra.tk ? ch.kc - kl : (int)ra.tk;
+  const int k0 = ch.k_lo + kl;
+  // a row's scales from the 16-byte boundary at or before them (a chunk may
+  // start 4 blocks = 8 bytes past one): scale_shift(k0) bytes of lead
+  const unsigned sh = scale_shift(k0);
+  const unsigned slen = ((unsigned)len / 16u + sh + 15u) & ~15u;
+  if (lane == 0) mbar_arrive_expect_tx(full, (unsigned)rows * ((unsigned)len + slen));
   __syncwarp();
   const int r = lane & 15;
   if (r < rows) {
@@ -204,7 +237,7 @@ __device__ __forceinline__ void issue(const MmaArgs& ra, long tile, int c, unsig
     if (lane < 16)
       bulk(st + r * ra.rs, m.wq + row * K + k0, (unsigned)len, full, pol);
     else
-      bulk(st + ra.s_off + r * ra.srs, m.ws + (row * (K >> 5) + (k0 >> 5)) * 2, (unsigned)len / 16u, full, pol);
+      bulk(st + ra.s_off + r * ra.srs, m.ws + (row * (K >> 5) + (k0 >> 5)) * 2 - sh, slen, full, pol);
   }
   __syncwarp();
 }
@@ -214,14 +247,16 @@ __device__ __forceinline__ void issue(const MmaArgs& ra, long tile, int c, unsig
 // rows by warp 0's bulk copies completing on act_bar (bounded wait).
 // Returns false when that wait gave up.
 template <int Q, bool A16>
-__device__ __forceinline__ bool load_rows(const MmaArgs& ra, int M, int row0, unsigned char* act, unsigned act_bar,
-                                          volatile int* abort_flag) {
+__device__ __forceinline__ bool load_rows(const MmaArgs& ra, const Chunk& ch, int M, int row0, unsigned char* act,
+                                          unsigned act_bar, volatile int* abort_flag) {
   const lkh::GemvProblem& a = ra.p;
-  const int K = a.K, nb = K >> 5;
-  // this block's group of activation rows: rows row0 .. row0 + M - 1
-  const int8_t* gxq = a.xq + (long)row0 * K;
-  const int8_t* gxl = Q == 2 ? a.xl + (long)row0 * K : nullptr;
-  const float* gxs = a.xs + (long)row0 * nb;
+  const int KG = a.K, nbg = KG >> 5;  // the rows' length in global memory
+  const int K = ch.kc, nb = K >> 5;   // the chunk's columns, held from offset 0
+  // this block's group of activation rows: rows row0 .. row0 + M - 1, from
+  // the chunk's first column
+  const int8_t* gxq = a.xq + (long)row0 * KG + ch.k_lo;
+  const int8_t* gxl = Q == 2 ? a.xl + (long)row0 * KG + ch.k_lo : nullptr;
+  const float* gxs = a.xs + (long)row0 * nbg + (ch.k_lo >> 5);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // the activation rows: int8 words (and low words) and scales, row-padded
   if (A16) {
@@ -237,7 +272,7 @@ __device__ __forceinline__ bool load_rows(const MmaArgs& ra, int M, int row0, un
           const int lo = Q == 2 && i >= M * runs;
           const int j = lo ? i - M * runs : i;
           const int row = j / runs, off = (j - row * runs) << 4;
-          v[u] = ld_cg16((lo ? gxl : gxq) + (long)row * K + off);
+          v[u] = ld_cg16((lo ? gxl : gxq) + (long)row * KG + off);
         }
       }
 #pragma unroll
@@ -260,7 +295,7 @@ __device__ __forceinline__ bool load_rows(const MmaArgs& ra, int M, int row0, un
     }
     for (int i = threadIdx.x; i < M * nb; i += blockDim.x) {
       const int row = i / nb, b = i - row * nb;
-      ((float*)(act + ra.a_xs))[(size_t)row * ra.xsr + b] = __ldcg(gxs + (long)row * nb + b);
+      ((float*)(act + ra.a_xs))[(size_t)row * ra.xsr + b] = __ldcg(gxs + (long)row * nbg + b);
     }
     __syncthreads();
   } else if (warp == 0) {
@@ -271,11 +306,11 @@ __device__ __forceinline__ bool load_rows(const MmaArgs& ra, int M, int row0, un
     if (lane == 0)
       mbar_arrive_expect_tx(act_bar, (unsigned)M * ((unsigned)K * (Q == 2 ? 2u : 1u) + (unsigned)nb * 4u));
     __syncwarp();
-    if (lane < M) bulk(act + (size_t)lane * ra.ar, gxq + (long)lane * K, (unsigned)K, act_bar, pol_a);
+    if (lane < M) bulk(act + (size_t)lane * ra.ar, gxq + (long)lane * KG, (unsigned)K, act_bar, pol_a);
     if (Q == 2 && lane >= 8 && lane < 8 + M)
-      bulk(act + ra.a_lo + (size_t)(lane - 8) * ra.ar, gxl + (long)(lane - 8) * K, (unsigned)K, act_bar, pol_a);
+      bulk(act + ra.a_lo + (size_t)(lane - 8) * ra.ar, gxl + (long)(lane - 8) * KG, (unsigned)K, act_bar, pol_a);
     if (lane >= 16 && lane < 16 + M)
-      bulk(act + ra.a_xs + (size_t)(lane - 16) * ra.xsr * 4, gxs + (long)(lane - 16) * nb, (unsigned)nb * 4u,
+      bulk(act + ra.a_xs + (size_t)(lane - 16) * ra.xsr * 4, gxs + (long)(lane - 16) * nbg, (unsigned)nb * 4u,
            act_bar, pol_a);
     __syncwarp();
   }
@@ -301,7 +336,10 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   const lkh::GemvProblem& a = ra.p;
   const int nw = ra.nw, D = ra.depth, NS = nw * D;
   const int row0 = TN * (int)blockIdx.y;                  // this block's group of activation rows
-  const int M = a.M - row0 < TN ? a.M - row0 : TN, K = a.K;
+  const int M = a.M - row0 < TN ? a.M - row0 : TN;
+  const Chunk ch = chunk_of(ra);
+  const int K = ch.kc;                                    // the chunk's bytes of K
+  const long ystep = ra.S > 1 ? (long)blockIdx.z * ra.part_stride : 0;  // this chunk's partials
   unsigned char* act = smem;
   unsigned char* ring = smem + ra.ring_off;
   unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
@@ -337,16 +375,16 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
   // (warps >= prefill fill their stages once the activation is loaded)
   const bool early = warp < ra.prefill;
   for (; early && issued < T && issued < D; ++issued, ic.next(tl))
-    issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
-          pol_w, lane);
+    issue(ra, ch, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes,
+          full0 + 8 * (warp * D + (int)issued), pol_w, lane);
 
   if (ra.pdl) griddep_wait();
   tstamp(ra.trace, ra.tslot, TR_WAITED);
-  bool ok = load_rows<Q, A16>(ra, M, row0, act, act_bar, abort_flag);
+  bool ok = load_rows<Q, A16>(ra, ch, M, row0, act, act_bar, abort_flag);
   tstamp(ra.trace, ra.tslot, TR_ACT);
   for (; !early && issued < T && issued < D; ++issued, ic.next(tl))
-    issue(ra, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes, full0 + 8 * (warp * D + (int)issued),
-          pol_w, lane);
+    issue(ra, ch, ic.tile, ic.c, ring + (size_t)(warp * D + issued) * ra.stage_bytes,
+          full0 + 8 * (warp * D + (int)issued), pol_w, lane);
   // activation row g's words and the scales of activation rows 2t, 2t+1
   const bool gx_ok = g < M;
   const unsigned char* XH = act + (size_t)g * ra.ar + (A16 ? 16 : 8) * t;
@@ -379,7 +417,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
     const int len = K - k0 < (int)ra.tk ? K - k0 : (int)ra.tk;
     const unsigned char* W0 = st + g * ra.rs + 8 * t;
     const unsigned char* W8 = W0 + 8 * ra.rs;
-    const unsigned char* S0 = st + ra.s_off + g * ra.srs;
+    const unsigned char* S0 = st + ra.s_off + g * ra.srs + scale_shift(ch.k_lo + k0);
     const unsigned char* S8 = S0 + 8 * ra.srs;
     const int b0 = k0 >> 5;
     const int ngrp = len >> 7;  // groups of 4 blocks (partials 0..3)
@@ -435,7 +473,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
     __syncwarp();
     if (issued < T) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(ra, ic.tile, ic.c, st, full0 + 8 * slot, pol_w, lane);
+      issue(ra, ch, ic.tile, ic.c, st, full0 + 8 * slot, pol_w, lane);
       ic.next(tl);
       ++issued;
     }
@@ -453,24 +491,24 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
       }
       if (r0 < mt.N) {
         if (t0 < M) {
-          mt.y[(long)(row0 + t0) * mt.N + r0] = yv[0];
+          mt.y[ystep + (long)(row0 + t0) * mt.N + r0] = yv[0];
           const unsigned long long k = amax_key(yv[0], (unsigned)r0);
           best0 = k > best0 ? k : best0;
         }
         if (t1 < M) {
-          mt.y[(long)(row0 + t1) * mt.N + r0] = yv[1];
+          mt.y[ystep + (long)(row0 + t1) * mt.N + r0] = yv[1];
           const unsigned long long k = amax_key(yv[1], (unsigned)r0);
           best1 = k > best1 ? k : best1;
         }
       }
       if (r8 < mt.N) {
         if (t0 < M) {
-          mt.y[(long)(row0 + t0) * mt.N + r8] = yv[2];
+          mt.y[ystep + (long)(row0 + t0) * mt.N + r8] = yv[2];
           const unsigned long long k = amax_key(yv[2], (unsigned)r8);
           best0 = k > best0 ? k : best0;
         }
         if (t1 < M) {
-          mt.y[(long)(row0 + t1) * mt.N + r8] = yv[3];
+          mt.y[ystep + (long)(row0 + t1) * mt.N + r8] = yv[3];
           const unsigned long long k = amax_key(yv[3], (unsigned)r8);
           best1 = k > best1 ? k : best1;
         }
@@ -542,7 +580,10 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
   const lkh::GemvProblem& a = ra.p;
   const int nw = ra.nw, NG = nw / G4, D = ra.depth, NS = NG * D;
   const int row0 = TN * (int)blockIdx.y;                  // this block's group of activation rows
-  const int M = a.M - row0 < TN ? a.M - row0 : TN, K = a.K;
+  const int M = a.M - row0 < TN ? a.M - row0 : TN;
+  const Chunk ch = chunk_of(ra);
+  const int K = ch.kc;                                    // the chunk's bytes of K
+  const long ystep = ra.S > 1 ? (long)blockIdx.z * ra.part_stride : 0;  // this chunk's partials
   unsigned char* act = smem;
   unsigned char* ring = smem + ra.ring_off;
   unsigned long long* bars = (unsigned long long*)(ring + (size_t)NS * ra.stage_bytes);
@@ -589,16 +630,16 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
   const bool early = grp < ra.prefill;  // groups that fill before the dependency wait
   if (leader)
     for (; early && issued < T && issued < D; ++issued, ic.next(tl))
-      issue(ra, ic.tile, ic.c, ring + (size_t)(grp * D + issued) * ra.stage_bytes, full0 + 8 * (grp * D + (int)issued),
-            pol_w, lane);
+      issue(ra, ch, ic.tile, ic.c, ring + (size_t)(grp * D + issued) * ra.stage_bytes,
+            full0 + 8 * (grp * D + (int)issued), pol_w, lane);
   if (ra.pdl) griddep_wait();
   tstamp(ra.trace, ra.tslot, TR_WAITED);
-  bool ok = load_rows<Q, A16>(ra, M, row0, act, act_bar, abort_flag);
+  bool ok = load_rows<Q, A16>(ra, ch, M, row0, act, act_bar, abort_flag);
   tstamp(ra.trace, ra.tslot, TR_ACT);
   if (leader)
     for (; !early && issued < T && issued < D; ++issued, ic.next(tl))
-      issue(ra, ic.tile, ic.c, ring + (size_t)(grp * D + issued) * ra.stage_bytes, full0 + 8 * (grp * D + (int)issued),
-            pol_w, lane);
+      issue(ra, ch, ic.tile, ic.c, ring + (size_t)(grp * D + issued) * ra.stage_bytes,
+            full0 + 8 * (grp * D + (int)issued), pol_w, lane);
 
   const bool gx_ok = g < M;
   const unsigned char* XH = act + (size_t)g * ra.ar + (A16 ? 16 : 8) * t;
@@ -626,7 +667,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
     const int len = K - k0 < (int)ra.tk ? K - k0 : (int)ra.tk;
     const unsigned char* W0 = st + g * ra.rs + 8 * t;
     const unsigned char* W8 = W0 + 8 * ra.rs;
-    const unsigned char* S0 = st + ra.s_off + g * ra.srs;
+    const unsigned char* S0 = st + ra.s_off + g * ra.srs + scale_shift(ch.k_lo + k0);
     const unsigned char* S8 = S0 + 8 * ra.srs;
     const int b0 = k0 >> 5, nblk = len >> 5;
 #pragma unroll 4
@@ -688,24 +729,24 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
         const int t0 = 2 * t, t1 = 2 * t + 1;
         if (r0 < mt.N) {
           if (t0 < M) {
-            mt.y[(long)(row0 + t0) * mt.N + r0] = yv[0];
+            mt.y[ystep + (long)(row0 + t0) * mt.N + r0] = yv[0];
             const unsigned long long k = amax_key(yv[0], (unsigned)r0);
             best0 = k > best0 ? k : best0;
           }
           if (t1 < M) {
-            mt.y[(long)(row0 + t1) * mt.N + r0] = yv[1];
+            mt.y[ystep + (long)(row0 + t1) * mt.N + r0] = yv[1];
             const unsigned long long k = amax_key(yv[1], (unsigned)r0);
             best1 = k > best1 ? k : best1;
           }
         }
         if (r8 < mt.N) {
           if (t0 < M) {
-            mt.y[(long)(row0 + t0) * mt.N + r8] = yv[2];
+            mt.y[ystep + (long)(row0 + t0) * mt.N + r8] = yv[2];
             const unsigned long long k = amax_key(yv[2], (unsigned)r8);
             best0 = k > best0 ? k : best0;
           }
           if (t1 < M) {
-            mt.y[(long)(row0 + t1) * mt.N + r8] = yv[3];
+            mt.y[ystep + (long)(row0 + t1) * mt.N + r8] = yv[3];
             const unsigned long long k = amax_key(yv[3], (unsigned)r8);
             best1 = k > best1 ? k : best1;
           }
@@ -723,7 +764,7 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_g4_kernel(const MmaArgs r
         break;
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(ra, ic.tile, ic.c, st, full0 + 8 * slot, pol_w, lane);
+      issue(ra, ch, ic.tile, ic.c, st, full0 + 8 * slot, pol_w, lane);
       ic.next(tl);
       ++issued;
     }
@@ -776,6 +817,18 @@ struct MmaLayout {
 
 unsigned round_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
 
+// Bytes of K a block holds: the whole row, or the longest split-K chunk.
+unsigned chunk_k(const lkh::GemvProblem& p) {
+  if (!p.split || p.S <= 1) return (unsigned)p.K;
+  const int nb = p.K / 32;
+  int m = 0;
+  for (int c = 0; c < p.S; ++c) {
+    const int w = splitk_bound(nb, p.S, c + 1) - splitk_bound(nb, p.S, c);
+    m = w > m ? w : m;
+  }
+  return 32u * (unsigned)m;
+}
+
 // Stage layout.  A warp computes its tiles alone, one 32-block after the
 // other, so two regimes (measured, 8 rows):
 //  * many tiles per SM (gate/up 24576 x 4096: 10 per SM): warps beat stages
@@ -788,7 +841,7 @@ unsigned round_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
 // Below 4 tiles per SM the second regime's layout is tried first.
 MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int smem_optin, bool a16) {
   MmaLayout L{};
-  const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)(p.M < TN ? p.M : TN);  // a block's rows
+  const unsigned K = chunk_k(p), nb = K / 32u, M = (unsigned)(p.M < TN ? p.M : TN);  // a block's rows
   L.a16 = a16;
   L.ar = a16 ? 2u * K + 64u : K + 32u;
   L.xsr = nb + 4u;
@@ -826,7 +879,7 @@ MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int sm
 // times faster than one warp), as many groups as fit, up to four.
 MmaLayout mma_layout_g4(const lkh::GemvProblem& p, int smem_optin, bool a16, unsigned tk_pref = 0) {
   MmaLayout L{};
-  const unsigned K = (unsigned)p.K, nb = K / 32u, M = (unsigned)(p.M < TN ? p.M : TN);  // a block's rows
+  const unsigned K = chunk_k(p), nb = K / 32u, M = (unsigned)(p.M < TN ? p.M : TN);  // a block's rows
   L.a16 = a16;
   L.g4 = true;
   L.ar = a16 ? 2u * K + 64u : K + 32u;
@@ -891,7 +944,7 @@ MmaLayout mma_layout(const lkh::GemvProblem& p, long ntiles, int sms, int smem_o
   // tile: its doubled activation area leaves four-warp groups too few
   // stages, down 64.2 -> 130.1 us.)
   if (p.cfg.mma_group == 0 && p.mode == LK_INT8ACT && ntiles < 4L * sms) {
-    const MmaLayout G = mma_layout_g4(p, smem_optin, false, p.K > 8192 ? 2048u : 1024u);
+    const MmaLayout G = mma_layout_g4(p, smem_optin, false, chunk_k(p) > 8192 ? 2048u : 1024u);
     if (mma_layout_ok(G)) return G;
   }
   if (p.cfg.mma_group == 4) {
@@ -932,9 +985,15 @@ int mma_group_blocks(int M, int sms) {
   return g > 0 ? g : 1;
 }
 
+// Split-K chunks of a launch (1 for the plain GEMV).
+int mma_chunks(const GemvProblem& p) { return p.split && p.S > 1 ? p.S : 1; }
+
 bool mma_supports(const GemvProblem& p) {
   if (p.mode != LK_INT8ACT && p.mode != LK_TWOPASS) return false;
-  if (p.split || p.fuse || p.F > 0) return false;
+  if (p.fuse || p.F > 0) return false;
+  // split-K: every chunk holds at least one group of four blocks (an empty
+  // chunk would have no tile to write its zero partials)
+  if (p.split && (p.S < 1 || p.K / 128 < p.S || p.amax)) return false;
   const int min_m = p.cfg.mma_min_m > 0 ? p.cfg.mma_min_m : 2;
   if (p.M < min_m || p.M > LK_MAX_BATCH) return false;
   if (p.K < 256 || p.K % 256 || p.N < 1) return false;
@@ -943,7 +1002,8 @@ bool mma_supports(const GemvProblem& p) {
   // each group's rows start 16-byte aligned (K % 256 == 0) and its scales too
   const DeviceInfo* d = device_info(nullptr);
   if (!d) return false;
-  return mma_layout_ok(mma_layout(p, (p.N + TR - 1) / TR, mma_group_blocks(p.M, d->sm_count), d->smem_optin));
+  return mma_layout_ok(mma_layout(p, (p.N + TR - 1) / TR * mma_chunks(p), mma_group_blocks(p.M, d->sm_count),
+                                  d->smem_optin));
 }
 
 // One launch over the matrices (wq[m], ws[m], N[m]) -> y[m], all reading
@@ -955,8 +1015,9 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   if (nmat < 1 || nmat > MG || (nmat > 1 && p.amax)) return LK_ERR_ARG;
   long all_tiles = 0;
   for (int m = 0; m < nmat; ++m) all_tiles += (N[m] + TR - 1) / TR;
-  const int ngrp = mma_groups(p.M), gsms = mma_group_blocks(p.M, d->sm_count);
-  const MmaLayout L = mma_layout(p, all_tiles, gsms, d->smem_optin);
+  const int ngrp = mma_groups(p.M), gsms = mma_group_blocks(p.M, d->sm_count), S = mma_chunks(p);
+  if (S > 1 && nmat > 1) return LK_ERR_ARG;
+  const MmaLayout L = mma_layout(p, all_tiles * S, gsms, d->smem_optin);
   if (!mma_layout_ok(L)) return LK_ERR_SHAPE;
   mma_fn f = L.i8 ? (p.mode == LK_TWOPASS ? gemv_mma_kernel<2, false, true> : gemv_mma_kernel<1, false, true>)
            : L.g4 ? (p.mode == LK_TWOPASS ? (L.a16 ? gemv_mma_g4_kernel<2, true> : gemv_mma_g4_kernel<2, false>)
@@ -985,9 +1046,12 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   if (tiles < 1) return LK_ERR_SHAPE;
   ra.nw = L.nw;
   ra.depth = L.depth;
-  long gx = p.cfg.grid_ctas > 0 ? p.cfg.grid_ctas : gsms;
+  // a row group's blocks, split evenly over the chunks
+  long gx = p.cfg.grid_ctas > 0 ? p.cfg.grid_ctas : (gsms / S > 0 ? gsms / S : 1);
   if (gx > ra.ntiles) gx = ra.ntiles;
   ra.gx = (int)gx;
+  ra.S = S;
+  ra.part_stride = (long)p.M * N[0];
   ra.tk = L.tk;
   ra.rs = L.rs;
   ra.srs = L.srs;
@@ -1007,7 +1071,7 @@ lk_status mma_launch(const GemvProblem& p, int nmat, const int8_t* const* wq, co
   ra.tslot = opt_trace == 3 ? trace_next_slot() : -1;
   ra.prefill = L.g4 ? prefill_warps(L.nw / G4, p.cfg.prefill) : prefill_warps(L.nw, p.cfg.prefill);  // groups, or warps
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)gx, (unsigned)ngrp);
+  cfg.gridDim = dim3((unsigned)gx, (unsigned)ngrp, (unsigned)S);
   cfg.blockDim = dim3(L.nw * 32);
   cfg.dynamicSmemBytes = L.total;
   cfg.stream = stream;

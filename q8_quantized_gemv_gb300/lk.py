@@ -22,6 +22,7 @@ LK_MAX_M = 8
 LK_MAX_BATCH = 64
 LK_MAX_SPLITK = 64
 LK_TRACE_REC = 8  # entries of one launch record of option "trace" 3
+LK_TRACE_MAX_RECORDS = 4096 // LK_TRACE_REC  # records the timeline keeps before wrapping
 
 STATUS = {0: "LK_OK", -1: "LK_ERR_ARG", -2: "LK_ERR_ALIGN", -3: "LK_ERR_SHAPE",
           -4: "LK_ERR_WORKSPACE", -5: "LK_ERR_CUDA", -6: "LK_ERR_DEVICE_TIMEOUT"}

@@ -139,7 +139,7 @@ def test_mma_declines():
     assert lk.lk_gemv_kernel_for(4096, 4096, 0, 8, 0) != 3   # Dequant
     assert lk.lk_gemv_kernel_for(4096, 4096, 1, 1, 0) != 3   # one row
     assert lk.lk_gemv_kernel_for(4096, 4128, 1, 8, 0) != 3   # K % 256 != 0
-    assert lk.lk_gemv_kernel_for(4096, 4096, 1, 8, 2) != 3   # split-K
+    assert lk.lk_gemv_kernel_for(4096, 4096, 1, 8, 2) == 3   # split-K too (each block: its chunk)
     # TwoPass activations of 8 rows x 12288 (209 KB) leave room for one warp's
     # two 512-byte stages: still taken
     assert lk.lk_gemv_kernel_for(4096, 12288, 2, 8, 0) == 3
@@ -212,15 +212,63 @@ def test_batch_past_eight_matches_groups_of_eight(mode):
 
 
 def test_past_eight_rows_needs_the_tensor_core_path():
-    """Past 8 rows only the tensor-core kernel runs: Dequant, split-K and
-    K % 256 != 0 are shape errors, not silent fallbacks."""
+    """Past 8 rows only the tensor-core kernel runs (split-K included):
+    Dequant and K % 256 != 0 are shape errors, not silent fallbacks."""
     assert lk.lk_gemv_kernel_for(4096, 4096, I8, 64, 0) == 3
     assert lk.lk_gemv_kernel_for(4096, 4096, I8, 65, 0) == 0
     assert lk.lk_gemv_kernel_for(4096, 4096, 0, 16, 0) == 0
     assert lk.lk_gemv_kernel_for(4096, 1056, I8, 16, 0) == 0
-    assert lk.lk_gemv_kernel_for(4096, 4096, I8, 16, 2) == 0
+    assert lk.lk_gemv_kernel_for(4096, 4096, I8, 16, 2) == 3
     wq, ws = to_dev(np.zeros((64, 1056), np.int8)), to_dev(np.zeros((64, 33), np.uint16))
     x = to_dev(np.zeros((16, 1056), np.float32))
     y = torch.empty((16, 64), dtype=torch.float32, device=DEV)
     with pytest.raises(lk.LkError):
         lk.lk_gemv_q8(wq, ws, 0, y, x=x, M=16)
+
+
+# ---- split-K on the tensor-core kernel -------------------------------------------------
+
+@pytest.mark.parametrize("layout", ["f16", "f16-g4", "i8"])
+@pytest.mark.parametrize("mode", [I8, TP])
+@pytest.mark.parametrize("M", [2, 8, 33, 64])
+@pytest.mark.parametrize("S", [2, 3, 8])
+@pytest.mark.parametrize("N,K", [(1000, 1280), (300, 12288), (2500, 4096)])
+def test_mma_splitk_matches_oracle(layout, mode, M, S, N, K):
+    """lk_gemv_q8_splitk on the tensor-core kernel (each block holds only its
+    chunk's columns of the activation rows): every chunk's partials bit for
+    bit the oracle's chunks, including chunks that start 4 blocks past a
+    16-byte scale boundary (S = 3), and the ascending combine bit for bit the
+    oracle's split-K value; run to run identical."""
+    cfg = mma(mma_i8=1 if layout == "i8" else 2, mma_group=4 if "g4" in layout else 1)
+    if lk.lk_gemv_kernel_for(N, K, mode, M, S, cfg=cfg) != 3:
+        pytest.skip("layout does not fit")
+    wq, ws = synth.q8_matrix(N, K, 9300 + N + K)
+    x = synth.activation(M, K, 9301 + M, outliers=True)
+    y_or, ch_or = oracle.gemv_splitk(wq, ws, mode, S, **oracle_acts(x, mode))
+    wq_d, ws_d, acts = to_dev(wq), to_dev(ws), dev_acts(x, mode)
+    outs = []
+    for _ in range(2):
+        part = torch.full((S, M, N), float("nan"), dtype=torch.float32, device=DEV)
+        lk.lk_gemv_q8_splitk(wq_d, ws_d, mode, S, part, M=M, cfg=cfg, **acts)
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+        lk.lk_splitk_combine(mode, part, S, M, N, y)
+        torch.cuda.synchronize()
+        assert lk.lk_device_error(reset=True) == 0
+        assert np.array_equal(bits(host(part)), bits(ch_or))
+        assert np.array_equal(bits(host(y)), bits(y_or))
+        outs.append(host(y).copy())
+    assert np.array_equal(bits(outs[0]), bits(outs[1]))
+
+
+def test_mma_splitk_declines_empty_chunks():
+    """A chunk with no block (S > K / 128) is not the tensor-core kernel's:
+    up to 8 rows the other kernels take it (with its zero partials), past 8
+    rows it is a shape error."""
+    assert lk.lk_gemv_kernel_for(64, 256, I8, 8, 4) in (1, 2)
+    assert lk.lk_gemv_kernel_for(64, 256, I8, 16, 4) == 0
+    assert lk.lk_gemv_kernel_for(64, 1024, I8, 16, 8) == 3
+    wq, ws = to_dev(np.zeros((64, 256), np.int8)), to_dev(np.zeros((64, 8), np.uint16))
+    xq, xs = to_dev(np.zeros((16, 256), np.int8)), to_dev(np.zeros((16, 8), np.float32))
+    part = torch.empty((4, 16, 64), dtype=torch.float32, device=DEV)
+    with pytest.raises(lk.LkError):
+        lk.lk_gemv_q8_splitk(wq, ws, I8, 4, part, xq=xq, xs=xs, M=16)
