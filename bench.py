@@ -442,7 +442,8 @@ def run_ours(a, rank, world):
                    "chain": stack.chain is not None,
                    "prefill": stack.prefill or "half of the warps",
                    "dataflow": "decoder (glu)" if stack.glu else "projections alone",
-                   "pdl": not a.no_pdl, "launch_cfg": a.cfg},
+                   "pdl": not a.no_pdl, "launch_cfg": a.cfg,
+                   "splitk": stack.splitk or "none (one activation row)"},
         "us_per_token": ms_max * 1e3,
         "pct_of_nominal_8TBs": value / world / NOMINAL_HBM_GBS,
         "roofline": roof,
@@ -547,7 +548,7 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
                 lk.lk_argmax(idx, B, N, parts=parts, n_parts=n)
         elif S > 1:
             lk.lk_gemv_q8_splitk(wq, ws, mode, S, part, M=B, cfg=cfg, **acts)
-            lk.lk_splitk_combine(mode, part, S, B, N, y)
+            lk.lk_splitk_combine(mode, part, S, B, N, y, cfg=cfg)
         else:
             n = lk.lk_gemv_q8(wq, ws, mode, y, M=B, argmax_parts=parts, cfg=cfg,
                               **({"x": xn} if xn is not None and a.norm else acts))
@@ -845,14 +846,90 @@ def roofline(stack, stream, a, torch):
     # taken on the current sources (profiles/traffic.txt), else null
     traffic = profile_traffic(f"gemv_{kname}_gateup_24576x4096_{mname}_b{stack.B}",
                               "mma" if kname == "mma" else "ring")
-    roof = {"bound": "hbm", "achieved": gu["GB/s"], "peak": peak, "unit": "GB/s",
-            "frac": gu["GB/s"] / peak, "traffic": traffic, "peak_source": src,
-            "kernel": f"gate/up GEMV 24576x4096 ({kname} kernel)", "algorithmic_bytes_per_launch": alg_bytes("gu"),
-            "avg_launch_us": gu["us"], "launches_timed": gu["launches"]}
+    b2b_us, n_b2b = gu_back_to_back(stack, stream, a, torch)
+    alg = alg_bytes("gu")
+    roof = {"bound": "hbm", "achieved": alg / (b2b_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
+            "frac": alg / (b2b_us * 1e-6) / 1e9 / peak, "traffic": traffic, "peak_source": src,
+            "kernel": f"gate/up GEMV 24576x4096 ({kname} kernel)", "algorithmic_bytes_per_launch": alg,
+            "avg_launch_us": b2b_us, "launches_timed": n_b2b,
+            "timing": "CUDA events around a graph of the token's gate/up launches back to back (every layer's "
+                      "matrix, each launch a programmatic dependent of the one before, as in the token)",
+            "event_bracketed_us": gu["us"],
+            "in_sequence_us": gu_in_sequence(stack, stream, torch)}
     tot_b = sum(alg_bytes(n) * len(ts) for n, ts in times.items())
     tot_t = sum(sum(ts) for ts in times.values())
-    roof["all_gemv_achieved"] = tot_b / (tot_t * 1e-3) / 1e9
+    roof["all_gemv_event_bracketed"] = tot_b / (tot_t * 1e-3) / 1e9
     return roof, per
+
+
+def _gu_launches(stack):
+    """The token's gate/up launch closures, in order (one token is run to
+    collect them; each closure repeats its launch with the same arguments)."""
+    got = []
+
+    def hook(name, launch):
+        if name == "gu":
+            got.append(launch)
+        return launch()
+
+    stack.run_token(hook=hook)
+    return got
+
+
+def gu_back_to_back(stack, stream, a, torch):
+    """Average duration of the dominant kernel launched back to back: one
+    graph of the token's gate/up launches (one per layer, each over its own
+    matrix, so nothing is reused through L2), replayed; CUDA events around
+    the replays on the launching stream.  Returns (us per launch, launches)."""
+    with torch.cuda.stream(stream):
+        launches = _gu_launches(stack)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for f in launches:
+                f()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(3, min(a.steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    n = reps * len(launches)
+    return e0.elapsed_time(e1) * 1e3 / n, n
+
+
+def gu_in_sequence(stack, stream, torch):
+    """The gate/up launches' share of one captured token, from the library's
+    launch timeline (%globaltimer, option "trace" 3): from the previous
+    launch's last block end to this launch's last block end, averaged over
+    the layers (us); None where the timeline does not cover the token."""
+    from q8_quantized_gemv_gb300 import lk
+    n = stack.launches_per_token() - 1  # every launch but the argmax reduce is recorded
+    if n > lk.LK_TRACE_MAX_RECORDS:
+        return None
+    lk.lk_set_option("trace", 3)
+    try:
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                stack.run_token()
+            g.replay()
+            torch.cuda.synchronize()
+            lk.lk_set_option("trace", 3)  # restart the record count, then one timed replay
+            g.replay()
+        torch.cuda.synchronize()
+        raw = lk.lk_trace_read(lk.LK_TRACE_REC * lk.LK_TRACE_MAX_RECORDS)
+    finally:
+        lk.lk_set_option("trace", 0)
+    R = lk.LK_TRACE_REC
+    rec = [raw[i * R:(i + 1) * R] for i in range(n)]
+    rows = 2 * stack.F
+    spans = [(rec[i][3] - rec[i - 1][3]) / 1e3 for i in range(1, n) if rec[i][6] == rows and rec[i][5] in (1, 3)]
+    return sum(spans) / len(spans) if spans else None
 
 
 def main():

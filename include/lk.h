@@ -366,14 +366,29 @@ lk_status lk_gemv_chain(const lk_chain_op* ops, const lk_chain_op* ops_dev, int 
  * Which GEMV kernel a call of this shape would launch with these settings,
  * for 16-byte aligned operands: 1 the direct-load kernel (any K % 32 == 0,
  * M <= LK_MAX_M), 2 the bulk-copy ring kernel (K % 256 == 0 and the
- * activation fits in shared memory), 3 the tensor-core kernel (lk_gemv_q8
- * only: LK_INT8ACT or LK_TWOPASS, cfg->mma_min_m (default 2) <= M <=
- * LK_MAX_BATCH, K % 256 == 0 and the activation fitting in shared memory
- * next to a weight ring), 0 none (invalid shape or settings, or a kernel
+ * activation fits in shared memory), 3 the tensor-core kernel (LK_INT8ACT
+ * or LK_TWOPASS, cfg->mma_min_m (default 2) <= M <= LK_MAX_BATCH,
+ * K % 256 == 0, no argmax keys, for split-K every chunk non-empty
+ * (S <= K / 128), and the activation (a chunk's columns under split-K)
+ * fitting in shared memory next to a weight ring), 0 none (invalid shape or
+ * settings, or a kernel
  * forced by cfg->path but not applicable).  S = 0 asks about lk_gemv_q8,
  * S >= 1 about lk_gemv_q8_splitk.  cfg may be NULL (the defaults).
  */
 int lk_gemv_kernel_for(int N, int K, lk_mode mode, int M, int S, const lk_launch_cfg* cfg);
+
+/*
+ * The split-K chunk count this library's measurements favour for a GEMV of
+ * this shape (GB300): S > 1 where, at 2..LK_MAX_BATCH activation rows of
+ * Int8Act / TwoPass on the tensor-core kernel, holding only a chunk of the
+ * activation rows per block (more weight stages in flight, more work units
+ * than tiles) outweighs the extra combine launch; 1 elsewhere (one row,
+ * Dequant, a shape the tensor-core kernel does not take).  Split-K is the
+ * pages' own operation with its own summation order: lk_gemv_q8_splitk +
+ * lk_splitk_combine do not give lk_gemv_q8's bits, so a caller chooses it
+ * (the library's extension: the pages fix S per projection by hand).
+ */
+int lk_splitk_chunks_for(int N, int K, lk_mode mode, int M);
 
 /*
  * Bytes of the split-K partial buffer for (mode, S, M, N): S*M*N values,
@@ -389,7 +404,11 @@ size_t lk_splitk_workspace_bytes(lk_mode mode, int S, int M, int N);
  * groups).  A chunk's value is lk_gemv_q8's rule restricted to its blocks
  * (partial index = global block index mod 4); Dequant chunks are f64 sums.
  * Writes part[c][t][o] (layout [S][M][N], f32 or f64 by mode).  1 <= S <= 64.
- * part_bytes must be >= lk_splitk_workspace_bytes(mode, S, M, N).
+ * part_bytes must be >= lk_splitk_workspace_bytes(mode, S, M, N).  Up to
+ * LK_MAX_M rows on any kernel; 2..LK_MAX_BATCH rows of Int8Act / TwoPass
+ * on the tensor-core kernel, each block holding only its chunk's columns of
+ * the activation rows (past LK_MAX_M rows the only kernel: LK_ERR_SHAPE
+ * where it does not take the shape).
  */
 lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, lk_mode mode,
                             const float* x, const int8_t* xq, const int8_t* xl, const float* xs,
@@ -400,10 +419,12 @@ lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, 
  * The split-K combine (QWEN38_EXTRA_KERNELS gk_sk_combine): a separate
  * kernel, never atomics: y[t][o] = (((0 + part[0][t][o]) + part[1][t][o]) +
  * ...) in ascending chunk order, in f32 (f64 then one rounding to f32 under
- * LK_DEQUANT).  Same inputs give the same bits on every run.
+ * LK_DEQUANT).  Same inputs give the same bits on every run.  0 <= M <=
+ * LK_MAX_BATCH.  cfg: pdl (it reads the partials only after the launch
+ * before it completes); the other fields do not apply.
  */
 lk_status lk_splitk_combine(lk_mode mode, const void* part, int S, int M, int N, float* y,
-                            cudaStream_t stream);
+                            const lk_launch_cfg* cfg, cudaStream_t stream);
 
 /* Upper bound on the argmax partial keys per activation row that lk_gemv_q8
  * writes for an N-row matrix. */
@@ -480,9 +501,10 @@ lk_status lk_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* xq, con
  *                 waits inside, after requesting the norm gains), [2] block
  *                 0's activation ready, [3] the last block's end, [4] block
  *                 0's end (all %globaltimer ns), [5] kernel (1 ring, 2 chain,
- *                 3 tensor-core, 4 norm, 5 quantize), [6] rows (steps, for a
- *                 chain), [7] block 0's first weight stages issued.  Setting
- *                 the option restarts the record count.
+ *                 3 tensor-core, 4 norm, 5 quantize, 6 split-K combine),
+ *                 [6] rows (steps, for a chain), [7] block 0's first weight
+ *                 stages issued.  Setting the option restarts the record
+ *                 count.
  *   "wait_us"     time limit of every device-side wait, microseconds
  *                 (0 = default, 2 s; at most 6 * 10^7)
  * Unknown names or out-of-range values return LK_ERR_ARG; lk_get_option

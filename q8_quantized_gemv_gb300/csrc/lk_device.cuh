@@ -35,7 +35,7 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 constexpr int TREC = 8;
 enum : int { TR_START = 0, TR_WAITED = 1, TR_ACT = 2, TR_END_MAX = 3, TR_END0 = 4, TR_KIND = 5, TR_ROWS = 6,
              TR_ISSUED = 7 };
-enum : int { TK_RING = 1, TK_CHAIN = 2, TK_MMA = 3, TK_NORM = 4, TK_QUANT = 5 };
+enum : int { TK_RING = 1, TK_CHAIN = 2, TK_MMA = 3, TK_NORM = 4, TK_QUANT = 5, TK_COMBINE = 6 };
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

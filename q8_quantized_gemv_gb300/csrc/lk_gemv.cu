@@ -225,23 +225,40 @@ GemvProblem make_problem(const int8_t* wq, const uint16_t* ws, int N, int K, lk_
   return p;
 }
 
-// Combine: y = (((0 + c0) + c1) + ...) in ascending chunk order.
+// One output of the combine: y = (((0 + c0) + c1) + ...) in ascending
+// chunk order, the partials read through L2 (an earlier kernel wrote them).
 template <bool F64>
-__global__ void __launch_bounds__(256) splitk_combine_kernel(const void* __restrict__ part, int S, long MN,
-                                                             float* __restrict__ y) {
-  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= MN) return;
+__device__ __forceinline__ void combine_one(const void* __restrict__ part, int S, long MN, float* __restrict__ y,
+                                            long i) {
   if (F64) {
     const double* pp = (const double*)part;
     double acc = 0.0;
-    for (int c = 0; c < S; ++c) acc = __dadd_rn(acc, pp[(long)c * MN + i]);
+    for (int c = 0; c < S; ++c) acc = __dadd_rn(acc, __ldcg(pp + (long)c * MN + i));
     y[i] = __double2float_rn(acc);
   } else {
     const float* pp = (const float*)part;
     float acc = 0.f;
-    for (int c = 0; c < S; ++c) acc = __fadd_rn(acc, pp[(long)c * MN + i]);
+    for (int c = 0; c < S; ++c) acc = __fadd_rn(acc, __ldcg(pp + (long)c * MN + i));
     y[i] = acc;
   }
+}
+
+// Combine: y = (((0 + c0) + c1) + ...) in ascending chunk order.  As a
+// programmatic dependent it lets its own dependent launch at once and reads
+// the partials only after the split-K launch before it has completed.
+template <bool F64>
+__global__ void __launch_bounds__(256) splitk_combine_kernel(const void* __restrict__ part, int S, long MN,
+                                                             float* __restrict__ y, unsigned long long* tr,
+                                                             int slot) {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+  trec_stamp(tr, slot, TR_START);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  trec_stamp(tr, slot, TR_WAITED);
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < MN) {
+    combine_one<F64>(part, S, MN, y, i);
+  }
+  trec_end(tr, slot, TK_COMBINE, MN);
 }
 
 }  // namespace
@@ -437,6 +454,38 @@ lk_status lk_gemv_q8_glu(const int8_t* wg, const uint16_t* wsg, const int8_t* wu
   return lk_swiglu_quant(gu, gu + (long)M * F, M, F, F, mode, h, hq, hl, hs, cfg, stream);
 }
 
+// Measured on GB300 (bench.py gemv workload, combine included, us; S = 1,
+// 2, 4, 8, 12, 16, 24) for q|k|v 6144 x 4096, o 4096 x 4096, gate/up
+// 24576 x 4096 and down 4096 x 12288:
+//  * up to 8 rows, S = 8 is best or within 3 % everywhere: down 27.6 ->
+//    17.6 (Int8Act, 8 rows), 64.2 -> 21.4 (TwoPass), q|k|v 14.0 -> 12.7,
+//    gate/up 36.2 -> 31.3 (TwoPass); S = 12 .. 24 lose again;
+//  * 16 rows: S = 8 (down 53.1 -> 26.7, q|k|v 23.7 -> 17.1), except where
+//    the tiles x chunks per block pass ~100 (gate/up: S = 4, 50.9 -> 46.9);
+//  * 64 rows (8 row groups of 19 SMs): the combine's reads grow with the
+//    rows and a K = 4096 activation chunk frees little shared memory:
+//    gate/up and o best at S = 1, q|k|v at 2, down at 2 (Int8Act, 139.6 ->
+//    87.7) to 8 (TwoPass, 406.6 -> 110.9).
+// Rule: S = 8 for one row group; 8 halved while the work units (tiles x S)
+// pass 100 per block of a row group; past 16 rows also at most the
+// activation bytes a block holds over 24 KB (a power of two).
+int lk_splitk_chunks_for(int N, int K, lk_mode mode, int M) {
+  if ((mode != LK_INT8ACT && mode != LK_TWOPASS) || M < 2 || M > LK_MAX_BATCH || N < 1 || K < 256 || K % 256)
+    return 1;
+  const DeviceInfo* d = device_info(nullptr);
+  if (!d) return 1;
+  const long tiles = ((long)N + 15) / 16;
+  const int groups = (M + LK_MAX_M - 1) / LK_MAX_M;
+  const long blocks = d->sm_count / groups > 0 ? d->sm_count / groups : 1;
+  int S = 8;
+  while (S > 1 && (tiles * S > 100 * blocks || K / 128 < S)) S >>= 1;
+  if (M > 2 * LK_MAX_M) {
+    const long act = (long)LK_MAX_M * K * (mode == LK_TWOPASS ? 2 : 1);
+    while (S > 1 && act / S < 24 * 1024) S >>= 1;
+  }
+  return S > 1 && lk_gemv_kernel_for(N, K, mode, M, S, nullptr) == 3 ? S : 1;
+}
+
 size_t lk_splitk_workspace_bytes(lk_mode mode, int S, int M, int N) {
   if (S < 1 || M < 0 || N < 0) return 0;
   return (size_t)S * (size_t)M * (size_t)N * (mode == LK_DEQUANT ? 8 : 4);
@@ -474,8 +523,8 @@ lk_status lk_gemv_q8_splitk(const int8_t* wq, const uint16_t* ws, int N, int K, 
 }
 
 lk_status lk_splitk_combine(lk_mode mode, const void* part, int S, int M, int N, float* y,
-                            cudaStream_t stream) {
-  if (mode < LK_DEQUANT || mode > LK_TWOPASS) return LK_ERR_ARG;
+                            const lk_launch_cfg* cfg, cudaStream_t stream) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS || check_launch_cfg(cfg)) return LK_ERR_ARG;
   if (S < 1 || S > LK_MAX_SPLITK || M < 0 || M > LK_MAX_BATCH || N < 0) return LK_ERR_SHAPE;
   if (N == 0 || M == 0) return LK_OK;
   if (!part || !y) return LK_ERR_ARG;
@@ -483,9 +532,11 @@ lk_status lk_splitk_combine(lk_mode mode, const void* part, int S, int M, int N,
   const long MN = (long)M * N;
   const long blocks = (MN + 255) / 256;
   if (mode == LK_DEQUANT)
-    splitk_combine_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(part, S, MN, y);
+    launch_pdl(splitk_combine_kernel<true>, dim3((unsigned)blocks), dim3(256), stream, cfg_pdl(cfg), part, S, MN, y,
+               tr_ptr(), tr_slot());
   else
-    splitk_combine_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(part, S, MN, y);
+    launch_pdl(splitk_combine_kernel<false>, dim3((unsigned)blocks), dim3(256), stream, cfg_pdl(cfg), part, S, MN, y,
+               tr_ptr(), tr_slot());
   return launch_status();
 }
 

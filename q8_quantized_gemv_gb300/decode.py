@@ -34,7 +34,7 @@ class DecodeStack:
     def __init__(self, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936,
                  batch=1, mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6,
                  fused=False, chain=False, group_qkv=True, prefill=None, glu=False, fused_qkv=True, pdl=False,
-                 path=0, tune=None):
+                 path=0, tune=None, splitk=True):
         self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
         self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
         # per projection (qkv, o, gu, down, lm): warps of a GEMV block that
@@ -136,6 +136,24 @@ class DecodeStack:
         self.qkv_one = self.fused_qkv and self.chain is None and (all(fq) or not any(fq))
         if self.qkv_one:
             self.out.update(self.qkv_views)
+        # split-K at 2 or more activation rows (the tensor-core kernel holds a
+        # chunk of the activation per block, so long rows keep more weight
+        # stages in flight): the chunk count the library favours for each
+        # projection (lk_splitk_chunks_for; 1 = the plain GEMV).  splitk=False
+        # turns it off, a dict {projection: S} sets it.
+        cand = {}
+        if self.qkv_one and not any(fq):
+            cand["qkv"] = (q_dim + 2 * kv_dim, hidden)
+        for n in ("o", "gu", "down"):
+            if not self.fused[n] and not (n == "gu" and self.glu):
+                cand[n] = self.shapes[n]
+        if splitk is False or B < 2 or self.chain is not None:
+            self.splitk = {}
+        elif isinstance(splitk, dict):
+            self.splitk = {n: int(v) for n, v in splitk.items() if n in cand and int(v) > 1}
+        else:
+            self.splitk = {n: S for n, (N, K) in cand.items() if (S := lk.lk_splitk_chunks_for(N, K, self.mode, B)) > 1}
+        self.part = {n: torch.empty((S * B * cand[n][0],), dtype=f32, device=dev) for n, S in self.splitk.items()}
 
     def _act_bufs(self, K):
         B = self.B
@@ -181,6 +199,13 @@ class DecodeStack:
                                     prefill=self.prefill.get(name, 0) if name else 0))
 
     def _gemv(self, w, y, acts, parts=None, name=None):
+        S = self.splitk.get(name, 1)
+        if S > 1 and parts is None:
+            # the split-K partials, then their combine in ascending chunk order
+            c = self._cfg(name)
+            lk.lk_gemv_q8_splitk(w[0], w[1], self.mode, S, self.part[name], M=self.B, cfg=c, **acts)
+            lk.lk_splitk_combine(self.mode, self.part[name], S, self.B, w[0].shape[0], y, cfg=c)
+            return 0
         return lk.lk_gemv_q8(w[0], w[1], self.mode, y, M=self.B, argmax_parts=parts, cfg=self._cfg(name), **acts)
 
     def _chain_ops(self):
@@ -209,7 +234,7 @@ class DecodeStack:
         GEMV over the fused q|k|v matrix, or one grouped GEMV over three."""
         c = self._cfg("qkv")
         if self.fused_qkv:
-            return lambda: lk.lk_gemv_q8(w["qkv"][0], w["qkv"][1], self.mode, self.out_qkv, M=self.B, cfg=c, **a)
+            return lambda: self._gemv(w["qkv"], self.out_qkv, a, name="qkv")
         return lambda: lk.lk_gemv_q8_group([(w[n][0], w[n][1], self.out[n]) for n in ("q", "k", "v")], self.mode,
                                            M=self.B, cfg=c, **a)
 
@@ -321,8 +346,9 @@ class DecodeStack:
             return 1
         if self.glu:
             # first norm; per layer q/k/v, [quantize], o, add+norm, gate/up
-            # pair, down, add+norm; lm-head, argmax
-            per_layer = 5 + (0 if self.mode == lk.LK_DEQUANT else 1) + self.glu_launches()
+            # pair, down, add+norm (and a combine per split-K projection);
+            # lm-head, argmax
+            per_layer = 5 + (0 if self.mode == lk.LK_DEQUANT else 1) + self.glu_launches() + len(self.splitk)
             return 1 + self.L * per_layer + 2
         n = 1  # argmax reduce
         f = self.fused
@@ -333,5 +359,5 @@ class DecodeStack:
             (not any(f[n] for n in ("q", "k", "v")) and self.kernel["q"] in (2, 3))
         per_layer = (4 if grouped else 6) + qkv_norm \
             + (0 if (f["o"] or self.mode == lk.LK_DEQUANT) else 1) + (0 if f["gu"] else 1) \
-            + (0 if (f["down"] or self.mode == lk.LK_DEQUANT) else 1)
+            + (0 if (f["down"] or self.mode == lk.LK_DEQUANT) else 1) + len(self.splitk)
         return n + self.L * per_layer + 1 + (0 if f["lm"] else 1)

@@ -95,7 +95,8 @@ def _load():
         "lk_gemv_q8": ([P, P, I, I, I, P, P, P, P, I, P, P, P, P, P], I),
         "lk_splitk_workspace_bytes": ([I, I, I, I], S),
         "lk_gemv_q8_splitk": ([P, P, I, I, I, P, P, P, P, I, I, P, S, P, P], I),
-        "lk_splitk_combine": ([I, P, I, I, I, P, P], I),
+        "lk_splitk_combine": ([I, P, I, I, I, P, P, P], I),
+        "lk_splitk_chunks_for": ([I, I, I, I], I),
         "lk_argmax_parts_max": ([I], I),
         "lk_argmax_scratch_entries": ([I], I),
         "lk_argmax": ([P, P, I, I, I, P, P, P], I),
@@ -130,7 +131,7 @@ def exported_symbols():
             "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout", "lk_gemv_kernel_for",
             "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain", "lk_trace_read",
             "lk_argmax_noalloc", "lk_gemv_q8_group", "lk_add_rmsnorm_quant", "lk_swiglu_quant",
-            "lk_gemv_q8_glu"]
+            "lk_gemv_q8_glu", "lk_splitk_chunks_for"]
 
 
 def _ok(st, where):
@@ -319,9 +320,15 @@ def lk_gemv_q8_splitk(wq, ws, mode, S, part, x=None, xq=None, xl=None, xs=None, 
         "lk_gemv_q8_splitk")
 
 
-def lk_splitk_combine(mode, part, S, M, N, y, stream=None):
+def lk_splitk_combine(mode, part, S, M, N, y, stream=None, cfg=None):
     _ok(_load().lk_splitk_combine(_mode(mode), _ptr(part, None, "part"), S, M, N, _ptr(y, _F32, "y"),
-                                  _stream(stream)), "lk_splitk_combine")
+                                  _cfg(cfg), _stream(stream)), "lk_splitk_combine")
+
+
+def lk_splitk_chunks_for(N, K, mode, M) -> int:
+    """The split-K chunk count the library favours for this shape (1: the
+    plain GEMV; see include/lk.h)."""
+    return _load().lk_splitk_chunks_for(N, K, _mode(mode), M)
 
 
 def lk_argmax_parts_max(N) -> int:

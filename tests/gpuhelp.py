@@ -163,14 +163,25 @@ def check_token(st, layers, final):
     TOL * sum|W x| per row (Dequant).  Bit-exact steps chained from the same
     first input make the GPU token the oracle's own token.  The argmax must be
     the oracle's first index of the maximum of the GPU's logits (and, for the
-    quantized modes, the logits are the oracle's bit for bit)."""
+    quantized modes, the logits are the oracle's bit for bit).  A projection
+    the stack runs as split-K (st.splitk) is the oracle's split-K value with
+    the same chunk count."""
     m = st.mode
     eps = st.eps
+
+    def chunks(what):
+        name = what.split()[-1]
+        name = "qkv" if name in ("q", "k", "v") else "gu" if name == "gate/up" else name
+        return st.splitk.get(name, 1)
 
     def step(wpair, x, gain, y_gpu, what):
         a = oracle.rmsnorm(x, host(gain), m, eps) if gain is not None else x
         wq, ws = wpair
-        y_or = oracle.gemv(wq, ws, m, **oracle_acts(a, m))
+        S = chunks(what)
+        if S > 1:
+            y_or = oracle.gemv_splitk(wq, ws, m, S, **oracle_acts(a, m))[0]
+        else:
+            y_or = oracle.gemv(wq, ws, m, **oracle_acts(a, m))
         try:
             assert_gemv_close(y_gpu, y_or, wq, ws, a, m)
         except AssertionError as e:

@@ -99,9 +99,11 @@ def test_splitk_and_combine_checks(lib):
     assert f(*args, 4, None, need, None, None) == -1
     assert f(*args, 4, P(FAKE), need, lk._cfg(lk.launch_cfg(pdl=3)), None) == -1
     c = lib.lk_splitk_combine
-    assert c(1, P(FAKE), 0, 1, 64, P(FAKE), None) == -3
-    assert c(0, P(FAKE + 4), 2, 1, 64, P(FAKE), None) == -2  # f64 partials
-    assert c(1, P(FAKE), 2, 0, 64, P(FAKE), None) == 0
+    assert c(1, P(FAKE), 0, 1, 64, P(FAKE), None, None) == -3
+    assert c(1, P(FAKE), 2, 65, 64, P(FAKE), None, None) == -3  # M <= LK_MAX_BATCH
+    assert c(0, P(FAKE + 4), 2, 1, 64, P(FAKE), None, None) == -2  # f64 partials
+    assert c(1, P(FAKE), 2, 0, 64, P(FAKE), None, None) == 0
+    assert c(1, P(FAKE), 2, 1, 64, P(FAKE), lk._cfg(lk.launch_cfg(pdl=5)), None) == -1
 
 
 def test_norm_quant_argmax_checks(lib):

@@ -11,7 +11,7 @@ from q8_quantized_gemv_gb300.decode import DecodeStack  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 SMALL = dict(layers=2, hidden=1024, q_dim=1024, kv_dim=256, ffn=1536, vocab=3000)
-KINDS = {1: "ring", 2: "chain", 3: "tensor-core", 4: "norm", 5: "quantize"}
+KINDS = {1: "ring", 2: "chain", 3: "tensor-core", 4: "norm", 5: "quantize", 6: "split-K combine"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -42,8 +42,13 @@ def test_timeline_records(batch):
     R = lk.LK_TRACE_REC
     used = [raw[i * R:(i + 1) * R] for i in range(n)]
     gemv = 1 if batch == 1 else 3
-    qkv = gemv  # one GEMV over the fused q|k|v matrix
-    want = [4, qkv, 5, gemv, 4, gemv, 5, gemv] * SMALL["layers"] + [4, gemv]
+    assert (batch == 1) == (not st.splitk)  # split-K: 2 or more rows
+
+    def g(name):  # one GEMV (over the fused q|k|v matrix for "qkv"), and its combine if split
+        return [gemv] + ([6] if name in st.splitk else [])
+
+    layer = [4] + g("qkv") + [5] + g("o") + [4] + g("gu") + [5] + g("down")
+    want = layer * SMALL["layers"] + [4, gemv]
     assert [r[5] for r in used] == want
     assert [r[6] for r in used if r[5] == 4] == [SMALL["hidden"]] * (2 * SMALL["layers"] + 1)
     for r in used:
