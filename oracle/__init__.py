@@ -3,15 +3,17 @@
 TEST INFRASTRUCTURE ONLY.  The tests, the package smoke check and the
 benchmark's CPU-baseline leg call it; the library (``q8_quantized_gemv_gb300``)
 never imports it, and it imports nothing from the library.  The arithmetic
-lives in ``oracle.c`` (plain C built with ``-ffp-contract=off``, one thread
-by default; its GEMV row loops can be spread over host threads without
-changing any bit); this module builds it and wraps it for numpy arrays.
+lives in ``oracle.c`` and, for the GGUF block formats other than Q8_0,
+``formats.c`` (plain C built with ``-ffp-contract=off``, one thread by
+default; its GEMV row loops can be spread over host threads without changing
+any bit); this module builds them and wraps them for numpy arrays.
 
 Sources, by page:
   * "kernels.rs" (logicaffeine_compile codegen_cuda lane kernel library):
     the numerics modes, the activation quantizer, the quantized block step and
     its four-partial order, RMSNorm and its reduction tree (with the residual
-    add), the gated projection pair (SwiGLU), the balanced split.
+    add), the gated projection pair (SwiGLU), the balanced split, and the
+    decoder library of block formats (lk_sub, lk_sub_dot, lk_row_dot).
   * the QWEN38_EXTRA_KERNELS constant: "SPLIT-K FOR THE NARROW PROJECTIONS",
     the fused add + norm + quantize kernels and the SwiGLU + requantize one.
   * model-as-a-kernel "megakernel.cu": the argmax's first index of equal maxima.
@@ -28,17 +30,18 @@ DEQUANT, INT8ACT, TWOPASS = 0, 1, 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "formats.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 
 def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so beside it (gcc, -O2 -ffp-contract=off)."""
-    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    stale = (not os.path.exists(_LIB)) or any(os.path.getmtime(_LIB) < os.path.getmtime(f) for f in _SRCS)
     if force or stale:
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.run(
-            ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+            ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-o", tmp] + _SRCS + ["-lm"],
             check=True,
         )
         os.replace(tmp, _LIB)
@@ -76,6 +79,12 @@ def _load():
     lib.oracle_get_threads.argtypes = []
     lib.oracle_get_threads.restype = i32
     lib.oracle_argmax.argtypes = [P, i64]
+    lib.oracle_format_row_bytes.argtypes = [i32, i32]
+    lib.oracle_format_row_bytes.restype = i64
+    lib.oracle_sub_decode.argtypes = [i32, P, i32, P, P, P]
+    lib.oracle_dequant_row.argtypes = [i32, P, i32, P]
+    lib.oracle_gemv_blk_rows.argtypes = [i32, P, i64, i32, i32, P, P, P, P, i64, i64, P]
+    lib.oracle_absdot_blk_rows.argtypes = [i32, P, i64, i32, P, i64, i64, P]
     lib.oracle_argmax.restype = i64
     _lib = lib
     return lib
@@ -279,3 +288,65 @@ def argmax(v) -> int:
     v = _c(v, np.float32).reshape(-1)
     assert v.size >= 1
     return int(_load().oracle_argmax(_p(v), v.size))
+
+
+# ---- the GGUF block formats other than Q8_0 (formats.c) --------------------------
+
+FORMATS = {"q4_0": 2, "q4_1": 3, "q5_0": 6, "q5_1": 7, "q2_k": 10, "q3_k": 11, "q4_k": 12, "q5_k": 13,
+           "q6_k": 14, "iq4_nl": 20, "iq4_xs": 23, "mxfp4": 39}
+
+
+def format_row_bytes(F: int, K: int) -> int:
+    """Bytes of a row of K values in format F (0: K not a whole number of blocks)."""
+    return int(_load().oracle_format_row_bytes(F, K))
+
+
+def sub_decode(F: int, row, sb: int):
+    """Sub-block sb of a row (uint8 bytes): (levels int8[32], d f32[2], c f32[2])."""
+    row = _c(row, np.uint8)
+    v = np.zeros(32, np.int8)
+    d = np.zeros(2, np.float32)
+    c = np.zeros(2, np.float32)
+    assert _load().oracle_sub_decode(F, _p(row), sb, _p(v), _p(d), _p(c)) == 0
+    return v, d, c
+
+
+def dequant(F: int, w, K: int) -> np.ndarray:
+    """w uint8 [N, row_bytes] -> the dequantized weights f32 [N, K]."""
+    w = _c(np.atleast_2d(w), np.uint8)
+    out = np.zeros((w.shape[0], K), np.float32)
+    for o in range(w.shape[0]):
+        assert _load().oracle_dequant_row(F, _p(w[o]), K, _p(out[o])) == 0
+    return out
+
+
+def gemv_blk(F: int, w, K: int, mode: int, x=None, hi=None, lo=None, s=None, rows=None) -> np.ndarray:
+    """Block-format GEMV rows [r0, r1) for every activation row: w uint8
+    [N, row_bytes]; activations as gemv.  Returns y [M, r1 - r0] f32."""
+    lib = _load()
+    w = _c(np.atleast_2d(w), np.uint8)
+    N, rb = w.shape
+    assert rb == format_row_bytes(F, K)
+    r0, r1 = _rows(rows, N)
+    acts = [_c(np.atleast_2d(a), dt) if a is not None else None
+            for a, dt in ((x, np.float32), (hi, np.int8), (lo, np.int8), (s, np.float32))]
+    M = next(a.shape[0] for a in acts if a is not None)
+    y = np.zeros((M, r1 - r0), np.float32)
+    for t in range(M):
+        xt, ht, lt, st = (None if a is None else a[t] for a in acts)
+        assert lib.oracle_gemv_blk_rows(F, _p(w), rb, K, mode, _p(xt), _p(ht), _p(lt), _p(st), r0, r1,
+                                        _p(y[t])) == 0
+    return y
+
+
+def absdot_blk(F: int, w, K: int, x, rows=None) -> np.ndarray:
+    """sum_k |w_k x_k| in f64 per row (w dequantized), [M, r1 - r0]."""
+    lib = _load()
+    w = _c(np.atleast_2d(w), np.uint8)
+    N, rb = w.shape
+    r0, r1 = _rows(rows, N)
+    x = _c(np.atleast_2d(x), np.float32)
+    out = np.zeros((x.shape[0], r1 - r0), np.float64)
+    for t in range(x.shape[0]):
+        assert lib.oracle_absdot_blk_rows(F, _p(w), rb, K, _p(x[t]), r0, r1, _p(out[t])) == 0
+    return out
