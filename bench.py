@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--K", type=int, default=4096)
     ap.add_argument("--S", type=int, default=1, help="split-K chunks (gemv workload)")
     ap.add_argument("--argmax", action="store_true", help="argmax epilogue + reduce (gemv workload)")
+    ap.add_argument("--format", default=None, choices=["q4_0", "q4_1", "q5_0", "q5_1", "iq4_nl", "mxfp4", "q2_k",
+                                                       "q3_k", "q4_k", "q5_k", "q6_k", "iq4_xs"],
+                    help="gemv workload: a GGUF block format other than Q8_0 (lk_gemv_blk)")
     ap.add_argument("--glu", action="store_true",
                     help="gemv workload: the gate/up pair (two N/2-row matrices) with the SwiGLU + quantize epilogue")
     ap.add_argument("--path", default="auto", choices=["auto", "direct", "ring", "mma"])
@@ -498,10 +501,13 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
     cfg = lk.launch_cfg(**dict(_tune(a), path=a.path, pdl=0 if a.no_pdl else 1))
     mode = lk.MODES[a.mode]
     N, K, B, S = a.N, a.K, a.batch, a.S
-    wbytes = N * K + N * K // 16
+    wbytes = N * lk.lk_format_row_bytes(a.format, K) if a.format else N * K + N * K // 16
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     R = max(2, -(-4 * l2 // wbytes))
-    mats = [synth.q8_matrix_torch(N, K, synth.SEED_BASE + 50 + r, dev) for r in range(R)]
+    if a.format:
+        mats = [(synth.blk_matrix_torch(a.format, N, K, synth.SEED_BASE + 50 + r, dev), None) for r in range(R)]
+    else:
+        mats = [synth.q8_matrix_torch(N, K, synth.SEED_BASE + 50 + r, dev) for r in range(R)]
     x = synth.activation_torch(B, K, synth.SEED_BASE + 49, dev, outliers=True)
     acts = {"x": x}
     if mode != lk.LK_DEQUANT:
@@ -532,6 +538,9 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
 
     def launch(r):
         wq, ws = mats[r % R]
+        if a.format:
+            lk.lk_gemv_blk(a.format, wq, K, mode, y, M=B, cfg=cfg, **acts)
+            return
         if a.glu:
             # the two halves of the copy as the gate and the up matrix
             lk.lk_gemv_q8_glu(wq[:F], ws[:F], wq[F:], ws[F:], mode, gu_buf, h=h_glu, cnt=cnt, M=B, cfg=cfg, **hact,
@@ -590,10 +599,11 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
     alg = wbytes + act_b + B * N * 4 + (2 * S * B * N * (8 if mode == lk.LK_DEQUANT else 4) if S > 1 else 0)
     peaks, src = measured_peaks()
     gbs = wbytes / (us * 1e-6) / 1e9
-    out = {"metric": "Q8_0 GEMV effective weight GB/s", "value": gbs, "unit": UNIT, "n_gpus": world,
+    out = {"metric": ("block-format" if a.format else "Q8_0") + " GEMV effective weight GB/s", "value": gbs, "unit": UNIT, "n_gpus": world,
            "steps": a.steps, "warmup": a.warmup, "ms_per_step": us * 1e-3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": _dtype(a.mode), "data": "synthetic",
-           "config": {"workload": f"Q8_0 GEMV N={N} K={K} batch {B} {a.mode} S={S}"
+           "config": {"workload": (f"{a.format.upper()} GEMV" if a.format else "Q8_0 GEMV")
+                                  + f" N={N} K={K} batch {B} {a.mode} S={S}"
                                   + (" gate/up pair + SwiGLU + quantize" if a.glu else "")
                                   + (" + argmax" if a.argmax else "") + (" fused norm+quant" if a.fused else "")
                                   + (" after a norm+quant launch" if a.norm and not a.fused else ""),
@@ -605,7 +615,8 @@ def run_gemv(a, rank, world, quiet=False, sample_clocks=True):
                         "peak_source": src, "algorithmic_bytes_per_launch": alg},
            "clocks": clk,
            "gpu_launches": a.steps * Rg * (1 + (1 if (S > 1 or a.argmax) else 0) + (1 if a.norm and not a.fused else 0)),
-           "kernel": {1: "direct", 2: "ring", 3: "mma", 0: "none"}[lk.lk_gemv_kernel_for(N, K, mode, B,
+           "kernel": "blk" if a.format else
+                     {1: "direct", 2: "ring", 3: "mma", 0: "none"}[lk.lk_gemv_kernel_for(N, K, mode, B,
                                                                                           S if S > 1 else 0,
                                                                                           cfg=cfg)]}
     del mats

@@ -475,6 +475,49 @@ lk_status lk_argmax(const float* logits, const uint64_t* parts, int n_parts, int
 lk_status lk_argmax_noalloc(const float* logits, int M, int N, int32_t* idx, cudaStream_t stream);
 
 /*
+ * The GGUF block formats other than Q8_0 ("kernels.rs" decoder library: lk_sub
+ * decodes a 32-value sub-block of any of them into int8 levels with a scale
+ * d and an offset c per half; lk_row_dot / lk_sub_dot run the projection).
+ * `format` is the ggml type number the pages use:
+ *   2 Q4_0, 3 Q4_1, 6 Q5_0, 7 Q5_1, 20 IQ4_NL, 39 MXFP4 (32 values a block),
+ *   10 Q2_K, 11 Q3_K, 12 Q4_K, 13 Q5_K, 14 Q6_K, 23 IQ4_XS (256 values a block),
+ * each block in the format's own byte layout (little-endian f16 scales).  A
+ * row of K values is lk_format_row_bytes(format, K) bytes (0: an unknown
+ * format or K not a whole number of blocks); a matrix is N such rows back
+ * to back, 16-byte aligned.
+ */
+size_t lk_format_row_bytes(int format, int K);
+
+/*
+ * y = W x for a block-format matrix w (N rows) and M <= LK_MAX_M activation
+ * rows, the activation as lk_gemv_q8's (x f32 under LK_DEQUANT; xq, xs and
+ * under LK_TWOPASS xl, from lk_quantize_act).  The weight of value i of a
+ * sub-block is RN(RN(d level_i) + c) in f32.  Quantized modes, bit-fixed
+ * ("kernels.rs" lk_row_dot with lk_sub_dot): sub-block sb of a row is in
+ * lane sb mod 32; with dh0/dh1 the exact int8 dots of the levels with the
+ * activation words over values 0..15 / 16..31 and sh0/sh1 the words' sums,
+ *   part = ((d0 dh0 + c0 sh0) + d1 dh1) + c1 sh1   (each op rounded to f32;
+ *          TwoPass: part + 2^-7 times the same with the low words),
+ * the lane's f32 sum gets s[sb] * part in ascending sb, and the lanes meet in
+ * the shuffle-down tree (lane l adds lane l + d, d = 16, 8, 4, 2, 1).
+ * Dequant: within 1e-5 of sum |w x| per row of the exact sum (the pages sum
+ * in f64; here each lane's products are summed in f32 with a compensation
+ * term, the lanes in f64).  K % 256 == 0 and a row a multiple of 16 bytes
+ * (LK_ERR_SHAPE otherwise; every format at K = 4096); K = 0 writes zeros.
+ * cfg: pdl, grid_ctas.  The library's extension of the Q8_0 path to the
+ * pages' other formats.
+ */
+lk_status lk_gemv_blk(int format, const uint8_t* w, int N, int K, lk_mode mode, const float* x, const int8_t* xq,
+                      const int8_t* xl, const float* xs, int M, float* y, const lk_launch_cfg* cfg,
+                      cudaStream_t stream);
+
+/*
+ * Test hook: the decoded weights out[o][k] = RN(RN(d level) + c) of a
+ * block-format matrix (f32 [N][K]), by the same decoders lk_gemv_blk uses.
+ */
+lk_status lk_dequant_blk(int format, const uint8_t* w, int N, int K, float* out, cudaStream_t stream);
+
+/*
  * Test hook: the exact int32 block dots of one activation row, computed by the
  * same lane arrangement the GEMV uses ("kernels.rs" lk_q8_block_dot).
  *   d[o][b] = sum_k wq[o][32b+k] * xq[32b+k];  e likewise with xl (if both xl

@@ -1,0 +1,550 @@
+// GEMV on the GGUF block formats other than Q8_0 ("kernels.rs" decoder
+// library: lk_sub, lk_sub_dot, lk_row_dot), sm_103a.
+//
+// Every format is read as 32-value sub-blocks: 32 int8 levels and, per half
+// (values 0..15, 16..31), a scale d and an offset c, the weight being
+// RN(RN(d level) + c).  The quantized modes' row value is fixed by the pages'
+// arrangement, so this kernel keeps it: sub-block sb of a row belongs to lane
+// sb mod 32, a lane adds s[sb] * part in ascending sb (f32 product, f32 sum)
+// with part = ((d0 dh0 + c0 sh0) + d1 dh1) + c1 sh1 -- dh the exact int8
+// dots of the levels with the activation words over each half, sh the
+// words' sums (TwoPass adds 2^-7 times the low words' part) -- and the lanes
+// meet in the shuffle-down tree (lane l adds lane l + d, d = 16 .. 1).
+// Dequant (f32 activations) is held to the tolerance instead: each lane
+// sums its sub-blocks' products in f32 with a compensation term and the
+// lanes' totals are added in f64.
+//
+// Data movement: a warp owns whole rows.  Its next row's bytes are copied
+// into one of the warp's two shared-memory buffers by 16-byte asynchronous
+// copies (cp.async) while it computes the current one; the lanes then decode
+// their sub-blocks from shared memory.  The activation rows are copied into
+// shared memory once per block, 16 bytes of padding after every 32 values so
+// that 32 lanes reading 32 consecutive sub-blocks hit every bank once.  The
+// levels are built directly as packed int8 x 4 words (per-byte subtraction
+// and bit spreading), so the dots are dp4a.
+#include <cuda_fp16.h>
+
+#include "lk_device.cuh"
+#include "lk_host.h"
+
+namespace lkblk {
+
+using namespace lk;
+
+constexpr int BW = 8;  // warps per block at most
+
+// Values of one block and bytes of one block, by format number (0: unknown).
+__host__ __device__ constexpr int blk_values(int F) {
+  return (F == 10 || F == 11 || F == 12 || F == 13 || F == 14 || F == 23) ? 256
+         : (F == 2 || F == 3 || F == 6 || F == 7 || F == 20 || F == 39) ? 32 : 0;
+}
+__host__ __device__ constexpr int blk_bytes(int F) {
+  return F == 2 ? 18 : F == 3 ? 20 : F == 6 ? 22 : F == 7 ? 24 : F == 20 ? 18 : F == 39 ? 17
+       : F == 10 ? 84 : F == 11 ? 110 : F == 12 ? 144 : F == 13 ? 176 : F == 14 ? 210 : F == 23 ? 136 : 0;
+}
+
+// Shared-memory byte helpers (the staged row: 16-byte aligned, arbitrary
+// byte offsets inside it).
+__device__ __forceinline__ unsigned u8(const unsigned char* p) { return *p; }
+__device__ __forceinline__ float half_at(const unsigned char* p) {
+  return __half2float(__ushort_as_half((unsigned short)(p[0] | (p[1] << 8))));
+}
+// Four bytes from any offset: the two aligned words around them.
+__device__ __forceinline__ unsigned w32(const unsigned char* p) {
+  const uintptr_t a = (uintptr_t)p;
+  const unsigned* q = (const unsigned*)(a & ~(uintptr_t)3);
+  const unsigned sh = 8u * (unsigned)(a & 3);
+  return sh ? __funnelshift_r(q[0], q[1], sh) : q[0];
+}
+// Bits 0..3 of b spread to bit 0 of bytes 0..3.
+__device__ __forceinline__ unsigned spread4(unsigned b) { return ((b & 15u) * 0x00204081u) & 0x01010101u; }
+
+// 16-entry int8 level table (shared memory) applied to the low and the high
+// nibbles of a word: bytes of `lo` = table[low nibbles], `hi` = table[high].
+__device__ __forceinline__ void table_word(const signed char* tab, unsigned q, unsigned& lo, unsigned& hi) {
+  lo = 0u;
+  hi = 0u;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const unsigned b = (q >> (8 * k)) & 0xFFu;
+    lo |= (unsigned)(unsigned char)tab[b & 15u] << (8 * k);
+    hi |= (unsigned)(unsigned char)tab[b >> 4] << (8 * k);
+  }
+}
+
+// Sub-block sb of a staged row in format F: w[0..7] the 32 levels four to a
+// word (value 4i + k in byte k of w[i]), d/c per half.
+template <int F>
+__device__ __forceinline__ void decode(const unsigned char* row, int sb, const signed char* tab, unsigned (&w)[8],
+                                       float (&d)[2], float (&c)[2]) {
+  c[0] = c[1] = 0.f;
+  if constexpr (F == 2 || F == 3 || F == 20) {
+    const unsigned char* b = row + sb * blk_bytes(F);
+    const unsigned char* qs = b + (F == 3 ? 4 : 2);
+    d[0] = d[1] = half_at(b);
+    if (F == 3) c[0] = c[1] = half_at(b + 2);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const unsigned q = w32(qs + 4 * i);
+      if constexpr (F == 20) {
+        table_word(tab, q, w[i], w[4 + i]);
+      } else {
+        w[i] = q & 0x0F0F0F0Fu;
+        w[4 + i] = (q >> 4) & 0x0F0F0F0Fu;
+        if (F == 2) {
+          w[i] = __vsub4(w[i], 0x08080808u);
+          w[4 + i] = __vsub4(w[4 + i], 0x08080808u);
+        }
+      }
+    }
+  } else if constexpr (F == 6 || F == 7) {
+    const unsigned char* b = row + sb * blk_bytes(F);
+    const unsigned char* hb = b + (F == 7 ? 4 : 2);
+    const unsigned qh = w32(hb);
+    d[0] = d[1] = half_at(b);
+    if (F == 7) c[0] = c[1] = half_at(b + 2);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const unsigned q = w32(hb + 4 + 4 * i);
+      w[i] = (q & 0x0F0F0F0Fu) | (spread4(qh >> (4 * i)) << 4);
+      w[4 + i] = ((q >> 4) & 0x0F0F0F0Fu) | (spread4(qh >> (16 + 4 * i)) << 4);
+      if (F == 6) {
+        w[i] = __vsub4(w[i], 0x10101010u);
+        w[4 + i] = __vsub4(w[4 + i], 0x10101010u);
+      }
+    }
+  } else if constexpr (F == 39) {
+    const unsigned char* b = row + sb * 17;
+    const unsigned e = u8(b);
+    // E8M0 exponent e is 2^(e - 127); halved for the doubled E2M1 values:
+    // 2^(e - 128), subnormal below e = 2
+    d[0] = d[1] = __uint_as_float(e < 2u ? (0x00200000u << e) : ((e - 1u) << 23));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) table_word(tab, w32(b + 1 + 4 * i), w[i], w[4 + i]);
+  } else if constexpr (F == 12 || F == 13) {
+    const unsigned char* sup = row + (sb >> 3) * blk_bytes(F);
+    const int j = sb & 7;
+    const unsigned char* sm = sup + 4;
+    int sc, m;
+    if (j < 4) {
+      sc = sm[j] & 63;
+      m = sm[j + 4] & 63;
+    } else {
+      sc = (sm[j + 4] & 15) | ((sm[j - 4] >> 6) << 4);
+      m = (sm[j + 4] >> 4) | ((sm[j] >> 6) << 4);
+    }
+    d[0] = d[1] = __fmul_rn(half_at(sup), (float)sc);
+    c[0] = c[1] = -__fmul_rn(half_at(sup + 2), (float)m);
+    const unsigned char* ql = sup + (F == 12 ? 16 : 48) + (j >> 1) * 32;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const unsigned q = w32(ql + 4 * i);
+      w[i] = (j & 1) ? ((q >> 4) & 0x0F0F0F0Fu) : (q & 0x0F0F0F0Fu);
+      if (F == 13) w[i] |= ((w32(sup + 16 + 4 * i) >> j) & 0x01010101u) << 4;
+    }
+  } else if constexpr (F == 10) {
+    const unsigned char* sup = row + (sb >> 3) * 84;
+    const int j = sb & 7, half = j >> 2, k = j & 3;
+    const unsigned char* q = sup + 16 + half * 32;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = (w32(q + 4 * i) >> (2 * k)) & 0x03030303u;
+    const float D = half_at(sup + 80), DM = half_at(sup + 82);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int s = sup[half * 8 + k * 2 + h];
+      d[h] = __fmul_rn(D, (float)(s & 15));
+      c[h] = -__fmul_rn(DM, (float)(s >> 4));
+    }
+  } else if constexpr (F == 11) {
+    const unsigned char* sup = row + (sb >> 3) * 110;
+    const int j = sb & 7, half = j >> 2, k = j & 3, bit = half * 4 + k;
+    const unsigned char* q = sup + 32 + half * 32;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const unsigned low2 = (w32(q + 4 * i) >> (2 * k)) & 0x03030303u;
+      const unsigned mb = (w32(sup + 4 * i) >> bit) & 0x01010101u;  // set: +0, clear: -4
+      w[i] = __vsub4(low2 | (mb << 2), 0x04040404u);
+    }
+    const unsigned char* s12 = sup + 96;
+    const float D = half_at(sup + 108);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = half * 8 + k * 2 + h;
+      const int lo4 = i < 8 ? (s12[i] & 15) : (s12[i - 8] >> 4);
+      const int hi2 = (s12[8 + (i & 3)] >> (2 * (i >> 2))) & 3;
+      d[h] = __fmul_rn(D, (float)((lo4 | (hi2 << 4)) - 32));
+    }
+  } else if constexpr (F == 14) {
+    const unsigned char* sup = row + (sb >> 3) * 210;
+    const int j = sb & 7, half = j >> 2, k = j & 3;
+    const unsigned char* ql = sup + half * 64 + (k & 1) * 32;
+    const unsigned char* qh = sup + 128 + half * 32;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const unsigned lo = (w32(ql + 4 * i) >> (4 * (k >> 1))) & 0x0F0F0F0Fu;
+      const unsigned hi = (w32(qh + 4 * i) >> (2 * k)) & 0x03030303u;
+      w[i] = __vsub4(lo | (hi << 4), 0x20202020u);
+    }
+    const float D = half_at(sup + 208);
+    d[0] = __fmul_rn(D, (float)(signed char)sup[192 + half * 8 + 2 * k]);
+    d[1] = __fmul_rn(D, (float)(signed char)sup[192 + half * 8 + 2 * k + 1]);
+  } else if constexpr (F == 23) {
+    const unsigned char* sup = row + (sb >> 3) * 136;
+    const int j = sb & 7;
+    const int sh = sup[2] | (sup[3] << 8);
+    const int ls = ((sup[4 + (j >> 1)] >> (4 * (j & 1))) & 15) | (((sh >> (2 * j)) & 3) << 4);
+    d[0] = d[1] = __fmul_rn(half_at(sup), (float)(ls - 32));
+    const unsigned char* qs = sup + 8 + 16 * j;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) table_word(tab, w32(qs + 4 * i), w[i], w[4 + i]);
+  }
+}
+
+// The level table a format looks up (IQ4 levels, doubled E2M1 values).
+__device__ __forceinline__ void load_table(int F, signed char* tab) {
+  // IQ4_NL / IQ4_XS: sixteen non-linear levels; MXFP4: E2M1 values x 2
+  const signed char iq4[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
+  const signed char mx[16] = {0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12};
+  if (threadIdx.x < 16) tab[threadIdx.x] = F == 39 ? mx[threadIdx.x] : iq4[threadIdx.x];
+}
+
+// f32 part of one sub-block for one activation row: ((d0 dh0 + c0 sh0) +
+// d1 dh1) + c1 sh1, each product and sum rounded.
+__device__ __forceinline__ float sub_part(const unsigned (&w)[8], const float (&d)[2], const float (&c)[2],
+                                          const unsigned (&h)[8]) {
+  int dh0 = 0, dh1 = 0, sh0 = 0, sh1 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    dh0 = __dp4a((int)w[i], (int)h[i], dh0);
+    sh0 = __dp4a(0x01010101, (int)h[i], sh0);
+    dh1 = __dp4a((int)w[4 + i], (int)h[4 + i], dh1);
+    sh1 = __dp4a(0x01010101, (int)h[4 + i], sh1);
+  }
+  float p = __fmul_rn(d[0], (float)dh0);
+  p = __fadd_rn(p, __fmul_rn(c[0], (float)sh0));
+  p = __fadd_rn(p, __fmul_rn(d[1], (float)dh1));
+  return __fadd_rn(p, __fmul_rn(c[1], (float)sh1));
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+struct BlkArgs {
+  const unsigned char* w;  // N rows of rb bytes (16-byte aligned, rb % 16 == 0)
+  long rb;
+  int N, K, M, mode;
+  const float* x;          // Dequant [M][K]
+  const int8_t* xq;        // [M][K]
+  const int8_t* xl;        // [M][K] (TwoPass)
+  const float* xs;         // [M][K/32]
+  float* y;                // [M][N]
+  float* dq;               // dequant hook: [N][K] (or NULL)
+  int pdl;
+  unsigned act_stride;     // bytes per activation row in shared memory
+  unsigned act_bytes;      // the activation area
+  unsigned rb_pad;         // one row buffer (rb rounded up to 16, plus 16)
+};
+
+// Padded shared-memory index of value k of an activation row: 16 bytes of
+// padding after every 32 values (of `bytes` bytes each).
+__device__ __forceinline__ unsigned pad_index(unsigned k, unsigned bytes) {
+  return (k >> 5) * (32u * bytes + 16u) + (k & 31u) * bytes;
+}
+
+// The activation rows into shared memory (all threads; after the dependency
+// wait): words (and low words) with the padding, scales dense; or f32 values.
+template <int Q, int MM>
+__device__ __forceinline__ void stage_act(const BlkArgs& a, unsigned char* act) {
+  const int K = a.K;
+  if constexpr (Q == 0) {
+    for (int t = 0; t < a.M; ++t)
+      for (int i = threadIdx.x; i < K / 4; i += blockDim.x) {
+        const float4 v = __ldcg((const float4*)(a.x + (long)t * K) + i);
+        *(float4*)(act + (size_t)t * a.act_stride + pad_index(4u * i, 4u)) = v;
+      }
+  } else {
+    const unsigned nb = (unsigned)K / 32u;
+    for (int t = 0; t < a.M; ++t) {
+      unsigned char* base = act + (size_t)t * a.act_stride;
+      for (int i = threadIdx.x; i < K / 16; i += blockDim.x) {
+        *(uint4*)(base + pad_index(16u * i, 1u)) = __ldcg((const uint4*)(a.xq + (long)t * K) + i);
+        if (Q == 2)
+          *(uint4*)(base + pad_index(16u * i, 1u) + nb * 48u) = __ldcg((const uint4*)(a.xl + (long)t * K) + i);
+      }
+      float* s = (float*)(base + nb * 48u * (Q == 2 ? 2u : 1u));
+      for (int i = threadIdx.x; i < (int)nb; i += blockDim.x) s[i] = __ldcg(a.xs + (long)t * nb + i);
+    }
+  }
+}
+
+template <int F, int Q, int MM>
+__global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ signed char tab[16];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned char* act = smem;
+  unsigned char* bufs = smem + a.act_bytes + (size_t)warp * 2 * a.rb_pad;
+  const int K = a.K, nb = K >> 5;
+  const long stride = (long)gridDim.x * nw;
+  long row = (long)blockIdx.x * nw + warp;
+  load_table(F, tab);
+  if (a.pdl && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" :::);
+  // the first row's bytes (weights: no dependence on the previous kernel)
+  auto fetch = [&](long r, unsigned char* dst) {
+    if (r < a.N) {
+      const unsigned char* src = a.w + r * a.rb;
+      for (long o = 16 * lane; o < a.rb; o += 512) cp_async16(dst + o, src + o);
+    }
+    cp_commit();
+  };
+  fetch(row, bufs);
+  if (a.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (a.dq == nullptr) stage_act<Q, MM>(a, act);
+  __syncthreads();
+  int cur = 0;
+  for (; row < a.N; row += stride) {
+    fetch(row + stride, bufs + (cur ^ 1) * a.rb_pad);
+    cp_wait<1>();
+    __syncwarp();
+    const unsigned char* rbuf = bufs + cur * a.rb_pad;
+    if (a.dq) {
+      // the decode hook: every value as the CPU dequantizer rounds it
+      for (int sb = lane; sb < nb; sb += 32) {
+        unsigned w[8];
+        float d[2], c[2];
+        decode<F>(rbuf, sb, tab, w, d, c);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float v = (float)(signed char)(w[i >> 2] >> (8 * (i & 3)));
+          a.dq[row * (long)K + 32 * sb + i] = __fadd_rn(__fmul_rn(d[i >> 4], v), c[i >> 4]);
+        }
+      }
+    } else if constexpr (Q == 0) {
+      float s1[MM], s2[MM];  // a lane's sum and its compensation, per activation row
+#pragma unroll
+      for (int t = 0; t < MM; ++t) s1[t] = s2[t] = 0.f;
+      for (int sb = lane; sb < nb; sb += 32) {
+        unsigned w[8];
+        float d[2], c[2];
+        decode<F>(rbuf, sb, tab, w, d, c);
+        float wv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          wv[i] = __fadd_rn(__fmul_rn(d[i >> 4], (float)(signed char)(w[i >> 2] >> (8 * (i & 3)))), c[i >> 4]);
+#pragma unroll
+        for (int t = 0; t < MM; ++t) {
+          if (t >= a.M) break;
+          const float* xr = (const float*)(act + (size_t)t * a.act_stride + pad_index(32u * sb, 4u));
+          float acc = 0.f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 xv = *(const float4*)(xr + 4 * q);
+            acc = __fmaf_rn(wv[4 * q], xv.x, acc);
+            acc = __fmaf_rn(wv[4 * q + 1], xv.y, acc);
+            acc = __fmaf_rn(wv[4 * q + 2], xv.z, acc);
+            acc = __fmaf_rn(wv[4 * q + 3], xv.w, acc);
+          }
+          // s1 + s2 += acc (Kahan-Babuska: the rounding error kept in s2)
+          const float sum = __fadd_rn(s1[t], acc);
+          const float bp = __fsub_rn(sum, s1[t]);
+          s2[t] = __fadd_rn(s2[t], __fadd_rn(__fsub_rn(s1[t], __fsub_rn(sum, bp)), __fsub_rn(acc, bp)));
+          s1[t] = sum;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < MM; ++t) {
+        if (t >= a.M) break;
+        double v = (double)s1[t] + (double)s2[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+        if (lane == 0) a.y[(long)t * a.N + row] = (float)v;
+      }
+    } else {
+      float acc[MM];
+#pragma unroll
+      for (int t = 0; t < MM; ++t) acc[t] = 0.f;
+      const unsigned nbu = (unsigned)nb;
+      for (int sb = lane; sb < nb; sb += 32) {
+        unsigned w[8];
+        float d[2], c[2];
+        decode<F>(rbuf, sb, tab, w, d, c);
+#pragma unroll
+        for (int t = 0; t < MM; ++t) {
+          if (t >= a.M) break;
+          const unsigned char* base = act + (size_t)t * a.act_stride;
+          const unsigned char* hp = base + pad_index(32u * sb, 1u);
+          unsigned h[8];
+          *(uint4*)&h[0] = *(const uint4*)hp;
+          *(uint4*)&h[4] = *(const uint4*)(hp + 16);
+          float part = sub_part(w, d, c, h);
+          if constexpr (Q == 2) {
+            const unsigned char* lp = hp + nbu * 48u;
+            unsigned l[8];
+            *(uint4*)&l[0] = *(const uint4*)lp;
+            *(uint4*)&l[4] = *(const uint4*)(lp + 16);
+            part = __fadd_rn(part, __fmul_rn(0.0078125f, sub_part(w, d, c, l)));
+          }
+          const float s = ((const float*)(base + nbu * 48u * (Q == 2 ? 2u : 1u)))[sb];
+          acc[t] = __fadd_rn(acc[t], __fmul_rn(s, part));
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < MM; ++t) {
+        if (t >= a.M) break;
+        float v = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, o));
+        if (lane == 0) a.y[(long)t * a.N + row] = v;
+      }
+    }
+    __syncwarp();
+    cur ^= 1;
+  }
+  cp_wait<0>();
+}
+
+typedef void (*blk_fn)(const BlkArgs);
+
+template <int F>
+blk_fn pick_q(int mode, int M) {
+  if (mode == 0) return M <= 1 ? gemv_blk_kernel<F, 0, 1> : M <= 4 ? gemv_blk_kernel<F, 0, 4> : gemv_blk_kernel<F, 0, 8>;
+  if (mode == 1) return M <= 1 ? gemv_blk_kernel<F, 1, 1> : M <= 4 ? gemv_blk_kernel<F, 1, 4> : gemv_blk_kernel<F, 1, 8>;
+  return M <= 1 ? gemv_blk_kernel<F, 2, 1> : M <= 4 ? gemv_blk_kernel<F, 2, 4> : gemv_blk_kernel<F, 2, 8>;
+}
+
+blk_fn pick(int F, int mode, int M) {
+  switch (F) {
+    case 2: return pick_q<2>(mode, M);
+    case 3: return pick_q<3>(mode, M);
+    case 6: return pick_q<6>(mode, M);
+    case 7: return pick_q<7>(mode, M);
+    case 10: return pick_q<10>(mode, M);
+    case 11: return pick_q<11>(mode, M);
+    case 12: return pick_q<12>(mode, M);
+    case 13: return pick_q<13>(mode, M);
+    case 14: return pick_q<14>(mode, M);
+    case 20: return pick_q<20>(mode, M);
+    case 23: return pick_q<23>(mode, M);
+    case 39: return pick_q<39>(mode, M);
+    default: return nullptr;
+  }
+}
+
+// Row bytes of format F at K values (0: unknown format or not whole blocks).
+long row_bytes(int F, int K) {
+  const int v = blk_values(F);
+  if (!v || K <= 0 || K % v) return 0;
+  return (long)(K / v) * blk_bytes(F);
+}
+
+lk_status launch(int F, const unsigned char* w, int N, int K, int mode, const float* x, const int8_t* xq,
+                 const int8_t* xl, const float* xs, int M, float* y, float* dq, const lk_launch_cfg* cfg,
+                 cudaStream_t stream) {
+  const lkh::DeviceInfo* dev = lkh::device_info(nullptr);
+  if (!dev) return LK_ERR_CUDA;
+  BlkArgs a;
+  a.w = w;
+  a.rb = row_bytes(F, K);
+  a.N = N;
+  a.K = K;
+  a.M = M;
+  a.mode = mode;
+  a.x = x;
+  a.xq = xq;
+  a.xl = xl;
+  a.xs = xs;
+  a.y = y;
+  a.dq = dq;
+  a.pdl = lkh::cfg_pdl(cfg);
+  const unsigned nb = (unsigned)K / 32u;
+  a.act_stride = dq ? 0u
+                    : mode == 0 ? nb * (32u * 4u + 16u)
+                                : ((nb * 48u * (mode == 2 ? 2u : 1u) + nb * 4u + 15u) & ~15u);
+  a.act_bytes = a.act_stride * (unsigned)(dq ? 0 : M);
+  // 16 bytes of slack after a row: a word read at the row's last bytes may
+  // load the aligned word after them
+  a.rb_pad = (unsigned)((a.rb + 15) & ~15L) + 16u;
+  // (less a margin for the kernel's static level table)
+  long room = (long)dev->smem_optin - 256L - (long)a.act_bytes;
+  int nw = room > 0 ? (int)(room / (2L * a.rb_pad)) : 0;
+  if (nw > BW) nw = BW;
+  if (nw < 1) return LK_ERR_SHAPE;
+  const unsigned total = a.act_bytes + (unsigned)nw * 2u * a.rb_pad;
+  blk_fn f = pick(F, dq ? 1 : mode, dq ? 1 : M);
+  if (!f) return LK_ERR_ARG;
+  // the dynamic cap: the device's opt-in maximum less the kernel's static
+  // shared memory (the two together may not exceed it)
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, f) != cudaSuccess) return LK_ERR_CUDA;
+  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           dev->smem_optin - (int)fa.sharedSizeBytes) != cudaSuccess)
+    return LK_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, nw * 32, total) != cudaSuccess || per_sm < 1)
+    return LK_ERR_SHAPE;
+  long blocks = ((long)N + nw - 1) / nw;
+  const long cap = (long)dev->sm_count * per_sm;
+  if (cfg && cfg->grid_ctas > 0) blocks = cfg->grid_ctas < blocks ? cfg->grid_ctas : blocks;
+  else if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)blocks);
+  lc.blockDim = dim3(nw * 32);
+  lc.dynamicSmemBytes = total;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = a.pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&lc, f, a) != cudaSuccess) return LK_ERR_CUDA;
+  return lkh::launch_status();
+}
+
+}  // namespace lkblk
+
+using lkh::aligned;
+
+extern "C" {
+
+size_t lk_format_row_bytes(int format, int K) { return (size_t)lkblk::row_bytes(format, K); }
+
+lk_status lk_gemv_blk(int format, const uint8_t* w, int N, int K, lk_mode mode, const float* x, const int8_t* xq,
+                      const int8_t* xl, const float* xs, int M, float* y, const lk_launch_cfg* cfg,
+                      cudaStream_t stream) {
+  if (mode < LK_DEQUANT || mode > LK_TWOPASS || lkh::check_launch_cfg(cfg)) return LK_ERR_ARG;
+  if (lkblk::blk_values(format) == 0) return LK_ERR_ARG;
+  const long rb = lkblk::row_bytes(format, K);
+  if (N < 0 || M < 0 || M > LK_MAX_M || K < 0 || (K > 0 && (rb == 0 || K % 256 || rb % 16))) return LK_ERR_SHAPE;
+  if (N == 0 || M == 0 || K == 0) {
+    if (K == 0 && N > 0 && M > 0 && y) cudaMemsetAsync(y, 0, sizeof(float) * (size_t)M * (size_t)N, stream);
+    return K == 0 && N > 0 && M > 0 && !y ? LK_ERR_ARG : LK_OK;
+  }
+  if (!w || !y) return LK_ERR_ARG;
+  if (mode == LK_DEQUANT ? !x : (!xq || !xs || (mode == LK_TWOPASS && !xl))) return LK_ERR_ARG;
+  if (!aligned(w, 16) || !aligned(y, 4)) return LK_ERR_ALIGN;
+  if (mode == LK_DEQUANT ? !aligned(x, 16)
+                         : (!aligned(xq, 16) || !aligned(xs, 4) || (mode == LK_TWOPASS && !aligned(xl, 16))))
+    return LK_ERR_ALIGN;
+  return lkblk::launch(format, w, N, K, mode, x, xq, xl, xs, M, y, nullptr, cfg, stream);
+}
+
+lk_status lk_dequant_blk(int format, const uint8_t* w, int N, int K, float* out, cudaStream_t stream) {
+  if (lkblk::blk_values(format) == 0) return LK_ERR_ARG;
+  const long rb = lkblk::row_bytes(format, K);
+  if (N < 0 || K < 0 || (K > 0 && (rb == 0 || K % 256 || rb % 16))) return LK_ERR_SHAPE;
+  if (N == 0 || K == 0) return LK_OK;
+  if (!w || !out) return LK_ERR_ARG;
+  if (!aligned(w, 16) || !aligned(out, 4)) return LK_ERR_ALIGN;
+  return lkblk::launch(format, w, N, K, LK_INT8ACT, nullptr, nullptr, nullptr, nullptr, 1, nullptr, out, nullptr,
+                       stream);
+}
+
+}  // extern "C"

@@ -97,6 +97,9 @@ def _load():
         "lk_gemv_q8_splitk": ([P, P, I, I, I, P, P, P, P, I, I, P, S, P, P], I),
         "lk_splitk_combine": ([I, P, I, I, I, P, P, P], I),
         "lk_splitk_chunks_for": ([I, I, I, I], I),
+        "lk_format_row_bytes": ([I, I], S),
+        "lk_gemv_blk": ([I, P, I, I, I, P, P, P, P, I, P, P, P], I),
+        "lk_dequant_blk": ([I, P, I, I, P, P], I),
         "lk_argmax_parts_max": ([I], I),
         "lk_argmax_scratch_entries": ([I], I),
         "lk_argmax": ([P, P, I, I, I, P, P, P], I),
@@ -131,7 +134,7 @@ def exported_symbols():
             "lk_set_option", "lk_get_option", "lk_device_error", "lk_selftest_wait_timeout", "lk_gemv_kernel_for",
             "lk_rmsnorm_quant_gemv_q8", "lk_chain_sync_bytes", "lk_gemv_chain", "lk_trace_read",
             "lk_argmax_noalloc", "lk_gemv_q8_group", "lk_add_rmsnorm_quant", "lk_swiglu_quant",
-            "lk_gemv_q8_glu", "lk_splitk_chunks_for"]
+            "lk_gemv_q8_glu", "lk_splitk_chunks_for", "lk_format_row_bytes", "lk_gemv_blk", "lk_dequant_blk"]
 
 
 def _ok(st, where):
@@ -414,3 +417,35 @@ def lk_argmax_noalloc(logits, idx, stream=None):
     M, N = logits.shape
     _ok(_load().lk_argmax_noalloc(_ptr(logits, _F32, "logits"), M, N, _ptr(idx, torch.int32, "idx"),
                                   _stream(stream)), "lk_argmax_noalloc")
+
+
+# ---- the GGUF block formats other than Q8_0 ------------------------------------------
+
+FORMATS = {"q4_0": 2, "q4_1": 3, "q5_0": 6, "q5_1": 7, "q2_k": 10, "q3_k": 11, "q4_k": 12, "q5_k": 13,
+           "q6_k": 14, "iq4_nl": 20, "iq4_xs": 23, "mxfp4": 39}
+
+
+def _fmt(fmt):
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def lk_format_row_bytes(fmt, K) -> int:
+    return int(_load().lk_format_row_bytes(_fmt(fmt), K))
+
+
+def lk_gemv_blk(fmt, w, K, mode, y, x=None, xq=None, xl=None, xs=None, M=None, stream=None, cfg=None):
+    """y[M, N] = W x for a block-format matrix w (uint8 [N, row_bytes])."""
+    N = w.shape[0]
+    if M is None:
+        M = (x if x is not None else xq).shape[0]
+    if w.shape[1] != lk_format_row_bytes(fmt, K):
+        raise ValueError("w rows must be lk_format_row_bytes(fmt, K) bytes")
+    _ok(_load().lk_gemv_blk(_fmt(fmt), _ptr(w, torch.uint8, "w"), N, K, _mode(mode), _ptr(x, _F32, "x"),
+                            _ptr(xq, _I8, "xq"), _ptr(xl, _I8, "xl"), _ptr(xs, _F32, "xs"), M, _ptr(y, _F32, "y"),
+                            _cfg(cfg), _stream(stream)), "lk_gemv_blk")
+
+
+def lk_dequant_blk(fmt, w, K, out, stream=None):
+    """The decoded weights f32 [N, K] of a block-format matrix (test hook)."""
+    _ok(_load().lk_dequant_blk(_fmt(fmt), _ptr(w, torch.uint8, "w"), w.shape[0], K, _ptr(out, _F32, "out"),
+                               _stream(stream)), "lk_dequant_blk")
