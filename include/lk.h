@@ -86,8 +86,9 @@ typedef int lk_status;
  *              (0: one per SM; a launch that writes argmax keys takes at most
  *              lk_argmax_parts_max(N), else LK_ERR_ARG)
  *   ring_tk    ring kernel: bytes of K per stage for rows longer than that, a
- *              multiple of 1024 up to 8192 (0: whole rows up to 8192, else
- *              4096)
+ *              multiple of 1024 up to 8192 (0: whole rows up to 8192, two
+ *              equal slices up to 16384 where a half is a multiple of 1024,
+ *              else 4096)
  *   mma_min_m  fewest activation rows that take the tensor-core kernel under
  *              path 0 (0: 2; LK_MAX_BATCH + 1: never)
  *   mma_tk     tensor-core kernel: bytes of K per ring stage (0 auto, else a

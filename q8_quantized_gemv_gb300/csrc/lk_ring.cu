@@ -106,8 +106,13 @@ Layout layout(const lkh::GemvProblem& p, int smem_optin, int /*sm_count*/) {
   const int S = p.split ? (p.S > 1 ? p.S : 1) : 1;
   L.act_len = 32u * (unsigned)max_chunk_blocks(nb, S);
   // whole quads (one copy of the levels, one per row of scales) up to TKMAX;
-  // longer rows in 4 KB slices
-  L.tk = p.K <= TKMAX ? (unsigned)p.K : 4096u;
+  // rows up to twice that in two equal slices (a multiple of 1 KB), longer
+  // ones in 4 KB slices.  Measured (sequence, down 4096 x 12288, batch 1):
+  // 4 KB slices 1790 us per token, 6 KB 1747, 2 KB 1770, 3 KB 1936, 8 KB
+  // 1844: with 6.7 quads a block, two slices a quad take one round trip
+  // fewer per busy warp than three.
+  const bool halves = p.K > TKMAX && p.K <= 2 * TKMAX && (p.K / 2) % 1024 == 0;
+  L.tk = p.K <= TKMAX ? (unsigned)p.K : halves ? (unsigned)(p.K / 2) : 4096u;
   if (p.cfg.ring_tk > 0 && p.cfg.ring_tk < p.K) L.tk = (unsigned)p.cfg.ring_tk;
   L.srow = L.tk / 16u + 16u;  // as make_geom (padded rows)
   L.s_off = QR * L.tk;
