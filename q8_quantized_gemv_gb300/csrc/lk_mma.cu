@@ -439,16 +439,38 @@ __global__ void __launch_bounds__(MW * 32, 1) gemv_mma_kernel(const MmaArgs ra) 
                            __half2float(__ushort_as_half((unsigned short)(sw8.y >> 16)))};
       const float xa[4] = {sx0.x, sx0.y, sx0.z, sx0.w};
       const float xb[4] = {sx1.x, sx1.y, sx1.z, sx1.w};
+      // int8 path: the group's four blocks' MMAs first, back to back, so
+      // their latencies overlap; the combines below then read them in order
+      int di[4][4], fi[4][4];
+      if constexpr (I8) {
+        const uint2 z = make_uint2(0u, 0u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int bb = 4 * gi + q;
+          const uint2 rw0 = *(const uint2*)(W0 + 32 * bb), rw8 = *(const uint2*)(W8 + 32 * bb);
+          const uint2 xh = gx_ok ? *(const uint2*)(XH + k0 + 32 * bb) : z;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) di[q][e] = fi[q][e] = 0;
+          imma16832(di[q], rw0.x, rw8.x, rw0.y, rw8.y, xh.x, xh.y);
+          if (Q == 2) {
+            const uint2 xl = gx_ok ? *(const uint2*)(XL + k0 + 32 * bb) : z;
+            imma16832(fi[q], rw0.x, rw8.x, rw0.y, rw8.y, xl.x, xl.y);
+          }
+        }
+      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int bb = 4 * gi + q;  // block within the slice; b0 % 4 == 0, so partial q
-        const uint2 rw0 = *(const uint2*)(W0 + 32 * bb), rw8 = *(const uint2*)(W8 + 32 * bb);
         float d[4], f[4];
         if constexpr (I8) {
-          const uint2 z = make_uint2(0u, 0u);
-          block_dot_i8(d, rw0, rw8, gx_ok ? *(const uint2*)(XH + k0 + 32 * bb) : z);
-          if (Q == 2) block_dot_i8(f, rw0, rw8, gx_ok ? *(const uint2*)(XL + k0 + 32 * bb) : z);
+          // exact int32 (|d| < 2^20) -> f32 by the magic-number add, as block_dot_i8
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            d[e] = __fadd_rn(__int_as_float(di[q][e] + 0x4B400000), -12582912.0f);
+            f[e] = __fadd_rn(__int_as_float(fi[q][e] + 0x4B400000), -12582912.0f);
+          }
         } else {
+          const uint2 rw0 = *(const uint2*)(W0 + 32 * bb), rw8 = *(const uint2*)(W8 + 32 * bb);
           const Frag8 fw0 = frag8(rw0), fw8 = frag8(rw8);
           block_dot(d, fw0, fw8, act_frag<A16>(XH, k0 + 32 * bb, gx_ok));
           if (Q == 2) block_dot(f, fw0, fw8, act_frag<A16>(XL, k0 + 32 * bb, gx_ok));
