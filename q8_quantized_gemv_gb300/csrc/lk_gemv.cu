@@ -466,9 +466,12 @@ lk_status lk_gemv_q8_glu(const int8_t* wg, const uint16_t* wsg, const int8_t* wu
 //    rows and a K = 4096 activation chunk frees little shared memory:
 //    gate/up and o best at S = 1, q|k|v at 2, down at 2 (Int8Act, 139.6 ->
 //    87.7) to 8 (TwoPass, 406.6 -> 110.9).
-// Rule: S = 8 for one row group; 8 halved while the work units (tiles x S)
-// pass 100 per block of a row group; past 16 rows also at most the
-// activation bytes a block holds over 24 KB (a power of two).
+// With 1 KB slices for split launches (the tensor-core layout's first choice
+// there), S = 4 then beat S = 8 at 8 rows: q|k|v 11.0 -> 9.4 us, gate/up
+// 26.3 -> 25.0, down 16.9 -> 16.4 (Int8Act); TwoPass down 19.6 -> 18.7.
+// Rule: S = 4 for one and two row groups; halved while the work units
+// (tiles x S) pass 100 per block of a row group; past 16 rows also at most
+// the activation bytes a block holds over 24 KB (a power of two).
 int lk_splitk_chunks_for(int N, int K, lk_mode mode, int M) {
   if ((mode != LK_INT8ACT && mode != LK_TWOPASS) || M < 2 || M > LK_MAX_BATCH || N < 1 || K < 256 || K % 256)
     return 1;
@@ -477,7 +480,7 @@ int lk_splitk_chunks_for(int N, int K, lk_mode mode, int M) {
   const long tiles = ((long)N + 15) / 16;
   const int groups = (M + LK_MAX_M - 1) / LK_MAX_M;
   const long blocks = d->sm_count / groups > 0 ? d->sm_count / groups : 1;
-  int S = 8;
+  int S = 4;
   while (S > 1 && (tiles * S > 100 * blocks || K / 128 < S)) S >>= 1;
   if (M > 2 * LK_MAX_M) {
     const long act = (long)LK_MAX_M * K * (mode == LK_TWOPASS ? 2 : 1);

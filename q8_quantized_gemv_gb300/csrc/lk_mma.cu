@@ -871,9 +871,16 @@ MmaLayout mma_layout_for(const lkh::GemvProblem& p, long ntiles, int sms, int sm
   L.a_xs = p.mode == LK_TWOPASS ? round_up(L.a_lo + M * L.ar, 128u) : L.a_lo;
   L.ring_off = round_up(L.a_xs + M * L.xsr * 4u, 128u);
   const bool few = ntiles < 4L * sms;
-  const unsigned cand_tk[4] = {1024u, 512u, 512u, 256u};
-  const int cand_d[4] = {2, 2, 1, 1};
-  for (int i = few ? 0 : 2; i < 4; ++i) {
+  // split-K launches (many work units of a short chunk each) take 1 KB
+  // slices, one stage per warp first: measured at 8 rows, S = 4 (q|k|v
+  // 6144 x 4096 11.4 -> 9.4 us, gate/up 26.4 -> 25.0, down 4096 x 12288
+  // 21.1 -> 16.4 against 512-byte slices)
+  const bool split = p.split && p.S > 1;
+  const unsigned cand_tk[5] = {1024u, 512u, 512u, 256u, 1024u};
+  const int cand_d[5] = {2, 2, 1, 1, 1};
+  const int order[2][4] = {{0, 1, 2, 3}, {4, 2, 3, 3}};
+  for (int j = split ? 0 : (few ? 0 : 2); j < 4; ++j) {
+    const int i = order[split ? 1 : 0][j];
     unsigned tk = p.cfg.mma_tk > 0 ? (unsigned)p.cfg.mma_tk : cand_tk[i];
     if (tk > round_up(K, 256u)) tk = round_up(K, 256u);
     L.tk = tk;
