@@ -189,14 +189,25 @@ __global__ void __launch_bounds__(256) rmsnorm_split256_kernel(const NormArgs a)
   }
   __syncthreads();
   const Den<A> den = make_den<A>(norm_div_add(total, K, a.eps));
+  // this block's values: groups g0 + 8 j of the [M][K] layout, normalized,
+  // then quantized four groups at a time (their chains interleave)
+  const long i0 = base + (long)VT * u_mine + 32 * warp + lane;
+  float yv[NJ];
+  bool ok[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     float mine = v[j][0];
 #pragma unroll
     for (int u = 1; u < KU_MAX; ++u)
       if (u == u_mine) mine = v[j][u];
-    finish_value<Q, ADD>(a, base + 32 * (warp + 8 * j) + lane + (long)VT * u_mine, mine, den, gv[j], lane);
+    const long i = i0 + 256 * j;
+    if (ADD && a.s) a.s[i] = mine;
+    if constexpr (sizeof(A) == 4) yv[j] = norm_scale_r(mine, den.d, den.r, gv[j]);
+    else yv[j] = norm_scale(mine, den.d, gv[j]);
+    if (a.xn) a.xn[i] = yv[j];
+    ok[j] = true;
   }
+  if constexpr (Q > 0) quant_groups<Q, NJ>(yv, ok, a.xq, a.xl, a.xs, i0 >> 5, 8, lane);
   trec_end(a.tr, a.slot, TK_NORM, K);
 }
 

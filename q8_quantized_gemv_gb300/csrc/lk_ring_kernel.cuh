@@ -534,7 +534,7 @@ __device__ __forceinline__ uint4 ld_cg16(const void* p) {
 // issued after the block's weight stages completes only after them (the
 // copy engine serves a block's copies in order), which held the activation
 // back by the whole ring fill, several microseconds.
-template <int Q, int M, int U = (M >= 4 ? 8 : 2)>  // U: loads in flight per thread
+template <int Q, int M, int U = (M >= 4 ? 8 : 4)>  // U: loads in flight per thread
 __device__ __forceinline__ void load_act(unsigned char* act, unsigned L, const lkh::GemvProblem& a, int k_lo) {
   const int K = a.K, nb = K >> 5, b_lo = k_lo >> 5;
   // 16-byte run i: its source and its place in the area
