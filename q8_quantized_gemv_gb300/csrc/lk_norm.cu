@@ -149,16 +149,20 @@ __global__ void __launch_bounds__(1024) rmsnorm_split_kernel(const NormArgs a) {
 // K / 1024 blocks of 256 threads per row (K a multiple of 1024, at most
 // 8192): warp w plays the norm's warps w, w + 8, w + 16, w + 24, so a block
 // needs few registers and can share an SM with a GEMV block of the
-// neighbouring launches (a 1024-thread block cannot).
+// neighbouring launches (a 1024-thread block cannot).  Under Dequant the
+// f64 division per value (GB300's FP64 pipe is narrow) is spread further:
+// JS = 4 blocks per 1024 values, each finishing one virtual warp per real
+// warp (blockIdx.y = 4 u + j).
 template <int Q, bool ADD>
 __global__ void __launch_bounds__(256) rmsnorm_split256_kernel(const NormArgs a) {
   typedef typename acc_of<Q>::t A;
   constexpr int KU_MAX = 8, VT = 1024, NJ = 4;  // virtual warps per real warp
+  constexpr int JS = Q == 0 ? 4 : 1;            // blocks per 1024 values
   __shared__ A red[32];
   __shared__ A total;
   asm volatile("griddepcontrol.launch_dependents;" :::);  // as in rmsnorm_row_kernel
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int K = a.K, KU = K / VT, u_mine = blockIdx.y;
+  const int K = a.K, KU = K / VT, u_mine = blockIdx.y / JS, j_mine = blockIdx.y % JS;
   const long base = (long)blockIdx.x * K;
   float gv[NJ];
 #pragma unroll
@@ -196,6 +200,7 @@ __global__ void __launch_bounds__(256) rmsnorm_split256_kernel(const NormArgs a)
   bool ok[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
+    if (JS > 1 && j % JS != j_mine) continue;
     float mine = v[j][0];
 #pragma unroll
     for (int u = 1; u < KU_MAX; ++u)
@@ -215,7 +220,7 @@ template <int Q, bool ADD>
 void launch_norm(const NormArgs& a, int M, int pdl, cudaStream_t stream) {
   const int K = a.K, vt = K < 1024 ? K : 1024;  // K % 32 == 0: roundup32(K) == K
   if (K % 1024 == 0 && K / 1024 <= 8)
-    launch_pdl(rmsnorm_split256_kernel<Q, ADD>, dim3(M, K / 1024), dim3(256), stream, pdl, a);
+    launch_pdl(rmsnorm_split256_kernel<Q, ADD>, dim3(M, K / 1024 * (Q == 0 ? 4 : 1)), dim3(256), stream, pdl, a);
   else if (K % vt == 0 && K / vt <= 8)
     launch_pdl(rmsnorm_split_kernel<Q, ADD>, dim3(M, K / vt), dim3(vt), stream, pdl, a);
   else
