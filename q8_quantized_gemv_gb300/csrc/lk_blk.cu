@@ -56,6 +56,31 @@ __device__ __forceinline__ unsigned w32(const unsigned char* p) {
   const unsigned sh = 8u * (unsigned)(a & 3);
   return sh ? __funnelshift_r(q[0], q[1], sh) : q[0];
 }
+// NW consecutive 4-byte words from any offset: the NW + 1 aligned words
+// around them, funnel-shifted by the offset's byte position (the same for
+// every word; no per-word branch).
+template <int NW>
+__device__ __forceinline__ void words_at(const unsigned char* p, unsigned (&out)[NW]) {
+  const uintptr_t a = (uintptr_t)p;
+  const unsigned* q = (const unsigned*)(a & ~(uintptr_t)3);
+  const unsigned sh = 8u * (unsigned)(a & 3);
+  unsigned v[NW + 1];
+#pragma unroll
+  for (int i = 0; i <= NW; ++i) v[i] = q[i];
+#pragma unroll
+  for (int i = 0; i < NW; ++i) out[i] = __funnelshift_r(v[i], v[i + 1], sh);
+}
+
+// Formats whose level words sit at 4-byte-aligned offsets of a staged row
+// (16-byte aligned): blocks of 20 or 24 bytes with 4- or 8-byte headers,
+// super-blocks of 84, 136, 144 or 176 bytes.  Their words are read as they
+// are; the others (17-, 18-, 22-, 110- and 210-byte blocks) go through w32.
+template <int F>
+__device__ __forceinline__ unsigned word_at(const unsigned char* p) {
+  if constexpr (F == 3 || F == 7 || F == 10 || F == 12 || F == 13 || F == 23) return *(const unsigned*)p;
+  return w32(p);
+}
+
 // Bits 0..3 of b spread to bit 0 of bytes 0..3.
 __device__ __forceinline__ unsigned spread4(unsigned b) { return ((b & 15u) * 0x00204081u) & 0x01010101u; }
 
@@ -83,9 +108,16 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
     const unsigned char* qs = b + (F == 3 ? 4 : 2);
     d[0] = d[1] = half_at(b);
     if (F == 3) c[0] = c[1] = half_at(b + 2);
+    unsigned qw[4];
+    if constexpr (F == 3) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qw[i] = word_at<F>(qs + 4 * i);
+    } else {
+      words_at<4>(qs, qw);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const unsigned q = w32(qs + 4 * i);
+      const unsigned q = qw[i];
       if constexpr (F == 20) {
         table_word(tab, q, w[i], w[4 + i]);
       } else {
@@ -100,12 +132,19 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
   } else if constexpr (F == 6 || F == 7) {
     const unsigned char* b = row + sb * blk_bytes(F);
     const unsigned char* hb = b + (F == 7 ? 4 : 2);
-    const unsigned qh = w32(hb);
+    unsigned hw[5];  // the high-bit word, then the four level words
+    if constexpr (F == 7) {
+#pragma unroll
+      for (int i = 0; i < 5; ++i) hw[i] = word_at<F>(hb + 4 * i);
+    } else {
+      words_at<5>(hb, hw);
+    }
+    const unsigned qh = hw[0];
     d[0] = d[1] = half_at(b);
     if (F == 7) c[0] = c[1] = half_at(b + 2);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const unsigned q = w32(hb + 4 + 4 * i);
+      const unsigned q = hw[1 + i];
       w[i] = (q & 0x0F0F0F0Fu) | (spread4(qh >> (4 * i)) << 4);
       w[4 + i] = ((q >> 4) & 0x0F0F0F0Fu) | (spread4(qh >> (16 + 4 * i)) << 4);
       if (F == 6) {
@@ -119,8 +158,10 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
     // E8M0 exponent e is 2^(e - 127); halved for the doubled E2M1 values:
     // 2^(e - 128), subnormal below e = 2
     d[0] = d[1] = __uint_as_float(e < 2u ? (0x00200000u << e) : ((e - 1u) << 23));
+    unsigned qw[4];
+    words_at<4>(b + 1, qw);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) table_word(tab, w32(b + 1 + 4 * i), w[i], w[4 + i]);
+    for (int i = 0; i < 4; ++i) table_word(tab, qw[i], w[i], w[4 + i]);
   } else if constexpr (F == 12 || F == 13) {
     const unsigned char* sup = row + (sb >> 3) * blk_bytes(F);
     const int j = sb & 7;
@@ -138,16 +179,16 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
     const unsigned char* ql = sup + (F == 12 ? 16 : 48) + (j >> 1) * 32;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const unsigned q = w32(ql + 4 * i);
+      const unsigned q = word_at<F>(ql + 4 * i);
       w[i] = (j & 1) ? ((q >> 4) & 0x0F0F0F0Fu) : (q & 0x0F0F0F0Fu);
-      if (F == 13) w[i] |= ((w32(sup + 16 + 4 * i) >> j) & 0x01010101u) << 4;
+      if (F == 13) w[i] |= ((word_at<F>(sup + 16 + 4 * i) >> j) & 0x01010101u) << 4;
     }
   } else if constexpr (F == 10) {
     const unsigned char* sup = row + (sb >> 3) * 84;
     const int j = sb & 7, half = j >> 2, k = j & 3;
     const unsigned char* q = sup + 16 + half * 32;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = (w32(q + 4 * i) >> (2 * k)) & 0x03030303u;
+    for (int i = 0; i < 8; ++i) w[i] = (word_at<F>(q + 4 * i) >> (2 * k)) & 0x03030303u;
     const float D = half_at(sup + 80), DM = half_at(sup + 82);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -159,10 +200,13 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
     const unsigned char* sup = row + (sb >> 3) * 110;
     const int j = sb & 7, half = j >> 2, k = j & 3, bit = half * 4 + k;
     const unsigned char* q = sup + 32 + half * 32;
+    unsigned qw[8], mw[8];
+    words_at<8>(q, qw);
+    words_at<8>(sup, mw);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const unsigned low2 = (w32(q + 4 * i) >> (2 * k)) & 0x03030303u;
-      const unsigned mb = (w32(sup + 4 * i) >> bit) & 0x01010101u;  // set: +0, clear: -4
+      const unsigned low2 = (qw[i] >> (2 * k)) & 0x03030303u;
+      const unsigned mb = (mw[i] >> bit) & 0x01010101u;  // set: +0, clear: -4
       w[i] = __vsub4(low2 | (mb << 2), 0x04040404u);
     }
     const unsigned char* s12 = sup + 96;
@@ -179,10 +223,13 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
     const int j = sb & 7, half = j >> 2, k = j & 3;
     const unsigned char* ql = sup + half * 64 + (k & 1) * 32;
     const unsigned char* qh = sup + 128 + half * 32;
+    unsigned lw[8], hw[8];
+    words_at<8>(ql, lw);
+    words_at<8>(qh, hw);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const unsigned lo = (w32(ql + 4 * i) >> (4 * (k >> 1))) & 0x0F0F0F0Fu;
-      const unsigned hi = (w32(qh + 4 * i) >> (2 * k)) & 0x03030303u;
+      const unsigned lo = (lw[i] >> (4 * (k >> 1))) & 0x0F0F0F0Fu;
+      const unsigned hi = (hw[i] >> (2 * k)) & 0x03030303u;
       w[i] = __vsub4(lo | (hi << 4), 0x20202020u);
     }
     const float D = half_at(sup + 208);
@@ -196,7 +243,7 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
     d[0] = d[1] = __fmul_rn(half_at(sup), (float)(ls - 32));
     const unsigned char* qs = sup + 8 + 16 * j;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) table_word(tab, w32(qs + 4 * i), w[i], w[4 + i]);
+    for (int i = 0; i < 4; ++i) table_word(tab, word_at<F>(qs + 4 * i), w[i], w[4 + i]);
   }
 }
 
@@ -209,16 +256,16 @@ __device__ __forceinline__ void load_table(int F, signed char* tab) {
 }
 
 // f32 part of one sub-block for one activation row: ((d0 dh0 + c0 sh0) +
-// d1 dh1) + c1 sh1, each product and sum rounded.
+// d1 dh1) + c1 sh1, each product and sum rounded; sh: the activation
+// halves' sums (exact integers, formed once when the rows are staged).
 __device__ __forceinline__ float sub_part(const unsigned (&w)[8], const float (&d)[2], const float (&c)[2],
-                                          const unsigned (&h)[8]) {
-  int dh0 = 0, dh1 = 0, sh0 = 0, sh1 = 0;
+                                          const unsigned (&h)[8], int2 sh) {
+  int dh0 = 0, dh1 = 0;
+  const int sh0 = sh.x, sh1 = sh.y;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     dh0 = __dp4a((int)w[i], (int)h[i], dh0);
-    sh0 = __dp4a(0x01010101, (int)h[i], sh0);
     dh1 = __dp4a((int)w[4 + i], (int)h[4 + i], dh1);
-    sh1 = __dp4a(0x01010101, (int)h[4 + i], sh1);
   }
   float p = __fmul_rn(d[0], (float)dh0);
   p = __fadd_rn(p, __fmul_rn(c[0], (float)sh0));
@@ -272,14 +319,27 @@ __device__ __forceinline__ void stage_act(const BlkArgs& a, unsigned char* act) 
       }
   } else {
     const unsigned nb = (unsigned)K / 32u;
+    // the byte sum of a 16-value half, exact
+    auto sum16 = [](uint4 v) {
+      int r = __dp4a((int)v.x, 0x01010101, 0);
+      r = __dp4a((int)v.y, 0x01010101, r);
+      r = __dp4a((int)v.z, 0x01010101, r);
+      return __dp4a((int)v.w, 0x01010101, r);
+    };
     for (int t = 0; t < a.M; ++t) {
       unsigned char* base = act + (size_t)t * a.act_stride;
-      for (int i = threadIdx.x; i < K / 16; i += blockDim.x) {
-        *(uint4*)(base + pad_index(16u * i, 1u)) = __ldcg((const uint4*)(a.xq + (long)t * K) + i);
-        if (Q == 2)
-          *(uint4*)(base + pad_index(16u * i, 1u) + nb * 48u) = __ldcg((const uint4*)(a.xl + (long)t * K) + i);
-      }
       float* s = (float*)(base + nb * 48u * (Q == 2 ? 2u : 1u));
+      int* sums = (int*)(s + nb);  // [2 nb] halves of the words, then [2 nb] of the low words
+      for (int i = threadIdx.x; i < K / 16; i += blockDim.x) {
+        const uint4 hv = __ldcg((const uint4*)(a.xq + (long)t * K) + i);
+        *(uint4*)(base + pad_index(16u * i, 1u)) = hv;
+        sums[i] = sum16(hv);
+        if (Q == 2) {
+          const uint4 lv = __ldcg((const uint4*)(a.xl + (long)t * K) + i);
+          *(uint4*)(base + pad_index(16u * i, 1u) + nb * 48u) = lv;
+          sums[2 * nb + i] = sum16(lv);
+        }
+      }
       for (int i = threadIdx.x; i < (int)nb; i += blockDim.x) s[i] = __ldcg(a.xs + (long)t * nb + i);
     }
   }
@@ -384,15 +444,17 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
           unsigned h[8];
           *(uint4*)&h[0] = *(const uint4*)hp;
           *(uint4*)&h[4] = *(const uint4*)(hp + 16);
-          float part = sub_part(w, d, c, h);
+          const float* srow = (const float*)(base + nbu * 48u * (Q == 2 ? 2u : 1u));
+          const int2* sums = (const int2*)(srow + nbu);
+          float part = sub_part(w, d, c, h, sums[sb]);
           if constexpr (Q == 2) {
             const unsigned char* lp = hp + nbu * 48u;
             unsigned l[8];
             *(uint4*)&l[0] = *(const uint4*)lp;
             *(uint4*)&l[4] = *(const uint4*)(lp + 16);
-            part = __fadd_rn(part, __fmul_rn(0.0078125f, sub_part(w, d, c, l)));
+            part = __fadd_rn(part, __fmul_rn(0.0078125f, sub_part(w, d, c, l, sums[nbu + sb])));
           }
-          const float s = ((const float*)(base + nbu * 48u * (Q == 2 ? 2u : 1u)))[sb];
+          const float s = srow[sb];
           acc[t] = __fadd_rn(acc[t], __fmul_rn(s, part));
         }
       }
@@ -467,7 +529,8 @@ lk_status launch(int F, const unsigned char* w, int N, int K, int mode, const fl
   const unsigned nb = (unsigned)K / 32u;
   a.act_stride = dq ? 0u
                     : mode == 0 ? nb * (32u * 4u + 16u)
-                                : ((nb * 48u * (mode == 2 ? 2u : 1u) + nb * 4u + 15u) & ~15u);
+                                : ((nb * 48u * (mode == 2 ? 2u : 1u) + nb * 4u + nb * 8u * (mode == 2 ? 2u : 1u) +
+                                    15u) & ~15u);
   a.act_bytes = a.act_stride * (unsigned)(dq ? 0 : M);
   // 16 bytes of slack after a row: a word read at the row's last bytes may
   // load the aligned word after them
