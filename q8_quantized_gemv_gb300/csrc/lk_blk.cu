@@ -395,23 +395,35 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
         unsigned w[8];
         float d[2], c[2];
         decode<F>(rbuf, sb, tab, w, d, c);
-        float wv[32];
+        // the weights RN(RN(d level) + c) as packed pairs (values 4q + k and
+        // 4q + k + 2 of word q): the level bytes placed in the mantissa of
+        // 2^23 + 128 + b and the bias subtracted (exact), then the scale and
+        // the offset, each rounded as the scalar form
+        f32x2 wv[16];
+        const f32x2 bias = f2_pack(-8388736.0f, -8388736.0f);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          wv[i] = __fadd_rn(__fmul_rn(d[i >> 4], (float)(signed char)(w[i >> 2] >> (8 * (i & 3)))), c[i >> 4]);
+        for (int q = 0; q < 8; ++q) {
+          const unsigned u = w[q] ^ 0x80808080u;
+          const f32x2 dd = f2_pack(d[q >> 2], d[q >> 2]), cc = f2_pack(c[q >> 2], c[q >> 2]);
+          wv[2 * q] = f2_add(f2_mul(dd, f2_add(f2_pack(i8_bits_f32(u, 0), i8_bits_f32(u, 2)), bias)), cc);
+          wv[2 * q + 1] = f2_add(f2_mul(dd, f2_add(f2_pack(i8_bits_f32(u, 1), i8_bits_f32(u, 3)), bias)), cc);
+        }
 #pragma unroll
         for (int t = 0; t < MM; ++t) {
           if (t >= a.M) break;
           const float* xr = (const float*)(act + (size_t)t * a.act_stride + pad_index(32u * sb, 4u));
-          float acc = 0.f;
+          // two interleaved chains of products (the tolerance, not the
+          // pages' order, binds Dequant), joined at the sub-block's end
+          f32x2 acc2 = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const float4 xv = *(const float4*)(xr + 4 * q);
-            acc = __fmaf_rn(wv[4 * q], xv.x, acc);
-            acc = __fmaf_rn(wv[4 * q + 1], xv.y, acc);
-            acc = __fmaf_rn(wv[4 * q + 2], xv.z, acc);
-            acc = __fmaf_rn(wv[4 * q + 3], xv.w, acc);
+            acc2 = f2_fma(wv[2 * q], f2_pack(xv.x, xv.z), acc2);
+            acc2 = f2_fma(wv[2 * q + 1], f2_pack(xv.y, xv.w), acc2);
           }
+          float a0, a1;
+          f2_unpack(acc2, a0, a1);
+          const float acc = __fadd_rn(a0, a1);
           // s1 + s2 += acc (Kahan-Babuska: the rounding error kept in s2)
           const float sum = __fadd_rn(s1[t], acc);
           const float bp = __fsub_rn(sum, s1[t]);
