@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
 #pragma unroll
       for (int t = 0; t < MM; ++t) acc[t] = 0.f;
       const unsigned nbu = (unsigned)nb;
+#pragma unroll 2
       for (int sb = lane; sb < nb; sb += 32) {
         unsigned w[8];
         float d[2], c[2];
