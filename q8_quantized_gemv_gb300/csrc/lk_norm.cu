@@ -35,6 +35,15 @@ struct NormArgs {
   int slot;
 };
 
+// The residual sum x + r, stored with an L2 evict-last hint: it is the next
+// residual add's r, read back after a GEMV or two whose weights (hundreds of
+// MB) stream through L2 meanwhile.
+__device__ __forceinline__ void store_keep(float* p, float v) {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+
 // Value i of the row the norm sees: x, or x + r rounded once to f32.  Both
 // reads go through L2: under a programmatic dependent launch the previous
 // kernel may have written them.
@@ -61,7 +70,7 @@ __device__ __forceinline__ Den<A> make_den(A d) {
 
 template <int Q, bool ADD, typename A>
 __device__ __forceinline__ void finish_value(const NormArgs& a, long i, float v, Den<A> den, float gv, int lane) {
-  if (ADD && a.s) a.s[i] = v;
+  if (ADD && a.s) store_keep(a.s + i, v);
   float yv;
   if constexpr (sizeof(A) == 4) yv = norm_scale_r(v, den.d, den.r, gv);
   else yv = norm_scale(v, den.d, gv);
@@ -206,7 +215,7 @@ __global__ void __launch_bounds__(256) rmsnorm_split256_kernel(const NormArgs a)
     for (int u = 1; u < KU_MAX; ++u)
       if (u == u_mine) mine = v[j][u];
     const long i = i0 + 256 * j;
-    if (ADD && a.s) a.s[i] = mine;
+    if (ADD && a.s) store_keep(a.s + i, mine);
     if constexpr (sizeof(A) == 4) yv[j] = norm_scale_r(mine, den.d, den.r, gv[j]);
     else yv[j] = norm_scale(mine, den.d, gv[j]);
     if (a.xn) a.xn[i] = yv[j];
