@@ -84,23 +84,48 @@ __device__ __forceinline__ unsigned word_at(const unsigned char* p) {
 // Bits 0..3 of b spread to bit 0 of bytes 0..3.
 __device__ __forceinline__ unsigned spread4(unsigned b) { return ((b & 15u) * 0x00204081u) & 0x01010101u; }
 
-// 16-entry int8 level table (shared memory) applied to the low and the high
-// nibbles of a word: bytes of `lo` = table[low nibbles], `hi` = table[high].
-__device__ __forceinline__ void table_word(const signed char* tab, unsigned q, unsigned& lo, unsigned& hi) {
-  lo = 0u;
-  hi = 0u;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const unsigned b = (q >> (8 * k)) & 0xFFu;
-    lo |= (unsigned)(unsigned char)tab[b & 15u] << (8 * k);
-    hi |= (unsigned)(unsigned char)tab[b >> 4] << (8 * k);
-  }
+// The 16-entry int8 level tables (IQ4_NL / IQ4_XS: sixteen non-linear
+// levels; MXFP4: the E2M1 values doubled), four entries to a word, held in
+// registers.
+struct Lut16 {
+  unsigned t0, t1, t2, t3;
+};
+__host__ __device__ constexpr unsigned pack4(int a, int b, int c, int d) {
+  return (unsigned)(a & 255) | ((unsigned)(b & 255) << 8) | ((unsigned)(c & 255) << 16) | ((unsigned)(d & 255) << 24);
+}
+template <int F>
+__device__ __forceinline__ Lut16 level_lut() {
+  if constexpr (F == 39)
+    return Lut16{pack4(0, 1, 2, 3), pack4(4, 6, 8, 12), pack4(0, -1, -2, -3), pack4(-4, -6, -8, -12)};
+  return Lut16{pack4(-127, -104, -83, -65), pack4(-49, -35, -22, -10), pack4(1, 13, 25, 38),
+               pack4(53, 69, 89, 113)};
+}
+
+// Table entries for the four nibble values n (one per byte, 0..15): the
+// byte permute picks entry n & 7 from the low and from the high eight, and
+// bit 3 of each n chooses between them.
+__device__ __forceinline__ unsigned lut_bytes(const Lut16& T, unsigned n) {
+  const unsigned s = n & 0x07070707u;
+  const unsigned sel = __byte_perm(s | (s >> 4), 0u, 0x4420u);  // the four 3-bit indices as nibbles
+  const unsigned lo = __byte_perm(T.t0, T.t1, sel);
+  const unsigned hi = __byte_perm(T.t2, T.t3, sel);
+  const unsigned m = ((n >> 3) & 0x01010101u) * 0xFFu;
+  return (lo & ~m) | (hi & m);
+}
+
+// The table applied to the low and the high nibbles of a word: bytes of
+// `lo` = table[low nibbles], `hi` = table[high nibbles].
+template <int F>
+__device__ __forceinline__ void table_word(unsigned q, unsigned& lo, unsigned& hi) {
+  const Lut16 T = level_lut<F>();
+  lo = lut_bytes(T, q & 0x0F0F0F0Fu);
+  hi = lut_bytes(T, (q >> 4) & 0x0F0F0F0Fu);
 }
 
 // Sub-block sb of a staged row in format F: w[0..7] the 32 levels four to a
 // word (value 4i + k in byte k of w[i]), d/c per half.
 template <int F>
-__device__ __forceinline__ void decode(const unsigned char* row, int sb, const signed char* tab, unsigned (&w)[8],
+__device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigned (&w)[8],
                                        float (&d)[2], float (&c)[2]) {
   c[0] = c[1] = 0.f;
   if constexpr (F == 2 || F == 3 || F == 20) {
@@ -119,7 +144,7 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
     for (int i = 0; i < 4; ++i) {
       const unsigned q = qw[i];
       if constexpr (F == 20) {
-        table_word(tab, q, w[i], w[4 + i]);
+        table_word<F>(q, w[i], w[4 + i]);
       } else {
         w[i] = q & 0x0F0F0F0Fu;
         w[4 + i] = (q >> 4) & 0x0F0F0F0Fu;
@@ -161,7 +186,7 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
     unsigned qw[4];
     words_at<4>(b + 1, qw);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) table_word(tab, qw[i], w[i], w[4 + i]);
+    for (int i = 0; i < 4; ++i) table_word<F>(qw[i], w[i], w[4 + i]);
   } else if constexpr (F == 12 || F == 13) {
     const unsigned char* sup = row + (sb >> 3) * blk_bytes(F);
     const int j = sb & 7;
@@ -243,17 +268,10 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, const s
     d[0] = d[1] = __fmul_rn(half_at(sup), (float)(ls - 32));
     const unsigned char* qs = sup + 8 + 16 * j;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) table_word(tab, word_at<F>(qs + 4 * i), w[i], w[4 + i]);
+    for (int i = 0; i < 4; ++i) table_word<F>(word_at<F>(qs + 4 * i), w[i], w[4 + i]);
   }
 }
 
-// The level table a format looks up (IQ4 levels, doubled E2M1 values).
-__device__ __forceinline__ void load_table(int F, signed char* tab) {
-  // IQ4_NL / IQ4_XS: sixteen non-linear levels; MXFP4: E2M1 values x 2
-  const signed char iq4[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
-  const signed char mx[16] = {0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12};
-  if (threadIdx.x < 16) tab[threadIdx.x] = F == 39 ? mx[threadIdx.x] : iq4[threadIdx.x];
-}
 
 // f32 part of one sub-block for one activation row: ((d0 dh0 + c0 sh0) +
 // d1 dh1) + c1 sh1, each product and sum rounded; sh: the activation
@@ -348,14 +366,12 @@ __device__ __forceinline__ void stage_act(const BlkArgs& a, unsigned char* act) 
 template <int F, int Q, int MM>
 __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ signed char tab[16];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   unsigned char* act = smem;
   unsigned char* bufs = smem + a.act_bytes + (size_t)warp * 2 * a.rb_pad;
   const int K = a.K, nb = K >> 5;
   const long stride = (long)gridDim.x * nw;
   long row = (long)blockIdx.x * nw + warp;
-  load_table(F, tab);
   if (a.pdl && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" :::);
   // the first row's bytes (weights: no dependence on the previous kernel)
   auto fetch = [&](long r, unsigned char* dst) {
@@ -380,7 +396,7 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
       for (int sb = lane; sb < nb; sb += 32) {
         unsigned w[8];
         float d[2], c[2];
-        decode<F>(rbuf, sb, tab, w, d, c);
+        decode<F>(rbuf, sb, w, d, c);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float v = (float)(signed char)(w[i >> 2] >> (8 * (i & 3)));
@@ -394,7 +410,7 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
       for (int sb = lane; sb < nb; sb += 32) {
         unsigned w[8];
         float d[2], c[2];
-        decode<F>(rbuf, sb, tab, w, d, c);
+        decode<F>(rbuf, sb, w, d, c);
         // the weights RN(RN(d level) + c) as packed pairs (values 4q + k and
         // 4q + k + 2 of word q): the level bytes placed in the mantissa of
         // 2^23 + 128 + b and the bias subtracted (exact), then the scale and
@@ -448,7 +464,7 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
       for (int sb = lane; sb < nb; sb += 32) {
         unsigned w[8];
         float d[2], c[2];
-        decode<F>(rbuf, sb, tab, w, d, c);
+        decode<F>(rbuf, sb, w, d, c);
 #pragma unroll
         for (int t = 0; t < MM; ++t) {
           if (t >= a.M) break;
@@ -548,7 +564,7 @@ lk_status launch(int F, const unsigned char* w, int N, int K, int mode, const fl
   // 16 bytes of slack after a row: a word read at the row's last bytes may
   // load the aligned word after them
   a.rb_pad = (unsigned)((a.rb + 15) & ~15L) + 16u;
-  // (less a margin for the kernel's static level table)
+  // (less a small margin)
   long room = (long)dev->smem_optin - 256L - (long)a.act_bytes;
   int nw = room > 0 ? (int)(room / (2L * a.rb_pad)) : 0;
   if (nw > BW) nw = BW;
