@@ -113,3 +113,23 @@ def test_gemv_blk_argument_checks():
     assert lib.lk_gemv_blk(2, P(w), 4, 256, 1, None, P(xq), None, P(xs), 9, P(y), None, None) == -3
     assert lib.lk_gemv_blk(2, P(w), 4, 256, 2, None, P(xq), None, P(xs), 1, P(y), None, None) == -1
     assert lk.lk_format_row_bytes("q6_k", 4096) == 16 * 210 and lk.lk_format_row_bytes("q4_k", 100) == 0
+
+
+@pytest.mark.parametrize("fmt,mode,M", [("q4_0", 1, 1), ("q4_k", 1, 1), ("q6_k", 2, 1), ("iq4_xs", 1, 8),
+                                        ("q5_1", 2, 8), ("mxfp4", 1, 3)])
+def test_gemv_blk_full_size_all_rows(fmt, mode, M):
+    """The gate/up-sized GEMV the bench times (24576 x 4096, the launch
+    `bench.py --workload gemv --format f` makes): every output bit for bit
+    the oracle's."""
+    N, K = 24576, 4096
+    F = oracle.FORMATS[fmt]
+    w = synth.blk_matrix(fmt, N, K, 600 + F)
+    x = synth.activation(M, K, 601 + M, outliers=True)
+    hi, lo, s = oracle.quantize(x, mode)
+    y_or = oracle.gemv_blk(F, w, K, mode, hi=hi, lo=lo, s=s)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    lk.lk_gemv_blk(fmt, to_dev(w), K, mode, y, xq=to_dev(hi), xs=to_dev(s),
+                   xl=to_dev(lo) if mode == 2 else None, M=M, cfg=lk.launch_cfg(pdl=1))
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) == 0
+    assert np.array_equal(bits(host(y)), bits(y_or))
