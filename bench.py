@@ -473,6 +473,152 @@ def run_ours(a, rank, world):
         dist.destroy_process_group()
 
 
+def run_blk_sequence(a, rank, world):
+    """The 36-layer projection sequence with every matrix in block format
+    `a.format` (BlkDecodeStack): one CUDA graph per token, timed like the
+    Q8_0 sequence; the line carries the same keys (roofline: the gate/up
+    launches of a token back to back; cpu_baseline: the oracle on one
+    layer's projections)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from q8_quantized_gemv_gb300 import build, lk
+    from q8_quantized_gemv_gb300.decode import BlkDecodeStack
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stack = BlkDecodeStack(a.format, layers=a.layers, batch=a.batch, mode=a.mode, device=dev, pdl=not a.no_pdl)
+    tok_bytes = stack.weight_bytes()
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            stack.run_token()
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        stack.run_token()
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.5)
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    tw0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(a.steps):
+            graph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.summary(tw0, tw1)
+    clocks.stop()
+    ms_max = _max_over_ranks(ev0.elapsed_time(ev1) / a.steps, dist, dev)
+    value = replica_value(tok_bytes, world, ms_max)
+    # e2e: the token input from pinned host memory, the argmax back, every step
+    x_host = stack.x0.cpu().pin_memory()
+    idx_host = torch.empty_like(stack.idx, device="cpu").pin_memory()
+    n_e2e = max(1, min(a.steps, 200))
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            stack.x_buf.copy_(x_host, non_blocking=True)
+            graph.replay()
+            idx_host.copy_(stack.idx, non_blocking=True)
+            stream.synchronize()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = _max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, dev)
+    # roofline: the token's gate/up launches back to back in one graph
+    got = []
+
+    def hook(name, launch):
+        if name == "gu":
+            got.append(launch)
+        return launch()
+
+    with torch.cuda.stream(stream):
+        stack.run_token(hook=hook)
+    torch.cuda.synchronize()
+    g_gu = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_gu, stream=stream):
+        for launch in got:
+            launch()
+    with torch.cuda.stream(stream):
+        g_gu.replay()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        reps = 5
+        for _ in range(reps):
+            g_gu.replay()
+        r1.record(stream)
+    torch.cuda.synchronize()
+    gu_us = r0.elapsed_time(r1) * 1e3 / (reps * len(got))
+    peaks, src = measured_peaks()
+    gu_bytes = stack.weight_bytes("gu")
+    act_b = a.batch * 4096 * (4 if stack.mode == lk.LK_DEQUANT else 2 if stack.mode == lk.LK_TWOPASS else 1)
+    alg = gu_bytes + act_b + a.batch * stack.shapes["gu"][0] * 4
+    roof = {"bound": "hbm", "achieved": alg / (gu_us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": alg / (gu_us * 1e-6) / 1e9 / peaks["hbm_gbs"], "traffic": None, "peak_source": src,
+            "kernel": f"gate/up {a.format.upper()} GEMV 24576x4096 (lk_gemv_blk)",
+            "algorithmic_bytes_per_launch": alg, "avg_launch_us": gu_us, "launches_timed": reps * len(got)}
+    out = {
+        "metric": f"{a.format.upper()} GEMV effective weight GB/s (36-layer decode projection sequence, per token)",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": _dtype(a.mode),
+        "data": f"synthetic (seeded {a.format.upper()} blocks: random levels, scales and offsets; N(0, 1) activations "
+                "with 1 % x20 outliers)",
+        "config": {"workload": workload_name(a) + f", weights {a.format.upper()}", "weight_bytes_per_step": tok_bytes,
+                   "l2": "inputs larger than L2", "parallelism": "replicas" if world > 1 else "single GPU"},
+        "us_per_token": ms_max * 1e3,
+        "roofline": roof,
+        "e2e": {"value": tok_bytes * world / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": idx_host.numel() * 4,
+                "ms_per_step": ms_e2e, "steps": n_e2e},
+        "clocks": clk,
+        "gpu_launches": stack.launches_per_token() * a.steps,
+    }
+    if rank == 0 and not a.no_cpu_baseline:
+        # the oracle on layer 0's four projections (host copies), one thread
+        F = oracle.FORMATS[a.format]
+        w0 = stack.layers[0]
+        host = {n: w0[n].cpu().numpy() for n in stack.shapes}
+        t0 = time.perf_counter()
+        nbytes = 0
+        for n, (N, K) in stack.shapes.items():
+            x = np.random.default_rng(0).standard_normal((a.batch, K)).astype(np.float32)
+            if stack.mode == lk.LK_DEQUANT:
+                oracle.gemv_blk(F, host[n], K, 0, x=x)
+            else:
+                hi, lo, sc = oracle.quantize(x, stack.mode)
+                oracle.gemv_blk(F, host[n], K, stack.mode, hi=hi, lo=lo, s=sc)
+            nbytes += stack.weight_bytes(n)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                               "sample": f"layer 0's q|k|v, o, gate/up and down ({a.format.upper()}), C oracle, "
+                                         "one thread", "seconds": dt}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def _tune(a):
     """The --cfg launch settings as a dict of lk_launch_cfg fields."""
     return {kv.split("=")[0]: int(kv.split("=")[1]) for kv in a.cfg}
@@ -955,6 +1101,9 @@ def main():
         return
     if a.workload == "gemv":
         run_gemv(a, rank, world)
+        return
+    if a.format:
+        run_blk_sequence(a, rank, world)
         return
     run_ours(a, rank, world)
 

@@ -361,3 +361,107 @@ class DecodeStack:
             + (0 if (f["o"] or self.mode == lk.LK_DEQUANT) else 1) + (0 if f["gu"] else 1) \
             + (0 if (f["down"] or self.mode == lk.LK_DEQUANT) else 1) + len(self.splitk)
         return n + self.L * per_layer + 1 + (0 if f["lm"] else 1)
+
+
+class BlkDecodeStack:
+    """The projections-alone decode sequence with every matrix in one of the
+    other GGUF block formats (lk_gemv_blk): per layer RMSNorm -> q|k|v (one
+    fused matrix) -> quantize -> o -> RMSNorm -> gate/up -> quantize -> down;
+    then RMSNorm -> lm-head -> argmax of the logits.  One to LK_MAX_M
+    activation rows, every mode; synthetic weights of the format's layout
+    (synth.blk_matrix), the same activations and gains as DecodeStack."""
+
+    def __init__(self, fmt, layers=36, hidden=4096, q_dim=4096, kv_dim=1024, ffn=12288, vocab=151936, batch=1,
+                 mode=lk.LK_INT8ACT, seed=synth.SEED_BASE + 4, device="cuda", eps=1e-6, pdl=True):
+        self.fmt = fmt
+        self.L, self.H, self.Q, self.KV, self.F, self.V = layers, hidden, q_dim, kv_dim, ffn, vocab
+        self.B, self.mode, self.eps, self.dev = batch, lk._mode(mode), eps, torch.device(device)
+        self.pdl = bool(pdl)
+        dev, s = self.dev, seed
+        self.shapes = {"qkv": (q_dim + 2 * kv_dim, hidden), "o": (hidden, q_dim), "gu": (2 * ffn, hidden),
+                       "down": (hidden, ffn)}
+        self.layers = []
+        for l in range(layers):
+            w = {n: synth.blk_matrix_torch(fmt, N, K, s + 1000 * l + i, dev)
+                 for i, (n, (N, K)) in enumerate(self.shapes.items())}
+            w["g_attn"] = synth.norm_gain_torch(hidden, s + 1000 * l + 10, dev)
+            w["g_mlp"] = synth.norm_gain_torch(hidden, s + 1000 * l + 11, dev)
+            w["o_in"] = synth.activation_torch(batch, q_dim, s + 1000 * l + 12, dev, outliers=True)
+            w["d_in"] = synth.activation_torch(batch, ffn, s + 1000 * l + 13, dev, outliers=True)
+            self.layers.append(w)
+        self.lm = synth.blk_matrix_torch(fmt, vocab, hidden, s + 999_000, dev)
+        self.g_final = synth.norm_gain_torch(hidden, s + 999_001, dev)
+        self.x0 = synth.activation_torch(batch, hidden, s + 999_002, dev, outliers=True)
+        self.x_buf = self.x0.clone()
+        f32, B = torch.float32, batch
+        self.h = torch.empty((B, hidden), dtype=f32, device=dev)
+        self.xn = {K: torch.empty((B, K), dtype=f32, device=dev) for K in {hidden, q_dim, ffn}}
+        self.acts = {}
+        for K in {hidden, q_dim, ffn}:
+            d = {"xq": torch.empty((B, K), dtype=torch.int8, device=dev),
+                 "xs": torch.empty((B, K // 32), dtype=torch.float32, device=dev)}
+            if self.mode == lk.LK_TWOPASS:
+                d["xl"] = torch.empty((B, K), dtype=torch.int8, device=dev)
+            self.acts[K] = d
+        self.out = {n: torch.empty((B, N), dtype=f32, device=dev) for n, (N, _) in self.shapes.items()}
+        self.logits = torch.empty((B, vocab), dtype=f32, device=dev)
+        self.scratch = torch.zeros((B * lk.lk_argmax_scratch_entries(vocab),), dtype=torch.int64, device=dev)
+        self.idx = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def _cfg(self):
+        return lk.launch_cfg(pdl=1 if self.pdl else 0)
+
+    def _norm(self, x, g):
+        K = x.shape[1]
+        if self.mode == lk.LK_DEQUANT:
+            lk.lk_rmsnorm_quant(x, g, self.mode, self.eps, self.xn[K], cfg=self._cfg())
+            return {"x": self.xn[K]}
+        a = self.acts[K]
+        lk.lk_rmsnorm_quant(x, g, self.mode, self.eps, None, a["xq"], a.get("xl"), a["xs"], cfg=self._cfg())
+        return a
+
+    def _quant(self, x):
+        if self.mode == lk.LK_DEQUANT:
+            return {"x": x}
+        a = self.acts[x.shape[1]]
+        lk.lk_quantize_act(x, self.mode, a["xq"], a.get("xl"), a["xs"], cfg=self._cfg())
+        return a
+
+    def _gemv(self, w, K, y, a):
+        lk.lk_gemv_blk(self.fmt, w, K, self.mode, y, M=self.B, cfg=self._cfg(), **a)
+
+    def run_token(self, x_in=None, hook=None):
+        """One token on the current stream; returns the device int32 [B]
+        argmax.  ``hook(name, launch)``, if given, wraps each GEMV launch."""
+        if x_in is not None and x_in.data_ptr() != self.x_buf.data_ptr():
+            self.x_buf.copy_(x_in)
+
+        def g(name, w, K, y, a):
+            def launch():
+                return self._gemv(w, K, y, a)
+            return launch() if hook is None else hook(name, launch)
+
+        x = self.x_buf
+        for w in self.layers:
+            g("qkv", w["qkv"], self.H, self.out["qkv"], self._norm(x, w["g_attn"]))
+            g("o", w["o"], self.Q, self.out["o"], self._quant(w["o_in"]))
+            g("gu", w["gu"], self.H, self.out["gu"], self._norm(self.out["o"], w["g_mlp"]))
+            g("down", w["down"], self.F, self.h, self._quant(w["d_in"]))
+            x = self.h
+        g("lm", self.lm, self.H, self.logits, self._norm(x, self.g_final))
+        lk.lk_argmax(self.idx, self.B, self.V, logits=self.logits, scratch=self.scratch)
+        return self.idx
+
+    def weight_bytes(self, name=None):
+        """The format's bytes of one token's matrices (or of projection `name`)."""
+        def mb(N, K):
+            return N * lk.lk_format_row_bytes(self.fmt, K)
+        if name == "lm":
+            return mb(self.V, self.H)
+        if name is not None:
+            return mb(*self.shapes[name])
+        return self.L * sum(mb(N, K) for N, K in self.shapes.values()) + mb(self.V, self.H)
+
+    def launches_per_token(self):
+        quant = 0 if self.mode == lk.LK_DEQUANT else 2
+        return self.L * (6 + quant) + 3

@@ -133,3 +133,50 @@ def test_gemv_blk_full_size_all_rows(fmt, mode, M):
     torch.cuda.synchronize()
     assert lk.lk_device_error(reset=True) == 0
     assert np.array_equal(bits(host(y)), bits(y_or))
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q4_0", "iq4_nl"])
+@pytest.mark.parametrize("mode,M", [(1, 1), (2, 3), (0, 1)])
+def test_blk_decode_stack_token(fmt, mode, M):
+    """A small block-format decode stack (3 layers, hidden 1024): every GEMV
+    of one token against the oracle on the GPU's own activation (bit for bit
+    under Int8Act / TwoPass, within 1e-5 * sum|w x| under Dequant), and the
+    argmax the oracle's first maximum of the GPU's logits."""
+    from q8_quantized_gemv_gb300.decode import BlkDecodeStack
+    st = BlkDecodeStack(fmt, layers=3, hidden=1024, q_dim=1024, kv_dim=256, ffn=1024, vocab=4096, batch=M,
+                        mode=mode, device=DEV, pdl=True)
+    F = oracle.FORMATS[fmt]
+    seen = []
+
+    def hook(name, launch):
+        r = launch()
+        torch.cuda.synchronize()
+        seen.append(name)
+        return r
+
+    # record each GEMV's activation and output as it runs
+    checks = []
+    orig = st._gemv
+
+    def gemv(w, K, y, a):
+        orig(w, K, y, a)
+        torch.cuda.synchronize()
+        checks.append((host(w), K, {k: host(v) for k, v in a.items() if v is not None}, host(y).copy()))
+
+    st._gemv = gemv
+    idx = st.run_token(hook=hook)
+    torch.cuda.synchronize()
+    assert lk.lk_device_error(reset=True) == 0
+    assert len(checks) == 3 * 4 + 1 and st.launches_per_token() == 3 * (8 if mode else 6) + 3
+    for w, K, a, y in checks:
+        if mode == 0:
+            y_or = oracle.gemv_blk(F, w, K, 0, x=a["x"])
+            mag = oracle.absdot_blk(F, w, K, a["x"])
+            err = np.abs(y.astype(np.float64) - y_or.astype(np.float64))
+            assert np.all(err <= 1e-5 * mag + 1e-30)
+        else:
+            y_or = oracle.gemv_blk(F, w, K, mode, hi=a["xq"], lo=a.get("xl"), s=a["xs"])
+            assert np.array_equal(bits(y), bits(y_or))
+    logits = host(st.logits)
+    for t in range(M):
+        assert int(host(idx)[t]) == oracle.argmax(logits[t])
