@@ -46,9 +46,10 @@ __host__ __device__ constexpr int blk_bytes(int F) {
 // Shared-memory byte helpers (the staged row: 16-byte aligned, arbitrary
 // byte offsets inside it).
 __device__ __forceinline__ unsigned u8(const unsigned char* p) { return *p; }
-__device__ __forceinline__ float half_at(const unsigned char* p) {
-  return __half2float(__ushort_as_half((unsigned short)(p[0] | (p[1] << 8))));
-}
+// (every f16 field of these layouts sits at an even offset of a 16-byte
+// aligned row: blocks of 18, 20, 22, 24 bytes, super-blocks of 84, 110,
+// 136, 144, 176, 210 bytes with even field offsets)
+__device__ __forceinline__ float half_at(const unsigned char* p) { return __half2float(*(const __half*)p); }
 // Four bytes from any offset: the two aligned words around them.
 __device__ __forceinline__ unsigned w32(const unsigned char* p) {
   const uintptr_t a = (uintptr_t)p;
@@ -190,17 +191,25 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
   } else if constexpr (F == 12 || F == 13) {
     const unsigned char* sup = row + (sb >> 3) * blk_bytes(F);
     const int j = sb & 7;
-    const unsigned char* sm = sup + 4;
+    // the super-block's 16-byte head (d, dmin, twelve packed 6-bit scales
+    // and mins) in one read: the super-blocks sit 16-byte aligned in the row
+    const uint4 hd = *(const uint4*)sup;
+    // byte 4 + i of the head (scales area byte i, 0 <= i < 12)
+    auto sm = [&](int i) {
+      const int b = 4 + i;
+      const unsigned wv = b < 8 ? hd.y : b < 12 ? hd.z : hd.w;
+      return (int)((wv >> (8 * (b & 3))) & 0xFFu);
+    };
     int sc, m;
     if (j < 4) {
-      sc = sm[j] & 63;
-      m = sm[j + 4] & 63;
+      sc = sm(j) & 63;
+      m = sm(j + 4) & 63;
     } else {
-      sc = (sm[j + 4] & 15) | ((sm[j - 4] >> 6) << 4);
-      m = (sm[j + 4] >> 4) | ((sm[j] >> 6) << 4);
+      sc = (sm(j + 4) & 15) | ((sm(j - 4) >> 6) << 4);
+      m = (sm(j + 4) >> 4) | ((sm(j) >> 6) << 4);
     }
-    d[0] = d[1] = __fmul_rn(half_at(sup), (float)sc);
-    c[0] = c[1] = -__fmul_rn(half_at(sup + 2), (float)m);
+    d[0] = d[1] = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu))), (float)sc);
+    c[0] = c[1] = -__fmul_rn(__half2float(__ushort_as_half((unsigned short)(hd.x >> 16))), (float)m);
     const unsigned char* ql = sup + (F == 12 ? 16 : 48) + (j >> 1) * 32;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
