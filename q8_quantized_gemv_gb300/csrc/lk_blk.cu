@@ -102,25 +102,35 @@ __device__ __forceinline__ Lut16 level_lut() {
                pack4(53, 69, 89, 113)};
 }
 
-// Table entries for the four nibble values n (one per byte, 0..15): the
-// byte permute picks entry n & 7 from the low and from the high eight, and
-// bit 3 of each n chooses between them.
-__device__ __forceinline__ unsigned lut_bytes(const Lut16& T, unsigned n) {
-  const unsigned s = n & 0x07070707u;
-  const unsigned sel = __byte_perm(s | (s >> 4), 0u, 0x4420u);  // the four 3-bit indices as nibbles
-  const unsigned lo = __byte_perm(T.t0, T.t1, sel);
-  const unsigned hi = __byte_perm(T.t2, T.t3, sel);
-  const unsigned m = ((n >> 3) & 0x01010101u) * 0xFFu;
-  return (lo & ~m) | (hi & m);
+// prmt.b32 in its generic mode: byte i of the result is byte (c_i & 7) of
+// {b:a} (a the low four), or, where bit 3 of selector nibble c_i is set,
+// that byte's bit 7 copied to all eight bits.  Only the selector's low 16
+// bits count.
+__device__ __forceinline__ unsigned prmt(unsigned a, unsigned b, unsigned c) {
+  unsigned r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
 }
 
 // The table applied to the low and the high nibbles of a word: bytes of
-// `lo` = table[low nibbles], `hi` = table[high nibbles].
+// `lo` = table[low nibbles], `hi` = table[high nibbles].  The word's eight
+// nibbles, in order low0 high0 low1 high1 ..., serve as byte selectors as
+// they stand: a nibble n < 8 picks entry n from the low eight; n ^ 8 picks
+// entry n from the high eight when n >= 8 (the other pick, in sign mode, is
+// discarded).  Bit 3 of each nibble, replicated over its byte (the msb of
+// each byte of q << 4 for the low nibbles, of q for the high ones), chooses
+// between the two; one last permute puts the lows and the highs in order.
 template <int F>
 __device__ __forceinline__ void table_word(unsigned q, unsigned& lo, unsigned& hi) {
   const Lut16 T = level_lut<F>();
-  lo = lut_bytes(T, q & 0x0F0F0F0Fu);
-  hi = lut_bytes(T, (q >> 4) & 0x0F0F0F0Fu);
+  const unsigned qx = q ^ 0x88888888u;
+  const unsigned q4 = q << 4;
+  const unsigned a0 = prmt(T.t0, T.t1, q), a1 = prmt(T.t2, T.t3, qx);                // low0 high0 low1 high1
+  const unsigned b0 = prmt(T.t0, T.t1, q >> 16), b1 = prmt(T.t2, T.t3, qx >> 16);    // low2 high2 low3 high3
+  const unsigned ma = prmt(q4, q, 0xD9C8u), mb = prmt(q4, q, 0xFBEAu);
+  const unsigned wa = (a0 & ~ma) | (a1 & ma), wb = (b0 & ~mb) | (b1 & mb);
+  lo = prmt(wa, wb, 0x6420u);
+  hi = prmt(wa, wb, 0x7531u);
 }
 
 // Sub-block sb of a staged row in format F: w[0..7] the 32 levels four to a
