@@ -133,8 +133,18 @@ __device__ __forceinline__ void table_word(unsigned q, unsigned& lo, unsigned& h
   hi = prmt(wa, wb, 0x7531u);
 }
 
-// Sub-block sb of a staged row in format F: w[0..7] the 32 levels four to a
-// word (value 4i + k in byte k of w[i]), d/c per half.
+// The constant some formats subtract from every stored level (Q4_0 8,
+// Q5_0 16, Q3_K 4, Q6_K 32).  decode leaves it in the level bytes; the
+// integer dots take it out once per half (dot(n - o, h) = dot(n, h) -
+// o sum(h), exact), Dequant in the bias of its float conversion.
+template <int F>
+__host__ __device__ constexpr int level_offset() {
+  return F == 2 ? 8 : F == 6 ? 16 : F == 11 ? 4 : F == 14 ? 32 : 0;
+}
+
+// Sub-block sb of a staged row in format F: w[0..7] the 32 stored levels
+// plus level_offset<F>() four to a word (value 4i + k in byte k of w[i]),
+// d/c per half.
 template <int F>
 __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigned (&w)[8],
                                        float (&d)[2], float (&c)[2]) {
@@ -159,10 +169,6 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
       } else {
         w[i] = q & 0x0F0F0F0Fu;
         w[4 + i] = (q >> 4) & 0x0F0F0F0Fu;
-        if (F == 2) {
-          w[i] = __vsub4(w[i], 0x08080808u);
-          w[4 + i] = __vsub4(w[4 + i], 0x08080808u);
-        }
       }
     }
   } else if constexpr (F == 6 || F == 7) {
@@ -183,10 +189,6 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
       const unsigned q = hw[1 + i];
       w[i] = (q & 0x0F0F0F0Fu) | (spread4(qh >> (4 * i)) << 4);
       w[4 + i] = ((q >> 4) & 0x0F0F0F0Fu) | (spread4(qh >> (16 + 4 * i)) << 4);
-      if (F == 6) {
-        w[i] = __vsub4(w[i], 0x10101010u);
-        w[4 + i] = __vsub4(w[4 + i], 0x10101010u);
-      }
     }
   } else if constexpr (F == 39) {
     const unsigned char* b = row + sb * 17;
@@ -251,7 +253,7 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
     for (int i = 0; i < 8; ++i) {
       const unsigned low2 = (qw[i] >> (2 * k)) & 0x03030303u;
       const unsigned mb = (mw[i] >> bit) & 0x01010101u;  // set: +0, clear: -4
-      w[i] = __vsub4(low2 | (mb << 2), 0x04040404u);
+      w[i] = low2 | (mb << 2);
     }
     const unsigned char* s12 = sup + 96;
     const float D = half_at(sup + 108);
@@ -274,7 +276,7 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
     for (int i = 0; i < 8; ++i) {
       const unsigned lo = (lw[i] >> (4 * (k >> 1))) & 0x0F0F0F0Fu;
       const unsigned hi = (hw[i] >> (2 * k)) & 0x03030303u;
-      w[i] = __vsub4(lo | (hi << 4), 0x20202020u);
+      w[i] = lo | (hi << 4);
     }
     const float D = half_at(sup + 208);
     d[0] = __fmul_rn(D, (float)(signed char)sup[192 + half * 8 + 2 * k]);
@@ -295,6 +297,7 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
 // f32 part of one sub-block for one activation row: ((d0 dh0 + c0 sh0) +
 // d1 dh1) + c1 sh1, each product and sum rounded; sh: the activation
 // halves' sums (exact integers, formed once when the rows are staged).
+template <int O>
 __device__ __forceinline__ float sub_part(const unsigned (&w)[8], const float (&d)[2], const float (&c)[2],
                                           const unsigned (&h)[8], int2 sh) {
   int dh0 = 0, dh1 = 0;
@@ -303,6 +306,10 @@ __device__ __forceinline__ float sub_part(const unsigned (&w)[8], const float (&
   for (int i = 0; i < 4; ++i) {
     dh0 = __dp4a((int)w[i], (int)h[i], dh0);
     dh1 = __dp4a((int)w[4 + i], (int)h[4 + i], dh1);
+  }
+  if (O) {
+    dh0 -= O * sh0;
+    dh1 -= O * sh1;
   }
   float p = __fmul_rn(d[0], (float)dh0);
   p = __fadd_rn(p, __fmul_rn(c[0], (float)sh0));
@@ -418,7 +425,7 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
         decode<F>(rbuf, sb, w, d, c);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float v = (float)(signed char)(w[i >> 2] >> (8 * (i & 3)));
+          const float v = (float)((int)(signed char)(w[i >> 2] >> (8 * (i & 3))) - level_offset<F>());
           a.dq[row * (long)K + 32 * sb + i] = __fadd_rn(__fmul_rn(d[i >> 4], v), c[i >> 4]);
         }
       }
@@ -435,7 +442,8 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
         // 2^23 + 128 + b and the bias subtracted (exact), then the scale and
         // the offset, each rounded as the scalar form
         f32x2 wv[16];
-        const f32x2 bias = f2_pack(-8388736.0f, -8388736.0f);
+        constexpr float B = -8388736.0f - (float)level_offset<F>();  // -(2^23 + 128 + offset), exact
+        const f32x2 bias = f2_pack(B, B);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const unsigned u = w[q] ^ 0x80808080u;
@@ -494,13 +502,13 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
           *(uint4*)&h[4] = *(const uint4*)(hp + 16);
           const float* srow = (const float*)(base + nbu * 48u * (Q == 2 ? 2u : 1u));
           const int2* sums = (const int2*)(srow + nbu);
-          float part = sub_part(w, d, c, h, sums[sb]);
+          float part = sub_part<level_offset<F>()>(w, d, c, h, sums[sb]);
           if constexpr (Q == 2) {
             const unsigned char* lp = hp + nbu * 48u;
             unsigned l[8];
             *(uint4*)&l[0] = *(const uint4*)lp;
             *(uint4*)&l[4] = *(const uint4*)(lp + 16);
-            part = __fadd_rn(part, __fmul_rn(0.0078125f, sub_part(w, d, c, l, sums[nbu + sb])));
+            part = __fadd_rn(part, __fmul_rn(0.0078125f, sub_part<level_offset<F>()>(w, d, c, l, sums[nbu + sb])));
           }
           const float s = srow[sb];
           acc[t] = __fadd_rn(acc[t], __fmul_rn(s, part));
