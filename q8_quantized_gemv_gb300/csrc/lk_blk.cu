@@ -72,6 +72,22 @@ __device__ __forceinline__ void words_at(const unsigned char* p, unsigned (&out)
   for (int i = 0; i < NW; ++i) out[i] = __funnelshift_r(v[i], v[i + 1], sh);
 }
 
+// The same, shifted right by e more bits (0 <= e <= 7): bit field e.. of
+// every byte in one funnel shift (the bits that enter from the next word
+// at bit 32 - e and above, past the top byte's field when it is at most
+// 8 - e bits wide).
+template <int NW>
+__device__ __forceinline__ void words_at_sh(const unsigned char* p, unsigned e, unsigned (&out)[NW]) {
+  const uintptr_t a = (uintptr_t)p;
+  const unsigned* q = (const unsigned*)(a & ~(uintptr_t)3);
+  const unsigned sh = 8u * (unsigned)(a & 3) + e;
+  unsigned v[NW + 1];
+#pragma unroll
+  for (int i = 0; i <= NW; ++i) v[i] = q[i];
+#pragma unroll
+  for (int i = 0; i < NW; ++i) out[i] = __funnelshift_r(v[i], v[i + 1], sh);
+}
+
 // Formats whose level words sit at 4-byte-aligned offsets of a staged row
 // (16-byte aligned): blocks of 20 or 24 bytes with 4- or 8-byte headers,
 // super-blocks of 84, 136, 144 or 176 bytes.  Their words are read as they
@@ -187,8 +203,8 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const unsigned q = hw[1 + i];
-      w[i] = (q & 0x0F0F0F0Fu) | (spread4(qh >> (4 * i)) << 4);
-      w[4 + i] = ((q >> 4) & 0x0F0F0F0Fu) | (spread4(qh >> (16 + 4 * i)) << 4);
+      w[i] = (q & 0x0F0F0F0Fu) + (spread4(qh >> (4 * i)) << 4);  // disjoint bits: shift-adds
+      w[4 + i] = ((q >> 4) & 0x0F0F0F0Fu) + (spread4(qh >> (16 + 4 * i)) << 4);
     }
   } else if constexpr (F == 39) {
     const unsigned char* b = row + sb * 17;
@@ -247,13 +263,13 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
     const int j = sb & 7, half = j >> 2, k = j & 3, bit = half * 4 + k;
     const unsigned char* q = sup + 32 + half * 32;
     unsigned qw[8], mw[8];
-    words_at<8>(q, qw);
-    words_at<8>(sup, mw);
+    words_at_sh<8>(q, 2u * k, qw);
+    words_at_sh<8>(sup, (unsigned)bit, mw);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const unsigned low2 = (qw[i] >> (2 * k)) & 0x03030303u;
-      const unsigned mb = (mw[i] >> bit) & 0x01010101u;  // set: +0, clear: -4
-      w[i] = low2 | (mb << 2);
+      const unsigned low2 = qw[i] & 0x03030303u;
+      const unsigned mb = mw[i] & 0x01010101u;  // set: +0, clear: -4
+      w[i] = low2 + (mb << 2);                    // disjoint bits: one shift-add
     }
     const unsigned char* s12 = sup + 96;
     const float D = half_at(sup + 108);
@@ -270,13 +286,13 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
     const unsigned char* ql = sup + half * 64 + (k & 1) * 32;
     const unsigned char* qh = sup + 128 + half * 32;
     unsigned lw[8], hw[8];
-    words_at<8>(ql, lw);
-    words_at<8>(qh, hw);
+    words_at_sh<8>(ql, 4u * (k >> 1), lw);
+    words_at_sh<8>(qh, 2u * k, hw);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const unsigned lo = (lw[i] >> (4 * (k >> 1))) & 0x0F0F0F0Fu;
-      const unsigned hi = (hw[i] >> (2 * k)) & 0x03030303u;
-      w[i] = lo | (hi << 4);
+      const unsigned lo = lw[i] & 0x0F0F0F0Fu;
+      const unsigned hi = hw[i] & 0x03030303u;
+      w[i] = lo + (hi << 4);  // disjoint bits: one shift-add
     }
     const float D = half_at(sup + 208);
     d[0] = __fmul_rn(D, (float)(signed char)sup[192 + half * 8 + 2 * k]);
