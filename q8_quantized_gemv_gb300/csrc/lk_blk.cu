@@ -149,6 +149,31 @@ __device__ __forceinline__ void table_word(unsigned q, unsigned& lo, unsigned& h
   hi = prmt(wa, wb, 0x7531u);
 }
 
+// The table formats' levels for the integer dots, as two words per four
+// values whose entries are all 0..127: P holds the entries of nibbles n < 8,
+// N those of n >= 8, each 0 where the other applies (the pick in sign mode
+// of a byte whose bit 7 is clear).  IQ4 (lower half negative, upper
+// positive): P = -T[n], N = T[n], level = N - P; MXFP4 (upper half the
+// negated lower): P = T[n], N = -T[n], level = P - N.  No choice between the
+// halves is formed: each half has its own dot.
+template <int F>
+__host__ __device__ constexpr bool is_table() { return F == 20 || F == 23 || F == 39; }
+template <int F>
+__device__ __forceinline__ void table_word_pn(unsigned q, unsigned& pl, unsigned& ph, unsigned& nl, unsigned& nh) {
+  constexpr bool mx = F == 39;
+  constexpr unsigned p0 = mx ? pack4(0, 1, 2, 3) : pack4(127, 104, 83, 65);
+  constexpr unsigned p1 = mx ? pack4(4, 6, 8, 12) : pack4(49, 35, 22, 10);
+  constexpr unsigned n0 = mx ? pack4(0, 1, 2, 3) : pack4(1, 13, 25, 38);
+  constexpr unsigned n1 = mx ? pack4(4, 6, 8, 12) : pack4(53, 69, 89, 113);
+  const unsigned qx = q ^ 0x88888888u;
+  const unsigned pa = prmt(p0, p1, q), pb = prmt(p0, p1, q >> 16);    // low0 high0 low1 high1, low2 ...
+  const unsigned na = prmt(n0, n1, qx), nb = prmt(n0, n1, qx >> 16);
+  pl = prmt(pa, pb, 0x6420u);
+  ph = prmt(pa, pb, 0x7531u);
+  nl = prmt(na, nb, 0x6420u);
+  nh = prmt(na, nb, 0x7531u);
+}
+
 // The constant some formats subtract from every stored level (Q4_0 8,
 // Q5_0 16, Q3_K 4, Q6_K 32).  decode leaves it in the level bytes; the
 // integer dots take it out once per half (dot(n - o, h) = dot(n, h) -
@@ -161,9 +186,11 @@ __host__ __device__ constexpr int level_offset() {
 // Sub-block sb of a staged row in format F: w[0..7] the 32 stored levels
 // plus level_offset<F>() four to a word (value 4i + k in byte k of w[i]),
 // d/c per half.
-template <int F>
-__device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigned (&w)[8],
-                                       float (&d)[2], float (&c)[2]) {
+// PN (the table formats only): w the P words and wn the N words of
+// table_word_pn instead of the levels.
+template <int F, bool PN>
+__device__ __forceinline__ void decode_impl(const unsigned char* row, int sb, unsigned (&w)[8],
+                                            float (&d)[2], float (&c)[2], unsigned (&wn)[8]) {
   c[0] = c[1] = 0.f;
   if constexpr (F == 2 || F == 3 || F == 20) {
     const unsigned char* b = row + sb * blk_bytes(F);
@@ -181,7 +208,8 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
     for (int i = 0; i < 4; ++i) {
       const unsigned q = qw[i];
       if constexpr (F == 20) {
-        table_word<F>(q, w[i], w[4 + i]);
+        if constexpr (PN) table_word_pn<F>(q, w[i], w[4 + i], wn[i], wn[4 + i]);
+        else table_word<F>(q, w[i], w[4 + i]);
       } else {
         w[i] = q & 0x0F0F0F0Fu;
         w[4 + i] = (q >> 4) & 0x0F0F0F0Fu;
@@ -215,7 +243,10 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
     unsigned qw[4];
     words_at<4>(b + 1, qw);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) table_word<F>(qw[i], w[i], w[4 + i]);
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (PN) table_word_pn<F>(qw[i], w[i], w[4 + i], wn[i], wn[4 + i]);
+      else table_word<F>(qw[i], w[i], w[4 + i]);
+    }
   } else if constexpr (F == 12 || F == 13) {
     const unsigned char* sup = row + (sb >> 3) * blk_bytes(F);
     const int j = sb & 7;
@@ -305,14 +336,33 @@ __device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigne
     d[0] = d[1] = __fmul_rn(half_at(sup), (float)(ls - 32));
     const unsigned char* qs = sup + 8 + 16 * j;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) table_word<F>(word_at<F>(qs + 4 * i), w[i], w[4 + i]);
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (PN) table_word_pn<F>(word_at<F>(qs + 4 * i), w[i], w[4 + i], wn[i], wn[4 + i]);
+      else table_word<F>(word_at<F>(qs + 4 * i), w[i], w[4 + i]);
+    }
   }
+}
+template <int F>
+__device__ __forceinline__ void decode(const unsigned char* row, int sb, unsigned (&w)[8], float (&d)[2],
+                                       float (&c)[2]) {
+  decode_impl<F, false>(row, sb, w, d, c, w);
 }
 
 
 // f32 part of one sub-block for one activation row: ((d0 dh0 + c0 sh0) +
 // d1 dh1) + c1 sh1, each product and sum rounded; sh: the activation
 // halves' sums (exact integers, formed once when the rows are staged).
+// A sub-block's term from its halves' exact integer dots dh0, dh1 and
+// activation sums sh0, sh1: ((d0 dh0 + c0 sh0) + d1 dh1) + c1 sh1, each
+// product and sum rounded to f32.
+__device__ __forceinline__ float sub_combine(const float (&d)[2], const float (&c)[2], int dh0, int dh1, int sh0,
+                                             int sh1) {
+  float p = __fmul_rn(d[0], (float)dh0);
+  p = __fadd_rn(p, __fmul_rn(c[0], (float)sh0));
+  p = __fadd_rn(p, __fmul_rn(d[1], (float)dh1));
+  return __fadd_rn(p, __fmul_rn(c[1], (float)sh1));
+}
+
 template <int O>
 __device__ __forceinline__ float sub_part(const unsigned (&w)[8], const float (&d)[2], const float (&c)[2],
                                           const unsigned (&h)[8], int2 sh) {
@@ -327,11 +377,26 @@ __device__ __forceinline__ float sub_part(const unsigned (&w)[8], const float (&
     dh0 -= O * sh0;
     dh1 -= O * sh1;
   }
-  float p = __fmul_rn(d[0], (float)dh0);
-  p = __fadd_rn(p, __fmul_rn(c[0], (float)sh0));
-  p = __fadd_rn(p, __fmul_rn(d[1], (float)dh1));
-  return __fadd_rn(p, __fmul_rn(c[1], (float)sh1));
+  return sub_combine(d, c, dh0, dh1, sh0, sh1);
 }
+
+// The table formats' term from their P and N words (table_word_pn): each
+// half's exact integer dot is the difference of two dots.
+template <int F>
+__device__ __forceinline__ float sub_part_pn(const unsigned (&wp)[8], const unsigned (&wn)[8], const float (&d)[2],
+                                             const float (&c)[2], const unsigned (&h)[8], int2 sh) {
+  int p0 = 0, p1 = 0, n0 = 0, n1 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    p0 = __dp4a((int)wp[i], (int)h[i], p0);
+    p1 = __dp4a((int)wp[4 + i], (int)h[4 + i], p1);
+    n0 = __dp4a((int)wn[i], (int)h[i], n0);
+    n1 = __dp4a((int)wn[4 + i], (int)h[4 + i], n1);
+  }
+  const int dh0 = F == 39 ? p0 - n0 : n0 - p0, dh1 = F == 39 ? p1 - n1 : n1 - p1;
+  return sub_combine(d, c, dh0, dh1, sh.x, sh.y);
+}
+
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(dst)),
@@ -505,9 +570,9 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
       const unsigned nbu = (unsigned)nb;
 #pragma unroll 2
       for (int sb = lane; sb < nb; sb += 32) {
-        unsigned w[8];
+        unsigned w[8], wn[8];
         float d[2], c[2];
-        decode<F>(rbuf, sb, w, d, c);
+        decode_impl<F, is_table<F>()>(rbuf, sb, w, d, c, wn);
 #pragma unroll
         for (int t = 0; t < MM; ++t) {
           if (t >= a.M) break;
@@ -518,13 +583,16 @@ __global__ void __launch_bounds__(BW * 32) gemv_blk_kernel(const BlkArgs a) {
           *(uint4*)&h[4] = *(const uint4*)(hp + 16);
           const float* srow = (const float*)(base + nbu * 48u * (Q == 2 ? 2u : 1u));
           const int2* sums = (const int2*)(srow + nbu);
-          float part = sub_part<level_offset<F>()>(w, d, c, h, sums[sb]);
+          float part = is_table<F>() ? sub_part_pn<F>(w, wn, d, c, h, sums[sb])
+                                     : sub_part<level_offset<F>()>(w, d, c, h, sums[sb]);
           if constexpr (Q == 2) {
             const unsigned char* lp = hp + nbu * 48u;
             unsigned l[8];
             *(uint4*)&l[0] = *(const uint4*)lp;
             *(uint4*)&l[4] = *(const uint4*)(lp + 16);
-            part = __fadd_rn(part, __fmul_rn(0.0078125f, sub_part<level_offset<F>()>(w, d, c, l, sums[nbu + sb])));
+            const float lpart = is_table<F>() ? sub_part_pn<F>(w, wn, d, c, l, sums[nbu + sb])
+                                              : sub_part<level_offset<F>()>(w, d, c, l, sums[nbu + sb]);
+            part = __fadd_rn(part, __fmul_rn(0.0078125f, lpart));
           }
           const float s = srow[sb];
           acc[t] = __fadd_rn(acc[t], __fmul_rn(s, part));
